@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 Adafactor step on Llama-3-8B-shaped parameters.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3_8b|llama3_8b_beta1|llama_layer|edge|tiny]
+
+One step = one full Adafactor step (all kernels of the launch sequence) over
+the whole tensor list of the workload, with synthetic inputs resident in HBM
+(48 GB for Llama-3-8B: fp32 params, bf16 grads; far larger than the 129 MB
+L2, so no flush is needed between steps).  Rank 0 prints one JSON line.
+
+--impl reference times the float64 CPU oracle (single thread) on a bounded
+sample of the same workload per step.  Under torchrun with N > 1 every rank
+runs an independent replica of the step on its own GPU (the step has no
+collective); value = total params/s over all ranks with the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from memory_efficient_optimizer_gb300 import binding, synth  # noqa: E402
+from memory_efficient_optimizer_gb300.optim import AdafactorStep, init_state  # noqa: E402
+
+METRIC = "Adafactor step params/sec and effective HBM GB/s (% of 8 TB/s), Llama-3-8B shapes"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "adafactor_kernels.cu")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if key in peaks and peaks[key]:
+                return float(peaks[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(shapes, grad_bytes, beta1, recompute_psq=False):
+    """Bytes the step must move at minimum: 3 reads of g, p read + write,
+    exp_avg read + write with beta1, the row/col (or full) second-moment state
+    read + write, and (only when RMS(p) is not carried over) one more p read.
+    Returns (per step, per k_apply launch)."""
+    step = apply = 0
+    for _, s in shapes:
+        n = 1
+        for d in s:
+            n *= int(d)
+        state = (2 * 4 * (n // (s[-2] * s[-1]) * (s[-2] + s[-1]))) if len(s) >= 2 else 2 * 4 * n
+        m1 = 8 * n if beta1 else 0
+        step += 3 * grad_bytes * n + 8 * n + m1 + state + (4 * n if recompute_psq else 0)
+        # apply: g + p read/write + exp_avg read/write + reads of row/col (or v)
+        apply += grad_bytes * n + 8 * n + m1 + state // 2
+    return step, apply
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi during a region."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for r in csv.reader(io.StringIO(self.out or "")):
+            r = [x.strip() for x in r]
+            if len(r) < 10:
+                continue
+            if self.uuid and self.uuid not in r[1]:
+                continue
+            rows.append(r)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def device_uuid(dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def traffic_record(kernel):
+    """dram bytes per full launch from the committed ncu summary, or None when
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+        entry = rec.get(kernel)
+        if entry and entry.get("kernel_source_sha256") == sha:
+            return float(entry["dram_bytes_per_full_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- our arm --
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.workload(args.workload)
+    shapes = [s for _, s in wl.shapes]
+    n_params = wl.numel
+    beta1 = wl.hparams.get("beta1")
+    params = [synth.make_param(s, k, device=dev, std=wl.param_std) for k, s in enumerate(shapes)]
+    grads = [synth.make_grad(s, k, 1, device=dev, std=wl.grad_std, dtype=wl.grad_dtype, kind=wl.grad_kind)
+             for k, s in enumerate(shapes)]
+    states = init_state(params, beta1=beta1)
+    step = AdafactorStep(params, grads, states, **wl.hparams)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    binding.adafactor_profile_read()  # drop anything recorded so far
+    binding.adafactor_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device_uuid(dev)) as clocks:
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            t += 1
+            step(t)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    binding.adafactor_profile_enable(False)
+    kernels = binding.adafactor_profile_read()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        x = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+        ms = float(x.item())
+        torch.distributed.barrier()
+    ms_per_step = ms / args.steps
+
+    # ---- end to end: host grads in, host params out, through the same API
+    e2e = None
+    if args.e2e_steps > 0:
+        host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
+        host_p = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in params]
+        for hg, g in zip(host_g, grads):
+            hg.copy_(g)
+        torch.cuda.synchronize(dev)
+        h2d = sum(g.numel() * g.element_size() for g in grads)
+        d2h = sum(p.numel() * p.element_size() for p in params)
+
+        def e2e_step():
+            nonlocal t
+            for g, hg in zip(grads, host_g):
+                g.copy_(hg, non_blocking=True)
+            t += 1
+            step(t)
+            for hp_, p in zip(host_p, params):
+                hp_.copy_(p, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            x = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+            ems = float(x.item())
+        e2e = {"value": world * n_params / (ems / args.e2e_steps / 1e3), "unit": "params/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "ms_per_step": ems / args.e2e_steps,
+               "path": "pinned host bf16 grads -> device, adafactor_step, device fp32 params -> pinned host"}
+        del host_g, host_p
+
+    grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
+    step_bytes, apply_bytes = algorithmic_bytes(wl.shapes, grad_bytes, beta1 is not None)
+    peak, peak_kind = measured_hbm_peak()
+    launches = sum(v[1] for v in kernels.values())
+    dom = max(kernels.items(), key=lambda kv: kv[1][0])
+    dom_name, (dom_ms, dom_n) = dom
+    per_launch_bytes = {"k_apply": apply_bytes}
+    roofline = None
+    if dom_n and dom_name in per_launch_bytes:
+        ach = per_launch_bytes[dom_name] / (dom_ms / dom_n / 1e3) / 1e9
+        roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
+                    "traffic": traffic_record(dom_name), "algorithmic_bytes_per_launch": apply_bytes,
+                    "avg_launch_ms": dom_ms / dom_n}
+    eff_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
+    clk = clocks.summary()
+    out = {
+        "metric": METRIC, "value": world * n_params / (ms_per_step / 1e3), "unit": "params/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) fp32 params, N(0,1e-3) bf16 grads resident in HBM)",
+        "config": {"workload": args.workload, "description": wl.description, "params": n_params,
+                   "tensors": len(shapes), "param_dtype": "fp32",
+                   "grad_dtype": "bf16" if grad_bytes == 2 else "fp32",
+                   "hparams": {k: v for k, v in wl.hparams.items()} or "defaults",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs (params+grads) far larger than L2; no flush"},
+        "effective_gbs": round(eff_gbs, 1),
+        "pct_of_8tbs": round(100 * eff_gbs / NOMINAL_HBM_GBS, 2),
+        "frac_of_hbm_peak": round(eff_gbs / peak, 4), "hbm_peak_gbs": peak, "hbm_peak_source": peak_kind,
+        "algorithmic_bytes_per_step": step_bytes,
+        "kernels_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in kernels.items() if v[1]},
+        "roofline": roofline, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+    }
+    return out, (wl, n_params)
+
+
+# ----------------------------------------------------------- oracle arms --
+def oracle_sample(wl, seconds_hint=10.0):
+    """A bounded sample of the workload for the CPU oracle: the tensors of one
+    decoder layer (Llama workloads) or the first tensors up to ~2e8 values."""
+    import numpy as np
+    shapes = wl.shapes
+    idx = [k for k, (name, _) in enumerate(shapes) if name.startswith("layers.0.")]
+    if not idx:
+        idx, tot = [], 0
+        for k, (_, s) in enumerate(shapes):
+            n = int(np.prod(s)) if s else 1
+            if tot + n > 2e8 and idx:
+                break
+            idx.append(k)
+            tot += n
+    return idx
+
+
+def time_oracle(wl, idx, steps, t0=1):
+    """Runs the oracle `steps` times over the sampled tensors; returns the
+    seconds spent inside the oracle and the values processed."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    hp = oracle.HParams(**wl.hparams)
+    shapes = [wl.shapes[k][1] for k in idx]
+    ps = [synth.make_param(s, k, std=wl.param_std).double().numpy() for s, k in zip(shapes, idx)]
+    sts = [oracle.State(s, beta1=wl.hparams.get("beta1") is not None) for s in shapes]
+    gs = [synth.make_grad(s, k, 1, std=wl.grad_std, dtype=wl.grad_dtype, kind=wl.grad_kind).double().numpy()
+          for s, k in zip(shapes, idx)]
+    per_step = []
+    for t in range(t0, t0 + steps):
+        a = time.perf_counter()
+        for p, g, st in zip(ps, gs, sts):
+            oracle.step(p, g, st, t, hp)
+        per_step.append(time.perf_counter() - a)
+    n = int(sum(np.prod(s) if s else 1 for s in shapes))
+    return per_step, n
+
+
+def cpu_baseline(wl, steps=2):
+    idx = oracle_sample(wl)
+    per_step, n = time_oracle(wl, idx, steps)
+    tot = sum(per_step)
+    return {"value": n * steps / tot, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(idx)} tensors ({n:,} values: "
+                      f"{'decoder layer 0' if wl.shapes[idx[0]][0].startswith('layers.0.') else 'leading tensors'}"
+                      f") x {steps} steps, float64 C oracle, single thread, inputs pre-generated",
+            "seconds": tot, "host_cpus": os.cpu_count()}
+
+
+def run_reference(args):
+    wl = synth.workload(args.workload)
+    idx = oracle_sample(wl)
+    warm, n = time_oracle(wl, idx, args.warmup) if args.warmup else ([], 0)
+    per_step, n = time_oracle(wl, idx, args.steps, t0=args.warmup + 1)
+    sec = sum(per_step) / len(per_step)
+    value = n / sec
+    return {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "params/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "description": wl.description, "params": wl.numel,
+                   "sampled_params_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{len(idx)} tensors ({n:,} values) per step, float64 C oracle, "
+                                   f"single thread"},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b",
+                    choices=["llama3_8b", "llama3_8b_beta1", "llama_layer", "llama_layer_bf16", "edge", "tiny"])
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    binding.load()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out, (wl, _) = run_ours(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * adafactor.h — C ABI of the GB300 Adafactor step library (libmeo_adafactor.so).
+ *
+ * One call, adafactor_step(), applies one Adafactor step to a whole list of
+ * tensors at once, on the caller's CUDA stream, with a fixed handful of kernel
+ * launches whatever the list length.  The method is the one described in the
+ * Colossal-AI distributed-optimizer article ("Colossal-AI 分布式优化器全解析：
+ * Adafactor、CAME、GaLore 与 LAMB 如何无缝对接 Tensor Parallel 与 ZeRO",
+ * blog.gitcode.com):
+ *   - optimizer table ("四种优化器：原理速览", Adafactor row): the [H, W] second
+ *     moment is kept as a row vector [H] and a column vector [W];
+ *   - Step 3: defaults, relative step size, the manual-lr error, warmup_init,
+ *     optional beta1 first moment, factored (ndim >= 2) vs. full second moment;
+ *   - Step 4: the RMS helper;
+ *   - Step 5: beta2t = 1 - t^decay_rate, the RMS clip of the update, the
+ *     relative-step lr scaled by max(eps[1], RMS(param)).
+ *
+ * Per tensor, with t the 1-based step and every RMS over the whole tensor:
+ *   rho   = relative_step ? min(warmup_init ? 1e-6 t : 1e-2, 1/sqrt(t)) : lr
+ *   alpha = scale_parameter ? rho * max(eps2, RMS(param before the step)) : rho
+ *   beta2 = 1 - t^decay_rate
+ *   ndim >= 2, viewed as [B, H, W] (B = product of the leading dims):
+ *     row[b,i] <- beta2 row[b,i] + (1-beta2) mean_j (g^2 + eps1)
+ *     col[b,j] <- beta2 col[b,j] + (1-beta2) mean_i (g^2 + eps1)
+ *     u = g * (row[b,i] / mean_i row[b,i])^-1/2 * col[b,j]^-1/2
+ *   ndim < 2:
+ *     v <- beta2 v + (1-beta2) (g^2 + eps1);   u = g / sqrt(v)
+ *   u <- alpha * u / max(1, RMS(u) / clip_threshold)
+ *   beta1 set:  exp_avg <- beta1 exp_avg + (1-beta1) u;  u <- exp_avg
+ *   param <- param - weight_decay * alpha * param - u
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     contiguous row-major.  The library never allocates device memory; the
+ *     caller owns params, grads, states and the workspace.
+ *   - Nothing is checked lazily: every argument check runs before the first
+ *     CUDA call, so a call that returns an error has changed nothing.
+ *   - No C++ exception crosses this interface.  A failing call returns a
+ *     non-zero adaf_status and leaves a message for adafactor_last_error()
+ *     (per host thread).
+ */
+#ifndef MEO_ADAFACTOR_H
+#define MEO_ADAFACTOR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum adaf_status {
+    ADAF_OK = 0,
+    ADAF_ERR_INVALID_ARGUMENT = 1,   /* bad hyper-parameter, pointer, shape or dtype */
+    ADAF_ERR_UNSUPPORTED = 2,        /* valid but outside what this build handles    */
+    ADAF_ERR_WORKSPACE_TOO_SMALL = 3,
+    ADAF_ERR_CUDA = 4                /* a CUDA runtime call or launch failed         */
+} adaf_status;
+
+typedef enum adaf_dtype {
+    ADAF_FLOAT32 = 0,
+    ADAF_BFLOAT16 = 1
+} adaf_dtype;
+
+#define ADAF_MAX_NDIM 8
+
+/* One parameter tensor and its gradient.
+ *   param      fp32 [N], updated in place; 4-byte aligned.
+ *   grad       grad_dtype [N], read only; aligned to its element size.
+ *   ndim       0..8.  ndim >= 2: factored over the last two dims
+ *              (B = shape[0]*...*shape[ndim-3], H = shape[ndim-2],
+ *              W = shape[ndim-1]).  ndim 0 or 1: full second moment.
+ *   shape      the first ndim entries are used; each >= 0.
+ * A tensor with N = 0 is skipped.  16-byte aligned param/grad/exp_avg with
+ * W a multiple of 8 take the vectorised kernels; anything else takes the
+ * element-wise kernels, with the same results. */
+typedef struct adaf_tensor {
+    float* param;
+    const void* grad;
+    int32_t grad_dtype;
+    int32_t ndim;
+    int64_t shape[ADAF_MAX_NDIM];
+} adaf_tensor;
+
+/* The optimizer state of one tensor (device pointers, fp32, zeroed by the
+ * caller before step 1).  Unused members may be NULL.
+ *   exp_avg_sq_row  [B*H]  factored tensors
+ *   exp_avg_sq_col  [B*W]  factored tensors
+ *   exp_avg_sq      [N]    tensors with ndim < 2
+ *   exp_avg         [N]    required when has_beta1
+ *   param_sq_sum    one double, optional.  When non-NULL the step writes
+ *                  sum(param^2) of the parameter it leaves behind, so that the
+ *                  next step can take RMS(param) without re-reading param
+ *                  (see adaf_hparams.param_sq_sum_valid). */
+typedef struct adaf_state {
+    float* exp_avg_sq_row;
+    float* exp_avg_sq_col;
+    float* exp_avg_sq;
+    float* exp_avg;
+    double* param_sq_sum;
+} adaf_state;
+
+/* Hyper-parameters (Step 3 of the article).  adafactor_default_hparams()
+ * fills the article's defaults: no lr, eps=(1e-30, 1e-3), clip_threshold 1.0,
+ * decay_rate -0.8, no beta1, weight_decay 0, scale_parameter, relative_step,
+ * no warmup_init.
+ *   param_sq_sum_valid  1 = every state's param_sq_sum holds sum(param^2) of
+ *                       the parameter as it is now (written by the previous
+ *                       step and untouched since); the step then skips one
+ *                       read of every parameter.  0 = recompute it.  Only read
+ *                       when scale_parameter is set. */
+typedef struct adaf_hparams {
+    double lr;
+    int32_t has_lr;
+    double eps1;
+    double eps2;
+    double clip_threshold;
+    double decay_rate;
+    double beta1;
+    int32_t has_beta1;
+    double weight_decay;
+    int32_t scale_parameter;
+    int32_t relative_step;
+    int32_t warmup_init;
+    int32_t param_sq_sum_valid;
+} adaf_hparams;
+
+/* Fills *hp with the article's defaults (Step 3).  hp must not be NULL. */
+void adafactor_default_hparams(adaf_hparams* hp);
+
+/* Checks the hyper-parameters alone (no CUDA call).  Errors, all
+ * ADAF_ERR_INVALID_ARGUMENT:
+ *   has_lr && relative_step      "Cannot combine manual lr and relative_step=True options"
+ *                                (the error quoted in Step 3)
+ *   warmup_init && !relative_step  (Step 3: warmup_init forces relative_step)
+ *   !has_lr && !relative_step    "relative_step=False requires a manual lr"
+ *   clip_threshold not finite or <= 0; has_lr with lr not finite or < 0;
+ *   eps1, eps2 or weight_decay not finite or < 0; decay_rate not finite;
+ *   has_beta1 with beta1 not in [0, 1). */
+adaf_status adafactor_validate(const adaf_hparams* hp);
+
+/* Bytes of device workspace adafactor_step() needs for this tensor list
+ * (256-byte aligned start required).  Pure host computation, no CUDA call.
+ * Fails with ADAF_ERR_INVALID_ARGUMENT on a malformed list (n < 0, NULL
+ * tensors with n > 0, bad ndim/shape/dtype) and ADAF_ERR_UNSUPPORTED when the
+ * list needs more than 2^31-1 work tiles. */
+adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size_t* bytes);
+
+/* One Adafactor step over tensors[0..n) with states[0..n), step t = `step`
+ * (>= 1), enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  The call only enqueues work: it never synchronises the host with
+ * the device, and it reads no device memory from the host.  Params and states
+ * are updated in place; grads are read only.  The workspace (>= the size
+ * reported by adafactor_workspace_size, 256-byte aligned) is scratch owned by
+ * this call until the enqueued work completes: calls that may run
+ * concurrently on the device need distinct workspaces.
+ * Errors: ADAF_ERR_INVALID_ARGUMENT (hyper-parameters as in
+ * adafactor_validate; step < 1; NULL or misaligned pointers; missing state
+ * buffers for a tensor's path; has_beta1 without exp_avg), ADAF_ERR_UNSUPPORTED,
+ * ADAF_ERR_WORKSPACE_TOO_SMALL, ADAF_ERR_CUDA (a CUDA call or a kernel launch
+ * failed; work enqueued before the failure may have run). */
+adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
+                           int64_t step, const adaf_hparams* hp, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* adafactor_last_error(void);
+
+/* Frees the library's host-side caches (pinned staging buffers, events) for
+ * every device.  Call only when no adafactor_step() work is in flight. */
+void adafactor_release_cache(void);
+
+/* ---- Kernel timing (CUDA events on the launching stream) ----------------
+ * adafactor_profile_enable(1) makes every following adafactor_step() record a
+ * CUDA event pair around each of its kernel launches on the launch stream;
+ * adafactor_profile_read() waits for the recorded events, adds the elapsed
+ * time per kernel kind into ms[k] and the launch count into launches[k] for
+ * k < min(nk, adafactor_num_kernels()), and forgets the records.
+ * adafactor_profile_enable(0) stops recording.  Errors: ADAF_ERR_CUDA. */
+adaf_status adafactor_profile_enable(int32_t on);
+adaf_status adafactor_profile_read(double* ms, int64_t* launches, int32_t nk);
+int32_t adafactor_num_kernels(void);
+const char* adafactor_kernel_name(int32_t k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEO_ADAFACTOR_H */

@@ -1,0 +1,169 @@
+"""ctypes binding of the C ABI in include/adafactor.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: all of the step runs in the CUDA library.  Loading
+fails loudly when the library has not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+ADAF_OK = 0
+ADAF_ERR_INVALID_ARGUMENT = 1
+ADAF_ERR_UNSUPPORTED = 2
+ADAF_ERR_WORKSPACE_TOO_SMALL = 3
+ADAF_ERR_CUDA = 4
+ADAF_FLOAT32 = 0
+ADAF_BFLOAT16 = 1
+ADAF_MAX_NDIM = 8
+
+# Entry points declared in include/adafactor.h.
+EXPORTS = (
+    "adafactor_default_hparams", "adafactor_validate", "adafactor_workspace_size",
+    "adafactor_step", "adafactor_last_error", "adafactor_release_cache",
+    "adafactor_profile_enable", "adafactor_profile_read", "adafactor_num_kernels",
+    "adafactor_kernel_name",
+)
+
+
+class adaf_tensor(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("grad_dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * ADAF_MAX_NDIM)]
+
+
+class adaf_state(ctypes.Structure):
+    _fields_ = [("exp_avg_sq_row", ctypes.c_void_p), ("exp_avg_sq_col", ctypes.c_void_p),
+                ("exp_avg_sq", ctypes.c_void_p), ("exp_avg", ctypes.c_void_p),
+                ("param_sq_sum", ctypes.c_void_p)]
+
+
+class adaf_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("has_lr", ctypes.c_int32),
+                ("eps1", ctypes.c_double), ("eps2", ctypes.c_double),
+                ("clip_threshold", ctypes.c_double), ("decay_rate", ctypes.c_double),
+                ("beta1", ctypes.c_double), ("has_beta1", ctypes.c_int32),
+                ("weight_decay", ctypes.c_double), ("scale_parameter", ctypes.c_int32),
+                ("relative_step", ctypes.c_int32), ("warmup_init", ctypes.c_int32),
+                ("param_sq_sum_valid", ctypes.c_int32)]
+
+
+class AdafactorError(RuntimeError):
+    """A non-zero adaf_status other than an argument error."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"adafactor status {status}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Loads libmeo_adafactor.so; raises if it is missing (no CPU fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -m memory_efficient_optimizer_gb300.build` "
+                    "(there is no fallback implementation)")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.POINTER
+        lib.adafactor_default_hparams.restype = None
+        lib.adafactor_default_hparams.argtypes = [P(adaf_hparams)]
+        lib.adafactor_validate.restype = ctypes.c_int
+        lib.adafactor_validate.argtypes = [P(adaf_hparams)]
+        lib.adafactor_workspace_size.restype = ctypes.c_int
+        lib.adafactor_workspace_size.argtypes = [P(adaf_tensor), ctypes.c_int32, P(ctypes.c_size_t)]
+        lib.adafactor_step.restype = ctypes.c_int
+        lib.adafactor_step.argtypes = [P(adaf_tensor), P(adaf_state), ctypes.c_int32, ctypes.c_int64,
+                                       P(adaf_hparams), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        lib.adafactor_last_error.restype = ctypes.c_char_p
+        lib.adafactor_last_error.argtypes = []
+        lib.adafactor_release_cache.restype = None
+        lib.adafactor_release_cache.argtypes = []
+        lib.adafactor_profile_enable.restype = ctypes.c_int
+        lib.adafactor_profile_enable.argtypes = [ctypes.c_int32]
+        lib.adafactor_profile_read.restype = ctypes.c_int
+        lib.adafactor_profile_read.argtypes = [P(ctypes.c_double), P(ctypes.c_int64), ctypes.c_int32]
+        lib.adafactor_num_kernels.restype = ctypes.c_int32
+        lib.adafactor_num_kernels.argtypes = []
+        lib.adafactor_kernel_name.restype = ctypes.c_char_p
+        lib.adafactor_kernel_name.argtypes = [ctypes.c_int32]
+        _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status == ADAF_OK:
+        return
+    msg = adafactor_last_error()
+    if status == ADAF_ERR_INVALID_ARGUMENT:
+        raise ValueError(msg)
+    raise AdafactorError(status, msg)
+
+
+def adafactor_default_hparams() -> adaf_hparams:
+    hp = adaf_hparams()
+    load().adafactor_default_hparams(ctypes.byref(hp))
+    return hp
+
+
+def adafactor_validate(hp: adaf_hparams) -> None:
+    _check(load().adafactor_validate(ctypes.byref(hp)))
+
+
+def adafactor_workspace_size(tensors, n: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().adafactor_workspace_size(tensors, int(n), ctypes.byref(out)))
+    return int(out.value)
+
+
+def adafactor_step(tensors, states, n: int, step: int, hp: adaf_hparams, workspace: int,
+                   workspace_bytes: int, stream: int) -> None:
+    _check(load().adafactor_step(tensors, states, int(n), int(step), ctypes.byref(hp),
+                                 ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes),
+                                 ctypes.c_void_p(stream)))
+
+
+def adafactor_last_error() -> str:
+    return load().adafactor_last_error().decode(errors="replace")
+
+
+def adafactor_release_cache() -> None:
+    load().adafactor_release_cache()
+
+
+def adafactor_profile_enable(on: bool) -> None:
+    _check(load().adafactor_profile_enable(1 if on else 0))
+
+
+def adafactor_num_kernels() -> int:
+    return int(load().adafactor_num_kernels())
+
+
+def adafactor_kernel_name(k: int) -> str:
+    return load().adafactor_kernel_name(int(k)).decode()
+
+
+def adafactor_profile_read() -> dict:
+    """{kernel name: (total ms, launches)} for the events recorded since the last read."""
+    nk = adafactor_num_kernels()
+    ms = (ctypes.c_double * nk)()
+    launches = (ctypes.c_int64 * nk)()
+    _check(load().adafactor_profile_read(ms, launches, nk))
+    return {adafactor_kernel_name(k): (float(ms[k]), int(launches[k])) for k in range(nk)}

@@ -1,0 +1,543 @@
+// Host side of the C ABI declared in include/adafactor.h: argument checks,
+// the per-call plan (tiling, workspace layout, device descriptor table), the
+// pinned staging of that table, the launch sequence and the optional
+// per-kernel event timing.
+#include "adafactor.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "adafactor_internal.h"
+
+namespace {
+
+using meo::DevTensor;
+using meo::KernelId;
+using meo::StepArgs;
+
+thread_local std::string g_last_error;
+
+adaf_status fail(adaf_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+adaf_status cuda_fail(cudaError_t e, const char* what) {
+  std::string m = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return fail(ADAF_ERR_CUDA, m);
+}
+
+bool finite_nonneg(double x) { return std::isfinite(x) && x >= 0.0; }
+
+adaf_status check_hparams(const adaf_hparams* hp) {
+  if (hp == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "hparams is NULL");
+  // Step 3 of the article: manual lr and relative_step exclude each other;
+  // warmup_init forces relative_step.
+  if (hp->has_lr && hp->relative_step)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "Cannot combine manual lr and relative_step=True options");
+  if (hp->warmup_init && !hp->relative_step)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "warmup_init=True requires relative_step=True");
+  if (!hp->has_lr && !hp->relative_step)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "relative_step=False requires a manual lr");
+  if (!(std::isfinite(hp->clip_threshold) && hp->clip_threshold > 0.0))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "clip_threshold must be finite and > 0");
+  if (hp->has_lr && !finite_nonneg(hp->lr))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "lr must be finite and >= 0");
+  if (!finite_nonneg(hp->eps1) || !finite_nonneg(hp->eps2))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "eps values must be finite and >= 0");
+  if (!std::isfinite(hp->decay_rate)) return fail(ADAF_ERR_INVALID_ARGUMENT, "decay_rate must be finite");
+  if (!finite_nonneg(hp->weight_decay))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "weight_decay must be finite and >= 0");
+  if (hp->has_beta1 && !(hp->beta1 >= 0.0 && hp->beta1 < 1.0))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "beta1 must be in [0, 1)");
+  return ADAF_OK;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Geometry of one call: device descriptors (pointers filled later) and the
+// workspace layout.  Tensors with no elements are dropped.
+struct Plan {
+  std::vector<DevTensor> dev;       // one per non-empty tensor
+  std::vector<int32_t> pf_tiles, pf_items;
+  // Per tensor class: member tensor indices and the prefix of their tiles.
+  std::vector<int32_t> cls_idx[meo::kNumClasses], cls_pf[meo::kNumClasses];
+  size_t off_pf_tiles = 0, off_pf_items = 0, header_bytes = 0;
+  size_t off_cls_idx[meo::kNumClasses] = {}, off_cls_pf[meo::kNumClasses] = {};
+  size_t off_alpha = 0, off_coef = 0, off_mrow = 0, off_rowchunk = 0, off_spart = 0, off_ppart = 0;
+  size_t off_rowpart = 0, off_colpart = 0, total_bytes = 0;
+  bool any_factored = false;
+};
+
+// Checks the tensor list and builds the plan.  With full == false (size
+// query) only the shapes and dtypes are read; states and hp are not touched.
+adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
+                      const adaf_hparams* hp, bool full, Plan* plan) {
+  if (n < 0) return fail(ADAF_ERR_INVALID_ARGUMENT, "n must be >= 0");
+  if (n > 0 && tensors == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "tensors is NULL");
+  int64_t tiles = 0, ftiles = 0, items = 0, nmrow = 0, nrowchunk = 0, nrowpart = 0, ncolpart = 0;
+  plan->dev.clear();
+  plan->dev.reserve(n);
+  for (int32_t k = 0; k < n; ++k) {
+    const adaf_tensor& t = tensors[k];
+    char pre[64];
+    std::snprintf(pre, sizeof(pre), "tensor %d: ", k);
+    if (t.ndim < 0 || t.ndim > ADAF_MAX_NDIM)
+      return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "ndim must be in [0, 8]");
+    if (t.grad_dtype != ADAF_FLOAT32 && t.grad_dtype != ADAF_BFLOAT16)
+      return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "grad_dtype must be ADAF_FLOAT32 or ADAF_BFLOAT16");
+    int64_t numel = 1;
+    for (int32_t d = 0; d < t.ndim; ++d) {
+      if (t.shape[d] < 0) return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "negative dimension");
+      if (t.shape[d] != 0 && numel > (int64_t(1) << 50) / t.shape[d])
+        return fail(ADAF_ERR_UNSUPPORTED, std::string(pre) + "more than 2^50 elements");
+      numel *= t.shape[d];
+    }
+    if (numel == 0) continue;
+    const size_t gsz = t.grad_dtype == ADAF_BFLOAT16 ? 2 : 4;
+    if (full) {
+      if (t.param == nullptr || !aligned(t.param, 4))
+        return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "param is NULL or not 4-byte aligned");
+      if (t.grad == nullptr || !aligned(t.grad, gsz))
+        return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "grad is NULL or misaligned");
+    }
+    DevTensor d;
+    std::memset(&d, 0, sizeof(d));
+    d.n = numel;
+    d.gdt = t.grad_dtype == ADAF_BFLOAT16 ? meo::kGradBF16 : meo::kGradF32;
+    int64_t ntiles;
+    if (t.ndim >= 2) {
+      const int64_t H = t.shape[t.ndim - 2], W = t.shape[t.ndim - 1];
+      const int64_t B = numel / (H * W);
+      if (B > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, std::string(pre) + "too many leading slices");
+      d.H = H;
+      d.W = W;
+      d.B = static_cast<int32_t>(B);
+      d.rb = static_cast<int32_t>(ceil_div(H, meo::kTileRows));
+      d.cb = static_cast<int32_t>(ceil_div(W, meo::kTileCols));
+      d.nrc = static_cast<int32_t>(ceil_div(H, meo::kRowChunk));
+      d.ncc = static_cast<int32_t>(ceil_div(W, meo::kColChunk));
+      ntiles = B * d.rb * d.cb;
+      ftiles += ntiles;
+      items += B * (d.nrc + d.ncc);
+      d.mslot = nmrow;
+      nmrow += B;
+      d.rowchunk = nrowchunk;
+      nrowchunk += B * d.nrc;
+      d.rowpart = nrowpart;
+      nrowpart += static_cast<int64_t>(d.cb) * B * H;
+      d.colpart = ncolpart;
+      ncolpart += B * d.rb * W;
+      plan->any_factored = true;
+    } else {
+      d.H = 1;
+      d.W = numel;
+      d.B = 1;
+      ntiles = ceil_div(numel, meo::kTile1D);
+      d.rb = 1;
+      d.cb = static_cast<int32_t>(ntiles > INT32_MAX ? INT32_MAX : ntiles);
+      d.kind = meo::kUnfactored;
+    }
+    d.tile0 = tiles;
+    tiles += ntiles;
+    if (tiles > INT32_MAX || items > INT32_MAX)
+      return fail(ADAF_ERR_UNSUPPORTED, "the tensor list needs more than 2^31-1 work tiles");
+    if (full) {
+      const adaf_state& s = states[k];
+      d.p = t.param;
+      d.g = t.grad;
+      if (t.ndim >= 2) {
+        if (s.exp_avg_sq_row == nullptr || s.exp_avg_sq_col == nullptr || !aligned(s.exp_avg_sq_row, 4) ||
+            !aligned(s.exp_avg_sq_col, 4))
+          return fail(ADAF_ERR_INVALID_ARGUMENT,
+                      std::string(pre) + "factored tensor needs exp_avg_sq_row and exp_avg_sq_col");
+        d.row = s.exp_avg_sq_row;
+        d.col = s.exp_avg_sq_col;
+      } else {
+        if (s.exp_avg_sq == nullptr || !aligned(s.exp_avg_sq, 4))
+          return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "tensor with ndim < 2 needs exp_avg_sq");
+        d.v = s.exp_avg_sq;
+      }
+      if (hp->has_beta1) {
+        if (s.exp_avg == nullptr || !aligned(s.exp_avg, 4))
+          return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "beta1 is set but exp_avg is NULL");
+        d.m1 = s.exp_avg;
+      }
+      if (s.param_sq_sum != nullptr && !aligned(s.param_sq_sum, 8))
+        return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "param_sq_sum is not 8-byte aligned");
+      if (hp->scale_parameter && hp->param_sq_sum_valid && s.param_sq_sum == nullptr)
+        return fail(ADAF_ERR_INVALID_ARGUMENT,
+                    std::string(pre) + "param_sq_sum_valid is set but param_sq_sum is NULL");
+      d.psq = s.param_sq_sum;
+      if (t.ndim >= 2) {
+        const bool vec = (d.W % 8 == 0) && aligned(t.param, 16) && aligned(t.grad, 16) &&
+                         (!hp->has_beta1 || aligned(s.exp_avg, 16));
+        d.kind = vec ? meo::kFactoredVec : meo::kFactoredScalar;
+      }
+    } else if (t.ndim >= 2) {
+      d.kind = meo::kFactoredScalar;
+    }
+    plan->dev.push_back(d);
+  }
+  const size_t nd = plan->dev.size();
+  plan->pf_tiles.assign(nd + 1, 0);
+  plan->pf_items.assign(nd + 1, 0);
+  for (int c = 0; c < meo::kNumClasses; ++c) {
+    plan->cls_idx[c].clear();
+    plan->cls_pf[c].assign(1, 0);
+  }
+  for (size_t k = 0; k < nd; ++k) {
+    const DevTensor& d = plan->dev[k];
+    const int64_t nt = d.kind == meo::kUnfactored ? d.cb : int64_t(d.B) * d.rb * d.cb;
+    plan->pf_tiles[k + 1] = plan->pf_tiles[k] + static_cast<int32_t>(nt);
+    plan->pf_items[k + 1] =
+        plan->pf_items[k] + (d.kind == meo::kUnfactored ? 0 : static_cast<int32_t>(int64_t(d.B) * (d.nrc + d.ncc)));
+    int c = meo::kClsUnfactored;
+    if (d.kind == meo::kFactoredVec) c = d.gdt == meo::kGradBF16 ? meo::kClsVecBF16 : meo::kClsVecF32;
+    if (d.kind == meo::kFactoredScalar) c = d.gdt == meo::kGradBF16 ? meo::kClsScalarBF16 : meo::kClsScalarF32;
+    plan->cls_idx[c].push_back(static_cast<int32_t>(k));
+    plan->cls_pf[c].push_back(plan->cls_pf[c].back() + static_cast<int32_t>(nt));
+  }
+  // Workspace layout: the header (uploaded each call) first, then scratch;
+  // every scratch region 256-byte aligned.
+  size_t off = align_up(nd * sizeof(DevTensor), 256);
+  plan->off_pf_tiles = off;
+  off += align_up((nd + 1) * sizeof(int32_t), 16);
+  plan->off_pf_items = off;
+  off += align_up((nd + 1) * sizeof(int32_t), 16);
+  for (int c = 0; c < meo::kNumClasses; ++c) {
+    plan->off_cls_pf[c] = off;
+    off += align_up(plan->cls_pf[c].size() * sizeof(int32_t), 16);
+    plan->off_cls_idx[c] = off;
+    off += align_up(plan->cls_idx[c].size() * sizeof(int32_t), 16);
+  }
+  plan->header_bytes = off;
+  off = align_up(off, 256);
+  plan->off_alpha = off;
+  off = align_up(off + nd * sizeof(double), 256);
+  plan->off_coef = off;
+  off = align_up(off + nd * sizeof(double), 256);
+  plan->off_mrow = off;
+  off = align_up(off + nmrow * sizeof(double), 256);
+  plan->off_rowchunk = off;
+  off = align_up(off + nrowchunk * sizeof(double), 256);
+  plan->off_spart = off;
+  off = align_up(off + tiles * sizeof(double), 256);
+  plan->off_ppart = off;
+  off = align_up(off + tiles * sizeof(double), 256);
+  plan->off_rowpart = off;
+  off = align_up(off + nrowpart * sizeof(float), 256);
+  plan->off_colpart = off;
+  off = align_up(off + ncolpart * sizeof(float), 256);
+  plan->total_bytes = off;
+  return ADAF_OK;
+}
+
+// ---- pinned staging of the descriptor table -------------------------------
+// A small ring of pinned host buffers per device; a slot is reused only after
+// the event recorded behind its previous copy has completed, so the host never
+// overwrites bytes a pending cudaMemcpyAsync still has to read.
+constexpr int kSlots = 4;
+struct Slot {
+  void* host = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;
+  bool pending = false;
+};
+struct DeviceCache {
+  Slot slots[kSlots];
+  int next = 0;
+  std::vector<cudaEvent_t> free_events;
+};
+
+struct ProfRecord {
+  int kernel;
+  int device;
+  cudaEvent_t start, stop;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceCache> g_cache;
+bool g_profile = false;
+std::vector<ProfRecord> g_prof;
+
+cudaError_t get_event(DeviceCache& dc, cudaEvent_t* ev) {
+  if (!dc.free_events.empty()) {
+    *ev = dc.free_events.back();
+    dc.free_events.pop_back();
+    return cudaSuccess;
+  }
+  return cudaEventCreate(ev);
+}
+
+}  // namespace
+
+extern "C" {
+
+void adafactor_default_hparams(adaf_hparams* hp) {
+  if (hp == nullptr) return;
+  std::memset(hp, 0, sizeof(*hp));
+  hp->lr = 0.0;
+  hp->has_lr = 0;
+  hp->eps1 = 1e-30;
+  hp->eps2 = 1e-3;
+  hp->clip_threshold = 1.0;
+  hp->decay_rate = -0.8;
+  hp->beta1 = 0.0;
+  hp->has_beta1 = 0;
+  hp->weight_decay = 0.0;
+  hp->scale_parameter = 1;
+  hp->relative_step = 1;
+  hp->warmup_init = 0;
+  hp->param_sq_sum_valid = 0;
+}
+
+adaf_status adafactor_validate(const adaf_hparams* hp) { return check_hparams(hp); }
+
+adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size_t* bytes) {
+  if (bytes == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  Plan plan;
+  adaf_status st = make_plan(tensors, nullptr, n, nullptr, false, &plan);
+  if (st != ADAF_OK) return st;
+  *bytes = plan.total_bytes;
+  return ADAF_OK;
+}
+
+adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
+                           const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream) {
+  adaf_status st = check_hparams(hp);
+  if (st != ADAF_OK) return st;
+  if (step < 1) return fail(ADAF_ERR_INVALID_ARGUMENT, "step must be >= 1");
+  if (n > 0 && states == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "states is NULL");
+  Plan plan;
+  st = make_plan(tensors, states, n, hp, true, &plan);
+  if (st != ADAF_OK) return st;
+  const size_t nd = plan.dev.size();
+  if (nd == 0) return ADAF_OK;
+  if (workspace == nullptr || !aligned(workspace, 256))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "workspace is NULL or not 256-byte aligned");
+  if (workspace_bytes < plan.total_bytes) {
+    char msg[128];
+    std::snprintf(msg, sizeof(msg), "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
+                  plan.total_bytes);
+    return fail(ADAF_ERR_WORKSPACE_TOO_SMALL, msg);
+  }
+
+  // Per-step scalars (Step 3 / Step 5 of the article), in double on the host.
+  const double t = static_cast<double>(step);
+  double rho = hp->lr;
+  if (hp->relative_step) {
+    const double cap = hp->warmup_init ? 1e-6 * t : 1e-2;
+    const double inv = 1.0 / std::sqrt(t);
+    rho = cap < inv ? cap : inv;
+  }
+  const double beta2 = 1.0 - std::pow(t, hp->decay_rate);
+  bool any_psq = false;
+  for (const DevTensor& d : plan.dev) any_psq = any_psq || d.psq != nullptr;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int grid_limit[meo::kNumKernels];
+  for (int k = 0; k < meo::kNumKernels; ++k) {
+    grid_limit[k] = meo::kernel_grid_limit(static_cast<KernelId>(k), device, &e);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel occupancy query");
+  }
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceCache& dc = g_cache[device];
+  // Stage the header (descriptors + prefix arrays) and copy it to the workspace.
+  Slot& slot = dc.slots[dc.next];
+  dc.next = (dc.next + 1) % kSlots;
+  if (slot.pending) {
+    e = cudaEventSynchronize(slot.done);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize (staging slot)");
+    slot.pending = false;
+  }
+  if (slot.cap < plan.header_bytes) {
+    if (slot.host != nullptr) cudaFreeHost(slot.host);
+    slot.host = nullptr;
+    slot.cap = 0;
+    const size_t cap = align_up(plan.header_bytes, size_t(1) << 16);
+    e = cudaHostAlloc(&slot.host, cap, cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc (staging)");
+    slot.cap = cap;
+  }
+  if (slot.done == nullptr) {
+    e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate (staging)");
+  }
+  unsigned char* h = static_cast<unsigned char*>(slot.host);
+  std::memcpy(h, plan.dev.data(), nd * sizeof(DevTensor));
+  std::memcpy(h + plan.off_pf_tiles, plan.pf_tiles.data(), (nd + 1) * sizeof(int32_t));
+  std::memcpy(h + plan.off_pf_items, plan.pf_items.data(), (nd + 1) * sizeof(int32_t));
+  for (int c = 0; c < meo::kNumClasses; ++c) {
+    std::memcpy(h + plan.off_cls_pf[c], plan.cls_pf[c].data(), plan.cls_pf[c].size() * sizeof(int32_t));
+    if (!plan.cls_idx[c].empty())
+      std::memcpy(h + plan.off_cls_idx[c], plan.cls_idx[c].data(), plan.cls_idx[c].size() * sizeof(int32_t));
+  }
+  e = cudaMemcpyAsync(ws, h, plan.header_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (descriptor table)");
+  e = cudaEventRecord(slot.done, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");
+  slot.pending = true;
+
+  StepArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.tensors = reinterpret_cast<const DevTensor*>(ws);
+  a.pf_tiles = reinterpret_cast<const int32_t*>(ws + plan.off_pf_tiles);
+  a.pf_items = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
+  a.alpha = reinterpret_cast<double*>(ws + plan.off_alpha);
+  a.coef = reinterpret_cast<double*>(ws + plan.off_coef);
+  a.mrow = reinterpret_cast<double*>(ws + plan.off_mrow);
+  a.rowchunk = reinterpret_cast<double*>(ws + plan.off_rowchunk);
+  a.spart = reinterpret_cast<double*>(ws + plan.off_spart);
+  a.ppart = reinterpret_cast<double*>(ws + plan.off_ppart);
+  a.rowpart = reinterpret_cast<float*>(ws + plan.off_rowpart);
+  a.colpart = reinterpret_cast<float*>(ws + plan.off_colpart);
+  a.beta2 = beta2;
+  a.rho = rho;
+  a.eps1 = hp->eps1;
+  a.eps2 = hp->eps2;
+  a.clip = hp->clip_threshold;
+  a.beta1 = hp->has_beta1 ? hp->beta1 : 0.0;
+  a.wd = hp->weight_decay;
+  a.scale_parameter = hp->scale_parameter ? 1 : 0;
+  a.has_beta1 = hp->has_beta1 ? 1 : 0;
+  a.psq_valid = (hp->scale_parameter && hp->param_sq_sum_valid) ? 1 : 0;
+  a.want_psq_out = any_psq ? 1 : 0;
+
+  // One launch helper: optional profiling events around the launch.
+  auto run = [&](KernelId k, auto&& launch) -> adaf_status {
+    ProfRecord rec{static_cast<int>(k), device, nullptr, nullptr};
+    cudaError_t err;
+    if (g_profile) {
+      if ((err = get_event(dc, &rec.start)) != cudaSuccess) return cuda_fail(err, "cudaEventCreate (profile)");
+      if ((err = get_event(dc, &rec.stop)) != cudaSuccess) return cuda_fail(err, "cudaEventCreate (profile)");
+      if ((err = cudaEventRecord(rec.start, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord (profile)");
+    }
+    err = launch();
+    if (err != cudaSuccess) return cuda_fail(err, meo::kernel_name(k));
+    if (g_profile) {
+      if ((err = cudaEventRecord(rec.stop, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord (profile)");
+      g_prof.push_back(rec);
+    }
+    return ADAF_OK;
+  };
+  // A streaming kind over every class that has members, in groups of at most
+  // kMaxGroup tensors (the kernels keep a group's prefix in shared memory).
+  auto stream_all = [&](KernelId k, bool factored_only) -> adaf_status {
+    for (int c = 0; c < meo::kNumClasses; ++c) {
+      if (factored_only && c == meo::kClsUnfactored) continue;
+      const int32_t m = static_cast<int32_t>(plan.cls_idx[c].size());
+      const int32_t* pf_dev = reinterpret_cast<const int32_t*>(ws + plan.off_cls_pf[c]);
+      const int32_t* idx_dev = reinterpret_cast<const int32_t*>(ws + plan.off_cls_idx[c]);
+      for (int32_t g0 = 0; g0 < m; g0 += meo::kMaxGroup) {
+        const int32_t g1 = g0 + meo::kMaxGroup < m ? g0 + meo::kMaxGroup : m;
+        const int64_t units = plan.cls_pf[c][g1] - plan.cls_pf[c][g0];
+        const int grid = static_cast<int>(units < grid_limit[k] ? units : grid_limit[k]);
+        const meo::Range r{pf_dev, idx_dev, g0, g1};
+        const meo::TensorClass tc = static_cast<meo::TensorClass>(c);
+        adaf_status rs = run(k, [&] { return meo::launch_stream(k, tc, a, r, grid, s); });
+        if (rs != ADAF_OK) return rs;
+      }
+    }
+    return ADAF_OK;
+  };
+  const int nd_i = static_cast<int>(nd);
+  if ((st = stream_all(meo::kKPass1, false)) != ADAF_OK) return st;
+  if (plan.any_factored) {
+    const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
+    for (int32_t g0 = 0; g0 < nd_i; g0 += meo::kMaxGroup) {
+      const int32_t g1 = g0 + meo::kMaxGroup < nd_i ? g0 + meo::kMaxGroup : nd_i;
+      const int64_t units = plan.pf_items[g1] - plan.pf_items[g0];
+      if (units == 0) continue;
+      const int grid = static_cast<int>(units < grid_limit[meo::kKStats] ? units : grid_limit[meo::kKStats]);
+      const meo::Range r{pf_items_dev, nullptr, g0, g1};
+      st = run(meo::kKStats, [&] { return meo::launch_stats(a, r, grid, s); });
+      if (st != ADAF_OK) return st;
+    }
+  }
+  st = run(meo::kKScalars, [&] { return meo::launch_per_tensor(meo::kKScalars, a, nd_i, s); });
+  if (st != ADAF_OK) return st;
+  if ((st = stream_all(meo::kKPass2, true)) != ADAF_OK) return st;
+  st = run(meo::kKClip, [&] { return meo::launch_per_tensor(meo::kKClip, a, nd_i, s); });
+  if (st != ADAF_OK) return st;
+  if ((st = stream_all(meo::kKApply, false)) != ADAF_OK) return st;
+  if (any_psq) {
+    st = run(meo::kKPsq, [&] { return meo::launch_per_tensor(meo::kKPsq, a, nd_i, s); });
+    if (st != ADAF_OK) return st;
+  }
+  return ADAF_OK;
+}
+
+const char* adafactor_last_error(void) { return g_last_error.c_str(); }
+
+void adafactor_release_cache(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  const bool have_dev = cudaGetDevice(&cur) == cudaSuccess;
+  for (auto& kv : g_cache) {
+    if (cudaSetDevice(kv.first) != cudaSuccess) continue;
+    for (Slot& sl : kv.second.slots) {
+      if (sl.pending && sl.done) cudaEventSynchronize(sl.done);
+      if (sl.done) cudaEventDestroy(sl.done);
+      if (sl.host) cudaFreeHost(sl.host);
+      sl = Slot();
+    }
+    for (cudaEvent_t ev : kv.second.free_events) cudaEventDestroy(ev);
+    kv.second.free_events.clear();
+  }
+  for (ProfRecord& r : g_prof) {
+    if (cudaSetDevice(r.device) == cudaSuccess) {
+      cudaEventDestroy(r.start);
+      cudaEventDestroy(r.stop);
+    }
+  }
+  g_prof.clear();
+  g_cache.clear();
+  if (have_dev) cudaSetDevice(cur);
+}
+
+adaf_status adafactor_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_profile = on != 0;
+  return ADAF_OK;
+}
+
+adaf_status adafactor_profile_read(double* ms, int64_t* launches, int32_t nk) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  adaf_status st = ADAF_OK;
+  for (ProfRecord& r : g_prof) {
+    float el = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&el, r.start, r.stop);
+    if (e != cudaSuccess && st == ADAF_OK) st = cuda_fail(e, "profile event");
+    if (r.kernel < nk) {
+      if (ms) ms[r.kernel] += el;
+      if (launches) launches[r.kernel] += 1;
+    }
+    DeviceCache& dc = g_cache[r.device];
+    dc.free_events.push_back(r.start);
+    dc.free_events.push_back(r.stop);
+  }
+  g_prof.clear();
+  return st;
+}
+
+int32_t adafactor_num_kernels(void) { return meo::kNumKernels; }
+
+const char* adafactor_kernel_name(int32_t k) { return meo::kernel_name(k); }
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// Internal definitions shared by the host planner (adafactor_api.cpp) and the
+// kernels (adafactor_kernels.cu).  Not part of the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace meo {
+
+// ---- tiling ---------------------------------------------------------------
+// A factored tensor [B, H, W] is cut into tiles of kTileRows rows x kTileCols
+// columns inside one slice b.  One CTA of kThreads threads streams a tile:
+// warp w takes rows w, w + kWarps, ...; each lane owns kTileCols / 32 columns
+// of the tile (8 consecutive ones per 256-column chunk on the vector path,
+// one per 32-column chunk on the element-wise path).
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTileRows = 256;
+constexpr int kTileCols = 1024;
+// A tensor with ndim < 2 is cut into flat tiles of kTile1D elements.
+constexpr int kTile1D = 8192;
+// Statistics kernel: a row item covers kRowChunk rows of one slice, a column
+// item kColChunk columns of one slice.
+constexpr int kRowChunk = 1024;
+constexpr int kColChunk = 256;
+// Tensors handled by one launch sequence (prefix arrays live in shared memory).
+constexpr int kMaxGroup = 4096;
+
+enum TensorKind : int32_t {
+  kFactoredVec = 0,   // ndim >= 2, W % 8 == 0, 16-byte aligned pointers
+  kFactoredScalar = 1,// ndim >= 2, anything else
+  kUnfactored = 2,    // ndim < 2
+};
+
+enum GradType : int32_t { kGradF32 = 0, kGradBF16 = 1 };
+
+// Device-side descriptor of one tensor (built on the host each call).
+struct DevTensor {
+  float* p;
+  const void* g;
+  float* row;     // [B*H]
+  float* col;     // [B*W]
+  float* v;       // [N]      unfactored
+  float* m1;      // [N]      beta1
+  double* psq;    // [1]      optional sum(p^2) carry
+  int64_t n;      // numel
+  int64_t H, W;   // factored: matrix dims; unfactored: 1, n
+  int32_t B;      // leading slices
+  int32_t kind;   // TensorKind
+  int32_t gdt;    // GradType
+  int32_t rb;     // row blocks per slice   (ceil(H / kTileRows)); unfactored: 1
+  int32_t cb;     // column blocks          (ceil(W / kTileCols)); unfactored: tiles
+  int32_t nrc;    // row chunks per slice   (ceil(H / kRowChunk))
+  int32_t ncc;    // column chunks per slice(ceil(W / kColChunk))
+  int32_t pad0;
+  int64_t tile0;      // global index of the tensor's first tile (Spart/Ppart slot)
+  int64_t rowpart;    // float offset of rowpart [cb][B*H]
+  int64_t colpart;    // float offset of colpart [B][rb][W]
+  int64_t rowchunk;   // double offset of row-chunk sums [B][nrc]
+  int64_t mslot;      // double offset of mean(row) [B]
+};
+static_assert(sizeof(DevTensor) % 8 == 0, "DevTensor must stay 8-byte packed");
+
+// Tensor classes: every streaming kernel is compiled per class so that each
+// instantiation gets its own register allocation, and one launch covers all
+// tensors of a class.
+enum TensorClass : int32_t {
+  kClsVecBF16 = 0,     // factored, vector path, bf16 grads
+  kClsVecF32 = 1,      // factored, vector path, fp32 grads
+  kClsScalarBF16 = 2,  // factored, element-wise path, bf16 grads
+  kClsScalarF32 = 3,   // factored, element-wise path, fp32 grads
+  kClsUnfactored = 4,  // ndim < 2 (any grad dtype)
+  kNumClasses = 5
+};
+
+// Per-call scalars and workspace regions, passed by value to every kernel.
+struct StepArgs {
+  const DevTensor* tensors;
+  const int32_t* pf_tiles;   // [n+1] prefix of tiles over all tensors (tile0)
+  const int32_t* pf_items;   // [n+1] prefix of statistics items (K2)
+  double* alpha;             // [n]   effective lr
+  double* coef;              // [n]   alpha / max(1, RMS(u)/d)
+  double* mrow;              // mean(row) per slice, via DevTensor::mslot
+  double* rowchunk;          // row-chunk sums of the updated row vector
+  double* spart;             // [tiles] partial sum(u^2)
+  double* ppart;             // [tiles] partial sum(p^2)
+  float* rowpart;
+  float* colpart;
+  double beta2;
+  double rho;
+  double eps1, eps2, clip, beta1, wd;
+  int32_t scale_parameter;
+  int32_t has_beta1;
+  int32_t psq_valid;         // use DevTensor::psq instead of re-reading p
+  int32_t want_psq_out;      // apply writes ppart for the carry
+};
+
+// The tensors one launch covers: members idx[m_begin..m_end) of a tensor
+// index list, with pf[m] the first unit (tile or item) of member m relative to
+// pf[m_begin] (the kernel copies pf[m_begin..m_end] to shared memory).
+struct Range {
+  const int32_t* pf;
+  const int32_t* idx;
+  int32_t m_begin, m_end;
+};
+
+// Kernel kinds, in launch order (also the profiling slots).
+enum KernelId : int {
+  kKPass1 = 0,     // read g (and p if needed): row/col partials, 1D v update
+  kKStats = 1,     // row/col EMA update from the partials
+  kKScalars = 2,   // per tensor: alpha, mean(row)
+  kKPass2 = 3,     // read g: partial sum(u^2)
+  kKClip = 4,      // per tensor: clip factor -> coef
+  kKApply = 5,     // read g, p (exp_avg): write p (exp_avg), partial sum(p^2)
+  kKPsq = 6,       // per tensor: sum(p^2) carry
+  kNumKernels = 7
+};
+
+// Launchers (adafactor_kernels.cu).  Streaming kinds (pass1, pass2, apply)
+// take a class and a member range; stats takes a member range over all
+// tensors; the per-tensor kinds take a tensor count as grid.  Each returns the
+// launch's cudaError_t.
+cudaError_t launch_stream(KernelId k, TensorClass c, const StepArgs& a, const Range& r, int grid,
+                          cudaStream_t s);
+cudaError_t launch_stats(const StepArgs& a, const Range& r, int grid, cudaStream_t s);
+cudaError_t launch_per_tensor(KernelId k, const StepArgs& a, int ntensors, cudaStream_t s);
+// Resident-CTA limit (CTAs per SM x SMs) for a kernel kind on a device.
+int kernel_grid_limit(KernelId k, int device, cudaError_t* err);
+const char* kernel_name(int k);
+
+}  // namespace meo

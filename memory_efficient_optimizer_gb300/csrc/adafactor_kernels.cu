@@ -1,0 +1,786 @@
+// Kernels of the GB300 Adafactor step.
+//
+// The step is bandwidth bound (a handful of flops per byte, no contraction),
+// so the kernels are built around streaming the gradient three times and the
+// parameter once (read + write) with coalesced 16-byte loads, persistent grids
+// sized to the SM count, and deterministic two-stage reductions: per-tile
+// partials written once, then summed in a fixed order (no float atomics, so
+// two runs give bit-identical results).
+//
+// Launch sequence of one step (all tensors of a group in every launch):
+//   pass1   g (and p when RMS(p) must be recomputed) -> row/col partial sums
+//           of g^2; tensors with ndim < 2 update exp_avg_sq in place and emit
+//           partial sum(u^2).
+//   stats   row/col partials -> EMA of row/col means (exp_avg_sq_row/col),
+//           plus per-chunk sums of the new row vector.
+//   scalars per tensor: alpha = rho * max(eps2, RMS(p)), mean(row) per slice.
+//   pass2   g -> partial sum(u^2) with u = g (row_i/m)^-1/2 col_j^-1/2.
+//   clip    per tensor: coef = alpha / max(1, RMS(u) / clip_threshold).
+//   apply   g, p (exp_avg) -> p (exp_avg); partial sum(p_new^2).
+//   psq     per tensor: sum(p_new^2) -> the optional carry slot.
+// Method: Colossal-AI distributed-optimizer article, Step 3 (factored rows/
+// cols, relative step, beta1), Step 4 (RMS), Step 5 (beta2t, clip, lr scale).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "adafactor_internal.h"
+
+namespace meo {
+namespace {
+
+// ---- small helpers --------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Deterministic CTA-wide sum: xor-butterfly inside each warp, then warp 0's
+// lane 0 adds the kWarps warp sums in index order.  Every thread gets the
+// result.  red must hold kWarps + 1 doubles.
+__device__ __forceinline__ double block_sum(double v, double* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += red[w];
+    red[kWarps] = s;
+  }
+  __syncthreads();
+  const double s = red[kWarps];
+  __syncthreads();
+  return s;
+}
+
+// Index of the tensor owning unit u: largest t with pf[t] <= u < pf[t+1].
+__device__ __forceinline__ int find_owner(const int32_t* pf, int ng, int64_t u) {
+  int lo = 0, hi = ng;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pf[mid] <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Raw (not yet widened) gradient registers for VEC elements.
+template <typename GT, int VEC> struct Raw;
+template <> struct Raw<__nv_bfloat16, 8> { uint4 u; };
+template <> struct Raw<float, 8> { float4 a, b; };
+template <> struct Raw<__nv_bfloat16, 1> { unsigned short h; };
+template <> struct Raw<float, 1> { float f; };
+
+__device__ __forceinline__ void load_raw(Raw<__nv_bfloat16, 8>& r, const __nv_bfloat16* p) {
+  r.u = __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void load_raw(Raw<float, 8>& r, const float* p) {
+  r.a = __ldcs(reinterpret_cast<const float4*>(p));
+  r.b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+}
+__device__ __forceinline__ void load_raw(Raw<__nv_bfloat16, 1>& r, const __nv_bfloat16* p) {
+  r.h = __ldcs(reinterpret_cast<const unsigned short*>(p));
+}
+__device__ __forceinline__ void load_raw(Raw<float, 1>& r, const float* p) { r.f = __ldcs(p); }
+
+// bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
+__device__ __forceinline__ void widen(const Raw<__nv_bfloat16, 8>& r, float (&x)[8]) {
+  const uint32_t w[4] = {r.u.x, r.u.y, r.u.z, r.u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(w[k] << 16);
+    x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void widen(const Raw<float, 8>& r, float (&x)[8]) {
+  x[0] = r.a.x; x[1] = r.a.y; x[2] = r.a.z; x[3] = r.a.w;
+  x[4] = r.b.x; x[5] = r.b.y; x[6] = r.b.z; x[7] = r.b.w;
+}
+__device__ __forceinline__ void widen(const Raw<__nv_bfloat16, 1>& r, float (&x)[1]) {
+  x[0] = __uint_as_float(static_cast<uint32_t>(r.h) << 16);
+}
+__device__ __forceinline__ void widen(const Raw<float, 1>& r, float (&x)[1]) { x[0] = r.f; }
+
+__device__ __forceinline__ float load_g1(const void* g, int gdt, int64_t e) {
+  if (gdt == kGradBF16) {
+    const unsigned short h = __ldcs(static_cast<const unsigned short*>(g) + e);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  return __ldcs(static_cast<const float*>(g) + e);
+}
+
+// fp32 vectors of VEC elements (params, exp_avg).
+template <int VEC> __device__ __forceinline__ void load_f(float (&y)[VEC], const float* p);
+template <> __device__ __forceinline__ void load_f<8>(float (&y)[8], const float* p) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w; y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
+}
+template <> __device__ __forceinline__ void load_f<1>(float (&y)[1], const float* p) { y[0] = __ldcs(p); }
+template <int VEC> __device__ __forceinline__ void store_f(float* p, const float (&y)[VEC]);
+template <> __device__ __forceinline__ void store_f<8>(float* p, const float (&y)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(y[4], y[5], y[6], y[7]));
+}
+template <> __device__ __forceinline__ void store_f<1>(float* p, const float (&y)[1]) { __stcs(p, y[0]); }
+
+// Position of tile `local` of a factored tensor: column block fastest, so
+// neighbouring CTAs read neighbouring pieces of the same rows.
+struct TilePos {
+  int64_t b, r, c;
+};
+__device__ __forceinline__ TilePos tile_pos(const DevTensor& d, int64_t local) {
+  TilePos t;
+  t.c = local % d.cb;
+  const int64_t q = local / d.cb;
+  t.r = q % d.rb;
+  t.b = q / d.rb;
+  return t;
+}
+
+// ---- pass 1: row / column partial sums of g^2 -----------------------------
+// Lane column layout inside a tile: chunk k, element v -> k*32*VEC + lane*VEC + v.
+// A row is streamed in groups of CG chunks; RPI rows are loaded per iteration
+// so that ~128 bytes of gradient per lane are in flight before any use.
+template <int VEC> struct Layout {
+  static constexpr int CH = kTileCols / (32 * VEC);  // chunks per tile row
+  static constexpr int CG = VEC == 8 ? 4 : 8;          // chunks per load group
+};
+
+template <typename GT, int VEC, bool PSQ>
+__device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArgs& a, int64_t local,
+                               float* colbuf, double* red) {
+  constexpr int CH = Layout<VEC>::CH, CG = Layout<VEC>::CG;
+  constexpr int RPI = PSQ ? 1 : ((VEC == 8 && sizeof(GT) == 4) ? 1 : 2);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const TilePos tp = tile_pos(d, local);
+  const int64_t H = d.H, W = d.W;
+  const int64_t i0 = tp.r * kTileRows;
+  const int64_t i1 = min(H, i0 + kTileRows);
+  const int64_t j0 = tp.c * kTileCols;
+  const GT* gb = static_cast<const GT*>(d.g) + tp.b * H * W;
+  const float* pb = d.p + tp.b * H * W;
+  float* rowpart = a.rowpart + d.rowpart + tp.c * (int64_t)d.B * H + tp.b * H;
+
+  float cacc[CH * VEC];
+#pragma unroll
+  for (int k = 0; k < CH * VEC; ++k) cacc[k] = 0.f;
+  float psq = 0.f;
+
+  for (int64_t i = i0 + warp; i < i1; i += RPI * kWarps) {
+    float rs[RPI];
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) rs[rr] = 0.f;
+#pragma unroll
+    for (int kg = 0; kg < CH; kg += CG) {
+      Raw<GT, VEC> raw[RPI][CG];
+#pragma unroll
+      for (int rr = 0; rr < RPI; ++rr) {
+        const int64_t ii = i + rr * kWarps;
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+          const int64_t j = j0 + (kg + k) * 32 * VEC + lane * VEC;
+          if (ii < i1 && j < W) load_raw(raw[rr][k], gb + ii * W + j);
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < RPI; ++rr) {
+        const int64_t ii = i + rr * kWarps;
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+          const int64_t j = j0 + (kg + k) * 32 * VEC + lane * VEC;
+          if (ii < i1 && j < W) {
+            float x[VEC];
+            widen(raw[rr][k], x);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+              const float q = x[v] * x[v];
+              cacc[(kg + k) * VEC + v] += q;
+              rs[rr] += q;
+            }
+            if (PSQ) {
+              float y[VEC];
+              load_f<VEC>(y, pb + ii * W + j);
+#pragma unroll
+              for (int v = 0; v < VEC; ++v) psq = fmaf(y[v], y[v], psq);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) {
+      const int64_t ii = i + rr * kWarps;
+      const float s = warp_sum(rs[rr]);
+      if (lane == 0 && ii < i1) rowpart[ii] = s;
+    }
+  }
+
+  // Column partials: the kWarps warps of the CTA covered disjoint rows of the
+  // same columns; add their accumulators in warp order through shared memory.
+  float* mine = colbuf + warp * kTileCols;
+#pragma unroll
+  for (int k = 0; k < CH; ++k) {
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) mine[k * 32 * VEC + lane * VEC + v] = cacc[k * VEC + v];
+  }
+  __syncthreads();
+  float* colpart = a.colpart + d.colpart + (tp.b * d.rb + tp.r) * W;
+  for (int cl = threadIdx.x; cl < kTileCols; cl += kThreads) {
+    const int64_t j = j0 + cl;
+    if (j < W) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) s += colbuf[w * kTileCols + cl];
+      colpart[j] = s;
+    }
+  }
+  if (PSQ) {
+    const double tot = block_sum(static_cast<double>(psq), red);
+    if (threadIdx.x == 0) a.ppart[d.tile0 + local] = tot;
+  } else {
+    __syncthreads();  // colbuf is reused by the next tile
+  }
+}
+
+// Full second moment (ndim < 2): v <- beta2 v + (1 - beta2)(g^2 + eps1) in
+// place, partial sum(g^2 / v) = sum(u^2), and sum(p^2) when needed.
+template <bool PSQ>
+__device__ __forceinline__ void pass1_unfactored(const DevTensor& d, const StepArgs& a, int64_t local, double* red) {
+  const int64_t e0 = local * kTile1D;
+  const int64_t e1 = min(d.n, e0 + kTile1D);
+  const float b2 = static_cast<float>(a.beta2);
+  const float omb2 = static_cast<float>(1.0 - a.beta2);
+  const float eps1 = static_cast<float>(a.eps1);
+  float s = 0.f, ps = 0.f;
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+    const float x = load_g1(d.g, d.gdt, e);
+    const float vn = fmaf(b2, d.v[e], omb2 * fmaf(x, x, eps1));
+    d.v[e] = vn;
+    s += (x * x) / vn;
+    if (PSQ) {
+      const float y = d.p[e];
+      ps = fmaf(y, y, ps);
+    }
+  }
+  const double S = block_sum(static_cast<double>(s), red);
+  double P = 0.0;
+  if (PSQ) P = block_sum(static_cast<double>(ps), red);
+  if (threadIdx.x == 0) {
+    a.spart[d.tile0 + local] = S;
+    if (PSQ) a.ppart[d.tile0 + local] = P;
+  }
+}
+
+// Shared-memory layout of the persistent kernels.
+constexpr size_t kColbufBytes = sizeof(float) * kWarps * kTileCols;
+constexpr size_t kRedBytes = sizeof(double) * 16;
+constexpr size_t kPrefixBytes = (sizeof(int32_t) * (kMaxGroup + 1) + 15) / 16 * 16;
+constexpr size_t kColfBytes = sizeof(float) * kTileCols;
+
+// Copies the launch's member prefix into shared memory; returns the member count.
+__device__ __forceinline__ int load_prefix(int32_t* pf, const Range& r) {
+  const int ng = r.m_end - r.m_begin;
+  for (int k = threadIdx.x; k <= ng; k += kThreads) pf[k] = r.pf[r.m_begin + k];
+  __syncthreads();
+  return ng;
+}
+
+// Tensor index of member m (identity when the range has no index list).
+__device__ __forceinline__ int member_tensor(const Range& r, int m) {
+  return r.idx ? r.idx[r.m_begin + m] : r.m_begin + m;
+}
+
+template <typename GT, int VEC, bool PSQ>
+__global__ void __launch_bounds__(kThreads, 2) k_pass1_f(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* colbuf = reinterpret_cast<float*>(smem);
+  double* red = reinterpret_cast<double*>(smem + kColbufBytes);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kColbufBytes + kRedBytes);
+  const int ng = load_prefix(pf, r);
+  const int64_t u1 = pf[ng];
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    pass1_factored<GT, VEC, PSQ>(d, a, u - pf[m], colbuf, red);
+  }
+}
+
+template <bool PSQ>
+__global__ void __launch_bounds__(kThreads) k_pass1_u(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* red = reinterpret_cast<double*>(smem);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
+  const int ng = load_prefix(pf, r);
+  const int64_t u1 = pf[ng];
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    pass1_unfactored<PSQ>(d, a, u - pf[m], red);
+  }
+}
+
+// ---- stats: EMA of row / column means -------------------------------------
+__device__ __forceinline__ void stats_row_item(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q, double* red) {
+  const int64_t H = d.H;
+  const int64_t i0 = q * kRowChunk;
+  const int64_t i1 = min(H, i0 + kRowChunk);
+  const float* rp = a.rowpart + d.rowpart + b * H;
+  const int64_t stride = static_cast<int64_t>(d.B) * H;
+  float* row = d.row + b * H;
+  const double inv_w = 1.0 / static_cast<double>(d.W);
+  double acc = 0.0;
+  for (int64_t i = i0 + threadIdx.x; i < i1; i += kThreads) {
+    double s = 0.0;
+    for (int c = 0; c < d.cb; ++c) s += static_cast<double>(rp[c * stride + i]);
+    const double mean = s * inv_w + a.eps1;
+    const float nr = static_cast<float>(a.beta2 * static_cast<double>(row[i]) + (1.0 - a.beta2) * mean);
+    row[i] = nr;
+    acc += static_cast<double>(nr);
+  }
+  const double tot = block_sum(acc, red);
+  if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + q] = tot;
+}
+
+__device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q) {
+  // No early return: the persistent loop around this call reaches barriers.
+  const int64_t W = d.W;
+  const int64_t j = q * kColChunk + threadIdx.x;
+  if (threadIdx.x < kColChunk && j < W) {
+    const float* cp = a.colpart + d.colpart + b * d.rb * W + j;
+    double s = 0.0;
+#pragma unroll 8
+    for (int r = 0; r < d.rb; ++r) s += static_cast<double>(cp[static_cast<int64_t>(r) * W]);
+    const double mean = s / static_cast<double>(d.H) + a.eps1;
+    float* col = d.col + b * W + j;
+    *col = static_cast<float>(a.beta2 * static_cast<double>(*col) + (1.0 - a.beta2) * mean);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* red = reinterpret_cast<double*>(smem);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
+  const int ng = load_prefix(pf, r);
+  const int64_t u1 = pf[ng];
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    const int64_t local = u - pf[m];
+    const int64_t per_slice = d.nrc + d.ncc;
+    const int64_t b = local / per_slice, k = local % per_slice;
+    if (k < d.nrc) stats_row_item(d, a, b, k, red);
+    else stats_col_item(d, a, b, k - d.nrc);
+  }
+}
+
+// ---- scalars: alpha and mean(row), one CTA per tensor ---------------------
+__global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ StepArgs a) {
+  __shared__ double red[16];
+  const int t = blockIdx.x;
+  const DevTensor d = a.tensors[t];
+  double alpha = a.rho;
+  if (a.scale_parameter) {
+    double psq;
+    if (a.psq_valid) {
+      psq = *d.psq;
+    } else {
+      const int64_t nt = a.pf_tiles[t + 1] - a.pf_tiles[t];
+      double acc = 0.0;
+      for (int64_t k = threadIdx.x; k < nt; k += kThreads) acc += a.ppart[d.tile0 + k];
+      psq = block_sum(acc, red);
+    }
+    const double r = sqrt(psq / static_cast<double>(d.n));
+    alpha = a.rho * (r > a.eps2 ? r : a.eps2);
+  }
+  if (threadIdx.x == 0) a.alpha[t] = alpha;
+  if (d.kind != kUnfactored) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t b = warp; b < d.B; b += kWarps) {
+      double s = 0.0;
+      for (int64_t q = lane; q < d.nrc; q += 32) s += a.rowchunk[d.rowchunk + b * d.nrc + q];
+      s = warp_sum(s);
+      if (lane == 0) a.mrow[d.mslot + b] = s / static_cast<double>(d.H);
+    }
+  }
+}
+
+// ---- pass 2: partial sum(u^2) ---------------------------------------------
+// sum_ij u_ij^2 = sum_i (m / row_i) * sum_j g_ij^2 / col_j, so a lane keeps one
+// running fp32 dot product per row and folds it into a double with m/row_i.
+// colf holds 1/col_j for the tile's columns (shared memory).
+template <typename GT, int VEC>
+__device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArgs& a, int64_t local, float* colf,
+                               double* red) {
+  constexpr int CH = Layout<VEC>::CH, CG = Layout<VEC>::CG;
+  constexpr int RPI = (VEC == 8 && sizeof(GT) == 4) ? 1 : 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const TilePos tp = tile_pos(d, local);
+  const int64_t H = d.H, W = d.W;
+  const int64_t i0 = tp.r * kTileRows;
+  const int64_t i1 = min(H, i0 + kTileRows);
+  const int64_t j0 = tp.c * kTileCols;
+  const GT* gb = static_cast<const GT*>(d.g) + tp.b * H * W;
+  const float* row = d.row + tp.b * H;
+  const float m = static_cast<float>(a.mrow[d.mslot + tp.b]);
+
+  __syncthreads();  // previous tile's readers of colf are done
+  for (int cl = threadIdx.x; cl < kTileCols; cl += kThreads) {
+    const int64_t j = j0 + cl;
+    colf[cl] = (j < W) ? 1.0f / d.col[tp.b * W + j] : 0.f;
+  }
+  __syncthreads();
+
+  double acc = 0.0;
+  for (int64_t i = i0 + warp; i < i1; i += RPI * kWarps) {
+    float ts[RPI];
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) ts[rr] = 0.f;
+#pragma unroll
+    for (int kg = 0; kg < CH; kg += CG) {
+      Raw<GT, VEC> raw[RPI][CG];
+#pragma unroll
+      for (int rr = 0; rr < RPI; ++rr) {
+        const int64_t ii = i + rr * kWarps;
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+          const int64_t j = j0 + (kg + k) * 32 * VEC + lane * VEC;
+          if (ii < i1 && j < W) load_raw(raw[rr][k], gb + ii * W + j);
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < RPI; ++rr) {
+        const int64_t ii = i + rr * kWarps;
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+          const int cl = (kg + k) * 32 * VEC + lane * VEC;
+          if (ii < i1 && j0 + cl < W) {
+            float x[VEC];
+            widen(raw[rr][k], x);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) ts[rr] = fmaf(x[v] * x[v], colf[cl + v], ts[rr]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) {
+      const int64_t ii = i + rr * kWarps;
+      if (ii < i1) {
+        const float a_i = m / row[ii];
+        acc = fma(static_cast<double>(a_i), static_cast<double>(ts[rr]), acc);
+      }
+    }
+  }
+  const double tot = block_sum(acc, red);
+  if (threadIdx.x == 0) a.spart[d.tile0 + local] = tot;
+}
+
+template <typename GT, int VEC>
+__global__ void __launch_bounds__(kThreads, 2) k_pass2_f(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* red = reinterpret_cast<double*>(smem);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
+  float* colf = reinterpret_cast<float*>(smem + kRedBytes + kPrefixBytes);
+  const int ng = load_prefix(pf, r);
+  const int64_t u1 = pf[ng];
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    pass2_factored<GT, VEC>(d, a, u - pf[m], colf, red);
+  }
+}
+
+// ---- clip: coef = alpha / max(1, RMS(u) / d), one CTA per tensor ----------
+__global__ void __launch_bounds__(kThreads) k_clip(const __grid_constant__ StepArgs a) {
+  __shared__ double red[16];
+  const int t = blockIdx.x;
+  const DevTensor d = a.tensors[t];
+  const int64_t nt = a.pf_tiles[t + 1] - a.pf_tiles[t];
+  double acc = 0.0;
+  for (int64_t k = threadIdx.x; k < nt; k += kThreads) acc += a.spart[d.tile0 + k];
+  const double S = block_sum(acc, red);
+  if (threadIdx.x == 0) {
+    const double rms_u = sqrt(S / static_cast<double>(d.n));
+    double div = rms_u / a.clip;
+    if (!(div > 1.0)) div = 1.0;
+    a.coef[t] = a.alpha[t] / div;
+  }
+}
+
+// ---- apply: p <- p - wd*alpha*p - update ----------------------------------
+// colf holds coef * col_j^-1/2 for the tile's columns (shared memory).
+template <typename GT, int VEC, bool B1, bool PSQ>
+__device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArgs& a, int t, int64_t local, float* colf,
+                               double* red) {
+  constexpr int CH = Layout<VEC>::CH, CG = Layout<VEC>::CG;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const TilePos tp = tile_pos(d, local);
+  const int64_t H = d.H, W = d.W;
+  const int64_t i0 = tp.r * kTileRows;
+  const int64_t i1 = min(H, i0 + kTileRows);
+  const int64_t j0 = tp.c * kTileCols;
+  const int64_t base = tp.b * H * W;
+  const GT* gb = static_cast<const GT*>(d.g) + base;
+  float* pb = d.p + base;
+  float* mb = B1 ? d.m1 + base : nullptr;
+  const float* row = d.row + tp.b * H;
+  const float m = static_cast<float>(a.mrow[d.mslot + tp.b]);
+  const float coef = static_cast<float>(a.coef[t]);
+  const float wda = static_cast<float>(a.wd * a.alpha[t]);
+  const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
+
+  __syncthreads();  // previous tile's readers of colf are done
+  for (int cl = threadIdx.x; cl < kTileCols; cl += kThreads) {
+    const int64_t j = j0 + cl;
+    colf[cl] = (j < W) ? coef * rsqrtf(d.col[tp.b * W + j]) : 0.f;
+  }
+  __syncthreads();
+
+  float psq = 0.f;
+  for (int64_t i = i0 + warp; i < i1; i += kWarps) {
+    const float r_i = rsqrtf(row[i] / m);
+#pragma unroll
+    for (int kg = 0; kg < CH; kg += CG) {
+      Raw<GT, VEC> raw[CG];
+      float pv[CG][VEC];
+      float mv[B1 ? CG : 1][VEC];
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int64_t j = j0 + (kg + k) * 32 * VEC + lane * VEC;
+        if (j < W) {
+          load_raw(raw[k], gb + i * W + j);
+          load_f<VEC>(pv[k], pb + i * W + j);
+          if (B1) load_f<VEC>(mv[B1 ? k : 0], mb + i * W + j);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int cl = (kg + k) * 32 * VEC + lane * VEC;
+        const int64_t j = j0 + cl;
+        if (j < W) {
+          float x[VEC];
+          widen(raw[k], x);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            float upd = (x[v] * r_i) * colf[cl + v];
+            if (B1) {
+              mv[B1 ? k : 0][v] = fmaf(b1, mv[B1 ? k : 0][v], omb1 * upd);
+              upd = mv[B1 ? k : 0][v];
+            }
+            const float pn = fmaf(-wda, pv[k][v], pv[k][v] - upd);
+            pv[k][v] = pn;
+            if (PSQ) psq = fmaf(pn, pn, psq);
+          }
+          store_f<VEC>(pb + i * W + j, pv[k]);
+          if (B1) store_f<VEC>(mb + i * W + j, mv[B1 ? k : 0]);
+        }
+      }
+    }
+  }
+  if (PSQ) {
+    const double tot = block_sum(static_cast<double>(psq), red);
+    if (threadIdx.x == 0) a.ppart[d.tile0 + local] = tot;
+  }
+}
+
+template <bool B1, bool PSQ>
+__device__ __forceinline__ void apply_unfactored(const DevTensor& d, const StepArgs& a, int t, int64_t local, double* red) {
+  const int64_t e0 = local * kTile1D;
+  const int64_t e1 = min(d.n, e0 + kTile1D);
+  const float coef = static_cast<float>(a.coef[t]);
+  const float wda = static_cast<float>(a.wd * a.alpha[t]);
+  const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
+  float psq = 0.f;
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+    const float x = load_g1(d.g, d.gdt, e);
+    float upd = coef * (x * rsqrtf(d.v[e]));
+    if (B1) {
+      const float mn = fmaf(b1, d.m1[e], omb1 * upd);
+      d.m1[e] = mn;
+      upd = mn;
+    }
+    const float p = d.p[e];
+    const float pn = fmaf(-wda, p, p - upd);
+    d.p[e] = pn;
+    if (PSQ) psq = fmaf(pn, pn, psq);
+  }
+  if (PSQ) {
+    const double tot = block_sum(static_cast<double>(psq), red);
+    if (threadIdx.x == 0) a.ppart[d.tile0 + local] = tot;
+  }
+}
+
+template <typename GT, int VEC, bool B1, bool PSQ>
+__global__ void __launch_bounds__(kThreads, 2) k_apply_f(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* red = reinterpret_cast<double*>(smem);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
+  float* colf = reinterpret_cast<float*>(smem + kRedBytes + kPrefixBytes);
+  const int ng = load_prefix(pf, r);
+  const int64_t u1 = pf[ng];
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const int t = member_tensor(r, m);
+    const DevTensor d = a.tensors[t];
+    apply_factored<GT, VEC, B1, PSQ>(d, a, t, u - pf[m], colf, red);
+  }
+}
+
+template <bool B1, bool PSQ>
+__global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* red = reinterpret_cast<double*>(smem);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
+  const int ng = load_prefix(pf, r);
+  const int64_t u1 = pf[ng];
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const int t = member_tensor(r, m);
+    const DevTensor d = a.tensors[t];
+    apply_unfactored<B1, PSQ>(d, a, t, u - pf[m], red);
+  }
+}
+
+// ---- psq: sum(p_new^2) carry, one CTA per tensor --------------------------
+__global__ void __launch_bounds__(kThreads) k_psq(const __grid_constant__ StepArgs a) {
+  __shared__ double red[16];
+  const int t = blockIdx.x;
+  const DevTensor d = a.tensors[t];
+  if (d.psq == nullptr) return;
+  const int64_t nt = a.pf_tiles[t + 1] - a.pf_tiles[t];
+  double acc = 0.0;
+  for (int64_t k = threadIdx.x; k < nt; k += kThreads) acc += a.ppart[d.tile0 + k];
+  const double S = block_sum(acc, red);
+  if (threadIdx.x == 0) *d.psq = S;
+}
+
+}  // namespace
+
+const char* kernel_name(int k) {
+  static const char* names[kNumKernels] = {"k_pass1", "k_stats", "k_scalars", "k_pass2",
+                                           "k_clip", "k_apply", "k_psq"};
+  return (k >= 0 && k < kNumKernels) ? names[k] : "";
+}
+
+namespace {
+
+// Dynamic shared memory of each streaming instantiation.
+size_t smem_of(KernelId k, TensorClass c) {
+  if (k == kKPass1) return c == kClsUnfactored ? kRedBytes + kPrefixBytes : kColbufBytes + kRedBytes + kPrefixBytes;
+  if (k == kKStats) return kRedBytes + kPrefixBytes;
+  if (k == kKApply && c == kClsUnfactored) return kRedBytes + kPrefixBytes;
+  return kRedBytes + kPrefixBytes + kColfBytes;
+}
+
+using KernelFn = void (*)(StepArgs, Range);
+
+// The instantiation of a streaming kind for a class and the per-call flags.
+template <typename GT, int VEC>
+KernelFn pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
+  switch (k) {
+    case kKPass1: return psq_in ? k_pass1_f<GT, VEC, true> : k_pass1_f<GT, VEC, false>;
+    case kKPass2: return k_pass2_f<GT, VEC>;
+    case kKApply:
+      if (b1) return psq_out ? k_apply_f<GT, VEC, true, true> : k_apply_f<GT, VEC, true, false>;
+      return psq_out ? k_apply_f<GT, VEC, false, true> : k_apply_f<GT, VEC, false, false>;
+    default: return nullptr;
+  }
+}
+
+KernelFn pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
+  switch (c) {
+    case kClsVecBF16: return pick_f<__nv_bfloat16, 8>(k, psq_in, b1, psq_out);
+    case kClsVecF32: return pick_f<float, 8>(k, psq_in, b1, psq_out);
+    case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, b1, psq_out);
+    case kClsScalarF32: return pick_f<float, 1>(k, psq_in, b1, psq_out);
+    case kClsUnfactored:
+      if (k == kKPass1) return psq_in ? k_pass1_u<true> : k_pass1_u<false>;
+      if (k == kKApply) {
+        if (b1) return psq_out ? k_apply_u<true, true> : k_apply_u<true, false>;
+        return psq_out ? k_apply_u<false, true> : k_apply_u<false, false>;
+      }
+      return nullptr;
+    default: return nullptr;
+  }
+}
+
+}  // namespace
+
+int kernel_grid_limit(KernelId k, int device, cudaError_t* err) {
+  // min over the kind's instantiations of (resident CTAs per SM) x SM count,
+  // cached per device.  Also raises the dynamic shared-memory limit where an
+  // instantiation needs more than the 48 KB default.
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev][kNumKernels] = {};
+  *err = cudaSuccess;
+  if (device < 0 || device >= kMaxDev) {
+    *err = cudaErrorInvalidDevice;
+    return 0;
+  }
+  if (cache[device][k] > 0) return cache[device][k];
+  int sms = 0;
+  *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (*err != cudaSuccess) return 0;
+  int per_sm = 1 << 30;
+  auto visit = [&](const void* fn, size_t smem) {
+    if (*err != cudaSuccess || fn == nullptr) return;
+    if (smem > 48 * 1024) {
+      *err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (*err != cudaSuccess) return;
+    }
+    int b = 0;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, smem);
+    if (*err == cudaSuccess && b < per_sm) per_sm = b;
+  };
+  if (k == kKPass1 || k == kKPass2 || k == kKApply) {
+    for (int c = 0; c < kNumClasses; ++c)
+      for (int v = 0; v < 8; ++v)
+        visit(reinterpret_cast<const void*>(pick(k, static_cast<TensorClass>(c), v & 1, v & 2, v & 4)),
+              smem_of(k, static_cast<TensorClass>(c)));
+  } else if (k == kKStats) {
+    visit(reinterpret_cast<const void*>(k_stats), smem_of(kKStats, kClsVecBF16));
+  } else {
+    per_sm = 8;  // per-tensor kernels: grid = tensor count, not limited here
+  }
+  if (*err != cudaSuccess) return 0;
+  if (per_sm < 1) per_sm = 1;
+  cache[device][k] = per_sm * sms;
+  return cache[device][k];
+}
+
+cudaError_t launch_stream(KernelId k, TensorClass c, const StepArgs& a, const Range& r, int grid,
+                          cudaStream_t s) {
+  if (grid <= 0 || r.m_end <= r.m_begin) return cudaSuccess;
+  const bool psq_in = a.scale_parameter && !a.psq_valid;
+  KernelFn fn = pick(k, c, psq_in, a.has_beta1 != 0, a.want_psq_out != 0);
+  if (fn == nullptr) return cudaErrorInvalidValue;
+  fn<<<grid, kThreads, smem_of(k, c), s>>>(a, r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats(const StepArgs& a, const Range& r, int grid, cudaStream_t s) {
+  if (grid <= 0 || r.m_end <= r.m_begin) return cudaSuccess;
+  k_stats<<<grid, kThreads, smem_of(kKStats, kClsVecBF16), s>>>(a, r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_per_tensor(KernelId k, const StepArgs& a, int ntensors, cudaStream_t s) {
+  if (ntensors <= 0) return cudaSuccess;
+  switch (k) {
+    case kKScalars: k_scalars<<<ntensors, kThreads, 0, s>>>(a); break;
+    case kKClip: k_clip<<<ntensors, kThreads, 0, s>>>(a); break;
+    case kKPsq: k_psq<<<ntensors, kThreads, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace meo

@@ -1,0 +1,230 @@
+"""PyTorch front end of the CUDA Adafactor step.
+
+PyTorch only provides device memory and streams here: these functions check
+and marshal arguments, allocate zeroed state and the workspace, and make one
+call into the C library per step.  The library does all of the arithmetic.
+
+Article: Colossal-AI distributed-optimizer article, Step 3 (defaults and
+argument rules, beta1 state, factored row/col state for ndim >= 2, full
+exp_avg_sq otherwise), Step 5 (the update).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Iterable, Sequence
+
+import torch
+
+from . import binding as B
+
+_GRAD_DTYPES = {torch.float32: B.ADAF_FLOAT32, torch.bfloat16: B.ADAF_BFLOAT16}
+
+
+def make_hparams(lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0, decay_rate=-0.8, beta1=None,
+                 weight_decay=0.0, scale_parameter=True, relative_step=True, warmup_init=False,
+                 param_sq_sum_valid=False) -> B.adaf_hparams:
+    """Builds and validates the hyper-parameter struct; invalid values raise
+    ValueError with the library's message (e.g. "Cannot combine manual lr and
+    relative_step=True options")."""
+    if len(tuple(eps)) != 2:
+        raise ValueError("eps must be a pair (eps1, eps2)")
+    hp = B.adaf_hparams()
+    hp.lr = 0.0 if lr is None else float(lr)
+    hp.has_lr = 0 if lr is None else 1
+    hp.eps1, hp.eps2 = float(eps[0]), float(eps[1])
+    hp.clip_threshold = float(clip_threshold)
+    hp.decay_rate = float(decay_rate)
+    hp.beta1 = 0.0 if beta1 is None else float(beta1)
+    hp.has_beta1 = 0 if beta1 is None else 1
+    hp.weight_decay = float(weight_decay)
+    hp.scale_parameter = int(bool(scale_parameter))
+    hp.relative_step = int(bool(relative_step))
+    hp.warmup_init = int(bool(warmup_init))
+    hp.param_sq_sum_valid = int(bool(param_sq_sum_valid))
+    B.adafactor_validate(hp)
+    return hp
+
+
+def factored_dims(shape):
+    """(B, H, W) for ndim >= 2 (B = product of the leading dims), else None."""
+    if len(shape) < 2:
+        return None
+    lead = 1
+    for s in shape[:-2]:
+        lead *= int(s)
+    return lead, int(shape[-2]), int(shape[-1])
+
+
+def init_state(params: Sequence[torch.Tensor], beta1=None, param_sq_sum: bool = True) -> list:
+    """Zeroed optimizer state for each parameter (fp32, on the parameter's device):
+    exp_avg_sq_row [*lead, H] and exp_avg_sq_col [*lead, W] for ndim >= 2, a full
+    exp_avg_sq otherwise, exp_avg when beta1 is set, and a float64 param_sq_sum
+    slot that carries sum(p^2) from one step to the next."""
+    out = []
+    for p in params:
+        st = {}
+        shape = tuple(p.shape)
+        if len(shape) >= 2:
+            st["exp_avg_sq_row"] = torch.zeros(shape[:-1], dtype=torch.float32, device=p.device)
+            st["exp_avg_sq_col"] = torch.zeros(shape[:-2] + shape[-1:], dtype=torch.float32, device=p.device)
+        else:
+            st["exp_avg_sq"] = torch.zeros(shape, dtype=torch.float32, device=p.device)
+        if beta1 is not None:
+            st["exp_avg"] = torch.zeros(shape, dtype=torch.float32, device=p.device)
+        if param_sq_sum:
+            st["param_sq_sum"] = torch.zeros(1, dtype=torch.float64, device=p.device)
+        out.append(st)
+    return out
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+class AdafactorStep:
+    """A marshalled multi-tensor step: the tensor/state descriptor arrays and
+    the workspace are built once; every call is one C-library call."""
+
+    def __init__(self, params: Sequence[torch.Tensor], grads: Sequence[torch.Tensor], states: Sequence[dict],
+                 **hparams):
+        params, grads = list(params), list(grads)
+        if len(params) != len(grads) or len(params) != len(states):
+            raise ValueError("params, grads and states must have the same length")
+        self.hparams = dict(hparams)
+        make_hparams(**self.hparams)  # validate early
+        self.params, self.grads, self.states = params, grads, list(states)
+        n = len(params)
+        self.n = n
+        self.device = params[0].device if n else None
+        self._tensors = (B.adaf_tensor * max(1, n))()
+        self._states = (B.adaf_state * max(1, n))()
+        for k, (p, g, st) in enumerate(zip(params, grads, self.states)):
+            if not isinstance(p, torch.Tensor) or p.dtype != torch.float32:
+                raise ValueError(f"tensor {k}: params must be float32 tensors")
+            if p.device.type != "cuda" or g.device != p.device or p.device != self.device:
+                raise ValueError(f"tensor {k}: params and grads must be CUDA tensors on one device")
+            if g.dtype not in _GRAD_DTYPES:
+                raise ValueError(f"tensor {k}: grad dtype must be float32 or bfloat16")
+            if tuple(g.shape) != tuple(p.shape):
+                raise ValueError(f"tensor {k}: grad shape {tuple(g.shape)} != param shape {tuple(p.shape)}")
+            if not p.is_contiguous() or not g.is_contiguous():
+                raise ValueError(f"tensor {k}: params and grads must be contiguous")
+            if p.dim() > B.ADAF_MAX_NDIM:
+                raise ValueError(f"tensor {k}: at most {B.ADAF_MAX_NDIM} dims")
+            for name, t in st.items():
+                if name == "param_sq_sum":
+                    if t.dtype != torch.float64 or t.device != p.device or t.numel() < 1:
+                        raise ValueError(f"tensor {k}: param_sq_sum must be a float64 CUDA tensor")
+                elif not (t.dtype == torch.float32 and t.device == p.device and t.is_contiguous()):
+                    raise ValueError(f"tensor {k}: state '{name}' must be contiguous float32 on the param's device")
+            fd = factored_dims(p.shape)
+            if fd is not None:
+                for name, size in (("exp_avg_sq_row", fd[0] * fd[1]), ("exp_avg_sq_col", fd[0] * fd[2])):
+                    if name not in st or st[name].numel() != size:
+                        raise ValueError(f"tensor {k}: state '{name}' must have {size} elements")
+            elif "exp_avg_sq" not in st or st["exp_avg_sq"].numel() != p.numel():
+                raise ValueError(f"tensor {k}: state 'exp_avg_sq' must have {p.numel()} elements")
+            if self.hparams.get("beta1") is not None and (
+                    "exp_avg" not in st or st["exp_avg"].numel() != p.numel()):
+                raise ValueError(f"tensor {k}: beta1 is set, state 'exp_avg' must have {p.numel()} elements")
+            td = self._tensors[k]
+            td.param, td.grad = _ptr(p), _ptr(g)
+            td.grad_dtype = _GRAD_DTYPES[g.dtype]
+            td.ndim = p.dim()
+            for d, s in enumerate(p.shape):
+                td.shape[d] = int(s)
+            sd = self._states[k]
+            sd.exp_avg_sq_row = _ptr(st.get("exp_avg_sq_row"))
+            sd.exp_avg_sq_col = _ptr(st.get("exp_avg_sq_col"))
+            sd.exp_avg_sq = _ptr(st.get("exp_avg_sq"))
+            sd.exp_avg = _ptr(st.get("exp_avg"))
+            sd.param_sq_sum = _ptr(st.get("param_sq_sum"))
+        self.workspace_bytes = B.adafactor_workspace_size(self._tensors, n) if n else 0
+        self.workspace = (torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=self.device)
+                          if n else None)
+        self._carry = all("param_sq_sum" in st for st in self.states)
+        self._versions = None
+
+    def _carry_valid(self) -> bool:
+        if not self._carry or self._versions is None:
+            return False
+        return self._versions == [(p.data_ptr(), p._version) for p in self.params]
+
+    def invalidate_param_sq_sum(self) -> None:
+        """Forget the carried sum(p^2) (call after changing params behind torch's back)."""
+        self._versions = None
+
+    def __call__(self, step: int, stream: torch.cuda.Stream | None = None) -> None:
+        if self.n == 0:
+            make_hparams(**self.hparams)
+            return
+        hp = make_hparams(**self.hparams, param_sq_sum_valid=self._carry_valid())
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        B.adafactor_step(self._tensors, self._states, self.n, int(step), hp, _ptr(self.workspace),
+                         self.workspace_bytes, int(stream.cuda_stream))
+        self._versions = ([(p.data_ptr(), p._version) for p in self.params] if self._carry else None)
+
+
+def adafactor_step(params, grads, states, step: int, lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0,
+                   decay_rate=-0.8, beta1=None, weight_decay=0.0, scale_parameter=True, relative_step=True,
+                   warmup_init=False, stream=None) -> None:
+    """One Adafactor step over a list of tensors (functional form).  States come
+    from init_state(); the step number t is 1-based.  Marshals every call; use
+    AdafactorStep to marshal once and call many times."""
+    hparams = dict(lr=lr, eps=eps, clip_threshold=clip_threshold, decay_rate=decay_rate, beta1=beta1,
+                   weight_decay=weight_decay, scale_parameter=scale_parameter, relative_step=relative_step,
+                   warmup_init=warmup_init)
+    make_hparams(**hparams)
+    AdafactorStep(params, grads, states, **hparams)(step, stream)
+
+
+class Adafactor(torch.optim.Optimizer):
+    """torch.optim.Optimizer wrapper with the article's Adafactor defaults.
+
+    Each parameter group is stepped with one call into the library (one
+    launch sequence for all of its tensors)."""
+
+    def __init__(self, params: Iterable, lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0, decay_rate=-0.8,
+                 beta1=None, weight_decay=0.0, scale_parameter=True, relative_step=True, warmup_init=False):
+        make_hparams(lr=lr, eps=eps, clip_threshold=clip_threshold, decay_rate=decay_rate, beta1=beta1,
+                     weight_decay=weight_decay, scale_parameter=scale_parameter, relative_step=relative_step,
+                     warmup_init=warmup_init)
+        defaults = dict(lr=lr, eps=eps, clip_threshold=clip_threshold, decay_rate=decay_rate, beta1=beta1,
+                        weight_decay=weight_decay, scale_parameter=scale_parameter, relative_step=relative_step,
+                        warmup_init=warmup_init)
+        super().__init__(params, defaults)
+        self._plans = {}
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        for gi, group in enumerate(self.param_groups):
+            hp = {k: group[k] for k in ("lr", "eps", "clip_threshold", "decay_rate", "beta1", "weight_decay",
+                                        "scale_parameter", "relative_step", "warmup_init")}
+            by_step = {}
+            for p in group["params"]:
+                if p.grad is None:
+                    continue
+                st = self.state[p]
+                if not st:
+                    st.update(init_state([p], beta1=hp["beta1"])[0])
+                    st["step"] = 0
+                st["step"] += 1
+                by_step.setdefault(st["step"], []).append(p)
+            for t, ps in by_step.items():
+                grads = [p.grad for p in ps]
+                key = (gi, t if len(by_step) > 1 else None, tuple(p.data_ptr() for p in ps),
+                       tuple(g.data_ptr() for g in grads), tuple(sorted(hp.items(), key=lambda kv: kv[0])).__repr__())
+                plan = self._plans.get(key)
+                if plan is None:
+                    states = [{k: v for k, v in self.state[p].items() if k != "step"} for p in ps]
+                    plan = AdafactorStep(ps, grads, states, **hp)
+                    if len(self._plans) > 16:
+                        self._plans.clear()
+                    self._plans[key] = plan
+                plan(t)
+        return loss

@@ -10,6 +10,8 @@ Workloads (shapes as PyTorch [out, in] weights):
   * ``llama_layer`` one Llama-style decoder layer (q/o 4096x4096, k/v
                     1024x4096, gate/up 14336x4096, down 4096x14336, two
                     4096 RMSNorm vectors), fp32 p and g ~ N(0, 1e-3), 10 steps.
+  * ``llama_layer_bf16``  the same layer with bf16 gradients (a small case
+                    of the kernels the full model runs).
   * ``llama3_8b``   32 such layers + embedding 128256x4096 + lm_head
                     128256x4096 + final norm 4096 (291 tensors,
                     8,030,261,248 values); fp32 p, bf16 g ~ N(0, 1e-3).
@@ -92,6 +94,9 @@ def workload(name: str, seed: int = 0) -> Workload:
     if name == "llama_layer":
         return Workload(name, llama_layer_shapes(), torch.float32, 1e-3, {}, 10,
                         description="one Llama-3-8B decoder layer, fp32 p and g, defaults")
+    if name == "llama_layer_bf16":
+        return Workload(name, llama_layer_shapes(), torch.bfloat16, 1e-3, {}, 10,
+                        description="one Llama-3-8B decoder layer, fp32 p, bf16 g, defaults")
     if name == "llama3_8b":
         return Workload(name, llama3_8b_shapes(), torch.bfloat16, 1e-3, {}, 7,
                         description="Llama-3-8B (291 tensors, 8,030,261,248 params), fp32 p, "
