@@ -48,6 +48,20 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (max) of a per-rank timing; identity at N = 1."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(n_params: int, world: int, ms_per_step: float) -> float:
+    """Whole-job params/s: every rank steps its own full replica."""
+    return world * n_params / (ms_per_step / 1e3)
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -61,48 +75,76 @@ def measured_hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def algorithmic_bytes(shapes, grad_bytes, beta1, recompute_psq=False):
-    """Bytes the step must move at minimum: 3 reads of g, p read + write,
-    exp_avg read + write with beta1, the row/col (or full) second-moment state
-    read + write, and (only when RMS(p) is not carried over) one more p read.
-    Returns (per step, per k_apply launch)."""
-    step = apply = 0
+def tensor_class(shape, grad_bytes):
+    """The library's tensor class of a contiguous, 256-byte aligned tensor."""
+    if len(shape) < 2:
+        return "1d"
+    vec = int(shape[-1]) % 8 == 0
+    return ("vec_" if vec else "elem_") + ("bf16" if grad_bytes == 2 else "f32")
+
+
+def algorithmic_bytes(shapes, grad_bytes, beta1):
+    """Minimum bytes moved: per step (3 reads of g, p read + write, exp_avg
+    read + write with beta1, the second-moment state read + write) and per
+    streaming launch slot ("k_pass1[vec_bf16]", "k_apply[1d]", ...): pass 1 and
+    pass 2 read g (1D pass 1 also reads and writes v), apply reads g and the
+    state and reads + writes p (and exp_avg)."""
+    step = 0
+    slots = {}
     for _, s in shapes:
         n = 1
         for d in s:
             n *= int(d)
-        state = (2 * 4 * (n // (s[-2] * s[-1]) * (s[-2] + s[-1]))) if len(s) >= 2 else 2 * 4 * n
+        cls = tensor_class(s, grad_bytes)
+        if len(s) >= 2:
+            lead = n // (int(s[-2]) * int(s[-1]))
+            state_rw = 2 * 4 * lead * (int(s[-2]) + int(s[-1]))
+            state_read = state_rw // 2
+            p1 = grad_bytes * n
+        else:
+            state_rw = 2 * 4 * n
+            state_read = 4 * n
+            p1 = grad_bytes * n + state_rw
         m1 = 8 * n if beta1 else 0
-        step += 3 * grad_bytes * n + 8 * n + m1 + state + (4 * n if recompute_psq else 0)
-        # apply: g + p read/write + exp_avg read/write + reads of row/col (or v)
-        apply += grad_bytes * n + 8 * n + m1 + state // 2
-    return step, apply
+        step += 3 * grad_bytes * n + 8 * n + m1 + state_rw
+        slots[f"k_pass1[{cls}]"] = slots.get(f"k_pass1[{cls}]", 0) + p1
+        if len(s) >= 2:
+            slots[f"k_pass2[{cls}]"] = slots.get(f"k_pass2[{cls}]", 0) + grad_bytes * n
+        slots[f"k_apply[{cls}]"] = slots.get(f"k_apply[{cls}]", 0) + grad_bytes * n + 8 * n + m1 + state_read
+    return step, slots
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons with nvidia-smi during a region."""
+    """Samples SM clock and throttle reasons with nvidia-smi (every 50 ms)
+    while the benchmark runs; summary() keeps the samples taken inside the
+    timed window (host wall clock), or the whole sampling span when the window
+    caught fewer than 3."""
 
-    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, uuid: str | None):
+    def __init__(self, uuid):
         self.uuid = uuid
         self.proc = None
+        self.out = ""
+        self.window = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
 
-    def __exit__(self, *exc):
-        self.out = ""
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.2)
             self.proc.terminate()
             try:
                 self.out, _ = self.proc.communicate(timeout=5)
@@ -110,19 +152,40 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
+    @staticmethod
+    def _ts(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         rows = []
         for r in csv.reader(io.StringIO(self.out or "")):
             r = [x.strip() for x in r]
-            if len(r) < 10:
-                continue
-            if self.uuid and self.uuid not in r[1]:
+            if len(r) < 10 or (self.uuid and self.uuid not in r[1]):
                 continue
             rows.append(r)
+        scope = "whole run"
+        if self.window and rows:
+            inside = [r for r in rows if (ts := self._ts(r[0])) is not None
+                      and self.window[0] - 0.05 <= ts <= self.window[1] + 0.05]
+            if len(inside) >= 3:
+                rows, scope = inside, "timed region"
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(r[2]) for r in rows) if v is not None]
+        mx = [v for v in (num(r[3]) for r in rows) if v is not None]
+        pw = [v for v in (num(r[4]) for r in rows) if v is not None]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
@@ -130,7 +193,8 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(rows), "scope": scope}
 
 
 def device_uuid(dev):
@@ -173,6 +237,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
+    clocks = ClockSampler(device_uuid(dev)).start()
     t = 0
     for _ in range(args.warmup):
         t += 1
@@ -183,21 +248,20 @@ def run_ours(args, world, rank, local):
     binding.adafactor_profile_read()  # drop anything recorded so far
     binding.adafactor_profile_enable(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device_uuid(dev)) as clocks:
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            t += 1
-            step(t)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        step(t)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(w0, time.time())
+    clocks.stop()
     binding.adafactor_profile_enable(False)
     kernels = binding.adafactor_profile_read()
-    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     if world > 1:
-        x = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-        ms = float(x.item())
         torch.distributed.barrier()
     ms_per_step = ms / args.steps
 
@@ -231,35 +295,37 @@ def run_ours(args, world, rank, local):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            x = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-            ems = float(x.item())
-        e2e = {"value": world * n_params / (ems / args.e2e_steps / 1e3), "unit": "params/s",
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": replica_throughput(n_params, world, ems / args.e2e_steps), "unit": "params/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": ems / args.e2e_steps,
                "path": "pinned host bf16 grads -> device, adafactor_step, device fp32 params -> pinned host"}
         del host_g, host_p
 
     grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
-    step_bytes, apply_bytes = algorithmic_bytes(wl.shapes, grad_bytes, beta1 is not None)
+    step_bytes, slot_bytes = algorithmic_bytes(wl.shapes, grad_bytes, beta1 is not None)
     peak, peak_kind = measured_hbm_peak()
     launches = sum(v[1] for v in kernels.values())
-    dom = max(kernels.items(), key=lambda kv: kv[1][0])
-    dom_name, (dom_ms, dom_n) = dom
-    per_launch_bytes = {"k_apply": apply_bytes}
+    per_kernel = {}
+    for name, (kms, kn) in kernels.items():
+        if not kn:
+            continue
+        entry = {"ms_per_step": round(kms / args.steps, 4), "launches": kn}
+        if name in slot_bytes and kms > 0:
+            entry["gbs"] = round(slot_bytes[name] / (kms / kn / 1e3) / 1e9, 1)
+        per_kernel[name] = entry
+    dom_name, (dom_ms, dom_n) = max(kernels.items(), key=lambda kv: kv[1][0])
     roofline = None
-    if dom_n and dom_name in per_launch_bytes:
-        ach = per_launch_bytes[dom_name] / (dom_ms / dom_n / 1e3) / 1e9
+    if dom_n and dom_name in slot_bytes:
+        ach = slot_bytes[dom_name] / (dom_ms / dom_n / 1e3) / 1e9
         roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
-                    "traffic": traffic_record(dom_name), "algorithmic_bytes_per_launch": apply_bytes,
+                    "traffic": traffic_record(dom_name), "algorithmic_bytes_per_launch": slot_bytes[dom_name],
                     "avg_launch_ms": dom_ms / dom_n}
     eff_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     clk = clocks.summary()
     out = {
-        "metric": METRIC, "value": world * n_params / (ms_per_step / 1e3), "unit": "params/s",
+        "metric": METRIC, "value": replica_throughput(n_params, world, ms_per_step), "unit": "params/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,0.02) fp32 params, N(0,1e-3) bf16 grads resident in HBM)",
@@ -273,7 +339,7 @@ def run_ours(args, world, rank, local):
         "pct_of_8tbs": round(100 * eff_gbs / NOMINAL_HBM_GBS, 2),
         "frac_of_hbm_peak": round(eff_gbs / peak, 4), "hbm_peak_gbs": peak, "hbm_peak_source": peak_kind,
         "algorithmic_bytes_per_step": step_bytes,
-        "kernels_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in kernels.items() if v[1]},
+        "kernels": per_kernel,
         "roofline": roofline, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
     }
     return out, (wl, n_params)

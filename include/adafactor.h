@@ -174,8 +174,10 @@ void adafactor_release_cache(void);
  * adafactor_profile_enable(1) makes every following adafactor_step() record a
  * CUDA event pair around each of its kernel launches on the launch stream;
  * adafactor_profile_read() waits for the recorded events, adds the elapsed
- * time per kernel kind into ms[k] and the launch count into launches[k] for
- * k < min(nk, adafactor_num_kernels()), and forgets the records.
+ * time per slot into ms[k] and the launch count into launches[k] for
+ * k < min(nk, adafactor_num_kernels()), and forgets the records.  A slot is
+ * one kernel kind, or one kind and tensor class for the streaming kernels;
+ * adafactor_kernel_name(k) names it ("k_apply[vec_bf16]", "k_stats", ...).
  * adafactor_profile_enable(0) stops recording.  Errors: ADAF_ERR_CUDA. */
 adaf_status adafactor_profile_enable(int32_t on);
 adaf_status adafactor_profile_read(double* ms, int64_t* launches, int32_t nk);

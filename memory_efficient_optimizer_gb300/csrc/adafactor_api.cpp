@@ -260,10 +260,34 @@ struct DeviceCache {
 };
 
 struct ProfRecord {
-  int kernel;
+  int slot;
   int device;
   cudaEvent_t start, stop;
 };
+
+// Profiling slots: one per streaming kernel and tensor class, one per other
+// kernel kind, in launch order.
+constexpr int kNumSlots = 18;
+const char* const kSlotNames[kNumSlots] = {
+    "k_pass1[vec_bf16]", "k_pass1[vec_f32]", "k_pass1[elem_bf16]", "k_pass1[elem_f32]", "k_pass1[1d]",
+    "k_stats", "k_scalars",
+    "k_pass2[vec_bf16]", "k_pass2[vec_f32]", "k_pass2[elem_bf16]", "k_pass2[elem_f32]",
+    "k_clip",
+    "k_apply[vec_bf16]", "k_apply[vec_f32]", "k_apply[elem_bf16]", "k_apply[elem_f32]", "k_apply[1d]",
+    "k_psq"};
+
+int profile_slot(KernelId k, int cls) {
+  switch (k) {
+    case meo::kKPass1: return 0 + cls;
+    case meo::kKStats: return 5;
+    case meo::kKScalars: return 6;
+    case meo::kKPass2: return 7 + cls;
+    case meo::kKClip: return 11;
+    case meo::kKApply: return 12 + cls;
+    case meo::kKPsq: return 17;
+    default: return 0;
+  }
+}
 
 std::mutex g_mu;
 std::map<int, DeviceCache> g_cache;
@@ -419,8 +443,8 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
   a.want_psq_out = any_psq ? 1 : 0;
 
   // One launch helper: optional profiling events around the launch.
-  auto run = [&](KernelId k, auto&& launch) -> adaf_status {
-    ProfRecord rec{static_cast<int>(k), device, nullptr, nullptr};
+  auto run = [&](KernelId k, int cls, auto&& launch) -> adaf_status {
+    ProfRecord rec{profile_slot(k, cls), device, nullptr, nullptr};
     cudaError_t err;
     if (g_profile) {
       if ((err = get_event(dc, &rec.start)) != cudaSuccess) return cuda_fail(err, "cudaEventCreate (profile)");
@@ -449,7 +473,7 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
         const int grid = static_cast<int>(units < grid_limit[k] ? units : grid_limit[k]);
         const meo::Range r{pf_dev, idx_dev, g0, g1};
         const meo::TensorClass tc = static_cast<meo::TensorClass>(c);
-        adaf_status rs = run(k, [&] { return meo::launch_stream(k, tc, a, r, grid, s); });
+        adaf_status rs = run(k, c, [&] { return meo::launch_stream(k, tc, a, r, grid, s); });
         if (rs != ADAF_OK) return rs;
       }
     }
@@ -465,18 +489,18 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
       if (units == 0) continue;
       const int grid = static_cast<int>(units < grid_limit[meo::kKStats] ? units : grid_limit[meo::kKStats]);
       const meo::Range r{pf_items_dev, nullptr, g0, g1};
-      st = run(meo::kKStats, [&] { return meo::launch_stats(a, r, grid, s); });
+      st = run(meo::kKStats, 0, [&] { return meo::launch_stats(a, r, grid, s); });
       if (st != ADAF_OK) return st;
     }
   }
-  st = run(meo::kKScalars, [&] { return meo::launch_per_tensor(meo::kKScalars, a, nd_i, s); });
+  st = run(meo::kKScalars, 0, [&] { return meo::launch_per_tensor(meo::kKScalars, a, nd_i, s); });
   if (st != ADAF_OK) return st;
   if ((st = stream_all(meo::kKPass2, true)) != ADAF_OK) return st;
-  st = run(meo::kKClip, [&] { return meo::launch_per_tensor(meo::kKClip, a, nd_i, s); });
+  st = run(meo::kKClip, 0, [&] { return meo::launch_per_tensor(meo::kKClip, a, nd_i, s); });
   if (st != ADAF_OK) return st;
   if ((st = stream_all(meo::kKApply, false)) != ADAF_OK) return st;
   if (any_psq) {
-    st = run(meo::kKPsq, [&] { return meo::launch_per_tensor(meo::kKPsq, a, nd_i, s); });
+    st = run(meo::kKPsq, 0, [&] { return meo::launch_per_tensor(meo::kKPsq, a, nd_i, s); });
     if (st != ADAF_OK) return st;
   }
   return ADAF_OK;
@@ -524,9 +548,9 @@ adaf_status adafactor_profile_read(double* ms, int64_t* launches, int32_t nk) {
     cudaError_t e = cudaEventSynchronize(r.stop);
     if (e == cudaSuccess) e = cudaEventElapsedTime(&el, r.start, r.stop);
     if (e != cudaSuccess && st == ADAF_OK) st = cuda_fail(e, "profile event");
-    if (r.kernel < nk) {
-      if (ms) ms[r.kernel] += el;
-      if (launches) launches[r.kernel] += 1;
+    if (r.slot < nk) {
+      if (ms) ms[r.slot] += el;
+      if (launches) launches[r.slot] += 1;
     }
     DeviceCache& dc = g_cache[r.device];
     dc.free_events.push_back(r.start);
@@ -536,8 +560,8 @@ adaf_status adafactor_profile_read(double* ms, int64_t* launches, int32_t nk) {
   return st;
 }
 
-int32_t adafactor_num_kernels(void) { return meo::kNumKernels; }
+int32_t adafactor_num_kernels(void) { return kNumSlots; }
 
-const char* adafactor_kernel_name(int32_t k) { return meo::kernel_name(k); }
+const char* adafactor_kernel_name(int32_t k) { return (k >= 0 && k < kNumSlots) ? kSlotNames[k] : ""; }
 
 }  // extern "C"

@@ -145,6 +145,28 @@ __device__ __forceinline__ TilePos tile_pos(const DevTensor& d, int64_t local) {
   return t;
 }
 
+// ---- per-tile column factors in shared memory -----------------------------
+// On the vector path lane l reads the 8 factors of its columns k*256 + l*8 + v
+// as two float4 loads; storing element v of lane l at
+// k*256 + (v/4)*128 + l*4 + v%4 makes both loads conflict-free (consecutive
+// lanes read consecutive 16-byte words).  The element-wise path needs no
+// swizzle (lane l reads column k*32 + l).
+template <int VEC> __device__ __forceinline__ int colf_index(int cl) {
+  if (VEC == 1) return cl;
+  const int k = cl >> 8, l = (cl >> 3) & 31, v = cl & 7;
+  return (k << 8) + ((v >> 2) << 7) + (l << 2) + (v & 3);
+}
+
+template <int VEC> __device__ __forceinline__ void load_colf(float (&f)[VEC], const float* colf, int k, int lane);
+template <> __device__ __forceinline__ void load_colf<8>(float (&f)[8], const float* colf, int k, int lane) {
+  const float4 a = *reinterpret_cast<const float4*>(colf + (k << 8) + (lane << 2));
+  const float4 b = *reinterpret_cast<const float4*>(colf + (k << 8) + 128 + (lane << 2));
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+template <> __device__ __forceinline__ void load_colf<1>(float (&f)[1], const float* colf, int k, int lane) {
+  f[0] = colf[(k << 5) + lane];
+}
+
 // ---- pass 1: row / column partial sums of g^2 -----------------------------
 // Lane column layout inside a tile: chunk k, element v -> k*32*VEC + lane*VEC + v.
 // A row is streamed in groups of CG chunks; RPI rows are loaded per iteration
@@ -284,6 +306,7 @@ constexpr size_t kColbufBytes = sizeof(float) * kWarps * kTileCols;
 constexpr size_t kRedBytes = sizeof(double) * 16;
 constexpr size_t kPrefixBytes = (sizeof(int32_t) * (kMaxGroup + 1) + 15) / 16 * 16;
 constexpr size_t kColfBytes = sizeof(float) * kTileCols;
+constexpr size_t kPartBytes = sizeof(float) * kWarps * kColChunk;
 
 // Copies the launch's member prefix into shared memory; returns the member count.
 __device__ __forceinline__ int load_prefix(int32_t* pf, const Range& r) {
@@ -349,16 +372,47 @@ __device__ __forceinline__ void stats_row_item(const DevTensor& d, const StepArg
   if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + q] = tot;
 }
 
-__device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q) {
-  // No early return: the persistent loop around this call reaches barriers.
+// Column item: kColChunk (256) columns of one slice.  Warp w adds the row
+// blocks r = w, w + 8, ... of the column partials (lane l owns columns
+// l + 32m, m < 8, so every warp load is one coalesced 128-byte line), with
+// compensated (Kahan) fp32 sums; the 8 warp sums are then added in warp order
+// in double.  Fixed order throughout, so the result is deterministic.
+__device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q,
+                                               float* part) {
+  constexpr int kPer = kColChunk / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t W = d.W;
-  const int64_t j = q * kColChunk + threadIdx.x;
+  const int64_t c0 = q * kColChunk;
+  const float* cp = a.colpart + d.colpart + b * d.rb * W;
+  float s[kPer], comp[kPer];
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) s[m] = comp[m] = 0.f;
+  for (int r = warp; r < d.rb; r += kWarps) {
+    const float* rowp = cp + static_cast<int64_t>(r) * W;
+    float x[kPer];
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int64_t j = c0 + lane + 32 * m;
+      x[m] = (j < W) ? rowp[j] : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const float y = x[m] - comp[m];
+      const float t = s[m] + y;
+      comp[m] = (t - s[m]) - y;
+      s[m] = t;
+    }
+  }
+  __syncthreads();  // part is free (previous item done reading it)
+#pragma unroll
+  for (int m = 0; m < kPer; ++m) part[warp * kColChunk + lane + 32 * m] = s[m];
+  __syncthreads();
+  const int64_t j = c0 + threadIdx.x;
   if (threadIdx.x < kColChunk && j < W) {
-    const float* cp = a.colpart + d.colpart + b * d.rb * W + j;
-    double s = 0.0;
-#pragma unroll 8
-    for (int r = 0; r < d.rb; ++r) s += static_cast<double>(cp[static_cast<int64_t>(r) * W]);
-    const double mean = s / static_cast<double>(d.H) + a.eps1;
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += static_cast<double>(part[w * kColChunk + threadIdx.x]);
+    const double mean = tot / static_cast<double>(d.H) + a.eps1;
     float* col = d.col + b * W + j;
     *col = static_cast<float>(a.beta2 * static_cast<double>(*col) + (1.0 - a.beta2) * mean);
   }
@@ -368,6 +422,7 @@ __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ Step
   extern __shared__ __align__(16) unsigned char smem[];
   double* red = reinterpret_cast<double*>(smem);
   int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
+  float* part = reinterpret_cast<float*>(smem + kRedBytes + kPrefixBytes);
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
@@ -377,7 +432,7 @@ __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ Step
     const int64_t per_slice = d.nrc + d.ncc;
     const int64_t b = local / per_slice, k = local % per_slice;
     if (k < d.nrc) stats_row_item(d, a, b, k, red);
-    else stats_col_item(d, a, b, k - d.nrc);
+    else stats_col_item(d, a, b, k - d.nrc, part);
   }
 }
 
@@ -434,11 +489,11 @@ __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArg
   __syncthreads();  // previous tile's readers of colf are done
   for (int cl = threadIdx.x; cl < kTileCols; cl += kThreads) {
     const int64_t j = j0 + cl;
-    colf[cl] = (j < W) ? 1.0f / d.col[tp.b * W + j] : 0.f;
+    colf[colf_index<VEC>(cl)] = (j < W) ? 1.0f / d.col[tp.b * W + j] : 0.f;
   }
   __syncthreads();
 
-  double acc = 0.0;
+  float acc = 0.f;  // this lane's share of sum(u^2) over the tile (<= 32 rows)
   for (int64_t i = i0 + warp; i < i1; i += RPI * kWarps) {
     float ts[RPI];
 #pragma unroll
@@ -462,10 +517,11 @@ __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArg
         for (int k = 0; k < CG; ++k) {
           const int cl = (kg + k) * 32 * VEC + lane * VEC;
           if (ii < i1 && j0 + cl < W) {
-            float x[VEC];
+            float x[VEC], f[VEC];
             widen(raw[rr][k], x);
+            load_colf<VEC>(f, colf, kg + k, lane);
 #pragma unroll
-            for (int v = 0; v < VEC; ++v) ts[rr] = fmaf(x[v] * x[v], colf[cl + v], ts[rr]);
+            for (int v = 0; v < VEC; ++v) ts[rr] = fmaf(x[v] * x[v], f[v], ts[rr]);
           }
         }
       }
@@ -475,11 +531,11 @@ __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArg
       const int64_t ii = i + rr * kWarps;
       if (ii < i1) {
         const float a_i = m / row[ii];
-        acc = fma(static_cast<double>(a_i), static_cast<double>(ts[rr]), acc);
+        acc = fmaf(a_i, ts[rr], acc);
       }
     }
   }
-  const double tot = block_sum(acc, red);
+  const double tot = block_sum(static_cast<double>(acc), red);
   if (threadIdx.x == 0) a.spart[d.tile0 + local] = tot;
 }
 
@@ -540,7 +596,7 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
   __syncthreads();  // previous tile's readers of colf are done
   for (int cl = threadIdx.x; cl < kTileCols; cl += kThreads) {
     const int64_t j = j0 + cl;
-    colf[cl] = (j < W) ? coef * rsqrtf(d.col[tp.b * W + j]) : 0.f;
+    colf[colf_index<VEC>(cl)] = (j < W) ? coef * rsqrtf(d.col[tp.b * W + j]) : 0.f;
   }
   __syncthreads();
 
@@ -566,11 +622,12 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
         const int cl = (kg + k) * 32 * VEC + lane * VEC;
         const int64_t j = j0 + cl;
         if (j < W) {
-          float x[VEC];
+          float x[VEC], f[VEC];
           widen(raw[k], x);
+          load_colf<VEC>(f, colf, kg + k, lane);
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
-            float upd = (x[v] * r_i) * colf[cl + v];
+            float upd = (x[v] * r_i) * f[v];
             if (B1) {
               mv[B1 ? k : 0][v] = fmaf(b1, mv[B1 ? k : 0][v], omb1 * upd);
               upd = mv[B1 ? k : 0][v];
@@ -675,7 +732,7 @@ namespace {
 // Dynamic shared memory of each streaming instantiation.
 size_t smem_of(KernelId k, TensorClass c) {
   if (k == kKPass1) return c == kClsUnfactored ? kRedBytes + kPrefixBytes : kColbufBytes + kRedBytes + kPrefixBytes;
-  if (k == kKStats) return kRedBytes + kPrefixBytes;
+  if (k == kKStats) return kRedBytes + kPrefixBytes + kPartBytes;
   if (k == kKApply && c == kClsUnfactored) return kRedBytes + kPrefixBytes;
   return kRedBytes + kPrefixBytes + kColfBytes;
 }

@@ -27,7 +27,13 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    """Compile the oracle with gcc (no fast-math, no FMA contraction).
+
+    ORACLE_LIB_OVERRIDE names an already-built library to load instead; the
+    mutation test uses it to run the pins against deliberately broken copies."""
+    override = os.environ.get("ORACLE_LIB_OVERRIDE")
+    if override:
+        return override
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(

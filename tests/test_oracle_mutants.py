@@ -1,0 +1,58 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each mutant is a copy of the oracle source with one deliberate slip, built on
+the CPU into a temporary library; the pin and brute-force suites are then run
+against it in a subprocess and must fail."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "adafactor_oracle.c")
+
+MUTANTS = {
+    "row mean drops eps1": ("for (int64_t j = 0; j < W; ++j) s += gb[i * W + j] * gb[i * W + j] + hp->eps1;",
+                            "for (int64_t j = 0; j < W; ++j) s += gb[i * W + j] * gb[i * W + j];"),
+    "EMA coefficients swapped": ("rb[i] = beta2 * rb[i] + (1.0 - beta2) * (s / (double)W);",
+                                 "rb[i] = (1.0 - beta2) * rb[i] + beta2 * (s / (double)W);"),
+    "beta2 exponent sign": ("return 1.0 - pow((double)t, hp->decay_rate);",
+                            "return 1.0 - pow((double)t, -hp->decay_rate);"),
+    "no mean(row) normalisation": ("double r_fac = 1.0 / sqrt(rb[i] / m);", "double r_fac = 1.0 / sqrt(rb[i]);"),
+    "column mean over the wrong axis": ("(colsum[j] / (double)H)", "(colsum[j] / (double)W)"),
+    "clip divides instead of multiplies": ("double clip_div = rms(u, n) / hp->clip_threshold;",
+                                           "double clip_div = rms(u, n) * hp->clip_threshold;"),
+    "clip never active": ("if (clip_div < 1.0) clip_div = 1.0;", "clip_div = 1.0;"),
+    "no eps2 floor on RMS(p)": ("alpha = rho * (hp->eps2 > r ? hp->eps2 : r);", "alpha = rho * r;"),
+    "relative step cap 1e-3": ("double cap = hp->warmup_init ? 1e-6 * (double)t : 1e-2;",
+                               "double cap = hp->warmup_init ? 1e-6 * (double)t : 1e-3;"),
+    "warmup cap not scaled by t": ("double cap = hp->warmup_init ? 1e-6 * (double)t : 1e-2;",
+                                   "double cap = hp->warmup_init ? 1e-6 : 1e-2;"),
+    "beta1 coefficients swapped": ("exp_avg[k] = hp->beta1 * exp_avg[k] + (1.0 - hp->beta1) * u[k];",
+                                   "exp_avg[k] = (1.0 - hp->beta1) * exp_avg[k] + hp->beta1 * u[k];"),
+    "weight decay with rho": ("p[k] = p[k] - hp->weight_decay * alpha * p[k];",
+                              "p[k] = p[k] - hp->weight_decay * rho * p[k];"),
+    "unfactored update without sqrt": ("u[k] = g[k] / sqrt(v[k]);", "u[k] = g[k] / v[k];"),
+    "RMS without the mean": ("return sqrt(s / (double)n);", "return sqrt(s);"),
+    "update not scaled by lr": ("u[k] = (u[k] / clip_div) * alpha;", "u[k] = (u[k] / clip_div);"),
+    "exp_avg not used as the update": ("u[k] = exp_avg[k];", "(void)0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found once: {old}"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", str(mut),
+                           "-o", str(lib), "-lm"])
+    env = dict(os.environ, ORACLE_LIB_OVERRIDE=str(lib))
+    res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_bruteforce.py")],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode != 0, f"mutant '{name}' survived the pins:\n{res.stdout[-2000:]}"
