@@ -163,6 +163,16 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
                            int64_t step, const adaf_hparams* hp, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* Device-side status of the most recent adafactor_step() that used this
+ * workspace: waits on the stream, then stores the status word in *status.
+ * 0 = no problem.  Bit 0 (ADAF_DEVICE_WAIT_TIMEOUT): a bounded wait inside a
+ * kernel gave up (about one second without progress) and the kernel stopped
+ * early, so that step's results are not valid.  The word is reset by every
+ * adafactor_step() call.  Synchronises the host with `stream`.
+ * Errors: ADAF_ERR_INVALID_ARGUMENT, ADAF_ERR_CUDA. */
+#define ADAF_DEVICE_WAIT_TIMEOUT 1
+adaf_status adafactor_device_status(const void* workspace, void* stream, int32_t* status);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* adafactor_last_error(void);
 

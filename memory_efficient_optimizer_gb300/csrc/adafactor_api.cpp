@@ -61,6 +61,10 @@ adaf_status check_hparams(const adaf_hparams* hp) {
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The device status word lives at workspace offset 0; the descriptor table
+// starts at kTableOffset.
+constexpr size_t kTableOffset = 256;
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -134,9 +138,9 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       d.rowchunk = nrowchunk;
       nrowchunk += B * d.nrc;
       d.rowpart = nrowpart;
-      nrowpart += static_cast<int64_t>(d.cb) * B * H;
-      d.colpart = ncolpart;
-      ncolpart += B * d.rb * W;
+      nrowpart += align_up(static_cast<int64_t>(d.cb) * B * H, 4);
+      d.colpart = ncolpart;  // multiple of 4 floats: 16-byte aligned column quads
+      ncolpart += align_up(B * d.rb * W, 4);
       plan->any_factored = true;
     } else {
       d.H = 1;
@@ -207,9 +211,10 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
     plan->cls_idx[c].push_back(static_cast<int32_t>(k));
     plan->cls_pf[c].push_back(plan->cls_pf[c].back() + static_cast<int32_t>(nt));
   }
-  // Workspace layout: the header (uploaded each call) first, then scratch;
-  // every scratch region 256-byte aligned.
-  size_t off = align_up(nd * sizeof(DevTensor), 256);
+  // Workspace layout: the header (uploaded each call: the device status word
+  // at offset 0, the descriptor table at kTableOffset, the prefix arrays)
+  // first, then scratch; every scratch region 256-byte aligned.
+  size_t off = kTableOffset + align_up(nd * sizeof(DevTensor), 256);
   plan->off_pf_tiles = off;
   off += align_up((nd + 1) * sizeof(int32_t), 16);
   plan->off_pf_items = off;
@@ -373,10 +378,13 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  int grid_limit[meo::kNumKernels];
+  int grid_limit[meo::kNumKernels][meo::kNumClasses];
   for (int k = 0; k < meo::kNumKernels; ++k) {
-    grid_limit[k] = meo::kernel_grid_limit(static_cast<KernelId>(k), device, &e);
-    if (e != cudaSuccess) return cuda_fail(e, "kernel occupancy query");
+    for (int c = 0; c < meo::kNumClasses; ++c) {
+      grid_limit[k][c] = meo::kernel_grid_limit(static_cast<KernelId>(k), static_cast<meo::TensorClass>(c),
+                                                device, &e);
+      if (e != cudaSuccess) return cuda_fail(e, "kernel occupancy query");
+    }
   }
 
   std::lock_guard<std::mutex> lock(g_mu);
@@ -403,7 +411,8 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate (staging)");
   }
   unsigned char* h = static_cast<unsigned char*>(slot.host);
-  std::memcpy(h, plan.dev.data(), nd * sizeof(DevTensor));
+  std::memset(h, 0, kTableOffset);  // status word := 0
+  std::memcpy(h + kTableOffset, plan.dev.data(), nd * sizeof(DevTensor));
   std::memcpy(h + plan.off_pf_tiles, plan.pf_tiles.data(), (nd + 1) * sizeof(int32_t));
   std::memcpy(h + plan.off_pf_items, plan.pf_items.data(), (nd + 1) * sizeof(int32_t));
   for (int c = 0; c < meo::kNumClasses; ++c) {
@@ -419,7 +428,8 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
 
   StepArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.tensors = reinterpret_cast<const DevTensor*>(ws);
+  a.tensors = reinterpret_cast<const DevTensor*>(ws + kTableOffset);
+  a.status = reinterpret_cast<int32_t*>(ws);
   a.pf_tiles = reinterpret_cast<const int32_t*>(ws + plan.off_pf_tiles);
   a.pf_items = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
   a.alpha = reinterpret_cast<double*>(ws + plan.off_alpha);
@@ -470,7 +480,7 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
       for (int32_t g0 = 0; g0 < m; g0 += meo::kMaxGroup) {
         const int32_t g1 = g0 + meo::kMaxGroup < m ? g0 + meo::kMaxGroup : m;
         const int64_t units = plan.cls_pf[c][g1] - plan.cls_pf[c][g0];
-        const int grid = static_cast<int>(units < grid_limit[k] ? units : grid_limit[k]);
+        const int grid = static_cast<int>(units < grid_limit[k][c] ? units : grid_limit[k][c]);
         const meo::Range r{pf_dev, idx_dev, g0, g1};
         const meo::TensorClass tc = static_cast<meo::TensorClass>(c);
         adaf_status rs = run(k, c, [&] { return meo::launch_stream(k, tc, a, r, grid, s); });
@@ -487,7 +497,8 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
       const int32_t g1 = g0 + meo::kMaxGroup < nd_i ? g0 + meo::kMaxGroup : nd_i;
       const int64_t units = plan.pf_items[g1] - plan.pf_items[g0];
       if (units == 0) continue;
-      const int grid = static_cast<int>(units < grid_limit[meo::kKStats] ? units : grid_limit[meo::kKStats]);
+      const int lim = grid_limit[meo::kKStats][0];
+      const int grid = static_cast<int>(units < lim ? units : lim);
       const meo::Range r{pf_items_dev, nullptr, g0, g1};
       st = run(meo::kKStats, 0, [&] { return meo::launch_stats(a, r, grid, s); });
       if (st != ADAF_OK) return st;
@@ -507,6 +518,18 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
 }
 
 const char* adafactor_last_error(void) { return g_last_error.c_str(); }
+
+adaf_status adafactor_device_status(const void* workspace, void* stream, int32_t* status) {
+  if (workspace == nullptr || status == nullptr || !aligned(workspace, 256))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "workspace or status is NULL, or workspace misaligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  *status = v;
+  return ADAF_OK;
+}
 
 void adafactor_release_cache(void) {
   std::lock_guard<std::mutex> lock(g_mu);

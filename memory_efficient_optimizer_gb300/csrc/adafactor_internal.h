@@ -95,7 +95,13 @@ struct StepArgs {
   int32_t has_beta1;
   int32_t psq_valid;         // use DevTensor::psq instead of re-reading p
   int32_t want_psq_out;      // apply writes ppart for the carry
+  int32_t* status;           // device status word (bit 0: a bounded wait gave up)
 };
+
+// Device status bits (the word is reset by every step call).
+constexpr int32_t kStatusWaitTimeout = 1;
+// A bounded wait gives up after this many SM clock cycles (~1 s).
+constexpr long long kWaitCycles = 2000000000LL;
 
 // The tensors one launch covers: members idx[m_begin..m_end) of a tensor
 // index list, with pf[m] the first unit (tile or item) of member m relative to
@@ -126,8 +132,9 @@ cudaError_t launch_stream(KernelId k, TensorClass c, const StepArgs& a, const Ra
                           cudaStream_t s);
 cudaError_t launch_stats(const StepArgs& a, const Range& r, int grid, cudaStream_t s);
 cudaError_t launch_per_tensor(KernelId k, const StepArgs& a, int ntensors, cudaStream_t s);
-// Resident-CTA limit (CTAs per SM x SMs) for a kernel kind on a device.
-int kernel_grid_limit(KernelId k, int device, cudaError_t* err);
+// Resident-CTA limit (CTAs per SM x SMs) of a kernel kind and tensor class
+// on a device (the class is ignored for the non-streaming kinds).
+int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err);
 const char* kernel_name(int k);
 
 }  // namespace meo

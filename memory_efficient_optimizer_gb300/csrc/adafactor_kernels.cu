@@ -706,6 +706,486 @@ __global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ St
   }
 }
 
+// ---- vector path: bulk-copy (TMA) staged rows --------------------------------
+// The three streaming passes over the vector-path tensors share one scheme.
+// One CTA per SM: warp 8 is the producer, warps 0-7 the consumers.  The
+// producer streams the tile rows (g, and p / exp_avg where the pass needs
+// them) into a ring of shared-memory stages of 8 rows with cp.async.bulk, one
+// copy per row segment, completion counted on the stage's "full" mbarrier.
+// Consumer warp w takes row w of every stage and releases the stage on its
+// "empty" mbarrier.  The bytes in flight are set by the ring depth, not by
+// registers.  In each 256-column chunk k, lane l handles the column quads
+// k*256 + 4l and k*256 + 128 + 4l, so shared-memory reads and global stores
+// are contiguous across the warp.
+// Every wait is bounded (kWaitCycles): after a timeout the kernel sets
+// kStatusWaitTimeout in the status word; the warp keeps meeting the consumer
+// barriers without touching the stages, so no warp is left waiting at one,
+// and all consumers leave together at the next tile boundary.
+constexpr int kTmaConsumers = kWarps;  // consumer warps = rows per stage
+constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
+
+template <typename GT, bool WP, bool WM, size_t kBudget>
+struct Ring {
+  static constexpr int kG = kTileCols * sizeof(GT);
+  static constexpr int kP = WP ? kTileCols * 4 : 0;
+  static constexpr int kM = WM ? kTileCols * 4 : 0;
+  static constexpr int kRow = kG + kP + kM;
+  static constexpr int kStage = kTmaConsumers * kRow;
+  static constexpr int kStages = kBudget / kStage < 16 ? static_cast<int>(kBudget / kStage) : 16;
+  static constexpr size_t kBytes = static_cast<size_t>(kStages) * kStage;
+  static_assert(kStages >= 2, "stage ring too small");
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of parity `parity` to complete; false after kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+// Bulk copy global -> this CTA's shared memory, completion on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
+}
+
+// Shared prologue: prefix copy and barrier init (all kTmaThreads threads).
+template <int kStages>
+__device__ __forceinline__ int tma_setup(int32_t* pf, const Range& r, uint64_t* full, uint64_t* empty) {
+  const int ng = r.m_end - r.m_begin;
+  for (int k = threadIdx.x; k <= ng; k += kTmaThreads) pf[k] = r.pf[r.m_begin + k];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTmaConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  return ng;
+}
+
+// The producer (one thread): every 8-row stage of every tile of this CTA.
+template <typename GT, class RG>
+__device__ __forceinline__ void tma_produce(const StepArgs& a, const Range& r, const int32_t* pf, int ng,
+                                            unsigned char* ring, uint64_t* full, uint64_t* empty) {
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    const TilePos tp = tile_pos(d, u - pf[m]);
+    const int64_t i0 = tp.r * kTileRows, i1 = min(d.H, i0 + kTileRows);
+    const int64_t j0 = tp.c * kTileCols;
+    const uint32_t ncol = static_cast<uint32_t>(min(static_cast<int64_t>(kTileCols), d.W - j0));
+    const int64_t base = tp.b * d.H * d.W;
+    for (int64_t rs = i0; rs < i1; rs += kTmaConsumers, ++it) {
+      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+      if (!mbar_wait(&empty[slot], ph ^ 1u)) {
+        atomicOr(a.status, kStatusWaitTimeout);
+        return;
+      }
+      const int nrows = static_cast<int>(min(static_cast<int64_t>(kTmaConsumers), i1 - rs));
+      const uint32_t per_row = ncol * static_cast<uint32_t>(sizeof(GT) + (RG::kP ? 4 : 0) + (RG::kM ? 4 : 0));
+      mbar_arrive_expect_tx(&full[slot], nrows * per_row);
+      unsigned char* st = ring + slot * RG::kStage;
+      for (int rr = 0; rr < nrows; ++rr) {
+        const int64_t off = base + (rs + rr) * d.W + j0;
+        unsigned char* row = st + rr * RG::kRow;
+        bulk_g2s(row, static_cast<const GT*>(d.g) + off, ncol * sizeof(GT), &full[slot]);
+        if (RG::kP) bulk_g2s(row + RG::kG, d.p + off, ncol * 4, &full[slot]);
+        if (RG::kM) bulk_g2s(row + RG::kG + RG::kP, d.m1 + off, ncol * 4, &full[slot]);
+      }
+    }
+  }
+}
+
+// Consumer-side wait for a stage; on timeout flags the status and `stop`.
+__device__ __forceinline__ bool tma_acquire(uint64_t* bar, uint32_t parity, const StepArgs& a, int* stop) {
+  if (mbar_wait(bar, parity)) return true;
+  if ((threadIdx.x & 31) == 0) atomicOr(a.status, kStatusWaitTimeout);
+  *stop = 1;
+  return false;
+}
+
+// After a timeout: give copies still in flight a bounded chance to land
+// before the CTA's shared memory goes away.
+template <int kStages>
+__device__ __forceinline__ void tma_drain(uint64_t* full, uint32_t it) {
+  for (uint32_t k = 0; k < static_cast<uint32_t>(kStages); ++k) {
+    const uint32_t j = it + k;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(&full[j % kStages], (j / kStages) & 1u)) {
+      if (clock64() - t0 > kWaitCycles / 8) break;
+    }
+  }
+}
+
+// 4 gradient values of one column quad from a staged row.
+template <typename GT>
+__device__ __forceinline__ void quad_g(float (&x)[4], const unsigned char* row, int cl) {
+  if (sizeof(GT) == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(row + cl * 2);
+    x[0] = __uint_as_float(w.x << 16);
+    x[1] = __uint_as_float(w.x & 0xffff0000u);
+    x[2] = __uint_as_float(w.y << 16);
+    x[3] = __uint_as_float(w.y & 0xffff0000u);
+  } else {
+    const float4 w = *reinterpret_cast<const float4*>(row + cl * 4);
+    x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+  }
+}
+
+// Consumer-only deterministic CTA sum (warp xor-trees, then warps in order);
+// valid in consumer thread 0.
+__device__ __forceinline__ double consumer_sum(float v, double* red) {
+  const float w = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = static_cast<double>(w);
+  consumer_sync();
+  double s = 0.0;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < kTmaConsumers; ++k) s += red[k];
+  }
+  return s;
+}
+
+// ---- pass 1 (vector path) --------------------------------------------------
+template <typename GT, bool PSQ>
+using Pass1Ring = Ring<GT, PSQ, false, 176 * 1024>;
+
+template <typename GT, bool PSQ>
+__global__ void __launch_bounds__(kTmaThreads, 1) k_pass1_tma(const __grid_constant__ StepArgs a, const Range r) {
+  using RG = Pass1Ring<GT, PSQ>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* ring = smem;
+  float* colbuf = reinterpret_cast<float*>(smem + RG::kBytes);          // kWarps x kTileCols
+  double* red = reinterpret_cast<double*>(colbuf + kWarps * kTileCols);  // 16
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 16);
+  uint64_t* empty = full + RG::kStages;
+  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
+  __shared__ int stop;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = tma_setup<RG::kStages>(pf, r, full, empty);
+  if (warp == kTmaConsumers) {
+    if (lane == 0) tma_produce<GT, RG>(a, r, pf, ng, ring, full, empty);
+    return;
+  }
+  if (threadIdx.x == 0) stop = 0;
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    const int64_t local = u - pf[m];
+    const TilePos tp = tile_pos(d, local);
+    const int64_t H = d.H, W = d.W;
+    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
+    const int64_t j0 = tp.c * kTileCols;
+    float* rowpart = a.rowpart + d.rowpart + tp.c * static_cast<int64_t>(d.B) * H + tp.b * H;
+    consumer_sync();  // stop is settled; colbuf / red of the previous tile are read
+    if (stop) break;
+    float cacc[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) cacc[q] = 0.f;
+    float psq = 0.f;
+    bool ok = true;
+    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaConsumers, ++it) {
+      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+      if (!tma_acquire(&full[slot], ph, a, &stop)) {
+        ok = false;
+        break;
+      }
+      const int64_t i = rs + warp;
+      if (i < i1) {
+        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < kTileCols / 256; ++k) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cl = k * 256 + h * 128 + lane * 4;
+            if (j0 + cl < W) {
+              float x[4];
+              quad_g<GT>(x, row, cl);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const float q = x[v] * x[v];
+                cacc[(k * 2 + h) * 4 + v] += q;
+                s += q;
+              }
+              if (PSQ) {
+                const float4 p = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
+                psq = fmaf(p.x, p.x, psq);
+                psq = fmaf(p.y, p.y, psq);
+                psq = fmaf(p.z, p.z, psq);
+                psq = fmaf(p.w, p.w, psq);
+              }
+            }
+          }
+        }
+        s = warp_sum(s);
+        if (lane == 0) rowpart[i] = s;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    // column partials: the 8 warps' accumulators added in warp order
+    float* mine = colbuf + warp * kTileCols;
+#pragma unroll
+    for (int k = 0; k < kTileCols / 256; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        *reinterpret_cast<float4*>(mine + k * 256 + h * 128 + lane * 4) =
+            make_float4(cacc[(k * 2 + h) * 4], cacc[(k * 2 + h) * 4 + 1], cacc[(k * 2 + h) * 4 + 2],
+                        cacc[(k * 2 + h) * 4 + 3]);
+      }
+    }
+    consumer_sync();
+    if (!stop) {
+      float* colpart = a.colpart + d.colpart + (tp.b * d.rb + tp.r) * W;
+      for (int cl = threadIdx.x * 4; cl < kTileCols; cl += kTmaConsumers * 32 * 4) {
+        if (j0 + cl < W) {  // W % 8 == 0: the whole quad is inside
+          float4 s = *reinterpret_cast<const float4*>(colbuf + cl);
+#pragma unroll
+          for (int w = 1; w < kWarps; ++w) {
+            const float4 t = *reinterpret_cast<const float4*>(colbuf + w * kTileCols + cl);
+            s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+          }
+          *reinterpret_cast<float4*>(colpart + j0 + cl) = s;
+        }
+      }
+    }
+    if (PSQ) {
+      const double tot = consumer_sum(psq, red);
+      if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + local] = tot;
+    }
+  }
+  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
+}
+
+// ---- pass 2 (vector path) --------------------------------------------------
+template <typename GT>
+using Pass2Ring = Ring<GT, false, false, 200 * 1024>;
+
+template <typename GT>
+__global__ void __launch_bounds__(kTmaThreads, 1) k_pass2_tma(const __grid_constant__ StepArgs a, const Range r) {
+  using RG = Pass2Ring<GT>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* ring = smem;
+  float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // 1 / col_j
+  float* rowf = colf + kTileCols;                              // mean(row) / row_i
+  double* red = reinterpret_cast<double*>(rowf + kTileRows);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 16);
+  uint64_t* empty = full + RG::kStages;
+  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
+  __shared__ int stop;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = tma_setup<RG::kStages>(pf, r, full, empty);
+  if (warp == kTmaConsumers) {
+    if (lane == 0) tma_produce<GT, RG>(a, r, pf, ng, ring, full, empty);
+    return;
+  }
+  if (threadIdx.x == 0) stop = 0;
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    const int64_t local = u - pf[m];
+    const TilePos tp = tile_pos(d, local);
+    const int64_t H = d.H, W = d.W;
+    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
+    const int64_t j0 = tp.c * kTileCols;
+    const float mr = static_cast<float>(a.mrow[d.mslot + tp.b]);
+    consumer_sync();  // stop is settled; colf / rowf / red of the previous tile are read
+    if (stop) break;
+    for (int cl = threadIdx.x; cl < kTileCols; cl += kTmaConsumers * 32) {
+      const int64_t j = j0 + cl;
+      colf[cl] = (j < W) ? 1.0f / d.col[tp.b * W + j] : 0.f;
+    }
+    for (int rl = threadIdx.x; rl < kTileRows; rl += kTmaConsumers * 32) {
+      const int64_t i = i0 + rl;
+      rowf[rl] = (i < i1) ? mr / d.row[tp.b * H + i] : 0.f;
+    }
+    consumer_sync();
+    float acc = 0.f;
+    bool ok = true;
+    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaConsumers, ++it) {
+      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+      if (!tma_acquire(&full[slot], ph, a, &stop)) {
+        ok = false;
+        break;
+      }
+      const int64_t i = rs + warp;
+      if (i < i1) {
+        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
+        float ts = 0.f;
+#pragma unroll
+        for (int k = 0; k < kTileCols / 256; ++k) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cl = k * 256 + h * 128 + lane * 4;
+            if (j0 + cl < W) {
+              float x[4];
+              quad_g<GT>(x, row, cl);
+              const float4 f = *reinterpret_cast<const float4*>(colf + cl);
+              ts = fmaf(x[0] * x[0], f.x, ts);
+              ts = fmaf(x[1] * x[1], f.y, ts);
+              ts = fmaf(x[2] * x[2], f.z, ts);
+              ts = fmaf(x[3] * x[3], f.w, ts);
+            }
+          }
+        }
+        acc = fmaf(rowf[i - i0], ts, acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    const double tot = consumer_sum(acc, red);
+    if (threadIdx.x == 0 && !stop) a.spart[d.tile0 + local] = tot;
+  }
+  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
+}
+
+// ---- apply (vector path) ---------------------------------------------------
+template <typename GT, bool B1>
+using ApplyRing = Ring<GT, true, B1, 200 * 1024>;
+
+template <typename GT, bool B1, bool PSQ>
+__global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_constant__ StepArgs a, const Range r) {
+  using RG = ApplyRing<GT, B1>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* ring = smem;
+  float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // coef * col_j^-1/2
+  float* rowf = colf + kTileCols;                              // (row_i / mean(row))^-1/2
+  double* red = reinterpret_cast<double*>(rowf + kTileRows);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 16);
+  uint64_t* empty = full + RG::kStages;
+  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
+  __shared__ int stop;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = tma_setup<RG::kStages>(pf, r, full, empty);
+  if (warp == kTmaConsumers) {
+    if (lane == 0) tma_produce<GT, RG>(a, r, pf, ng, ring, full, empty);
+    return;
+  }
+  if (threadIdx.x == 0) stop = 0;
+  const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const int t = member_tensor(r, m);
+    const DevTensor d = a.tensors[t];
+    const int64_t local = u - pf[m];
+    const TilePos tp = tile_pos(d, local);
+    const int64_t H = d.H, W = d.W;
+    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
+    const int64_t j0 = tp.c * kTileCols;
+    const int64_t base = tp.b * H * W;
+    const float mr = static_cast<float>(a.mrow[d.mslot + tp.b]);
+    const float coef = static_cast<float>(a.coef[t]);
+    const float wda = static_cast<float>(a.wd * a.alpha[t]);
+    consumer_sync();  // stop is settled; colf / rowf / red of the previous tile are read
+    if (stop) break;
+    for (int cl = threadIdx.x; cl < kTileCols; cl += kTmaConsumers * 32) {
+      const int64_t j = j0 + cl;
+      colf[cl] = (j < W) ? coef * rsqrtf(d.col[tp.b * W + j]) : 0.f;
+    }
+    for (int rl = threadIdx.x; rl < kTileRows; rl += kTmaConsumers * 32) {
+      const int64_t i = i0 + rl;
+      rowf[rl] = (i < i1) ? rsqrtf(d.row[tp.b * H + i] / mr) : 0.f;
+    }
+    consumer_sync();
+    float psq = 0.f;
+    bool ok = true;
+    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaConsumers, ++it) {
+      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+      if (!tma_acquire(&full[slot], ph, a, &stop)) {
+        ok = false;
+        break;
+      }
+      const int64_t i = rs + warp;
+      if (i < i1) {
+        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
+        const float r_i = rowf[i - i0];
+        float* pg = d.p + base + i * W + j0;
+        float* mg = B1 ? d.m1 + base + i * W + j0 : nullptr;
+#pragma unroll
+        for (int k = 0; k < kTileCols / 256; ++k) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cl = k * 256 + h * 128 + lane * 4;
+            if (j0 + cl < W) {
+              float x[4];
+              quad_g<GT>(x, row, cl);
+              const float4 f = *reinterpret_cast<const float4*>(colf + cl);
+              float4 pv = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
+              float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (B1) mv = *reinterpret_cast<const float4*>(row + RG::kG + RG::kP + cl * 4);
+              float* pp = &pv.x;
+              float* mp = &mv.x;
+              const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float upd = (x[v] * r_i) * fv[v];
+                if (B1) {
+                  mp[v] = fmaf(b1, mp[v], omb1 * upd);
+                  upd = mp[v];
+                }
+                const float pn = fmaf(-wda, pp[v], pp[v] - upd);
+                pp[v] = pn;
+                if (PSQ) psq = fmaf(pn, pn, psq);
+              }
+              __stcs(reinterpret_cast<float4*>(pg + cl), pv);
+              if (B1) __stcs(reinterpret_cast<float4*>(mg + cl), mv);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (PSQ) {
+      const double tot = consumer_sum(psq, red);
+      if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + local] = tot;
+    }
+  }
+  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
+}
+
 // ---- psq: sum(p_new^2) carry, one CTA per tensor --------------------------
 __global__ void __launch_bounds__(kThreads) k_psq(const __grid_constant__ StepArgs a) {
   __shared__ double red[16];
@@ -729,103 +1209,144 @@ const char* kernel_name(int k) {
 
 namespace {
 
-// Dynamic shared memory of each streaming instantiation.
-size_t smem_of(KernelId k, TensorClass c) {
-  if (k == kKPass1) return c == kClsUnfactored ? kRedBytes + kPrefixBytes : kColbufBytes + kRedBytes + kPrefixBytes;
-  if (k == kKStats) return kRedBytes + kPrefixBytes + kPartBytes;
-  if (k == kKApply && c == kClsUnfactored) return kRedBytes + kPrefixBytes;
-  return kRedBytes + kPrefixBytes + kColfBytes;
+// Dynamic shared memory of the bulk-copy kernels: ring, per-tile factors or
+// column buffer, reduction scratch, mbarriers, prefix.
+template <class RG>
+constexpr size_t tma_smem(size_t extra) {
+  return RG::kBytes + extra + sizeof(double) * 16 + sizeof(uint64_t) * 2 * RG::kStages + kPrefixBytes;
 }
+constexpr size_t kFactorBytes = sizeof(float) * (kTileCols + kTileRows);
 
 using KernelFn = void (*)(StepArgs, Range);
 
-// The instantiation of a streaming kind for a class and the per-call flags.
+// One launchable instantiation: function, block size, dynamic shared memory.
+struct Inst {
+  KernelFn fn = nullptr;
+  int threads = kThreads;
+  size_t smem = 0;
+};
+
 template <typename GT, int VEC>
-KernelFn pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
+Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
+  Inst x;
   switch (k) {
-    case kKPass1: return psq_in ? k_pass1_f<GT, VEC, true> : k_pass1_f<GT, VEC, false>;
-    case kKPass2: return k_pass2_f<GT, VEC>;
+    case kKPass1:
+      if (VEC == 8) {
+        x.threads = kTmaThreads;
+        x.fn = psq_in ? k_pass1_tma<GT, true> : k_pass1_tma<GT, false>;
+        x.smem = psq_in ? tma_smem<Pass1Ring<GT, true>>(kColbufBytes) : tma_smem<Pass1Ring<GT, false>>(kColbufBytes);
+        return x;
+      }
+      x.fn = psq_in ? k_pass1_f<GT, VEC, true> : k_pass1_f<GT, VEC, false>;
+      x.smem = kColbufBytes + kRedBytes + kPrefixBytes;
+      return x;
+    case kKPass2:
+      if (VEC == 8) {
+        x.threads = kTmaThreads;
+        x.fn = k_pass2_tma<GT>;
+        x.smem = tma_smem<Pass2Ring<GT>>(kFactorBytes);
+        return x;
+      }
+      x.fn = k_pass2_f<GT, VEC>;
+      x.smem = kRedBytes + kPrefixBytes + kColfBytes;
+      return x;
     case kKApply:
-      if (b1) return psq_out ? k_apply_f<GT, VEC, true, true> : k_apply_f<GT, VEC, true, false>;
-      return psq_out ? k_apply_f<GT, VEC, false, true> : k_apply_f<GT, VEC, false, false>;
-    default: return nullptr;
+      if (VEC == 8) {  // vector path: bulk-copy staged rows
+        x.threads = kTmaThreads;
+        if (b1) {
+          x.fn = psq_out ? k_apply_tma<GT, true, true> : k_apply_tma<GT, true, false>;
+          x.smem = tma_smem<ApplyRing<GT, true>>(kFactorBytes);
+        } else {
+          x.fn = psq_out ? k_apply_tma<GT, false, true> : k_apply_tma<GT, false, false>;
+          x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
+        }
+        return x;
+      }
+      if (b1) x.fn = psq_out ? k_apply_f<GT, VEC, true, true> : k_apply_f<GT, VEC, true, false>;
+      else x.fn = psq_out ? k_apply_f<GT, VEC, false, true> : k_apply_f<GT, VEC, false, false>;
+      x.smem = kRedBytes + kPrefixBytes + kColfBytes;
+      return x;
+    default: return x;
   }
 }
 
-KernelFn pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
+Inst pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
+  Inst x;
   switch (c) {
     case kClsVecBF16: return pick_f<__nv_bfloat16, 8>(k, psq_in, b1, psq_out);
     case kClsVecF32: return pick_f<float, 8>(k, psq_in, b1, psq_out);
     case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, b1, psq_out);
     case kClsScalarF32: return pick_f<float, 1>(k, psq_in, b1, psq_out);
     case kClsUnfactored:
-      if (k == kKPass1) return psq_in ? k_pass1_u<true> : k_pass1_u<false>;
+      x.smem = kRedBytes + kPrefixBytes;
+      if (k == kKPass1) x.fn = psq_in ? k_pass1_u<true> : k_pass1_u<false>;
       if (k == kKApply) {
-        if (b1) return psq_out ? k_apply_u<true, true> : k_apply_u<true, false>;
-        return psq_out ? k_apply_u<false, true> : k_apply_u<false, false>;
+        if (b1) x.fn = psq_out ? k_apply_u<true, true> : k_apply_u<true, false>;
+        else x.fn = psq_out ? k_apply_u<false, true> : k_apply_u<false, false>;
       }
-      return nullptr;
-    default: return nullptr;
+      return x;
+    default: return x;
   }
 }
 
 }  // namespace
 
-int kernel_grid_limit(KernelId k, int device, cudaError_t* err) {
-  // min over the kind's instantiations of (resident CTAs per SM) x SM count,
-  // cached per device.  Also raises the dynamic shared-memory limit where an
-  // instantiation needs more than the 48 KB default.
+int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err) {
+  // min over the instantiations of (kind, class) of (resident CTAs per SM) x
+  // SM count, cached per device.  Also raises the dynamic shared-memory limit
+  // of every instantiation that needs more than the 48 KB default.
   constexpr int kMaxDev = 64;
-  static int cache[kMaxDev][kNumKernels] = {};
+  static int cache[kMaxDev][kNumKernels][kNumClasses] = {};
   *err = cudaSuccess;
   if (device < 0 || device >= kMaxDev) {
     *err = cudaErrorInvalidDevice;
     return 0;
   }
-  if (cache[device][k] > 0) return cache[device][k];
+  if (cache[device][k][c] > 0) return cache[device][k][c];
   int sms = 0;
   *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (*err != cudaSuccess) return 0;
   int per_sm = 1 << 30;
-  auto visit = [&](const void* fn, size_t smem) {
+  auto visit = [&](const void* fn, int threads, size_t smem) {
     if (*err != cudaSuccess || fn == nullptr) return;
     if (smem > 48 * 1024) {
       *err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (*err != cudaSuccess) return;
     }
     int b = 0;
-    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, smem);
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
     if (*err == cudaSuccess && b < per_sm) per_sm = b;
   };
   if (k == kKPass1 || k == kKPass2 || k == kKApply) {
-    for (int c = 0; c < kNumClasses; ++c)
-      for (int v = 0; v < 8; ++v)
-        visit(reinterpret_cast<const void*>(pick(k, static_cast<TensorClass>(c), v & 1, v & 2, v & 4)),
-              smem_of(k, static_cast<TensorClass>(c)));
+    for (int v = 0; v < 8; ++v) {
+      const Inst x = pick(k, c, v & 1, v & 2, v & 4);
+      visit(reinterpret_cast<const void*>(x.fn), x.threads, x.smem);
+    }
   } else if (k == kKStats) {
-    visit(reinterpret_cast<const void*>(k_stats), smem_of(kKStats, kClsVecBF16));
+    visit(reinterpret_cast<const void*>(k_stats), kThreads, kRedBytes + kPrefixBytes + kPartBytes);
   } else {
     per_sm = 8;  // per-tensor kernels: grid = tensor count, not limited here
   }
   if (*err != cudaSuccess) return 0;
   if (per_sm < 1) per_sm = 1;
-  cache[device][k] = per_sm * sms;
-  return cache[device][k];
+  if (per_sm == (1 << 30)) per_sm = 1;
+  cache[device][k][c] = per_sm * sms;
+  return cache[device][k][c];
 }
 
 cudaError_t launch_stream(KernelId k, TensorClass c, const StepArgs& a, const Range& r, int grid,
                           cudaStream_t s) {
   if (grid <= 0 || r.m_end <= r.m_begin) return cudaSuccess;
   const bool psq_in = a.scale_parameter && !a.psq_valid;
-  KernelFn fn = pick(k, c, psq_in, a.has_beta1 != 0, a.want_psq_out != 0);
-  if (fn == nullptr) return cudaErrorInvalidValue;
-  fn<<<grid, kThreads, smem_of(k, c), s>>>(a, r);
+  const Inst x = pick(k, c, psq_in, a.has_beta1 != 0, a.want_psq_out != 0);
+  if (x.fn == nullptr) return cudaErrorInvalidValue;
+  x.fn<<<grid, x.threads, x.smem, s>>>(a, r);
   return cudaGetLastError();
 }
 
 cudaError_t launch_stats(const StepArgs& a, const Range& r, int grid, cudaStream_t s) {
   if (grid <= 0 || r.m_end <= r.m_begin) return cudaSuccess;
-  k_stats<<<grid, kThreads, smem_of(kKStats, kClsVecBF16), s>>>(a, r);
+  k_stats<<<grid, kThreads, kRedBytes + kPrefixBytes + kPartBytes, s>>>(a, r);
   return cudaGetLastError();
 }
 

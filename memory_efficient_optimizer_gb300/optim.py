@@ -150,6 +150,14 @@ class AdafactorStep:
             return False
         return self._versions == [(p.data_ptr(), p._version) for p in self.params]
 
+    def device_status(self, stream: torch.cuda.Stream | None = None) -> int:
+        """Status word of the last step (0 = fine); synchronises with the stream."""
+        if self.n == 0:
+            return 0
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        return B.adafactor_device_status(_ptr(self.workspace), int(stream.cuda_stream))
+
     def invalidate_param_sq_sum(self) -> None:
         """Forget the carried sum(p^2) (call after changing params behind torch's back)."""
         self._versions = None

@@ -106,6 +106,7 @@ def run_parity(workload: synth.Workload, steps=None, sample=None, gen_device="cp
             del before
         del host_g
     torch.cuda.synchronize()
+    assert run.step_fn.device_status() == 0, "a bounded wait inside a kernel gave up"
     report = {}
     for k in idxs:
         nm = f"{workload.name}[{k}]{shapes[k]}"
