@@ -307,6 +307,7 @@ constexpr size_t kRedBytes = sizeof(double) * 16;
 constexpr size_t kPrefixBytes = (sizeof(int32_t) * (kMaxGroup + 1) + 15) / 16 * 16;
 constexpr size_t kColfBytes = sizeof(float) * kTileCols;
 constexpr size_t kPartBytes = sizeof(float) * kWarps * kColChunk;
+constexpr size_t kRowfBytes = sizeof(float) * kTileRows;
 
 // Copies the launch's member prefix into shared memory; returns the member count.
 __device__ __forceinline__ int load_prefix(int32_t* pf, const Range& r) {
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ St
 // colf holds 1/col_j for the tile's columns (shared memory).
 template <typename GT, int VEC>
 __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArgs& a, int64_t local, float* colf,
-                               double* red) {
+                               float* rowf, double* red) {
   constexpr int CH = Layout<VEC>::CH, CG = Layout<VEC>::CG;
   constexpr int RPI = (VEC == 8 && sizeof(GT) == 4) ? 1 : 2;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -486,10 +487,14 @@ __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArg
   const float* row = d.row + tp.b * H;
   const float m = static_cast<float>(a.mrow[d.mslot + tp.b]);
 
-  __syncthreads();  // previous tile's readers of colf are done
+  __syncthreads();  // previous tile's readers of colf / rowf are done
   for (int cl = threadIdx.x; cl < kTileCols; cl += kThreads) {
     const int64_t j = j0 + cl;
     colf[colf_index<VEC>(cl)] = (j < W) ? 1.0f / d.col[tp.b * W + j] : 0.f;
+  }
+  for (int rl = threadIdx.x; rl < kTileRows; rl += kThreads) {
+    const int64_t i = i0 + rl;
+    rowf[rl] = (i < i1) ? m / row[i] : 0.f;
   }
   __syncthreads();
 
@@ -530,8 +535,7 @@ __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArg
     for (int rr = 0; rr < RPI; ++rr) {
       const int64_t ii = i + rr * kWarps;
       if (ii < i1) {
-        const float a_i = m / row[ii];
-        acc = fmaf(a_i, ts[rr], acc);
+        acc = fmaf(rowf[ii - i0], ts[rr], acc);
       }
     }
   }
@@ -545,12 +549,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass2_f(const __grid_constant__
   double* red = reinterpret_cast<double*>(smem);
   int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
   float* colf = reinterpret_cast<float*>(smem + kRedBytes + kPrefixBytes);
+  float* rowf = colf + kTileCols;
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
-    pass2_factored<GT, VEC>(d, a, u - pf[m], colf, red);
+    pass2_factored<GT, VEC>(d, a, u - pf[m], colf, rowf, red);
   }
 }
 
@@ -706,11 +711,10 @@ __global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ St
   }
 }
 
-// ---- vector path: bulk-copy (TMA) staged rows --------------------------------
-// The three streaming passes over the vector-path tensors share one scheme.
+// ---- vector path of apply: bulk-copy (TMA) staged rows ----------------------
 // One CTA per SM: warp 8 is the producer, warps 0-7 the consumers.  The
-// producer streams the tile rows (g, and p / exp_avg where the pass needs
-// them) into a ring of shared-memory stages of 8 rows with cp.async.bulk, one
+// producer streams the tile rows of g, p (and exp_avg) into a ring of
+// shared-memory stages of 8 rows with cp.async.bulk, one
 // copy per row segment, completion counted on the stage's "full" mbarrier.
 // Consumer warp w takes row w of every stage and releases the stage on its
 // "empty" mbarrier.  The bytes in flight are set by the ring depth, not by
@@ -881,204 +885,6 @@ __device__ __forceinline__ double consumer_sum(float v, double* red) {
   return s;
 }
 
-// ---- pass 1 (vector path) --------------------------------------------------
-template <typename GT, bool PSQ>
-using Pass1Ring = Ring<GT, PSQ, false, 176 * 1024>;
-
-template <typename GT, bool PSQ>
-__global__ void __launch_bounds__(kTmaThreads, 1) k_pass1_tma(const __grid_constant__ StepArgs a, const Range r) {
-  using RG = Pass1Ring<GT, PSQ>;
-  extern __shared__ __align__(16) unsigned char smem[];
-  unsigned char* ring = smem;
-  float* colbuf = reinterpret_cast<float*>(smem + RG::kBytes);          // kWarps x kTileCols
-  double* red = reinterpret_cast<double*>(colbuf + kWarps * kTileCols);  // 16
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 16);
-  uint64_t* empty = full + RG::kStages;
-  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
-  __shared__ int stop;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ng = tma_setup<RG::kStages>(pf, r, full, empty);
-  if (warp == kTmaConsumers) {
-    if (lane == 0) tma_produce<GT, RG>(a, r, pf, ng, ring, full, empty);
-    return;
-  }
-  if (threadIdx.x == 0) stop = 0;
-  const int64_t u1 = pf[ng];
-  uint32_t it = 0;
-  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
-    const int m = find_owner(pf, ng, u);
-    const DevTensor d = a.tensors[member_tensor(r, m)];
-    const int64_t local = u - pf[m];
-    const TilePos tp = tile_pos(d, local);
-    const int64_t H = d.H, W = d.W;
-    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
-    const int64_t j0 = tp.c * kTileCols;
-    float* rowpart = a.rowpart + d.rowpart + tp.c * static_cast<int64_t>(d.B) * H + tp.b * H;
-    consumer_sync();  // stop is settled; colbuf / red of the previous tile are read
-    if (stop) break;
-    float cacc[32];
-#pragma unroll
-    for (int q = 0; q < 32; ++q) cacc[q] = 0.f;
-    float psq = 0.f;
-    bool ok = true;
-    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaConsumers, ++it) {
-      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
-      if (!tma_acquire(&full[slot], ph, a, &stop)) {
-        ok = false;
-        break;
-      }
-      const int64_t i = rs + warp;
-      if (i < i1) {
-        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
-        float s = 0.f;
-#pragma unroll
-        for (int k = 0; k < kTileCols / 256; ++k) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int cl = k * 256 + h * 128 + lane * 4;
-            if (j0 + cl < W) {
-              float x[4];
-              quad_g<GT>(x, row, cl);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const float q = x[v] * x[v];
-                cacc[(k * 2 + h) * 4 + v] += q;
-                s += q;
-              }
-              if (PSQ) {
-                const float4 p = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
-                psq = fmaf(p.x, p.x, psq);
-                psq = fmaf(p.y, p.y, psq);
-                psq = fmaf(p.z, p.z, psq);
-                psq = fmaf(p.w, p.w, psq);
-              }
-            }
-          }
-        }
-        s = warp_sum(s);
-        if (lane == 0) rowpart[i] = s;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-    }
-    // column partials: the 8 warps' accumulators added in warp order
-    float* mine = colbuf + warp * kTileCols;
-#pragma unroll
-    for (int k = 0; k < kTileCols / 256; ++k) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        *reinterpret_cast<float4*>(mine + k * 256 + h * 128 + lane * 4) =
-            make_float4(cacc[(k * 2 + h) * 4], cacc[(k * 2 + h) * 4 + 1], cacc[(k * 2 + h) * 4 + 2],
-                        cacc[(k * 2 + h) * 4 + 3]);
-      }
-    }
-    consumer_sync();
-    if (!stop) {
-      float* colpart = a.colpart + d.colpart + (tp.b * d.rb + tp.r) * W;
-      for (int cl = threadIdx.x * 4; cl < kTileCols; cl += kTmaConsumers * 32 * 4) {
-        if (j0 + cl < W) {  // W % 8 == 0: the whole quad is inside
-          float4 s = *reinterpret_cast<const float4*>(colbuf + cl);
-#pragma unroll
-          for (int w = 1; w < kWarps; ++w) {
-            const float4 t = *reinterpret_cast<const float4*>(colbuf + w * kTileCols + cl);
-            s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
-          }
-          *reinterpret_cast<float4*>(colpart + j0 + cl) = s;
-        }
-      }
-    }
-    if (PSQ) {
-      const double tot = consumer_sum(psq, red);
-      if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + local] = tot;
-    }
-  }
-  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
-}
-
-// ---- pass 2 (vector path) --------------------------------------------------
-template <typename GT>
-using Pass2Ring = Ring<GT, false, false, 200 * 1024>;
-
-template <typename GT>
-__global__ void __launch_bounds__(kTmaThreads, 1) k_pass2_tma(const __grid_constant__ StepArgs a, const Range r) {
-  using RG = Pass2Ring<GT>;
-  extern __shared__ __align__(16) unsigned char smem[];
-  unsigned char* ring = smem;
-  float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // 1 / col_j
-  float* rowf = colf + kTileCols;                              // mean(row) / row_i
-  double* red = reinterpret_cast<double*>(rowf + kTileRows);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 16);
-  uint64_t* empty = full + RG::kStages;
-  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
-  __shared__ int stop;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ng = tma_setup<RG::kStages>(pf, r, full, empty);
-  if (warp == kTmaConsumers) {
-    if (lane == 0) tma_produce<GT, RG>(a, r, pf, ng, ring, full, empty);
-    return;
-  }
-  if (threadIdx.x == 0) stop = 0;
-  const int64_t u1 = pf[ng];
-  uint32_t it = 0;
-  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
-    const int m = find_owner(pf, ng, u);
-    const DevTensor d = a.tensors[member_tensor(r, m)];
-    const int64_t local = u - pf[m];
-    const TilePos tp = tile_pos(d, local);
-    const int64_t H = d.H, W = d.W;
-    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
-    const int64_t j0 = tp.c * kTileCols;
-    const float mr = static_cast<float>(a.mrow[d.mslot + tp.b]);
-    consumer_sync();  // stop is settled; colf / rowf / red of the previous tile are read
-    if (stop) break;
-    for (int cl = threadIdx.x; cl < kTileCols; cl += kTmaConsumers * 32) {
-      const int64_t j = j0 + cl;
-      colf[cl] = (j < W) ? 1.0f / d.col[tp.b * W + j] : 0.f;
-    }
-    for (int rl = threadIdx.x; rl < kTileRows; rl += kTmaConsumers * 32) {
-      const int64_t i = i0 + rl;
-      rowf[rl] = (i < i1) ? mr / d.row[tp.b * H + i] : 0.f;
-    }
-    consumer_sync();
-    float acc = 0.f;
-    bool ok = true;
-    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaConsumers, ++it) {
-      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
-      if (!tma_acquire(&full[slot], ph, a, &stop)) {
-        ok = false;
-        break;
-      }
-      const int64_t i = rs + warp;
-      if (i < i1) {
-        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
-        float ts = 0.f;
-#pragma unroll
-        for (int k = 0; k < kTileCols / 256; ++k) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int cl = k * 256 + h * 128 + lane * 4;
-            if (j0 + cl < W) {
-              float x[4];
-              quad_g<GT>(x, row, cl);
-              const float4 f = *reinterpret_cast<const float4*>(colf + cl);
-              ts = fmaf(x[0] * x[0], f.x, ts);
-              ts = fmaf(x[1] * x[1], f.y, ts);
-              ts = fmaf(x[2] * x[2], f.z, ts);
-              ts = fmaf(x[3] * x[3], f.w, ts);
-            }
-          }
-        }
-        acc = fmaf(rowf[i - i0], ts, acc);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-    }
-    const double tot = consumer_sum(acc, red);
-    if (threadIdx.x == 0 && !stop) a.spart[d.tile0 + local] = tot;
-  }
-  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
-}
-
 // ---- apply (vector path) ---------------------------------------------------
 template <typename GT, bool B1>
 using ApplyRing = Ring<GT, true, B1, 200 * 1024>;
@@ -1231,27 +1037,15 @@ Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
   Inst x;
   switch (k) {
     case kKPass1:
-      if (VEC == 8) {
-        x.threads = kTmaThreads;
-        x.fn = psq_in ? k_pass1_tma<GT, true> : k_pass1_tma<GT, false>;
-        x.smem = psq_in ? tma_smem<Pass1Ring<GT, true>>(kColbufBytes) : tma_smem<Pass1Ring<GT, false>>(kColbufBytes);
-        return x;
-      }
       x.fn = psq_in ? k_pass1_f<GT, VEC, true> : k_pass1_f<GT, VEC, false>;
       x.smem = kColbufBytes + kRedBytes + kPrefixBytes;
       return x;
     case kKPass2:
-      if (VEC == 8) {
-        x.threads = kTmaThreads;
-        x.fn = k_pass2_tma<GT>;
-        x.smem = tma_smem<Pass2Ring<GT>>(kFactorBytes);
-        return x;
-      }
       x.fn = k_pass2_f<GT, VEC>;
-      x.smem = kRedBytes + kPrefixBytes + kColfBytes;
+      x.smem = kRedBytes + kPrefixBytes + kColfBytes + kRowfBytes;
       return x;
     case kKApply:
-      if (VEC == 8) {  // vector path: bulk-copy staged rows
+      if constexpr (VEC == 8) {  // vector path: bulk-copy staged rows
         x.threads = kTmaThreads;
         if (b1) {
           x.fn = psq_out ? k_apply_tma<GT, true, true> : k_apply_tma<GT, true, false>;
@@ -1261,11 +1055,12 @@ Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
           x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
         }
         return x;
+      } else {
+        if (b1) x.fn = psq_out ? k_apply_f<GT, VEC, true, true> : k_apply_f<GT, VEC, true, false>;
+        else x.fn = psq_out ? k_apply_f<GT, VEC, false, true> : k_apply_f<GT, VEC, false, false>;
+        x.smem = kRedBytes + kPrefixBytes + kColfBytes;
+        return x;
       }
-      if (b1) x.fn = psq_out ? k_apply_f<GT, VEC, true, true> : k_apply_f<GT, VEC, true, false>;
-      else x.fn = psq_out ? k_apply_f<GT, VEC, false, true> : k_apply_f<GT, VEC, false, false>;
-      x.smem = kRedBytes + kPrefixBytes + kColfBytes;
-      return x;
     default: return x;
   }
 }
