@@ -26,7 +26,7 @@ EXPORTS = (
     "adafactor_default_hparams", "adafactor_validate", "adafactor_workspace_size",
     "adafactor_step", "adafactor_device_status", "adafactor_last_error", "adafactor_release_cache",
     "adafactor_profile_enable", "adafactor_profile_read", "adafactor_num_kernels",
-    "adafactor_kernel_name",
+    "adafactor_kernel_name", "adafactor_step_noalloc",
 )
 
 
@@ -92,6 +92,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.adafactor_step.restype = ctypes.c_int
         lib.adafactor_step.argtypes = [P(adaf_tensor), P(adaf_state), ctypes.c_int32, ctypes.c_int64,
                                        P(adaf_hparams), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        lib.adafactor_step_noalloc.restype = ctypes.c_int
+        lib.adafactor_step_noalloc.argtypes = [P(adaf_tensor), P(adaf_state), ctypes.c_int32, ctypes.c_int64,
+                                               P(adaf_hparams), ctypes.c_void_p]
         lib.adafactor_device_status.restype = ctypes.c_int
         lib.adafactor_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, P(ctypes.c_int32)]
         lib.adafactor_last_error.restype = ctypes.c_char_p
@@ -140,6 +143,12 @@ def adafactor_step(tensors, states, n: int, step: int, hp: adaf_hparams, workspa
     _check(load().adafactor_step(tensors, states, int(n), int(step), ctypes.byref(hp),
                                  ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes),
                                  ctypes.c_void_p(stream)))
+
+
+def adafactor_step_noalloc(tensors, states, n: int, step: int, hp: adaf_hparams, stream: int) -> None:
+    """The step with the library's fixed scratch area (no workspace argument)."""
+    _check(load().adafactor_step_noalloc(tensors, states, int(n), int(step), ctypes.byref(hp),
+                                         ctypes.c_void_p(stream)))
 
 
 def adafactor_device_status(workspace: int, stream: int) -> int:

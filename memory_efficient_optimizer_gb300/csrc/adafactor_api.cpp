@@ -308,41 +308,29 @@ cudaError_t get_event(DeviceCache& dc, cudaEvent_t* ev) {
   return cudaEventCreate(ev);
 }
 
+// Writes the uploaded header: status word 0, descriptor table, prefix arrays.
+void fill_header(unsigned char* h, const Plan& plan) {
+  const size_t nd = plan.dev.size();
+  std::memset(h, 0, kTableOffset);  // status word := 0
+  std::memcpy(h + kTableOffset, plan.dev.data(), nd * sizeof(DevTensor));
+  std::memcpy(h + plan.off_pf_tiles, plan.pf_tiles.data(), (nd + 1) * sizeof(int32_t));
+  std::memcpy(h + plan.off_pf_items, plan.pf_items.data(), (nd + 1) * sizeof(int32_t));
+  for (int c = 0; c < meo::kNumClasses; ++c) {
+    std::memcpy(h + plan.off_cls_pf[c], plan.cls_pf[c].data(), plan.cls_pf[c].size() * sizeof(int32_t));
+    if (!plan.cls_idx[c].empty())
+      std::memcpy(h + plan.off_cls_idx[c], plan.cls_idx[c].data(), plan.cls_idx[c].size() * sizeof(int32_t));
+  }
+}
+
 }  // namespace
 
-extern "C" {
+namespace meo {
 
-void adafactor_default_hparams(adaf_hparams* hp) {
-  if (hp == nullptr) return;
-  std::memset(hp, 0, sizeof(*hp));
-  hp->lr = 0.0;
-  hp->has_lr = 0;
-  hp->eps1 = 1e-30;
-  hp->eps2 = 1e-3;
-  hp->clip_threshold = 1.0;
-  hp->decay_rate = -0.8;
-  hp->beta1 = 0.0;
-  hp->has_beta1 = 0;
-  hp->weight_decay = 0.0;
-  hp->scale_parameter = 1;
-  hp->relative_step = 1;
-  hp->warmup_init = 0;
-  hp->param_sq_sum_valid = 0;
-}
-
-adaf_status adafactor_validate(const adaf_hparams* hp) { return check_hparams(hp); }
-
-adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size_t* bytes) {
-  if (bytes == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "bytes is NULL");
-  Plan plan;
-  adaf_status st = make_plan(tensors, nullptr, n, nullptr, false, &plan);
-  if (st != ADAF_OK) return st;
-  *bytes = plan.total_bytes;
-  return ADAF_OK;
-}
-
-adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
-                           const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream) {
+// The whole step: checks, plan, header upload, launch sequence.  Every
+// argument check runs before the first CUDA call.
+adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
+                      const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream,
+                      HeaderStaging staging) {
   adaf_status st = check_hparams(hp);
   if (st != ADAF_OK) return st;
   if (step < 1) return fail(ADAF_ERR_INVALID_ARGUMENT, "step must be >= 1");
@@ -389,42 +377,44 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
 
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceCache& dc = g_cache[device];
-  // Stage the header (descriptors + prefix arrays) and copy it to the workspace.
-  Slot& slot = dc.slots[dc.next];
-  dc.next = (dc.next + 1) % kSlots;
-  if (slot.pending) {
-    e = cudaEventSynchronize(slot.done);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize (staging slot)");
-    slot.pending = false;
+  if (staging == kStagePinned) {
+    // Stage the header (descriptors + prefix arrays) in a pinned ring slot and
+    // copy it to the workspace.
+    Slot& slot = dc.slots[dc.next];
+    dc.next = (dc.next + 1) % kSlots;
+    if (slot.pending) {
+      e = cudaEventSynchronize(slot.done);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize (staging slot)");
+      slot.pending = false;
+    }
+    if (slot.cap < plan.header_bytes) {
+      if (slot.host != nullptr) cudaFreeHost(slot.host);
+      slot.host = nullptr;
+      slot.cap = 0;
+      const size_t cap = align_up(plan.header_bytes, size_t(1) << 16);
+      e = cudaHostAlloc(&slot.host, cap, cudaHostAllocPortable);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc (staging)");
+      slot.cap = cap;
+    }
+    if (slot.done == nullptr) {
+      e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate (staging)");
+    }
+    fill_header(static_cast<unsigned char*>(slot.host), plan);
+    e = cudaMemcpyAsync(ws, slot.host, plan.header_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (descriptor table)");
+    e = cudaEventRecord(slot.done, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");
+    slot.pending = true;
+  } else {
+    // Pageable staging: the runtime copies the host bytes out before the
+    // call returns, so a local buffer suffices.
+    std::vector<unsigned char> h(plan.header_bytes);
+    fill_header(h.data(), plan);
+    e = cudaMemcpyAsync(ws, h.data(), plan.header_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (descriptor table)");
   }
-  if (slot.cap < plan.header_bytes) {
-    if (slot.host != nullptr) cudaFreeHost(slot.host);
-    slot.host = nullptr;
-    slot.cap = 0;
-    const size_t cap = align_up(plan.header_bytes, size_t(1) << 16);
-    e = cudaHostAlloc(&slot.host, cap, cudaHostAllocPortable);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc (staging)");
-    slot.cap = cap;
-  }
-  if (slot.done == nullptr) {
-    e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate (staging)");
-  }
-  unsigned char* h = static_cast<unsigned char*>(slot.host);
-  std::memset(h, 0, kTableOffset);  // status word := 0
-  std::memcpy(h + kTableOffset, plan.dev.data(), nd * sizeof(DevTensor));
-  std::memcpy(h + plan.off_pf_tiles, plan.pf_tiles.data(), (nd + 1) * sizeof(int32_t));
-  std::memcpy(h + plan.off_pf_items, plan.pf_items.data(), (nd + 1) * sizeof(int32_t));
-  for (int c = 0; c < meo::kNumClasses; ++c) {
-    std::memcpy(h + plan.off_cls_pf[c], plan.cls_pf[c].data(), plan.cls_pf[c].size() * sizeof(int32_t));
-    if (!plan.cls_idx[c].empty())
-      std::memcpy(h + plan.off_cls_idx[c], plan.cls_idx[c].data(), plan.cls_idx[c].size() * sizeof(int32_t));
-  }
-  e = cudaMemcpyAsync(ws, h, plan.header_bytes, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (descriptor table)");
-  e = cudaEventRecord(slot.done, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");
-  slot.pending = true;
+  const bool profile = g_profile && staging == kStagePinned;
 
   StepArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -456,14 +446,14 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
   auto run = [&](KernelId k, int cls, auto&& launch) -> adaf_status {
     ProfRecord rec{profile_slot(k, cls), device, nullptr, nullptr};
     cudaError_t err;
-    if (g_profile) {
+    if (profile) {
       if ((err = get_event(dc, &rec.start)) != cudaSuccess) return cuda_fail(err, "cudaEventCreate (profile)");
       if ((err = get_event(dc, &rec.stop)) != cudaSuccess) return cuda_fail(err, "cudaEventCreate (profile)");
       if ((err = cudaEventRecord(rec.start, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord (profile)");
     }
     err = launch();
     if (err != cudaSuccess) return cuda_fail(err, meo::kernel_name(k));
-    if (g_profile) {
+    if (profile) {
       if ((err = cudaEventRecord(rec.stop, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord (profile)");
       g_prof.push_back(rec);
     }
@@ -515,6 +505,46 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
     if (st != ADAF_OK) return st;
   }
   return ADAF_OK;
+}
+
+adaf_status set_last_error(adaf_status st, const char* msg) { return fail(st, msg); }
+
+}  // namespace meo
+
+extern "C" {
+
+void adafactor_default_hparams(adaf_hparams* hp) {
+  if (hp == nullptr) return;
+  std::memset(hp, 0, sizeof(*hp));
+  hp->lr = 0.0;
+  hp->has_lr = 0;
+  hp->eps1 = 1e-30;
+  hp->eps2 = 1e-3;
+  hp->clip_threshold = 1.0;
+  hp->decay_rate = -0.8;
+  hp->beta1 = 0.0;
+  hp->has_beta1 = 0;
+  hp->weight_decay = 0.0;
+  hp->scale_parameter = 1;
+  hp->relative_step = 1;
+  hp->warmup_init = 0;
+  hp->param_sq_sum_valid = 0;
+}
+
+adaf_status adafactor_validate(const adaf_hparams* hp) { return check_hparams(hp); }
+
+adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size_t* bytes) {
+  if (bytes == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  Plan plan;
+  adaf_status st = make_plan(tensors, nullptr, n, nullptr, false, &plan);
+  if (st != ADAF_OK) return st;
+  *bytes = plan.total_bytes;
+  return ADAF_OK;
+}
+
+adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
+                           const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream) {
+  return meo::step_impl(tensors, states, n, step, hp, workspace, workspace_bytes, stream, meo::kStagePinned);
 }
 
 const char* adafactor_last_error(void) { return g_last_error.c_str(); }

@@ -137,4 +137,22 @@ cudaError_t launch_per_tensor(KernelId k, const StepArgs& a, int ntensors, cudaS
 int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err);
 const char* kernel_name(int k);
 
+// How adafactor-step host code uploads the per-call header to the workspace.
+enum HeaderStaging : int {
+  kStagePinned = 0,    // library-owned pinned ring (cudaHostAlloc once), async copy
+  kStagePageable = 1,  // pageable host buffer; no allocation by the CUDA runtime API
+};
+
+}  // namespace meo
+
+#include "adafactor.h"
+
+namespace meo {
+// The step behind adafactor_step() (adafactor_api.cpp).  Per-kernel event
+// timing is recorded only with kStagePinned.
+adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
+                      const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream,
+                      HeaderStaging staging);
+// Records msg for adafactor_last_error() on this thread; returns st.
+adaf_status set_last_error(adaf_status st, const char* msg);
 }  // namespace meo

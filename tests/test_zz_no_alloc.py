@@ -1,0 +1,75 @@
+"""adafactor_step_noalloc: the step for callers that cannot allocate.
+
+Some callers cannot hand the library any device memory: code that runs while a
+memory pool owns the whole device and forbids cudaMalloc, code where an
+allocation would synchronise the device at the wrong moment, or hosts without
+an allocator of their own.  adafactor_step_noalloc() serves them with a fixed
+scratch array compiled into the library.  These tests check, through the C
+ABI, that it gives the same results as adafactor_step() with a caller
+workspace on two calls in a row, and that a list too large for its scratch is
+turned away with a clear error.  This file is named to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from memory_efficient_optimizer_gb300 import binding as B
+from memory_efficient_optimizer_gb300 import synth
+from memory_efficient_optimizer_gb300.optim import AdafactorStep, init_state, make_hparams
+
+SHAPES = [(600, 2100), (33, 520), (77, 13), (300,), (2, 64, 40), (1, 4096)]
+HP = dict(beta1=0.9, weight_decay=0.01)
+
+
+@pytest.mark.gpu
+def test_noalloc_step_matches_workspace_step_on_two_calls():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    p_ws = [synth.make_param(s, k).to(dev) for k, s in enumerate(SHAPES)]
+    p_na = [p.clone() for p in p_ws]
+    g = [torch.empty(s, device=dev, dtype=torch.bfloat16) for s in SHAPES]
+    st_ws = init_state(p_ws, beta1=HP["beta1"])
+    st_na = init_state(p_na, beta1=HP["beta1"])
+    with_ws = AdafactorStep(p_ws, g, st_ws, **HP)
+    marshal = AdafactorStep(p_na, g, st_na, **HP)  # only its descriptor arrays are used
+    stream = torch.cuda.current_stream(dev)
+    for t in (1, 2):
+        for k, s in enumerate(SHAPES):
+            g[k].copy_(synth.make_grad(s, k, t, dtype=torch.bfloat16))
+        with_ws(t)
+        hp = make_hparams(**HP, param_sq_sum_valid=(t > 1))
+        B.adafactor_step_noalloc(marshal._tensors, marshal._states, len(SHAPES), t, hp, int(stream.cuda_stream))
+        torch.cuda.synchronize()
+        for k in range(len(SHAPES)):
+            a = p_na[k].double().cpu().numpy()
+            b = p_ws[k].double().cpu().numpy()
+            assert np.all(np.abs(a - b) <= 1e-7 + 2e-5 * np.abs(b)), (t, k)
+            for name in st_ws[k]:
+                x = st_na[k][name].double().cpu().numpy()
+                y = st_ws[k][name].double().cpu().numpy()
+                assert np.all(np.abs(x - y) <= 1e-7 + 2e-5 * np.abs(y)), (t, k, name)
+
+
+def test_noalloc_rejects_a_list_beyond_its_scratch():
+    """Llama-3-8B needs ~157 MB of scratch: more than the fixed area, so the
+    call fails before touching CUDA, naming both sizes."""
+    shapes = [s for _, s in synth.llama3_8b_shapes()]
+    n = len(shapes)
+    ts = (B.adaf_tensor * n)()
+    ss = (B.adaf_state * n)()
+    for k, s in enumerate(shapes):
+        ts[k].param = ts[k].grad = 1 << 20
+        ts[k].grad_dtype = B.ADAF_BFLOAT16
+        ts[k].ndim = len(s)
+        for d, v in enumerate(s):
+            ts[k].shape[d] = v
+    hp = B.adafactor_default_hparams()
+    rc = B.load().adafactor_step_noalloc(ts, ss, n, 1, ctypes.byref(hp), None)
+    assert rc == B.ADAF_ERR_WORKSPACE_TOO_SMALL
+    msg = B.adafactor_last_error()
+    need = B.adafactor_workspace_size(ts, n)
+    assert str(need) in msg and str(64 << 20) in msg
