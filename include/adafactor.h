@@ -203,6 +203,15 @@ adaf_status adafactor_step_noalloc(const adaf_tensor* tensors, const adaf_state*
 #define ADAF_DEVICE_WAIT_TIMEOUT 1
 adaf_status adafactor_device_status(const void* workspace, void* stream, int32_t* status);
 
+/* Testing hook for the device-side failure detection.  With
+ * adafactor_debug_stall_copies(1), the bulk-copy producers of every following
+ * adafactor_step() on any thread issue no copies, so the consumers' bounded
+ * waits run out (about a second each): the step then ends early with
+ * ADAF_DEVICE_WAIT_TIMEOUT in the device status word and garbage results, and
+ * the CUDA context stays usable.  adafactor_debug_stall_copies(0) restores
+ * normal operation.  For tests only; no other effect. */
+void adafactor_debug_stall_copies(int32_t on);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* adafactor_last_error(void);
 

@@ -20,13 +20,14 @@ ADAF_ERR_CUDA = 4
 ADAF_FLOAT32 = 0
 ADAF_BFLOAT16 = 1
 ADAF_MAX_NDIM = 8
+ADAF_DEVICE_WAIT_TIMEOUT = 1
 
 # Entry points declared in include/adafactor.h.
 EXPORTS = (
     "adafactor_default_hparams", "adafactor_validate", "adafactor_workspace_size",
     "adafactor_step", "adafactor_device_status", "adafactor_last_error", "adafactor_release_cache",
     "adafactor_profile_enable", "adafactor_profile_read", "adafactor_num_kernels",
-    "adafactor_kernel_name", "adafactor_step_noalloc",
+    "adafactor_kernel_name", "adafactor_step_noalloc", "adafactor_debug_stall_copies",
 )
 
 
@@ -97,6 +98,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                                P(adaf_hparams), ctypes.c_void_p]
         lib.adafactor_device_status.restype = ctypes.c_int
         lib.adafactor_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, P(ctypes.c_int32)]
+        lib.adafactor_debug_stall_copies.restype = None
+        lib.adafactor_debug_stall_copies.argtypes = [ctypes.c_int32]
         lib.adafactor_last_error.restype = ctypes.c_char_p
         lib.adafactor_last_error.argtypes = []
         lib.adafactor_release_cache.restype = None
@@ -155,6 +158,11 @@ def adafactor_device_status(workspace: int, stream: int) -> int:
     out = ctypes.c_int32(0)
     _check(load().adafactor_device_status(ctypes.c_void_p(workspace), ctypes.c_void_p(stream), ctypes.byref(out)))
     return int(out.value)
+
+
+def adafactor_debug_stall_copies(on: bool) -> None:
+    """Testing hook: make the bulk-copy producers issue nothing (see the header)."""
+    load().adafactor_debug_stall_copies(1 if on else 0)
 
 
 def adafactor_last_error() -> str:

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -73,22 +74,36 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 struct Plan {
   std::vector<DevTensor> dev;       // one per non-empty tensor
   std::vector<int32_t> pf_tiles, pf_items;
-  // Per tensor class: member tensor indices and the prefix of their tiles.
-  std::vector<int32_t> cls_idx[meo::kNumClasses], cls_pf[meo::kNumClasses];
+  // Per tensor class: member tensor indices and, per streaming kind, the
+  // prefix of their work units (pass 1, pass 2, apply).
+  std::vector<int32_t> cls_idx[meo::kNumClasses];
+  std::vector<int32_t> cls_pf[3][meo::kNumClasses];
   size_t off_pf_tiles = 0, off_pf_items = 0, header_bytes = 0;
-  size_t off_cls_idx[meo::kNumClasses] = {}, off_cls_pf[meo::kNumClasses] = {};
-  size_t off_alpha = 0, off_coef = 0, off_mrow = 0, off_rowchunk = 0, off_spart = 0, off_ppart = 0;
-  size_t off_rowpart = 0, off_colpart = 0, total_bytes = 0;
+  size_t off_cls_idx[meo::kNumClasses] = {}, off_cls_pf[3][meo::kNumClasses] = {};
+  size_t off_alpha = 0, off_coef = 0, off_ssum = 0, off_mrow = 0, off_rowchunk = 0, off_dsum = 0;
+  size_t off_spart = 0, off_ppart = 0, off_rowpart = 0, off_colpart = 0, off_dpart = 0, total_bytes = 0;
   bool any_factored = false;
 };
 
+// Index of a streaming kind in Plan::cls_pf.
+int stream_slot(KernelId k) { return k == meo::kKPass1 ? 0 : (k == meo::kKPass2 ? 1 : 2); }
+
+// Rows per panel of the fused pass: about 2^20 values (256 rows of 4096).
+int32_t panel_rows(int64_t W) {
+  return static_cast<int32_t>(ceil_div((int64_t(1) << 20) / W, 4) * 4);
+}
+
 // Checks the tensor list and builds the plan.  With full == false (size
 // query) only the shapes and dtypes are read; states and hp are not touched.
+// The workspace layout is the same either way: it reserves room for both
+// factored paths a tensor may take (which one depends on pointer alignment,
+// known only at step time).
 adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
                       const adaf_hparams* hp, bool full, Plan* plan) {
   if (n < 0) return fail(ADAF_ERR_INVALID_ARGUMENT, "n must be >= 0");
   if (n > 0 && tensors == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "tensors is NULL");
-  int64_t tiles = 0, ftiles = 0, items = 0, nmrow = 0, nrowchunk = 0, nrowpart = 0, ncolpart = 0;
+  int64_t tiles = 0, p1units = 0, items = 0, nmrow = 0, nrowchunk = 0, ndsum = 0;
+  int64_t nrowpart = 0, ncolpart = 0, ndpart = 0;
   plan->dev.clear();
   plan->dev.reserve(n);
   for (int32_t k = 0; k < n; ++k) {
@@ -118,43 +133,6 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
     std::memset(&d, 0, sizeof(d));
     d.n = numel;
     d.gdt = t.grad_dtype == ADAF_BFLOAT16 ? meo::kGradBF16 : meo::kGradF32;
-    int64_t ntiles;
-    if (t.ndim >= 2) {
-      const int64_t H = t.shape[t.ndim - 2], W = t.shape[t.ndim - 1];
-      const int64_t B = numel / (H * W);
-      if (B > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, std::string(pre) + "too many leading slices");
-      d.H = H;
-      d.W = W;
-      d.B = static_cast<int32_t>(B);
-      d.rb = static_cast<int32_t>(ceil_div(H, meo::kTileRows));
-      d.cb = static_cast<int32_t>(ceil_div(W, meo::kTileCols));
-      d.nrc = static_cast<int32_t>(ceil_div(H, meo::kRowChunk));
-      d.ncc = static_cast<int32_t>(ceil_div(W, meo::kColChunk));
-      ntiles = B * d.rb * d.cb;
-      ftiles += ntiles;
-      items += B * (d.nrc + d.ncc);
-      d.mslot = nmrow;
-      nmrow += B;
-      d.rowchunk = nrowchunk;
-      nrowchunk += B * d.nrc;
-      d.rowpart = nrowpart;
-      nrowpart += align_up(static_cast<int64_t>(d.cb) * B * H, 4);
-      d.colpart = ncolpart;  // multiple of 4 floats: 16-byte aligned column quads
-      ncolpart += align_up(B * d.rb * W, 4);
-      plan->any_factored = true;
-    } else {
-      d.H = 1;
-      d.W = numel;
-      d.B = 1;
-      ntiles = ceil_div(numel, meo::kTile1D);
-      d.rb = 1;
-      d.cb = static_cast<int32_t>(ntiles > INT32_MAX ? INT32_MAX : ntiles);
-      d.kind = meo::kUnfactored;
-    }
-    d.tile0 = tiles;
-    tiles += ntiles;
-    if (tiles > INT32_MAX || items > INT32_MAX)
-      return fail(ADAF_ERR_UNSUPPORTED, "the tensor list needs more than 2^31-1 work tiles");
     if (full) {
       const adaf_state& s = states[k];
       d.p = t.param;
@@ -182,14 +160,80 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
         return fail(ADAF_ERR_INVALID_ARGUMENT,
                     std::string(pre) + "param_sq_sum_valid is set but param_sq_sum is NULL");
       d.psq = s.param_sq_sum;
-      if (t.ndim >= 2) {
-        const bool vec = (d.W % 8 == 0) && aligned(t.param, 16) && aligned(t.grad, 16) &&
-                         (!hp->has_beta1 || aligned(s.exp_avg, 16));
-        d.kind = vec ? meo::kFactoredVec : meo::kFactoredScalar;
-      }
-    } else if (t.ndim >= 2) {
-      d.kind = meo::kFactoredScalar;
     }
+    int64_t ntiles, nunits;
+    if (t.ndim >= 2) {
+      const int64_t H = t.shape[t.ndim - 2], W = t.shape[t.ndim - 1];
+      const int64_t B = numel / (H * W);
+      if (B > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, std::string(pre) + "too many leading slices");
+      d.H = H;
+      d.W = W;
+      d.B = static_cast<int32_t>(B);
+      d.rb = static_cast<int32_t>(ceil_div(H, meo::kTileRows));
+      d.cb = static_cast<int32_t>(ceil_div(W, meo::kTileCols));
+      d.ncc = static_cast<int32_t>(ceil_div(W, meo::kColChunk));
+      ntiles = B * d.rb * d.cb;
+      // Path: vector (16-byte aligned rows) or element-wise; a vector tensor
+      // with W <= kMaxRowsW takes the fused row-panel pass 1.
+      const bool vec_shape = (W % 8 == 0);
+      const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxRowsW;
+      bool vec = vec_shape;
+      if (full) {
+        vec = vec_shape && aligned(t.param, 16) && aligned(t.grad, 16) &&
+              (!hp->has_beta1 || aligned(d.m1, 16));
+        d.kind = !vec ? meo::kFactoredScalar : (rows_shape ? meo::kFactoredRows : meo::kFactoredVec);
+      } else {
+        d.kind = rows_shape ? meo::kFactoredRows : meo::kFactoredScalar;
+      }
+      // Row-panel geometry (also reserved in the size query for rows_shape).
+      int32_t prb_rows = 0;
+      if (rows_shape) {
+        d.seg = static_cast<int32_t>(ceil_div(W, 256));
+        d.pr = panel_rows(W);
+        prb_rows = static_cast<int32_t>(ceil_div(H, d.pr));
+      }
+      const bool fused = d.kind == meo::kFactoredRows;
+      // The layout reserves room for every path the tensor may take (which
+      // one depends on pointer alignment), so the workspace size does not
+      // depend on the pointers.
+      const bool need_tiled = true;
+      const bool need_rows = rows_shape;
+      d.nrc = fused ? prb_rows : static_cast<int32_t>(ceil_div(H, meo::kRowChunk));
+      d.prb = fused ? prb_rows : d.rb;
+      nunits = fused ? B * prb_rows : ntiles;
+      items += B * (fused ? d.ncc : (d.nrc + d.ncc));
+      d.mslot = nmrow;
+      nmrow += B;
+      d.rowchunk = nrowchunk;
+      const int64_t nrc_max = std::max<int64_t>(d.nrc, need_tiled ? ceil_div(H, meo::kRowChunk) : 0);
+      nrowchunk += B * std::max<int64_t>(nrc_max, need_rows ? prb_rows : 0);
+      d.rowpart = nrowpart;
+      if (need_tiled) nrowpart += align_up(static_cast<int64_t>(d.cb) * B * H, 4);
+      d.colpart = ncolpart;  // multiple of 4 floats: 16-byte aligned column quads
+      ncolpart += align_up(B * std::max<int64_t>(need_tiled ? d.rb : 0, need_rows ? prb_rows : 0) * W, 4);
+      d.dpart = ndpart;
+      if (need_rows) ndpart += align_up(B * prb_rows * W, 4);
+      d.dsum = ndsum;
+      if (need_rows) ndsum += B * d.ncc;
+      plan->any_factored = true;
+    } else {
+      d.H = 1;
+      d.W = numel;
+      d.B = 1;
+      ntiles = ceil_div(numel, meo::kTile1D);
+      nunits = ntiles;
+      d.rb = 1;
+      d.cb = static_cast<int32_t>(ntiles > INT32_MAX ? INT32_MAX : ntiles);
+      d.kind = meo::kUnfactored;
+    }
+    d.ntiles = ntiles;
+    d.tile0 = tiles;
+    tiles += ntiles;
+    d.p1_0 = p1units;
+    d.p1_n = nunits;
+    p1units += nunits;
+    if (tiles > INT32_MAX || items > INT32_MAX || p1units > INT32_MAX)
+      return fail(ADAF_ERR_UNSUPPORTED, "the tensor list needs more than 2^31-1 work tiles");
     plan->dev.push_back(d);
   }
   const size_t nd = plan->dev.size();
@@ -197,19 +241,24 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
   plan->pf_items.assign(nd + 1, 0);
   for (int c = 0; c < meo::kNumClasses; ++c) {
     plan->cls_idx[c].clear();
-    plan->cls_pf[c].assign(1, 0);
+    for (int q = 0; q < 3; ++q) plan->cls_pf[q][c].assign(1, 0);
   }
   for (size_t k = 0; k < nd; ++k) {
     const DevTensor& d = plan->dev[k];
-    const int64_t nt = d.kind == meo::kUnfactored ? d.cb : int64_t(d.B) * d.rb * d.cb;
-    plan->pf_tiles[k + 1] = plan->pf_tiles[k] + static_cast<int32_t>(nt);
+    plan->pf_tiles[k + 1] = plan->pf_tiles[k] + static_cast<int32_t>(d.ntiles);
+    const int64_t per_slice = d.kind == meo::kFactoredRows ? d.ncc : (d.nrc + d.ncc);
     plan->pf_items[k + 1] =
-        plan->pf_items[k] + (d.kind == meo::kUnfactored ? 0 : static_cast<int32_t>(int64_t(d.B) * (d.nrc + d.ncc)));
+        plan->pf_items[k] + (d.kind == meo::kUnfactored ? 0 : static_cast<int32_t>(int64_t(d.B) * per_slice));
     int c = meo::kClsUnfactored;
-    if (d.kind == meo::kFactoredVec) c = d.gdt == meo::kGradBF16 ? meo::kClsVecBF16 : meo::kClsVecF32;
-    if (d.kind == meo::kFactoredScalar) c = d.gdt == meo::kGradBF16 ? meo::kClsScalarBF16 : meo::kClsScalarF32;
+    const bool bf = d.gdt == meo::kGradBF16;
+    if (d.kind == meo::kFactoredVec) c = bf ? meo::kClsVecBF16 : meo::kClsVecF32;
+    if (d.kind == meo::kFactoredScalar) c = bf ? meo::kClsScalarBF16 : meo::kClsScalarF32;
+    if (d.kind == meo::kFactoredRows) c = bf ? meo::kClsRowsBF16 : meo::kClsRowsF32;
+    const bool two_pass = d.kind == meo::kFactoredVec || d.kind == meo::kFactoredScalar;
     plan->cls_idx[c].push_back(static_cast<int32_t>(k));
-    plan->cls_pf[c].push_back(plan->cls_pf[c].back() + static_cast<int32_t>(nt));
+    plan->cls_pf[0][c].push_back(plan->cls_pf[0][c].back() + static_cast<int32_t>(d.p1_n));
+    plan->cls_pf[1][c].push_back(plan->cls_pf[1][c].back() + (two_pass ? static_cast<int32_t>(d.ntiles) : 0));
+    plan->cls_pf[2][c].push_back(plan->cls_pf[2][c].back() + static_cast<int32_t>(d.ntiles));
   }
   // Workspace layout: the header (uploaded each call: the device status word
   // at offset 0, the descriptor table at kTableOffset, the prefix arrays)
@@ -220,29 +269,31 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
   plan->off_pf_items = off;
   off += align_up((nd + 1) * sizeof(int32_t), 16);
   for (int c = 0; c < meo::kNumClasses; ++c) {
-    plan->off_cls_pf[c] = off;
-    off += align_up(plan->cls_pf[c].size() * sizeof(int32_t), 16);
+    for (int q = 0; q < 3; ++q) {
+      plan->off_cls_pf[q][c] = off;
+      off += align_up(plan->cls_pf[q][c].size() * sizeof(int32_t), 16);
+    }
     plan->off_cls_idx[c] = off;
     off += align_up(plan->cls_idx[c].size() * sizeof(int32_t), 16);
   }
   plan->header_bytes = off;
   off = align_up(off, 256);
-  plan->off_alpha = off;
-  off = align_up(off + nd * sizeof(double), 256);
-  plan->off_coef = off;
-  off = align_up(off + nd * sizeof(double), 256);
-  plan->off_mrow = off;
-  off = align_up(off + nmrow * sizeof(double), 256);
-  plan->off_rowchunk = off;
-  off = align_up(off + nrowchunk * sizeof(double), 256);
-  plan->off_spart = off;
-  off = align_up(off + tiles * sizeof(double), 256);
-  plan->off_ppart = off;
-  off = align_up(off + tiles * sizeof(double), 256);
-  plan->off_rowpart = off;
-  off = align_up(off + nrowpart * sizeof(float), 256);
-  plan->off_colpart = off;
-  off = align_up(off + ncolpart * sizeof(float), 256);
+  const int64_t nppart = std::max(tiles, p1units);
+  auto region = [&](size_t* where, size_t bytes) {
+    *where = off;
+    off = align_up(off + bytes, 256);
+  };
+  region(&plan->off_alpha, nd * sizeof(double));
+  region(&plan->off_coef, nd * sizeof(double));
+  region(&plan->off_ssum, nd * sizeof(double));
+  region(&plan->off_mrow, nmrow * sizeof(double));
+  region(&plan->off_rowchunk, nrowchunk * sizeof(double));
+  region(&plan->off_dsum, ndsum * sizeof(double));
+  region(&plan->off_spart, tiles * sizeof(double));
+  region(&plan->off_ppart, nppart * sizeof(double));
+  region(&plan->off_rowpart, nrowpart * sizeof(float));
+  region(&plan->off_colpart, ncolpart * sizeof(float));
+  region(&plan->off_dpart, ndpart * sizeof(float));
   plan->total_bytes = off;
   return ADAF_OK;
 }
@@ -270,31 +321,46 @@ struct ProfRecord {
   cudaEvent_t start, stop;
 };
 
-// Profiling slots: one per streaming kernel and tensor class, one per other
-// kernel kind, in launch order.
-constexpr int kNumSlots = 18;
-const char* const kSlotNames[kNumSlots] = {
-    "k_pass1[vec_bf16]", "k_pass1[vec_f32]", "k_pass1[elem_bf16]", "k_pass1[elem_f32]", "k_pass1[1d]",
-    "k_stats", "k_scalars",
-    "k_pass2[vec_bf16]", "k_pass2[vec_f32]", "k_pass2[elem_bf16]", "k_pass2[elem_f32]",
-    "k_clip",
-    "k_apply[vec_bf16]", "k_apply[vec_f32]", "k_apply[elem_bf16]", "k_apply[elem_f32]", "k_apply[1d]",
-    "k_psq"};
+// Profiling slots: one per streaming kernel kind and tensor class, one per
+// other kernel kind, in launch order.
+constexpr int kNumSlots = 3 * meo::kNumClasses + 4;
+const char* const kClassNames[meo::kNumClasses] = {"vec_bf16", "vec_f32",  "elem_bf16", "elem_f32",
+                                                   "1d",       "rows_bf16", "rows_f32"};
 
 int profile_slot(KernelId k, int cls) {
+  const int C = meo::kNumClasses;
   switch (k) {
-    case meo::kKPass1: return 0 + cls;
-    case meo::kKStats: return 5;
-    case meo::kKScalars: return 6;
-    case meo::kKPass2: return 7 + cls;
-    case meo::kKClip: return 11;
-    case meo::kKApply: return 12 + cls;
-    case meo::kKPsq: return 17;
+    case meo::kKPass1: return cls;
+    case meo::kKStats: return C;
+    case meo::kKScalars: return C + 1;
+    case meo::kKPass2: return C + 2 + cls;
+    case meo::kKClip: return 2 * C + 2;
+    case meo::kKApply: return 2 * C + 3 + cls;
+    case meo::kKPsq: return 3 * C + 3;
     default: return 0;
   }
 }
 
+const char* slot_name(int slot) {
+  static std::string names[kNumSlots];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const int C = meo::kNumClasses;
+    for (int c = 0; c < C; ++c) {
+      names[c] = std::string("k_pass1[") + kClassNames[c] + "]";
+      names[C + 2 + c] = std::string("k_pass2[") + kClassNames[c] + "]";
+      names[2 * C + 3 + c] = std::string("k_apply[") + kClassNames[c] + "]";
+    }
+    names[C] = "k_stats";
+    names[C + 1] = "k_scalars";
+    names[2 * C + 2] = "k_clip";
+    names[3 * C + 3] = "k_psq";
+  });
+  return (slot >= 0 && slot < kNumSlots) ? names[slot].c_str() : "";
+}
+
 std::mutex g_mu;
+std::atomic<int> g_stall_copies{0};
 std::map<int, DeviceCache> g_cache;
 bool g_profile = false;
 std::vector<ProfRecord> g_prof;
@@ -316,7 +382,8 @@ void fill_header(unsigned char* h, const Plan& plan) {
   std::memcpy(h + plan.off_pf_tiles, plan.pf_tiles.data(), (nd + 1) * sizeof(int32_t));
   std::memcpy(h + plan.off_pf_items, plan.pf_items.data(), (nd + 1) * sizeof(int32_t));
   for (int c = 0; c < meo::kNumClasses; ++c) {
-    std::memcpy(h + plan.off_cls_pf[c], plan.cls_pf[c].data(), plan.cls_pf[c].size() * sizeof(int32_t));
+    for (int q = 0; q < 3; ++q)
+      std::memcpy(h + plan.off_cls_pf[q][c], plan.cls_pf[q][c].data(), plan.cls_pf[q][c].size() * sizeof(int32_t));
     if (!plan.cls_idx[c].empty())
       std::memcpy(h + plan.off_cls_idx[c], plan.cls_idx[c].data(), plan.cls_idx[c].size() * sizeof(int32_t));
   }
@@ -426,6 +493,9 @@ adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int3
   a.coef = reinterpret_cast<double*>(ws + plan.off_coef);
   a.mrow = reinterpret_cast<double*>(ws + plan.off_mrow);
   a.rowchunk = reinterpret_cast<double*>(ws + plan.off_rowchunk);
+  a.ssum = reinterpret_cast<double*>(ws + plan.off_ssum);
+  a.dsum = reinterpret_cast<double*>(ws + plan.off_dsum);
+  a.dpart = reinterpret_cast<float*>(ws + plan.off_dpart);
   a.spart = reinterpret_cast<double*>(ws + plan.off_spart);
   a.ppart = reinterpret_cast<double*>(ws + plan.off_ppart);
   a.rowpart = reinterpret_cast<float*>(ws + plan.off_rowpart);
@@ -441,6 +511,7 @@ adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int3
   a.has_beta1 = hp->has_beta1 ? 1 : 0;
   a.psq_valid = (hp->scale_parameter && hp->param_sq_sum_valid) ? 1 : 0;
   a.want_psq_out = any_psq ? 1 : 0;
+  a.stall_copies = g_stall_copies.load();
 
   // One launch helper: optional profiling events around the launch.
   auto run = [&](KernelId k, int cls, auto&& launch) -> adaf_status {
@@ -465,11 +536,13 @@ adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int3
     for (int c = 0; c < meo::kNumClasses; ++c) {
       if (factored_only && c == meo::kClsUnfactored) continue;
       const int32_t m = static_cast<int32_t>(plan.cls_idx[c].size());
-      const int32_t* pf_dev = reinterpret_cast<const int32_t*>(ws + plan.off_cls_pf[c]);
+      const int q = stream_slot(k);
+      const int32_t* pf_dev = reinterpret_cast<const int32_t*>(ws + plan.off_cls_pf[q][c]);
       const int32_t* idx_dev = reinterpret_cast<const int32_t*>(ws + plan.off_cls_idx[c]);
       for (int32_t g0 = 0; g0 < m; g0 += meo::kMaxGroup) {
         const int32_t g1 = g0 + meo::kMaxGroup < m ? g0 + meo::kMaxGroup : m;
-        const int64_t units = plan.cls_pf[c][g1] - plan.cls_pf[c][g0];
+        const int64_t units = plan.cls_pf[q][c][g1] - plan.cls_pf[q][c][g0];
+        if (units == 0) continue;
         const int grid = static_cast<int>(units < grid_limit[k][c] ? units : grid_limit[k][c]);
         const meo::Range r{pf_dev, idx_dev, g0, g1};
         const meo::TensorClass tc = static_cast<meo::TensorClass>(c);
@@ -549,6 +622,8 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
 
 const char* adafactor_last_error(void) { return g_last_error.c_str(); }
 
+void adafactor_debug_stall_copies(int32_t on) { g_stall_copies.store(on != 0 ? 1 : 0); }
+
 adaf_status adafactor_device_status(const void* workspace, void* stream, int32_t* status) {
   if (workspace == nullptr || status == nullptr || !aligned(workspace, 256))
     return fail(ADAF_ERR_INVALID_ARGUMENT, "workspace or status is NULL, or workspace misaligned");
@@ -615,6 +690,6 @@ adaf_status adafactor_profile_read(double* ms, int64_t* launches, int32_t nk) {
 
 int32_t adafactor_num_kernels(void) { return kNumSlots; }
 
-const char* adafactor_kernel_name(int32_t k) { return (k >= 0 && k < kNumSlots) ? kSlotNames[k] : ""; }
+const char* adafactor_kernel_name(int32_t k) { return slot_name(k); }
 
 }  // extern "C"

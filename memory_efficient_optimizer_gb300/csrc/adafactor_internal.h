@@ -29,10 +29,22 @@ constexpr int kColChunk = 256;
 constexpr int kMaxGroup = 4096;
 
 enum TensorKind : int32_t {
-  kFactoredVec = 0,   // ndim >= 2, W % 8 == 0, 16-byte aligned pointers
+  kFactoredVec = 0,   // ndim >= 2, W % 8 == 0, 16-byte aligned pointers, W > kMaxRowsW
   kFactoredScalar = 1,// ndim >= 2, anything else
   kUnfactored = 2,    // ndim < 2
+  kFactoredRows = 3,  // as kFactoredVec with kMinRowsW <= W <= kMaxRowsW: fused pass 1 over row panels
 };
+
+// Fused pass 1 (kFactoredRows, kMinRowsW <= W <= kMaxRowsW): one CTA per SM
+// with kPanelConsumers consumer warps and one producer warp streams panels of
+// full rows, in ring stages of whole rows (one contiguous bulk copy each).
+// Consumer warp w owns the 256-column segment w of every row and keeps its
+// column sums in registers; a row's total is known after one barrier per
+// stage.
+constexpr int kPanelConsumers = 16;
+constexpr int kPanelThreads = (kPanelConsumers + 1) * 32;
+constexpr int kMinRowsW = 2048;                     // narrower rows keep the tiled two-pass path
+constexpr int kMaxRowsW = kPanelConsumers * 256;    // 4096: one segment per consumer warp
 
 enum GradType : int32_t { kGradF32 = 0, kGradBF16 = 1 };
 
@@ -52,9 +64,16 @@ struct DevTensor {
   int32_t gdt;    // GradType
   int32_t rb;     // row blocks per slice   (ceil(H / kTileRows)); unfactored: 1
   int32_t cb;     // column blocks          (ceil(W / kTileCols)); unfactored: tiles
-  int32_t nrc;    // row chunks per slice   (ceil(H / kRowChunk))
+  int32_t nrc;    // row-sum chunks per slice: ceil(H / kRowChunk), or panels (kFactoredRows)
   int32_t ncc;    // column chunks per slice(ceil(W / kColChunk))
-  int32_t pad0;
+  int32_t prb;    // row blocks of the column partials: rb, or panels per slice (kFactoredRows)
+  int32_t pr;     // rows per panel (kFactoredRows)
+  int32_t seg;    // 256-column segments per row (kFactoredRows)
+  int32_t lanes;  // unused (0)
+  int64_t ntiles;     // apply tiles
+  int64_t p1_0, p1_n; // pass-1 units: global base (Ppart slot) and count
+  int64_t dpart;      // float offset of the weighted column partials [B][prb][W] (kFactoredRows)
+  int64_t dsum;       // double offset of per-chunk sum_j D_j / col_j [B][ncc] (kFactoredRows)
   int64_t tile0;      // global index of the tensor's first tile (Spart/Ppart slot)
   int64_t rowpart;    // float offset of rowpart [cb][B*H]
   int64_t colpart;    // float offset of colpart [B][rb][W]
@@ -72,7 +91,9 @@ enum TensorClass : int32_t {
   kClsScalarBF16 = 2,  // factored, element-wise path, bf16 grads
   kClsScalarF32 = 3,   // factored, element-wise path, fp32 grads
   kClsUnfactored = 4,  // ndim < 2 (any grad dtype)
-  kNumClasses = 5
+  kClsRowsBF16 = 5,    // fused pass 1, bf16 grads
+  kClsRowsF32 = 6,     // fused pass 1, fp32 grads
+  kNumClasses = 7
 };
 
 // Per-call scalars and workspace regions, passed by value to every kernel.
@@ -85,9 +106,12 @@ struct StepArgs {
   double* mrow;              // mean(row) per slice, via DevTensor::mslot
   double* rowchunk;          // row-chunk sums of the updated row vector
   double* spart;             // [tiles] partial sum(u^2)
-  double* ppart;             // [tiles] partial sum(p^2)
+  double* ppart;             // [max(tiles, pass-1 units)] partial sum(p^2)
+  double* ssum;              // [n] sum(u^2) of fused tensors
+  double* dsum;              // per-chunk sum_j D_j / col_j of fused tensors
   float* rowpart;
   float* colpart;
+  float* dpart;              // fused: column partials of g^2 / row_i
   double beta2;
   double rho;
   double eps1, eps2, clip, beta1, wd;
@@ -96,6 +120,7 @@ struct StepArgs {
   int32_t psq_valid;         // use DevTensor::psq instead of re-reading p
   int32_t want_psq_out;      // apply writes ppart for the carry
   int32_t* status;           // device status word (bit 0: a bounded wait gave up)
+  int32_t stall_copies;      // testing hook: bulk-copy producers issue nothing
 };
 
 // Device status bits (the word is reset by every step call).

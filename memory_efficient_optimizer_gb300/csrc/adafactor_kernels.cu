@@ -108,6 +108,19 @@ __device__ __forceinline__ void widen(const Raw<__nv_bfloat16, 1>& r, float (&x)
 }
 __device__ __forceinline__ void widen(const Raw<float, 1>& r, float (&x)[1]) { x[0] = r.f; }
 
+// The same 8 values as 4 pairs, for the paired fp32 instructions (fma.rn.f32x2).
+__device__ __forceinline__ void widen2(const Raw<__nv_bfloat16, 8>& r, float2 (&x)[4]) {
+  const uint32_t w[4] = {r.u.x, r.u.y, r.u.z, r.u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) x[k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
+}
+__device__ __forceinline__ void widen2(const Raw<float, 8>& r, float2 (&x)[4]) {
+  x[0] = make_float2(r.a.x, r.a.y);
+  x[1] = make_float2(r.a.z, r.a.w);
+  x[2] = make_float2(r.b.x, r.b.y);
+  x[3] = make_float2(r.b.z, r.b.w);
+}
+
 __device__ __forceinline__ float load_g1(const void* g, int gdt, int64_t e) {
   if (gdt == kGradBF16) {
     const unsigned short h = __ldcs(static_cast<const unsigned short*>(g) + e);
@@ -125,10 +138,6 @@ template <> __device__ __forceinline__ void load_f<8>(float (&y)[8], const float
 }
 template <> __device__ __forceinline__ void load_f<1>(float (&y)[1], const float* p) { y[0] = __ldcs(p); }
 template <int VEC> __device__ __forceinline__ void store_f(float* p, const float (&y)[VEC]);
-template <> __device__ __forceinline__ void store_f<8>(float* p, const float (&y)[8]) {
-  __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
-  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(y[4], y[5], y[6], y[7]));
-}
 template <> __device__ __forceinline__ void store_f<1>(float* p, const float (&y)[1]) { __stcs(p, y[0]); }
 
 // Position of tile `local` of a factored tensor: column block fastest, so
@@ -266,7 +275,7 @@ __device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArg
   }
   if (PSQ) {
     const double tot = block_sum(static_cast<double>(psq), red);
-    if (threadIdx.x == 0) a.ppart[d.tile0 + local] = tot;
+    if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = tot;
   } else {
     __syncthreads();  // colbuf is reused by the next tile
   }
@@ -297,7 +306,7 @@ __device__ __forceinline__ void pass1_unfactored(const DevTensor& d, const StepA
   if (PSQ) P = block_sum(static_cast<double>(ps), red);
   if (threadIdx.x == 0) {
     a.spart[d.tile0 + local] = S;
-    if (PSQ) a.ppart[d.tile0 + local] = P;
+    if (PSQ) a.ppart[d.p1_0 + local] = P;
   }
 }
 
@@ -306,13 +315,13 @@ constexpr size_t kColbufBytes = sizeof(float) * kWarps * kTileCols;
 constexpr size_t kRedBytes = sizeof(double) * 16;
 constexpr size_t kPrefixBytes = (sizeof(int32_t) * (kMaxGroup + 1) + 15) / 16 * 16;
 constexpr size_t kColfBytes = sizeof(float) * kTileCols;
-constexpr size_t kPartBytes = sizeof(float) * kWarps * kColChunk;
+constexpr size_t kPartBytes = sizeof(float) * 2 * kWarps * kColChunk;
 constexpr size_t kRowfBytes = sizeof(float) * kTileRows;
 
 // Copies the launch's member prefix into shared memory; returns the member count.
 __device__ __forceinline__ int load_prefix(int32_t* pf, const Range& r) {
   const int ng = r.m_end - r.m_begin;
-  for (int k = threadIdx.x; k <= ng; k += kThreads) pf[k] = r.pf[r.m_begin + k];
+  for (int k = threadIdx.x; k <= ng; k += blockDim.x) pf[k] = r.pf[r.m_begin + k];
   __syncthreads();
   return ng;
 }
@@ -378,44 +387,74 @@ __device__ __forceinline__ void stats_row_item(const DevTensor& d, const StepArg
 // l + 32m, m < 8, so every warp load is one coalesced 128-byte line), with
 // compensated (Kahan) fp32 sums; the 8 warp sums are then added in warp order
 // in double.  Fixed order throughout, so the result is deterministic.
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = x - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+}
+
+// Column item: kColChunk (256) columns of one slice.  Warp w adds the row
+// blocks r = w, w + 8, ... of the column partials (lane l owns columns
+// l + 32m, m < 8, so every warp load is one coalesced 128-byte line), with
+// compensated (Kahan) fp32 sums; the 8 warp sums are then added in warp order
+// in double.  Fixed order throughout, so the result is deterministic.  For
+// fused tensors the weighted partials D_j are reduced the same way and the
+// chunk's sum_j D_j / col_j goes to dsum.
 __device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q,
-                                               float* part) {
+                                               float* part, double* red) {
   constexpr int kPer = kColChunk / 32;
+  const bool fused = d.kind == kFactoredRows;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t W = d.W;
   const int64_t c0 = q * kColChunk;
-  const float* cp = a.colpart + d.colpart + b * d.rb * W;
-  float s[kPer], comp[kPer];
+  const float* cp = a.colpart + d.colpart + b * d.prb * W;
+  const float* dp = a.dpart + d.dpart + b * d.prb * W;
+  float s[kPer], comp[kPer], ds[kPer], dcomp[kPer];
 #pragma unroll
-  for (int m = 0; m < kPer; ++m) s[m] = comp[m] = 0.f;
-  for (int r = warp; r < d.rb; r += kWarps) {
-    const float* rowp = cp + static_cast<int64_t>(r) * W;
-    float x[kPer];
+  for (int m = 0; m < kPer; ++m) s[m] = comp[m] = ds[m] = dcomp[m] = 0.f;
+  for (int r = warp; r < d.prb; r += kWarps) {
+    const int64_t roff = static_cast<int64_t>(r) * W;
+    float x[kPer], y[kPer];
 #pragma unroll
     for (int m = 0; m < kPer; ++m) {
       const int64_t j = c0 + lane + 32 * m;
-      x[m] = (j < W) ? rowp[j] : 0.f;
+      x[m] = (j < W) ? cp[roff + j] : 0.f;
+      y[m] = (fused && j < W) ? dp[roff + j] : 0.f;
     }
 #pragma unroll
     for (int m = 0; m < kPer; ++m) {
-      const float y = x[m] - comp[m];
-      const float t = s[m] + y;
-      comp[m] = (t - s[m]) - y;
-      s[m] = t;
+      kahan_add(s[m], comp[m], x[m]);
+      if (fused) kahan_add(ds[m], dcomp[m], y[m]);
     }
   }
   __syncthreads();  // part is free (previous item done reading it)
 #pragma unroll
-  for (int m = 0; m < kPer; ++m) part[warp * kColChunk + lane + 32 * m] = s[m];
+  for (int m = 0; m < kPer; ++m) {
+    part[warp * kColChunk + lane + 32 * m] = s[m];
+    if (fused) part[(kWarps + warp) * kColChunk + lane + 32 * m] = ds[m];
+  }
   __syncthreads();
   const int64_t j = c0 + threadIdx.x;
+  double term = 0.0;
   if (threadIdx.x < kColChunk && j < W) {
     double tot = 0.0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) tot += static_cast<double>(part[w * kColChunk + threadIdx.x]);
     const double mean = tot / static_cast<double>(d.H) + a.eps1;
     float* col = d.col + b * W + j;
-    *col = static_cast<float>(a.beta2 * static_cast<double>(*col) + (1.0 - a.beta2) * mean);
+    const float cn = static_cast<float>(a.beta2 * static_cast<double>(*col) + (1.0 - a.beta2) * mean);
+    *col = cn;
+    if (fused) {
+      double dt = 0.0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) dt += static_cast<double>(part[(kWarps + w) * kColChunk + threadIdx.x]);
+      term = dt / static_cast<double>(cn);
+    }
+  }
+  if (fused) {
+    const double tot = block_sum(term, red);
+    if (threadIdx.x == 0) a.dsum[d.dsum + b * d.ncc + q] = tot;
   }
 }
 
@@ -430,14 +469,18 @@ __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ Step
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
     const int64_t local = u - pf[m];
+    if (d.kind == kFactoredRows) {  // rows were updated by the fused pass 1
+      stats_col_item(d, a, local / d.ncc, local % d.ncc, part, red);
+      continue;
+    }
     const int64_t per_slice = d.nrc + d.ncc;
     const int64_t b = local / per_slice, k = local % per_slice;
     if (k < d.nrc) stats_row_item(d, a, b, k, red);
-    else stats_col_item(d, a, b, k - d.nrc, part);
+    else stats_col_item(d, a, b, k - d.nrc, part, red);
   }
 }
 
-// ---- scalars: alpha and mean(row), one CTA per tensor ---------------------
+// ---- scalars: alpha, mean(row), fused sum(u^2); one CTA per tensor ----------
 __global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ StepArgs a) {
   __shared__ double red[16];
   const int t = blockIdx.x;
@@ -448,9 +491,8 @@ __global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ St
     if (a.psq_valid) {
       psq = *d.psq;
     } else {
-      const int64_t nt = a.pf_tiles[t + 1] - a.pf_tiles[t];
       double acc = 0.0;
-      for (int64_t k = threadIdx.x; k < nt; k += kThreads) acc += a.ppart[d.tile0 + k];
+      for (int64_t k = threadIdx.x; k < d.p1_n; k += kThreads) acc += a.ppart[d.p1_0 + k];
       psq = block_sum(acc, red);
     }
     const double r = sqrt(psq / static_cast<double>(d.n));
@@ -458,12 +500,32 @@ __global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ St
   }
   if (threadIdx.x == 0) a.alpha[t] = alpha;
   if (d.kind != kUnfactored) {
+    // mean(row) per slice; for fused tensors also sum(u^2) =
+    // sum_b mean(row_b) * sum_j D_bj / col_bj (slices in order within a warp,
+    // then warps in order).
+    const bool fused = d.kind == kFactoredRows;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    double su = 0.0;
     for (int64_t b = warp; b < d.B; b += kWarps) {
       double s = 0.0;
       for (int64_t q = lane; q < d.nrc; q += 32) s += a.rowchunk[d.rowchunk + b * d.nrc + q];
       s = warp_sum(s);
-      if (lane == 0) a.mrow[d.mslot + b] = s / static_cast<double>(d.H);
+      const double mb = s / static_cast<double>(d.H);
+      if (lane == 0) a.mrow[d.mslot + b] = mb;
+      if (fused) {
+        double ds = 0.0;
+        for (int64_t q = lane; q < d.ncc; q += 32) ds += a.dsum[d.dsum + b * d.ncc + q];
+        su += mb * warp_sum(ds);
+      }
+    }
+    if (fused) {
+      if (lane == 0) red[warp] = su;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int w = 0; w < kWarps; ++w) tot += red[w];
+        a.ssum[t] = tot;
+      }
     }
   }
 }
@@ -564,10 +626,14 @@ __global__ void __launch_bounds__(kThreads) k_clip(const __grid_constant__ StepA
   __shared__ double red[16];
   const int t = blockIdx.x;
   const DevTensor d = a.tensors[t];
-  const int64_t nt = a.pf_tiles[t + 1] - a.pf_tiles[t];
-  double acc = 0.0;
-  for (int64_t k = threadIdx.x; k < nt; k += kThreads) acc += a.spart[d.tile0 + k];
-  const double S = block_sum(acc, red);
+  double S;
+  if (d.kind == kFactoredRows) {
+    S = a.ssum[t];
+  } else {
+    double acc = 0.0;
+    for (int64_t k = threadIdx.x; k < d.ntiles; k += kThreads) acc += a.spart[d.tile0 + k];
+    S = block_sum(acc, red);
+  }
   if (threadIdx.x == 0) {
     const double rms_u = sqrt(S / static_cast<double>(d.n));
     double div = rms_u / a.clip;
@@ -804,6 +870,7 @@ __device__ __forceinline__ int tma_setup(int32_t* pf, const Range& r, uint64_t* 
 template <typename GT, class RG>
 __device__ __forceinline__ void tma_produce(const StepArgs& a, const Range& r, const int32_t* pf, int ng,
                                             unsigned char* ring, uint64_t* full, uint64_t* empty) {
+  if (a.stall_copies) return;  // testing hook: the consumers' waits run out
   const int64_t u1 = pf[ng];
   uint32_t it = 0;
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
@@ -883,6 +950,236 @@ __device__ __forceinline__ double consumer_sum(float v, double* red) {
     for (int k = 0; k < kTmaConsumers; ++k) s += red[k];
   }
   return s;
+}
+
+// ---- fused pass 1 over row panels (kFactoredRows) --------------------------
+// One CTA per SM: 16 consumer warps and a producer warp.  A work unit is a
+// panel of d.pr full rows of one slice (2048 <= W <= 4096).  The producer
+// copies it in stages of kPanelRowsPerStage whole rows, contiguous in memory,
+// with one bulk copy per stage into a ring.  Consumer warp w owns the
+// 256-column segment w of every row (lane l: columns 256 w + 8 l + [0, 8)).
+// Per stage, every warp:
+//   A. squares its segment of each staged row (the squares stay in registers),
+//      adds them into its column sums C_j and writes its share of each row
+//      total to shared memory (one reduce-scatter over the lanes for all the
+//      stage's rows);
+//   -- barrier among the consumer warps --
+//   B. lane r adds the 16 shares of row r in warp order, forms the updated row
+//      statistic row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W + eps1) and
+//      its reciprocal; every lane then adds g_rj^2 / row_r into its second
+//      column sums D_j, and the stage is released.
+// With the column statistic of the step, sum(u^2) = mean(row) * sum_j D_j/col_j,
+// so no second pass over g is needed.  Per panel the warps write C_j and D_j
+// (column partials), warp 0 the updated rows and sum_r row_r (for mean(row)).
+// The arithmetic uses the paired fp32 instructions (fma.rn.f32x2).  Waits are
+// bounded as in the apply ring.
+constexpr int kPanelRowsPerStage = 4;
+constexpr size_t kPanelRingBytes = 192 * 1024;
+
+template <typename GT>
+struct PanelRing {
+  static constexpr int kStage = kPanelRowsPerStage * kMaxRowsW * static_cast<int>(sizeof(GT));
+  static constexpr int kStages = static_cast<int>(kPanelRingBytes / kStage);
+};
+
+template <typename GT>
+constexpr size_t panel_smem() {
+  return kPanelRingBytes + sizeof(float) * 2 * kPanelConsumers * kPanelRowsPerStage +
+         sizeof(double) * 2 * kPanelConsumers + sizeof(uint64_t) * 2 * PanelRing<GT>::kStages + kPrefixBytes;
+}
+
+__device__ __forceinline__ void panel_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kPanelConsumers * 32) : "memory");
+}
+
+// Reduce-scatter of 4 per-lane values over the warp: afterwards lane l holds
+// the warp total of value ((l >> 4) & 1) * 2 + ((l >> 3) & 1), complete in
+// lanes 0, 8, 16, 24.  Fixed exchange pattern, so the sums are deterministic.
+__device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) {
+  const bool h16 = lane & 16, h8 = lane & 8;
+  float k0 = h16 ? v[2] : v[0], k1 = h16 ? v[3] : v[1];
+  const float s0 = h16 ? v[0] : v[2], s1 = h16 ? v[1] : v[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float k = h8 ? k1 : k0;
+  const float s = h8 ? k0 : k1;
+  k += __shfl_xor_sync(0xffffffffu, s, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
+template <typename GT, bool PSQ>
+__global__ void __launch_bounds__(kPanelThreads, 1) k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
+  using RG = PanelRing<GT>;
+  constexpr int RS = kPanelRowsPerStage;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* ring = smem;
+  float* part = reinterpret_cast<float*>(smem + kPanelRingBytes);  // [2][16 warps][RS rows]
+  double* red = reinterpret_cast<double*>(part + 2 * kPanelConsumers * RS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kPanelConsumers);
+  uint64_t* empty = full + RG::kStages;
+  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
+  __shared__ int stop;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = r.m_end - r.m_begin;
+  for (int k = threadIdx.x; k <= ng; k += kPanelThreads) pf[k] = r.pf[r.m_begin + k];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RG::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kPanelConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    stop = 0;
+  }
+  __syncthreads();
+  const int64_t u1 = pf[ng];
+
+  if (warp == kPanelConsumers) {
+    // ---- producer: one bulk copy per stage --------------------------------
+    if (lane != 0 || a.stall_copies) return;
+    uint32_t it = 0;
+    for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+      const int m = find_owner(pf, ng, u);
+      const DevTensor d = a.tensors[member_tensor(r, m)];
+      const int64_t local = u - pf[m];
+      const int64_t b = local / d.prb, panel = local % d.prb;
+      const int64_t r0 = panel * d.pr, r1 = min(d.H, r0 + d.pr);
+      for (int64_t rs = r0; rs < r1; rs += RS, ++it) {
+        const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+        if (!mbar_wait(&empty[slot], ph ^ 1u)) {
+          atomicOr(a.status, kStatusWaitTimeout);
+          return;
+        }
+        const int64_t nrows = min(static_cast<int64_t>(RS), r1 - rs);
+        const uint32_t bytes = static_cast<uint32_t>(nrows * d.W * static_cast<int64_t>(sizeof(GT)));
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        bulk_g2s(ring + static_cast<size_t>(slot) * RG::kStage, static_cast<const GT*>(d.g) + (b * d.H + rs) * d.W,
+                 bytes, &full[slot]);
+      }
+    }
+    return;
+  }
+
+  // ---- consumers -------------------------------------------------------------
+  const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
+  const float eps1 = static_cast<float>(a.eps1);
+  uint32_t it = 0;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    const int64_t local = u - pf[m];
+    const int64_t b = local / d.prb, panel = local % d.prb;
+    const int64_t H = d.H, W = d.W;
+    const int64_t r0 = panel * d.pr, r1 = min(H, r0 + d.pr);
+    const int64_t j = static_cast<int64_t>(warp) * 256 + lane * 8;  // this lane's 8 columns
+    const bool has = j < W;
+    float* rowst = d.row + b * H;
+    const float* pb = d.p + b * H * W;
+    const float invw = 1.0f / static_cast<float>(W);
+    panel_sync();  // stop is settled; part / red of the previous panel are read
+    if (stop) break;
+    float2 cacc[4], dacc[4];  // column sums of adjacent column pairs
+#pragma unroll
+    for (int v = 0; v < 4; ++v) cacc[v] = dacc[v] = make_float2(0.f, 0.f);
+    float psq = 0.f, rsum = 0.f;
+    // After a timed-out wait the warp is "dead" for the rest of the panel: it
+    // skips the stages but still meets every consumer barrier, so the warps
+    // never disagree on which barrier they are at.
+    bool dead = false;
+    for (int64_t rs = r0; rs < r1; rs += RS, ++it) {
+      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+      const int nrows = static_cast<int>(min(static_cast<int64_t>(RS), r1 - rs));
+      // previous row statistic of this lane's row, fetched while the stage lands
+      const float row_old = (!dead && lane < nrows) ? rowst[rs + lane] : 0.f;
+      if (!dead && !tma_acquire(&full[slot], ph, a, &stop)) dead = true;
+      const GT* st = reinterpret_cast<const GT*>(ring + static_cast<size_t>(slot) * RG::kStage);
+      float* pbuf = part + (it & 1) * kPanelConsumers * RS;
+      float2 q[RS][4];  // squares of this lane's columns, per staged row
+      if (!dead) {
+        // A: squares, column sums, row shares
+        float rpart[RS];
+#pragma unroll
+        for (int rr = 0; rr < RS; ++rr) {
+          float2 s2 = make_float2(0.f, 0.f);
+          if (has && rr < nrows) {
+            float2 x[4];
+            widen2(*reinterpret_cast<const Raw<GT, 8>*>(st + rr * W + j), x);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              q[rr][v] = __fmul2_rn(x[v], x[v]);
+              cacc[v] = __fadd2_rn(cacc[v], q[rr][v]);
+              s2 = __fadd2_rn(s2, q[rr][v]);
+            }
+            if (PSQ) {
+              float y[8];
+              load_f<8>(y, pb + (rs + rr) * W + j);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) q[rr][v] = make_float2(0.f, 0.f);
+          }
+          rpart[rr] = s2.x + s2.y;
+        }
+        const float tot = reduce_scatter4(rpart, lane);
+        if ((lane & 7) == 0) pbuf[warp * RS + (((lane >> 4) & 1) << 1) + ((lane >> 3) & 1)] = tot;
+      }
+      panel_sync();
+      if (stop) dead = true;  // some warp gave up: the stage's row shares are incomplete
+      if (dead) continue;
+      // B: row totals (lane rr owns row rr), updated rows, weighted column sums
+      float w_lane = 0.f;
+      if (lane < nrows) {
+        float R = 0.f;
+        for (int w2 = 0; w2 < kPanelConsumers; ++w2) R += pbuf[w2 * RS + lane];
+        const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
+        w_lane = 1.0f / rn;
+        if (warp == 0) {
+          rowst[rs + lane] = rn;
+          rsum += rn;
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < RS; ++rr) {
+        const float w_r = __shfl_sync(0xffffffffu, w_lane, rr);
+        const float2 w2 = make_float2(w_r, w_r);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dacc[v] = __ffma2_rn(q[rr][v], w2, dacc[v]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (!stop && has) {
+      float* cp = a.colpart + d.colpart + (b * d.prb + panel) * W + j;
+      float* dp = a.dpart + d.dpart + (b * d.prb + panel) * W + j;
+      *reinterpret_cast<float4*>(cp) = make_float4(cacc[0].x, cacc[0].y, cacc[1].x, cacc[1].y);
+      *reinterpret_cast<float4*>(cp + 4) = make_float4(cacc[2].x, cacc[2].y, cacc[3].x, cacc[3].y);
+      *reinterpret_cast<float4*>(dp) = make_float4(dacc[0].x, dacc[0].y, dacc[1].x, dacc[1].y);
+      *reinterpret_cast<float4*>(dp + 4) = make_float4(dacc[2].x, dacc[2].y, dacc[3].x, dacc[3].y);
+    }
+    // sum_r row_r (warp 0, lanes in order through the xor tree), sum(p^2)
+    if (warp == 0) {
+      const float t = warp_sum(rsum);
+      if (lane == 0) red[0] = static_cast<double>(t);
+    }
+    if (PSQ) {
+      const float t = warp_sum(psq);
+      if (lane == 0) red[kPanelConsumers + warp] = static_cast<double>(t);
+    }
+    panel_sync();
+    if (threadIdx.x == 0 && !stop) {
+      a.rowchunk[d.rowchunk + b * d.nrc + panel] = red[0];
+      if (PSQ) {
+        double p2 = 0.0;
+        for (int w2 = 0; w2 < kPanelConsumers; ++w2) p2 += red[kPanelConsumers + w2];
+        a.ppart[d.p1_0 + local] = p2;
+      }
+    }
+  }
+  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
 }
 
 // ---- apply (vector path) ---------------------------------------------------
@@ -998,9 +1295,8 @@ __global__ void __launch_bounds__(kThreads) k_psq(const __grid_constant__ StepAr
   const int t = blockIdx.x;
   const DevTensor d = a.tensors[t];
   if (d.psq == nullptr) return;
-  const int64_t nt = a.pf_tiles[t + 1] - a.pf_tiles[t];
   double acc = 0.0;
-  for (int64_t k = threadIdx.x; k < nt; k += kThreads) acc += a.ppart[d.tile0 + k];
+  for (int64_t k = threadIdx.x; k < d.ntiles; k += kThreads) acc += a.ppart[d.tile0 + k];
   const double S = block_sum(acc, red);
   if (threadIdx.x == 0) *d.psq = S;
 }
@@ -1065,6 +1361,20 @@ Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
   }
 }
 
+// Fused pass 1 and the bulk-copy apply for one gradient type (row-panel classes).
+template <typename GT>
+Inst pick_rows(KernelId k, bool psq_in, bool b1, bool psq_out) {
+  Inst x;
+  if (k == kKPass1) {
+    x.threads = kPanelThreads;
+    x.fn = psq_in ? k_pass1_panel<GT, true> : k_pass1_panel<GT, false>;
+    x.smem = panel_smem<GT>();
+  } else if (k == kKApply) {
+    x = pick_f<GT, 8>(k, psq_in, b1, psq_out);
+  }
+  return x;
+}
+
 Inst pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
   Inst x;
   switch (c) {
@@ -1072,6 +1382,8 @@ Inst pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
     case kClsVecF32: return pick_f<float, 8>(k, psq_in, b1, psq_out);
     case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, b1, psq_out);
     case kClsScalarF32: return pick_f<float, 1>(k, psq_in, b1, psq_out);
+    case kClsRowsBF16: return pick_rows<__nv_bfloat16>(k, psq_in, b1, psq_out);
+    case kClsRowsF32: return pick_rows<float>(k, psq_in, b1, psq_out);
     case kClsUnfactored:
       x.smem = kRedBytes + kPrefixBytes;
       if (k == kKPass1) x.fn = psq_in ? k_pass1_u<true> : k_pass1_u<false>;

@@ -152,10 +152,11 @@ def test_valid_call_without_gpu_reports_a_cuda_error(lib):
 
 def test_kernel_names(lib):
     names = [B.adafactor_kernel_name(k) for k in range(B.adafactor_num_kernels())]
-    assert len(names) == 18 and len(set(names)) == 18
+    assert len(names) == 25 and len(set(names)) == 25
     for kind in ("k_pass1", "k_pass2", "k_apply"):
-        assert f"{kind}[vec_bf16]" in names and f"{kind}[elem_f32]" in names
-    assert {"k_stats", "k_scalars", "k_clip", "k_psq", "k_pass1[1d]", "k_apply[1d]"} <= set(names)
+        for cls in ("vec_bf16", "vec_f32", "elem_bf16", "elem_f32", "1d", "rows_bf16", "rows_f32"):
+            assert f"{kind}[{cls}]" in names
+    assert {"k_stats", "k_scalars", "k_clip", "k_psq"} <= set(names)
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
