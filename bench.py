@@ -80,7 +80,7 @@ def tensor_class(shape, grad_bytes):
     if len(shape) < 2:
         return "1d"
     w = int(shape[-1])
-    kind = "elem_" if w % 8 else ("rows_" if 2048 <= w <= 4096 else "vec_")
+    kind = "elem_" if w % 8 else ("rows_" if 2048 <= w <= 4096 and grad_bytes == 2 else "vec_")
     return kind + ("bf16" if grad_bytes == 2 else "f32")
 
 

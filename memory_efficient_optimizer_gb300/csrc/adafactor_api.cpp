@@ -88,10 +88,8 @@ struct Plan {
 // Index of a streaming kind in Plan::cls_pf.
 int stream_slot(KernelId k) { return k == meo::kKPass1 ? 0 : (k == meo::kKPass2 ? 1 : 2); }
 
-// Rows per panel of the fused pass: about 2^20 values (256 rows of 4096).
-int32_t panel_rows(int64_t W) {
-  return static_cast<int32_t>(ceil_div((int64_t(1) << 20) / W, 4) * 4);
-}
+// Rows per work unit of the fused pass.
+int32_t panel_rows(int64_t) { return meo::kRowsChunk; }
 
 // Checks the tensor list and builds the plan.  With full == false (size
 // query) only the shapes and dtypes are read; states and hp are not touched.
@@ -176,7 +174,9 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       // Path: vector (16-byte aligned rows) or element-wise; a vector tensor
       // with W <= kMaxRowsW takes the fused row-panel pass 1.
       const bool vec_shape = (W % 8 == 0);
-      const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxRowsW;
+      // (bf16 gradients only: with fp32 ones the tiled passes are faster.)
+      const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxRowsW &&
+                              t.grad_dtype == ADAF_BFLOAT16;
       bool vec = vec_shape;
       if (full) {
         vec = vec_shape && aligned(t.param, 16) && aligned(t.grad, 16) &&

@@ -32,19 +32,15 @@ enum TensorKind : int32_t {
   kFactoredVec = 0,   // ndim >= 2, W % 8 == 0, 16-byte aligned pointers, W > kMaxRowsW
   kFactoredScalar = 1,// ndim >= 2, anything else
   kUnfactored = 2,    // ndim < 2
-  kFactoredRows = 3,  // as kFactoredVec with kMinRowsW <= W <= kMaxRowsW: fused pass 1 over row panels
+  kFactoredRows = 3,  // as kFactoredVec with kMinRowsW <= W <= kMaxRowsW, bf16 grads: fused pass 1
 };
 
-// Fused pass 1 (kFactoredRows, kMinRowsW <= W <= kMaxRowsW): one CTA per SM
-// with kPanelConsumers consumer warps and one producer warp streams panels of
-// full rows, in ring stages of whole rows (one contiguous bulk copy each).
-// Consumer warp w owns the 256-column segment w of every row and keeps its
-// column sums in registers; a row's total is known after one barrier per
-// stage.
-constexpr int kPanelConsumers = 16;
-constexpr int kPanelThreads = (kPanelConsumers + 1) * 32;
-constexpr int kMinRowsW = 2048;                     // narrower rows keep the tiled two-pass path
-constexpr int kMaxRowsW = kPanelConsumers * 256;    // 4096: one segment per consumer warp
+// Fused pass 1 (kFactoredRows, kMinRowsW <= W <= kMaxRowsW): a CTA of
+// kWarps warps takes chunks of d.pr full rows; warp w owns the 512-column
+// segment w of every row and keeps its column sums in registers.
+constexpr int kMinRowsW = 2048;          // narrower rows keep the tiled two-pass path
+constexpr int kMaxRowsW = kWarps * 512;  // 4096: one segment per warp
+constexpr int kRowsChunk = 256;          // rows per work unit
 
 enum GradType : int32_t { kGradF32 = 0, kGradBF16 = 1 };
 

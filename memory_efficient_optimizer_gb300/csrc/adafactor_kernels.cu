@@ -413,19 +413,28 @@ __device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArg
   float s[kPer], comp[kPer], ds[kPer], dcomp[kPer];
 #pragma unroll
   for (int m = 0; m < kPer; ++m) s[m] = comp[m] = ds[m] = dcomp[m] = 0.f;
-  for (int r = warp; r < d.prb; r += kWarps) {
-    const int64_t roff = static_cast<int64_t>(r) * W;
-    float x[kPer], y[kPer];
+  // Two row blocks per iteration: twice the loads in flight, same order.
+  for (int r = warp; r < d.prb; r += 2 * kWarps) {
+    const bool second = r + kWarps < d.prb;
+    float x[2][kPer], y[2][kPer];
 #pragma unroll
-    for (int m = 0; m < kPer; ++m) {
-      const int64_t j = c0 + lane + 32 * m;
-      x[m] = (j < W) ? cp[roff + j] : 0.f;
-      y[m] = (fused && j < W) ? dp[roff + j] : 0.f;
+    for (int h = 0; h < 2; ++h) {
+      const int64_t roff = static_cast<int64_t>(r + h * kWarps) * W;
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int64_t j = c0 + lane + 32 * m;
+        const bool ok = (h == 0 || second) && j < W;
+        x[h][m] = ok ? cp[roff + j] : 0.f;
+        y[h][m] = (fused && ok) ? dp[roff + j] : 0.f;
+      }
     }
 #pragma unroll
-    for (int m = 0; m < kPer; ++m) {
-      kahan_add(s[m], comp[m], x[m]);
-      if (fused) kahan_add(ds[m], dcomp[m], y[m]);
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        kahan_add(s[m], comp[m], x[h][m]);
+        if (fused) kahan_add(ds[m], dcomp[m], y[h][m]);
+      }
     }
   }
   __syncthreads();  // part is free (previous item done reading it)
@@ -952,46 +961,6 @@ __device__ __forceinline__ double consumer_sum(float v, double* red) {
   return s;
 }
 
-// ---- fused pass 1 over row panels (kFactoredRows) --------------------------
-// One CTA per SM: 16 consumer warps and a producer warp.  A work unit is a
-// panel of d.pr full rows of one slice (2048 <= W <= 4096).  The producer
-// copies it in stages of kPanelRowsPerStage whole rows, contiguous in memory,
-// with one bulk copy per stage into a ring.  Consumer warp w owns the
-// 256-column segment w of every row (lane l: columns 256 w + 8 l + [0, 8)).
-// Per stage, every warp:
-//   A. squares its segment of each staged row (the squares stay in registers),
-//      adds them into its column sums C_j and writes its share of each row
-//      total to shared memory (one reduce-scatter over the lanes for all the
-//      stage's rows);
-//   -- barrier among the consumer warps --
-//   B. lane r adds the 16 shares of row r in warp order, forms the updated row
-//      statistic row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W + eps1) and
-//      its reciprocal; every lane then adds g_rj^2 / row_r into its second
-//      column sums D_j, and the stage is released.
-// With the column statistic of the step, sum(u^2) = mean(row) * sum_j D_j/col_j,
-// so no second pass over g is needed.  Per panel the warps write C_j and D_j
-// (column partials), warp 0 the updated rows and sum_r row_r (for mean(row)).
-// The arithmetic uses the paired fp32 instructions (fma.rn.f32x2).  Waits are
-// bounded as in the apply ring.
-constexpr int kPanelRowsPerStage = 4;
-constexpr size_t kPanelRingBytes = 192 * 1024;
-
-template <typename GT>
-struct PanelRing {
-  static constexpr int kStage = kPanelRowsPerStage * kMaxRowsW * static_cast<int>(sizeof(GT));
-  static constexpr int kStages = static_cast<int>(kPanelRingBytes / kStage);
-};
-
-template <typename GT>
-constexpr size_t panel_smem() {
-  return kPanelRingBytes + sizeof(float) * 2 * kPanelConsumers * kPanelRowsPerStage +
-         sizeof(double) * 2 * kPanelConsumers + sizeof(uint64_t) * 2 * PanelRing<GT>::kStages + kPrefixBytes;
-}
-
-__device__ __forceinline__ void panel_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kPanelConsumers * 32) : "memory");
-}
-
 // Reduce-scatter of 4 per-lane values over the warp: afterwards lane l holds
 // the warp total of value ((l >> 4) & 1) * 2 + ((l >> 3) & 1), complete in
 // lanes 0, 8, 16, 24.  Fixed exchange pattern, so the sums are deterministic.
@@ -1010,176 +979,200 @@ __device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) 
   return k;
 }
 
+// ---- fused pass 1 over row chunks (kFactoredRows) --------------------------
+// A work unit is a chunk of d.pr full rows of one slice (2048 <= W <= 4096),
+// taken by one CTA of 8 warps in sub-panels of kSubRows rows.  Warp w owns
+// the 512-column segment w of every row (lane l: columns 512 w + 256 c + 8 l
+// + [0, 8), c = 0, 1) and keeps its column sums in registers.  Per sub-panel:
+//   A. the warps stream their segments of the sub-panel's rows (128 bytes of
+//      loads in flight per lane), add the squares into the column
+//      sums C_j and write their share of each row total to shared memory;
+//   -- barrier --
+//   thread r adds the 8 shares of row r in warp order and forms the updated
+//   row statistic row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W + eps1)
+//   and its reciprocal;
+//   -- barrier --
+//   B. the warps stream the same rows again and add g_rj^2 / row_r into the
+//      second column sums D_j.  A sub-panel is 128 KB (16 rows of 4096 bf16),
+//      read first with an L2 evict_last policy and then with evict_first, so
+//      the second read is served by L2 while the whole GPU has only ~40 MB of
+//      sub-panels live.
+// With the column statistic of the step, sum(u^2) = mean(row) * sum_j D_j/col_j,
+// so g is read from HBM once here instead of twice.  Per chunk the warps
+// write C_j and D_j (column partials), and sum_r row_r goes to the row-chunk
+// sums (for mean(row)).  No waits: plain loads and CTA barriers only.
+constexpr int kSubRows = 16;
+
+// L2 policies for the two reads of a sub-panel: keep it for the second read
+// (evict_last), drop it after (evict_first).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_hint(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void load_raw_hint(Raw<__nv_bfloat16, 8>& r, const __nv_bfloat16* p, uint64_t pol) {
+  r.u = ld_hint(p, pol);
+}
+__device__ __forceinline__ void load_raw_hint(Raw<float, 8>& r, const float* p, uint64_t pol) {
+  const uint4 a = ld_hint(p, pol), b = ld_hint(p + 4, pol);
+  r.a = make_float4(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z), __uint_as_float(a.w));
+  r.b = make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w));
+}
+
+// Rows loaded per step of the fused pass (3 CTAs per SM: 64 bytes of bf16
+// gradient, 128 of fp32, in flight per lane).
+template <typename GT> struct PanelGroup { static constexpr int kRows = 2; };
+
+template <typename GT, int RG>
+__device__ __forceinline__ void seg_load(Raw<GT, 8> (&raw)[RG][2], const GT* gb, int64_t W, int64_t i, int64_t i1,
+                                         int64_t j0, int lane, uint64_t pol) {
+#pragma unroll
+  for (int rr = 0; rr < RG; ++rr) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int64_t j = j0 + c * 256 + lane * 8;
+      if (i + rr < i1 && j < W) load_raw_hint(raw[rr][c], gb + (i + rr) * W + j, pol);
+    }
+  }
+}
+
 template <typename GT, bool PSQ>
-__global__ void __launch_bounds__(kPanelThreads, 1) k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
-  using RG = PanelRing<GT>;
-  constexpr int RS = kPanelRowsPerStage;
+__global__ void __launch_bounds__(kThreads, 3) k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
+  constexpr int RG = PanelGroup<GT>::kRows;
   extern __shared__ __align__(16) unsigned char smem[];
-  unsigned char* ring = smem;
-  float* part = reinterpret_cast<float*>(smem + kPanelRingBytes);  // [2][16 warps][RS rows]
-  double* red = reinterpret_cast<double*>(part + 2 * kPanelConsumers * RS);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kPanelConsumers);
-  uint64_t* empty = full + RG::kStages;
-  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
-  __shared__ int stop;
+  float* part = reinterpret_cast<float*>(smem);           // [kSubRows][kWarps]
+  float* wsm = part + kSubRows * kWarps;                   // [kSubRows] 1 / row_r
+  double* red = reinterpret_cast<double*>(wsm + kSubRows);  // 16
+  int32_t* pf = reinterpret_cast<int32_t*>(red + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ng = r.m_end - r.m_begin;
-  for (int k = threadIdx.x; k <= ng; k += kPanelThreads) pf[k] = r.pf[r.m_begin + k];
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < RG::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kPanelConsumers);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    stop = 0;
-  }
-  __syncthreads();
+  const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
-
-  if (warp == kPanelConsumers) {
-    // ---- producer: one bulk copy per stage --------------------------------
-    if (lane != 0 || a.stall_copies) return;
-    uint32_t it = 0;
-    for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
-      const int m = find_owner(pf, ng, u);
-      const DevTensor d = a.tensors[member_tensor(r, m)];
-      const int64_t local = u - pf[m];
-      const int64_t b = local / d.prb, panel = local % d.prb;
-      const int64_t r0 = panel * d.pr, r1 = min(d.H, r0 + d.pr);
-      for (int64_t rs = r0; rs < r1; rs += RS, ++it) {
-        const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
-        if (!mbar_wait(&empty[slot], ph ^ 1u)) {
-          atomicOr(a.status, kStatusWaitTimeout);
-          return;
-        }
-        const int64_t nrows = min(static_cast<int64_t>(RS), r1 - rs);
-        const uint32_t bytes = static_cast<uint32_t>(nrows * d.W * static_cast<int64_t>(sizeof(GT)));
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s(ring + static_cast<size_t>(slot) * RG::kStage, static_cast<const GT*>(d.g) + (b * d.H + rs) * d.W,
-                 bytes, &full[slot]);
-      }
-    }
-    return;
-  }
-
-  // ---- consumers -------------------------------------------------------------
   const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
   const float eps1 = static_cast<float>(a.eps1);
-  uint32_t it = 0;
+  const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
     const int64_t local = u - pf[m];
-    const int64_t b = local / d.prb, panel = local % d.prb;
+    const int64_t b = local / d.prb, chunk = local % d.prb;
     const int64_t H = d.H, W = d.W;
-    const int64_t r0 = panel * d.pr, r1 = min(H, r0 + d.pr);
-    const int64_t j = static_cast<int64_t>(warp) * 256 + lane * 8;  // this lane's 8 columns
-    const bool has = j < W;
-    float* rowst = d.row + b * H;
+    const int64_t c0 = chunk * d.pr, c1 = min(H, c0 + d.pr);
+    const int64_t j0 = static_cast<int64_t>(warp) * 512;
+    const GT* gb = static_cast<const GT*>(d.g) + b * H * W;
     const float* pb = d.p + b * H * W;
+    float* rowst = d.row + b * H;
     const float invw = 1.0f / static_cast<float>(W);
-    panel_sync();  // stop is settled; part / red of the previous panel are read
-    if (stop) break;
-    float2 cacc[4], dacc[4];  // column sums of adjacent column pairs
+    float2 cacc[2][4], dacc[2][4];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) cacc[v] = dacc[v] = make_float2(0.f, 0.f);
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) cacc[c][v] = dacc[c][v] = make_float2(0.f, 0.f);
+    }
     float psq = 0.f, rsum = 0.f;
-    // After a timed-out wait the warp is "dead" for the rest of the panel: it
-    // skips the stages but still meets every consumer barrier, so the warps
-    // never disagree on which barrier they are at.
-    bool dead = false;
-    for (int64_t rs = r0; rs < r1; rs += RS, ++it) {
-      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
-      const int nrows = static_cast<int>(min(static_cast<int64_t>(RS), r1 - rs));
-      // previous row statistic of this lane's row, fetched while the stage lands
-      const float row_old = (!dead && lane < nrows) ? rowst[rs + lane] : 0.f;
-      if (!dead && !tma_acquire(&full[slot], ph, a, &stop)) dead = true;
-      const GT* st = reinterpret_cast<const GT*>(ring + static_cast<size_t>(slot) * RG::kStage);
-      float* pbuf = part + (it & 1) * kPanelConsumers * RS;
-      float2 q[RS][4];  // squares of this lane's columns, per staged row
-      if (!dead) {
-        // A: squares, column sums, row shares
-        float rpart[RS];
+    for (int64_t s0 = c0; s0 < c1; s0 += kSubRows) {
+      const int64_t s1 = min(c1, s0 + kSubRows);
+      const float row_old = (threadIdx.x < s1 - s0) ? rowst[s0 + threadIdx.x] : 0.f;
+      // A: squares into C_j, row shares
+      for (int64_t i = s0; i < s1; i += RG) {
+        Raw<GT, 8> raw[RG][2];
+        seg_load<GT, RG>(raw, gb, W, i, s1, j0, lane, keep);
+        float rp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int rr = 0; rr < RS; ++rr) {
+        for (int rr = 0; rr < RG; ++rr) {
           float2 s2 = make_float2(0.f, 0.f);
-          if (has && rr < nrows) {
-            float2 x[4];
-            widen2(*reinterpret_cast<const Raw<GT, 8>*>(st + rr * W + j), x);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              q[rr][v] = __fmul2_rn(x[v], x[v]);
-              cacc[v] = __fadd2_rn(cacc[v], q[rr][v]);
-              s2 = __fadd2_rn(s2, q[rr][v]);
+          for (int c = 0; c < 2; ++c) {
+            const int64_t j = j0 + c * 256 + lane * 8;
+            if (i + rr < s1 && j < W) {
+              float2 x[4];
+              widen2(raw[rr][c], x);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const float2 q = __fmul2_rn(x[v], x[v]);
+                cacc[c][v] = __fadd2_rn(cacc[c][v], q);
+                s2 = __fadd2_rn(s2, q);
+              }
+              if (PSQ) {
+                float y[8];
+                load_f<8>(y, pb + (i + rr) * W + j);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
+              }
             }
-            if (PSQ) {
-              float y[8];
-              load_f<8>(y, pb + (rs + rr) * W + j);
-#pragma unroll
-              for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
-            }
-          } else {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) q[rr][v] = make_float2(0.f, 0.f);
           }
-          rpart[rr] = s2.x + s2.y;
+          rp[rr] = s2.x + s2.y;
         }
-        const float tot = reduce_scatter4(rpart, lane);
-        if ((lane & 7) == 0) pbuf[warp * RS + (((lane >> 4) & 1) << 1) + ((lane >> 3) & 1)] = tot;
+        const float tot = reduce_scatter4(rp, lane);
+        const int rr = (((lane >> 4) & 1) << 1) + ((lane >> 3) & 1);
+        if ((lane & 7) == 0 && rr < RG && i + rr < s1) part[(i + rr - s0) * kWarps + warp] = tot;
       }
-      panel_sync();
-      if (stop) dead = true;  // some warp gave up: the stage's row shares are incomplete
-      if (dead) continue;
-      // B: row totals (lane rr owns row rr), updated rows, weighted column sums
-      float w_lane = 0.f;
-      if (lane < nrows) {
+      __syncthreads();
+      if (threadIdx.x < s1 - s0) {
         float R = 0.f;
-        for (int w2 = 0; w2 < kPanelConsumers; ++w2) R += pbuf[w2 * RS + lane];
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) R += part[threadIdx.x * kWarps + w2];
         const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
-        w_lane = 1.0f / rn;
-        if (warp == 0) {
-          rowst[rs + lane] = rn;
-          rsum += rn;
+        rowst[s0 + threadIdx.x] = rn;
+        wsm[threadIdx.x] = 1.0f / rn;
+        rsum += rn;
+      }
+      __syncthreads();
+      // B: the same rows again (from L2), weighted squares into D_j
+      for (int64_t i = s0; i < s1; i += RG) {
+        Raw<GT, 8> raw[RG][2];
+        seg_load<GT, RG>(raw, gb, W, i, s1, j0, lane, drop);
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) {
+          if (i + rr < s1) {
+            const float wr = wsm[i + rr - s0];
+            const float2 w2 = make_float2(wr, wr);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int64_t j = j0 + c * 256 + lane * 8;
+              if (j < W) {
+                float2 x[4];
+                widen2(raw[rr][c], x);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) dacc[c][v] = __ffma2_rn(__fmul2_rn(x[v], w2), x[v], dacc[c][v]);
+              }
+            }
+          }
         }
       }
+      __syncthreads();  // part / wsm are free for the next sub-panel
+    }
+    // column partials of the chunk
+    float* cp = a.colpart + d.colpart + (b * d.prb + chunk) * W;
+    float* dp = a.dpart + d.dpart + (b * d.prb + chunk) * W;
 #pragma unroll
-      for (int rr = 0; rr < RS; ++rr) {
-        const float w_r = __shfl_sync(0xffffffffu, w_lane, rr);
-        const float2 w2 = make_float2(w_r, w_r);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) dacc[v] = __ffma2_rn(q[rr][v], w2, dacc[v]);
+    for (int c = 0; c < 2; ++c) {
+      const int64_t j = j0 + c * 256 + lane * 8;
+      if (j < W) {
+        *reinterpret_cast<float4*>(cp + j) = make_float4(cacc[c][0].x, cacc[c][0].y, cacc[c][1].x, cacc[c][1].y);
+        *reinterpret_cast<float4*>(cp + j + 4) = make_float4(cacc[c][2].x, cacc[c][2].y, cacc[c][3].x, cacc[c][3].y);
+        *reinterpret_cast<float4*>(dp + j) = make_float4(dacc[c][0].x, dacc[c][0].y, dacc[c][1].x, dacc[c][1].y);
+        *reinterpret_cast<float4*>(dp + j + 4) = make_float4(dacc[c][2].x, dacc[c][2].y, dacc[c][3].x, dacc[c][3].y);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    if (!stop && has) {
-      float* cp = a.colpart + d.colpart + (b * d.prb + panel) * W + j;
-      float* dp = a.dpart + d.dpart + (b * d.prb + panel) * W + j;
-      *reinterpret_cast<float4*>(cp) = make_float4(cacc[0].x, cacc[0].y, cacc[1].x, cacc[1].y);
-      *reinterpret_cast<float4*>(cp + 4) = make_float4(cacc[2].x, cacc[2].y, cacc[3].x, cacc[3].y);
-      *reinterpret_cast<float4*>(dp) = make_float4(dacc[0].x, dacc[0].y, dacc[1].x, dacc[1].y);
-      *reinterpret_cast<float4*>(dp + 4) = make_float4(dacc[2].x, dacc[2].y, dacc[3].x, dacc[3].y);
-    }
-    // sum_r row_r (warp 0, lanes in order through the xor tree), sum(p^2)
-    if (warp == 0) {
-      const float t = warp_sum(rsum);
-      if (lane == 0) red[0] = static_cast<double>(t);
-    }
+    const double rtot = block_sum(static_cast<double>(rsum), red);
     if (PSQ) {
-      const float t = warp_sum(psq);
-      if (lane == 0) red[kPanelConsumers + warp] = static_cast<double>(t);
+      const double ptot = block_sum(static_cast<double>(psq), red);
+      if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = ptot;
     }
-    panel_sync();
-    if (threadIdx.x == 0 && !stop) {
-      a.rowchunk[d.rowchunk + b * d.nrc + panel] = red[0];
-      if (PSQ) {
-        double p2 = 0.0;
-        for (int w2 = 0; w2 < kPanelConsumers; ++w2) p2 += red[kPanelConsumers + w2];
-        a.ppart[d.p1_0 + local] = p2;
-      }
-    }
+    if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + chunk] = rtot;
   }
-  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
 }
 
 // ---- apply (vector path) ---------------------------------------------------
@@ -1366,9 +1359,8 @@ template <typename GT>
 Inst pick_rows(KernelId k, bool psq_in, bool b1, bool psq_out) {
   Inst x;
   if (k == kKPass1) {
-    x.threads = kPanelThreads;
     x.fn = psq_in ? k_pass1_panel<GT, true> : k_pass1_panel<GT, false>;
-    x.smem = panel_smem<GT>();
+    x.smem = sizeof(float) * (kSubRows * kWarps + kSubRows) + kRedBytes + kPrefixBytes;
   } else if (k == kKApply) {
     x = pick_f<GT, 8>(k, psq_in, b1, psq_out);
   }

@@ -18,8 +18,8 @@
 
 namespace {
 
-// 64 MiB: enough for the scratch of about 1.6e9 parameters in 2D tensors of
-// Llama-like shapes (the workspace is ~1/24 byte per parameter plus a small
+// 64 MiB: enough for the scratch of about 2.1e9 parameters in 2D tensors of
+// Llama-like shapes (the workspace is ~1/32 byte per parameter plus a small
 // per-tensor part).
 constexpr size_t kNoAllocScratchBytes = ADAF_NOALLOC_SCRATCH_BYTES;
 

@@ -55,7 +55,7 @@ def test_noalloc_step_matches_workspace_step_on_two_calls():
 
 
 def test_noalloc_rejects_a_list_beyond_its_scratch():
-    """Llama-3-8B needs ~331 MB of scratch: more than the fixed area, so the
+    """Llama-3-8B needs ~254 MB of scratch: more than the fixed area, so the
     call fails before touching CUDA, naming both sizes."""
     shapes = [s for _, s in synth.llama3_8b_shapes()]
     n = len(shapes)
