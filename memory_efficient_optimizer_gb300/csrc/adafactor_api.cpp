@@ -176,7 +176,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       const bool vec_shape = (W % 8 == 0);
       // (bf16 gradients only: with fp32 ones the tiled passes are faster.)
       const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxRowsW &&
-                              t.grad_dtype == ADAF_BFLOAT16;
+                              H <= INT32_MAX && t.grad_dtype == ADAF_BFLOAT16;
       bool vec = vec_shape;
       if (full) {
         vec = vec_shape && aligned(t.param, 16) && aligned(t.grad, 16) &&

@@ -983,96 +983,114 @@ __device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) 
 // A work unit is a chunk of d.pr full rows of one slice (2048 <= W <= 4096),
 // taken by one CTA of 8 warps in sub-panels of kSubRows rows.  Warp w owns
 // the 512-column segment w of every row (lane l: columns 512 w + 256 c + 8 l
-// + [0, 8), c = 0, 1) and keeps its column sums in registers.  Per sub-panel:
-//   A. the warps stream their segments of the sub-panel's rows (128 bytes of
-//      loads in flight per lane), add the squares into the column
-//      sums C_j and write their share of each row total to shared memory;
-//   -- barrier --
-//   thread r adds the 8 shares of row r in warp order and forms the updated
-//   row statistic row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W + eps1)
-//   and its reciprocal;
-//   -- barrier --
-//   B. the warps stream the same rows again and add g_rj^2 / row_r into the
-//      second column sums D_j.  A sub-panel is 128 KB (16 rows of 4096 bf16),
-//      read first with an L2 evict_last policy and then with evict_first, so
-//      the second read is served by L2 while the whole GPU has only ~40 MB of
-//      sub-panels live.
+// + [0, 8), c = 0, 1) and keeps its column sums C_j and D_j in registers.
+//
+// Staging: every lane copies its own 16-byte pieces of each sub-panel into
+// its own shared-memory slots with cp.async (completion tracked per thread by
+// commit/wait groups: no spin loop, no mbarrier).  A ring of kPanelStages
+// sub-panels per CTA keeps two sub-panels in flight while one is processed,
+// so the bytes in flight do not cost registers, and the second use of the
+// values (phase B) reads shared memory instead of L2 or HBM.  Since a lane
+// only ever reads the slots it filled, the staged data needs no barrier.
+// Per sub-panel k:
+//   wait for this thread's copies of sub-panel k;
+//   A. add the squares into C_j; the warp's share of each row total goes to
+//      shared memory (one reduce-scatter over the lanes covers the 4 rows);
+//   -- barrier -- (row shares complete; every lane has finished sub-panel
+//      k - 1, whose stage is refilled now with sub-panel k + 2)
+//   every warp sums the 8 shares of each row (lane l: row l/8, warp l%8) and
+//   forms row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W + eps1) and its
+//   reciprocal; warp 0 stores row_r;
+//   B. add g_rj^2 / row_r into D_j from the same staged values.
 // With the column statistic of the step, sum(u^2) = mean(row) * sum_j D_j/col_j,
 // so g is read from HBM once here instead of twice.  Per chunk the warps
 // write C_j and D_j (column partials), and sum_r row_r goes to the row-chunk
-// sums (for mean(row)).  No waits: plain loads and CTA barriers only.
-constexpr int kSubRows = 16;
+// sums (for mean(row)).
+constexpr int kSubRows = 4;      // rows per sub-panel
+constexpr int kPanelStages = 3;  // sub-panels resident per CTA
+static_assert(kSubRows * kWarps == 32, "the row statistics take one (row, warp) share per lane");
 
-// L2 policies for the two reads of a sub-panel: keep it for the second read
-// (evict_last), drop it after (evict_first).
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint4 ld_hint(const void* ptr, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(pol));
-  return v;
-}
-__device__ __forceinline__ void load_raw_hint(Raw<__nv_bfloat16, 8>& r, const __nv_bfloat16* p, uint64_t pol) {
-  r.u = ld_hint(p, pol);
-}
-__device__ __forceinline__ void load_raw_hint(Raw<float, 8>& r, const float* p, uint64_t pol) {
-  const uint4 a = ld_hint(p, pol), b = ld_hint(p + 4, pol);
-  r.a = make_float4(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z), __uint_as_float(a.w));
-  r.b = make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w));
+// Shared-memory ring of the fused pass: per stage and warp, slot
+// ((rr * 2 + c) * kPieces + q) * 32 + lane holds 16 bytes (piece q of the 8
+// values of row rr, column group c, lane), so every warp-wide copy and read
+// touches 512 contiguous bytes.
+template <typename GT> struct PanelStage {
+  static constexpr int kPieces = static_cast<int>(sizeof(GT)) / 2;  // 16-byte pieces per 8 values
+  static constexpr int kWarpBytes = kSubRows * 2 * kPieces * 32 * 16;
+  static constexpr int kBytes = kWarpBytes * kWarps;
+};
+template <typename GT>
+constexpr size_t panel_smem_bytes() {
+  return static_cast<size_t>(kPanelStages) * PanelStage<GT>::kBytes + sizeof(float) * 2 * 32 + kRedBytes +
+         kPrefixBytes;
 }
 
-// Rows loaded per step of the fused pass (3 CTAs per SM: 64 bytes of bf16
-// gradient, 128 of fp32, in flight per lane).
-template <typename GT> struct PanelGroup { static constexpr int kRows = 2; };
+// 16-byte asynchronous global -> shared copy (bypasses L1).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-template <typename GT, int RG>
-__device__ __forceinline__ void seg_load(Raw<GT, 8> (&raw)[RG][2], const GT* gb, int64_t W, int64_t i, int64_t i1,
-                                         int64_t j0, int lane, uint64_t pol) {
+// This lane's copies of rows [q0, min(q0 + kSubRows, q1)) into its slots of
+// one stage (dst: shared address of the lane's first slot in that stage).
+template <typename GT>
+__device__ __forceinline__ void panel_issue(uint32_t dst, const GT* gb, int32_t W, int32_t q0, int32_t q1,
+                                            int32_t j0, int lane) {
+  constexpr int P = PanelStage<GT>::kPieces;
 #pragma unroll
-  for (int rr = 0; rr < RG; ++rr) {
+  for (int rr = 0; rr < kSubRows; ++rr) {
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      const int64_t j = j0 + c * 256 + lane * 8;
-      if (i + rr < i1 && j < W) load_raw_hint(raw[rr][c], gb + (i + rr) * W + j, pol);
+      const int32_t i = q0 + rr, j = j0 + c * 256 + lane * 8;
+      if (i < q1 && j < W) {
+        const GT* src = gb + static_cast<int64_t>(i) * W + j;
+#pragma unroll
+        for (int q = 0; q < P; ++q)
+          cp_async16(dst + ((rr * 2 + c) * P + q) * 512, src + q * (16 / static_cast<int>(sizeof(GT))));
+      }
     }
   }
 }
 
+__device__ __forceinline__ void panel_read(Raw<__nv_bfloat16, 8>& r, const unsigned char* slot) {
+  r.u = *reinterpret_cast<const uint4*>(slot);
+}
+__device__ __forceinline__ void panel_read(Raw<float, 8>& r, const unsigned char* slot) {
+  r.a = *reinterpret_cast<const float4*>(slot);
+  r.b = *reinterpret_cast<const float4*>(slot + 512);
+}
+
 template <typename GT, bool PSQ>
-__global__ void __launch_bounds__(kThreads, 3) k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
-  constexpr int RG = PanelGroup<GT>::kRows;
+__global__ void __launch_bounds__(kThreads, 2) k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
+  using PS = PanelStage<GT>;
+  constexpr int P = PS::kPieces;
   extern __shared__ __align__(16) unsigned char smem[];
-  float* part = reinterpret_cast<float*>(smem);           // [kSubRows][kWarps]
-  float* wsm = part + kSubRows * kWarps;                   // [kSubRows] 1 / row_r
-  double* red = reinterpret_cast<double*>(wsm + kSubRows);  // 16
+  float* part = reinterpret_cast<float*>(smem + kPanelStages * PS::kBytes);  // [2][kSubRows][kWarps]
+  double* red = reinterpret_cast<double*>(part + 2 * 32);
   int32_t* pf = reinterpret_cast<int32_t*>(red + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
   const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
   const float eps1 = static_cast<float>(a.eps1);
-  const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+  const unsigned char* mine = smem + warp * PS::kWarpBytes + lane * 16;
+  const uint32_t mine_s = static_cast<uint32_t>(__cvta_generic_to_shared(mine));
+  const int rl = lane >> 3;  // row of this lane's (row, warp) share
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
-    const int64_t local = u - pf[m];
-    const int64_t b = local / d.prb, chunk = local % d.prb;
-    const int64_t H = d.H, W = d.W;
-    const int64_t c0 = chunk * d.pr, c1 = min(H, c0 + d.pr);
-    const int64_t j0 = static_cast<int64_t>(warp) * 512;
-    const GT* gb = static_cast<const GT*>(d.g) + b * H * W;
-    const float* pb = d.p + b * H * W;
-    float* rowst = d.row + b * H;
+    // Row indices within a slice fit in int32 (the plan requires H <= INT32_MAX).
+    const int32_t local = static_cast<int32_t>(u - pf[m]);
+    const int32_t b = local / d.prb, chunk = local % d.prb;
+    const int32_t H = static_cast<int32_t>(d.H), W = static_cast<int32_t>(d.W);
+    const int32_t c0 = chunk * d.pr, c1 = min(H, c0 + d.pr);
+    const int32_t nsub = (c1 - c0 + kSubRows - 1) / kSubRows;
+    const int32_t j0 = warp * 512;
+    const GT* gb = static_cast<const GT*>(d.g) + static_cast<int64_t>(b) * H * W;
+    const float* pb = d.p + static_cast<int64_t>(b) * H * W;
+    float* rowst = d.row + static_cast<int64_t>(b) * H;
     const float invw = 1.0f / static_cast<float>(W);
     float2 cacc[2][4], dacc[2][4];
 #pragma unroll
@@ -1081,84 +1099,97 @@ __global__ void __launch_bounds__(kThreads, 3) k_pass1_panel(const __grid_consta
       for (int v = 0; v < 4; ++v) cacc[c][v] = dacc[c][v] = make_float2(0.f, 0.f);
     }
     float psq = 0.f, rsum = 0.f;
-    for (int64_t s0 = c0; s0 < c1; s0 += kSubRows) {
-      const int64_t s1 = min(c1, s0 + kSubRows);
-      const float row_old = (threadIdx.x < s1 - s0) ? rowst[s0 + threadIdx.x] : 0.f;
+    // Prologue: sub-panels 0 .. kPanelStages - 2 (one commit group each,
+    // empty past the chunk's end, so the group count stays in step).
+#pragma unroll
+    for (int k = 0; k < kPanelStages - 1; ++k) {
+      if (k < nsub) panel_issue<GT>(mine_s + k * PS::kBytes, gb, W, c0 + k * kSubRows, c1, j0, lane);
+      cp_async_commit();
+    }
+    int stage = 0;
+    for (int32_t k = 0; k < nsub; ++k) {
+      const int32_t s0 = c0 + k * kSubRows, s1 = min(c1, s0 + kSubRows);
+      const float row_old = (s0 + rl < s1) ? rowst[s0 + rl] : 0.f;
+      cp_async_wait_one_pending();  // groups up to sub-panel k are complete
+      const unsigned char* st = mine + stage * PS::kBytes;
+      float* pk = part + (k & 1) * 32;
       // A: squares into C_j, row shares
-      for (int64_t i = s0; i < s1; i += RG) {
-        Raw<GT, 8> raw[RG][2];
-        seg_load<GT, RG>(raw, gb, W, i, s1, j0, lane, keep);
-        float rp[4] = {0.f, 0.f, 0.f, 0.f};
+      float rp[kSubRows];
 #pragma unroll
-        for (int rr = 0; rr < RG; ++rr) {
-          float2 s2 = make_float2(0.f, 0.f);
+      for (int rr = 0; rr < kSubRows; ++rr) {
+        float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int64_t j = j0 + c * 256 + lane * 8;
-            if (i + rr < s1 && j < W) {
-              float2 x[4];
-              widen2(raw[rr][c], x);
+        for (int c = 0; c < 2; ++c) {
+          const int32_t j = j0 + c * 256 + lane * 8;
+          if (s0 + rr < s1 && j < W) {
+            Raw<GT, 8> raw;
+            panel_read(raw, st + (rr * 2 + c) * P * 512);
+            float2 x[4];
+            widen2(raw, x);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const float2 q = __fmul2_rn(x[v], x[v]);
-                cacc[c][v] = __fadd2_rn(cacc[c][v], q);
-                s2 = __fadd2_rn(s2, q);
-              }
-              if (PSQ) {
-                float y[8];
-                load_f<8>(y, pb + (i + rr) * W + j);
+            for (int v = 0; v < 4; ++v) {
+              const float2 q = __fmul2_rn(x[v], x[v]);
+              cacc[c][v] = __fadd2_rn(cacc[c][v], q);
+              s2 = __fadd2_rn(s2, q);
+            }
+            if (PSQ) {
+              float y[8];
+              load_f<8>(y, pb + static_cast<int64_t>(s0 + rr) * W + j);
 #pragma unroll
-                for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
-              }
+              for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
             }
           }
-          rp[rr] = s2.x + s2.y;
         }
-        const float tot = reduce_scatter4(rp, lane);
-        const int rr = (((lane >> 4) & 1) << 1) + ((lane >> 3) & 1);
-        if ((lane & 7) == 0 && rr < RG && i + rr < s1) part[(i + rr - s0) * kWarps + warp] = tot;
+        rp[rr] = s2.x + s2.y;
       }
+      const float tot = reduce_scatter4(rp, lane);  // warp total of row rl
+      if ((lane & 7) == 0) pk[rl * kWarps + warp] = tot;
       __syncthreads();
-      if (threadIdx.x < s1 - s0) {
-        float R = 0.f;
-#pragma unroll
-        for (int w2 = 0; w2 < kWarps; ++w2) R += part[threadIdx.x * kWarps + w2];
-        const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
-        rowst[s0 + threadIdx.x] = rn;
-        wsm[threadIdx.x] = 1.0f / rn;
+      // Refill the stage of sub-panel k - 1 (every lane is past it) with k + kPanelStages - 1.
+      {
+        const int32_t kk = k + kPanelStages - 1;
+        const int fill = stage == 0 ? kPanelStages - 1 : stage - 1;
+        if (kk < nsub) panel_issue<GT>(mine_s + fill * PS::kBytes, gb, W, c0 + kk * kSubRows, c1, j0, lane);
+        cp_async_commit();
+      }
+      // Row statistics of the sub-panel, in every warp: lane l adds the
+      // shares of row l/8 over the warps (fixed xor tree).
+      float R = pk[lane];
+      R += __shfl_xor_sync(0xffffffffu, R, 4);
+      R += __shfl_xor_sync(0xffffffffu, R, 2);
+      R += __shfl_xor_sync(0xffffffffu, R, 1);
+      const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
+      const float winv = 1.0f / rn;
+      if (warp == 0 && (lane & 7) == 0 && s0 + rl < s1) {
+        rowst[s0 + rl] = rn;
         rsum += rn;
       }
-      __syncthreads();
-      // B: the same rows again (from L2), weighted squares into D_j
-      for (int64_t i = s0; i < s1; i += RG) {
-        Raw<GT, 8> raw[RG][2];
-        seg_load<GT, RG>(raw, gb, W, i, s1, j0, lane, drop);
+      // B: weighted squares into D_j from the same staged values
 #pragma unroll
-        for (int rr = 0; rr < RG; ++rr) {
-          if (i + rr < s1) {
-            const float wr = wsm[i + rr - s0];
-            const float2 w2 = make_float2(wr, wr);
+      for (int rr = 0; rr < kSubRows; ++rr) {
+        const float wr = __shfl_sync(0xffffffffu, winv, rr * 8);
+        const float2 w2 = make_float2(wr, wr);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int64_t j = j0 + c * 256 + lane * 8;
-              if (j < W) {
-                float2 x[4];
-                widen2(raw[rr][c], x);
+        for (int c = 0; c < 2; ++c) {
+          const int32_t j = j0 + c * 256 + lane * 8;
+          if (s0 + rr < s1 && j < W) {
+            Raw<GT, 8> raw;
+            panel_read(raw, st + (rr * 2 + c) * P * 512);
+            float2 x[4];
+            widen2(raw, x);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) dacc[c][v] = __ffma2_rn(__fmul2_rn(x[v], w2), x[v], dacc[c][v]);
-              }
-            }
+            for (int v = 0; v < 4; ++v) dacc[c][v] = __ffma2_rn(__fmul2_rn(x[v], w2), x[v], dacc[c][v]);
           }
         }
       }
-      __syncthreads();  // part / wsm are free for the next sub-panel
+      stage = stage == kPanelStages - 1 ? 0 : stage + 1;
     }
     // column partials of the chunk
-    float* cp = a.colpart + d.colpart + (b * d.prb + chunk) * W;
-    float* dp = a.dpart + d.dpart + (b * d.prb + chunk) * W;
+    float* cp = a.colpart + d.colpart + static_cast<int64_t>(b * d.prb + chunk) * W;
+    float* dp = a.dpart + d.dpart + static_cast<int64_t>(b * d.prb + chunk) * W;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      const int64_t j = j0 + c * 256 + lane * 8;
+      const int32_t j = j0 + c * 256 + lane * 8;
       if (j < W) {
         *reinterpret_cast<float4*>(cp + j) = make_float4(cacc[c][0].x, cacc[c][0].y, cacc[c][1].x, cacc[c][1].y);
         *reinterpret_cast<float4*>(cp + j + 4) = make_float4(cacc[c][2].x, cacc[c][2].y, cacc[c][3].x, cacc[c][3].y);
@@ -1166,6 +1197,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_pass1_panel(const __grid_consta
         *reinterpret_cast<float4*>(dp + j + 4) = make_float4(dacc[c][2].x, dacc[c][2].y, dacc[c][3].x, dacc[c][3].y);
       }
     }
+    // (block_sum's barriers also order this chunk's last reads of the ring
+    // before the next chunk's prologue refills it)
     const double rtot = block_sum(static_cast<double>(rsum), red);
     if (PSQ) {
       const double ptot = block_sum(static_cast<double>(psq), red);
@@ -1173,6 +1206,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_pass1_panel(const __grid_consta
     }
     if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + chunk] = rtot;
   }
+  cp_async_wait_all();  // only empty groups can be pending here
 }
 
 // ---- apply (vector path) ---------------------------------------------------
@@ -1360,7 +1394,7 @@ Inst pick_rows(KernelId k, bool psq_in, bool b1, bool psq_out) {
   Inst x;
   if (k == kKPass1) {
     x.fn = psq_in ? k_pass1_panel<GT, true> : k_pass1_panel<GT, false>;
-    x.smem = sizeof(float) * (kSubRows * kWarps + kSubRows) + kRedBytes + kPrefixBytes;
+    x.smem = panel_smem_bytes<GT>();
   } else if (k == kKApply) {
     x = pick_f<GT, 8>(k, psq_in, b1, psq_out);
   }
