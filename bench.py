@@ -75,13 +75,22 @@ def measured_hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# Classes whose pass 1 is the fused row-chunk pass (g read twice per step, not three times).
+FUSED_CLASSES = ("rows_bf16", "wide_bf16")
+
+
 def tensor_class(shape, grad_bytes):
     """The library's tensor class of a contiguous, 256-byte aligned tensor."""
     if len(shape) < 2:
         return "1d"
     w = int(shape[-1])
-    kind = "elem_" if w % 8 else ("rows_" if 2048 <= w <= 4096 and grad_bytes == 2 else "vec_")
-    return kind + ("bf16" if grad_bytes == 2 else "f32")
+    if w % 8:
+        return "elem_" + ("bf16" if grad_bytes == 2 else "f32")
+    if grad_bytes == 2 and 2048 <= w <= 4096:
+        return "rows_bf16"
+    if grad_bytes == 2 and 4096 < w <= 16384:
+        return "wide_bf16"
+    return "vec_" + ("bf16" if grad_bytes == 2 else "f32")
 
 
 def algorithmic_bytes(shapes, grad_bytes, beta1):
@@ -103,14 +112,14 @@ def algorithmic_bytes(shapes, grad_bytes, beta1):
             lead = n // (int(s[-2]) * int(s[-1]))
             state_rw = 2 * 4 * lead * (int(s[-2]) + int(s[-1]))
             state_read = state_rw // 2
-            p1 = grad_bytes * n + (2 * 4 * lead * int(s[-2]) if cls.startswith("rows") else 0)
+            p1 = grad_bytes * n + (2 * 4 * lead * int(s[-2]) if cls in FUSED_CLASSES else 0)
         else:
             state_rw = 2 * 4 * n
             state_read = 4 * n
             p1 = grad_bytes * n + state_rw
         m1 = 8 * n if beta1 else 0
         step += 3 * grad_bytes * n + 8 * n + m1 + state_rw
-        impl += (2 if cls.startswith(("rows", "1d")) else 3) * grad_bytes * n + 8 * n + m1 + state_rw
+        impl += (2 if cls in FUSED_CLASSES or cls == "1d" else 3) * grad_bytes * n + 8 * n + m1 + state_rw
         slots[f"k_pass1[{cls}]"] = slots.get(f"k_pass1[{cls}]", 0) + p1
         if cls.startswith(("vec", "elem")):
             slots[f"k_pass2[{cls}]"] = slots.get(f"k_pass2[{cls}]", 0) + grad_bytes * n

@@ -89,7 +89,7 @@ struct Plan {
 int stream_slot(KernelId k) { return k == meo::kKPass1 ? 0 : (k == meo::kKPass2 ? 1 : 2); }
 
 // Rows per work unit of the fused pass.
-int32_t panel_rows(int64_t) { return meo::kRowsChunk; }
+int32_t panel_rows(int64_t W) { return W <= meo::kMaxRowsW ? meo::kRowsChunk : meo::kWideChunk; }
 
 // Checks the tensor list and builds the plan.  With full == false (size
 // query) only the shapes and dtypes are read; states and hp are not touched.
@@ -172,10 +172,10 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       d.ncc = static_cast<int32_t>(ceil_div(W, meo::kColChunk));
       ntiles = B * d.rb * d.cb;
       // Path: vector (16-byte aligned rows) or element-wise; a vector tensor
-      // with W <= kMaxRowsW takes the fused row-panel pass 1.
+      // with bf16 gradients and kMinRowsW <= W <= kMaxWideW takes the fused
+      // row-chunk pass 1 (fp32 gradients keep the tiled passes).
       const bool vec_shape = (W % 8 == 0);
-      // (bf16 gradients only: with fp32 ones the tiled passes are faster.)
-      const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxRowsW &&
+      const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxWideW &&
                               H <= INT32_MAX && t.grad_dtype == ADAF_BFLOAT16;
       bool vec = vec_shape;
       if (full) {
@@ -188,7 +188,6 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       // Row-panel geometry (also reserved in the size query for rows_shape).
       int32_t prb_rows = 0;
       if (rows_shape) {
-        d.seg = static_cast<int32_t>(ceil_div(W, 256));
         d.pr = panel_rows(W);
         prb_rows = static_cast<int32_t>(ceil_div(H, d.pr));
       }
@@ -253,7 +252,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
     const bool bf = d.gdt == meo::kGradBF16;
     if (d.kind == meo::kFactoredVec) c = bf ? meo::kClsVecBF16 : meo::kClsVecF32;
     if (d.kind == meo::kFactoredScalar) c = bf ? meo::kClsScalarBF16 : meo::kClsScalarF32;
-    if (d.kind == meo::kFactoredRows) c = bf ? meo::kClsRowsBF16 : meo::kClsRowsF32;
+    if (d.kind == meo::kFactoredRows) c = d.W <= meo::kMaxRowsW ? meo::kClsRowsBF16 : meo::kClsWideBF16;
     const bool two_pass = d.kind == meo::kFactoredVec || d.kind == meo::kFactoredScalar;
     plan->cls_idx[c].push_back(static_cast<int32_t>(k));
     plan->cls_pf[0][c].push_back(plan->cls_pf[0][c].back() + static_cast<int32_t>(d.p1_n));
@@ -325,7 +324,7 @@ struct ProfRecord {
 // other kernel kind, in launch order.
 constexpr int kNumSlots = 3 * meo::kNumClasses + 4;
 const char* const kClassNames[meo::kNumClasses] = {"vec_bf16", "vec_f32",  "elem_bf16", "elem_f32",
-                                                   "1d",       "rows_bf16", "rows_f32"};
+                                                   "1d",       "rows_bf16", "wide_bf16"};
 
 int profile_slot(KernelId k, int cls) {
   const int C = meo::kNumClasses;

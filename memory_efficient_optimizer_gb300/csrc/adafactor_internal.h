@@ -29,18 +29,22 @@ constexpr int kColChunk = 256;
 constexpr int kMaxGroup = 4096;
 
 enum TensorKind : int32_t {
-  kFactoredVec = 0,   // ndim >= 2, W % 8 == 0, 16-byte aligned pointers, W > kMaxRowsW
+  kFactoredVec = 0,   // ndim >= 2, W % 8 == 0, 16-byte aligned pointers (tiled passes 1 and 2)
   kFactoredScalar = 1,// ndim >= 2, anything else
   kUnfactored = 2,    // ndim < 2
-  kFactoredRows = 3,  // as kFactoredVec with kMinRowsW <= W <= kMaxRowsW, bf16 grads: fused pass 1
+  kFactoredRows = 3,  // as kFactoredVec with kMinRowsW <= W <= kMaxWideW, bf16 grads: fused pass 1
 };
 
-// Fused pass 1 (kFactoredRows, kMinRowsW <= W <= kMaxRowsW): a CTA of
-// kWarps warps takes chunks of d.pr full rows; warp w owns the 512-column
-// segment w of every row and keeps its column sums in registers.
-constexpr int kMinRowsW = 2048;          // narrower rows keep the tiled two-pass path
-constexpr int kMaxRowsW = kWarps * 512;  // 4096: one segment per warp
-constexpr int kRowsChunk = 256;          // rows per work unit
+// Fused pass 1 (kFactoredRows): a CTA takes chunks of d.pr full rows and
+// keeps the column sums of the chunk in registers, 8 values x G column
+// groups of 256 per lane.  Two configurations:
+//   rows:  2048 <= W <= 4096,  8 warps x 2 groups, 256-row chunks;
+//   wide:  4096 <  W <= 16384, 16 warps x 4 groups, 128-row chunks.
+constexpr int kMinRowsW = 2048;   // narrower rows keep the tiled two-pass path
+constexpr int kMaxRowsW = 4096;   // 8 warps x 2 groups x 256 columns
+constexpr int kMaxWideW = 16384;  // 16 warps x 4 groups x 256 columns
+constexpr int kRowsChunk = 256;   // rows per work unit (rows configuration)
+constexpr int kWideChunk = 128;   // rows per work unit (wide configuration)
 
 enum GradType : int32_t { kGradF32 = 0, kGradBF16 = 1 };
 
@@ -64,7 +68,7 @@ struct DevTensor {
   int32_t ncc;    // column chunks per slice(ceil(W / kColChunk))
   int32_t prb;    // row blocks of the column partials: rb, or panels per slice (kFactoredRows)
   int32_t pr;     // rows per panel (kFactoredRows)
-  int32_t seg;    // 256-column segments per row (kFactoredRows)
+  int32_t seg;    // unused (0)
   int32_t lanes;  // unused (0)
   int64_t ntiles;     // apply tiles
   int64_t p1_0, p1_n; // pass-1 units: global base (Ppart slot) and count
@@ -87,8 +91,8 @@ enum TensorClass : int32_t {
   kClsScalarBF16 = 2,  // factored, element-wise path, bf16 grads
   kClsScalarF32 = 3,   // factored, element-wise path, fp32 grads
   kClsUnfactored = 4,  // ndim < 2 (any grad dtype)
-  kClsRowsBF16 = 5,    // fused pass 1, bf16 grads
-  kClsRowsF32 = 6,     // fused pass 1, fp32 grads
+  kClsRowsBF16 = 5,    // fused pass 1, bf16 grads, 2048 <= W <= 4096
+  kClsWideBF16 = 6,    // fused pass 1, bf16 grads, 4096 < W <= 16384
   kNumClasses = 7
 };
 

@@ -114,12 +114,6 @@ __device__ __forceinline__ void widen2(const Raw<__nv_bfloat16, 8>& r, float2 (&
 #pragma unroll
   for (int k = 0; k < 4; ++k) x[k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
 }
-__device__ __forceinline__ void widen2(const Raw<float, 8>& r, float2 (&x)[4]) {
-  x[0] = make_float2(r.a.x, r.a.y);
-  x[1] = make_float2(r.a.z, r.a.w);
-  x[2] = make_float2(r.b.x, r.b.y);
-  x[3] = make_float2(r.b.z, r.b.w);
-}
 
 __device__ __forceinline__ float load_g1(const void* g, int gdt, int64_t e) {
   if (gdt == kGradBF16) {
@@ -980,10 +974,12 @@ __device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) 
 }
 
 // ---- fused pass 1 over row chunks (kFactoredRows) --------------------------
-// A work unit is a chunk of d.pr full rows of one slice (2048 <= W <= 4096),
-// taken by one CTA of 8 warps in sub-panels of kSubRows rows.  Warp w owns
-// the 512-column segment w of every row (lane l: columns 512 w + 256 c + 8 l
-// + [0, 8), c = 0, 1) and keeps its column sums C_j and D_j in registers.
+// A work unit is a chunk of d.pr full rows of one slice, taken by one CTA of
+// NW warps in sub-panels of SR = 32 / NW rows.  Lane l of warp w owns the
+// column groups c * NW + w (c < G) of 256 columns, 8 consecutive columns
+// (256 (c NW + w) + 8 l + [0, 8)) in each, and keeps their column sums C_j
+// and D_j in registers.  Configurations: NW = 8, G = 2 for W <= 4096
+// (2 CTAs per SM); NW = 16, G = 4 for W <= 16384 (1 CTA per SM).
 //
 // Staging: every lane copies its own 16-byte pieces of each sub-panel into
 // its own shared-memory slots with cp.async (completion tracked per thread by
@@ -995,35 +991,33 @@ __device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) 
 // Per sub-panel k:
 //   wait for this thread's copies of sub-panel k;
 //   A. add the squares into C_j; the warp's share of each row total goes to
-//      shared memory (one reduce-scatter over the lanes covers the 4 rows);
+//      shared memory (one reduce-scatter over the lanes covers the SR rows);
 //   -- barrier -- (row shares complete; every lane has finished sub-panel
 //      k - 1, whose stage is refilled now with sub-panel k + 2)
-//   every warp sums the 8 shares of each row (lane l: row l/8, warp l%8) and
-//   forms row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W + eps1) and its
-//   reciprocal; warp 0 stores row_r;
+//   every warp sums the NW shares of each row (lane l: row l / NW, warp
+//   l % NW) and forms row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W +
+//   eps1) and its reciprocal; warp 0 stores row_r;
 //   B. add g_rj^2 / row_r into D_j from the same staged values.
 // With the column statistic of the step, sum(u^2) = mean(row) * sum_j D_j/col_j,
 // so g is read from HBM once here instead of twice.  Per chunk the warps
 // write C_j and D_j (column partials), and sum_r row_r goes to the row-chunk
 // sums (for mean(row)).
-constexpr int kSubRows = 4;      // rows per sub-panel
 constexpr int kPanelStages = 3;  // sub-panels resident per CTA
-static_assert(kSubRows * kWarps == 32, "the row statistics take one (row, warp) share per lane");
 
 // Shared-memory ring of the fused pass: per stage and warp, slot
-// ((rr * 2 + c) * kPieces + q) * 32 + lane holds 16 bytes (piece q of the 8
+// ((rr * G + c) * kPieces + q) * 32 + lane holds 16 bytes (piece q of the 8
 // values of row rr, column group c, lane), so every warp-wide copy and read
 // touches 512 contiguous bytes.
-template <typename GT> struct PanelStage {
+template <typename GT, int NW, int G> struct PanelCfg {
+  static constexpr int kSubRows = 32 / NW;
   static constexpr int kPieces = static_cast<int>(sizeof(GT)) / 2;  // 16-byte pieces per 8 values
-  static constexpr int kWarpBytes = kSubRows * 2 * kPieces * 32 * 16;
-  static constexpr int kBytes = kWarpBytes * kWarps;
+  static constexpr int kWarpBytes = kSubRows * G * kPieces * 32 * 16;
+  static constexpr int kStageBytes = kWarpBytes * NW;
+  static constexpr size_t kRedOff = static_cast<size_t>(kPanelStages) * kStageBytes + sizeof(float) * 2 * 32;
+  static constexpr size_t kSmem = kRedOff + sizeof(double) * 32 + kPrefixBytes;
+  static_assert(kSubRows * NW == 32, "the row statistics take one (row, warp) share per lane");
+  static_assert(NW + 1 <= 32, "the CTA sum needs NW + 1 doubles");
 };
-template <typename GT>
-constexpr size_t panel_smem_bytes() {
-  return static_cast<size_t>(kPanelStages) * PanelStage<GT>::kBytes + sizeof(float) * 2 * 32 + kRedBytes +
-         kPrefixBytes;
-}
 
 // 16-byte asynchronous global -> shared copy (bypasses L1).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -1033,22 +1027,23 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// This lane's copies of rows [q0, min(q0 + kSubRows, q1)) into its slots of
-// one stage (dst: shared address of the lane's first slot in that stage).
-template <typename GT>
-__device__ __forceinline__ void panel_issue(uint32_t dst, const GT* gb, int32_t W, int32_t q0, int32_t q1,
-                                            int32_t j0, int lane) {
-  constexpr int P = PanelStage<GT>::kPieces;
+// This lane's copies of rows [q0, min(q0 + SR, q1)) into its slots of one
+// stage (dst: shared address of the lane's first slot in that stage).
+template <typename GT, int NW, int G>
+__device__ __forceinline__ void panel_issue(uint32_t dst, const GT* gb, int32_t W, int32_t q0, int32_t q1, int warp,
+                                            int lane) {
+  using C = PanelCfg<GT, NW, G>;
+  constexpr int P = C::kPieces;
 #pragma unroll
-  for (int rr = 0; rr < kSubRows; ++rr) {
+  for (int rr = 0; rr < C::kSubRows; ++rr) {
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int32_t i = q0 + rr, j = j0 + c * 256 + lane * 8;
+    for (int c = 0; c < G; ++c) {
+      const int32_t i = q0 + rr, j = (c * NW + warp) * 256 + lane * 8;
       if (i < q1 && j < W) {
         const GT* src = gb + static_cast<int64_t>(i) * W + j;
 #pragma unroll
         for (int q = 0; q < P; ++q)
-          cp_async16(dst + ((rr * 2 + c) * P + q) * 512, src + q * (16 / static_cast<int>(sizeof(GT))));
+          cp_async16(dst + ((rr * G + c) * P + q) * 512, src + q * (16 / static_cast<int>(sizeof(GT))));
       }
     }
   }
@@ -1057,27 +1052,56 @@ __device__ __forceinline__ void panel_issue(uint32_t dst, const GT* gb, int32_t 
 __device__ __forceinline__ void panel_read(Raw<__nv_bfloat16, 8>& r, const unsigned char* slot) {
   r.u = *reinterpret_cast<const uint4*>(slot);
 }
-__device__ __forceinline__ void panel_read(Raw<float, 8>& r, const unsigned char* slot) {
-  r.a = *reinterpret_cast<const float4*>(slot);
-  r.b = *reinterpret_cast<const float4*>(slot + 512);
+
+// Two-row version of reduce_scatter4: lane l gets the warp total of value
+// l >> 4 (complete in lanes 0 and 16).
+__device__ __forceinline__ float reduce_scatter2(const float (&v)[2], int lane) {
+  const bool h16 = lane & 16;
+  float k = h16 ? v[1] : v[0];
+  k += __shfl_xor_sync(0xffffffffu, h16 ? v[0] : v[1], 16);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) k += __shfl_xor_sync(0xffffffffu, k, o);
+  return k;
+}
+__device__ __forceinline__ float panel_row_shares(const float (&v)[4], int lane) { return reduce_scatter4(v, lane); }
+__device__ __forceinline__ float panel_row_shares(const float (&v)[2], int lane) { return reduce_scatter2(v, lane); }
+
+// CTA-wide sum over NW warps in a fixed order (red: NW + 1 doubles).
+template <int NW>
+__device__ __forceinline__ double panel_block_sum(double v, double* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) s += red[w];
+    red[NW] = s;
+  }
+  __syncthreads();
+  const double s = red[NW];
+  __syncthreads();
+  return s;
 }
 
-template <typename GT, bool PSQ>
-__global__ void __launch_bounds__(kThreads, 2) k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
-  using PS = PanelStage<GT>;
-  constexpr int P = PS::kPieces;
+template <typename GT, int NW, int G, bool PSQ>
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1)
+    k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
+  using C = PanelCfg<GT, NW, G>;
+  constexpr int SR = C::kSubRows, P = C::kPieces;
   extern __shared__ __align__(16) unsigned char smem[];
-  float* part = reinterpret_cast<float*>(smem + kPanelStages * PS::kBytes);  // [2][kSubRows][kWarps]
-  double* red = reinterpret_cast<double*>(part + 2 * 32);
-  int32_t* pf = reinterpret_cast<int32_t*>(red + 16);
+  float* part = reinterpret_cast<float*>(smem + kPanelStages * C::kStageBytes);  // [2][SR][NW]
+  double* red = reinterpret_cast<double*>(smem + C::kRedOff);
+  int32_t* pf = reinterpret_cast<int32_t*>(red + 32);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
   const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
   const float eps1 = static_cast<float>(a.eps1);
-  const unsigned char* mine = smem + warp * PS::kWarpBytes + lane * 16;
+  const unsigned char* mine = smem + warp * C::kWarpBytes + lane * 16;
   const uint32_t mine_s = static_cast<uint32_t>(__cvta_generic_to_shared(mine));
-  const int rl = lane >> 3;  // row of this lane's (row, warp) share
+  const int rl = lane / NW;  // row of this lane's (row, warp) share
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
@@ -1086,15 +1110,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_panel(const __grid_consta
     const int32_t b = local / d.prb, chunk = local % d.prb;
     const int32_t H = static_cast<int32_t>(d.H), W = static_cast<int32_t>(d.W);
     const int32_t c0 = chunk * d.pr, c1 = min(H, c0 + d.pr);
-    const int32_t nsub = (c1 - c0 + kSubRows - 1) / kSubRows;
-    const int32_t j0 = warp * 512;
+    const int32_t nsub = (c1 - c0 + SR - 1) / SR;
     const GT* gb = static_cast<const GT*>(d.g) + static_cast<int64_t>(b) * H * W;
     const float* pb = d.p + static_cast<int64_t>(b) * H * W;
     float* rowst = d.row + static_cast<int64_t>(b) * H;
     const float invw = 1.0f / static_cast<float>(W);
-    float2 cacc[2][4], dacc[2][4];
+    float2 cacc[G][4], dacc[G][4];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < G; ++c) {
 #pragma unroll
       for (int v = 0; v < 4; ++v) cacc[c][v] = dacc[c][v] = make_float2(0.f, 0.f);
     }
@@ -1103,27 +1126,27 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_panel(const __grid_consta
     // empty past the chunk's end, so the group count stays in step).
 #pragma unroll
     for (int k = 0; k < kPanelStages - 1; ++k) {
-      if (k < nsub) panel_issue<GT>(mine_s + k * PS::kBytes, gb, W, c0 + k * kSubRows, c1, j0, lane);
+      if (k < nsub) panel_issue<GT, NW, G>(mine_s + k * C::kStageBytes, gb, W, c0 + k * SR, c1, warp, lane);
       cp_async_commit();
     }
     int stage = 0;
     for (int32_t k = 0; k < nsub; ++k) {
-      const int32_t s0 = c0 + k * kSubRows, s1 = min(c1, s0 + kSubRows);
+      const int32_t s0 = c0 + k * SR, s1 = min(c1, s0 + SR);
       const float row_old = (s0 + rl < s1) ? rowst[s0 + rl] : 0.f;
       cp_async_wait_one_pending();  // groups up to sub-panel k are complete
-      const unsigned char* st = mine + stage * PS::kBytes;
+      const unsigned char* st = mine + stage * C::kStageBytes;
       float* pk = part + (k & 1) * 32;
       // A: squares into C_j, row shares
-      float rp[kSubRows];
+      float rp[SR];
 #pragma unroll
-      for (int rr = 0; rr < kSubRows; ++rr) {
+      for (int rr = 0; rr < SR; ++rr) {
         float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int32_t j = j0 + c * 256 + lane * 8;
+        for (int c = 0; c < G; ++c) {
+          const int32_t j = (c * NW + warp) * 256 + lane * 8;
           if (s0 + rr < s1 && j < W) {
             Raw<GT, 8> raw;
-            panel_read(raw, st + (rr * 2 + c) * P * 512);
+            panel_read(raw, st + (rr * G + c) * P * 512);
             float2 x[4];
             widen2(raw, x);
 #pragma unroll
@@ -1142,39 +1165,38 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_panel(const __grid_consta
         }
         rp[rr] = s2.x + s2.y;
       }
-      const float tot = reduce_scatter4(rp, lane);  // warp total of row rl
-      if ((lane & 7) == 0) pk[rl * kWarps + warp] = tot;
+      const float tot = panel_row_shares(rp, lane);  // warp total of row rl
+      if (lane % NW == 0) pk[rl * NW + warp] = tot;
       __syncthreads();
       // Refill the stage of sub-panel k - 1 (every lane is past it) with k + kPanelStages - 1.
       {
         const int32_t kk = k + kPanelStages - 1;
         const int fill = stage == 0 ? kPanelStages - 1 : stage - 1;
-        if (kk < nsub) panel_issue<GT>(mine_s + fill * PS::kBytes, gb, W, c0 + kk * kSubRows, c1, j0, lane);
+        if (kk < nsub) panel_issue<GT, NW, G>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
         cp_async_commit();
       }
       // Row statistics of the sub-panel, in every warp: lane l adds the
-      // shares of row l/8 over the warps (fixed xor tree).
+      // shares of row l / NW over the warps (fixed xor tree).
       float R = pk[lane];
-      R += __shfl_xor_sync(0xffffffffu, R, 4);
-      R += __shfl_xor_sync(0xffffffffu, R, 2);
-      R += __shfl_xor_sync(0xffffffffu, R, 1);
+#pragma unroll
+      for (int o = NW / 2; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
       const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
       const float winv = 1.0f / rn;
-      if (warp == 0 && (lane & 7) == 0 && s0 + rl < s1) {
+      if (warp == 0 && lane % NW == 0 && s0 + rl < s1) {
         rowst[s0 + rl] = rn;
         rsum += rn;
       }
       // B: weighted squares into D_j from the same staged values
 #pragma unroll
-      for (int rr = 0; rr < kSubRows; ++rr) {
-        const float wr = __shfl_sync(0xffffffffu, winv, rr * 8);
+      for (int rr = 0; rr < SR; ++rr) {
+        const float wr = __shfl_sync(0xffffffffu, winv, rr * NW);
         const float2 w2 = make_float2(wr, wr);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int32_t j = j0 + c * 256 + lane * 8;
+        for (int c = 0; c < G; ++c) {
+          const int32_t j = (c * NW + warp) * 256 + lane * 8;
           if (s0 + rr < s1 && j < W) {
             Raw<GT, 8> raw;
-            panel_read(raw, st + (rr * 2 + c) * P * 512);
+            panel_read(raw, st + (rr * G + c) * P * 512);
             float2 x[4];
             widen2(raw, x);
 #pragma unroll
@@ -1188,8 +1210,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_panel(const __grid_consta
     float* cp = a.colpart + d.colpart + static_cast<int64_t>(b * d.prb + chunk) * W;
     float* dp = a.dpart + d.dpart + static_cast<int64_t>(b * d.prb + chunk) * W;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int32_t j = j0 + c * 256 + lane * 8;
+    for (int c = 0; c < G; ++c) {
+      const int32_t j = (c * NW + warp) * 256 + lane * 8;
       if (j < W) {
         *reinterpret_cast<float4*>(cp + j) = make_float4(cacc[c][0].x, cacc[c][0].y, cacc[c][1].x, cacc[c][1].y);
         *reinterpret_cast<float4*>(cp + j + 4) = make_float4(cacc[c][2].x, cacc[c][2].y, cacc[c][3].x, cacc[c][3].y);
@@ -1197,11 +1219,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_panel(const __grid_consta
         *reinterpret_cast<float4*>(dp + j + 4) = make_float4(dacc[c][2].x, dacc[c][2].y, dacc[c][3].x, dacc[c][3].y);
       }
     }
-    // (block_sum's barriers also order this chunk's last reads of the ring
-    // before the next chunk's prologue refills it)
-    const double rtot = block_sum(static_cast<double>(rsum), red);
+    // (the barriers of the CTA sums also order this chunk's last reads of
+    // the ring before the next chunk's prologue refills it)
+    const double rtot = panel_block_sum<NW>(static_cast<double>(rsum), red);
     if (PSQ) {
-      const double ptot = block_sum(static_cast<double>(psq), red);
+      const double ptot = panel_block_sum<NW>(static_cast<double>(psq), red);
       if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = ptot;
     }
     if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + chunk] = rtot;
@@ -1388,13 +1410,15 @@ Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
   }
 }
 
-// Fused pass 1 and the bulk-copy apply for one gradient type (row-panel classes).
-template <typename GT>
+// Fused pass 1 (NW warps, G column groups per lane) and the bulk-copy apply
+// of the row-chunk classes.
+template <typename GT, int NW, int G>
 Inst pick_rows(KernelId k, bool psq_in, bool b1, bool psq_out) {
   Inst x;
   if (k == kKPass1) {
-    x.fn = psq_in ? k_pass1_panel<GT, true> : k_pass1_panel<GT, false>;
-    x.smem = panel_smem_bytes<GT>();
+    x.fn = psq_in ? k_pass1_panel<GT, NW, G, true> : k_pass1_panel<GT, NW, G, false>;
+    x.threads = NW * 32;
+    x.smem = PanelCfg<GT, NW, G>::kSmem;
   } else if (k == kKApply) {
     x = pick_f<GT, 8>(k, psq_in, b1, psq_out);
   }
@@ -1408,8 +1432,8 @@ Inst pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
     case kClsVecF32: return pick_f<float, 8>(k, psq_in, b1, psq_out);
     case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, b1, psq_out);
     case kClsScalarF32: return pick_f<float, 1>(k, psq_in, b1, psq_out);
-    case kClsRowsBF16: return pick_rows<__nv_bfloat16>(k, psq_in, b1, psq_out);
-    case kClsRowsF32: return pick_rows<float>(k, psq_in, b1, psq_out);
+    case kClsRowsBF16: return pick_rows<__nv_bfloat16, 8, 2>(k, psq_in, b1, psq_out);
+    case kClsWideBF16: return pick_rows<__nv_bfloat16, 16, 4>(k, psq_in, b1, psq_out);
     case kClsUnfactored:
       x.smem = kRedBytes + kPrefixBytes;
       if (k == kKPass1) x.fn = psq_in ? k_pass1_u<true> : k_pass1_u<false>;

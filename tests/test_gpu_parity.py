@@ -66,7 +66,13 @@ def test_llama3_8b_beta1_student_t_sampled():
 
 
 SMALL_SHAPES = [(1, 1), (2, 3), (3, 2), (1, 5), (5, 1), (2, 2, 3), (4,), (), (600, 2100), (257, 1025),
-                (3, 4097), (1000, 1032), (2, 3, 520, 264), (7, 1, 9), (1, 65536), (9000,)]
+                (3, 4097), (1000, 1032), (2, 3, 520, 264), (7, 1, 9), (1, 65536), (9000,),
+                # bf16: fused row-chunk pass, 8-warp configuration (2048 <= W <= 4096): a
+                # one-lane last column group, two chunks with a ragged one, B = 2 slices
+                (300, 2056), (2, 130, 4096),
+                # bf16: 16-warp configuration (4096 < W <= 16384): ragged chunks and
+                # sub-panels, the widest row; W = 16392 and W = 2040 stay tiled
+                (131, 4104), (67, 14336), (3, 16384), (5, 16392), (9, 2040)]
 FLAGS = [
     dict(),
     dict(beta1=0.9, weight_decay=0.1),
@@ -90,7 +96,7 @@ def test_small_shapes_all_flags(flags, grad_dtype):
 def test_misaligned_views_take_the_elementwise_path(carry):
     """Params/grads offset by one element from a 16-byte boundary cannot use
     the vector kernels; results must not change."""
-    shapes = [(64, 1024), (33, 520), (100,)]
+    shapes = [(64, 1024), (33, 520), (100,), (20, 2048), (9, 4104)]
     hp = dict(beta1=0.9)
     import oracle
     from parity_util import oracle_hp
@@ -125,10 +131,13 @@ def _run_steps(shapes, hp, t0, t1, params, states, grad_dtype=torch.float32):
     torch.cuda.synchronize()
 
 
-def test_bitwise_deterministic_and_resumable():
+@pytest.mark.parametrize("shapes,grad_dtype", [
+    ([(600, 2100), (300,), (8, 64, 40)], torch.float32),
+    ([(300, 2056), (131, 4104), (1000, 1032), (300,)], torch.bfloat16),  # fused, fused wide, tiled
+])
+def test_bitwise_deterministic_and_resumable(shapes, grad_dtype):
     """Two runs are bit-identical (fixed-order reductions, no atomics), and 5
     steps + copying params/state out and back + 5 steps equals 10 steps."""
-    shapes = [(600, 2100), (300,), (8, 64, 40)]
     hp = dict(beta1=0.9, weight_decay=0.01)
 
     def fresh():
@@ -136,18 +145,18 @@ def test_bitwise_deterministic_and_resumable():
         return params, init_state(params, beta1=0.9, param_sq_sum=False)
 
     pa, sa = fresh()
-    _run_steps(shapes, hp, 1, 11, pa, sa)
+    _run_steps(shapes, hp, 1, 11, pa, sa, grad_dtype)
     pb, sb = fresh()
-    _run_steps(shapes, hp, 1, 11, pb, sb)
+    _run_steps(shapes, hp, 1, 11, pb, sb, grad_dtype)
     for x, y in zip(pa, pb):
         assert torch.equal(x, y)
     pc, sc = fresh()
-    _run_steps(shapes, hp, 1, 6, pc, sc)
+    _run_steps(shapes, hp, 1, 6, pc, sc, grad_dtype)
     saved_p = [p.cpu().clone() for p in pc]
     saved_s = [{k: v.cpu().clone() for k, v in st.items()} for st in sc]
     pd = [p.cuda() for p in saved_p]
     sd = [{k: v.cuda() for k, v in st.items()} for st in saved_s]
-    _run_steps(shapes, hp, 6, 11, pd, sd)
+    _run_steps(shapes, hp, 6, 11, pd, sd, grad_dtype)
     for x, y in zip(pa, pd):
         assert torch.equal(x, y)
     for x, y in zip(sa, sd):
@@ -158,7 +167,7 @@ def test_bitwise_deterministic_and_resumable():
 def test_guard_bands_untouched():
     """Every tensor lives inside a larger buffer filled with a sentinel; after
     10 steps the bytes around each tensor are unchanged."""
-    shapes = [(517, 1029), (1024, 1032), (77,), (3, 5, 7)]
+    shapes = [(517, 1029), (1024, 1032), (77,), (3, 5, 7), (130, 2056), (67, 4104)]
     pad = 4096
     hp = dict(beta1=0.9)
 
