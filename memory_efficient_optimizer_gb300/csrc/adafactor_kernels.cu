@@ -275,6 +275,8 @@ __device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArg
   }
 }
 
+constexpr int kBatch1D = 8;  // elements per thread in flight in the 1D kernels
+
 // Full second moment (ndim < 2): v <- beta2 v + (1 - beta2)(g^2 + eps1) in
 // place, partial sum(g^2 / v) = sum(u^2), and sum(p^2) when needed.
 template <bool PSQ>
@@ -285,14 +287,29 @@ __device__ __forceinline__ void pass1_unfactored(const DevTensor& d, const StepA
   const float omb2 = static_cast<float>(1.0 - a.beta2);
   const float eps1 = static_cast<float>(a.eps1);
   float s = 0.f, ps = 0.f;
-  for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
-    const float x = load_g1(d.g, d.gdt, e);
-    const float vn = fmaf(b2, d.v[e], omb2 * fmaf(x, x, eps1));
-    d.v[e] = vn;
-    s += (x * x) / vn;
-    if (PSQ) {
-      const float y = d.p[e];
-      ps = fmaf(y, y, ps);
+  // kBatch1D elements per thread are loaded before any is used, so their
+  // loads are in flight together; the sums still run in element order.
+  for (int64_t e00 = e0 + threadIdx.x; e00 < e1; e00 += kBatch1D * kThreads) {
+    float x[kBatch1D], v[kBatch1D], y[kBatch1D];
+#pragma unroll
+    for (int k = 0; k < kBatch1D; ++k) {
+      const int64_t e = e00 + k * kThreads;
+      x[k] = v[k] = y[k] = 0.f;
+      if (e < e1) {
+        x[k] = load_g1(d.g, d.gdt, e);
+        v[k] = d.v[e];
+        if (PSQ) y[k] = d.p[e];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch1D; ++k) {
+      const int64_t e = e00 + k * kThreads;
+      if (e < e1) {
+        const float vn = fmaf(b2, v[k], omb2 * fmaf(x[k], x[k], eps1));
+        d.v[e] = vn;
+        s += (x[k] * x[k]) / vn;
+        if (PSQ) ps = fmaf(y[k], y[k], ps);
+      }
     }
   }
   const double S = block_sum(static_cast<double>(s), red);
@@ -354,6 +371,14 @@ __global__ void __launch_bounds__(kThreads) k_pass1_u(const __grid_constant__ St
   }
 }
 
+// Compensated (Kahan) fp32 accumulation: s += x with the running error in c.
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = x - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+}
+
 // ---- stats: EMA of row / column means -------------------------------------
 __device__ __forceinline__ void stats_row_item(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q, double* red) {
   const int64_t H = d.H;
@@ -362,68 +387,84 @@ __device__ __forceinline__ void stats_row_item(const DevTensor& d, const StepArg
   const float* rp = a.rowpart + d.rowpart + b * H;
   const int64_t stride = static_cast<int64_t>(d.B) * H;
   float* row = d.row + b * H;
-  const double inv_w = 1.0 / static_cast<double>(d.W);
-  double acc = 0.0;
+  const float w = static_cast<float>(d.W), eps1 = static_cast<float>(a.eps1);
+  const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
+  float acc = 0.f;  // at most kRowChunk / kThreads = 4 rows per thread
   for (int64_t i = i0 + threadIdx.x; i < i1; i += kThreads) {
-    double s = 0.0;
-    for (int c = 0; c < d.cb; ++c) s += static_cast<double>(rp[c * stride + i]);
-    const double mean = s * inv_w + a.eps1;
-    const float nr = static_cast<float>(a.beta2 * static_cast<double>(row[i]) + (1.0 - a.beta2) * mean);
+    float s = 0.f, c = 0.f;  // fp32 with Kahan compensation (see stats_col_item)
+    for (int k = 0; k < d.cb; ++k) kahan_add(s, c, rp[k * stride + i]);
+    const float mean = s / w + eps1;
+    const float nr = fmaf(b2, row[i], omb2 * mean);
     row[i] = nr;
-    acc += static_cast<double>(nr);
+    acc += nr;
   }
-  const double tot = block_sum(acc, red);
+  const double tot = block_sum(static_cast<double>(acc), red);
   if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + q] = tot;
 }
 
-// Column item: kColChunk (256) columns of one slice.  Warp w adds the row
-// blocks r = w, w + 8, ... of the column partials (lane l owns columns
-// l + 32m, m < 8, so every warp load is one coalesced 128-byte line), with
-// compensated (Kahan) fp32 sums; the 8 warp sums are then added in warp order
-// in double.  Fixed order throughout, so the result is deterministic.
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
-  const float y = x - c;
-  const float t = s + y;
-  c = (t - s) - y;
-  s = t;
-}
 
 // Column item: kColChunk (256) columns of one slice.  Warp w adds the row
-// blocks r = w, w + 8, ... of the column partials (lane l owns columns
-// l + 32m, m < 8, so every warp load is one coalesced 128-byte line), with
+// blocks r = w, w + 8, w + 16, ... of the column partials in that order, with
 // compensated (Kahan) fp32 sums; the 8 warp sums are then added in warp order
-// in double.  Fixed order throughout, so the result is deterministic.  For
-// fused tensors the weighted partials D_j are reduced the same way and the
-// chunk's sum_j D_j / col_j goes to dsum.
+// in double.  Fixed order throughout, so the result is deterministic.  With
+// W % 4 == 0 lane l owns the column quads 4l and 128 + 4l (16-byte loads) and
+// a warp has kStatsRows rows of loads in flight; otherwise lane l owns
+// columns l + 32m, m < 8 (scalar loads, two rows in flight).  For fused
+// tensors the weighted partials D_j are reduced the same way and the chunk's
+// sum_j D_j / col_j goes to dsum.
+constexpr int kStatsRows = 4;
+
+template <bool Q4>
 __device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q,
                                                float* part, double* red) {
   constexpr int kPer = kColChunk / 32;
+  constexpr int R = Q4 ? kStatsRows : 2;  // row blocks per warp and iteration
   const bool fused = d.kind == kFactoredRows;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t W = d.W;
   const int64_t c0 = q * kColChunk;
   const float* cp = a.colpart + d.colpart + b * d.prb * W;
   const float* dp = a.dpart + d.dpart + b * d.prb * W;
+  // The old column statistic, loaded now so that its latency overlaps the row loop.
+  const int64_t jt = c0 + threadIdx.x;
+  float* colp = d.col + b * W + jt;
+  const float col_old = (threadIdx.x < kColChunk && jt < W) ? *colp : 0.f;
+  // lane's column of slot m: quads (Q4) or strided singles
+  auto col_of = [&](int m) -> int64_t {
+    return Q4 ? c0 + (m >> 2) * 128 + 4 * lane + (m & 3) : c0 + lane + 32 * m;
+  };
   float s[kPer], comp[kPer], ds[kPer], dcomp[kPer];
 #pragma unroll
   for (int m = 0; m < kPer; ++m) s[m] = comp[m] = ds[m] = dcomp[m] = 0.f;
-  // Two row blocks per iteration: twice the loads in flight, same order.
-  for (int r = warp; r < d.prb; r += 2 * kWarps) {
-    const bool second = r + kWarps < d.prb;
-    float x[2][kPer], y[2][kPer];
+  for (int r0 = warp; r0 < d.prb; r0 += R * kWarps) {
+    float x[R][kPer], y[R][kPer];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t roff = static_cast<int64_t>(r + h * kWarps) * W;
+    for (int h = 0; h < R; ++h) {
+      const int r = r0 + h * kWarps;
+      const int64_t roff = static_cast<int64_t>(r) * W;
+      if (Q4) {
 #pragma unroll
-      for (int m = 0; m < kPer; ++m) {
-        const int64_t j = c0 + lane + 32 * m;
-        const bool ok = (h == 0 || second) && j < W;
-        x[h][m] = ok ? cp[roff + j] : 0.f;
-        y[h][m] = (fused && ok) ? dp[roff + j] : 0.f;
+        for (int e = 0; e < 2; ++e) {
+          const int64_t j = col_of(4 * e);
+          const bool ok = r < d.prb && j < W;
+          const float4 cv = ok ? *reinterpret_cast<const float4*>(cp + roff + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 dv = (fused && ok) ? *reinterpret_cast<const float4*>(dp + roff + j)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[h][4 * e] = cv.x; x[h][4 * e + 1] = cv.y; x[h][4 * e + 2] = cv.z; x[h][4 * e + 3] = cv.w;
+          y[h][4 * e] = dv.x; y[h][4 * e + 1] = dv.y; y[h][4 * e + 2] = dv.z; y[h][4 * e + 3] = dv.w;
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+          const int64_t j = col_of(m);
+          const bool ok = r < d.prb && j < W;
+          x[h][m] = ok ? cp[roff + j] : 0.f;
+          y[h][m] = (fused && ok) ? dp[roff + j] : 0.f;
+        }
       }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < R; ++h) {
 #pragma unroll
       for (int m = 0; m < kPer; ++m) {
         kahan_add(s[m], comp[m], x[h][m]);
@@ -434,31 +475,38 @@ __device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArg
   __syncthreads();  // part is free (previous item done reading it)
 #pragma unroll
   for (int m = 0; m < kPer; ++m) {
-    part[warp * kColChunk + lane + 32 * m] = s[m];
-    if (fused) part[(kWarps + warp) * kColChunk + lane + 32 * m] = ds[m];
+    const int cl = static_cast<int>(col_of(m) - c0);
+    part[warp * kColChunk + cl] = s[m];
+    if (fused) part[(kWarps + warp) * kColChunk + cl] = ds[m];
   }
   __syncthreads();
-  const int64_t j = c0 + threadIdx.x;
-  double term = 0.0;
-  if (threadIdx.x < kColChunk && j < W) {
-    double tot = 0.0;
+  // Per-column arithmetic in fp32 (this GPU's FP64 rate is a small fraction
+  // of its FP32 rate); the 8 warp sums are added with Kahan compensation.
+  float term = 0.f;
+  if (threadIdx.x < kColChunk && jt < W) {
+    float tot = 0.f, tc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += static_cast<double>(part[w * kColChunk + threadIdx.x]);
-    const double mean = tot / static_cast<double>(d.H) + a.eps1;
-    float* col = d.col + b * W + j;
-    const float cn = static_cast<float>(a.beta2 * static_cast<double>(*col) + (1.0 - a.beta2) * mean);
-    *col = cn;
+    for (int w = 0; w < kWarps; ++w) kahan_add(tot, tc, part[w * kColChunk + threadIdx.x]);
+    const float mean = tot / static_cast<float>(d.H) + static_cast<float>(a.eps1);
+    const float cn = fmaf(static_cast<float>(a.beta2), col_old, static_cast<float>(1.0 - a.beta2) * mean);
+    *colp = cn;
     if (fused) {
-      double dt = 0.0;
+      float dt = 0.f, dc = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) dt += static_cast<double>(part[(kWarps + w) * kColChunk + threadIdx.x]);
-      term = dt / static_cast<double>(cn);
+      for (int w = 0; w < kWarps; ++w) kahan_add(dt, dc, part[(kWarps + w) * kColChunk + threadIdx.x]);
+      term = dt / cn;
     }
   }
   if (fused) {
-    const double tot = block_sum(term, red);
+    const double tot = block_sum(static_cast<double>(term), red);
     if (threadIdx.x == 0) a.dsum[d.dsum + b * d.ncc + q] = tot;
   }
+}
+
+__device__ __forceinline__ void stats_col_any(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q,
+                                              float* part, double* red) {
+  if (d.W % 4 == 0) stats_col_item<true>(d, a, b, q, part, red);
+  else stats_col_item<false>(d, a, b, q, part, red);
 }
 
 __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ StepArgs a, const Range r) {
@@ -473,13 +521,13 @@ __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ Step
     const DevTensor d = a.tensors[member_tensor(r, m)];
     const int64_t local = u - pf[m];
     if (d.kind == kFactoredRows) {  // rows were updated by the fused pass 1
-      stats_col_item(d, a, local / d.ncc, local % d.ncc, part, red);
+      stats_col_any(d, a, local / d.ncc, local % d.ncc, part, red);
       continue;
     }
     const int64_t per_slice = d.nrc + d.ncc;
     const int64_t b = local / per_slice, k = local % per_slice;
     if (k < d.nrc) stats_row_item(d, a, b, k, red);
-    else stats_col_item(d, a, b, k - d.nrc, part, red);
+    else stats_col_any(d, a, b, k - d.nrc, part, red);
   }
 }
 
@@ -730,18 +778,35 @@ __device__ __forceinline__ void apply_unfactored(const DevTensor& d, const StepA
   const float wda = static_cast<float>(a.wd * a.alpha[t]);
   const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
   float psq = 0.f;
-  for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
-    const float x = load_g1(d.g, d.gdt, e);
-    float upd = coef * (x * rsqrtf(d.v[e]));
-    if (B1) {
-      const float mn = fmaf(b1, d.m1[e], omb1 * upd);
-      d.m1[e] = mn;
-      upd = mn;
+  for (int64_t e00 = e0 + threadIdx.x; e00 < e1; e00 += kBatch1D * kThreads) {
+    float x[kBatch1D], v[kBatch1D], m[kBatch1D], pv[kBatch1D];
+#pragma unroll
+    for (int k = 0; k < kBatch1D; ++k) {
+      const int64_t e = e00 + k * kThreads;
+      x[k] = m[k] = pv[k] = 0.f;
+      v[k] = 1.f;
+      if (e < e1) {
+        x[k] = load_g1(d.g, d.gdt, e);
+        v[k] = d.v[e];
+        if (B1) m[k] = d.m1[e];
+        pv[k] = d.p[e];
+      }
     }
-    const float p = d.p[e];
-    const float pn = fmaf(-wda, p, p - upd);
-    d.p[e] = pn;
-    if (PSQ) psq = fmaf(pn, pn, psq);
+#pragma unroll
+    for (int k = 0; k < kBatch1D; ++k) {
+      const int64_t e = e00 + k * kThreads;
+      if (e < e1) {
+        float upd = coef * (x[k] * rsqrtf(v[k]));
+        if (B1) {
+          const float mn = fmaf(b1, m[k], omb1 * upd);
+          d.m1[e] = mn;
+          upd = mn;
+        }
+        const float pn = fmaf(-wda, pv[k], pv[k] - upd);
+        d.p[e] = pn;
+        if (PSQ) psq = fmaf(pn, pn, psq);
+      }
+    }
   }
   if (PSQ) {
     const double tot = block_sum(static_cast<double>(psq), red);
