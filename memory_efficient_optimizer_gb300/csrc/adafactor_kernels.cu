@@ -1048,8 +1048,8 @@ __device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) 
 //
 // Staging: every lane copies its own 16-byte pieces of each sub-panel into
 // its own shared-memory slots with cp.async (completion tracked per thread by
-// commit/wait groups: no spin loop, no mbarrier).  A ring of kPanelStages
-// sub-panels per CTA keeps two sub-panels in flight while one is processed,
+// commit/wait groups: no spin loop, no mbarrier).  A ring of S sub-panels
+// per CTA keeps S - 1 sub-panels in flight while one is processed,
 // so the bytes in flight do not cost registers, and the second use of the
 // values (phase B) reads shared memory instead of L2 or HBM.  Since a lane
 // only ever reads the slots it filled, the staged data needs no barrier.
@@ -1067,21 +1067,25 @@ __device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) 
 // so g is read from HBM once here instead of twice.  Per chunk the warps
 // write C_j and D_j (column partials), and sum_r row_r goes to the row-chunk
 // sums (for mean(row)).
-constexpr int kPanelStages = 3;  // sub-panels resident per CTA
+
+// Configuration of the 2048 <= W <= 4096 class: warps, column groups per
+// lane, ring stages, CTAs per SM.
+constexpr int kRowsNW = 8, kRowsG = 2, kRowsS = 3, kRowsMinB = 2;
 
 // Shared-memory ring of the fused pass: per stage and warp, slot
 // ((rr * G + c) * kPieces + q) * 32 + lane holds 16 bytes (piece q of the 8
 // values of row rr, column group c, lane), so every warp-wide copy and read
 // touches 512 contiguous bytes.
-template <typename GT, int NW, int G> struct PanelCfg {
+template <typename GT, int NW, int G, int S> struct PanelCfg {
+  static constexpr int kStages = S;  // sub-panels resident per CTA (S - 1 in flight)
   static constexpr int kSubRows = 32 / NW;
   static constexpr int kPieces = static_cast<int>(sizeof(GT)) / 2;  // 16-byte pieces per 8 values
   static constexpr int kWarpBytes = kSubRows * G * kPieces * 32 * 16;
   static constexpr int kStageBytes = kWarpBytes * NW;
-  static constexpr size_t kRedOff = static_cast<size_t>(kPanelStages) * kStageBytes + sizeof(float) * 2 * 32;
-  static constexpr size_t kSmem = kRedOff + sizeof(double) * 32 + kPrefixBytes;
+  static constexpr size_t kRedOff = static_cast<size_t>(S) * kStageBytes + sizeof(float) * 2 * 32;
+  static constexpr size_t kSmem = kRedOff + sizeof(double) * 64 + kPrefixBytes;
   static_assert(kSubRows * NW == 32, "the row statistics take one (row, warp) share per lane");
-  static_assert(NW + 1 <= 32, "the CTA sum needs NW + 1 doubles");
+  static_assert(NW + 1 <= 64, "the CTA sum needs NW + 1 doubles");
 };
 
 // 16-byte asynchronous global -> shared copy (bypasses L1).
@@ -1089,15 +1093,19 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// Waits until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // This lane's copies of rows [q0, min(q0 + SR, q1)) into its slots of one
 // stage (dst: shared address of the lane's first slot in that stage).
-template <typename GT, int NW, int G>
+template <typename GT, int NW, int G, int S>
 __device__ __forceinline__ void panel_issue(uint32_t dst, const GT* gb, int32_t W, int32_t q0, int32_t q1, int warp,
                                             int lane) {
-  using C = PanelCfg<GT, NW, G>;
+  using C = PanelCfg<GT, NW, G, S>;
   constexpr int P = C::kPieces;
 #pragma unroll
   for (int rr = 0; rr < C::kSubRows; ++rr) {
@@ -1129,6 +1137,7 @@ __device__ __forceinline__ float reduce_scatter2(const float (&v)[2], int lane) 
   return k;
 }
 __device__ __forceinline__ float panel_row_shares(const float (&v)[4], int lane) { return reduce_scatter4(v, lane); }
+__device__ __forceinline__ float panel_row_shares(const float (&v)[1], int) { return warp_sum(v[0]); }
 __device__ __forceinline__ float panel_row_shares(const float (&v)[2], int lane) { return reduce_scatter2(v, lane); }
 
 // CTA-wide sum over NW warps in a fixed order (red: NW + 1 doubles).
@@ -1150,15 +1159,78 @@ __device__ __forceinline__ double panel_block_sum(double v, double* red) {
   return s;
 }
 
-template <typename GT, int NW, int G, bool PSQ>
-__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1)
+// Phase A of the fused pass over the staged values of one sub-panel: squares
+// into C_j and this warp's share of each row total (rp).  FULL: every row of
+// the sub-panel and every column group of the lane is in range, so no
+// per-element predicates.  x^2 is exact in fp32 for a bf16 x, so
+// fma(x, x, acc) equals acc + x * x.
+template <bool FULL, typename GT, int NW, int G, bool PSQ>
+__device__ __forceinline__ void panel_phase_a(const unsigned char* st, int32_t s0, int32_t s1, int32_t W, int warp,
+                                              int lane, const float* pb, float2 (&cacc)[G][4],
+                                              float (&rp)[32 / NW], float& psq) {
+  constexpr int SR = 32 / NW, P = PanelCfg<GT, NW, G, 3>::kPieces;
+#pragma unroll
+  for (int rr = 0; rr < SR; ++rr) {
+    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < G; ++c) {
+      const int32_t j = (c * NW + warp) * 256 + lane * 8;
+      if (FULL || (s0 + rr < s1 && j < W)) {
+        Raw<GT, 8> raw;
+        panel_read(raw, st + (rr * G + c) * P * 512);
+        float2 x[4];
+        widen2(raw, x);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          cacc[c][v] = __ffma2_rn(x[v], x[v], cacc[c][v]);
+          s2 = __ffma2_rn(x[v], x[v], s2);
+        }
+        if (PSQ) {
+          float y[8];
+          load_f<8>(y, pb + static_cast<int64_t>(s0 + rr) * W + j);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
+        }
+      }
+    }
+    rp[rr] = s2.x + s2.y;
+  }
+}
+
+// Phase B: g^2 / row_r into D_j (lane rr * NW holds 1 / row of row rr).
+template <bool FULL, typename GT, int NW, int G>
+__device__ __forceinline__ void panel_phase_b(const unsigned char* st, int32_t s0, int32_t s1, int32_t W, int warp,
+                                              int lane, float winv, float2 (&dacc)[G][4]) {
+  constexpr int SR = 32 / NW, P = PanelCfg<GT, NW, G, 3>::kPieces;
+#pragma unroll
+  for (int rr = 0; rr < SR; ++rr) {
+    const float wr = __shfl_sync(0xffffffffu, winv, rr * NW);
+    const float2 w2 = make_float2(wr, wr);
+#pragma unroll
+    for (int c = 0; c < G; ++c) {
+      const int32_t j = (c * NW + warp) * 256 + lane * 8;
+      if (FULL || (s0 + rr < s1 && j < W)) {
+        Raw<GT, 8> raw;
+        panel_read(raw, st + (rr * G + c) * P * 512);
+        float2 x[4];
+        widen2(raw, x);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dacc[c][v] = __ffma2_rn(__fmul2_rn(x[v], w2), x[v], dacc[c][v]);
+      }
+    }
+  }
+}
+
+template <typename GT, int NW, int G, int S, int MINB, bool PSQ>
+__global__ void __launch_bounds__(NW * 32, MINB)
     k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
-  using C = PanelCfg<GT, NW, G>;
+  using C = PanelCfg<GT, NW, G, S>;
   constexpr int SR = C::kSubRows, P = C::kPieces;
+  static_assert(S >= 2, "the ring needs the stage in use and one in flight");
   extern __shared__ __align__(16) unsigned char smem[];
-  float* part = reinterpret_cast<float*>(smem + kPanelStages * C::kStageBytes);  // [2][SR][NW]
+  float* part = reinterpret_cast<float*>(smem + S * C::kStageBytes);  // [2][SR][NW]
   double* red = reinterpret_cast<double*>(smem + C::kRedOff);
-  int32_t* pf = reinterpret_cast<int32_t*>(red + 32);
+  int32_t* pf = reinterpret_cast<int32_t*>(red + 64);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
@@ -1187,57 +1259,34 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1)
       for (int v = 0; v < 4; ++v) cacc[c][v] = dacc[c][v] = make_float2(0.f, 0.f);
     }
     float psq = 0.f, rsum = 0.f;
-    // Prologue: sub-panels 0 .. kPanelStages - 2 (one commit group each,
-    // empty past the chunk's end, so the group count stays in step).
+    // Prologue: sub-panels 0 .. S - 2 (one commit group each, empty past
+    // the chunk's end, so the group count stays in step).
 #pragma unroll
-    for (int k = 0; k < kPanelStages - 1; ++k) {
-      if (k < nsub) panel_issue<GT, NW, G>(mine_s + k * C::kStageBytes, gb, W, c0 + k * SR, c1, warp, lane);
+    for (int k = 0; k < S - 1; ++k) {
+      if (k < nsub) panel_issue<GT, NW, G, S>(mine_s + k * C::kStageBytes, gb, W, c0 + k * SR, c1, warp, lane);
       cp_async_commit();
     }
+    // Column groups of this warp all inside the row (warp-uniform).
+    const bool cols_full = ((G - 1) * NW + warp + 1) * 256 <= W;
     int stage = 0;
     for (int32_t k = 0; k < nsub; ++k) {
       const int32_t s0 = c0 + k * SR, s1 = min(c1, s0 + SR);
+      const bool full = cols_full && s1 - s0 == SR;
       const float row_old = (s0 + rl < s1) ? rowst[s0 + rl] : 0.f;
-      cp_async_wait_one_pending();  // groups up to sub-panel k are complete
+      cp_async_wait<S - 2>();  // groups up to sub-panel k are complete
       const unsigned char* st = mine + stage * C::kStageBytes;
       float* pk = part + (k & 1) * 32;
-      // A: squares into C_j, row shares
       float rp[SR];
-#pragma unroll
-      for (int rr = 0; rr < SR; ++rr) {
-        float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < G; ++c) {
-          const int32_t j = (c * NW + warp) * 256 + lane * 8;
-          if (s0 + rr < s1 && j < W) {
-            Raw<GT, 8> raw;
-            panel_read(raw, st + (rr * G + c) * P * 512);
-            float2 x[4];
-            widen2(raw, x);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const float2 q = __fmul2_rn(x[v], x[v]);
-              cacc[c][v] = __fadd2_rn(cacc[c][v], q);
-              s2 = __fadd2_rn(s2, q);
-            }
-            if (PSQ) {
-              float y[8];
-              load_f<8>(y, pb + static_cast<int64_t>(s0 + rr) * W + j);
-#pragma unroll
-              for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
-            }
-          }
-        }
-        rp[rr] = s2.x + s2.y;
-      }
+      if (full) panel_phase_a<true, GT, NW, G, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
+      else panel_phase_a<false, GT, NW, G, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
       const float tot = panel_row_shares(rp, lane);  // warp total of row rl
       if (lane % NW == 0) pk[rl * NW + warp] = tot;
       __syncthreads();
-      // Refill the stage of sub-panel k - 1 (every lane is past it) with k + kPanelStages - 1.
+      // Refill the stage of sub-panel k - 1 (every lane is past it) with k + S - 1.
       {
-        const int32_t kk = k + kPanelStages - 1;
-        const int fill = stage == 0 ? kPanelStages - 1 : stage - 1;
-        if (kk < nsub) panel_issue<GT, NW, G>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
+        const int32_t kk = k + S - 1;
+        const int fill = stage == 0 ? S - 1 : stage - 1;
+        if (kk < nsub) panel_issue<GT, NW, G, S>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
         cp_async_commit();
       }
       // Row statistics of the sub-panel, in every warp: lane l adds the
@@ -1246,30 +1295,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1)
 #pragma unroll
       for (int o = NW / 2; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
       const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
-      const float winv = 1.0f / rn;
+      const float winv = __frcp_rn(rn);  // correctly rounded 1 / rn
       if (warp == 0 && lane % NW == 0 && s0 + rl < s1) {
         rowst[s0 + rl] = rn;
         rsum += rn;
       }
-      // B: weighted squares into D_j from the same staged values
-#pragma unroll
-      for (int rr = 0; rr < SR; ++rr) {
-        const float wr = __shfl_sync(0xffffffffu, winv, rr * NW);
-        const float2 w2 = make_float2(wr, wr);
-#pragma unroll
-        for (int c = 0; c < G; ++c) {
-          const int32_t j = (c * NW + warp) * 256 + lane * 8;
-          if (s0 + rr < s1 && j < W) {
-            Raw<GT, 8> raw;
-            panel_read(raw, st + (rr * G + c) * P * 512);
-            float2 x[4];
-            widen2(raw, x);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) dacc[c][v] = __ffma2_rn(__fmul2_rn(x[v], w2), x[v], dacc[c][v]);
-          }
-        }
-      }
-      stage = stage == kPanelStages - 1 ? 0 : stage + 1;
+      if (full) panel_phase_b<true, GT, NW, G>(st, s0, s1, W, warp, lane, winv, dacc);
+      else panel_phase_b<false, GT, NW, G>(st, s0, s1, W, warp, lane, winv, dacc);
+      stage = stage == S - 1 ? 0 : stage + 1;
     }
     // column partials of the chunk
     float* cp = a.colpart + d.colpart + static_cast<int64_t>(b * d.prb + chunk) * W;
@@ -1477,13 +1510,13 @@ Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
 
 // Fused pass 1 (NW warps, G column groups per lane) and the bulk-copy apply
 // of the row-chunk classes.
-template <typename GT, int NW, int G>
+template <typename GT, int NW, int G, int S, int MINB>
 Inst pick_rows(KernelId k, bool psq_in, bool b1, bool psq_out) {
   Inst x;
   if (k == kKPass1) {
-    x.fn = psq_in ? k_pass1_panel<GT, NW, G, true> : k_pass1_panel<GT, NW, G, false>;
+    x.fn = psq_in ? k_pass1_panel<GT, NW, G, S, MINB, true> : k_pass1_panel<GT, NW, G, S, MINB, false>;
     x.threads = NW * 32;
-    x.smem = PanelCfg<GT, NW, G>::kSmem;
+    x.smem = PanelCfg<GT, NW, G, S>::kSmem;
   } else if (k == kKApply) {
     x = pick_f<GT, 8>(k, psq_in, b1, psq_out);
   }
@@ -1497,8 +1530,8 @@ Inst pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
     case kClsVecF32: return pick_f<float, 8>(k, psq_in, b1, psq_out);
     case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, b1, psq_out);
     case kClsScalarF32: return pick_f<float, 1>(k, psq_in, b1, psq_out);
-    case kClsRowsBF16: return pick_rows<__nv_bfloat16, 8, 2>(k, psq_in, b1, psq_out);
-    case kClsWideBF16: return pick_rows<__nv_bfloat16, 16, 4>(k, psq_in, b1, psq_out);
+    case kClsRowsBF16: return pick_rows<__nv_bfloat16, kRowsNW, kRowsG, kRowsS, kRowsMinB>(k, psq_in, b1, psq_out);
+    case kClsWideBF16: return pick_rows<__nv_bfloat16, 16, 4, 3, 1>(k, psq_in, b1, psq_out);
     case kClsUnfactored:
       x.smem = kRedBytes + kPrefixBytes;
       if (k == kKPass1) x.fn = psq_in ? k_pass1_u<true> : k_pass1_u<false>;
