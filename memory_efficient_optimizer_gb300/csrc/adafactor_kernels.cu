@@ -1101,19 +1101,21 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // This lane's copies of rows [q0, min(q0 + SR, q1)) into its slots of one
-// stage (dst: shared address of the lane's first slot in that stage).
-template <typename GT, int NW, int G, int S>
+// stage (dst: shared address of the lane's first slot in that stage).  FULL:
+// all SR rows and all of the lane's column groups are in range.
+template <bool FULL, typename GT, int NW, int G, int S>
 __device__ __forceinline__ void panel_issue(uint32_t dst, const GT* gb, int32_t W, int32_t q0, int32_t q1, int warp,
                                             int lane) {
   using C = PanelCfg<GT, NW, G, S>;
   constexpr int P = C::kPieces;
+  const GT* src0 = gb + static_cast<int64_t>(q0) * W + warp * 256 + lane * 8;
 #pragma unroll
   for (int rr = 0; rr < C::kSubRows; ++rr) {
 #pragma unroll
     for (int c = 0; c < G; ++c) {
-      const int32_t i = q0 + rr, j = (c * NW + warp) * 256 + lane * 8;
-      if (i < q1 && j < W) {
-        const GT* src = gb + static_cast<int64_t>(i) * W + j;
+      const int32_t j = (c * NW + warp) * 256 + lane * 8;
+      if (FULL || (q0 + rr < q1 && j < W)) {
+        const GT* src = src0 + static_cast<int64_t>(rr) * W + c * NW * 256;
 #pragma unroll
         for (int q = 0; q < P; ++q)
           cp_async16(dst + ((rr * G + c) * P + q) * 512, src + q * (16 / static_cast<int>(sizeof(GT))));
@@ -1263,7 +1265,7 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     // the chunk's end, so the group count stays in step).
 #pragma unroll
     for (int k = 0; k < S - 1; ++k) {
-      if (k < nsub) panel_issue<GT, NW, G, S>(mine_s + k * C::kStageBytes, gb, W, c0 + k * SR, c1, warp, lane);
+      if (k < nsub) panel_issue<false, GT, NW, G, S>(mine_s + k * C::kStageBytes, gb, W, c0 + k * SR, c1, warp, lane);
       cp_async_commit();
     }
     // Column groups of this warp all inside the row (warp-uniform).
@@ -1286,7 +1288,12 @@ __global__ void __launch_bounds__(NW * 32, MINB)
       {
         const int32_t kk = k + S - 1;
         const int fill = stage == 0 ? S - 1 : stage - 1;
-        if (kk < nsub) panel_issue<GT, NW, G, S>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
+        if (kk < nsub) {
+          if (cols_full && c0 + (kk + 1) * SR <= c1)
+            panel_issue<true, GT, NW, G, S>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
+          else
+            panel_issue<false, GT, NW, G, S>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
+        }
         cp_async_commit();
       }
       // Row statistics of the sub-panel, in every warp: lane l adds the
