@@ -21,6 +21,7 @@ import csv
 import hashlib
 import io
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -39,6 +40,7 @@ METRIC = "Adafactor step params/sec and effective HBM GB/s (% of 8 TB/s), Llama-
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "adafactor_kernels.cu")
+KERNEL_HDR = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "adafactor_internal.h")
 
 
 def dist_env():
@@ -218,14 +220,35 @@ def device_uuid(dev):
         return None
 
 
+# Sections of the kernel source (by their "// ---- <title>" banner) that hold
+# a launch slot's code; the traffic record of the slot stays valid while
+# these sections and the shared header are unchanged.
+KERNEL_SECTIONS = {
+    "k_apply": ("small helpers", "per-tile column factors", "apply: ", "vector path of apply", "apply (vector path)"),
+}
+
+
+def kernel_source_digest(kernel):
+    """sha256 of the source a launch slot's kernel is built from: the shared
+    header plus the slot's sections of the kernel file (the whole file for
+    slots without a section list)."""
+    text = open(KERNEL_SRC, encoding="utf-8").read()
+    titles = KERNEL_SECTIONS.get(kernel.split("[")[0])
+    if titles:
+        parts = re.split(r"(?m)^// ---- ", text)[1:]
+        text = "".join(p for p in parts if p.startswith(titles))
+    header = open(KERNEL_HDR, encoding="utf-8").read()
+    return hashlib.sha256((header + text).encode()).hexdigest()
+
+
 def traffic_record(kernel):
     """dram bytes per full launch from the committed ncu summary, or None when
-    the kernel source changed since the counters were taken."""
+    the kernel's source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()
+        sha = kernel_source_digest(kernel)
         entry = rec.get(kernel)
         if entry and entry.get("kernel_source_sha256") == sha:
             return float(entry["dram_bytes_per_full_launch"])
