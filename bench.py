@@ -34,7 +34,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from memory_efficient_optimizer_gb300 import binding, synth  # noqa: E402
-from memory_efficient_optimizer_gb300.optim import AdafactorStep, init_state  # noqa: E402
+from memory_efficient_optimizer_gb300.optim import AdafactorShardStep, AdafactorStep, init_state  # noqa: E402
 
 METRIC = "Adafactor step params/sec and effective HBM GB/s (% of 8 TB/s), Llama-3-8B shapes"
 FALLBACK_HBM_GBS = 6800.0
@@ -347,6 +347,44 @@ def run_e2e(args, wl, params, grads, states, step, t, world, dev):
     return out, t
 
 
+class EmulatedRowShards:
+    """The workload split by rows into R blocks, each stepped by its own
+    AdafactorShardStep (the row-sharded step of the article's Step 4), the R
+    "ranks" running in turn on this GPU and the all-reduces between the
+    library calls done as device-side sums of the R exchange buffers.  One
+    call = one step of the whole job."""
+
+    def __init__(self, params, grads, states_fn, nshards, hparams):
+        self.steps = []
+        for r in range(nshards):
+            ps, gs, rows = [], [], []
+            for p, g in zip(params, grads):
+                fact = p.dim() >= 2
+                n = p.shape[-2] if fact else p.numel()
+                a, b = (n * r) // nshards, (n * (r + 1)) // nshards
+                ps.append((p[..., a:b, :] if fact else p.reshape(-1)[a:b]).contiguous())
+                gs.append((g[..., a:b, :] if fact else g.reshape(-1)[a:b]).contiguous())
+                rows.append(n)
+            self.steps.append(AdafactorShardStep(ps, gs, states_fn(ps), rows, **hparams))
+        self.round_bytes = self.steps[0].round1.numel() * 8 + self.steps[0].round2.numel() * 8
+
+    def __call__(self, t):
+        for st in self.steps:
+            st.begin(t)
+        if len(self.steps) > 1:
+            tot = torch.stack([st.round1 for st in self.steps]).sum(0)
+            for st in self.steps:
+                st.round1.copy_(tot)
+        for st in self.steps:
+            st.middle(t)
+        if len(self.steps) > 1:
+            tot = torch.stack([st.round2 for st in self.steps]).sum(0)
+            for st in self.steps:
+                st.round2.copy_(tot)
+        for st in self.steps:
+            st.end(t)
+
+
 def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -357,8 +395,14 @@ def run_ours(args, world, rank, local):
     params = [synth.make_param(s, k, device=dev, std=wl.param_std) for k, s in enumerate(shapes)]
     grads = [synth.make_grad(s, k, 1, device=dev, std=wl.grad_std, dtype=wl.grad_dtype, kind=wl.grad_kind)
              for k, s in enumerate(shapes)]
-    states = init_state(params, beta1=beta1)
-    step = AdafactorStep(params, grads, states, **wl.hparams)
+    if args.shards:
+        # row-sharded step, every shard on this GPU (the whole tensors are freed)
+        step = EmulatedRowShards(params, grads, lambda ps: init_state(ps, beta1=beta1), args.shards, wl.hparams)
+        params = grads = states = None
+        torch.cuda.empty_cache()
+    else:
+        states = init_state(params, beta1=beta1)
+        step = AdafactorStep(params, grads, states, **wl.hparams)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
 
@@ -392,7 +436,7 @@ def run_ours(args, world, rank, local):
 
     # ---- end to end: host grads in, host params out, through the same API
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not args.shards:
         e2e, t = run_e2e(args, wl, params, grads, states, step, t, world, dev)
 
     grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
@@ -404,17 +448,20 @@ def run_ours(args, world, rank, local):
         if not kn:
             continue
         entry = {"ms_per_step": round(kms / args.steps, 4), "launches": kn}
+        # a slot's bytes are per step; with row shards one step is several launches
+        per = args.steps if args.shards else kn
         if name in slot_bytes and kms > 0:
-            entry["gbs"] = round(slot_bytes[name] / (kms / kn / 1e3) / 1e9, 1)
+            entry["gbs"] = round(slot_bytes[name] / (kms / per / 1e3) / 1e9, 1)
         per_kernel[name] = entry
     dom_name, (dom_ms, dom_n) = max(kernels.items(), key=lambda kv: kv[1][0])
     roofline = None
     if dom_n and dom_name in slot_bytes:
-        ach = slot_bytes[dom_name] / (dom_ms / dom_n / 1e3) / 1e9
+        dom_per = args.steps if args.shards else dom_n
+        ach = slot_bytes[dom_name] / (dom_ms / dom_per / 1e3) / 1e9
         roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
                     "traffic": traffic_record(dom_name), "algorithmic_bytes_per_launch": slot_bytes[dom_name],
-                    "avg_launch_ms": dom_ms / dom_n}
+                    "avg_launch_ms": dom_ms / dom_per}
     eff_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     clk = clocks.summary()
     out = {
@@ -426,7 +473,9 @@ def run_ours(args, world, rank, local):
                    "tensors": len(shapes), "param_dtype": "fp32",
                    "grad_dtype": "bf16" if grad_bytes == 2 else "fp32",
                    "hparams": {k: v for k, v in wl.hparams.items()} or "defaults",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": (f"row shards x{args.shards} on one GPU (ranks in turn, exchange summed on "
+                                   "the device)" if args.shards else
+                                   (f"replicas x{world}" if world > 1 else "single GPU")),
                    "l2": "inputs (params+grads) far larger than L2; no flush"},
         "effective_gbs": round(eff_gbs, 1),
         "pct_of_8tbs": round(100 * eff_gbs / NOMINAL_HBM_GBS, 2),
@@ -437,6 +486,8 @@ def run_ours(args, world, rank, local):
         "kernels": per_kernel,
         "roofline": roofline, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
     }
+    if args.shards:
+        out["row_shards"] = {"shards": args.shards, "exchange_bytes_per_rank_per_step": step.round_bytes}
     return out, (wl, n_params)
 
 
@@ -522,6 +573,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--readback-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shards", type=int, default=0,
+                    help="run the row-sharded step with this many row shards on one GPU (exchange on the device)")
     args = ap.parse_args()
     world, rank, local = dist_env()
 

@@ -193,6 +193,68 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
 adaf_status adafactor_step_noalloc(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
                                    int64_t step, const adaf_hparams* hp, void* stream);
 
+/* ---- Row-sharded step (tensor rows split over several ranks) ------------
+ * Step 4 of the article runs Adafactor on parameters split over a tensor-
+ * parallel / ZeRO group: the factored statistics and the RMS partial sums are
+ * summed over the group (all-reduce) before the update.  These three calls
+ * are that step for a rank that holds a contiguous block of rows of every
+ * tensor (a row shard); the sums over the group are the caller's collective
+ * (e.g. an NCCL or gloo all-reduce), made between the calls.  Everything that
+ * needs only the rank's own rows stays local: the row statistics, the update
+ * and the parameters.
+ *
+ * Per tensor k, the rank passes its shard as an ordinary adaf_tensor (shape
+ * with the rank's rows: [..., h_k, W] for ndim >= 2, [n_k] for ndim < 2, at
+ * least one row or element) and shards[k].global_rows = the rows per slice of
+ * the whole tensor (ndim >= 2) or its numel (ndim < 2).  States: exp_avg_sq_row,
+ * exp_avg, exp_avg_sq hold the rank's rows / elements; exp_avg_sq_col holds
+ * the whole [B*W] column statistic on every rank (every rank updates it
+ * identically); param_sq_sum carries the rank's own sum(param^2).  Every rank
+ * passes the same tensor order, the same leading dims and W, step and
+ * hyper-parameters.
+ *
+ *   adafactor_shard_begin   pass 1 over the rank's rows, then writes to
+ *                           round1 the rank's column sums of g^2, its sum of
+ *                           the updated row statistic per slice, and its
+ *                           sum(param^2).
+ *   caller                  round1 <- sum of round1 over the ranks (float64)
+ *   adafactor_shard_middle  column statistics, mean(row) and RMS(param) from
+ *                           the summed round1; writes to round2 the rank's
+ *                           sum(u^2) per tensor.
+ *   caller                  round2 <- sum of round2 over the ranks (float64)
+ *   adafactor_shard_end     the RMS clip from the summed round2, the update.
+ *
+ * The three calls of one step take the same arguments and the same workspace
+ * (which carries intermediate results from call to call: do not use it for
+ * anything else in between), on the same stream or with the order kept by
+ * the caller.  round1 / round2 are device buffers of float64 of the sizes
+ * adafactor_shard_sizes() gives (the same on every rank); they are read only
+ * after the caller's sum.  With one rank and no collective the three calls
+ * compute what adafactor_step() computes (sums in another order).
+ * Errors: those of adafactor_step(), plus ADAF_ERR_INVALID_ARGUMENT for NULL
+ * shards or round buffers, global_rows smaller than the shard's rows, or a
+ * shard with no row of some tensor. */
+typedef struct adaf_shard {
+    int64_t global_rows;
+} adaf_shard;
+
+/* Sizes for a row-sharded step over tensors[0..n) (host only, no CUDA call):
+ * the workspace (256-byte aligned start) and the two exchange buffers. */
+adaf_status adafactor_shard_sizes(const adaf_tensor* tensors, const adaf_shard* shards, int32_t n,
+                                  size_t* workspace_bytes, size_t* round1_bytes, size_t* round2_bytes);
+adaf_status adafactor_shard_begin(const adaf_tensor* tensors, const adaf_state* states,
+                                  const adaf_shard* shards, int32_t n, int64_t step,
+                                  const adaf_hparams* hp, void* workspace, size_t workspace_bytes,
+                                  double* round1, void* stream);
+adaf_status adafactor_shard_middle(const adaf_tensor* tensors, const adaf_state* states,
+                                   const adaf_shard* shards, int32_t n, int64_t step,
+                                   const adaf_hparams* hp, void* workspace, size_t workspace_bytes,
+                                   const double* round1, double* round2, void* stream);
+adaf_status adafactor_shard_end(const adaf_tensor* tensors, const adaf_state* states,
+                                const adaf_shard* shards, int32_t n, int64_t step,
+                                const adaf_hparams* hp, void* workspace, size_t workspace_bytes,
+                                const double* round2, void* stream);
+
 /* Device-side status of the most recent adafactor_step() that used this
  * workspace: waits on the stream, then stores the status word in *status.
  * 0 = no problem.  Bit 0 (ADAF_DEVICE_WAIT_TIMEOUT): a bounded wait inside a

@@ -7,7 +7,8 @@ a ``torch.optim.Optimizer`` wrapper.  There is no CPU fallback: without the
 built library every entry point raises.
 """
 from .binding import AdafactorError, library_path  # noqa: F401
-from .optim import Adafactor, AdafactorStep, adafactor_step, init_state, make_hparams  # noqa: F401
+from .optim import (Adafactor, AdafactorShardStep, AdafactorStep, adafactor_step,  # noqa: F401
+                    init_state, make_hparams)
 
-__all__ = ["Adafactor", "AdafactorStep", "AdafactorError", "adafactor_step", "init_state",
+__all__ = ["Adafactor", "AdafactorStep", "AdafactorShardStep", "AdafactorError", "adafactor_step", "init_state",
            "make_hparams", "library_path"]

@@ -28,6 +28,7 @@ EXPORTS = (
     "adafactor_step", "adafactor_device_status", "adafactor_last_error", "adafactor_release_cache",
     "adafactor_profile_enable", "adafactor_profile_read", "adafactor_num_kernels",
     "adafactor_kernel_name", "adafactor_step_noalloc", "adafactor_debug_stall_copies",
+    "adafactor_shard_sizes", "adafactor_shard_begin", "adafactor_shard_middle", "adafactor_shard_end",
 )
 
 
@@ -51,6 +52,10 @@ class adaf_hparams(ctypes.Structure):
                 ("weight_decay", ctypes.c_double), ("scale_parameter", ctypes.c_int32),
                 ("relative_step", ctypes.c_int32), ("warmup_init", ctypes.c_int32),
                 ("param_sq_sum_valid", ctypes.c_int32)]
+
+
+class adaf_shard(ctypes.Structure):
+    _fields_ = [("global_rows", ctypes.c_int64)]
 
 
 class AdafactorError(RuntimeError):
@@ -112,6 +117,17 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.adafactor_num_kernels.argtypes = []
         lib.adafactor_kernel_name.restype = ctypes.c_char_p
         lib.adafactor_kernel_name.argtypes = [ctypes.c_int32]
+        lib.adafactor_shard_sizes.restype = ctypes.c_int
+        lib.adafactor_shard_sizes.argtypes = [P(adaf_tensor), P(adaf_shard), ctypes.c_int32, P(ctypes.c_size_t),
+                                              P(ctypes.c_size_t), P(ctypes.c_size_t)]
+        shard_head = [P(adaf_tensor), P(adaf_state), P(adaf_shard), ctypes.c_int32, ctypes.c_int64,
+                      P(adaf_hparams), ctypes.c_void_p, ctypes.c_size_t]
+        lib.adafactor_shard_begin.restype = ctypes.c_int
+        lib.adafactor_shard_begin.argtypes = shard_head + [ctypes.c_void_p, ctypes.c_void_p]
+        lib.adafactor_shard_middle.restype = ctypes.c_int
+        lib.adafactor_shard_middle.argtypes = shard_head + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        lib.adafactor_shard_end.restype = ctypes.c_int
+        lib.adafactor_shard_end.argtypes = shard_head + [ctypes.c_void_p, ctypes.c_void_p]
         _lib = lib
         return lib
 
@@ -152,6 +168,35 @@ def adafactor_step_noalloc(tensors, states, n: int, step: int, hp: adaf_hparams,
     """The step with the library's fixed scratch area (no workspace argument)."""
     _check(load().adafactor_step_noalloc(tensors, states, int(n), int(step), ctypes.byref(hp),
                                          ctypes.c_void_p(stream)))
+
+
+def adafactor_shard_sizes(tensors, shards, n: int):
+    """(workspace bytes, round-1 bytes, round-2 bytes) of a row-sharded step."""
+    ws, r1, r2 = ctypes.c_size_t(0), ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().adafactor_shard_sizes(tensors, shards, int(n), ctypes.byref(ws), ctypes.byref(r1),
+                                        ctypes.byref(r2)))
+    return int(ws.value), int(r1.value), int(r2.value)
+
+
+def adafactor_shard_begin(tensors, states, shards, n: int, step: int, hp: adaf_hparams, workspace: int,
+                          workspace_bytes: int, round1: int, stream: int) -> None:
+    _check(load().adafactor_shard_begin(tensors, states, shards, int(n), int(step), ctypes.byref(hp),
+                                        ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes),
+                                        ctypes.c_void_p(round1), ctypes.c_void_p(stream)))
+
+
+def adafactor_shard_middle(tensors, states, shards, n: int, step: int, hp: adaf_hparams, workspace: int,
+                           workspace_bytes: int, round1: int, round2: int, stream: int) -> None:
+    _check(load().adafactor_shard_middle(tensors, states, shards, int(n), int(step), ctypes.byref(hp),
+                                         ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes),
+                                         ctypes.c_void_p(round1), ctypes.c_void_p(round2), ctypes.c_void_p(stream)))
+
+
+def adafactor_shard_end(tensors, states, shards, n: int, step: int, hp: adaf_hparams, workspace: int,
+                        workspace_bytes: int, round2: int, stream: int) -> None:
+    _check(load().adafactor_shard_end(tensors, states, shards, int(n), int(step), ctypes.byref(hp),
+                                      ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes),
+                                      ctypes.c_void_p(round2), ctypes.c_void_p(stream)))
 
 
 def adafactor_device_status(workspace: int, stream: int) -> int:

@@ -82,6 +82,8 @@ struct Plan {
   size_t off_cls_idx[meo::kNumClasses] = {}, off_cls_pf[3][meo::kNumClasses] = {};
   size_t off_alpha = 0, off_coef = 0, off_ssum = 0, off_mrow = 0, off_rowchunk = 0, off_dsum = 0;
   size_t off_spart = 0, off_ppart = 0, off_rowpart = 0, off_colpart = 0, off_dpart = 0, total_bytes = 0;
+  size_t off_dloc = 0;                       // row-sharded plans only
+  size_t round1_doubles = 0, round2_doubles = 0;  // row-sharded plans only
   bool any_factored = false;
 };
 
@@ -95,13 +97,16 @@ int32_t panel_rows(int64_t W) { return W <= meo::kMaxRowsW ? meo::kRowsChunk : m
 // query) only the shapes and dtypes are read; states and hp are not touched.
 // The workspace layout is the same either way: it reserves room for both
 // factored paths a tensor may take (which one depends on pointer alignment,
-// known only at step time).
+// known only at step time).  shards != NULL: every tensor is one row shard
+// of a larger tensor (global rows in shards[k]); the plan then also lays out
+// the exchange buffers and the shard's D_j region.
 adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
-                      const adaf_hparams* hp, bool full, Plan* plan) {
+                      const adaf_hparams* hp, bool full, Plan* plan, const adaf_shard* shards = nullptr) {
   if (n < 0) return fail(ADAF_ERR_INVALID_ARGUMENT, "n must be >= 0");
   if (n > 0 && tensors == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "tensors is NULL");
   int64_t tiles = 0, p1units = 0, items = 0, nmrow = 0, nrowchunk = 0, ndsum = 0;
   int64_t nrowpart = 0, ncolpart = 0, ndpart = 0;
+  int64_t nx1col = 0, nx1row = 0, ndloc = 0;
   plan->dev.clear();
   plan->dev.reserve(n);
   for (int32_t k = 0; k < n; ++k) {
@@ -119,7 +124,12 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
         return fail(ADAF_ERR_UNSUPPORTED, std::string(pre) + "more than 2^50 elements");
       numel *= t.shape[d];
     }
-    if (numel == 0) continue;
+    if (numel == 0) {
+      if (shards != nullptr)
+        return fail(ADAF_ERR_INVALID_ARGUMENT,
+                    std::string(pre) + "a row shard must hold at least one row of every tensor");
+      continue;
+    }
     const size_t gsz = t.grad_dtype == ADAF_BFLOAT16 ? 2 : 4;
     if (full) {
       if (t.param == nullptr || !aligned(t.param, 4))
@@ -225,6 +235,28 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       d.cb = static_cast<int32_t>(ntiles > INT32_MAX ? INT32_MAX : ntiles);
       d.kind = meo::kUnfactored;
     }
+    // Normalisation over the whole tensor, and the exchange layout of a row
+    // shard (identical on every shard: it depends on B and W only).
+    const int64_t local_rows = d.kind == meo::kUnfactored ? numel : d.H;
+    d.hg = local_rows;
+    d.ng = numel;
+    if (shards != nullptr) {
+      const int64_t gr = shards[k].global_rows;
+      if (gr < local_rows)
+        return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "global_rows is smaller than the shard's rows");
+      d.hg = gr;
+      d.ng = d.kind == meo::kUnfactored ? gr : static_cast<int64_t>(d.B) * gr * d.W;
+      if (d.kind != meo::kUnfactored) {
+        d.x1c = nx1col;
+        nx1col += static_cast<int64_t>(d.B) * d.W;
+        d.x1r = nx1row;  // relative until the column block's size is known
+        nx1row += d.B;
+      }
+      if (d.pr > 0) {  // may take the fused pass (reserved whatever the pointers' alignment)
+        d.dloc = ndloc;
+        ndloc += align_up(static_cast<int64_t>(d.B) * d.W, 4);
+      }
+    }
     d.ntiles = ntiles;
     d.tile0 = tiles;
     tiles += ntiles;
@@ -236,6 +268,16 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
     plan->dev.push_back(d);
   }
   const size_t nd = plan->dev.size();
+  if (shards != nullptr) {
+    // round 1: [column sums of every factored tensor][sum_i row_i per slice][sum(p^2) per tensor]
+    for (size_t k = 0; k < nd; ++k) {
+      DevTensor& d = plan->dev[k];
+      if (d.kind != meo::kUnfactored) d.x1r += nx1col;
+      d.x1p = nx1col + nx1row + static_cast<int64_t>(k);
+    }
+    plan->round1_doubles = static_cast<size_t>(nx1col + nx1row) + nd;
+    plan->round2_doubles = nd;
+  }
   plan->pf_tiles.assign(nd + 1, 0);
   plan->pf_items.assign(nd + 1, 0);
   for (int c = 0; c < meo::kNumClasses; ++c) {
@@ -293,6 +335,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
   region(&plan->off_rowpart, nrowpart * sizeof(float));
   region(&plan->off_colpart, ncolpart * sizeof(float));
   region(&plan->off_dpart, ndpart * sizeof(float));
+  if (shards != nullptr) region(&plan->off_dloc, ndloc * sizeof(float));
   plan->total_bytes = off;
   return ADAF_OK;
 }
@@ -392,17 +435,23 @@ void fill_header(unsigned char* h, const Plan& plan) {
 
 namespace meo {
 
-// The whole step: checks, plan, header upload, launch sequence.  Every
+// The whole step (phase 0) or one call of a row-sharded step (phases 1-3:
+// begin, middle, end): checks, plan, header upload, launch sequence.  Every
 // argument check runs before the first CUDA call.
-adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
-                      const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream,
-                      HeaderStaging staging) {
+adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, const adaf_shard* shards, int32_t n,
+                      int64_t step, const adaf_hparams* hp, void* workspace, size_t workspace_bytes,
+                      int phase, double* round1, double* round2, void* stream, HeaderStaging staging) {
   adaf_status st = check_hparams(hp);
   if (st != ADAF_OK) return st;
   if (step < 1) return fail(ADAF_ERR_INVALID_ARGUMENT, "step must be >= 1");
   if (n > 0 && states == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "states is NULL");
+  if (phase != 0 && n > 0 && shards == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "shards is NULL");
+  if ((phase == 1 || phase == 2) && (round1 == nullptr || !aligned(round1, 8)))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "round1 is NULL or not 8-byte aligned");
+  if ((phase == 2 || phase == 3) && (round2 == nullptr || !aligned(round2, 8)))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "round2 is NULL or not 8-byte aligned");
   Plan plan;
-  st = make_plan(tensors, states, n, hp, true, &plan);
+  st = make_plan(tensors, states, n, hp, true, &plan, phase != 0 ? shards : nullptr);
   if (st != ADAF_OK) return st;
   const size_t nd = plan.dev.size();
   if (nd == 0) return ADAF_OK;
@@ -511,6 +560,10 @@ adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int3
   a.psq_valid = (hp->scale_parameter && hp->param_sq_sum_valid) ? 1 : 0;
   a.want_psq_out = any_psq ? 1 : 0;
   a.stall_copies = g_stall_copies.load();
+  a.phase = phase;
+  a.round1 = round1;
+  a.round2 = round2;
+  a.dloc = phase != 0 ? reinterpret_cast<float*>(ws + plan.off_dloc) : nullptr;
 
   // One launch helper: optional profiling events around the launch.
   auto run = [&](KernelId k, int cls, auto&& launch) -> adaf_status {
@@ -552,6 +605,43 @@ adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int3
     return ADAF_OK;
   };
   const int nd_i = static_cast<int>(nd);
+  // Phase 0: everything.  Row-sharded: 1 = pass 1, this shard's statistics
+  // into round 1; 2 = column statistics from round 1, pass 2, this shard's
+  // sum(u^2) into round 2; 3 = clip from round 2, apply.
+  auto stats = [&]() -> adaf_status {
+    if (!plan.any_factored) return ADAF_OK;
+    const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
+    for (int32_t g0 = 0; g0 < nd_i; g0 += meo::kMaxGroup) {
+      const int32_t g1 = g0 + meo::kMaxGroup < nd_i ? g0 + meo::kMaxGroup : nd_i;
+      const int64_t units = plan.pf_items[g1] - plan.pf_items[g0];
+      if (units == 0) continue;
+      const int lim = grid_limit[meo::kKStats][0];
+      const int grid = static_cast<int>(units < lim ? units : lim);
+      const meo::Range r{pf_items_dev, nullptr, g0, g1};
+      adaf_status rs = run(meo::kKStats, 0, [&] { return meo::launch_stats(a, r, grid, s); });
+      if (rs != ADAF_OK) return rs;
+    }
+    return ADAF_OK;
+  };
+  auto per_tensor = [&](KernelId k) {
+    return run(k, 0, [&] { return meo::launch_per_tensor(k, a, nd_i, s); });
+  };
+  if (phase == 1) {
+    if ((st = stream_all(meo::kKPass1, false)) != ADAF_OK) return st;
+    if ((st = stats()) != ADAF_OK) return st;
+    return per_tensor(meo::kKScalars);
+  }
+  if (phase == 2) {
+    if ((st = stats()) != ADAF_OK) return st;
+    if ((st = per_tensor(meo::kKScalars)) != ADAF_OK) return st;
+    if ((st = stream_all(meo::kKPass2, true)) != ADAF_OK) return st;
+    return per_tensor(meo::kKClip);
+  }
+  if (phase == 3) {
+    if ((st = per_tensor(meo::kKClip)) != ADAF_OK) return st;
+    if ((st = stream_all(meo::kKApply, false)) != ADAF_OK) return st;
+    return any_psq ? per_tensor(meo::kKPsq) : ADAF_OK;
+  }
   if ((st = stream_all(meo::kKPass1, false)) != ADAF_OK) return st;
   if (plan.any_factored) {
     const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
@@ -577,6 +667,13 @@ adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int3
     if (st != ADAF_OK) return st;
   }
   return ADAF_OK;
+}
+
+adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
+                      const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream,
+                      HeaderStaging staging) {
+  return step_core(tensors, states, nullptr, n, step, hp, workspace, workspace_bytes, 0, nullptr, nullptr, stream,
+                   staging);
 }
 
 adaf_status set_last_error(adaf_status st, const char* msg) { return fail(st, msg); }
@@ -617,6 +714,41 @@ adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size
 adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states, int32_t n, int64_t step,
                            const adaf_hparams* hp, void* workspace, size_t workspace_bytes, void* stream) {
   return meo::step_impl(tensors, states, n, step, hp, workspace, workspace_bytes, stream, meo::kStagePinned);
+}
+
+adaf_status adafactor_shard_sizes(const adaf_tensor* tensors, const adaf_shard* shards, int32_t n,
+                                  size_t* workspace_bytes, size_t* round1_bytes, size_t* round2_bytes) {
+  if (workspace_bytes == nullptr || round1_bytes == nullptr || round2_bytes == nullptr)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "an output pointer is NULL");
+  if (n > 0 && shards == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "shards is NULL");
+  Plan plan;
+  adaf_status st = make_plan(tensors, nullptr, n, nullptr, false, &plan, shards);
+  if (st != ADAF_OK) return st;
+  *workspace_bytes = plan.total_bytes;
+  *round1_bytes = plan.round1_doubles * sizeof(double);
+  *round2_bytes = plan.round2_doubles * sizeof(double);
+  return ADAF_OK;
+}
+
+adaf_status adafactor_shard_begin(const adaf_tensor* tensors, const adaf_state* states, const adaf_shard* shards,
+                                  int32_t n, int64_t step, const adaf_hparams* hp, void* workspace,
+                                  size_t workspace_bytes, double* round1, void* stream) {
+  return meo::step_core(tensors, states, shards, n, step, hp, workspace, workspace_bytes, 1, round1, nullptr,
+                        stream, meo::kStagePinned);
+}
+
+adaf_status adafactor_shard_middle(const adaf_tensor* tensors, const adaf_state* states, const adaf_shard* shards,
+                                   int32_t n, int64_t step, const adaf_hparams* hp, void* workspace,
+                                   size_t workspace_bytes, const double* round1, double* round2, void* stream) {
+  return meo::step_core(tensors, states, shards, n, step, hp, workspace, workspace_bytes, 2,
+                        const_cast<double*>(round1), round2, stream, meo::kStagePinned);
+}
+
+adaf_status adafactor_shard_end(const adaf_tensor* tensors, const adaf_state* states, const adaf_shard* shards,
+                                int32_t n, int64_t step, const adaf_hparams* hp, void* workspace,
+                                size_t workspace_bytes, const double* round2, void* stream) {
+  return meo::step_core(tensors, states, shards, n, step, hp, workspace, workspace_bytes, 3, nullptr,
+                        const_cast<double*>(round2), stream, meo::kStagePinned);
 }
 
 const char* adafactor_last_error(void) { return g_last_error.c_str(); }

@@ -79,6 +79,15 @@ struct DevTensor {
   int64_t colpart;    // float offset of colpart [B][rb][W]
   int64_t rowchunk;   // double offset of row-chunk sums [B][nrc]
   int64_t mslot;      // double offset of mean(row) [B]
+  // Normalisation: rows and elements of the whole tensor (H and n unless the
+  // tensor is one row shard of a larger one).
+  int64_t hg;         // factored: rows per slice of the whole tensor; ndim < 2: its numel
+  int64_t ng;         // numel of the whole tensor
+  // Row-sharded steps only (0 otherwise).
+  int64_t x1c;        // double offset in round 1 of the column sums of g^2 [B][W]
+  int64_t x1r;        // double offset in round 1 of sum_i row_i per slice [B]
+  int64_t x1p;        // double offset in round 1 of sum(p^2)
+  int64_t dloc;       // float offset in the workspace of this shard's D_j [B][W] (fused)
 };
 static_assert(sizeof(DevTensor) % 8 == 0, "DevTensor must stay 8-byte packed");
 
@@ -121,6 +130,13 @@ struct StepArgs {
   int32_t want_psq_out;      // apply writes ppart for the carry
   int32_t* status;           // device status word (bit 0: a bounded wait gave up)
   int32_t stall_copies;      // testing hook: bulk-copy producers issue nothing
+  // Row-sharded step (phase 0 = the single-call step; 1, 2, 3 = the begin,
+  // middle and end calls).  round1/round2: the exchange buffers (sums over
+  // all shards in the phase after the one that packs them).
+  int32_t phase;
+  double* round1;
+  double* round2;
+  float* dloc;
 };
 
 // Device status bits (the word is reset by every step call).

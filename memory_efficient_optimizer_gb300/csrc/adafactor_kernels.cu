@@ -482,12 +482,30 @@ __device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArg
   __syncthreads();
   // Per-column arithmetic in fp32 (this GPU's FP64 rate is a small fraction
   // of its FP32 rate); the 8 warp sums are added with Kahan compensation.
+  if (a.phase == 1) {
+    // Row-sharded begin: this shard's column sums go to the exchange buffer
+    // (and D_j to the workspace); the column statistic waits for the sum
+    // over all shards.
+    if (threadIdx.x < kColChunk && jt < W) {
+      float tot = 0.f, tc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) kahan_add(tot, tc, part[w * kColChunk + threadIdx.x]);
+      a.round1[d.x1c + b * W + jt] = static_cast<double>(tot);
+      if (fused) {
+        float dt = 0.f, dc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) kahan_add(dt, dc, part[(kWarps + w) * kColChunk + threadIdx.x]);
+        a.dloc[d.dloc + b * W + jt] = dt;
+      }
+    }
+    return;
+  }
   float term = 0.f;
   if (threadIdx.x < kColChunk && jt < W) {
     float tot = 0.f, tc = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) kahan_add(tot, tc, part[w * kColChunk + threadIdx.x]);
-    const float mean = tot / static_cast<float>(d.H) + static_cast<float>(a.eps1);
+    const float mean = tot / static_cast<float>(d.hg) + static_cast<float>(a.eps1);
     const float cn = fmaf(static_cast<float>(a.beta2), col_old, static_cast<float>(1.0 - a.beta2) * mean);
     *colp = cn;
     if (fused) {
@@ -509,6 +527,29 @@ __device__ __forceinline__ void stats_col_any(const DevTensor& d, const StepArgs
   else stats_col_item<false>(d, a, b, q, part, red);
 }
 
+// Row-sharded middle: the column statistic from the column sums of g^2 over
+// all shards (round 1), and for fused tensors this shard's
+// sum_j D_j / col_j over the chunk's columns.
+__device__ __forceinline__ void stats_col_global(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q,
+                                                 double* red) {
+  const bool fused = d.kind == kFactoredRows;
+  const int64_t W = d.W;
+  const int64_t jt = q * kColChunk + threadIdx.x;
+  float term = 0.f;
+  if (threadIdx.x < kColChunk && jt < W) {
+    float* colp = d.col + b * W + jt;
+    const float tot = static_cast<float>(a.round1[d.x1c + b * W + jt]);
+    const float mean = tot / static_cast<float>(d.hg) + static_cast<float>(a.eps1);
+    const float cn = fmaf(static_cast<float>(a.beta2), *colp, static_cast<float>(1.0 - a.beta2) * mean);
+    *colp = cn;
+    if (fused) term = a.dloc[d.dloc + b * W + jt] / cn;
+  }
+  if (fused) {
+    const double tot = block_sum(static_cast<double>(term), red);
+    if (threadIdx.x == 0) a.dsum[d.dsum + b * d.ncc + q] = tot;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ StepArgs a, const Range r) {
   extern __shared__ __align__(16) unsigned char smem[];
   double* red = reinterpret_cast<double*>(smem);
@@ -521,13 +562,19 @@ __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ Step
     const DevTensor d = a.tensors[member_tensor(r, m)];
     const int64_t local = u - pf[m];
     if (d.kind == kFactoredRows) {  // rows were updated by the fused pass 1
-      stats_col_any(d, a, local / d.ncc, local % d.ncc, part, red);
+      if (a.phase == 2) stats_col_global(d, a, local / d.ncc, local % d.ncc, red);
+      else stats_col_any(d, a, local / d.ncc, local % d.ncc, part, red);
       continue;
     }
     const int64_t per_slice = d.nrc + d.ncc;
     const int64_t b = local / per_slice, k = local % per_slice;
-    if (k < d.nrc) stats_row_item(d, a, b, k, red);
-    else stats_col_any(d, a, b, k - d.nrc, part, red);
+    if (k < d.nrc) {
+      if (a.phase != 2) stats_row_item(d, a, b, k, red);  // rows are local to a shard
+    } else if (a.phase == 2) {
+      stats_col_global(d, a, b, k - d.nrc, red);
+    } else {
+      stats_col_any(d, a, b, k - d.nrc, part, red);
+    }
   }
 }
 
@@ -536,17 +583,46 @@ __global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ St
   __shared__ double red[16];
   const int t = blockIdx.x;
   const DevTensor d = a.tensors[t];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (a.phase == 1) {
+    // Row-sharded begin: this shard's sum(p^2) and sum_i row_i per slice go
+    // to the exchange buffer.
+    if (a.scale_parameter) {
+      double psq;
+      if (a.psq_valid) {
+        psq = *d.psq;
+      } else {
+        double acc = 0.0;
+        for (int64_t k = threadIdx.x; k < d.p1_n; k += kThreads) acc += a.ppart[d.p1_0 + k];
+        psq = block_sum(acc, red);
+      }
+      if (threadIdx.x == 0) a.round1[d.x1p] = psq;
+    } else if (threadIdx.x == 0) {
+      a.round1[d.x1p] = 0.0;
+    }
+    if (d.kind != kUnfactored) {
+      for (int64_t b = warp; b < d.B; b += kWarps) {
+        double sr = 0.0;
+        for (int64_t q = lane; q < d.nrc; q += 32) sr += a.rowchunk[d.rowchunk + b * d.nrc + q];
+        sr = warp_sum(sr);
+        if (lane == 0) a.round1[d.x1r + b] = sr;
+      }
+    }
+    return;
+  }
   double alpha = a.rho;
   if (a.scale_parameter) {
     double psq;
-    if (a.psq_valid) {
+    if (a.phase == 2) {
+      psq = a.round1[d.x1p];  // sum over all shards
+    } else if (a.psq_valid) {
       psq = *d.psq;
     } else {
       double acc = 0.0;
       for (int64_t k = threadIdx.x; k < d.p1_n; k += kThreads) acc += a.ppart[d.p1_0 + k];
       psq = block_sum(acc, red);
     }
-    const double r = sqrt(psq / static_cast<double>(d.n));
+    const double r = sqrt(psq / static_cast<double>(d.ng));
     alpha = a.rho * (r > a.eps2 ? r : a.eps2);
   }
   if (threadIdx.x == 0) a.alpha[t] = alpha;
@@ -555,13 +631,16 @@ __global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ St
     // sum_b mean(row_b) * sum_j D_bj / col_bj (slices in order within a warp,
     // then warps in order).
     const bool fused = d.kind == kFactoredRows;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     double su = 0.0;
     for (int64_t b = warp; b < d.B; b += kWarps) {
       double s = 0.0;
-      for (int64_t q = lane; q < d.nrc; q += 32) s += a.rowchunk[d.rowchunk + b * d.nrc + q];
-      s = warp_sum(s);
-      const double mb = s / static_cast<double>(d.H);
+      if (a.phase == 2) {
+        s = a.round1[d.x1r + b];  // sum over all shards
+      } else {
+        for (int64_t q = lane; q < d.nrc; q += 32) s += a.rowchunk[d.rowchunk + b * d.nrc + q];
+        s = warp_sum(s);
+      }
+      const double mb = s / static_cast<double>(d.hg);
       if (lane == 0) a.mrow[d.mslot + b] = mb;
       if (fused) {
         double ds = 0.0;
@@ -678,15 +757,21 @@ __global__ void __launch_bounds__(kThreads) k_clip(const __grid_constant__ StepA
   const int t = blockIdx.x;
   const DevTensor d = a.tensors[t];
   double S;
-  if (d.kind == kFactoredRows) {
+  if (a.phase == 3) {
+    S = a.round2[t];  // sum over all shards
+  } else if (d.kind == kFactoredRows) {
     S = a.ssum[t];
   } else {
     double acc = 0.0;
     for (int64_t k = threadIdx.x; k < d.ntiles; k += kThreads) acc += a.spart[d.tile0 + k];
     S = block_sum(acc, red);
   }
+  if (a.phase == 2) {  // row-sharded middle: this shard's sum(u^2) to round 2
+    if (threadIdx.x == 0) a.round2[t] = S;
+    return;
+  }
   if (threadIdx.x == 0) {
-    const double rms_u = sqrt(S / static_cast<double>(d.n));
+    const double rms_u = sqrt(S / static_cast<double>(d.ng));
     double div = rms_u / a.clip;
     if (!(div > 1.0)) div = 1.0;
     a.coef[t] = a.alpha[t] / div;

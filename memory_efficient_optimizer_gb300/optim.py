@@ -174,6 +174,76 @@ class AdafactorStep:
         self._versions = ([(p.data_ptr(), p._version) for p in self.params] if self._carry else None)
 
 
+class AdafactorShardStep(AdafactorStep):
+    """The step for one rank of a group that splits every tensor by rows
+    (the distributed step of the article's Step 4).
+
+    params / grads are this rank's row blocks: [..., h_k, W] of a tensor whose
+    slices have global_rows[k] rows, or n_k of global_rows[k] elements for
+    ndim < 2 (every rank at least one).  states come from init_state(params):
+    the row and full second moments are this rank's, the column statistic
+    [..., W] is the whole one and stays equal on every rank.  allreduce(t)
+    must sum a float64 CUDA tensor in place over the group (for example
+    ``torch.distributed.all_reduce``); None means a group of one.  Each call
+    is begin, allreduce(round 1), middle, allreduce(round 2), end."""
+
+    def __init__(self, params, grads, states, global_rows, allreduce=None, **hparams):
+        super().__init__(params, grads, states, **hparams)
+        if len(global_rows) != self.n:
+            raise ValueError("global_rows needs one entry per tensor")
+        self._shards = (B.adaf_shard * max(1, self.n))()
+        for k, (p, gr) in enumerate(zip(self.params, global_rows)):
+            if p.numel() == 0:
+                raise ValueError(f"tensor {k}: a shard must hold at least one row")
+            self._shards[k].global_rows = int(gr)
+        self.allreduce = allreduce
+        if self.n:
+            ws, r1, r2 = B.adafactor_shard_sizes(self._tensors, self._shards, self.n)
+            self.workspace_bytes = ws
+            self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device)
+            self.round1 = torch.zeros(r1 // 8, dtype=torch.float64, device=self.device)
+            self.round2 = torch.zeros(r2 // 8, dtype=torch.float64, device=self.device)
+
+    def _args(self, step, stream):
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        return ((self._tensors, self._states, self._shards, self.n, int(step), self._hp, _ptr(self.workspace),
+                 self.workspace_bytes), int(stream.cuda_stream))
+
+    # The three library calls of one step, for callers that run the exchange
+    # themselves: begin(t); sum round1 over the group; middle(t); sum round2;
+    # end(t).
+    def begin(self, step: int, stream: torch.cuda.Stream | None = None) -> None:
+        self._hp = make_hparams(**self.hparams, param_sq_sum_valid=self._carry_valid())
+        if self.n:
+            args, cs = self._args(step, stream)
+            B.adafactor_shard_begin(*args, _ptr(self.round1), cs)
+
+    def middle(self, step: int, stream: torch.cuda.Stream | None = None) -> None:
+        if self.n:
+            args, cs = self._args(step, stream)
+            B.adafactor_shard_middle(*args, _ptr(self.round1), _ptr(self.round2), cs)
+
+    def end(self, step: int, stream: torch.cuda.Stream | None = None) -> None:
+        if self.n:
+            args, cs = self._args(step, stream)
+            B.adafactor_shard_end(*args, _ptr(self.round2), cs)
+        self._versions = ([(p.data_ptr(), p._version) for p in self.params] if self._carry else None)
+
+    def __call__(self, step: int, stream: torch.cuda.Stream | None = None) -> None:
+        if stream is None and self.n:
+            stream = torch.cuda.current_stream(self.device)
+        self.begin(step, stream)
+        if self.allreduce is not None and self.n:
+            with torch.cuda.stream(stream):
+                self.allreduce(self.round1)
+        self.middle(step, stream)
+        if self.allreduce is not None and self.n:
+            with torch.cuda.stream(stream):
+                self.allreduce(self.round2)
+        self.end(step, stream)
+
+
 def adafactor_step(params, grads, states, step: int, lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0,
                    decay_rate=-0.8, beta1=None, weight_decay=0.0, scale_parameter=True, relative_step=True,
                    warmup_init=False, stream=None) -> None:

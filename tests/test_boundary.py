@@ -150,6 +150,51 @@ def test_valid_call_without_gpu_reports_a_cuda_error(lib):
     assert B.adafactor_last_error()
 
 
+def fake_shards(rows):
+    sh = (B.adaf_shard * len(rows))()
+    for k, r in enumerate(rows):
+        sh[k].global_rows = r
+    return sh
+
+
+def call_shard(fn, ts, ss, sh, n, rounds, step=1, ws=1 << 40, wsb=1 << 40):
+    hp = B.adafactor_default_hparams()
+    return getattr(B.load(), fn)(ts, ss, sh, n, step, ctypes.byref(hp), ctypes.c_void_p(ws), wsb,
+                                 *[ctypes.c_void_p(r) for r in rounds], None)
+
+
+def test_shard_sizes_and_argument_errors_before_any_cuda_call(lib):
+    """Row-sharded entry points: the exchange sizes depend on the leading dims
+    and W only (not on a shard's rows), and every argument error is reported
+    before the first CUDA call."""
+    shapes = [(300, 2056), (2, 130, 4096), (9000,)]
+    ts, ss = fake_list(shapes)
+    sh = fake_shards([900, 390, 27000])
+    ws, r1, r2 = B.adafactor_shard_sizes(ts, sh, 3)
+    assert r1 == 8 * (2056 + 2 * 4096 + 1 + 2 + 3) and r2 == 8 * 3
+    assert ws >= B.adafactor_workspace_size(ts, 3)
+    other, _ = fake_list([(17, 2056), (2, 1, 4096), (5,)])
+    assert B.adafactor_shard_sizes(other, sh, 3)[1:] == (r1, r2)
+    R1, R2 = 1 << 41, 1 << 42
+    inv = B.ADAF_ERR_INVALID_ARGUMENT
+    assert call_shard("adafactor_shard_begin", ts, ss, None, 3, [R1]) == inv
+    assert "shards" in B.adafactor_last_error()
+    assert call_shard("adafactor_shard_begin", ts, ss, sh, 3, [0]) == inv
+    assert "round1" in B.adafactor_last_error()
+    assert call_shard("adafactor_shard_middle", ts, ss, sh, 3, [R1, 0]) == inv
+    assert "round2" in B.adafactor_last_error()
+    assert call_shard("adafactor_shard_end", ts, ss, sh, 3, [R2 + 4]) == inv
+    assert "round2" in B.adafactor_last_error()
+    small = fake_shards([100, 390, 27000])  # fewer global rows than the shard holds
+    assert call_shard("adafactor_shard_begin", ts, ss, small, 3, [R1]) == inv
+    assert "global_rows" in B.adafactor_last_error()
+    empty, ess = fake_list([(0, 2056), (2, 130, 4096), (9000,)])
+    assert call_shard("adafactor_shard_begin", empty, ess, sh, 3, [R1]) == inv
+    assert "at least one row" in B.adafactor_last_error()
+    with pytest.raises(ValueError, match="global_rows"):
+        B.adafactor_shard_sizes(ts, small, 3)
+
+
 def test_kernel_names(lib):
     names = [B.adafactor_kernel_name(k) for k in range(B.adafactor_num_kernels())]
     assert len(names) == 25 and len(set(names)) == 25
