@@ -65,6 +65,11 @@ def _load():
             lib.oracle_adafactor_step.argtypes = [
                 dp, dp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), dp, dp, dp, dp,
                 ctypes.c_int64, ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
+            lib.oracle_adafactor_step_q8.restype = ctypes.c_int
+            lib.oracle_adafactor_step_q8.argtypes = [
+                dp, dp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), dp, dp, dp,
+                ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_float),
+                ctypes.c_int64, ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
             lib.oracle_check_hparams.restype = ctypes.c_int
             lib.oracle_check_hparams.argtypes = [ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
             lib.oracle_rho.restype = ctypes.c_double
@@ -119,10 +124,24 @@ def beta2(hp: HParams, t: int) -> float:
     return _load().oracle_beta2(ctypes.byref(c), int(t))
 
 
-class State:
-    """float64 optimizer state of one tensor, zero-initialised."""
+Q8_GROUP = 128  # values per group of the 8-bit first moment (along the last dim)
 
-    def __init__(self, shape, beta1: bool):
+
+def q8_groups(shape):
+    """(rows, groups per row) of the 8-bit first moment of a tensor."""
+    shape = tuple(int(s) for s in shape)
+    n = int(np.prod(shape)) if shape else 1
+    last = shape[-1] if len(shape) >= 2 else n
+    rows = n // last if last else 0
+    return rows, (last + Q8_GROUP - 1) // Q8_GROUP
+
+
+class State:
+    """float64 optimizer state of one tensor, zero-initialised.  q8: the first
+    moment is held as int8 codes and fp32 group scales (exp_avg_codes,
+    exp_avg_scales) instead of float64 exp_avg."""
+
+    def __init__(self, shape, beta1: bool, q8: bool = False):
         shape = tuple(int(s) for s in shape)
         self.shape = shape
         n = int(np.prod(shape)) if shape else 1
@@ -134,7 +153,14 @@ class State:
         else:
             self.row = self.col = None
             self.v = np.zeros(n, np.float64)
-        self.exp_avg = np.zeros(n, np.float64) if beta1 else None
+        self.exp_avg = np.zeros(n, np.float64) if beta1 and not q8 else None
+        self.q8 = bool(q8)
+        if q8:
+            rows, groups = q8_groups(shape)
+            self.exp_avg_codes = np.zeros(n, np.int8)
+            self.exp_avg_scales = np.zeros(rows * groups, np.float32)
+        else:
+            self.exp_avg_codes = self.exp_avg_scales = None
 
 
 def _ptr(a):
@@ -153,6 +179,17 @@ def step(p: np.ndarray, g: np.ndarray, state: State, t: int, hp: HParams) -> Non
     shape = (ctypes.c_int64 * max(1, len(state.shape)))(*state.shape) if state.shape else (ctypes.c_int64 * 1)(1)
     err = ctypes.create_string_buffer(256)
     c = hp._c()
+    if state.q8:
+        codes, scales = state.exp_avg_codes, state.exp_avg_scales
+        assert codes.dtype == np.int8 and scales.dtype == np.float32
+        assert codes.flags["C_CONTIGUOUS"] and scales.flags["C_CONTIGUOUS"]
+        rc = _load().oracle_adafactor_step_q8(
+            _ptr(p_flat), _ptr(g_flat), len(state.shape), shape, _ptr(state.row), _ptr(state.col),
+            _ptr(state.v), codes.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)),
+            scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), int(t), ctypes.byref(c), err, 256)
+        if rc != 0:
+            raise OracleError(err.value.decode())
+        return
     rc = _load().oracle_adafactor_step(
         _ptr(p_flat), _ptr(g_flat), len(state.shape), shape, _ptr(state.row), _ptr(state.col),
         _ptr(state.v), _ptr(state.exp_avg), int(t), ctypes.byref(c), err, 256)

@@ -39,6 +39,21 @@
  *   - a tensor with no elements is left untouched (nothing to update).
  *
  * Every quantity is float64; the step count t is 1-based.
+ *
+ * 8-bit first moment (oracle_adafactor_step_q8): the block-quantisation of
+ * the ms-swift GaLore / Q-GaLore article ("Q-GaLore" section: groups of 128
+ * values, a per-group scale absmax / 127, symmetric int8 codes) applied to
+ * exp_avg.  Readings:
+ *   - groups are 128 consecutive values along the last dim (a tensor with
+ *     ndim < 2 is one row); the last group of a row may be shorter;
+ *   - the stored state is the codes and one fp32 scale per group; the old
+ *     moment is code * scale (an fp32 product); the new moment
+ *     beta1 * old + (1 - beta1) * u is used unquantised for this step's
+ *     update, then quantised: amax = max |m| over the group (m rounded to
+ *     fp32), scale = amax / 127, code = rint(m * (127 / amax)) (fp32
+ *     arithmetic, ties to even; code and scale 0 for an all-zero group).
+ *     The rounding decision is taken in fp32, the precision of the stored
+ *     state and of the CUDA kernels.
  */
 #include <math.h>
 #include <stdint.h>
@@ -126,9 +141,13 @@ static double rms(const double* x, int64_t n) {
  *   t        1-based step number
  * Returns ORACLE_OK, or ORACLE_INVALID with a message in err.
  */
-int oracle_adafactor_step(double* p, const double* g, int32_t ndim, const int64_t* shape,
-                          double* row, double* col, double* v, double* exp_avg, int64_t t,
-                          const oracle_hparams* hp, char* err, int errlen) {
+/* The clipped, lr-scaled update u [N] of one step (before the first moment),
+ * updating the second-moment state in place; *alpha_out = the step's lr.
+ * *u_out is malloc'ed (NULL for an empty tensor). */
+static int compute_update(const double* p, const double* g, int32_t ndim, const int64_t* shape,
+                          double* row, double* col, double* v, int64_t t, const oracle_hparams* hp,
+                          double** u_out, double* alpha_out, int64_t* n_out, char* err, int errlen) {
+    *u_out = NULL;
     int rc = oracle_check_hparams(hp, err, errlen);
     if (rc != ORACLE_OK) return rc;
     if (t < 1) {
@@ -141,6 +160,7 @@ int oracle_adafactor_step(double* p, const double* g, int32_t ndim, const int64_
     }
     int64_t n = 1;
     for (int32_t k = 0; k < ndim; ++k) n *= shape[k];
+    *n_out = n;
     if (n == 0) return ORACLE_OK;
 
     /* Step 3 / Step 5: lr = rho_t, times max(eps[1], RMS(p)) when
@@ -212,6 +232,27 @@ int oracle_adafactor_step(double* p, const double* g, int32_t ndim, const int64_
     double clip_div = rms(u, n) / hp->clip_threshold;
     if (clip_div < 1.0) clip_div = 1.0;
     for (int64_t k = 0; k < n; ++k) u[k] = (u[k] / clip_div) * alpha;
+    *u_out = u;
+    *alpha_out = alpha;
+    return ORACLE_OK;
+}
+
+/* Decoupled weight decay, then the update u (Step 3 / the readings above). */
+static void apply_update(double* p, const double* u, int64_t n, double alpha, const oracle_hparams* hp) {
+    if (hp->weight_decay != 0.0) {
+        for (int64_t k = 0; k < n; ++k) p[k] = p[k] - hp->weight_decay * alpha * p[k];
+    }
+    for (int64_t k = 0; k < n; ++k) p[k] = p[k] - u[k];
+}
+
+int oracle_adafactor_step(double* p, const double* g, int32_t ndim, const int64_t* shape,
+                          double* row, double* col, double* v, double* exp_avg, int64_t t,
+                          const oracle_hparams* hp, char* err, int errlen) {
+    double* u = NULL;
+    double alpha = 0.0;
+    int64_t n = 0;
+    int rc = compute_update(p, g, ndim, shape, row, col, v, t, hp, &u, &alpha, &n, err, errlen);
+    if (rc != ORACLE_OK || n == 0) return rc;
 
     /* Step 3: with beta1, exp_avg <- beta1 exp_avg + (1 - beta1) u; u <- exp_avg. */
     if (hp->has_beta1) {
@@ -220,12 +261,69 @@ int oracle_adafactor_step(double* p, const double* g, int32_t ndim, const int64_
             u[k] = exp_avg[k];
         }
     }
-    /* Decoupled weight decay, then the update. */
-    if (hp->weight_decay != 0.0) {
-        for (int64_t k = 0; k < n; ++k) p[k] = p[k] - hp->weight_decay * alpha * p[k];
-    }
-    for (int64_t k = 0; k < n; ++k) p[k] = p[k] - u[k];
+    apply_update(p, u, n, alpha, hp);
+    free(u);
+    return ORACLE_OK;
+}
 
+/* Groups of the 8-bit first moment: 128 values along the last dim. */
+enum { ORACLE_Q8_GROUP = 128 };
+
+/* One step with the first moment held as int8 codes [N] and fp32 scales
+ * [rows * ceil(last_dim / 128)] (rows = N / last_dim; last_dim = N for
+ * ndim < 2).  Requires beta1.  Other arguments as oracle_adafactor_step. */
+int oracle_adafactor_step_q8(double* p, const double* g, int32_t ndim, const int64_t* shape,
+                             double* row, double* col, double* v, int8_t* codes, float* scales,
+                             int64_t t, const oracle_hparams* hp, char* err, int errlen) {
+    if (!hp->has_beta1) {
+        set_err(err, errlen, "the 8-bit first moment needs beta1");
+        return ORACLE_INVALID;
+    }
+    double* u = NULL;
+    double alpha = 0.0;
+    int64_t n = 0;
+    int rc = compute_update(p, g, ndim, shape, row, col, v, t, hp, &u, &alpha, &n, err, errlen);
+    if (rc != ORACLE_OK || n == 0) return rc;
+    const int64_t last = ndim >= 2 ? shape[ndim - 1] : n;
+    const int64_t rows = n / last;
+    const int64_t groups = (last + ORACLE_Q8_GROUP - 1) / ORACLE_Q8_GROUP;
+    float* mq = (float*)malloc((size_t)ORACLE_Q8_GROUP * sizeof(float));
+    if (!mq) {
+        free(u);
+        set_err(err, errlen, "out of host memory");
+        return ORACLE_NOMEM;
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t k = 0; k < groups; ++k) {
+            const int64_t j0 = k * ORACLE_Q8_GROUP;
+            const int64_t j1 = j0 + ORACLE_Q8_GROUP < last ? j0 + ORACLE_Q8_GROUP : last;
+            float* sc = &scales[r * groups + k];
+            float amax = 0.0f;
+            for (int64_t j = j0; j < j1; ++j) {
+                const int64_t e = r * last + j;
+                /* old moment: code * scale in fp32; new moment in float64 */
+                const float old = (float)codes[e] * (*sc);
+                const double m = hp->beta1 * (double)old + (1.0 - hp->beta1) * u[e];
+                u[e] = m;  /* this step's update uses the unquantised moment */
+                mq[j - j0] = (float)m;
+                const float a = fabsf(mq[j - j0]);
+                if (a > amax) amax = a;
+            }
+            if (amax > 0.0f) {
+                const float inv = 127.0f / amax;
+                *sc = amax / 127.0f;
+                for (int64_t j = j0; j < j1; ++j) {
+                    const float x = mq[j - j0] * inv;
+                    codes[r * last + j] = (int8_t)rintf(x);
+                }
+            } else {
+                *sc = 0.0f;
+                for (int64_t j = j0; j < j1; ++j) codes[r * last + j] = 0;
+            }
+        }
+    }
+    free(mq);
+    apply_update(p, u, n, alpha, hp);
     free(u);
     return ORACLE_OK;
 }

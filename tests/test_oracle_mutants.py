@@ -37,6 +37,12 @@ MUTANTS = {
     "RMS without the mean": ("return sqrt(s / (double)n);", "return sqrt(s);"),
     "update not scaled by lr": ("u[k] = (u[k] / clip_div) * alpha;", "u[k] = (u[k] / clip_div);"),
     "exp_avg not used as the update": ("u[k] = exp_avg[k];", "(void)0;"),
+    "8-bit codes floored": ("codes[r * last + j] = (int8_t)rintf(x);", "codes[r * last + j] = (int8_t)floorf(x);"),
+    "8-bit scale over 128": ("*sc = amax / 127.0f;", "*sc = amax / 128.0f;"),
+    "8-bit groups flat across rows": ("const int64_t last = ndim >= 2 ? shape[ndim - 1] : n;",
+                                      "const int64_t last = n;"),
+    "8-bit moment not used as the update": ("u[e] = m;  /* this step's update uses the unquantised moment */",
+                                            "(void)0;"),
 }
 
 
@@ -53,6 +59,7 @@ def test_pins_catch_mutant(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB_OVERRIDE=str(lib))
     res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                           os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_q8_pins.py"),
                           os.path.join(ROOT, "tests", "test_oracle_bruteforce.py")],
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert res.returncode != 0, f"mutant '{name}' survived the pins:\n{res.stdout[-2000:]}"
