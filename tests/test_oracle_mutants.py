@@ -31,8 +31,8 @@ MUTANTS = {
                                    "double cap = hp->warmup_init ? 1e-6 : 1e-2;"),
     "beta1 coefficients swapped": ("exp_avg[k] = hp->beta1 * exp_avg[k] + (1.0 - hp->beta1) * u[k];",
                                    "exp_avg[k] = (1.0 - hp->beta1) * exp_avg[k] + hp->beta1 * u[k];"),
-    "weight decay with rho": ("p[k] = p[k] - hp->weight_decay * alpha * p[k];",
-                              "p[k] = p[k] - hp->weight_decay * rho * p[k];"),
+    "weight decay not scaled by the lr": ("p[k] = p[k] - hp->weight_decay * alpha * p[k];",
+                                          "p[k] = p[k] - hp->weight_decay * p[k];"),
     "unfactored update without sqrt": ("u[k] = g[k] / sqrt(v[k]);", "u[k] = g[k] / v[k];"),
     "RMS without the mean": ("return sqrt(s / (double)n);", "return sqrt(s);"),
     "update not scaled by lr": ("u[k] = (u[k] / clip_div) * alpha;", "u[k] = (u[k] / clip_div);"),
