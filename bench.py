@@ -95,7 +95,15 @@ def tensor_class(shape, grad_bytes):
     return "vec_" + ("bf16" if grad_bytes == 2 else "f32")
 
 
-def algorithmic_bytes(shapes, grad_bytes, beta1):
+def first_moment_bytes(n, beta1, q8, group_scales=0):
+    """Read + write bytes of the first moment of n values: fp32 exp_avg, or
+    int8 codes plus one fp32 scale per group."""
+    if not beta1:
+        return 0
+    return 2 * (n + 4 * group_scales) if q8 else 8 * n
+
+
+def algorithmic_bytes(shapes, grad_bytes, beta1, q8=False):
     """Minimum bytes per step as the roofline of the method counts them (three
     reads of g: the statistics pass, the sum(u^2) pass and the update; p read +
     write; exp_avg read + write with beta1; the second-moment state read +
@@ -119,7 +127,8 @@ def algorithmic_bytes(shapes, grad_bytes, beta1):
             state_rw = 2 * 4 * n
             state_read = 4 * n
             p1 = grad_bytes * n + state_rw
-        m1 = 8 * n if beta1 else 0
+        last = int(s[-1]) if len(s) >= 2 else n
+        m1 = first_moment_bytes(n, beta1, q8, (n // last if last else 0) * ((last + 127) // 128))
         step += 3 * grad_bytes * n + 8 * n + m1 + state_rw
         impl += (2 if cls in FUSED_CLASSES or cls == "1d" else 3) * grad_bytes * n + 8 * n + m1 + state_rw
         slots[f"k_pass1[{cls}]"] = slots.get(f"k_pass1[{cls}]", 0) + p1
@@ -392,16 +401,18 @@ def run_ours(args, world, rank, local):
     shapes = [s for _, s in wl.shapes]
     n_params = wl.numel
     beta1 = wl.hparams.get("beta1")
+    q8 = bool(wl.hparams.get("exp_avg_int8"))
     params = [synth.make_param(s, k, device=dev, std=wl.param_std) for k, s in enumerate(shapes)]
     grads = [synth.make_grad(s, k, 1, device=dev, std=wl.grad_std, dtype=wl.grad_dtype, kind=wl.grad_kind)
              for k, s in enumerate(shapes)]
     if args.shards:
         # row-sharded step, every shard on this GPU (the whole tensors are freed)
-        step = EmulatedRowShards(params, grads, lambda ps: init_state(ps, beta1=beta1), args.shards, wl.hparams)
+        step = EmulatedRowShards(params, grads, lambda ps: init_state(ps, beta1=beta1, exp_avg_int8=q8), args.shards,
+                                 wl.hparams)
         params = grads = states = None
         torch.cuda.empty_cache()
     else:
-        states = init_state(params, beta1=beta1)
+        states = init_state(params, beta1=beta1, exp_avg_int8=q8)
         step = AdafactorStep(params, grads, states, **wl.hparams)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
@@ -440,7 +451,7 @@ def run_ours(args, world, rank, local):
         e2e, t = run_e2e(args, wl, params, grads, states, step, t, world, dev)
 
     grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
-    step_bytes, impl_bytes, slot_bytes = algorithmic_bytes(wl.shapes, grad_bytes, beta1 is not None)
+    step_bytes, impl_bytes, slot_bytes = algorithmic_bytes(wl.shapes, grad_bytes, beta1 is not None, q8)
     peak, peak_kind = measured_hbm_peak()
     launches = sum(v[1] for v in kernels.values())
     per_kernel = {}
@@ -569,7 +580,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b",
-                    choices=["llama3_8b", "llama3_8b_beta1", "llama_layer", "llama_layer_bf16", "edge", "tiny"])
+                    choices=["llama3_8b", "llama3_8b_beta1", "llama3_8b_beta1_int8", "llama_layer", "llama_layer_bf16",
+                             "edge", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--readback-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -98,6 +98,13 @@ typedef struct adaf_state {
     float* exp_avg_sq;
     float* exp_avg;
     double* param_sq_sum;
+    /* 8-bit first moment (adaf_hparams.exp_avg_int8; exp_avg is then unused):
+     *   exp_avg_codes   int8 [N], 4-byte aligned (16-byte for the vector path)
+     *   exp_avg_scales  fp32 [R * ceil(L / 128)], L = the last dim (N for
+     *                   ndim < 2), R = N / L: one scale per group of 128
+     *                   values along the last dim.  Zeroed before step 1. */
+    int8_t* exp_avg_codes;
+    float* exp_avg_scales;
 } adaf_state;
 
 /* Hyper-parameters (Step 3 of the article).  adafactor_default_hparams()
@@ -123,6 +130,15 @@ typedef struct adaf_hparams {
     int32_t relative_step;
     int32_t warmup_init;
     int32_t param_sq_sum_valid;
+    /* 1 = keep the beta1 first moment as int8 codes with one fp32 scale per
+     * group of 128 values along the last dim (the block quantisation of the
+     * ms-swift article's Q-GaLore section: scale = absmax / 127, symmetric
+     * codes).  Each step dequantises the old moment (code * scale), forms
+     * beta1 * old + (1 - beta1) * u, uses it unquantised for the update and
+     * stores it re-quantised: scale = amax / 127, code = rint(m * (127 / amax))
+     * in fp32, amax the group's max |m| (code and scale 0 if amax = 0).
+     * Requires has_beta1.  Default 0. */
+    int32_t exp_avg_int8;
 } adaf_hparams;
 
 /* Fills *hp with the article's defaults (Step 3).  hp must not be NULL. */
@@ -136,7 +152,8 @@ void adafactor_default_hparams(adaf_hparams* hp);
  *   !has_lr && !relative_step    "relative_step=False requires a manual lr"
  *   clip_threshold not finite or <= 0; has_lr with lr not finite or < 0;
  *   eps1, eps2 or weight_decay not finite or < 0; decay_rate not finite;
- *   has_beta1 with beta1 not in [0, 1). */
+ *   has_beta1 with beta1 not in [0, 1);
+ *   exp_avg_int8 without has_beta1. */
 adaf_status adafactor_validate(const adaf_hparams* hp);
 
 /* Bytes of device workspace adafactor_step() needs for this tensor list

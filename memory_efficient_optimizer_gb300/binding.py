@@ -41,7 +41,8 @@ class adaf_tensor(ctypes.Structure):
 class adaf_state(ctypes.Structure):
     _fields_ = [("exp_avg_sq_row", ctypes.c_void_p), ("exp_avg_sq_col", ctypes.c_void_p),
                 ("exp_avg_sq", ctypes.c_void_p), ("exp_avg", ctypes.c_void_p),
-                ("param_sq_sum", ctypes.c_void_p)]
+                ("param_sq_sum", ctypes.c_void_p),
+                ("exp_avg_codes", ctypes.c_void_p), ("exp_avg_scales", ctypes.c_void_p)]
 
 
 class adaf_hparams(ctypes.Structure):
@@ -51,7 +52,7 @@ class adaf_hparams(ctypes.Structure):
                 ("beta1", ctypes.c_double), ("has_beta1", ctypes.c_int32),
                 ("weight_decay", ctypes.c_double), ("scale_parameter", ctypes.c_int32),
                 ("relative_step", ctypes.c_int32), ("warmup_init", ctypes.c_int32),
-                ("param_sq_sum_valid", ctypes.c_int32)]
+                ("param_sq_sum_valid", ctypes.c_int32), ("exp_avg_int8", ctypes.c_int32)]
 
 
 class adaf_shard(ctypes.Structure):

@@ -58,6 +58,8 @@ adaf_status check_hparams(const adaf_hparams* hp) {
     return fail(ADAF_ERR_INVALID_ARGUMENT, "weight_decay must be finite and >= 0");
   if (hp->has_beta1 && !(hp->beta1 >= 0.0 && hp->beta1 < 1.0))
     return fail(ADAF_ERR_INVALID_ARGUMENT, "beta1 must be in [0, 1)");
+  if (hp->exp_avg_int8 && !hp->has_beta1)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "exp_avg_int8 needs beta1 (there is no first moment without it)");
   return ADAF_OK;
 }
 
@@ -157,7 +159,14 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
           return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "tensor with ndim < 2 needs exp_avg_sq");
         d.v = s.exp_avg_sq;
       }
-      if (hp->has_beta1) {
+      if (hp->has_beta1 && hp->exp_avg_int8) {
+        if (s.exp_avg_codes == nullptr || !aligned(s.exp_avg_codes, 4) || s.exp_avg_scales == nullptr ||
+            !aligned(s.exp_avg_scales, 4))
+          return fail(ADAF_ERR_INVALID_ARGUMENT,
+                      std::string(pre) + "exp_avg_int8 needs 4-byte aligned exp_avg_codes and exp_avg_scales");
+        d.mq = s.exp_avg_codes;
+        d.ms = s.exp_avg_scales;
+      } else if (hp->has_beta1) {
         if (s.exp_avg == nullptr || !aligned(s.exp_avg, 4))
           return fail(ADAF_ERR_INVALID_ARGUMENT, std::string(pre) + "beta1 is set but exp_avg is NULL");
         d.m1 = s.exp_avg;
@@ -180,6 +189,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       d.rb = static_cast<int32_t>(ceil_div(H, meo::kTileRows));
       d.cb = static_cast<int32_t>(ceil_div(W, meo::kTileCols));
       d.ncc = static_cast<int32_t>(ceil_div(W, meo::kColChunk));
+      d.qg = ceil_div(W, meo::kQ8Group);
       ntiles = B * d.rb * d.cb;
       // Path: vector (16-byte aligned rows) or element-wise; a vector tensor
       // with bf16 gradients and kMinRowsW <= W <= kMaxWideW takes the fused
@@ -190,7 +200,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       bool vec = vec_shape;
       if (full) {
         vec = vec_shape && aligned(t.param, 16) && aligned(t.grad, 16) &&
-              (!hp->has_beta1 || aligned(d.m1, 16));
+              (!hp->has_beta1 || (hp->exp_avg_int8 ? aligned(d.mq, 16) : aligned(d.m1, 16)));
         d.kind = !vec ? meo::kFactoredScalar : (rows_shape ? meo::kFactoredRows : meo::kFactoredVec);
       } else {
         d.kind = rows_shape ? meo::kFactoredRows : meo::kFactoredScalar;
@@ -234,6 +244,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       d.rb = 1;
       d.cb = static_cast<int32_t>(ntiles > INT32_MAX ? INT32_MAX : ntiles);
       d.kind = meo::kUnfactored;
+      d.qg = ceil_div(numel, meo::kQ8Group);
     }
     // Normalisation over the whole tensor, and the exchange layout of a row
     // shard (identical on every shard: it depends on B and W only).
@@ -561,6 +572,7 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
   a.want_psq_out = any_psq ? 1 : 0;
   a.stall_copies = g_stall_copies.load();
   a.phase = phase;
+  a.q8 = (hp->has_beta1 && hp->exp_avg_int8) ? 1 : 0;
   a.round1 = round1;
   a.round2 = round2;
   a.dloc = phase != 0 ? reinterpret_cast<float*>(ws + plan.off_dloc) : nullptr;

@@ -44,6 +44,7 @@ constexpr int kMinRowsW = 2048;   // narrower rows keep the tiled two-pass path
 constexpr int kMaxRowsW = 4096;   // 8 warps x 2 groups x 256 columns
 constexpr int kMaxWideW = 16384;  // 16 warps x 4 groups x 256 columns
 constexpr int kRowsChunk = 256;   // rows per work unit (rows configuration)
+constexpr int kQ8Group = 128;     // values per group of the 8-bit first moment
 constexpr int kWideChunk = 128;   // rows per work unit (wide configuration)
 
 enum GradType : int32_t { kGradF32 = 0, kGradBF16 = 1 };
@@ -88,6 +89,11 @@ struct DevTensor {
   int64_t x1r;        // double offset in round 1 of sum_i row_i per slice [B]
   int64_t x1p;        // double offset in round 1 of sum(p^2)
   int64_t dloc;       // float offset in the workspace of this shard's D_j [B][W] (fused)
+  // 8-bit first moment (beta1 with exp_avg_int8): int8 codes [N] and fp32
+  // scales, one per group of kQ8Group values along the last dim.
+  int8_t* mq;
+  float* ms;          // [rows * qg]
+  int64_t qg;         // groups per row: ceil(W / kQ8Group), ceil(n / kQ8Group) for ndim < 2
 };
 static_assert(sizeof(DevTensor) % 8 == 0, "DevTensor must stay 8-byte packed");
 
@@ -134,6 +140,7 @@ struct StepArgs {
   // middle and end calls).  round1/round2: the exchange buffers (sums over
   // all shards in the phase after the one that packs them).
   int32_t phase;
+  int32_t q8;                // beta1 moment as int8 codes + group scales (DevTensor::mq, ms)
   double* round1;
   double* round2;
   float* dloc;

@@ -778,11 +778,40 @@ __global__ void __launch_bounds__(kThreads) k_clip(const __grid_constant__ StepA
   }
 }
 
+// ---- 8-bit first moment ----------------------------------------------------
+// The ms-swift GaLore / Q-GaLore article's block quantisation ("Q-GaLore":
+// groups of 128, scale absmax / 127, symmetric int8 codes) applied to
+// exp_avg.  Groups are kQ8Group values along the last dim; a group's state is
+// its codes and one fp32 scale, value = code * scale.  After the moment EMA
+// the new moment is used unquantised for the update, and the group is
+// re-quantised: amax = max |m|, scale = amax / 127, code = rint(m * (127 /
+// amax)), all in fp32 (code 0 and scale 0 for an all-zero group).
+__device__ __forceinline__ float q8_value(uint32_t codes4, int v, float scale) {
+  const int c = static_cast<int>(static_cast<int8_t>((codes4 >> (8 * v)) & 0xffu));
+  return static_cast<float>(c) * scale;
+}
+// Warp maximum of non-negative floats: their bit patterns order like
+// unsigned integers, so one redux.sync.max.u32 does it.
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+// Codes of 4 values, packed little-endian; inv = 127 / amax (0 if amax = 0).
+__device__ __forceinline__ uint32_t q8_pack4(const float (&m)[4], float inv) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int v = 0; v < 4; ++v) w |= (static_cast<uint32_t>(__float2int_rn(__fmul_rn(m[v], inv))) & 0xffu) << (8 * v);
+  return w;
+}
+__device__ __forceinline__ float q8_inv(float amax) { return amax > 0.f ? 127.0f / amax : 0.f; }
+__device__ __forceinline__ float q8_scale(float amax) { return amax > 0.f ? amax / 127.0f : 0.f; }
+
 // ---- apply: p <- p - wd*alpha*p - update ----------------------------------
 // colf holds coef * col_j^-1/2 for the tile's columns (shared memory).
-template <typename GT, int VEC, bool B1, bool PSQ>
+template <typename GT, int VEC, bool B1, bool Q8, bool PSQ>
 __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArgs& a, int t, int64_t local, float* colf,
                                double* red) {
+  static_assert(!Q8 || (B1 && VEC == 1 && Layout<VEC>::CG * 32 % kQ8Group == 0),
+                "8-bit moment: element-wise layout, whole groups per load group");
   constexpr int CH = Layout<VEC>::CH, CG = Layout<VEC>::CG;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const TilePos tp = tile_pos(d, local);
@@ -793,7 +822,8 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
   const int64_t base = tp.b * H * W;
   const GT* gb = static_cast<const GT*>(d.g) + base;
   float* pb = d.p + base;
-  float* mb = B1 ? d.m1 + base : nullptr;
+  float* mb = (B1 && !Q8) ? d.m1 + base : nullptr;
+  int8_t* qb = Q8 ? d.mq + base : nullptr;
   const float* row = d.row + tp.b * H;
   const float m = static_cast<float>(a.mrow[d.mslot + tp.b]);
   const float coef = static_cast<float>(a.coef[t]);
@@ -815,13 +845,23 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
       Raw<GT, VEC> raw[CG];
       float pv[CG][VEC];
       float mv[B1 ? CG : 1][VEC];
+      constexpr int QPG = kQ8Group / 32;  // element-wise chunks per 8-bit group
+      float qs[Q8 ? CG / QPG : 1];        // group scales of this load group
 #pragma unroll
       for (int k = 0; k < CG; ++k) {
         const int64_t j = j0 + (kg + k) * 32 * VEC + lane * VEC;
         if (j < W) {
           load_raw(raw[k], gb + i * W + j);
           load_f<VEC>(pv[k], pb + i * W + j);
-          if (B1) load_f<VEC>(mv[B1 ? k : 0], mb + i * W + j);
+          if (B1 && !Q8) load_f<VEC>(mv[B1 ? k : 0], mb + i * W + j);
+          if (Q8) mv[B1 ? k : 0][0] = static_cast<float>(qb[i * W + j]);
+        }
+      }
+      if (Q8) {
+#pragma unroll
+        for (int q = 0; q < CG / QPG; ++q) {
+          const int64_t jg = j0 + (kg + q * QPG) * 32;
+          qs[Q8 ? q : 0] = jg < W ? d.ms[(tp.b * H + i) * d.qg + jg / kQ8Group] : 0.f;
         }
       }
 #pragma unroll
@@ -836,7 +876,8 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
           for (int v = 0; v < VEC; ++v) {
             float upd = (x[v] * r_i) * f[v];
             if (B1) {
-              mv[B1 ? k : 0][v] = fmaf(b1, mv[B1 ? k : 0][v], omb1 * upd);
+              const float old = Q8 ? mv[B1 ? k : 0][v] * qs[Q8 ? k / QPG : 0] : mv[B1 ? k : 0][v];
+              mv[B1 ? k : 0][v] = fmaf(b1, old, omb1 * upd);
               upd = mv[B1 ? k : 0][v];
             }
             const float pn = fmaf(-wda, pv[k][v], pv[k][v] - upd);
@@ -844,7 +885,29 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
             if (PSQ) psq = fmaf(pn, pn, psq);
           }
           store_f<VEC>(pb + i * W + j, pv[k]);
-          if (B1) store_f<VEC>(mb + i * W + j, mv[B1 ? k : 0]);
+          if (B1 && !Q8) store_f<VEC>(mb + i * W + j, mv[B1 ? k : 0]);
+        }
+      }
+      if (Q8) {
+        // re-quantise each group of QPG chunks: warp max of |m|, then codes
+#pragma unroll
+        for (int q = 0; q < CG / QPG; ++q) {
+          float amax = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < QPG; ++kk) {
+            const int k = q * QPG + kk;
+            if (j0 + (kg + k) * 32 + lane < W) amax = fmaxf(amax, fabsf(mv[B1 ? k : 0][0]));
+          }
+          amax = warp_max_nonneg(amax);
+          const float inv = q8_inv(amax);
+#pragma unroll
+          for (int kk = 0; kk < QPG; ++kk) {
+            const int k = q * QPG + kk;
+            const int64_t j = j0 + (kg + k) * 32 + lane;
+            if (j < W) qb[i * W + j] = static_cast<int8_t>(__float2int_rn(__fmul_rn(mv[B1 ? k : 0][0], inv)));
+          }
+          const int64_t jg = j0 + (kg + q * QPG) * 32;
+          if (lane == 0 && jg < W) d.ms[(tp.b * H + i) * d.qg + jg / kQ8Group] = q8_scale(amax);
         }
       }
     }
@@ -899,7 +962,71 @@ __device__ __forceinline__ void apply_unfactored(const DevTensor& d, const StepA
   }
 }
 
-template <typename GT, int VEC, bool B1, bool PSQ>
+// 1D tensors with the 8-bit moment: warp w takes the groups w, w + 8, ... of
+// the tile (lane l: values 4l .. 4l + 3 of a group), two groups per pass.
+template <bool PSQ>
+__device__ __forceinline__ void apply_unfactored_q8(const DevTensor& d, const StepArgs& a, int t, int64_t local,
+                                                    double* red) {
+  const int64_t e0 = local * kTile1D;
+  const int64_t e1 = min(d.n, e0 + kTile1D);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float coef = static_cast<float>(a.coef[t]);
+  const float wda = static_cast<float>(a.wd * a.alpha[t]);
+  const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
+  constexpr int GP = 2;  // groups per warp and pass
+  float psq = 0.f;
+  for (int64_t g0 = e0 / kQ8Group + warp * GP; g0 * kQ8Group < e1; g0 += kWarps * GP) {
+    float x[GP][4], v[GP][4], pv[GP][4], m[GP][4], sc[GP];
+#pragma unroll
+    for (int q = 0; q < GP; ++q) {
+      const int64_t gb = (g0 + q) * kQ8Group;
+      sc[q] = gb < e1 ? d.ms[g0 + q] : 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t e = gb + lane * 4 + k;
+        x[q][k] = pv[q][k] = m[q][k] = 0.f;
+        v[q][k] = 1.f;
+        if (e < e1) {
+          x[q][k] = load_g1(d.g, d.gdt, e);
+          v[q][k] = d.v[e];
+          pv[q][k] = d.p[e];
+          m[q][k] = static_cast<float>(d.mq[e]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < GP; ++q) {
+      const int64_t gb = (g0 + q) * kQ8Group;
+      float amax = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t e = gb + lane * 4 + k;
+        if (e < e1) {
+          const float upd = coef * (x[q][k] * rsqrtf(v[q][k]));
+          m[q][k] = fmaf(b1, m[q][k] * sc[q], omb1 * upd);
+          amax = fmaxf(amax, fabsf(m[q][k]));
+          const float pn = fmaf(-wda, pv[q][k], pv[q][k] - m[q][k]);
+          d.p[e] = pn;
+          if (PSQ) psq = fmaf(pn, pn, psq);
+        }
+      }
+      amax = warp_max_nonneg(amax);  // warp-uniform: gb < e1 for the whole warp or none
+      const float inv = q8_inv(amax);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t e = gb + lane * 4 + k;
+        if (e < e1) d.mq[e] = static_cast<int8_t>(__float2int_rn(__fmul_rn(m[q][k], inv)));
+      }
+      if (lane == 0 && gb < e1) d.ms[g0 + q] = q8_scale(amax);
+    }
+  }
+  if (PSQ) {
+    const double tot = block_sum(static_cast<double>(psq), red);
+    if (threadIdx.x == 0) a.ppart[d.tile0 + local] = tot;
+  }
+}
+
+template <typename GT, int VEC, bool B1, bool Q8, bool PSQ>
 __global__ void __launch_bounds__(kThreads, 2) k_apply_f(const __grid_constant__ StepArgs a, const Range r) {
   extern __shared__ __align__(16) unsigned char smem[];
   double* red = reinterpret_cast<double*>(smem);
@@ -911,11 +1038,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_apply_f(const __grid_constant__
     const int m = find_owner(pf, ng, u);
     const int t = member_tensor(r, m);
     const DevTensor d = a.tensors[t];
-    apply_factored<GT, VEC, B1, PSQ>(d, a, t, u - pf[m], colf, red);
+    apply_factored<GT, VEC, B1, Q8, PSQ>(d, a, t, u - pf[m], colf, red);
   }
 }
 
-template <bool B1, bool PSQ>
+template <bool B1, bool Q8, bool PSQ>
 __global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ StepArgs a, const Range r) {
   extern __shared__ __align__(16) unsigned char smem[];
   double* red = reinterpret_cast<double*>(smem);
@@ -926,7 +1053,8 @@ __global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ St
     const int m = find_owner(pf, ng, u);
     const int t = member_tensor(r, m);
     const DevTensor d = a.tensors[t];
-    apply_unfactored<B1, PSQ>(d, a, t, u - pf[m], red);
+    if (Q8) apply_unfactored_q8<PSQ>(d, a, t, u - pf[m], red);
+    else apply_unfactored<B1, PSQ>(d, a, t, u - pf[m], red);
   }
 }
 
@@ -1162,7 +1290,6 @@ constexpr int kRowsNW = 8, kRowsG = 2, kRowsS = 3, kRowsMinB = 2;
 // values of row rr, column group c, lane), so every warp-wide copy and read
 // touches 512 contiguous bytes.
 template <typename GT, int NW, int G, int S> struct PanelCfg {
-  static constexpr int kStages = S;  // sub-panels resident per CTA (S - 1 in flight)
   static constexpr int kSubRows = 32 / NW;
   static constexpr int kPieces = static_cast<int>(sizeof(GT)) / 2;  // 16-byte pieces per 8 values
   static constexpr int kWarpBytes = kSubRows * G * kPieces * 32 * 16;
@@ -1224,7 +1351,6 @@ __device__ __forceinline__ float reduce_scatter2(const float (&v)[2], int lane) 
   return k;
 }
 __device__ __forceinline__ float panel_row_shares(const float (&v)[4], int lane) { return reduce_scatter4(v, lane); }
-__device__ __forceinline__ float panel_row_shares(const float (&v)[1], int) { return warp_sum(v[0]); }
 __device__ __forceinline__ float panel_row_shares(const float (&v)[2], int lane) { return reduce_scatter2(v, lane); }
 
 // CTA-wide sum over NW warps in a fixed order (red: NW + 1 doubles).
@@ -1312,7 +1438,7 @@ template <typename GT, int NW, int G, int S, int MINB, bool PSQ>
 __global__ void __launch_bounds__(NW * 32, MINB)
     k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
   using C = PanelCfg<GT, NW, G, S>;
-  constexpr int SR = C::kSubRows, P = C::kPieces;
+  constexpr int SR = C::kSubRows;
   static_assert(S >= 2, "the ring needs the stage in use and one in flight");
   extern __shared__ __align__(16) unsigned char smem[];
   float* part = reinterpret_cast<float*>(smem + S * C::kStageBytes);  // [2][SR][NW]
@@ -1425,9 +1551,29 @@ __global__ void __launch_bounds__(NW * 32, MINB)
 template <typename GT, bool B1>
 using ApplyRing = Ring<GT, true, B1, 200 * 1024>;
 
-template <typename GT, bool B1, bool PSQ>
+// Codes (4 per lane and 128-column half-chunk: exactly one 8-bit group) and
+// this lane's group scale (lanes 0..7: the segment's 8 groups) of one row
+// segment, read straight from global memory one row ahead of their use.
+struct Q8Row {
+  uint32_t q[kTileCols / 128];
+  float s;
+};
+__device__ __forceinline__ void q8_load_row(Q8Row& out, const DevTensor& d, int64_t rowg, int64_t base_row,
+                                            int64_t j0, int lane) {
+  const int8_t* qb = d.mq + base_row + j0;
+#pragma unroll
+  for (int q = 0; q < kTileCols / 128; ++q) {
+    const int cl = q * 128 + lane * 4;
+    out.q[q] = (j0 + cl < d.W) ? *reinterpret_cast<const uint32_t*>(qb + cl) : 0u;
+  }
+  out.s = (lane < kTileCols / 128 && j0 + lane * 128 < d.W) ? d.ms[rowg * d.qg + j0 / 128 + lane] : 0.f;
+}
+
+template <typename GT, bool B1, bool Q8, bool PSQ>
 __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_constant__ StepArgs a, const Range r) {
-  using RG = ApplyRing<GT, B1>;
+  static_assert(!Q8 || B1, "the 8-bit moment needs beta1");
+  static_assert(kQ8Group == 128, "a 128-column half-chunk is one 8-bit group");
+  using RG = ApplyRing<GT, B1 && !Q8>;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* ring = smem;
   float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // coef * col_j^-1/2
@@ -1473,30 +1619,40 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_const
     consumer_sync();
     float psq = 0.f;
     bool ok = true;
+    Q8Row qnext;  // codes / scales of this warp's next row
+    if (Q8 && i0 + warp < i1) q8_load_row(qnext, d, tp.b * H + i0 + warp, base + (i0 + warp) * W, j0, lane);
     for (int64_t rs = i0; rs < i1 && ok; rs += kTmaConsumers, ++it) {
+      const int64_t i = rs + warp;
+      Q8Row qcur;
+      if (Q8) {
+        qcur = qnext;
+        const int64_t inext = i + kTmaConsumers;
+        if (inext < i1) q8_load_row(qnext, d, tp.b * H + inext, base + inext * W, j0, lane);
+      }
       const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
       if (!tma_acquire(&full[slot], ph, a, &stop)) {
         ok = false;
         break;
       }
-      const int64_t i = rs + warp;
       if (i < i1) {
         const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
         const float r_i = rowf[i - i0];
         float* pg = d.p + base + i * W + j0;
-        float* mg = B1 ? d.m1 + base + i * W + j0 : nullptr;
+        float* mg = (B1 && !Q8) ? d.m1 + base + i * W + j0 : nullptr;
 #pragma unroll
         for (int k = 0; k < kTileCols / 256; ++k) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int cl = k * 256 + h * 128 + lane * 4;
+            const float gs = Q8 ? __shfl_sync(0xffffffffu, qcur.s, k * 2 + h) : 0.f;  // group scale
+            float mq[4] = {0.f, 0.f, 0.f, 0.f};
             if (j0 + cl < W) {
               float x[4];
               quad_g<GT>(x, row, cl);
               const float4 f = *reinterpret_cast<const float4*>(colf + cl);
               float4 pv = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
               float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (B1) mv = *reinterpret_cast<const float4*>(row + RG::kG + RG::kP + cl * 4);
+              if (B1 && !Q8) mv = *reinterpret_cast<const float4*>(row + RG::kG + RG::kP + cl * 4);
               float* pp = &pv.x;
               float* mp = &mv.x;
               const float fv[4] = {f.x, f.y, f.z, f.w};
@@ -1504,15 +1660,25 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_const
               for (int v = 0; v < 4; ++v) {
                 float upd = (x[v] * r_i) * fv[v];
                 if (B1) {
-                  mp[v] = fmaf(b1, mp[v], omb1 * upd);
+                  const float old = Q8 ? q8_value(qcur.q[k * 2 + h], v, gs) : mp[v];
+                  mp[v] = fmaf(b1, old, omb1 * upd);
                   upd = mp[v];
+                  if (Q8) mq[v] = mp[v];
                 }
                 const float pn = fmaf(-wda, pp[v], pp[v] - upd);
                 pp[v] = pn;
                 if (PSQ) psq = fmaf(pn, pn, psq);
               }
               __stcs(reinterpret_cast<float4*>(pg + cl), pv);
-              if (B1) __stcs(reinterpret_cast<float4*>(mg + cl), mv);
+              if (B1 && !Q8) __stcs(reinterpret_cast<float4*>(mg + cl), mv);
+            }
+            if (Q8) {  // re-quantise the group (the whole warp, in or out of range)
+              float amax = fmaxf(fmaxf(fabsf(mq[0]), fabsf(mq[1])), fmaxf(fabsf(mq[2]), fabsf(mq[3])));
+              amax = warp_max_nonneg(amax);
+              if (j0 + cl < W)
+                *reinterpret_cast<uint32_t*>(d.mq + base + i * W + j0 + cl) = q8_pack4(mq, q8_inv(amax));
+              if (lane == 0 && j0 + k * 256 + h * 128 < W)
+                d.ms[(tp.b * H + i) * d.qg + (j0 + k * 256 + h * 128) / 128] = q8_scale(amax);
             }
           }
         }
@@ -1568,7 +1734,8 @@ struct Inst {
 };
 
 template <typename GT, int VEC>
-Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
+Inst pick_f(KernelId k, bool psq_in, int mom, bool psq_out) {
+  const bool b1 = mom != 0;
   Inst x;
   switch (k) {
     case kKPass1:
@@ -1582,17 +1749,21 @@ Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
     case kKApply:
       if constexpr (VEC == 8) {  // vector path: bulk-copy staged rows
         x.threads = kTmaThreads;
-        if (b1) {
-          x.fn = psq_out ? k_apply_tma<GT, true, true> : k_apply_tma<GT, true, false>;
+        if (mom == 2) {
+          x.fn = psq_out ? k_apply_tma<GT, true, true, true> : k_apply_tma<GT, true, true, false>;
+          x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
+        } else if (b1) {
+          x.fn = psq_out ? k_apply_tma<GT, true, false, true> : k_apply_tma<GT, true, false, false>;
           x.smem = tma_smem<ApplyRing<GT, true>>(kFactorBytes);
         } else {
-          x.fn = psq_out ? k_apply_tma<GT, false, true> : k_apply_tma<GT, false, false>;
+          x.fn = psq_out ? k_apply_tma<GT, false, false, true> : k_apply_tma<GT, false, false, false>;
           x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
         }
         return x;
       } else {
-        if (b1) x.fn = psq_out ? k_apply_f<GT, VEC, true, true> : k_apply_f<GT, VEC, true, false>;
-        else x.fn = psq_out ? k_apply_f<GT, VEC, false, true> : k_apply_f<GT, VEC, false, false>;
+        if (mom == 2) x.fn = psq_out ? k_apply_f<GT, VEC, true, true, true> : k_apply_f<GT, VEC, true, true, false>;
+        else if (b1) x.fn = psq_out ? k_apply_f<GT, VEC, true, false, true> : k_apply_f<GT, VEC, true, false, false>;
+        else x.fn = psq_out ? k_apply_f<GT, VEC, false, false, true> : k_apply_f<GT, VEC, false, false, false>;
         x.smem = kRedBytes + kPrefixBytes + kColfBytes;
         return x;
       }
@@ -1603,33 +1774,35 @@ Inst pick_f(KernelId k, bool psq_in, bool b1, bool psq_out) {
 // Fused pass 1 (NW warps, G column groups per lane) and the bulk-copy apply
 // of the row-chunk classes.
 template <typename GT, int NW, int G, int S, int MINB>
-Inst pick_rows(KernelId k, bool psq_in, bool b1, bool psq_out) {
+Inst pick_rows(KernelId k, bool psq_in, int mom, bool psq_out) {
   Inst x;
   if (k == kKPass1) {
     x.fn = psq_in ? k_pass1_panel<GT, NW, G, S, MINB, true> : k_pass1_panel<GT, NW, G, S, MINB, false>;
     x.threads = NW * 32;
     x.smem = PanelCfg<GT, NW, G, S>::kSmem;
   } else if (k == kKApply) {
-    x = pick_f<GT, 8>(k, psq_in, b1, psq_out);
+    x = pick_f<GT, 8>(k, psq_in, mom, psq_out);
   }
   return x;
 }
 
-Inst pick(KernelId k, TensorClass c, bool psq_in, bool b1, bool psq_out) {
+// mom: first moment none (0), fp32 exp_avg (1), 8-bit codes + scales (2).
+Inst pick(KernelId k, TensorClass c, bool psq_in, int mom, bool psq_out) {
   Inst x;
   switch (c) {
-    case kClsVecBF16: return pick_f<__nv_bfloat16, 8>(k, psq_in, b1, psq_out);
-    case kClsVecF32: return pick_f<float, 8>(k, psq_in, b1, psq_out);
-    case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, b1, psq_out);
-    case kClsScalarF32: return pick_f<float, 1>(k, psq_in, b1, psq_out);
-    case kClsRowsBF16: return pick_rows<__nv_bfloat16, kRowsNW, kRowsG, kRowsS, kRowsMinB>(k, psq_in, b1, psq_out);
-    case kClsWideBF16: return pick_rows<__nv_bfloat16, 16, 4, 3, 1>(k, psq_in, b1, psq_out);
+    case kClsVecBF16: return pick_f<__nv_bfloat16, 8>(k, psq_in, mom, psq_out);
+    case kClsVecF32: return pick_f<float, 8>(k, psq_in, mom, psq_out);
+    case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, mom, psq_out);
+    case kClsScalarF32: return pick_f<float, 1>(k, psq_in, mom, psq_out);
+    case kClsRowsBF16: return pick_rows<__nv_bfloat16, kRowsNW, kRowsG, kRowsS, kRowsMinB>(k, psq_in, mom, psq_out);
+    case kClsWideBF16: return pick_rows<__nv_bfloat16, 16, 4, 3, 1>(k, psq_in, mom, psq_out);
     case kClsUnfactored:
       x.smem = kRedBytes + kPrefixBytes;
       if (k == kKPass1) x.fn = psq_in ? k_pass1_u<true> : k_pass1_u<false>;
       if (k == kKApply) {
-        if (b1) x.fn = psq_out ? k_apply_u<true, true> : k_apply_u<true, false>;
-        else x.fn = psq_out ? k_apply_u<false, true> : k_apply_u<false, false>;
+        if (mom == 2) x.fn = psq_out ? k_apply_u<true, true, true> : k_apply_u<true, true, false>;
+        else if (mom == 1) x.fn = psq_out ? k_apply_u<true, false, true> : k_apply_u<true, false, false>;
+        else x.fn = psq_out ? k_apply_u<false, false, true> : k_apply_u<false, false, false>;
       }
       return x;
     default: return x;
@@ -1665,8 +1838,8 @@ int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err) {
     if (*err == cudaSuccess && b < per_sm) per_sm = b;
   };
   if (k == kKPass1 || k == kKPass2 || k == kKApply) {
-    for (int v = 0; v < 8; ++v) {
-      const Inst x = pick(k, c, v & 1, v & 2, v & 4);
+    for (int v = 0; v < 12; ++v) {
+      const Inst x = pick(k, c, v & 1, (v >> 1) % 3, v >= 6);
       visit(reinterpret_cast<const void*>(x.fn), x.threads, x.smem);
     }
   } else if (k == kKStats) {
@@ -1685,7 +1858,7 @@ cudaError_t launch_stream(KernelId k, TensorClass c, const StepArgs& a, const Ra
                           cudaStream_t s) {
   if (grid <= 0 || r.m_end <= r.m_begin) return cudaSuccess;
   const bool psq_in = a.scale_parameter && !a.psq_valid;
-  const Inst x = pick(k, c, psq_in, a.has_beta1 != 0, a.want_psq_out != 0);
+  const Inst x = pick(k, c, psq_in, a.has_beta1 ? (a.q8 ? 2 : 1) : 0, a.want_psq_out != 0);
   if (x.fn == nullptr) return cudaErrorInvalidValue;
   x.fn<<<grid, x.threads, x.smem, s>>>(a, r);
   return cudaGetLastError();

@@ -22,7 +22,7 @@ _GRAD_DTYPES = {torch.float32: B.ADAF_FLOAT32, torch.bfloat16: B.ADAF_BFLOAT16}
 
 def make_hparams(lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0, decay_rate=-0.8, beta1=None,
                  weight_decay=0.0, scale_parameter=True, relative_step=True, warmup_init=False,
-                 param_sq_sum_valid=False) -> B.adaf_hparams:
+                 exp_avg_int8=False, param_sq_sum_valid=False) -> B.adaf_hparams:
     """Builds and validates the hyper-parameter struct; invalid values raise
     ValueError with the library's message (e.g. "Cannot combine manual lr and
     relative_step=True options")."""
@@ -41,6 +41,7 @@ def make_hparams(lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0, decay_rate=-0.8
     hp.relative_step = int(bool(relative_step))
     hp.warmup_init = int(bool(warmup_init))
     hp.param_sq_sum_valid = int(bool(param_sq_sum_valid))
+    hp.exp_avg_int8 = int(bool(exp_avg_int8))
     B.adafactor_validate(hp)
     return hp
 
@@ -55,11 +56,28 @@ def factored_dims(shape):
     return lead, int(shape[-2]), int(shape[-1])
 
 
-def init_state(params: Sequence[torch.Tensor], beta1=None, param_sq_sum: bool = True) -> list:
+Q8_GROUP = 128  # values per group of the 8-bit first moment, along the last dim
+
+
+def q8_scale_count(shape) -> int:
+    """Group scales of the 8-bit first moment of a tensor: one per 128 values
+    along the last dim (a tensor with ndim < 2 is one row)."""
+    n = 1
+    for s in shape:
+        n *= int(s)
+    last = int(shape[-1]) if len(shape) >= 2 else n
+    rows = n // last if last else 0
+    return rows * ((last + Q8_GROUP - 1) // Q8_GROUP)
+
+
+def init_state(params: Sequence[torch.Tensor], beta1=None, param_sq_sum: bool = True,
+               exp_avg_int8: bool = False) -> list:
     """Zeroed optimizer state for each parameter (fp32, on the parameter's device):
     exp_avg_sq_row [*lead, H] and exp_avg_sq_col [*lead, W] for ndim >= 2, a full
-    exp_avg_sq otherwise, exp_avg when beta1 is set, and a float64 param_sq_sum
-    slot that carries sum(p^2) from one step to the next."""
+    exp_avg_sq otherwise, exp_avg when beta1 is set (or, with exp_avg_int8,
+    int8 exp_avg_codes [N] and fp32 exp_avg_scales, one per 128 values along the
+    last dim), and a float64 param_sq_sum slot that carries sum(p^2) from one
+    step to the next."""
     out = []
     for p in params:
         st = {}
@@ -69,7 +87,10 @@ def init_state(params: Sequence[torch.Tensor], beta1=None, param_sq_sum: bool = 
             st["exp_avg_sq_col"] = torch.zeros(shape[:-2] + shape[-1:], dtype=torch.float32, device=p.device)
         else:
             st["exp_avg_sq"] = torch.zeros(shape, dtype=torch.float32, device=p.device)
-        if beta1 is not None:
+        if beta1 is not None and exp_avg_int8:
+            st["exp_avg_codes"] = torch.zeros(shape, dtype=torch.int8, device=p.device)
+            st["exp_avg_scales"] = torch.zeros(max(1, q8_scale_count(shape)), dtype=torch.float32, device=p.device)
+        elif beta1 is not None:
             st["exp_avg"] = torch.zeros(shape, dtype=torch.float32, device=p.device)
         if param_sq_sum:
             st["param_sq_sum"] = torch.zeros(1, dtype=torch.float64, device=p.device)
@@ -115,6 +136,9 @@ class AdafactorStep:
                 if name == "param_sq_sum":
                     if t.dtype != torch.float64 or t.device != p.device or t.numel() < 1:
                         raise ValueError(f"tensor {k}: param_sq_sum must be a float64 CUDA tensor")
+                elif name == "exp_avg_codes":
+                    if not (t.dtype == torch.int8 and t.device == p.device and t.is_contiguous()):
+                        raise ValueError(f"tensor {k}: exp_avg_codes must be contiguous int8 on the param's device")
                 elif not (t.dtype == torch.float32 and t.device == p.device and t.is_contiguous()):
                     raise ValueError(f"tensor {k}: state '{name}' must be contiguous float32 on the param's device")
             fd = factored_dims(p.shape)
@@ -124,7 +148,12 @@ class AdafactorStep:
                         raise ValueError(f"tensor {k}: state '{name}' must have {size} elements")
             elif "exp_avg_sq" not in st or st["exp_avg_sq"].numel() != p.numel():
                 raise ValueError(f"tensor {k}: state 'exp_avg_sq' must have {p.numel()} elements")
-            if self.hparams.get("beta1") is not None and (
+            if self.hparams.get("beta1") is not None and self.hparams.get("exp_avg_int8"):
+                if ("exp_avg_codes" not in st or st["exp_avg_codes"].numel() != p.numel()
+                        or "exp_avg_scales" not in st or st["exp_avg_scales"].numel() < q8_scale_count(p.shape)):
+                    raise ValueError(f"tensor {k}: exp_avg_int8 needs 'exp_avg_codes' ({p.numel()}) and "
+                                     f"'exp_avg_scales' ({q8_scale_count(p.shape)}) states")
+            elif self.hparams.get("beta1") is not None and (
                     "exp_avg" not in st or st["exp_avg"].numel() != p.numel()):
                 raise ValueError(f"tensor {k}: beta1 is set, state 'exp_avg' must have {p.numel()} elements")
             td = self._tensors[k]
@@ -139,6 +168,8 @@ class AdafactorStep:
             sd.exp_avg_sq = _ptr(st.get("exp_avg_sq"))
             sd.exp_avg = _ptr(st.get("exp_avg"))
             sd.param_sq_sum = _ptr(st.get("param_sq_sum"))
+            sd.exp_avg_codes = _ptr(st.get("exp_avg_codes"))
+            sd.exp_avg_scales = _ptr(st.get("exp_avg_scales"))
         self.workspace_bytes = B.adafactor_workspace_size(self._tensors, n) if n else 0
         self.workspace = (torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=self.device)
                           if n else None)
@@ -246,13 +277,13 @@ class AdafactorShardStep(AdafactorStep):
 
 def adafactor_step(params, grads, states, step: int, lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0,
                    decay_rate=-0.8, beta1=None, weight_decay=0.0, scale_parameter=True, relative_step=True,
-                   warmup_init=False, stream=None) -> None:
+                   warmup_init=False, exp_avg_int8=False, stream=None) -> None:
     """One Adafactor step over a list of tensors (functional form).  States come
     from init_state(); the step number t is 1-based.  Marshals every call; use
     AdafactorStep to marshal once and call many times."""
     hparams = dict(lr=lr, eps=eps, clip_threshold=clip_threshold, decay_rate=decay_rate, beta1=beta1,
                    weight_decay=weight_decay, scale_parameter=scale_parameter, relative_step=relative_step,
-                   warmup_init=warmup_init)
+                   warmup_init=warmup_init, exp_avg_int8=exp_avg_int8)
     make_hparams(**hparams)
     AdafactorStep(params, grads, states, **hparams)(step, stream)
 
@@ -264,13 +295,14 @@ class Adafactor(torch.optim.Optimizer):
     launch sequence for all of its tensors)."""
 
     def __init__(self, params: Iterable, lr=None, eps=(1e-30, 1e-3), clip_threshold=1.0, decay_rate=-0.8,
-                 beta1=None, weight_decay=0.0, scale_parameter=True, relative_step=True, warmup_init=False):
+                 beta1=None, weight_decay=0.0, scale_parameter=True, relative_step=True, warmup_init=False,
+                 exp_avg_int8=False):
         make_hparams(lr=lr, eps=eps, clip_threshold=clip_threshold, decay_rate=decay_rate, beta1=beta1,
                      weight_decay=weight_decay, scale_parameter=scale_parameter, relative_step=relative_step,
-                     warmup_init=warmup_init)
+                     warmup_init=warmup_init, exp_avg_int8=exp_avg_int8)
         defaults = dict(lr=lr, eps=eps, clip_threshold=clip_threshold, decay_rate=decay_rate, beta1=beta1,
                         weight_decay=weight_decay, scale_parameter=scale_parameter, relative_step=relative_step,
-                        warmup_init=warmup_init)
+                        warmup_init=warmup_init, exp_avg_int8=exp_avg_int8)
         super().__init__(params, defaults)
         self._plans = {}
 
@@ -282,14 +314,14 @@ class Adafactor(torch.optim.Optimizer):
                 loss = closure()
         for gi, group in enumerate(self.param_groups):
             hp = {k: group[k] for k in ("lr", "eps", "clip_threshold", "decay_rate", "beta1", "weight_decay",
-                                        "scale_parameter", "relative_step", "warmup_init")}
+                                        "scale_parameter", "relative_step", "warmup_init", "exp_avg_int8")}
             by_step = {}
             for p in group["params"]:
                 if p.grad is None:
                     continue
                 st = self.state[p]
                 if not st:
-                    st.update(init_state([p], beta1=hp["beta1"])[0])
+                    st.update(init_state([p], beta1=hp["beta1"], exp_avg_int8=hp["exp_avg_int8"])[0])
                     st["step"] = 0
                 st["step"] += 1
                 by_step.setdefault(st["step"], []).append(p)

@@ -68,7 +68,7 @@ def _load():
             lib.oracle_adafactor_step_q8.restype = ctypes.c_int
             lib.oracle_adafactor_step_q8.argtypes = [
                 dp, dp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), dp, dp, dp,
-                ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_float),
+                ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_float), dp,
                 ctypes.c_int64, ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
             lib.oracle_check_hparams.restype = ctypes.c_int
             lib.oracle_check_hparams.argtypes = [ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
@@ -159,8 +159,9 @@ class State:
             rows, groups = q8_groups(shape)
             self.exp_avg_codes = np.zeros(n, np.int8)
             self.exp_avg_scales = np.zeros(rows * groups, np.float32)
+            self.moment = np.zeros(n, np.float64)  # the last step's unquantised moment
         else:
-            self.exp_avg_codes = self.exp_avg_scales = None
+            self.exp_avg_codes = self.exp_avg_scales = self.moment = None
 
 
 def _ptr(a):
@@ -186,7 +187,8 @@ def step(p: np.ndarray, g: np.ndarray, state: State, t: int, hp: HParams) -> Non
         rc = _load().oracle_adafactor_step_q8(
             _ptr(p_flat), _ptr(g_flat), len(state.shape), shape, _ptr(state.row), _ptr(state.col),
             _ptr(state.v), codes.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)),
-            scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), int(t), ctypes.byref(c), err, 256)
+            scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), _ptr(state.moment), int(t), ctypes.byref(c),
+            err, 256)
         if rc != 0:
             raise OracleError(err.value.decode())
         return

@@ -271,10 +271,12 @@ enum { ORACLE_Q8_GROUP = 128 };
 
 /* One step with the first moment held as int8 codes [N] and fp32 scales
  * [rows * ceil(last_dim / 128)] (rows = N / last_dim; last_dim = N for
- * ndim < 2).  Requires beta1.  Other arguments as oracle_adafactor_step. */
+ * ndim < 2).  Requires beta1.  moment_out [N] (may be NULL) receives the
+ * unquantised new moment.  Other arguments as oracle_adafactor_step. */
 int oracle_adafactor_step_q8(double* p, const double* g, int32_t ndim, const int64_t* shape,
                              double* row, double* col, double* v, int8_t* codes, float* scales,
-                             int64_t t, const oracle_hparams* hp, char* err, int errlen) {
+                             double* moment_out, int64_t t, const oracle_hparams* hp, char* err,
+                             int errlen) {
     if (!hp->has_beta1) {
         set_err(err, errlen, "the 8-bit first moment needs beta1");
         return ORACLE_INVALID;
@@ -305,6 +307,7 @@ int oracle_adafactor_step_q8(double* p, const double* g, int32_t ndim, const int
                 const float old = (float)codes[e] * (*sc);
                 const double m = hp->beta1 * (double)old + (1.0 - hp->beta1) * u[e];
                 u[e] = m;  /* this step's update uses the unquantised moment */
+                if (moment_out) moment_out[e] = m;
                 mq[j - j0] = (float)m;
                 const float a = fabsf(mq[j - j0]);
                 if (a > amax) amax = a;
