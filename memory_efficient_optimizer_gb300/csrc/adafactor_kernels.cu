@@ -205,6 +205,7 @@ __device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArg
     for (int rr = 0; rr < RPI; ++rr) rs[rr] = 0.f;
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
+      if (j0 + kg * 32 * VEC >= W) break;  // the rest of the tile is past the row's end (warp-uniform)
       Raw<GT, VEC> raw[RPI][CG];
 #pragma unroll
       for (int rr = 0; rr < RPI; ++rr) {
@@ -251,16 +252,18 @@ __device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArg
   // Column partials: the kWarps warps of the CTA covered disjoint rows of the
   // same columns; add their accumulators in warp order through shared memory.
   float* mine = colbuf + warp * kTileCols;
+  const int ncl = static_cast<int>(min(static_cast<int64_t>(kTileCols), W - j0));  // columns of this tile
 #pragma unroll
   for (int k = 0; k < CH; ++k) {
+    if (k * 32 * VEC >= ncl) break;
 #pragma unroll
     for (int v = 0; v < VEC; ++v) mine[k * 32 * VEC + lane * VEC + v] = cacc[k * VEC + v];
   }
   __syncthreads();
   float* colpart = a.colpart + d.colpart + (tp.b * d.rb + tp.r) * W;
-  for (int cl = threadIdx.x; cl < kTileCols; cl += kThreads) {
+  for (int cl = threadIdx.x; cl < ncl; cl += kThreads) {
     const int64_t j = j0 + cl;
-    if (j < W) {
+    {
       float s = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) s += colbuf[w * kTileCols + cl];
@@ -697,6 +700,7 @@ __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArg
     for (int rr = 0; rr < RPI; ++rr) ts[rr] = 0.f;
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
+      if (j0 + kg * 32 * VEC >= W) break;  // the rest of the tile is past the row's end (warp-uniform)
       Raw<GT, VEC> raw[RPI][CG];
 #pragma unroll
       for (int rr = 0; rr < RPI; ++rr) {
@@ -842,6 +846,7 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
     const float r_i = rsqrtf(row[i] / m);
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
+      if (j0 + kg * 32 * VEC >= W) break;  // the rest of the tile is past the row's end (warp-uniform)
       Raw<GT, VEC> raw[CG];
       float pv[CG][VEC];
       float mv[B1 ? CG : 1][VEC];
