@@ -1,23 +1,29 @@
 // Kernels of the GB300 Adafactor step.
 //
 // The step is bandwidth bound (a handful of flops per byte, no contraction),
-// so the kernels are built around streaming the gradient three times and the
-// parameter once (read + write) with coalesced 16-byte loads, persistent grids
-// sized to the SM count, and deterministic two-stage reductions: per-tile
+// so the kernels are built around streaming the gradient (twice for the
+// row-chunk classes, whose pass 1 also forms sum(u^2); three times for the
+// tiled classes) and the parameter once (read + write), with persistent grids
+// sized to the SM count and deterministic two-stage reductions: per-unit
 // partials written once, then summed in a fixed order (no float atomics, so
 // two runs give bit-identical results).
 //
-// Launch sequence of one step (all tensors of a group in every launch):
+// Launch sequence of one step (one launch per tensor class and kind):
 //   pass1   g (and p when RMS(p) must be recomputed) -> row/col partial sums
-//           of g^2; tensors with ndim < 2 update exp_avg_sq in place and emit
-//           partial sum(u^2).
+//           of g^2 (row-chunk classes: the updated row statistic and the
+//           column partials of g^2 / row_i as well); tensors with ndim < 2
+//           update exp_avg_sq in place and emit partial sum(u^2).
 //   stats   row/col partials -> EMA of row/col means (exp_avg_sq_row/col),
 //           plus per-chunk sums of the new row vector.
-//   scalars per tensor: alpha = rho * max(eps2, RMS(p)), mean(row) per slice.
-//   pass2   g -> partial sum(u^2) with u = g (row_i/m)^-1/2 col_j^-1/2.
+//   scalars per tensor: alpha = rho * max(eps2, RMS(p)), mean(row) per slice,
+//           sum(u^2) of the row-chunk classes.
+//   pass2   tiled classes: g -> partial sum(u^2), u = g (row_i/m)^-1/2 col_j^-1/2.
 //   clip    per tensor: coef = alpha / max(1, RMS(u) / clip_threshold).
-//   apply   g, p (exp_avg) -> p (exp_avg); partial sum(p_new^2).
+//   apply   g, p (exp_avg, or its 8-bit codes and scales) -> p (exp_avg);
+//           partial sum(p_new^2).
 //   psq     per tensor: sum(p_new^2) -> the optional carry slot.
+// The row-sharded step runs the same kernels in three calls (phases 1-3 in
+// StepArgs::phase), with the sums over the shards made by the caller.
 // Method: Colossal-AI distributed-optimizer article, Step 3 (factored rows/
 // cols, relative step, beta1), Step 4 (RMS), Step 5 (beta2t, clip, lr scale).
 #include <cuda_bf16.h>
@@ -1068,7 +1074,8 @@ __global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ St
 // producer streams the tile rows of g, p (and exp_avg) into a ring of
 // shared-memory stages of 8 rows with cp.async.bulk, one
 // copy per row segment, completion counted on the stage's "full" mbarrier.
-// Consumer warp w takes row w of every stage and releases the stage on its
+// Consumer warp w takes row w % kTmaRows of every stage, column block
+// w / kTmaRows of kTileCols / SPLIT, and releases the stage on its
 // "empty" mbarrier.  The bytes in flight are set by the ring depth, not by
 // registers.  In each 256-column chunk k, lane l handles the column quads
 // k*256 + 4l and k*256 + 128 + 4l, so shared-memory reads and global stores
@@ -1077,8 +1084,16 @@ __global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ St
 // kStatusWaitTimeout in the status word; the warp keeps meeting the consumer
 // barriers without touching the stages, so no warp is left waiting at one,
 // and all consumers leave together at the next tile boundary.
-constexpr int kTmaConsumers = kWarps;  // consumer warps = rows per stage
-constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
+constexpr int kTmaRows = kWarps;  // rows per stage
+// SPLIT consumer warps per row (column blocks of kTileCols / SPLIT): 1 for
+// the plain and fp32-moment apply, 2 for the 8-bit moment, whose per-group
+// re-quantisation needs more warps to hide its dependent arithmetic.
+template <int SPLIT> struct TmaCfg {
+  static constexpr int kConsumers = kTmaRows * SPLIT;
+  static constexpr int kThreads = (kConsumers + 1) * 32;
+  static_assert(kTileCols % (256 * SPLIT) == 0, "a consumer warp takes whole 256-column chunks");
+  static_assert(kConsumers <= 32, "consumer warp sums fit the reduction buffer");
+};
 
 template <typename GT, bool WP, bool WM, size_t kBudget>
 struct Ring {
@@ -1086,7 +1101,7 @@ struct Ring {
   static constexpr int kP = WP ? kTileCols * 4 : 0;
   static constexpr int kM = WM ? kTileCols * 4 : 0;
   static constexpr int kRow = kG + kP + kM;
-  static constexpr int kStage = kTmaConsumers * kRow;
+  static constexpr int kStage = kTmaRows * kRow;
   static constexpr int kStages = kBudget / kStage < 16 ? static_cast<int>(kBudget / kStage) : 16;
   static constexpr size_t kBytes = static_cast<size_t>(kStages) * kStage;
   static_assert(kStages >= 2, "stage ring too small");
@@ -1132,19 +1147,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+template <int NC>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NC * 32) : "memory");
 }
 
-// Shared prologue: prefix copy and barrier init (all kTmaThreads threads).
-template <int kStages>
+// Shared prologue: prefix copy and barrier init (all threads of the CTA;
+// NC consumer warps arrive on each "empty" barrier).
+template <int kStages, int NC>
 __device__ __forceinline__ int tma_setup(int32_t* pf, const Range& r, uint64_t* full, uint64_t* empty) {
   const int ng = r.m_end - r.m_begin;
-  for (int k = threadIdx.x; k <= ng; k += kTmaThreads) pf[k] = r.pf[r.m_begin + k];
+  for (int k = threadIdx.x; k <= ng; k += blockDim.x) pf[k] = r.pf[r.m_begin + k];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kTmaConsumers);
+      mbar_init(&empty[s], NC);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1167,13 +1184,13 @@ __device__ __forceinline__ void tma_produce(const StepArgs& a, const Range& r, c
     const int64_t j0 = tp.c * kTileCols;
     const uint32_t ncol = static_cast<uint32_t>(min(static_cast<int64_t>(kTileCols), d.W - j0));
     const int64_t base = tp.b * d.H * d.W;
-    for (int64_t rs = i0; rs < i1; rs += kTmaConsumers, ++it) {
+    for (int64_t rs = i0; rs < i1; rs += kTmaRows, ++it) {
       const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
       if (!mbar_wait(&empty[slot], ph ^ 1u)) {
         atomicOr(a.status, kStatusWaitTimeout);
         return;
       }
-      const int nrows = static_cast<int>(min(static_cast<int64_t>(kTmaConsumers), i1 - rs));
+      const int nrows = static_cast<int>(min(static_cast<int64_t>(kTmaRows), i1 - rs));
       const uint32_t per_row = ncol * static_cast<uint32_t>(sizeof(GT) + (RG::kP ? 4 : 0) + (RG::kM ? 4 : 0));
       mbar_arrive_expect_tx(&full[slot], nrows * per_row);
       unsigned char* st = ring + slot * RG::kStage;
@@ -1224,16 +1241,17 @@ __device__ __forceinline__ void quad_g(float (&x)[4], const unsigned char* row, 
   }
 }
 
-// Consumer-only deterministic CTA sum (warp xor-trees, then warps in order);
-// valid in consumer thread 0.
+// Consumer-only deterministic CTA sum over NC consumer warps (warp
+// xor-trees, then warps in order); valid in consumer thread 0.
+template <int NC>
 __device__ __forceinline__ double consumer_sum(float v, double* red) {
   const float w = warp_sum(v);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = static_cast<double>(w);
-  consumer_sync();
+  consumer_sync<NC>();
   double s = 0.0;
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int k = 0; k < kTmaConsumers; ++k) s += red[k];
+    for (int k = 0; k < NC; ++k) s += red[k];
   }
   return s;
 }
@@ -1559,23 +1577,29 @@ using ApplyRing = Ring<GT, true, B1, 200 * 1024>;
 // Codes (4 per lane and 128-column half-chunk: exactly one 8-bit group) and
 // this lane's group scale (lanes 0..7: the segment's 8 groups) of one row
 // segment, read straight from global memory one row ahead of their use.
+constexpr int kQ8Split = 2;                             // consumer warps per row with the 8-bit moment
+constexpr int kQ8PerWarp = kTileCols / 128 / kQ8Split;  // 8-bit groups of one consumer warp's columns
 struct Q8Row {
-  uint32_t q[kTileCols / 128];
+  uint32_t q[kQ8PerWarp];
   float s;
 };
+// jw: the warp's first column in the row (tile start + column block).
 __device__ __forceinline__ void q8_load_row(Q8Row& out, const DevTensor& d, int64_t rowg, int64_t base_row,
-                                            int64_t j0, int lane) {
-  const int8_t* qb = d.mq + base_row + j0;
+                                            int64_t jw, int lane) {
+  const int8_t* qb = d.mq + base_row + jw;
 #pragma unroll
-  for (int q = 0; q < kTileCols / 128; ++q) {
+  for (int q = 0; q < kQ8PerWarp; ++q) {
     const int cl = q * 128 + lane * 4;
-    out.q[q] = (j0 + cl < d.W) ? *reinterpret_cast<const uint32_t*>(qb + cl) : 0u;
+    out.q[q] = (jw + cl < d.W) ? *reinterpret_cast<const uint32_t*>(qb + cl) : 0u;
   }
-  out.s = (lane < kTileCols / 128 && j0 + lane * 128 < d.W) ? d.ms[rowg * d.qg + j0 / 128 + lane] : 0.f;
+  out.s = (lane < kQ8PerWarp && jw + lane * 128 < d.W) ? d.ms[rowg * d.qg + jw / 128 + lane] : 0.f;
 }
 
 template <typename GT, bool B1, bool Q8, bool PSQ>
-__global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_constant__ StepArgs a, const Range r) {
+__global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
+    k_apply_tma(const __grid_constant__ StepArgs a, const Range r) {
+  constexpr int SPLIT = Q8 ? kQ8Split : 1;
+  constexpr int NC = TmaCfg<SPLIT>::kConsumers;
   static_assert(!Q8 || B1, "the 8-bit moment needs beta1");
   static_assert(kQ8Group == 128, "a 128-column half-chunk is one 8-bit group");
   using RG = ApplyRing<GT, B1 && !Q8>;
@@ -1583,14 +1607,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_const
   unsigned char* ring = smem;
   float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // coef * col_j^-1/2
   float* rowf = colf + kTileCols;                              // (row_i / mean(row))^-1/2
-  double* red = reinterpret_cast<double*>(rowf + kTileRows);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 16);
+  double* red = reinterpret_cast<double*>(rowf + kTileRows);  // NC <= 32 warp sums
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 32);
   uint64_t* empty = full + RG::kStages;
   int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
   __shared__ int stop;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ng = tma_setup<RG::kStages>(pf, r, full, empty);
-  if (warp == kTmaConsumers) {
+  const int ng = tma_setup<RG::kStages, NC>(pf, r, full, empty);
+  if (warp == NC) {
     if (lane == 0) tma_produce<GT, RG>(a, r, pf, ng, ring, full, empty);
     return;
   }
@@ -1611,28 +1635,32 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_const
     const float mr = static_cast<float>(a.mrow[d.mslot + tp.b]);
     const float coef = static_cast<float>(a.coef[t]);
     const float wda = static_cast<float>(a.wd * a.alpha[t]);
-    consumer_sync();  // stop is settled; colf / rowf / red of the previous tile are read
+    consumer_sync<NC>();  // stop is settled; colf / rowf / red of the previous tile are read
     if (stop) break;
-    for (int cl = threadIdx.x; cl < kTileCols; cl += kTmaConsumers * 32) {
+    for (int cl = threadIdx.x; cl < kTileCols; cl += NC * 32) {
       const int64_t j = j0 + cl;
       colf[cl] = (j < W) ? coef * rsqrtf(d.col[tp.b * W + j]) : 0.f;
     }
-    for (int rl = threadIdx.x; rl < kTileRows; rl += kTmaConsumers * 32) {
+    for (int rl = threadIdx.x; rl < kTileRows; rl += NC * 32) {
       const int64_t i = i0 + rl;
       rowf[rl] = (i < i1) ? rsqrtf(d.row[tp.b * H + i] / mr) : 0.f;
     }
-    consumer_sync();
+    consumer_sync<NC>();
     float psq = 0.f;
     bool ok = true;
+    const int wr = warp % kTmaRows;                              // row of the stage
+    constexpr int KW = kTileCols / 256 / SPLIT;                   // 256-column chunks per warp
+    const int k0 = (warp / kTmaRows) * KW;                        // first chunk of this warp
+    const int64_t jw = j0 + k0 * 256;
     Q8Row qnext;  // codes / scales of this warp's next row
-    if (Q8 && i0 + warp < i1) q8_load_row(qnext, d, tp.b * H + i0 + warp, base + (i0 + warp) * W, j0, lane);
-    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaConsumers, ++it) {
-      const int64_t i = rs + warp;
+    if (Q8 && i0 + wr < i1) q8_load_row(qnext, d, tp.b * H + i0 + wr, base + (i0 + wr) * W, jw, lane);
+    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaRows, ++it) {
+      const int64_t i = rs + wr;
       Q8Row qcur;
       if (Q8) {
         qcur = qnext;
-        const int64_t inext = i + kTmaConsumers;
-        if (inext < i1) q8_load_row(qnext, d, tp.b * H + inext, base + inext * W, j0, lane);
+        const int64_t inext = i + kTmaRows;
+        if (inext < i1) q8_load_row(qnext, d, tp.b * H + inext, base + inext * W, jw, lane);
       }
       const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
       if (!tma_acquire(&full[slot], ph, a, &stop)) {
@@ -1640,16 +1668,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_const
         break;
       }
       if (i < i1) {
-        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
+        const unsigned char* row = ring + slot * RG::kStage + wr * RG::kRow;
         const float r_i = rowf[i - i0];
         float* pg = d.p + base + i * W + j0;
         float* mg = (B1 && !Q8) ? d.m1 + base + i * W + j0 : nullptr;
 #pragma unroll
-        for (int k = 0; k < kTileCols / 256; ++k) {
+        for (int kk = 0; kk < KW; ++kk) {
+          const int k = k0 + kk;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int cl = k * 256 + h * 128 + lane * 4;
-            const float gs = Q8 ? __shfl_sync(0xffffffffu, qcur.s, k * 2 + h) : 0.f;  // group scale
+            const float gs = Q8 ? __shfl_sync(0xffffffffu, qcur.s, kk * 2 + h) : 0.f;  // group scale
             float mq[4] = {0.f, 0.f, 0.f, 0.f};
             if (j0 + cl < W) {
               float x[4];
@@ -1665,7 +1694,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_const
               for (int v = 0; v < 4; ++v) {
                 float upd = (x[v] * r_i) * fv[v];
                 if (B1) {
-                  const float old = Q8 ? q8_value(qcur.q[k * 2 + h], v, gs) : mp[v];
+                  const float old = Q8 ? q8_value(qcur.q[kk * 2 + h], v, gs) : mp[v];
                   mp[v] = fmaf(b1, old, omb1 * upd);
                   upd = mp[v];
                   if (Q8) mq[v] = mp[v];
@@ -1692,7 +1721,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_apply_tma(const __grid_const
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
     if (PSQ) {
-      const double tot = consumer_sum(psq, red);
+      const double tot = consumer_sum<NC>(psq, red);
       if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + local] = tot;
     }
   }
@@ -1725,7 +1754,7 @@ namespace {
 // column buffer, reduction scratch, mbarriers, prefix.
 template <class RG>
 constexpr size_t tma_smem(size_t extra) {
-  return RG::kBytes + extra + sizeof(double) * 16 + sizeof(uint64_t) * 2 * RG::kStages + kPrefixBytes;
+  return RG::kBytes + extra + sizeof(double) * 32 + sizeof(uint64_t) * 2 * RG::kStages + kPrefixBytes;
 }
 constexpr size_t kFactorBytes = sizeof(float) * (kTileCols + kTileRows);
 
@@ -1753,7 +1782,7 @@ Inst pick_f(KernelId k, bool psq_in, int mom, bool psq_out) {
       return x;
     case kKApply:
       if constexpr (VEC == 8) {  // vector path: bulk-copy staged rows
-        x.threads = kTmaThreads;
+        x.threads = mom == 2 ? TmaCfg<kQ8Split>::kThreads : TmaCfg<1>::kThreads;
         if (mom == 2) {
           x.fn = psq_out ? k_apply_tma<GT, true, true, true> : k_apply_tma<GT, true, true, false>;
           x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);

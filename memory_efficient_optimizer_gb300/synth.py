@@ -107,6 +107,11 @@ def workload(name: str, seed: int = 0) -> Workload:
                              weight_decay=0.01), 5, grad_kind="student_t_zero_rows",
                         description="Llama-3-8B shapes, lr 1e-3, beta1 0.9, wd 0.01, "
                                     "Student-t(3) bf16 grads with 1% rows zeroed")
+    if name == "llama_layer_bf16_int8":
+        return Workload(name, llama_layer_shapes(), torch.bfloat16, 1e-3,
+                        dict(lr=1e-3, relative_step=False, scale_parameter=False, beta1=0.9,
+                             weight_decay=0.01, exp_avg_int8=True), 5, grad_kind="student_t_zero_rows",
+                        description="one Llama-3-8B decoder layer, bf16 grads, beta1 0.9 with the 8-bit exp_avg")
     if name == "llama3_8b_beta1_int8":
         return Workload(name, llama3_8b_shapes(), torch.bfloat16, 1e-3,
                         dict(lr=1e-3, relative_step=False, scale_parameter=False, beta1=0.9,
