@@ -593,7 +593,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b",
                     choices=["llama3_8b", "llama3_8b_beta1", "llama3_8b_beta1_int8", "llama_layer", "llama_layer_bf16",
-                             "edge", "tiny"])
+                             "llama_layer_bf16_int8", "edge", "tiny"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--readback-steps", type=int, default=2)
     ap.add_argument("--e2e-streams", type=int, default=1,

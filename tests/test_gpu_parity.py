@@ -229,3 +229,16 @@ def test_native_library_is_loaded():
     maps = open("/proc/self/maps").read()
     assert os.path.realpath(binding.library_path()) in maps
     assert lib is not None
+
+
+def test_more_tensors_than_one_launch_group():
+    """4,500 tensors: more than one launch group (4,096 tensors share one
+    launch's prefix array), in every class (vector, element-wise, fused, 1D),
+    against the oracle."""
+    rng = np.random.default_rng(4500)
+    kinds = [(3, 5), (16, 24), (2, 2056), (7,), (9, 1)]
+    shapes = [kinds[k % len(kinds)] if k % 7 else (int(rng.integers(1, 9)), int(rng.integers(1, 40)))
+              for k in range(4500)]
+    wl = synth.Workload("groups", [(f"t{k}", s) for k, s in enumerate(shapes)], torch.bfloat16, 1e-2,
+                        dict(beta1=0.9, weight_decay=0.01), 3)
+    run_parity(wl)
