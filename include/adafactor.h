@@ -165,15 +165,19 @@ adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size
 
 /* One Adafactor step over tensors[0..n) with states[0..n), step t = `step`
  * (>= 1), enqueued on `stream` (a cudaStream_t; NULL = the legacy default
- * stream).  The call only enqueues work: it never synchronises the host with
- * the device, and it reads no device memory from the host.  Params and states
+ * stream).  The call only enqueues work and reads no device memory from the
+ * host.  The per-call descriptor table is uploaded from a ring of 4 pinned
+ * host buffers per device: a call waits on the host only when the upload of
+ * the call 4 calls earlier (on any stream of the device) has not yet run,
+ * i.e. when more than 4 steps are queued ahead of the GPU.  Params and states
  * are updated in place; grads are read only.  The workspace (>= the size
  * reported by adafactor_workspace_size, 256-byte aligned) is scratch owned by
  * this call until the enqueued work completes: calls that may run
  * concurrently on the device need distinct workspaces.
  * Errors: ADAF_ERR_INVALID_ARGUMENT (hyper-parameters as in
  * adafactor_validate; step < 1; NULL or misaligned pointers; missing state
- * buffers for a tensor's path; has_beta1 without exp_avg), ADAF_ERR_UNSUPPORTED,
+ * buffers for a tensor's path; has_beta1 without exp_avg or, with
+ * exp_avg_int8, without exp_avg_codes / exp_avg_scales), ADAF_ERR_UNSUPPORTED,
  * ADAF_ERR_WORKSPACE_TOO_SMALL, ADAF_ERR_CUDA (a CUDA call or a kernel launch
  * failed; work enqueued before the failure may have run). */
 adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
