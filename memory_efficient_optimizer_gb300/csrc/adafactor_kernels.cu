@@ -1595,6 +1595,38 @@ __device__ __forceinline__ void q8_load_row(Q8Row& out, const DevTensor& d, int6
   out.s = (lane < kQ8PerWarp && jw + lane * 128 < d.W) ? d.ms[rowg * d.qg + jw / 128 + lane] : 0.f;
 }
 
+// What a consumer thread needs of a tile before its rows: the tensor, the
+// tile index within it, coef and mean(row), and the raw column / row
+// statistics behind this thread's entries of the per-tile factors.
+template <int NC> struct TileStats {
+  static constexpr int kCols = kTileCols / (NC * 32);
+  static_assert(kTileCols % (NC * 32) == 0 && kTileRows <= NC * 32, "one row factor per thread at most");
+  int t;
+  int64_t local;
+  float coef, mr;
+  float col[kCols];
+  float row;
+};
+template <int NC>
+__device__ __forceinline__ void tile_stats_load(TileStats<NC>& s, const StepArgs& a, const Range& r,
+                                                const int32_t* pf, int ng, int64_t u) {
+  const int m = find_owner(pf, ng, u);
+  s.t = member_tensor(r, m);
+  const DevTensor& d = a.tensors[s.t];
+  s.local = u - pf[m];
+  const TilePos tp = tile_pos(d, s.local);
+  const int64_t j0 = tp.c * kTileCols, i0 = tp.r * kTileRows;
+  s.coef = static_cast<float>(a.coef[s.t]);
+  s.mr = static_cast<float>(a.mrow[d.mslot + tp.b]);
+#pragma unroll
+  for (int q = 0; q < TileStats<NC>::kCols; ++q) {
+    const int64_t j = j0 + threadIdx.x + q * NC * 32;
+    s.col[q] = j < d.W ? d.col[tp.b * d.W + j] : 1.f;
+  }
+  const int64_t i = i0 + threadIdx.x;
+  s.row = (threadIdx.x < kTileRows && i < d.H) ? d.row[tp.b * d.H + i] : 1.f;
+}
+
 template <typename GT, bool B1, bool Q8, bool PSQ>
 __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
     k_apply_tma(const __grid_constant__ StepArgs a, const Range r) {
@@ -1622,30 +1654,36 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
   const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
   const int64_t u1 = pf[ng];
   uint32_t it = 0;
+  // The per-tile statistics (this thread's column and row values, coef,
+  // mean(row)) are loaded one tile ahead, while the previous tile's rows are
+  // processed, so a tile starts without a round trip to global memory.  Not
+  // with the 8-bit moment: that variant has no registers to spare, and the
+  // prefetch measured 0.3 % faster for the others but 0.5 % slower for it.
+  constexpr bool kAhead = !Q8;
+  TileStats<NC> next;
+  if (kAhead && pf[0] + blockIdx.x < u1) tile_stats_load(next, a, r, pf, ng, pf[0] + blockIdx.x);
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
-    const int m = find_owner(pf, ng, u);
-    const int t = member_tensor(r, m);
+    TileStats<NC> cur;
+    if (kAhead) cur = next;
+    else tile_stats_load(cur, a, r, pf, ng, u);
+    const int t = cur.t;
     const DevTensor d = a.tensors[t];
-    const int64_t local = u - pf[m];
-    const TilePos tp = tile_pos(d, local);
+    const TilePos tp = tile_pos(d, cur.local);
     const int64_t H = d.H, W = d.W;
     const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
     const int64_t j0 = tp.c * kTileCols;
     const int64_t base = tp.b * H * W;
-    const float mr = static_cast<float>(a.mrow[d.mslot + tp.b]);
-    const float coef = static_cast<float>(a.coef[t]);
     const float wda = static_cast<float>(a.wd * a.alpha[t]);
     consumer_sync<NC>();  // stop is settled; colf / rowf / red of the previous tile are read
     if (stop) break;
-    for (int cl = threadIdx.x; cl < kTileCols; cl += NC * 32) {
-      const int64_t j = j0 + cl;
-      colf[cl] = (j < W) ? coef * rsqrtf(d.col[tp.b * W + j]) : 0.f;
+#pragma unroll
+    for (int q = 0; q < TileStats<NC>::kCols; ++q) {
+      const int cl = threadIdx.x + q * NC * 32;
+      colf[cl] = (j0 + cl < W) ? cur.coef * rsqrtf(cur.col[q]) : 0.f;
     }
-    for (int rl = threadIdx.x; rl < kTileRows; rl += NC * 32) {
-      const int64_t i = i0 + rl;
-      rowf[rl] = (i < i1) ? rsqrtf(d.row[tp.b * H + i] / mr) : 0.f;
-    }
+    if (threadIdx.x < kTileRows) rowf[threadIdx.x] = (i0 + threadIdx.x < i1) ? rsqrtf(cur.row / cur.mr) : 0.f;
     consumer_sync<NC>();
+    if (kAhead && u + gridDim.x < u1) tile_stats_load(next, a, r, pf, ng, u + gridDim.x);
     float psq = 0.f;
     bool ok = true;
     const int wr = warp % kTmaRows;                              // row of the stage
@@ -1722,7 +1760,7 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
     }
     if (PSQ) {
       const double tot = consumer_sum<NC>(psq, red);
-      if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + local] = tot;
+      if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + cur.local] = tot;
     }
   }
   if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
