@@ -180,16 +180,185 @@ template <> __device__ __forceinline__ void load_colf<1>(float (&f)[1], const fl
 // Lane column layout inside a tile: chunk k, element v -> k*32*VEC + lane*VEC + v.
 // A row is streamed in groups of CG chunks; RPI rows are loaded per iteration
 // so that ~128 bytes of gradient per lane are in flight before any use.
+// ---- flat processing of narrow tiles (element-wise path, W <= kTileCols) ---
+// Such a tile holds whole rows [i0, i1) and is one contiguous range of
+// (i1 - i0) * W values; threads stream it by flat index (coalesced whatever
+// W is) and recover (row, column) with row = (int)((e + 0.5f) * (1.0f / W)).
+// In fp32 that is exact for every W <= 1024 and e < 256 * W (checked
+// exhaustively): the fractional part of (e + 0.5) / W is at least 0.5 / W,
+// far above the rounding error of the product.
+// Where the tile's start is aligned, threads move 4 consecutive values per
+// load (16 bytes of fp32, 8 of bf16) and step (row, column) along them.
+constexpr int kFlatPass2 = 16;  // scalar values per thread in flight, pass 2
+constexpr int kFlatApply = 8;   // scalar values per thread in flight, apply
+constexpr int kFlatVec1 = kWarps * kTileCols / 4 / kThreads;  // 4-value loads per thread, pass-1 chunk
+constexpr int kFlatVec2 = 8;    // 4-value loads per thread in flight, pass 2
+constexpr int kFlatVecA = 4;    // 4-value loads per stream and thread in flight, apply (3 with exp_avg)
+__device__ __forceinline__ int flat_row(int e, float invw) {
+  return static_cast<int>(__fmul_rn(__fadd_rn(static_cast<float>(e), 0.5f), invw));
+}
+template <typename GT> __device__ __forceinline__ float load_g_scalar(const GT* p);
+template <> __device__ __forceinline__ float load_g_scalar<float>(const float* p) { return __ldcs(p); }
+template <> __device__ __forceinline__ float load_g_scalar<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(__ldcs(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+
+template <typename GT> struct Raw4;
+template <> struct Raw4<float> { float4 v; };
+template <> struct Raw4<__nv_bfloat16> { uint2 v; };
+__device__ __forceinline__ void load_raw4(Raw4<float>& r, const float* p) {
+  r.v = __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void load_raw4(Raw4<__nv_bfloat16>& r, const __nv_bfloat16* p) {
+  r.v = __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ void widen4(const Raw4<float>& r, float (&x)[4]) {
+  x[0] = r.v.x; x[1] = r.v.y; x[2] = r.v.z; x[3] = r.v.w;
+}
+__device__ __forceinline__ void widen4(const Raw4<__nv_bfloat16>& r, float (&x)[4]) {
+  x[0] = __uint_as_float(r.v.x << 16); x[1] = __uint_as_float(r.v.x & 0xffff0000u);
+  x[2] = __uint_as_float(r.v.y << 16); x[3] = __uint_as_float(r.v.y & 0xffff0000u);
+}
+template <typename GT> __device__ __forceinline__ bool vec4_aligned(const GT* p) {
+  return (reinterpret_cast<uintptr_t>(p) & (4 * sizeof(GT) - 1)) == 0;
+}
+// Next (row, column) of a flat walk over rows of w values.
+__device__ __forceinline__ void flat_next(int& i, int& j, int w) {
+  if (++j == w) { j = 0; ++i; }
+}
+
 template <int VEC> struct Layout {
   static constexpr int CH = kTileCols / (32 * VEC);  // chunks per tile row
   static constexpr int CG = VEC == 8 ? 4 : 8;          // chunks per load group
 };
+
+// Flat pass 1 of a narrow tile: chunks of whole rows are squared into the
+// shared staging area (the column-buffer space, kWarps * kTileCols floats),
+// then summed twice in fixed orders: down each column by the thread that owns
+// it, and along each row by a segment of L = min(32, next power of 2 >= w)
+// lanes.  The next chunk's loads are in flight meanwhile.  Returns false, with
+// nothing done, where the tile does not qualify (wide rows, unaligned start).
+template <typename GT, bool PSQ>
+__device__ __forceinline__ void flat_chunk_issue(Raw4<GT> (&raw)[kFlatVec1], float& tail, const GT* src,
+                                                 const float* psrc, int cn, float& psq) {
+  const int nv = cn >> 2;
+#pragma unroll
+  for (int k = 0; k < kFlatVec1; ++k) {
+    const int v = threadIdx.x + k * kThreads;
+    if (v < nv) load_raw4(raw[k], src + 4 * v);
+  }
+  const int te = (nv << 2) + threadIdx.x;  // at most 3 values past the last whole load
+  if (te < cn) tail = load_g_scalar<GT>(src + te);
+  if (PSQ) {
+#pragma unroll
+    for (int k = 0; k < kFlatVec1; ++k) {
+      const int v = threadIdx.x + k * kThreads;
+      if (v < nv) {
+        const float4 y = __ldcs(reinterpret_cast<const float4*>(psrc + 4 * v));
+        psq = fmaf(y.x, y.x, psq); psq = fmaf(y.y, y.y, psq);
+        psq = fmaf(y.z, y.z, psq); psq = fmaf(y.w, y.w, psq);
+      }
+    }
+    if (te < cn) {
+      const float y = __ldcs(psrc + te);
+      psq = fmaf(y, y, psq);
+    }
+  }
+}
+
+template <typename GT, bool PSQ>
+__device__ __forceinline__ bool pass1_flat(const DevTensor& d, const StepArgs& a, int64_t local, float* stage,
+                                           double* red) {
+  constexpr int kStage = kWarps * kTileCols;
+  const int64_t H = d.H, W = d.W;
+  if (W > kTileCols) return false;
+  const TilePos tp = tile_pos(d, local);  // tp.c == 0: one column block
+  const int64_t i0 = tp.r * kTileRows;
+  const GT* gt = static_cast<const GT*>(d.g) + tp.b * H * W + i0 * W;
+  const float* pt = d.p + tp.b * H * W + i0 * W;
+  if (!vec4_aligned(gt) || (PSQ && !vec4_aligned(pt))) return false;
+  const int w = static_cast<int>(W);
+  const int nr = static_cast<int>(min(H, i0 + kTileRows) - i0);
+  const int R = min(nr, (kStage / w) & ~3);  // rows per chunk: chunk starts stay on 4-value boundaries
+  int lg = 0;
+  while ((1 << lg) < w && lg < 5) ++lg;  // L = 1 << lg lanes per row
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane >> lg, cl0 = lane & ((1 << lg) - 1);
+  const int rpw = 32 >> lg;  // rows per warp pass
+  float* rowpart = a.rowpart + d.rowpart + tp.b * H + i0;
+
+  float cacc[kTileCols / kThreads];
+#pragma unroll
+  for (int k = 0; k < kTileCols / kThreads; ++k) cacc[k] = 0.f;
+  float psq = 0.f, tail = 0.f;
+  Raw4<GT> raw[kFlatVec1];
+  flat_chunk_issue<GT, PSQ>(raw, tail, gt, pt, R * w, psq);
+  for (int r0 = 0; r0 < nr; r0 += R) {
+    const int rows = min(R, nr - r0);
+    const int cn = rows * w, nv = cn >> 2;
+#pragma unroll
+    for (int k = 0; k < kFlatVec1; ++k) {
+      const int v = threadIdx.x + k * kThreads;
+      if (v < nv) {
+        float x[4];
+        widen4(raw[k], x);
+        *reinterpret_cast<float4*>(stage + 4 * v) = make_float4(x[0] * x[0], x[1] * x[1], x[2] * x[2], x[3] * x[3]);
+      }
+    }
+    const int te = (nv << 2) + threadIdx.x;
+    if (te < cn) stage[te] = tail * tail;
+    __syncthreads();
+    const int r1 = r0 + R;
+    if (r1 < nr) flat_chunk_issue<GT, PSQ>(raw, tail, gt + r1 * w, pt + r1 * w, min(R, nr - r1) * w, psq);
+    // columns: thread c sums rows in order, four interleaved partials
+#pragma unroll
+    for (int k = 0; k < kTileCols / kThreads; ++k) {
+      const int c = threadIdx.x + k * kThreads;
+      if (c < w) {
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        int r = 0;
+        for (; r + 4 <= rows; r += 4) {
+          s0 += stage[r * w + c];
+          s1 += stage[(r + 1) * w + c];
+          s2 += stage[(r + 2) * w + c];
+          s3 += stage[(r + 3) * w + c];
+        }
+        for (; r < rows; ++r) s0 += stage[r * w + c];
+        cacc[k] += (s0 + s1) + (s2 + s3);
+      }
+    }
+    // rows: segments of L lanes, a xor tree inside each segment
+    for (int rb = warp * rpw; rb < rows; rb += kWarps * rpw) {
+      const int r = rb + sub;
+      float sr = 0.f;
+      if (r < rows)
+        for (int c = cl0; c < w; c += 1 << lg) sr += stage[r * w + c];
+      for (int o = (1 << lg) >> 1; o > 0; o >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, o);
+      if (cl0 == 0 && r < rows) rowpart[r0 + r] = sr;
+    }
+    __syncthreads();  // the stage is rewritten next
+  }
+  float* colpart = a.colpart + d.colpart + (tp.b * d.rb + tp.r) * W;
+#pragma unroll
+  for (int k = 0; k < kTileCols / kThreads; ++k) {
+    const int c = threadIdx.x + k * kThreads;
+    if (c < w) colpart[c] = cacc[k];
+  }
+  if (PSQ) {
+    const double tot = block_sum(static_cast<double>(psq), red);
+    if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = tot;
+  }
+  return true;
+}
 
 template <typename GT, int VEC, bool PSQ>
 __device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArgs& a, int64_t local,
                                float* colbuf, double* red) {
   constexpr int CH = Layout<VEC>::CH, CG = Layout<VEC>::CG;
   constexpr int RPI = PSQ ? 1 : ((VEC == 8 && sizeof(GT) == 4) ? 1 : 2);
+  if constexpr (VEC == 1) {
+    if (pass1_flat<GT, PSQ>(d, a, local, colbuf, red)) return;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const TilePos tp = tile_pos(d, local);
   const int64_t H = d.H, W = d.W;
@@ -699,6 +868,62 @@ __device__ __forceinline__ void pass2_factored(const DevTensor& d, const StepArg
   }
   __syncthreads();
 
+  if constexpr (VEC == 1) {
+    if (W <= kTileCols) {  // whole rows: stream the tile by flat index
+      const int cnt = static_cast<int>((i1 - i0) * W);
+      const GT* gt = gb + i0 * W;
+      const float invw = 1.0f / static_cast<float>(W);
+      const int w32 = static_cast<int>(W);
+      float acc = 0.f;
+      int start = 0;  // first value left to the scalar loop
+      if (vec4_aligned(gt)) {
+        const int nv = cnt >> 2;
+        for (int v0 = threadIdx.x; v0 < nv; v0 += kFlatVec2 * kThreads) {
+          Raw4<GT> raw[kFlatVec2];
+#pragma unroll
+          for (int k = 0; k < kFlatVec2; ++k) {
+            const int v = v0 + k * kThreads;
+            if (v < nv) load_raw4(raw[k], gt + 4 * v);
+          }
+#pragma unroll
+          for (int k = 0; k < kFlatVec2; ++k) {
+            const int v = v0 + k * kThreads;
+            if (v < nv) {
+              float x[4];
+              widen4(raw[k], x);
+              int i = flat_row(4 * v, invw), j = 4 * v - i * w32;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                acc = fmaf(rowf[i], (x[q] * x[q]) * colf[j], acc);
+                flat_next(i, j, w32);
+              }
+            }
+          }
+        }
+        start = nv << 2;
+      }
+      for (int e0 = start + threadIdx.x; e0 < cnt; e0 += kFlatPass2 * kThreads) {
+        float x[kFlatPass2];
+#pragma unroll
+        for (int k = 0; k < kFlatPass2; ++k) {
+          const int e = e0 + k * kThreads;
+          x[k] = e < cnt ? load_g_scalar<GT>(gt + e) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kFlatPass2; ++k) {
+          const int e = e0 + k * kThreads;
+          if (e < cnt) {
+            const int i = flat_row(e, invw), j = e - i * w32;
+            acc = fmaf(rowf[i], (x[k] * x[k]) * colf[j], acc);
+          }
+        }
+      }
+      const double tot = block_sum(static_cast<double>(acc), red);
+      if (threadIdx.x == 0) a.spart[d.tile0 + local] = tot;
+      return;
+    }
+  }
+
   float acc = 0.f;  // this lane's share of sum(u^2) over the tile (<= 32 rows)
   for (int64_t i = i0 + warp; i < i1; i += RPI * kWarps) {
     float ts[RPI];
@@ -819,7 +1044,7 @@ __device__ __forceinline__ float q8_scale(float amax) { return amax > 0.f ? amax
 // colf holds coef * col_j^-1/2 for the tile's columns (shared memory).
 template <typename GT, int VEC, bool B1, bool Q8, bool PSQ>
 __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArgs& a, int t, int64_t local, float* colf,
-                               double* red) {
+                               float* rowf, double* red) {
   static_assert(!Q8 || (B1 && VEC == 1 && Layout<VEC>::CG * 32 % kQ8Group == 0),
                 "8-bit moment: element-wise layout, whole groups per load group");
   constexpr int CH = Layout<VEC>::CH, CG = Layout<VEC>::CG;
@@ -845,9 +1070,102 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
     const int64_t j = j0 + cl;
     colf[colf_index<VEC>(cl)] = (j < W) ? coef * rsqrtf(d.col[tp.b * W + j]) : 0.f;
   }
+  constexpr bool kFlat = VEC == 1 && !Q8;  // 8-bit groups need the row-by-row layout
+  if (kFlat && W <= kTileCols) {
+    for (int rl = threadIdx.x; rl < kTileRows; rl += kThreads) {
+      const int64_t i = i0 + rl;
+      rowf[rl] = (i < i1) ? rsqrtf(row[i] / m) : 0.f;
+    }
+  }
   __syncthreads();
 
   float psq = 0.f;
+  if constexpr (kFlat) {
+    if (W <= kTileCols) {  // whole rows: stream the tile by flat index
+      const int cnt = static_cast<int>((i1 - i0) * W);
+      const int64_t o = i0 * W;
+      const float invw = 1.0f / static_cast<float>(W);
+      const int w32 = static_cast<int>(W);
+      int start = 0;  // first value left to the scalar loop
+      if (vec4_aligned(gb + o) && vec4_aligned(pb + o) && (!B1 || vec4_aligned(mb + o))) {
+        constexpr int UA = B1 ? kFlatVecA - 1 : kFlatVecA;
+        const int nv = cnt >> 2;
+        for (int v0 = threadIdx.x; v0 < nv; v0 += UA * kThreads) {
+          Raw4<GT> raw[UA];
+          float4 p4[UA], m4[B1 ? UA : 1];
+#pragma unroll
+          for (int k = 0; k < UA; ++k) {
+            const int v = v0 + k * kThreads;
+            if (v < nv) {
+              load_raw4(raw[k], gb + o + 4 * v);
+              p4[k] = __ldcs(reinterpret_cast<const float4*>(pb + o + 4 * v));
+              if (B1) m4[B1 ? k : 0] = __ldcs(reinterpret_cast<const float4*>(mb + o + 4 * v));
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < UA; ++k) {
+            const int v = v0 + k * kThreads;
+            if (v < nv) {
+              float x[4], pv[4] = {p4[k].x, p4[k].y, p4[k].z, p4[k].w}, mv[4];
+              if (B1) {
+                const float4 mm = m4[B1 ? k : 0];
+                mv[0] = mm.x; mv[1] = mm.y; mv[2] = mm.z; mv[3] = mm.w;
+              }
+              widen4(raw[k], x);
+              int i = flat_row(4 * v, invw), j = 4 * v - i * w32;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float upd = (x[q] * rowf[i]) * colf[j];
+                if (B1) {
+                  mv[q] = fmaf(b1, mv[q], omb1 * upd);
+                  upd = mv[q];
+                }
+                pv[q] = fmaf(-wda, pv[q], pv[q] - upd);
+                if (PSQ) psq = fmaf(pv[q], pv[q], psq);
+                flat_next(i, j, w32);
+              }
+              __stcs(reinterpret_cast<float4*>(pb + o + 4 * v), make_float4(pv[0], pv[1], pv[2], pv[3]));
+              if (B1) __stcs(reinterpret_cast<float4*>(mb + o + 4 * v), make_float4(mv[0], mv[1], mv[2], mv[3]));
+            }
+          }
+        }
+        start = nv << 2;
+      }
+      for (int e0 = start + threadIdx.x; e0 < cnt; e0 += kFlatApply * kThreads) {
+        float x[kFlatApply], pv[kFlatApply], mv[B1 ? kFlatApply : 1];
+#pragma unroll
+        for (int k = 0; k < kFlatApply; ++k) {
+          const int e = e0 + k * kThreads;
+          if (e < cnt) {
+            x[k] = load_g_scalar<GT>(gb + o + e);
+            pv[k] = __ldcs(pb + o + e);
+            if (B1) mv[B1 ? k : 0] = __ldcs(mb + o + e);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kFlatApply; ++k) {
+          const int e = e0 + k * kThreads;
+          if (e < cnt) {
+            const int i = flat_row(e, invw), j = e - i * w32;
+            float upd = (x[k] * rowf[i]) * colf[j];
+            if (B1) {
+              mv[B1 ? k : 0] = fmaf(b1, mv[B1 ? k : 0], omb1 * upd);
+              upd = mv[B1 ? k : 0];
+              __stcs(mb + o + e, mv[B1 ? k : 0]);
+            }
+            const float pn = fmaf(-wda, pv[k], pv[k] - upd);
+            __stcs(pb + o + e, pn);
+            if (PSQ) psq = fmaf(pn, pn, psq);
+          }
+        }
+      }
+      if (PSQ) {
+        const double tot = block_sum(static_cast<double>(psq), red);
+        if (threadIdx.x == 0) a.ppart[d.tile0 + local] = tot;
+      }
+      return;
+    }
+  }
   for (int64_t i = i0 + warp; i < i1; i += kWarps) {
     const float r_i = rsqrtf(row[i] / m);
 #pragma unroll
@@ -1043,13 +1361,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_apply_f(const __grid_constant__
   double* red = reinterpret_cast<double*>(smem);
   int32_t* pf = reinterpret_cast<int32_t*>(smem + kRedBytes);
   float* colf = reinterpret_cast<float*>(smem + kRedBytes + kPrefixBytes);
+  float* rowf = colf + kTileCols;  // allocated for the element-wise layout only
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const int t = member_tensor(r, m);
     const DevTensor d = a.tensors[t];
-    apply_factored<GT, VEC, B1, Q8, PSQ>(d, a, t, u - pf[m], colf, red);
+    apply_factored<GT, VEC, B1, Q8, PSQ>(d, a, t, u - pf[m], colf, rowf, red);
   }
 }
 
@@ -1836,7 +2155,7 @@ Inst pick_f(KernelId k, bool psq_in, int mom, bool psq_out) {
         if (mom == 2) x.fn = psq_out ? k_apply_f<GT, VEC, true, true, true> : k_apply_f<GT, VEC, true, true, false>;
         else if (b1) x.fn = psq_out ? k_apply_f<GT, VEC, true, false, true> : k_apply_f<GT, VEC, true, false, false>;
         else x.fn = psq_out ? k_apply_f<GT, VEC, false, false, true> : k_apply_f<GT, VEC, false, false, false>;
-        x.smem = kRedBytes + kPrefixBytes + kColfBytes;
+        x.smem = kRedBytes + kPrefixBytes + kColfBytes + (VEC == 1 ? kRowfBytes : 0);
         return x;
       }
     default: return x;

@@ -67,6 +67,9 @@ def test_llama3_8b_beta1_student_t_sampled():
 
 SMALL_SHAPES = [(1, 1), (2, 3), (3, 2), (1, 5), (5, 1), (2, 2, 3), (4,), (), (600, 2100), (257, 1025),
                 (3, 4097), (1000, 1032), (2, 3, 520, 264), (7, 1, 9), (1, 65536), (9000,),
+                # flat walk over whole rows (W <= 1024, not a multiple of 8): several
+                # staged chunks per tile and a ragged last chunk, 1..8-lane row segments
+                (700, 33), (300, 1023), (513, 7), (260, 1), (1030, 3),
                 # bf16: fused row-chunk pass, 8-warp configuration (2048 <= W <= 4096): a
                 # one-lane last column group, two chunks with a ragged one, B = 2 slices
                 (300, 2056), (2, 130, 4096),
@@ -92,23 +95,26 @@ def test_small_shapes_all_flags(flags, grad_dtype):
     run_parity(wl)
 
 
-@pytest.mark.parametrize("carry", [True, False])
-def test_misaligned_views_take_the_elementwise_path(carry):
-    """Params/grads offset by one element from a 16-byte boundary cannot use
-    the vector kernels; results must not change."""
-    shapes = [(64, 1024), (33, 520), (100,), (20, 2048), (9, 4104)]
+@pytest.mark.parametrize("carry,offset", [(True, "both"), (False, "both"), (False, "params"), (True, "grads")])
+def test_misaligned_views_take_the_elementwise_path(carry, offset):
+    """Params and/or grads offset by one element from a 16-byte boundary
+    cannot use the vector kernels or the 4-value loads of the flat walk;
+    results must not change."""
+    shapes = [(64, 1024), (33, 520), (100,), (20, 2048), (9, 4104), (300, 77)]
     hp = dict(beta1=0.9)
     import oracle
     from parity_util import oracle_hp
+    po = 1 if offset in ("both", "params") else 0
+    go = 1 if offset in ("both", "grads") else 0
     bufs_p = [torch.zeros(int(np.prod(s)) + 1, device="cuda") for s in shapes]
-    params = [b[1:].view(s) for b, s in zip(bufs_p, shapes)]
+    params = [b[po:po + int(np.prod(s))].view(s) for b, s in zip(bufs_p, shapes)]
     for k, (p, s) in enumerate(zip(params, shapes)):
         p.copy_(synth.make_param(s, k))
     p0 = [to64(p) for p in params]
     refs = [x.copy() for x in p0]
     rst = [oracle.State(s, True) for s in shapes]
     gbufs = [torch.zeros(int(np.prod(s)) + 1, device="cuda", dtype=torch.bfloat16) for s in shapes]
-    grads = [b[1:].view(s) for b, s in zip(gbufs, shapes)]
+    grads = [b[go:go + int(np.prod(s))].view(s) for b, s in zip(gbufs, shapes)]
     states = init_state(params, beta1=0.9, param_sq_sum=carry)
     step = AdafactorStep(params, grads, states, **hp)
     for t in range(1, 6):
