@@ -63,3 +63,38 @@ def test_pins_catch_mutant(name, tmp_path):
                           os.path.join(ROOT, "tests", "test_oracle_bruteforce.py")],
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert res.returncode != 0, f"mutant '{name}' survived the pins:\n{res.stdout[-2000:]}"
+
+
+LAMB_SRC = os.path.join(ROOT, "oracle", "lamb_oracle.c")
+LAMB_MUTANTS = {
+    "bias correction with power t + 1": ("1.0 - pow(hp->beta1, (double)t)", "1.0 - pow(hp->beta1, (double)(t + 1))"),
+    "second-moment EMA coefficients swapped": (
+        "v[i] = hp->beta2 * v[i] + (1.0 - hp->beta2) * g[i] * g[i];",
+        "v[i] = (1.0 - hp->beta2) * v[i] + hp->beta2 * g[i] * g[i];"),
+    "no square root of vh": ("return mh / (sqrt(vh) + hp->eps) + hp->weight_decay * p;",
+                             "return mh / (vh + hp->eps) + hp->weight_decay * p;"),
+    "eps inside the square root": ("return mh / (sqrt(vh) + hp->eps) + hp->weight_decay * p;",
+                                   "return mh / sqrt(vh + hp->eps) + hp->weight_decay * p;"),
+    "trust ratio inverted": ("? pn / rn : 1.0;", "? rn / pn : 1.0;"),
+    "zero norm gives trust 0": ("? pn / rn : 1.0;", "? pn / rn : 0.0;"),
+    "weight decay left out of the direction": ("return mh / (sqrt(vh) + hp->eps) + hp->weight_decay * p;",
+                                               "return mh / (sqrt(vh) + hp->eps);"),
+    "lr not applied": ("p[i] = p[i] - hp->lr * trust * r;", "p[i] = p[i] - trust * r;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAMB_MUTANTS))
+def test_lamb_pins_catch_mutant(name, tmp_path):
+    old, new = LAMB_MUTANTS[name]
+    src = open(LAMB_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found once: {old}"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", str(mut),
+                           "-o", str(lib), "-lm"])
+    env = dict(os.environ, ORACLE_LAMB_LIB_OVERRIDE=str(lib))
+    res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_lamb_pins.py")],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode != 0, f"mutant '{name}' survived the pins:\n{res.stdout[-2000:]}"
