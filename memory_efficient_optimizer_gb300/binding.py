@@ -1,4 +1,5 @@
-"""ctypes binding of the C ABI in include/adafactor.h (argument marshalling only).
+"""ctypes binding of the C ABI in include/adafactor.h and include/lamb.h
+(argument marshalling only).
 
 Every function here has the name of the C entry point it calls and does no
 arithmetic of the method: all of the step runs in the CUDA library.  Loading
@@ -30,6 +31,11 @@ EXPORTS = (
     "adafactor_kernel_name", "adafactor_step_noalloc", "adafactor_debug_stall_copies",
     "adafactor_shard_sizes", "adafactor_shard_begin", "adafactor_shard_middle", "adafactor_shard_end",
 )
+# Entry points declared in include/lamb.h.
+LAMB_EXPORTS = (
+    "lamb_validate", "lamb_workspace_size", "lamb_step", "lamb_trust_ratios", "lamb_profile_enable",
+    "lamb_profile_read", "lamb_num_kernels", "lamb_kernel_name",
+)
 
 
 class adaf_tensor(ctypes.Structure):
@@ -57,6 +63,16 @@ class adaf_hparams(ctypes.Structure):
 
 class adaf_shard(ctypes.Structure):
     _fields_ = [("global_rows", ctypes.c_int64)]
+
+
+class lamb_tensor(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("grad_dtype", ctypes.c_int32),
+                ("numel", ctypes.c_int64), ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p)]
+
+
+class lamb_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("bias_correction", ctypes.c_int32)]
 
 
 class AdafactorError(RuntimeError):
@@ -129,6 +145,23 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.adafactor_shard_middle.argtypes = shard_head + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.adafactor_shard_end.restype = ctypes.c_int
         lib.adafactor_shard_end.argtypes = shard_head + [ctypes.c_void_p, ctypes.c_void_p]
+        lib.lamb_validate.restype = ctypes.c_int
+        lib.lamb_validate.argtypes = [P(lamb_hparams)]
+        lib.lamb_workspace_size.restype = ctypes.c_int
+        lib.lamb_workspace_size.argtypes = [P(lamb_tensor), ctypes.c_int32, P(ctypes.c_size_t)]
+        lib.lamb_step.restype = ctypes.c_int
+        lib.lamb_step.argtypes = [P(lamb_tensor), ctypes.c_int32, ctypes.c_int64, P(lamb_hparams),
+                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        lib.lamb_trust_ratios.restype = ctypes.c_int
+        lib.lamb_trust_ratios.argtypes = [ctypes.c_void_p, ctypes.c_int32, P(ctypes.c_double), ctypes.c_void_p]
+        lib.lamb_profile_enable.restype = ctypes.c_int
+        lib.lamb_profile_enable.argtypes = [ctypes.c_int32]
+        lib.lamb_profile_read.restype = ctypes.c_int
+        lib.lamb_profile_read.argtypes = [P(ctypes.c_double), P(ctypes.c_int64), ctypes.c_int32]
+        lib.lamb_num_kernels.restype = ctypes.c_int32
+        lib.lamb_num_kernels.argtypes = []
+        lib.lamb_kernel_name.restype = ctypes.c_char_p
+        lib.lamb_kernel_name.argtypes = [ctypes.c_int32]
         _lib = lib
         return lib
 
@@ -238,3 +271,48 @@ def adafactor_profile_read() -> dict:
     launches = (ctypes.c_int64 * nk)()
     _check(load().adafactor_profile_read(ms, launches, nk))
     return {adafactor_kernel_name(k): (float(ms[k]), int(launches[k])) for k in range(nk)}
+
+
+# ---- LAMB (include/lamb.h) --------------------------------------------------
+
+def lamb_validate(hp: lamb_hparams) -> None:
+    _check(load().lamb_validate(ctypes.byref(hp)))
+
+
+def lamb_workspace_size(tensors, n: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().lamb_workspace_size(tensors, int(n), ctypes.byref(out)))
+    return int(out.value)
+
+
+def lamb_step(tensors, n: int, step: int, hp: lamb_hparams, workspace: int, workspace_bytes: int,
+              stream: int) -> None:
+    _check(load().lamb_step(tensors, int(n), int(step), ctypes.byref(hp), ctypes.c_void_p(workspace),
+                            ctypes.c_size_t(workspace_bytes), ctypes.c_void_p(stream)))
+
+
+def lamb_trust_ratios(workspace: int, n: int, stream: int) -> list:
+    out = (ctypes.c_double * max(1, int(n)))()
+    _check(load().lamb_trust_ratios(ctypes.c_void_p(workspace), int(n), out, ctypes.c_void_p(stream)))
+    return [float(out[k]) for k in range(int(n))]
+
+
+def lamb_profile_enable(on: bool) -> None:
+    _check(load().lamb_profile_enable(1 if on else 0))
+
+
+def lamb_num_kernels() -> int:
+    return int(load().lamb_num_kernels())
+
+
+def lamb_kernel_name(k: int) -> str:
+    return load().lamb_kernel_name(int(k)).decode()
+
+
+def lamb_profile_read() -> dict:
+    """{kernel name: (total ms, launches)} for the LAMB events recorded since the last read."""
+    nk = lamb_num_kernels()
+    ms = (ctypes.c_double * nk)()
+    launches = (ctypes.c_int64 * nk)()
+    _check(load().lamb_profile_read(ms, launches, nk))
+    return {lamb_kernel_name(k): (float(ms[k]), int(launches[k])) for k in range(nk)}

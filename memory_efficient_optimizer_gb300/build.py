@@ -1,7 +1,7 @@
 """Builds libmeo_adafactor.so (the C-ABI CUDA library) in-tree with nvcc.
 
 Usage: ``python -m memory_efficient_optimizer_gb300.build [--force]``.
-The two translation units are compiled in parallel for sm_103a only, then
+The translation units are compiled in parallel for sm_103a only, then
 linked into ``memory_efficient_optimizer_gb300/lib/libmeo_adafactor.so`` with
 the CUDA runtime linked statically (the library needs no torch at link time).
 """
@@ -20,8 +20,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmeo_adafactor.so")
-SOURCES = ["adafactor_kernels.cu", "adafactor_api.cpp", "adafactor_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "adafactor_internal.h"), os.path.join(INCLUDE, "adafactor.h")]
+SOURCES = ["adafactor_kernels.cu", "adafactor_api.cpp", "adafactor_noalloc.cu", "lamb.cu"]
+HEADERS = [os.path.join(CSRC, "adafactor_internal.h"), os.path.join(INCLUDE, "adafactor.h"),
+           os.path.join(INCLUDE, "lamb.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

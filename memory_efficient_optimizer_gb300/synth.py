@@ -19,6 +19,10 @@ Workloads (shapes as PyTorch [out, in] weights):
                     relative_step and scale_parameter off, beta1 0.9, weight
                     decay 0.01; g = Student-t(3 dof) * 1e-3 in bf16 with 1% of
                     the rows of every matrix zeroed (rows fixed per tensor).
+  * ``llama3_8b_lamb``, ``llama_layer_lamb``  the LAMB step (article
+                    defaults: lr 1e-3, betas (0.9, 0.999), eps 1e-6, bias
+                    correction, weight decay 0.01) on the Llama-3-8B list or one
+                    decoder layer; fp32 p, bf16 g ~ N(0, 1e-3).
   * ``edge``        1x65536, 65536x1, 4097x3, 3x4097, 17x100003,
                     [8,1024,1024] and 2,000 matrices with H, W ~ U[1, 512];
                     fp32, g ~ N(0, 1e-2), defaults plus beta1 0.9, 10 steps.
@@ -80,6 +84,7 @@ class Workload:
     grad_kind: str = "normal"         # "normal" | "student_t_zero_rows"
     param_std: float = 0.02
     description: str = ""
+    optimizer: str = "adafactor"      # "adafactor" | "lamb"
     extra: dict = field(default_factory=dict)
 
     @property
@@ -118,6 +123,14 @@ def workload(name: str, seed: int = 0) -> Workload:
                              weight_decay=0.01, exp_avg_int8=True), 5, grad_kind="student_t_zero_rows",
                         description="Llama-3-8B shapes, lr 1e-3, beta1 0.9 (8-bit exp_avg, groups of 128), "
                                     "wd 0.01, Student-t(3) bf16 grads with 1% rows zeroed")
+    if name == "llama3_8b_lamb":
+        return Workload(name, llama3_8b_shapes(), torch.bfloat16, 1e-3, dict(weight_decay=0.01), 5,
+                        description="Llama-3-8B shapes, LAMB (lr 1e-3, betas (0.9, 0.999), eps 1e-6, "
+                                    "bias correction, wd 0.01), bf16 grads", optimizer="lamb")
+    if name == "llama_layer_lamb":
+        return Workload(name, llama_layer_shapes(), torch.bfloat16, 1e-3, dict(weight_decay=0.01), 5,
+                        description="one Llama-3-8B decoder layer, LAMB (article defaults, wd 0.01), "
+                                    "bf16 grads", optimizer="lamb")
     if name == "edge":
         return Workload(name, edge_shapes(seed), torch.float32, 1e-2, dict(beta1=0.9), 10,
                         description="edge shapes + 2,000 small matrices, fp32, beta1 0.9")

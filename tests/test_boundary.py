@@ -1,5 +1,5 @@
 """The C-ABI boundary without a GPU: the library loads, exports every entry
-point declared in include/adafactor.h, and rejects bad arguments before any
+point declared in include/*.h, and rejects bad arguments before any
 CUDA call (so a failing call changes nothing)."""
 import ctypes
 import os
@@ -26,14 +26,14 @@ def declared_functions():
         if fn.endswith(".h"):
             src = open(os.path.join(ROOT, "include", fn)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names |= set(re.findall(r"\b(adafactor_\w+)\s*\(", src))
+            names |= set(re.findall(r"\b((?:adafactor|lamb|came)_\w+)\s*\(", src))
     return names
 
 
 def test_every_declared_symbol_is_exported(lib):
     declared = declared_functions()
     assert declared, "no declarations found"
-    assert declared == set(B.EXPORTS)
+    assert declared == set(B.EXPORTS) | set(B.LAMB_EXPORTS)
     for name in declared:
         assert hasattr(lib, name), name
 
