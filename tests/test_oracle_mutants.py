@@ -98,3 +98,45 @@ def test_lamb_pins_catch_mutant(name, tmp_path):
                           os.path.join(ROOT, "tests", "test_oracle_lamb_pins.py")],
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert res.returncode != 0, f"mutant '{name}' survived the pins:\n{res.stdout[-2000:]}"
+
+
+CAME_SRC = os.path.join(ROOT, "oracle", "came_oracle.c")
+CAME_MUTANTS = {
+    "instability against the old momentum": (
+        """        exp_avg[k] = hp->beta1 * exp_avg[k] + (1.0 - hp->beta1) * u[k];
+        const double dlt = u[k] - exp_avg[k];""",
+        """        const double dlt = u[k] - exp_avg[k];
+        exp_avg[k] = hp->beta1 * exp_avg[k] + (1.0 - hp->beta1) * u[k];"""),
+    "eps2 dropped": ("x[k] = dlt * dlt + hp->eps2;", "x[k] = dlt * dlt;"),
+    "beta2 used for the instability": ("hp->beta3, res_row + b * H", "hp->beta2, res_row + b * H"),
+    "no mean normalisation of the factors": ("f[i * W + j] = rb[i] * cb[j] / mr;", "f[i * W + j] = rb[i] * cb[j];"),
+    "column mean over the wrong axis": ("cb[j] = beta * cb[j] + (1.0 - beta) * (s / (double)H);",
+                                        "cb[j] = beta * cb[j] + (1.0 - beta) * (s / (double)W);"),
+    "clip inverted": ("double clip_div = rms(u, n) / hp->clip_threshold;",
+                      "double clip_div = rms(u, n) * hp->clip_threshold;"),
+    "no square root of S": ("p[k] = p[k] - hp->lr * exp_avg[k] / sqrt(f[k]);",
+                            "p[k] = p[k] - hp->lr * exp_avg[k] / f[k];"),
+    "weight decay without the lr": ("p[k] = p[k] - hp->weight_decay * hp->lr * p[k];",
+                                    "p[k] = p[k] - hp->weight_decay * p[k];"),
+    "momentum coefficients swapped": ("exp_avg[k] = hp->beta1 * exp_avg[k] + (1.0 - hp->beta1) * u[k];",
+                                      "exp_avg[k] = (1.0 - hp->beta1) * exp_avg[k] + hp->beta1 * u[k];"),
+    "vector path without eps1": ("for (int64_t k = 0; k < n; ++k) x[k] = g[k] * g[k] + hp->eps1;",
+                                 "for (int64_t k = 0; k < n; ++k) x[k] = g[k] * g[k];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CAME_MUTANTS))
+def test_came_pins_catch_mutant(name, tmp_path):
+    old, new = CAME_MUTANTS[name]
+    src = open(CAME_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found once: {old}"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", str(mut),
+                           "-o", str(lib), "-lm"])
+    env = dict(os.environ, ORACLE_CAME_LIB_OVERRIDE=str(lib))
+    res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_came_pins.py")],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode != 0, f"mutant '{name}' survived the pins:\n{res.stdout[-2000:]}"
