@@ -9,8 +9,9 @@ the whole tensor list of the workload, with synthetic inputs resident in HBM
 (48 GB for Llama-3-8B: fp32 params, bf16 grads; far larger than the 129 MB
 L2, so no flush is needed between steps).  Rank 0 prints one JSON line.
 
-The ``*_lamb`` workloads run the multi-tensor LAMB step (include/lamb.h)
-instead, with the same JSON line (metric LAMB_METRIC).
+The ``*_lamb`` and ``*_came`` workloads run the multi-tensor LAMB
+(include/lamb.h) or CAME (include/came.h) step instead, with the same JSON
+line (metrics LAMB_METRIC, CAME_METRIC).
 
 --impl reference times the float64 CPU oracle (single thread) on a bounded
 sample of the same workload per step.  Under torchrun with N > 1 every rank
@@ -37,17 +38,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from memory_efficient_optimizer_gb300 import binding, synth  # noqa: E402
+from memory_efficient_optimizer_gb300.came import CameStep, init_came_state  # noqa: E402
 from memory_efficient_optimizer_gb300.lamb import LambStep, init_lamb_state  # noqa: E402
 from memory_efficient_optimizer_gb300.optim import AdafactorShardStep, AdafactorStep, init_state  # noqa: E402
 
 METRIC = "Adafactor step params/sec and effective HBM GB/s (% of 8 TB/s), Llama-3-8B shapes"
 LAMB_METRIC = "LAMB step params/sec and effective HBM GB/s, Llama-3-8B shapes"
+CAME_METRIC = "CAME step params/sec and effective HBM GB/s, Llama-3-8B shapes"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "adafactor_kernels.cu")
 KERNEL_HDR = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "adafactor_internal.h")
 LAMB_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "lamb.cu")
 LAMB_HDR = os.path.join(ROOT, "include", "lamb.h")
+CAME_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "came.cu")
+CAME_HDR = os.path.join(ROOT, "include", "came.h")
 
 
 def dist_env():
@@ -247,11 +252,12 @@ KERNEL_SECTIONS = {
 def kernel_source_digest(kernel):
     """sha256 of the source a launch slot's kernel is built from: the shared
     header plus the slot's sections of the kernel file (the whole file for
-    slots without a section list); for the LAMB kernels, lamb.cu and its
-    header."""
-    if kernel.startswith("k_lamb"):
-        text = "".join(open(f, encoding="utf-8").read() for f in (LAMB_SRC, LAMB_HDR))
-        return hashlib.sha256(text.encode()).hexdigest()
+    slots without a section list); for the LAMB and CAME kernels, their
+    own source file and header."""
+    for prefix, files in (("k_lamb", (LAMB_SRC, LAMB_HDR)), ("k_came", (CAME_SRC, CAME_HDR))):
+        if kernel.startswith(prefix):
+            text = "".join(open(f, encoding="utf-8").read() for f in files)
+            return hashlib.sha256(text.encode()).hexdigest()
     text = open(KERNEL_SRC, encoding="utf-8").read()
     titles = KERNEL_SECTIONS.get(kernel.split("[")[0])
     if titles:
@@ -675,6 +681,190 @@ def run_lamb(args, world, rank, local):
     return out, (wl, wl.numel)
 
 
+# ------------------------------------------------------------------ CAME --
+def came_bytes(shapes, grad_bytes):
+    """Algorithmic HBM bytes of a CAME step per launch slot of this design.
+    Factored tensors: pass a reads g; pass b reads g; pass c reads g and m and
+    writes m; pass d reads m and p and writes p.  1D tensors: pass a reads g
+    and v and writes v; pass c reads g, v, m, S, p and writes m, S, p.  (The
+    row/column statistics and partial sums are under 0.2 % and left out.)
+    Returns (slots, per step, one-pass minimum g + m and p read and written)."""
+    nf = n1 = 0
+    for _, s in shapes:
+        n = 1
+        for d in s:
+            n *= int(d)
+        if len(s) >= 2:
+            nf += n
+        else:
+            n1 += n
+    g = grad_bytes
+    slots = {"k_came_pass_a": nf * g + n1 * (g + 8), "k_came_pass_b": nf * g,
+             "k_came_pass_c": nf * (g + 8) + n1 * (g + 28), "k_came_pass_d": nf * 12}
+    return slots, sum(slots.values()), (nf + n1) * (g + 16)
+
+
+def run_came(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.workload(args.workload)
+    shapes = [s for _, s in wl.shapes]
+    params = [synth.make_param(s, k, device=dev, std=wl.param_std) for k, s in enumerate(shapes)]
+    grads = [synth.make_grad(s, k, 1, device=dev, std=wl.grad_std, dtype=wl.grad_dtype, kind=wl.grad_kind)
+             for k, s in enumerate(shapes)]
+    states = init_came_state(params)
+    step = CameStep(params, grads, states, **wl.hparams)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(device_uuid(dev)).start()
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    binding.came_profile_read()
+    binding.came_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    w0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        t += 1
+        step(t)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(w0, time.time())
+    clocks.stop()
+    binding.came_profile_enable(False)
+    kernels = binding.came_profile_read()
+    ms_per_step = max_over_ranks(ev0.elapsed_time(ev1), world, dev) / args.steps
+    grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
+    slot_bytes, design_bytes, one_pass_bytes = came_bytes(wl.shapes, grad_bytes)
+    peak, peak_kind = measured_hbm_peak()
+    per_kernel = {}
+    for name, (kms, kn) in kernels.items():
+        if not kn:
+            continue
+        entry = {"ms_per_step": round(kms / args.steps, 4), "launches": kn}
+        if name in slot_bytes and kms > 0:
+            # a slot launches one kernel per tensor class: bytes per step over the slot's time per step
+            entry["gbs"] = round(slot_bytes[name] / (kms / args.steps / 1e3) / 1e9, 1)
+        per_kernel[name] = entry
+    dom_name, (dom_ms, dom_n) = max(kernels.items(), key=lambda kv: kv[1][0])
+    ach = slot_bytes[dom_name] / (dom_ms / args.steps / 1e3) / 1e9
+    roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_source": peak_kind, "traffic": traffic_record(dom_name),
+                "algorithmic_bytes_per_launch": slot_bytes[dom_name], "avg_launch_ms": dom_ms / args.steps}
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_came_e2e(args, wl, params, grads, states, step, t, world, dev)
+    eff = design_bytes / (ms_per_step / 1e3) / 1e9
+    out = {
+        "metric": CAME_METRIC, "value": replica_throughput(wl.numel, world, ms_per_step), "unit": "params/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) fp32 params, N(0,1e-3) bf16 grads resident in HBM)",
+        "config": {"workload": args.workload, "description": wl.description, "params": wl.numel,
+                   "tensors": len(shapes), "param_dtype": "fp32", "grad_dtype": "bf16" if grad_bytes == 2 else "fp32",
+                   "hparams": dict(wl.hparams), "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs (params+grads+states) far larger than L2; no flush"},
+        "effective_gbs": round(eff, 1), "frac_of_hbm_peak": round(eff / peak, 4), "hbm_peak_gbs": peak,
+        "hbm_peak_source": peak_kind, "algorithmic_bytes_per_step": design_bytes,
+        "one_pass_bytes_per_step": one_pass_bytes, "kernels": per_kernel, "roofline": roofline,
+        "gpu_launches": sum(v[1] for v in kernels.values()), "clocks": clocks.summary(), "e2e": e2e,
+    }
+    return out, (wl, wl.numel)
+
+
+def run_came_e2e(args, wl, params, grads, states, step, t, world, dev):
+    """End to end through CameStep: every step copies the step's bf16 grads
+    from pinned host memory (one stream, into the second of two grad buffers
+    while the previous step runs), runs the step, and reads back one value
+    per tensor (the first updated parameter value) to pinned host memory."""
+    n = len(params)
+    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
+    for hg, g in zip(host_g, grads):
+        hg.copy_(g)
+    grads2 = [torch.empty_like(g) for g in grads]
+    steps = [step, CameStep(params, grads2, states, **wl.hparams)]
+    bufs = [grads, grads2]
+    heads = torch.empty(n, dtype=torch.float32, device=dev)
+    host_h = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    s_in = torch.cuda.Stream(dev)
+    s_comp = torch.cuda.current_stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_step = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+    h2d = sum(g.numel() * g.element_size() for g in grads)
+    firsts = [p.view(-1)[:1] for p in params]
+
+    def upload(k):
+        b = k % 2
+        if used[b]:
+            s_in.wait_event(ev_step[b])
+        with torch.cuda.stream(s_in):
+            for j in range(n):
+                bufs[b][j].copy_(host_g[j], non_blocking=True)
+            ev_in[b].record(s_in)
+
+    def compute(k):
+        nonlocal t
+        b = k % 2
+        s_comp.wait_event(ev_in[b])
+        t += 1
+        steps[b](t, stream=s_comp)
+        used[b] = True
+        torch.cat(firsts, out=heads)
+        host_h.copy_(heads, non_blocking=True)
+        ev_step[b].record(s_comp)
+
+    def run(nsteps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(s_comp)
+        s_in.wait_event(e0)
+        upload(0)
+        for k in range(nsteps):
+            if k + 1 < nsteps:
+                upload(k + 1)
+            compute(k)
+        e1.record(s_comp)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / nsteps
+
+    run(2)
+    ms = run(args.e2e_steps)
+    out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": n * 4, "steps": args.e2e_steps, "ms_per_step": ms,
+           "result_read": f"first updated value of each tensor ({n} float32)",
+           "path": "pinned host bf16 grads -> device (double-buffered, 1 copy stream, overlapping the previous "
+                   "step), CameStep, device->host read of one value per tensor"}
+    del host_g, grads2
+    return out
+
+
+def time_came_oracle(wl, idx, steps, t0=1):
+    """The CAME oracle over the sampled tensors; (seconds per step, values)."""
+    import numpy as np
+    from oracle import came as came_oracle
+    came_oracle.build()
+    hp = came_oracle.CameHParams(**wl.hparams)
+    shapes = [wl.shapes[k][1] for k in idx]
+    ps = [synth.make_param(s, k, std=wl.param_std).double().numpy() for s, k in zip(shapes, idx)]
+    sts = [came_oracle.CameState(s) for s in shapes]
+    gs = [synth.make_grad(s, k, 1, std=wl.grad_std, dtype=wl.grad_dtype, kind=wl.grad_kind).double().numpy()
+          for s, k in zip(shapes, idx)]
+    per_step = []
+    for t in range(t0, t0 + steps):
+        a = time.perf_counter()
+        for p, g, st in zip(ps, gs, sts):
+            came_oracle.step(p, g, st, t, hp)
+        per_step.append(time.perf_counter() - a)
+    return per_step, int(sum(np.prod(s) if s else 1 for s in shapes))
+
+
 def time_lamb_oracle(wl, idx, steps, t0=1):
     """The LAMB oracle over the sampled tensors; (seconds per step, values)."""
     import numpy as np
@@ -737,7 +927,7 @@ def time_oracle(wl, idx, steps, t0=1):
 
 def cpu_baseline(wl, steps=2):
     idx = oracle_sample(wl)
-    per_step, n = (time_lamb_oracle if wl.optimizer == "lamb" else time_oracle)(wl, idx, steps)
+    per_step, n = ORACLE_TIMERS[wl.optimizer](wl, idx, steps)
     tot = sum(per_step)
     return {"value": n * steps / tot, "unit": "params/s", "cores": 1, "kind": "oracle",
             "sample": f"{len(idx)} tensors ({n:,} values: "
@@ -746,16 +936,20 @@ def cpu_baseline(wl, steps=2):
             "seconds": tot, "host_cpus": os.cpu_count()}
 
 
+ORACLE_TIMERS = {"adafactor": time_oracle, "lamb": time_lamb_oracle, "came": time_came_oracle}
+
+
 def run_reference(args):
     wl = synth.workload(args.workload)
     idx = oracle_sample(wl)
-    timer = time_lamb_oracle if wl.optimizer == "lamb" else time_oracle
+    timer = ORACLE_TIMERS[wl.optimizer]
     warm, n = timer(wl, idx, args.warmup) if args.warmup else ([], 0)
     per_step, n = timer(wl, idx, args.steps, t0=args.warmup + 1)
     sec = sum(per_step) / len(per_step)
     value = n / sec
     return {
-        "metric": LAMB_METRIC if wl.optimizer == "lamb" else METRIC, "impl": "reference", "value": value, "unit": "params/s", "n_gpus": 1,
+        "metric": {"lamb": LAMB_METRIC, "came": CAME_METRIC}.get(wl.optimizer, METRIC), "impl": "reference",
+        "value": value, "unit": "params/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "description": wl.description, "params": wl.numel,
@@ -775,7 +969,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b",
                     choices=["llama3_8b", "llama3_8b_beta1", "llama3_8b_beta1_int8", "llama_layer", "llama_layer_bf16",
-                             "llama_layer_bf16_int8", "edge", "tiny", "llama3_8b_lamb", "llama_layer_lamb"])
+                             "llama_layer_bf16_int8", "edge", "tiny", "llama3_8b_lamb", "llama_layer_lamb", "llama3_8b_came",
+                             "llama_layer_came"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--readback-steps", type=int, default=2)
     ap.add_argument("--e2e-streams", type=int, default=1,
@@ -795,10 +990,8 @@ def main():
     if world > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    if synth.workload(args.workload).optimizer == "lamb":
-        out, (wl, _) = run_lamb(args, world, rank, local)
-    else:
-        out, (wl, _) = run_ours(args, world, rank, local)
+    runner = {"lamb": run_lamb, "came": run_came}.get(synth.workload(args.workload).optimizer, run_ours)
+    out, (wl, _) = runner(args, world, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl)

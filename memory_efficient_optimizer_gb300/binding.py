@@ -1,5 +1,5 @@
-"""ctypes binding of the C ABI in include/adafactor.h and include/lamb.h
-(argument marshalling only).
+"""ctypes binding of the C ABI in include/adafactor.h, include/lamb.h and
+include/came.h (argument marshalling only).
 
 Every function here has the name of the C entry point it calls and does no
 arithmetic of the method: all of the step runs in the CUDA library.  Loading
@@ -30,6 +30,11 @@ EXPORTS = (
     "adafactor_profile_enable", "adafactor_profile_read", "adafactor_num_kernels",
     "adafactor_kernel_name", "adafactor_step_noalloc", "adafactor_debug_stall_copies",
     "adafactor_shard_sizes", "adafactor_shard_begin", "adafactor_shard_middle", "adafactor_shard_end",
+)
+# Entry points declared in include/came.h.
+CAME_EXPORTS = (
+    "came_default_hparams", "came_validate", "came_workspace_size", "came_step", "came_profile_enable",
+    "came_profile_read", "came_num_kernels", "came_kernel_name",
 )
 # Entry points declared in include/lamb.h.
 LAMB_EXPORTS = (
@@ -73,6 +78,24 @@ class lamb_tensor(ctypes.Structure):
 class lamb_hparams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("bias_correction", ctypes.c_int32)]
+
+
+class came_tensor(ctypes.Structure):
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("grad_dtype", ctypes.c_int32),
+                ("ndim", ctypes.c_int32), ("shape", ctypes.c_int64 * ADAF_MAX_NDIM)]
+
+
+class came_state(ctypes.Structure):
+    _fields_ = [("exp_avg", ctypes.c_void_p), ("exp_avg_sq_row", ctypes.c_void_p),
+                ("exp_avg_sq_col", ctypes.c_void_p), ("exp_avg_res_row", ctypes.c_void_p),
+                ("exp_avg_res_col", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("exp_avg_res", ctypes.c_void_p)]
+
+
+class came_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("eps1", ctypes.c_double), ("eps2", ctypes.c_double),
+                ("clip_threshold", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("beta3", ctypes.c_double), ("weight_decay", ctypes.c_double)]
 
 
 class AdafactorError(RuntimeError):
@@ -145,6 +168,23 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.adafactor_shard_middle.argtypes = shard_head + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.adafactor_shard_end.restype = ctypes.c_int
         lib.adafactor_shard_end.argtypes = shard_head + [ctypes.c_void_p, ctypes.c_void_p]
+        lib.came_default_hparams.restype = None
+        lib.came_default_hparams.argtypes = [P(came_hparams)]
+        lib.came_validate.restype = ctypes.c_int
+        lib.came_validate.argtypes = [P(came_hparams)]
+        lib.came_workspace_size.restype = ctypes.c_int
+        lib.came_workspace_size.argtypes = [P(came_tensor), ctypes.c_int32, P(ctypes.c_size_t)]
+        lib.came_step.restype = ctypes.c_int
+        lib.came_step.argtypes = [P(came_tensor), P(came_state), ctypes.c_int32, ctypes.c_int64, P(came_hparams),
+                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        lib.came_profile_enable.restype = ctypes.c_int
+        lib.came_profile_enable.argtypes = [ctypes.c_int32]
+        lib.came_profile_read.restype = ctypes.c_int
+        lib.came_profile_read.argtypes = [P(ctypes.c_double), P(ctypes.c_int64), ctypes.c_int32]
+        lib.came_num_kernels.restype = ctypes.c_int32
+        lib.came_num_kernels.argtypes = []
+        lib.came_kernel_name.restype = ctypes.c_char_p
+        lib.came_kernel_name.argtypes = [ctypes.c_int32]
         lib.lamb_validate.restype = ctypes.c_int
         lib.lamb_validate.argtypes = [P(lamb_hparams)]
         lib.lamb_workspace_size.restype = ctypes.c_int
@@ -316,3 +356,48 @@ def lamb_profile_read() -> dict:
     launches = (ctypes.c_int64 * nk)()
     _check(load().lamb_profile_read(ms, launches, nk))
     return {lamb_kernel_name(k): (float(ms[k]), int(launches[k])) for k in range(nk)}
+
+
+# ---- CAME (include/came.h) --------------------------------------------------
+
+def came_default_hparams() -> came_hparams:
+    hp = came_hparams()
+    load().came_default_hparams(ctypes.byref(hp))
+    return hp
+
+
+def came_validate(hp: came_hparams) -> None:
+    _check(load().came_validate(ctypes.byref(hp)))
+
+
+def came_workspace_size(tensors, n: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().came_workspace_size(tensors, int(n), ctypes.byref(out)))
+    return int(out.value)
+
+
+def came_step(tensors, states, n: int, step: int, hp: came_hparams, workspace: int, workspace_bytes: int,
+              stream: int) -> None:
+    _check(load().came_step(tensors, states, int(n), int(step), ctypes.byref(hp), ctypes.c_void_p(workspace),
+                            ctypes.c_size_t(workspace_bytes), ctypes.c_void_p(stream)))
+
+
+def came_profile_enable(on: bool) -> None:
+    _check(load().came_profile_enable(1 if on else 0))
+
+
+def came_num_kernels() -> int:
+    return int(load().came_num_kernels())
+
+
+def came_kernel_name(k: int) -> str:
+    return load().came_kernel_name(int(k)).decode()
+
+
+def came_profile_read() -> dict:
+    """{kernel name: (total ms, launches)} for the CAME events recorded since the last read."""
+    nk = came_num_kernels()
+    ms = (ctypes.c_double * nk)()
+    launches = (ctypes.c_int64 * nk)()
+    _check(load().came_profile_read(ms, launches, nk))
+    return {came_kernel_name(k): (float(ms[k]), int(launches[k])) for k in range(nk)}

@@ -1,0 +1,978 @@
+// Multi-tensor CAME step for sm_103a: the C ABI of include/came.h.
+//
+// CAME (the Colossal-AI distributed-optimizer article, overview table and
+// "其余优化器的关键参数速查" / DistributedCAME; the rule is the CAME algorithm of
+// arXiv:2307.02047) keeps Adafactor's factored second moment and adds a
+// momentum m of the clipped update and a factored "instability" statistic
+// of (uh - m)^2 that scales the final step.  Three results are needed over
+// whole slices or tensors before an element can move on (the second-moment
+// factors, RMS(u), the instability factors), so a step is four streaming
+// passes with small reductions between them:
+//
+//   k_came_pass_a   g -> per-tile row and column sums of g^2        (read g)
+//   k_came_stats    row/col EMAs of the means (+ eps1), row-chunk sums
+//   k_came_means    mean(r) per slice
+//   k_came_pass_b   per-tile sum(u^2), u = g (r_i/mean r)^-1/2 c_j^-1/2 (read g)
+//   k_came_clip     coef = 1 / max(1, RMS(u) / d) per tensor
+//   k_came_pass_c   uh = coef u; m <- b1 m + (1-b1) uh; per-tile row/column
+//                   sums of U = (uh - m)^2, formed as (b1 (uh - m_old))^2
+//                   (equal, without the rounding of m)   (read g, m; write m)
+//   k_came_stats    R/C EMAs of the means (+ eps2), row-chunk sums
+//   k_came_means    mean(R) per slice
+//   k_came_pass_d   p <- p - wd lr p - lr m (R_i/mean R)^-1/2 C_j^-1/2
+//                                                     (read m, p; write p)
+//
+// Tensors with ndim < 2 are one row (full per-element v and S); their units
+// run inside pass a (v and sum(u^2)) and pass c (m, S and p) and need no
+// factored statistics.  Factored tensors are cut into tiles of 256 rows x
+// 1024 columns of one slice.  A CTA of 8 warps streams a tile: warp w takes
+// rows w, w + 8, ...; each lane owns 8 consecutive columns per 256-column
+// chunk (16-byte loads; "vec" class) or one column per 32-column chunk
+// ("scalar" class: odd widths, unaligned views), keeps their column sums in
+// registers, and the warp reduces each row with a xor tree.  All sums are
+// deterministic (fixed orders, no atomics).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "adafactor_internal.h"
+#include "came.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTR = 256;          // tile rows
+constexpr int kTC = 1024;         // tile columns
+constexpr int64_t kUnit1D = 8192; // values per 1D work unit
+constexpr int kRowItem = 1024;    // rows per statistics item
+constexpr int kColItem = 256;     // columns per statistics item
+constexpr int kClasses = 3;
+enum Cls : int32_t { kVec = 0, kScalar = 1, k1D = 2 };
+
+struct CDev {
+  float* p;
+  const void* g;
+  float* m;
+  float* row;   // second moment factors [B*H], [B*W]
+  float* col;
+  float* rrow;  // instability factors
+  float* rcol;
+  float* v;     // 1D: full second moment, full instability
+  float* res;
+  int64_t B, H, W, n;
+  int64_t cb, rb;      // column / row tiles per slice
+  int64_t rowpart;     // float offset of [cb][B*H] row partials
+  int64_t colpart;     // float offset of [rb][B*W] column partials
+  int64_t sp0, nsp;    // sum(u^2) partial slots
+  int64_t slice0;      // per-slice mean slots
+  int64_t rc0, nrc;    // row-chunk sum slots: B * nrc
+  int64_t ncc;         // column items per slice
+  int32_t gdt, cls;
+};
+
+struct CArgs {
+  const CDev* dev;
+  const int64_t* pf[kClasses];   // per class: first tile of each member, then the total
+  const int32_t* idx[kClasses];  // per class: tensor index of each member
+  int32_t nmem[kClasses];
+  const int64_t* item_pf;        // statistics items of factored tensors
+  const int32_t* item_idx;
+  int32_t nfact;
+  float* rowpart;
+  float* colpart;
+  double* uspart;
+  double* rchunk;
+  double* mean;   // per slice: mean(r) or mean(R) of the current phase
+  double* coef;   // per tensor
+  int32_t n;
+  int32_t phase;  // statistics kernels: 0 = second moment, 1 = instability
+  float b1, omb1, b2, omb2, b3, omb3, eps1, eps2, lr, wdl, clip;
+};
+
+// ---- loads -----------------------------------------------------------------
+template <int VEC> struct GRaw;
+template <> struct GRaw<8> { uint4 a, b; };
+template <> struct GRaw<1> { float f; };
+
+// 8 (or 1) gradient values at e, of either dtype, widened to fp32 (exact).
+__device__ __forceinline__ void load_g(GRaw<8>& r, const void* g, int gdt, int64_t e) {
+  if (gdt == ADAF_BFLOAT16) {
+    r.a = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(g) + e));
+  } else {
+    const uint4* q = reinterpret_cast<const uint4*>(static_cast<const float*>(g) + e);
+    r.a = __ldcs(q);
+    r.b = __ldcs(q + 1);
+  }
+}
+__device__ __forceinline__ void load_g(GRaw<1>& r, const void* g, int gdt, int64_t e) {
+  r.f = gdt == ADAF_BFLOAT16
+            ? __uint_as_float(static_cast<uint32_t>(__ldcs(static_cast<const unsigned short*>(g) + e)) << 16)
+            : __ldcs(static_cast<const float*>(g) + e);
+}
+__device__ __forceinline__ void widen(const GRaw<8>& r, int gdt, float (&x)[8]) {
+  if (gdt == ADAF_BFLOAT16) {
+    const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(w[k] << 16);
+      x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  } else {
+    const uint32_t w[8] = {r.a.x, r.a.y, r.a.z, r.a.w, r.b.x, r.b.y, r.b.z, r.b.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = __uint_as_float(w[k]);
+  }
+}
+__device__ __forceinline__ void widen(const GRaw<1>& r, int, float (&x)[1]) { x[0] = r.f; }
+
+template <int VEC> __device__ __forceinline__ void load_f(float (&y)[VEC], const float* p);
+template <> __device__ __forceinline__ void load_f<8>(float (&y)[8], const float* p) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w; y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
+}
+template <> __device__ __forceinline__ void load_f<1>(float (&y)[1], const float* p) { y[0] = __ldcs(p); }
+template <int VEC> __device__ __forceinline__ void store_f(float* p, const float (&y)[VEC]);
+template <> __device__ __forceinline__ void store_f<8>(float* p, const float (&y)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(y[4], y[5], y[6], y[7]));
+}
+template <> __device__ __forceinline__ void store_f<1>(float* p, const float (&y)[1]) { __stcs(p, y[0]); }
+
+// ---- reductions --------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// Deterministic CTA sum; the result is valid in thread 0.
+__device__ __forceinline__ double block_sum(double v, double* red) {
+  v = warp_sum_d(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();  // red of the previous use is read
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  double s = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kWarps; ++w) s += red[w];
+  return s;
+}
+
+// ---- tile geometry -------------------------------------------------------------
+template <int VEC> struct Lay {
+  static constexpr int CH = kTC / (32 * VEC);  // chunks per tile row
+  static constexpr int CG = VEC == 8 ? CH : 8;  // chunks loaded together (registers)
+  // lane's first column of chunk k inside the tile
+  static __device__ __forceinline__ int col(int k, int lane) { return k * 32 * VEC + lane * VEC; }
+};
+
+struct Tile {
+  int64_t b, r, c;  // slice, row tile, column tile
+  int64_t i0, i1, j0;
+};
+__device__ __forceinline__ Tile tile_of(const CDev& d, int64_t local) {
+  Tile t;
+  t.c = local % d.cb;
+  const int64_t q = local / d.cb;
+  t.r = q % d.rb;
+  t.b = q / d.rb;
+  t.i0 = t.r * kTR;
+  t.i1 = min(d.H, t.i0 + kTR);
+  t.j0 = t.c * kTC;
+  return t;
+}
+
+// Column sums of the tile's rows, held per lane, added across the warps in
+// warp order through shared memory and stored to the column partials.
+template <int VEC>
+__device__ __forceinline__ void store_col_sums(const CDev& d, const CArgs& a, const Tile& tl,
+                                               const float (&cacc)[Lay<VEC>::CH * VEC], float* colbuf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* mine = colbuf + warp * kTC;
+#pragma unroll
+  for (int k = 0; k < Lay<VEC>::CH; ++k)
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) mine[Lay<VEC>::col(k, lane) + v] = cacc[k * VEC + v];
+  __syncthreads();
+  const int ncl = static_cast<int>(min(static_cast<int64_t>(kTC), d.W - tl.j0));
+  float* cp = a.colpart + d.colpart + tl.r * (d.B * d.W) + tl.b * d.W + tl.j0;
+  for (int cl = threadIdx.x; cl < ncl; cl += kThreads) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += colbuf[w * kTC + cl];
+    cp[cl] = s;
+  }
+  __syncthreads();  // colbuf is reused by the next tile
+}
+
+// Walks the tiles of one class: calls body(d, t, local) for each.
+template <typename Body>
+__device__ __forceinline__ void walk(const CArgs& a, int cls, Body&& body) {
+  const int64_t* pf = a.pf[cls];
+  const int nm = a.nmem[cls];
+  int k = 0;
+  for (int64_t u = blockIdx.x; u < pf[nm]; u += gridDim.x) {
+    while (pf[k + 1] <= u) ++k;
+    const int t = a.idx[cls][k];
+    body(a.dev[t], t, u - pf[k]);
+  }
+}
+
+// ---- pass a: row / column sums of g^2 (factored), v and sum(u^2) (1D) -------
+template <int VEC>
+__device__ __forceinline__ void pass_a_tile(const CDev& d, const CArgs& a, int64_t local, float* colbuf) {
+  constexpr int CH = Lay<VEC>::CH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Tile tl = tile_of(d, local);
+  const int64_t base = tl.b * d.H * d.W;
+  float cacc[CH * VEC];
+#pragma unroll
+  for (int k = 0; k < CH * VEC; ++k) cacc[k] = 0.f;
+  float* rp = a.rowpart + d.rowpart + tl.c * (d.B * d.H) + tl.b * d.H;
+  constexpr int CG = Lay<VEC>::CG;
+  for (int64_t i = tl.i0 + warp; i < tl.i1; i += kWarps) {
+    float rs = 0.f;
+#pragma unroll
+    for (int kg = 0; kg < CH; kg += CG) {
+      if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;  // past the row's end (warp-uniform)
+      GRaw<VEC> raw[CG];
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+        if (j < d.W) load_g(raw[k], d.g, d.gdt, base + i * d.W + j);
+      }
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+        if (j < d.W) {
+          float x[VEC];
+          widen(raw[k], d.gdt, x);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            const float q = x[v] * x[v];
+            cacc[(kg + k) * VEC + v] += q;
+            rs += q;
+          }
+        }
+      }
+    }
+    rs = warp_sum(rs);
+    if (lane == 0) rp[i] = rs;
+  }
+  store_col_sums<VEC>(d, a, tl, cacc, colbuf);
+}
+
+__device__ __forceinline__ void pass_a_1d(const CDev& d, const CArgs& a, int64_t local, double* red) {
+  const int64_t e0 = local * kUnit1D, e1 = min(d.n, e0 + kUnit1D);
+  float acc = 0.f;
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+    GRaw<1> r;
+    load_g(r, d.g, d.gdt, e);
+    const float x = r.f;
+    const float vn = fmaf(a.b2, d.v[e], a.omb2 * fmaf(x, x, a.eps1));
+    d.v[e] = vn;
+    const float u = x * rsqrtf(vn);
+    acc = fmaf(u, u, acc);
+  }
+  const double s = block_sum(static_cast<double>(acc), red);
+  if (threadIdx.x == 0) a.uspart[d.sp0 + local] = s;
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads, 2) k_came_pass_a(const __grid_constant__ CArgs a, int cls) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* colbuf = reinterpret_cast<float*>(smem);
+  double* red = reinterpret_cast<double*>(smem + sizeof(float) * kWarps * kTC);
+  walk(a, cls, [&](const CDev& d, int, int64_t local) {
+    if (cls == k1D) pass_a_1d(d, a, local, red);
+    else pass_a_tile<VEC>(d, a, local, colbuf);
+  });
+}
+
+// ---- statistics: EMAs of the row / column means, row-chunk sums ------------
+// phase 0: r, c from the g^2 partials (beta2, eps1); phase 1: R, C from the
+// U partials (beta3, eps2).  Items: B * nrc row chunks, then B * ncc column
+// chunks of each factored tensor.
+__global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__ CArgs a) {
+  __shared__ double red[kWarps];
+  const float beta = a.phase ? a.b3 : a.b2;
+  const float omb = a.phase ? a.omb3 : a.omb2;
+  const double eps = a.phase ? a.eps2 : a.eps1;
+  int k = 0;
+  for (int64_t it = blockIdx.x; it < a.item_pf[a.nfact]; it += gridDim.x) {
+    while (a.item_pf[k + 1] <= it) ++k;
+    const CDev d = a.dev[a.item_idx[k]];
+    float* rowst = a.phase ? d.rrow : d.row;
+    float* colst = a.phase ? d.rcol : d.col;
+    const int64_t local = it - a.item_pf[k];
+    if (local < d.B * d.nrc) {
+      const int64_t b = local / d.nrc, q = local % d.nrc;
+      const int64_t i0 = q * kRowItem, i1 = min(d.H, i0 + kRowItem);
+      double acc = 0.0;
+      for (int64_t i = i0 + threadIdx.x; i < i1; i += kThreads) {
+        double s = 0.0;
+        for (int64_t c = 0; c < d.cb; ++c) s += a.rowpart[d.rowpart + c * (d.B * d.H) + b * d.H + i];
+        const float mean = static_cast<float>(s / static_cast<double>(d.W) + eps);
+        const float rn = fmaf(beta, rowst[b * d.H + i], omb * mean);
+        rowst[b * d.H + i] = rn;
+        acc += rn;
+      }
+      const double tot = block_sum(acc, red);
+      if (threadIdx.x == 0) a.rchunk[d.rc0 + local] = tot;
+    } else {
+      const int64_t l2 = local - d.B * d.nrc;
+      const int64_t b = l2 / d.ncc, q = l2 % d.ncc;
+      const int64_t j = q * kColItem + threadIdx.x;
+      if (j < d.W) {
+        double s = 0.0;
+        for (int64_t r = 0; r < d.rb; ++r) s += a.colpart[d.colpart + r * (d.B * d.W) + b * d.W + j];
+        const float mean = static_cast<float>(s / static_cast<double>(d.H) + eps);
+        colst[b * d.W + j] = fmaf(beta, colst[b * d.W + j], omb * mean);
+      }
+    }
+  }
+}
+
+// mean(r) (phase 0) or mean(R) (phase 1) of every slice: one CTA per factored tensor.
+__global__ void __launch_bounds__(kThreads) k_came_means(const __grid_constant__ CArgs a) {
+  __shared__ double red[kWarps];
+  const CDev d = a.dev[a.item_idx[blockIdx.x]];
+  for (int64_t b = 0; b < d.B; ++b) {
+    double s = 0.0;
+    for (int64_t q = threadIdx.x; q < d.nrc; q += kThreads) s += a.rchunk[d.rc0 + b * d.nrc + q];
+    const double tot = block_sum(s, red);
+    if (threadIdx.x == 0) a.mean[d.slice0 + b] = tot / static_cast<double>(d.H);
+  }
+}
+
+// ---- pass b: sum(u^2) per tile ------------------------------------------------
+// sum_ij u^2 = sum_i (mean r / r_i) sum_j g^2 / c_j.
+template <int VEC>
+__device__ __forceinline__ void pass_b_tile(const CDev& d, const CArgs& a, int64_t local, float* cinv, double* red) {
+  constexpr int CH = Lay<VEC>::CH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Tile tl = tile_of(d, local);
+  const int64_t base = tl.b * d.H * d.W;
+  const float mr = static_cast<float>(a.mean[d.slice0 + tl.b]);
+  __syncthreads();  // cinv of the previous tile is read
+  for (int cl = threadIdx.x; cl < kTC; cl += kThreads) {
+    const int64_t j = tl.j0 + cl;
+    cinv[cl] = j < d.W ? 1.0f / d.col[tl.b * d.W + j] : 0.f;
+  }
+  __syncthreads();
+  constexpr int CG = Lay<VEC>::CG;
+  float acc = 0.f;
+  for (int64_t i = tl.i0 + warp; i < tl.i1; i += kWarps) {
+    float ts = 0.f;
+#pragma unroll
+    for (int kg = 0; kg < CH; kg += CG) {
+      if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;
+      GRaw<VEC> raw[CG];
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+        if (j < d.W) load_g(raw[k], d.g, d.gdt, base + i * d.W + j);
+      }
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int cl = Lay<VEC>::col(kg + k, lane);
+        if (tl.j0 + cl < d.W) {
+          float x[VEC];
+          widen(raw[k], d.gdt, x);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) ts = fmaf(x[v] * x[v], cinv[cl + v], ts);
+        }
+      }
+    }
+    acc = fmaf(mr / d.row[tl.b * d.H + i], ts, acc);
+  }
+  const double s = block_sum(static_cast<double>(acc), red);
+  if (threadIdx.x == 0) a.uspart[d.sp0 + local] = s;
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads, 2) k_came_pass_b(const __grid_constant__ CArgs a, int cls) {
+  __shared__ __align__(16) float cinv[kTC];
+  __shared__ double red[kWarps];
+  walk(a, cls, [&](const CDev& d, int, int64_t local) { pass_b_tile<VEC>(d, a, local, cinv, red); });
+}
+
+// ---- clip: coef = 1 / max(1, RMS(u) / d), one CTA per tensor ---------------
+__global__ void __launch_bounds__(kThreads) k_came_clip(const __grid_constant__ CArgs a) {
+  __shared__ double red[kWarps];
+  const CDev d = a.dev[blockIdx.x];
+  double s = 0.0;
+  for (int64_t k = threadIdx.x; k < d.nsp; k += kThreads) s += a.uspart[d.sp0 + k];
+  const double tot = block_sum(s, red);
+  if (threadIdx.x == 0) {
+    const double r = d.n > 0 ? sqrt(tot / static_cast<double>(d.n)) / static_cast<double>(a.clip) : 0.0;
+    a.coef[blockIdx.x] = 1.0 / (r > 1.0 ? r : 1.0);
+  }
+}
+
+// ---- pass c: momentum and the instability sums (factored); the whole
+// remaining step of 1D tensors ---------------------------------------------------
+template <int VEC>
+__device__ __forceinline__ void pass_c_tile(const CDev& d, const CArgs& a, int t, int64_t local, float* colbuf,
+                                            float* colf) {
+  constexpr int CH = Lay<VEC>::CH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Tile tl = tile_of(d, local);
+  const int64_t base = tl.b * d.H * d.W;
+  const float mr = static_cast<float>(a.mean[d.slice0 + tl.b]);
+  const float coef = static_cast<float>(a.coef[t]);
+  __syncthreads();  // colf of the previous tile is read
+  for (int cl = threadIdx.x; cl < kTC; cl += kThreads) {
+    const int64_t j = tl.j0 + cl;
+    colf[cl] = j < d.W ? coef * rsqrtf(d.col[tl.b * d.W + j]) : 0.f;
+  }
+  __syncthreads();
+  float cacc[CH * VEC];
+#pragma unroll
+  for (int k = 0; k < CH * VEC; ++k) cacc[k] = 0.f;
+  float* rp = a.rowpart + d.rowpart + tl.c * (d.B * d.H) + tl.b * d.H;
+  constexpr int CG = Lay<VEC>::CG;
+  for (int64_t i = tl.i0 + warp; i < tl.i1; i += kWarps) {
+    const float rf = rsqrtf(d.row[tl.b * d.H + i] / mr);
+    float rs = 0.f;
+#pragma unroll
+    for (int kg = 0; kg < CH; kg += CG) {
+      if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;
+      GRaw<VEC> raw[CG];
+      float mv[CG][VEC];
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+        if (j < d.W) {
+          load_g(raw[k], d.g, d.gdt, base + i * d.W + j);
+          load_f<VEC>(mv[k], d.m + base + i * d.W + j);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int cl = Lay<VEC>::col(kg + k, lane);
+        if (tl.j0 + cl < d.W) {
+          float x[VEC];
+          widen(raw[k], d.gdt, x);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            const float uh = (x[v] * rf) * colf[cl + v];
+            const float dl = a.b1 * (uh - mv[k][v]);  // = uh - m_new, without rounding m_new first
+            const float mn = fmaf(a.b1, mv[k][v], a.omb1 * uh);
+            mv[k][v] = mn;
+            const float q = dl * dl;
+            cacc[(kg + k) * VEC + v] += q;
+            rs += q;
+          }
+          store_f<VEC>(d.m + base + i * d.W + tl.j0 + cl, mv[k]);
+        }
+      }
+    }
+    rs = warp_sum(rs);
+    if (lane == 0) rp[i] = rs;
+  }
+  store_col_sums<VEC>(d, a, tl, cacc, colbuf);
+}
+
+__device__ __forceinline__ void pass_c_1d(const CDev& d, const CArgs& a, int t, int64_t local) {
+  const int64_t e0 = local * kUnit1D, e1 = min(d.n, e0 + kUnit1D);
+  const float coef = static_cast<float>(a.coef[t]);
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+    GRaw<1> r;
+    load_g(r, d.g, d.gdt, e);
+    const float uh = (r.f * rsqrtf(d.v[e])) * coef;
+    const float mo = d.m[e];
+    const float dl = a.b1 * (uh - mo);  // = uh - m_new, without rounding m_new first
+    const float mn = fmaf(a.b1, mo, a.omb1 * uh);
+    d.m[e] = mn;
+    const float sn = fmaf(a.b3, d.res[e], a.omb3 * (dl * dl + a.eps2));
+    d.res[e] = sn;
+    const float p = d.p[e];
+    d.p[e] = fmaf(-a.wdl, p, p - a.lr * (mn * rsqrtf(sn)));
+  }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads, 2) k_came_pass_c(const __grid_constant__ CArgs a, int cls) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* colbuf = reinterpret_cast<float*>(smem);
+  float* colf = colbuf + kWarps * kTC;
+  walk(a, cls, [&](const CDev& d, int t, int64_t local) {
+    if (cls == k1D) pass_c_1d(d, a, t, local);
+    else pass_c_tile<VEC>(d, a, t, local, colbuf, colf);
+  });
+}
+
+// ---- pass d: p <- p - wd lr p - lr m (R_i / mean R)^-1/2 C_j^-1/2 ------------
+template <int VEC>
+__device__ __forceinline__ void pass_d_tile(const CDev& d, const CArgs& a, int64_t local, float* cf) {
+  constexpr int CH = Lay<VEC>::CH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Tile tl = tile_of(d, local);
+  const int64_t base = tl.b * d.H * d.W;
+  const float mR = static_cast<float>(a.mean[d.slice0 + tl.b]);
+  __syncthreads();
+  for (int cl = threadIdx.x; cl < kTC; cl += kThreads) {
+    const int64_t j = tl.j0 + cl;
+    cf[cl] = j < d.W ? a.lr * rsqrtf(d.rcol[tl.b * d.W + j]) : 0.f;
+  }
+  __syncthreads();
+  constexpr int CG = Lay<VEC>::CG;
+  for (int64_t i = tl.i0 + warp; i < tl.i1; i += kWarps) {
+    const float rf = rsqrtf(d.rrow[tl.b * d.H + i] / mR);
+#pragma unroll
+    for (int kg = 0; kg < CH; kg += CG) {
+      if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;
+      float mv[CG][VEC], pv[CG][VEC];
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+        if (j < d.W) {
+          load_f<VEC>(mv[k], d.m + base + i * d.W + j);
+          load_f<VEC>(pv[k], d.p + base + i * d.W + j);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < CG; ++k) {
+        const int cl = Lay<VEC>::col(kg + k, lane);
+        if (tl.j0 + cl < d.W) {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            const float upd = (mv[k][v] * rf) * cf[cl + v];
+            pv[k][v] = fmaf(-a.wdl, pv[k][v], pv[k][v] - upd);
+          }
+          store_f<VEC>(d.p + base + i * d.W + tl.j0 + cl, pv[k]);
+        }
+      }
+    }
+  }
+}
+
+template <int VEC>
+__global__ void __launch_bounds__(kThreads, 2) k_came_pass_d(const __grid_constant__ CArgs a, int cls) {
+  __shared__ __align__(16) float cf[kTC];
+  walk(a, cls, [&](const CDev& d, int, int64_t local) { pass_d_tile<VEC>(d, a, local, cf); });
+}
+
+// ---- host side ------------------------------------------------------------------
+adaf_status fail(adaf_status st, const std::string& msg) { return meo::set_last_error(st, msg.c_str()); }
+adaf_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ADAF_ERR_CUDA, std::string("came: ") + what + ": " + cudaGetErrorString(e));
+}
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr size_t kColbufBytes = sizeof(float) * kWarps * kTC;
+constexpr size_t kPassASmem = kColbufBytes + sizeof(double) * kWarps;
+constexpr size_t kPassCSmem = kColbufBytes + sizeof(float) * kTC;
+
+// The plan of one call: descriptors, class lists, statistics items, offsets.
+struct Plan {
+  std::vector<CDev> dev;
+  std::vector<int64_t> pf[kClasses];
+  std::vector<int32_t> idx[kClasses];
+  std::vector<int64_t> item_pf;
+  std::vector<int32_t> item_idx;
+  int64_t rowpart = 0, colpart = 0, usp = 0, slices = 0, rchunks = 0;
+  size_t off_hdr = 0, hdr_bytes = 0, off_pf[kClasses] = {}, off_idx[kClasses] = {}, off_ipf = 0, off_iidx = 0;
+  size_t off_rowpart = 0, off_colpart = 0, off_usp = 0, off_rchunk = 0, off_mean0 = 0, off_mean1 = 0, off_coef = 0;
+  size_t bytes = 0;
+};
+
+adaf_status make_plan(const came_tensor* tensors, const came_state* states, int32_t n, bool need_ptrs, Plan* P) {
+  if (n < 0) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: n < 0");
+  if (n > 0 && tensors == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: tensors is NULL");
+  if (need_ptrs && n > 0 && states == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: states is NULL");
+  P->dev.resize(n);
+  for (int c = 0; c < kClasses; ++c) P->pf[c].assign(1, 0);
+  P->item_pf.assign(1, 0);
+  for (int32_t t = 0; t < n; ++t) {
+    const came_tensor& x = tensors[t];
+    const std::string who = "came: tensor " + std::to_string(t);
+    if (x.ndim < 0 || x.ndim > ADAF_MAX_NDIM) return fail(ADAF_ERR_INVALID_ARGUMENT, who + ": bad ndim");
+    if (x.grad_dtype != ADAF_FLOAT32 && x.grad_dtype != ADAF_BFLOAT16)
+      return fail(ADAF_ERR_INVALID_ARGUMENT, who + ": unknown grad_dtype");
+    int64_t numel = 1;
+    for (int32_t k = 0; k < x.ndim; ++k) {
+      if (x.shape[k] < 0) return fail(ADAF_ERR_INVALID_ARGUMENT, who + ": negative dim");
+      if (x.shape[k] > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, who + ": a dim above 2^31");
+      numel = x.shape[k] == 0 ? 0 : numel;
+      if (numel > 0 && numel > (int64_t{1} << 40) / x.shape[k]) return fail(ADAF_ERR_UNSUPPORTED, who + ": more than 2^40 values");
+      numel *= x.shape[k];
+    }
+    CDev d{};
+    d.n = numel;
+    d.gdt = x.grad_dtype;
+    const bool fact = x.ndim >= 2;
+    d.H = fact ? x.shape[x.ndim - 2] : 1;
+    d.W = fact ? x.shape[x.ndim - 1] : numel;
+    d.B = (fact && d.H > 0 && d.W > 0) ? numel / (d.H * d.W) : 1;
+    if (need_ptrs && numel > 0) {
+      const came_state& s = states[t];
+      if (!x.p || !x.g || !s.exp_avg) return fail(ADAF_ERR_INVALID_ARGUMENT, who + ": NULL p, g or exp_avg");
+      if (fact && (!s.exp_avg_sq_row || !s.exp_avg_sq_col || !s.exp_avg_res_row || !s.exp_avg_res_col))
+        return fail(ADAF_ERR_INVALID_ARGUMENT, who + ": factored state pointer is NULL");
+      if (!fact && (!s.exp_avg_sq || !s.exp_avg_res))
+        return fail(ADAF_ERR_INVALID_ARGUMENT, who + ": exp_avg_sq / exp_avg_res is NULL");
+      const size_t ge = x.grad_dtype == ADAF_BFLOAT16 ? 2 : 4;
+      if (!aligned(x.p, 4) || !aligned(x.g, ge) || !aligned(s.exp_avg, 4))
+        return fail(ADAF_ERR_INVALID_ARGUMENT, who + ": not element-aligned");
+      d.p = x.p;
+      d.g = x.g;
+      d.m = s.exp_avg;
+      d.row = s.exp_avg_sq_row;
+      d.col = s.exp_avg_sq_col;
+      d.rrow = s.exp_avg_res_row;
+      d.rcol = s.exp_avg_res_col;
+      d.v = s.exp_avg_sq;
+      d.res = s.exp_avg_res;
+    }
+    int64_t ntiles = 0;
+    if (numel == 0) {
+      d.cls = k1D;
+    } else if (fact) {
+      const bool vec = d.W % 8 == 0 && (!need_ptrs || (aligned(d.p, 16) && aligned(d.g, 16) && aligned(d.m, 16)));
+      d.cls = vec ? kVec : kScalar;
+      d.cb = cdiv(d.W, kTC);
+      d.rb = cdiv(d.H, kTR);
+      ntiles = d.B * d.rb * d.cb;
+      d.rowpart = P->rowpart;
+      P->rowpart += d.cb * d.B * d.H;
+      d.colpart = P->colpart;
+      P->colpart += d.rb * d.B * d.W;
+      d.slice0 = P->slices;
+      P->slices += d.B;
+      d.nrc = cdiv(d.H, kRowItem);
+      d.ncc = cdiv(d.W, kColItem);
+      d.rc0 = P->rchunks;
+      P->rchunks += d.B * d.nrc;
+      P->item_idx.push_back(t);
+      P->item_pf.push_back(P->item_pf.back() + d.B * (d.nrc + d.ncc));
+    } else {
+      d.cls = k1D;
+      ntiles = cdiv(numel, kUnit1D);
+    }
+    d.sp0 = P->usp;
+    d.nsp = ntiles;
+    P->usp += ntiles;
+    if (ntiles > 0) {
+      P->idx[d.cls].push_back(t);
+      P->pf[d.cls].push_back(P->pf[d.cls].back() + ntiles);
+    }
+    P->dev[t] = d;
+  }
+  for (int c = 0; c < kClasses; ++c)
+    if (P->pf[c].back() > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, "came: more than 2^31 tiles");
+  if (P->item_pf.back() > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, "came: more than 2^31 statistics items");
+  // layout: header (descriptors, class lists, items), then the scratch arrays
+  size_t o = 0;
+  P->off_hdr = o;
+  o += sizeof(CDev) * n;
+  for (int c = 0; c < kClasses; ++c) {
+    o = round_up(o, 8);
+    P->off_pf[c] = o;
+    o += sizeof(int64_t) * P->pf[c].size();
+    P->off_idx[c] = o;
+    o += sizeof(int32_t) * P->idx[c].size();
+  }
+  o = round_up(o, 8);
+  P->off_ipf = o;
+  o += sizeof(int64_t) * P->item_pf.size();
+  P->off_iidx = o;
+  o += sizeof(int32_t) * P->item_idx.size();
+  P->hdr_bytes = o - P->off_hdr;
+  o = round_up(o, 256);
+  P->off_rowpart = o; o = round_up(o + sizeof(float) * P->rowpart, 256);
+  P->off_colpart = o; o = round_up(o + sizeof(float) * P->colpart, 256);
+  P->off_usp = o;     o = round_up(o + sizeof(double) * P->usp, 256);
+  P->off_rchunk = o;  o = round_up(o + sizeof(double) * P->rchunks, 256);
+  P->off_mean0 = o;   o = round_up(o + sizeof(double) * P->slices, 256);
+  P->off_mean1 = o;   o = round_up(o + sizeof(double) * P->slices, 256);
+  P->off_coef = o;    o = round_up(o + sizeof(double) * n, 256);
+  P->bytes = o;
+  return ADAF_OK;
+}
+
+adaf_status check_hp(const came_hparams* hp) {
+  if (hp == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: hparams is NULL");
+  if (!std::isfinite(hp->lr) || hp->lr < 0.0) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: invalid learning rate");
+  if (!std::isfinite(hp->eps1) || hp->eps1 < 0.0 || !std::isfinite(hp->eps2) || hp->eps2 < 0.0)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "came: invalid eps");
+  if (!std::isfinite(hp->clip_threshold) || hp->clip_threshold <= 0.0)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "came: invalid clip_threshold (needs > 0)");
+  const double b[3] = {hp->beta1, hp->beta2, hp->beta3};
+  for (int k = 0; k < 3; ++k)
+    if (!std::isfinite(b[k]) || b[k] < 0.0 || b[k] >= 1.0)
+      return fail(ADAF_ERR_INVALID_ARGUMENT, "came: invalid beta" + std::to_string(k + 1) + " (needs 0 <= beta < 1)");
+  if (!std::isfinite(hp->weight_decay) || hp->weight_decay < 0.0)
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "came: invalid weight_decay");
+  return ADAF_OK;
+}
+
+constexpr int kRing = 4;
+struct Slot {
+  void* host = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;
+  bool used = false;
+};
+struct DeviceState {
+  Slot ring[kRing];
+  int next = 0;
+  int sms = 0;
+  std::vector<cudaEvent_t> free_events;
+};
+
+enum KernelSlot { kSA = 0, kSStats, kSMeans, kSB, kSClip, kSC, kSD, kNumKernels };
+const char* const kKernelNames[kNumKernels] = {"k_came_pass_a", "k_came_stats", "k_came_means", "k_came_pass_b",
+                                               "k_came_clip",   "k_came_pass_c", "k_came_pass_d"};
+struct ProfRecord {
+  int slot, device;
+  cudaEvent_t start, stop;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+bool g_profile = false;
+std::vector<ProfRecord> g_prof;
+
+cudaError_t get_event(DeviceState& ds, cudaEvent_t* ev) {
+  if (!ds.free_events.empty()) {
+    *ev = ds.free_events.back();
+    ds.free_events.pop_back();
+    return cudaSuccess;
+  }
+  return cudaEventCreate(ev);
+}
+
+bool g_attr_done = false;
+cudaError_t set_smem_attrs() {
+  if (g_attr_done) return cudaSuccess;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_a<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassASmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_a<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassASmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_c<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_c<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
+  g_attr_done = true;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+void came_default_hparams(came_hparams* hp) {
+  if (hp == nullptr) return;
+  hp->lr = 0.0;
+  hp->eps1 = 1e-30;
+  hp->eps2 = 1e-16;
+  hp->clip_threshold = 1.0;
+  hp->beta1 = 0.9;
+  hp->beta2 = 0.999;
+  hp->beta3 = 0.9999;
+  hp->weight_decay = 0.0;
+}
+
+adaf_status came_validate(const came_hparams* hp) { return check_hp(hp); }
+
+adaf_status came_workspace_size(const came_tensor* tensors, int32_t n, size_t* bytes) {
+  if (bytes == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: bytes is NULL");
+  Plan P;
+  adaf_status st = make_plan(tensors, nullptr, n, false, &P);
+  if (st != ADAF_OK) return st;
+  *bytes = n == 0 ? 0 : P.bytes;
+  return ADAF_OK;
+}
+
+adaf_status came_step(const came_tensor* tensors, const came_state* states, int32_t n, int64_t step,
+                      const came_hparams* hp, void* workspace, size_t workspace_bytes, void* stream) {
+  adaf_status st = check_hp(hp);
+  if (st != ADAF_OK) return st;
+  if (step < 1) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: step must be >= 1");
+  Plan P;
+  st = make_plan(tensors, states, n, true, &P);
+  if (st != ADAF_OK) return st;
+  if (n == 0) return ADAF_OK;
+  if (workspace == nullptr || !aligned(workspace, 256))
+    return fail(ADAF_ERR_INVALID_ARGUMENT, "came: workspace is NULL or not 256-byte aligned");
+  if (workspace_bytes < P.bytes)
+    return fail(ADAF_ERR_WORKSPACE_TOO_SMALL, "came: workspace needs " + std::to_string(P.bytes) + " bytes");
+
+  std::vector<unsigned char> h(P.hdr_bytes);
+  std::memcpy(h.data(), P.dev.data(), sizeof(CDev) * n);
+  for (int c = 0; c < kClasses; ++c) {
+    std::memcpy(h.data() + P.off_pf[c], P.pf[c].data(), sizeof(int64_t) * P.pf[c].size());
+    if (!P.idx[c].empty()) std::memcpy(h.data() + P.off_idx[c], P.idx[c].data(), sizeof(int32_t) * P.idx[c].size());
+  }
+  std::memcpy(h.data() + P.off_ipf, P.item_pf.data(), sizeof(int64_t) * P.item_pf.size());
+  if (!P.item_idx.empty()) std::memcpy(h.data() + P.off_iidx, P.item_idx.data(), sizeof(int32_t) * P.item_idx.size());
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  CArgs a{};
+  a.dev = reinterpret_cast<const CDev*>(ws + P.off_hdr);
+  for (int c = 0; c < kClasses; ++c) {
+    a.pf[c] = reinterpret_cast<const int64_t*>(ws + P.off_pf[c]);
+    a.idx[c] = reinterpret_cast<const int32_t*>(ws + P.off_idx[c]);
+    a.nmem[c] = static_cast<int32_t>(P.idx[c].size());
+  }
+  a.item_pf = reinterpret_cast<const int64_t*>(ws + P.off_ipf);
+  a.item_idx = reinterpret_cast<const int32_t*>(ws + P.off_iidx);
+  a.nfact = static_cast<int32_t>(P.item_idx.size());
+  a.rowpart = reinterpret_cast<float*>(ws + P.off_rowpart);
+  a.colpart = reinterpret_cast<float*>(ws + P.off_colpart);
+  a.uspart = reinterpret_cast<double*>(ws + P.off_usp);
+  a.rchunk = reinterpret_cast<double*>(ws + P.off_rchunk);
+  a.coef = reinterpret_cast<double*>(ws + P.off_coef);
+  a.n = n;
+  a.b1 = static_cast<float>(hp->beta1);
+  a.omb1 = static_cast<float>(1.0 - hp->beta1);
+  a.b2 = static_cast<float>(hp->beta2);
+  a.omb2 = static_cast<float>(1.0 - hp->beta2);
+  a.b3 = static_cast<float>(hp->beta3);
+  a.omb3 = static_cast<float>(1.0 - hp->beta3);
+  a.eps1 = static_cast<float>(hp->eps1);
+  a.eps2 = static_cast<float>(hp->eps2);
+  a.lr = static_cast<float>(hp->lr);
+  a.wdl = static_cast<float>(hp->weight_decay * hp->lr);
+  a.clip = static_cast<float>(hp->clip_threshold);
+  double* mean0 = reinterpret_cast<double*>(ws + P.off_mean0);
+  double* mean1 = reinterpret_cast<double*>(ws + P.off_mean1);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if ((err = set_smem_attrs()) != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute");
+  DeviceState& ds = g_dev[device];
+  if (ds.sms == 0 && (err = cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+    return cuda_fail(err, "cudaDeviceGetAttribute");
+  Slot& sl = ds.ring[ds.next];
+  ds.next = (ds.next + 1) % kRing;
+  if (sl.used && (err = cudaEventSynchronize(sl.done)) != cudaSuccess)
+    return cuda_fail(err, "cudaEventSynchronize (upload ring)");
+  if (sl.cap < P.hdr_bytes) {
+    if (sl.host) cudaFreeHost(sl.host);
+    sl.host = nullptr;
+    sl.cap = 0;
+    if ((err = cudaMallocHost(&sl.host, P.hdr_bytes)) != cudaSuccess) return cuda_fail(err, "cudaMallocHost");
+    sl.cap = P.hdr_bytes;
+  }
+  if (sl.done == nullptr && (err = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess)
+    return cuda_fail(err, "cudaEventCreate");
+  std::memcpy(sl.host, h.data(), P.hdr_bytes);
+  if ((err = cudaMemcpyAsync(ws + P.off_hdr, sl.host, P.hdr_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(err, "cudaMemcpyAsync (descriptors)");
+  if ((err = cudaEventRecord(sl.done, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
+  sl.used = true;
+
+  const int persist = 2 * ds.sms;  // 2 CTAs of 256 threads per SM
+  auto grid_for = [&](int64_t units) { return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(persist, units))); };
+  const int64_t tiles[kClasses] = {P.pf[kVec].back(), P.pf[kScalar].back(), P.pf[k1D].back()};
+  const int64_t items = P.item_pf.back();
+
+  // launch helper: profiling events around each launch
+  auto launch = [&](int slot, auto&& fn) -> adaf_status {
+    ProfRecord rec{slot, device, nullptr, nullptr};
+    cudaError_t e;
+    if (g_profile) {
+      if ((e = get_event(ds, &rec.start)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate (profile)");
+      if ((e = get_event(ds, &rec.stop)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate (profile)");
+      if ((e = cudaEventRecord(rec.start, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord (profile)");
+    }
+    fn();
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, kKernelNames[slot]);
+    if (g_profile) {
+      if ((e = cudaEventRecord(rec.stop, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord (profile)");
+      g_prof.push_back(rec);
+    }
+    return ADAF_OK;
+  };
+#define CAME_TRY(x)                 \
+  do {                              \
+    adaf_status st_ = (x);          \
+    if (st_ != ADAF_OK) return st_; \
+  } while (0)
+
+  // pass a (and the 1D second moment + sum(u^2))
+  CAME_TRY(launch(kSA, [&] {
+    if (tiles[kVec]) k_came_pass_a<8><<<grid_for(tiles[kVec]), kThreads, kPassASmem, s>>>(a, kVec);
+    if (tiles[kScalar]) k_came_pass_a<1><<<grid_for(tiles[kScalar]), kThreads, kPassASmem, s>>>(a, kScalar);
+    if (tiles[k1D]) k_came_pass_a<1><<<grid_for(tiles[k1D]), kThreads, kPassASmem, s>>>(a, k1D);
+  }));
+  if (items) {
+    a.phase = 0;
+    a.mean = mean0;
+    CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
+    CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
+    CAME_TRY(launch(kSB, [&] {
+      if (tiles[kVec]) k_came_pass_b<8><<<grid_for(tiles[kVec]), kThreads, 0, s>>>(a, kVec);
+      if (tiles[kScalar]) k_came_pass_b<1><<<grid_for(tiles[kScalar]), kThreads, 0, s>>>(a, kScalar);
+    }));
+  }
+  CAME_TRY(launch(kSClip, [&] { k_came_clip<<<n, kThreads, 0, s>>>(a); }));
+  CAME_TRY(launch(kSC, [&] {
+    if (tiles[kVec]) k_came_pass_c<8><<<grid_for(tiles[kVec]), kThreads, kPassCSmem, s>>>(a, kVec);
+    if (tiles[kScalar]) k_came_pass_c<1><<<grid_for(tiles[kScalar]), kThreads, kPassCSmem, s>>>(a, kScalar);
+    if (tiles[k1D]) k_came_pass_c<1><<<grid_for(tiles[k1D]), kThreads, kPassCSmem, s>>>(a, k1D);
+  }));
+  if (items) {
+    a.phase = 1;
+    a.mean = mean1;
+    CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
+    CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
+    CAME_TRY(launch(kSD, [&] {
+      if (tiles[kVec]) k_came_pass_d<8><<<grid_for(tiles[kVec]), kThreads, 0, s>>>(a, kVec);
+      if (tiles[kScalar]) k_came_pass_d<1><<<grid_for(tiles[kScalar]), kThreads, 0, s>>>(a, kScalar);
+    }));
+  }
+#undef CAME_TRY
+  return ADAF_OK;
+}
+
+adaf_status came_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_profile = on != 0;
+  return ADAF_OK;
+}
+
+adaf_status came_profile_read(double* ms, int64_t* launches, int32_t nk) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  adaf_status st = ADAF_OK;
+  for (ProfRecord& r : g_prof) {
+    float el = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&el, r.start, r.stop);
+    if (e != cudaSuccess && st == ADAF_OK) st = cuda_fail(e, "profile event");
+    if (r.slot < nk) {
+      if (ms) ms[r.slot] += el;
+      if (launches) launches[r.slot] += 1;
+    }
+    DeviceState& ds = g_dev[r.device];
+    ds.free_events.push_back(r.start);
+    ds.free_events.push_back(r.stop);
+  }
+  g_prof.clear();
+  return st;
+}
+
+int32_t came_num_kernels(void) { return kNumKernels; }
+
+const char* came_kernel_name(int32_t k) { return (k >= 0 && k < kNumKernels) ? kKernelNames[k] : ""; }
+
+}  // extern "C"

@@ -23,6 +23,10 @@ Workloads (shapes as PyTorch [out, in] weights):
                     defaults: lr 1e-3, betas (0.9, 0.999), eps 1e-6, bias
                     correction, weight decay 0.01) on the Llama-3-8B list or one
                     decoder layer; fp32 p, bf16 g ~ N(0, 1e-3).
+  * ``llama3_8b_came``, ``llama_layer_came``  the CAME step (article
+                    defaults: eps (1e-30, 1e-16), clip 1.0, betas (0.9, 0.999,
+                    0.9999); lr 1e-4 and weight decay 0.01 chosen here, since
+                    the article gives no lr) on the same shapes, bf16 g.
   * ``edge``        1x65536, 65536x1, 4097x3, 3x4097, 17x100003,
                     [8,1024,1024] and 2,000 matrices with H, W ~ U[1, 512];
                     fp32, g ~ N(0, 1e-2), defaults plus beta1 0.9, 10 steps.
@@ -84,7 +88,7 @@ class Workload:
     grad_kind: str = "normal"         # "normal" | "student_t_zero_rows"
     param_std: float = 0.02
     description: str = ""
-    optimizer: str = "adafactor"      # "adafactor" | "lamb"
+    optimizer: str = "adafactor"      # "adafactor" | "lamb" | "came"
     extra: dict = field(default_factory=dict)
 
     @property
@@ -131,6 +135,14 @@ def workload(name: str, seed: int = 0) -> Workload:
         return Workload(name, llama_layer_shapes(), torch.bfloat16, 1e-3, dict(weight_decay=0.01), 5,
                         description="one Llama-3-8B decoder layer, LAMB (article defaults, wd 0.01), "
                                     "bf16 grads", optimizer="lamb")
+    if name == "llama3_8b_came":
+        return Workload(name, llama3_8b_shapes(), torch.bfloat16, 1e-3, dict(lr=1e-4, weight_decay=0.01), 5,
+                        description="Llama-3-8B shapes, CAME (eps (1e-30, 1e-16), clip 1.0, betas (0.9, 0.999, "
+                                    "0.9999), lr 1e-4, wd 0.01), bf16 grads", optimizer="came")
+    if name == "llama_layer_came":
+        return Workload(name, llama_layer_shapes(), torch.bfloat16, 1e-3, dict(lr=1e-4, weight_decay=0.01), 5,
+                        description="one Llama-3-8B decoder layer, CAME (article defaults, lr 1e-4, wd 0.01), "
+                                    "bf16 grads", optimizer="came")
     if name == "edge":
         return Workload(name, edge_shapes(seed), torch.float32, 1e-2, dict(beta1=0.9), 10,
                         description="edge shapes + 2,000 small matrices, fp32, beta1 0.9")
