@@ -244,34 +244,44 @@ __device__ __forceinline__ void pass_a_tile(const CDev& d, const CArgs& a, int64
   for (int k = 0; k < CH * VEC; ++k) cacc[k] = 0.f;
   float* rp = a.rowpart + d.rowpart + tl.c * (d.B * d.H) + tl.b * d.H;
   constexpr int CG = Lay<VEC>::CG;
-  for (int64_t i = tl.i0 + warp; i < tl.i1; i += kWarps) {
-    float rs = 0.f;
+  constexpr int RPI = 2;  // rows per iteration (rows i, i + kWarps): twice the loads in flight
+  for (int64_t i = tl.i0 + warp; i < tl.i1; i += RPI * kWarps) {
+    float rs[RPI];
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) rs[rr] = 0.f;
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
       if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;  // past the row's end (warp-uniform)
-      GRaw<VEC> raw[CG];
+      GRaw<VEC> raw[RPI][CG];
 #pragma unroll
-      for (int k = 0; k < CG; ++k) {
-        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
-        if (j < d.W) load_g(raw[k], d.g, d.gdt, base + i * d.W + j);
-      }
+      for (int rr = 0; rr < RPI; ++rr)
 #pragma unroll
-      for (int k = 0; k < CG; ++k) {
-        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
-        if (j < d.W) {
-          float x[VEC];
-          widen(raw[k], d.gdt, x);
+        for (int k = 0; k < CG; ++k) {
+          const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+          if (i + rr * kWarps < tl.i1 && j < d.W) load_g(raw[rr][k], d.g, d.gdt, base + (i + rr * kWarps) * d.W + j);
+        }
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) {
-            const float q = x[v] * x[v];
-            cacc[(kg + k) * VEC + v] += q;
-            rs += q;
+      for (int rr = 0; rr < RPI; ++rr)
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+          const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+          if (i + rr * kWarps < tl.i1 && j < d.W) {
+            float x[VEC];
+            widen(raw[rr][k], d.gdt, x);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+              const float q = x[v] * x[v];
+              cacc[(kg + k) * VEC + v] += q;
+              rs[rr] += q;
+            }
           }
         }
-      }
     }
-    rs = warp_sum(rs);
-    if (lane == 0) rp[i] = rs;
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) {
+      const float t = warp_sum(rs[rr]);
+      if (lane == 0 && i + rr * kWarps < tl.i1) rp[i + rr * kWarps] = t;
+    }
   }
   store_col_sums<VEC>(d, a, tl, cacc, colbuf);
 }
@@ -376,29 +386,38 @@ __device__ __forceinline__ void pass_b_tile(const CDev& d, const CArgs& a, int64
   __syncthreads();
   constexpr int CG = Lay<VEC>::CG;
   float acc = 0.f;
-  for (int64_t i = tl.i0 + warp; i < tl.i1; i += kWarps) {
-    float ts = 0.f;
+  constexpr int RPI = 2;  // rows per iteration (rows i, i + kWarps): twice the loads in flight
+  for (int64_t i = tl.i0 + warp; i < tl.i1; i += RPI * kWarps) {
+    float ts[RPI];
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr) ts[rr] = 0.f;
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
       if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;
-      GRaw<VEC> raw[CG];
+      GRaw<VEC> raw[RPI][CG];
 #pragma unroll
-      for (int k = 0; k < CG; ++k) {
-        const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
-        if (j < d.W) load_g(raw[k], d.g, d.gdt, base + i * d.W + j);
-      }
+      for (int rr = 0; rr < RPI; ++rr)
 #pragma unroll
-      for (int k = 0; k < CG; ++k) {
-        const int cl = Lay<VEC>::col(kg + k, lane);
-        if (tl.j0 + cl < d.W) {
-          float x[VEC];
-          widen(raw[k], d.gdt, x);
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) ts = fmaf(x[v] * x[v], cinv[cl + v], ts);
+        for (int k = 0; k < CG; ++k) {
+          const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
+          if (i + rr * kWarps < tl.i1 && j < d.W) load_g(raw[rr][k], d.g, d.gdt, base + (i + rr * kWarps) * d.W + j);
         }
-      }
+#pragma unroll
+      for (int rr = 0; rr < RPI; ++rr)
+#pragma unroll
+        for (int k = 0; k < CG; ++k) {
+          const int cl = Lay<VEC>::col(kg + k, lane);
+          if (i + rr * kWarps < tl.i1 && tl.j0 + cl < d.W) {
+            float x[VEC];
+            widen(raw[rr][k], d.gdt, x);
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) ts[rr] = fmaf(x[v] * x[v], cinv[cl + v], ts[rr]);
+          }
+        }
     }
-    acc = fmaf(mr / d.row[tl.b * d.H + i], ts, acc);
+#pragma unroll
+    for (int rr = 0; rr < RPI; ++rr)
+      if (i + rr * kWarps < tl.i1) acc = fmaf(mr / d.row[tl.b * d.H + i + rr * kWarps], ts[rr], acc);
   }
   const double s = block_sum(static_cast<double>(acc), red);
   if (threadIdx.x == 0) a.uspart[d.sp0 + local] = s;
