@@ -55,8 +55,9 @@ constexpr int kTC = 1024;         // tile columns
 constexpr int64_t kUnit1D = 8192; // values per 1D work unit
 constexpr int kRowItem = 1024;    // rows per statistics item
 constexpr int kColItem = 256;     // columns per statistics item
-constexpr int kClasses = 3;
-enum Cls : int32_t { kVec = 0, kScalar = 1, k1D = 2 };
+constexpr int kClasses = 4;
+// vector path with bf16 / fp32 gradients, one column per lane, 1D
+enum Cls : int32_t { kVecBF = 0, kVecF = 1, kScalar = 2, k1D = 3 };
 
 struct CDev {
   float* p;
@@ -148,6 +149,33 @@ template <> __device__ __forceinline__ void store_f<8>(float* p, const float (&y
 }
 template <> __device__ __forceinline__ void store_f<1>(float* p, const float (&y)[1]) { __stcs(p, y[0]); }
 
+// Gradient loads of the tile passes.  GK = 0: the dtype is read at run time
+// (fp32 vectors take two 16-byte loads); GK = 1: bf16 on the vector path,
+// one 16-byte load into 4 registers, which leaves room for more rows in
+// flight in the read-only passes.
+struct GRawB8 { uint4 a; };
+template <int VEC, int GK> struct GSel {
+  using Raw = GRaw<VEC>;
+  static constexpr int RPI_A = 2, RPI_B = 2;  // rows per iteration, passes a and b
+  static __device__ __forceinline__ void load(Raw& r, const void* g, int gdt, int64_t e) { load_g(r, g, gdt, e); }
+  static __device__ __forceinline__ void unpack(const Raw& r, int gdt, float (&x)[VEC]) { widen(r, gdt, x); }
+};
+template <> struct GSel<8, 1> {
+  using Raw = GRawB8;
+  static constexpr int RPI_A = 3, RPI_B = 4;
+  static __device__ __forceinline__ void load(Raw& r, const void* g, int, int64_t e) {
+    r.a = __ldcs(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(g) + e));
+  }
+  static __device__ __forceinline__ void unpack(const Raw& r, int, float (&x)[8]) {
+    const uint32_t w[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = __uint_as_float(w[k] << 16);
+      x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+};
+
 // ---- reductions --------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -233,7 +261,7 @@ __device__ __forceinline__ void walk(const CArgs& a, int cls, Body&& body) {
 }
 
 // ---- pass a: row / column sums of g^2 (factored), v and sum(u^2) (1D) -------
-template <int VEC>
+template <int VEC, int GK>
 __device__ __forceinline__ void pass_a_tile(const CDev& d, const CArgs& a, int64_t local, float* colbuf) {
   constexpr int CH = Lay<VEC>::CH;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -244,7 +272,8 @@ __device__ __forceinline__ void pass_a_tile(const CDev& d, const CArgs& a, int64
   for (int k = 0; k < CH * VEC; ++k) cacc[k] = 0.f;
   float* rp = a.rowpart + d.rowpart + tl.c * (d.B * d.H) + tl.b * d.H;
   constexpr int CG = Lay<VEC>::CG;
-  constexpr int RPI = 2;  // rows per iteration (rows i, i + kWarps): twice the loads in flight
+  using G = GSel<VEC, GK>;
+  constexpr int RPI = G::RPI_A;  // rows per iteration (rows i, i + kWarps, ...): more loads in flight
   for (int64_t i = tl.i0 + warp; i < tl.i1; i += RPI * kWarps) {
     float rs[RPI];
 #pragma unroll
@@ -252,13 +281,13 @@ __device__ __forceinline__ void pass_a_tile(const CDev& d, const CArgs& a, int64
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
       if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;  // past the row's end (warp-uniform)
-      GRaw<VEC> raw[RPI][CG];
+      typename G::Raw raw[RPI][CG];
 #pragma unroll
       for (int rr = 0; rr < RPI; ++rr)
 #pragma unroll
         for (int k = 0; k < CG; ++k) {
           const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
-          if (i + rr * kWarps < tl.i1 && j < d.W) load_g(raw[rr][k], d.g, d.gdt, base + (i + rr * kWarps) * d.W + j);
+          if (i + rr * kWarps < tl.i1 && j < d.W) G::load(raw[rr][k], d.g, d.gdt, base + (i + rr * kWarps) * d.W + j);
         }
 #pragma unroll
       for (int rr = 0; rr < RPI; ++rr)
@@ -267,7 +296,7 @@ __device__ __forceinline__ void pass_a_tile(const CDev& d, const CArgs& a, int64
           const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
           if (i + rr * kWarps < tl.i1 && j < d.W) {
             float x[VEC];
-            widen(raw[rr][k], d.gdt, x);
+            G::unpack(raw[rr][k], d.gdt, x);
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
               const float q = x[v] * x[v];
@@ -302,14 +331,14 @@ __device__ __forceinline__ void pass_a_1d(const CDev& d, const CArgs& a, int64_t
   if (threadIdx.x == 0) a.uspart[d.sp0 + local] = s;
 }
 
-template <int VEC>
+template <int VEC, int GK>
 __global__ void __launch_bounds__(kThreads, 2) k_came_pass_a(const __grid_constant__ CArgs a, int cls) {
   extern __shared__ __align__(16) unsigned char smem[];
   float* colbuf = reinterpret_cast<float*>(smem);
   double* red = reinterpret_cast<double*>(smem + sizeof(float) * kWarps * kTC);
   walk(a, cls, [&](const CDev& d, int, int64_t local) {
     if (cls == k1D) pass_a_1d(d, a, local, red);
-    else pass_a_tile<VEC>(d, a, local, colbuf);
+    else pass_a_tile<VEC, GK>(d, a, local, colbuf);
   });
 }
 
@@ -371,7 +400,7 @@ __global__ void __launch_bounds__(kThreads) k_came_means(const __grid_constant__
 
 // ---- pass b: sum(u^2) per tile ------------------------------------------------
 // sum_ij u^2 = sum_i (mean r / r_i) sum_j g^2 / c_j.
-template <int VEC>
+template <int VEC, int GK>
 __device__ __forceinline__ void pass_b_tile(const CDev& d, const CArgs& a, int64_t local, float* cinv, double* red) {
   constexpr int CH = Lay<VEC>::CH;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -386,7 +415,8 @@ __device__ __forceinline__ void pass_b_tile(const CDev& d, const CArgs& a, int64
   __syncthreads();
   constexpr int CG = Lay<VEC>::CG;
   float acc = 0.f;
-  constexpr int RPI = 2;  // rows per iteration (rows i, i + kWarps): twice the loads in flight
+  using G = GSel<VEC, GK>;
+  constexpr int RPI = G::RPI_B;  // rows per iteration (rows i, i + kWarps, ...): more loads in flight
   for (int64_t i = tl.i0 + warp; i < tl.i1; i += RPI * kWarps) {
     float ts[RPI];
 #pragma unroll
@@ -394,13 +424,13 @@ __device__ __forceinline__ void pass_b_tile(const CDev& d, const CArgs& a, int64
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
       if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;
-      GRaw<VEC> raw[RPI][CG];
+      typename G::Raw raw[RPI][CG];
 #pragma unroll
       for (int rr = 0; rr < RPI; ++rr)
 #pragma unroll
         for (int k = 0; k < CG; ++k) {
           const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
-          if (i + rr * kWarps < tl.i1 && j < d.W) load_g(raw[rr][k], d.g, d.gdt, base + (i + rr * kWarps) * d.W + j);
+          if (i + rr * kWarps < tl.i1 && j < d.W) G::load(raw[rr][k], d.g, d.gdt, base + (i + rr * kWarps) * d.W + j);
         }
 #pragma unroll
       for (int rr = 0; rr < RPI; ++rr)
@@ -409,7 +439,7 @@ __device__ __forceinline__ void pass_b_tile(const CDev& d, const CArgs& a, int64
           const int cl = Lay<VEC>::col(kg + k, lane);
           if (i + rr * kWarps < tl.i1 && tl.j0 + cl < d.W) {
             float x[VEC];
-            widen(raw[rr][k], d.gdt, x);
+            G::unpack(raw[rr][k], d.gdt, x);
 #pragma unroll
             for (int v = 0; v < VEC; ++v) ts[rr] = fmaf(x[v] * x[v], cinv[cl + v], ts[rr]);
           }
@@ -423,11 +453,11 @@ __device__ __forceinline__ void pass_b_tile(const CDev& d, const CArgs& a, int64
   if (threadIdx.x == 0) a.uspart[d.sp0 + local] = s;
 }
 
-template <int VEC>
+template <int VEC, int GK>
 __global__ void __launch_bounds__(kThreads, 2) k_came_pass_b(const __grid_constant__ CArgs a, int cls) {
   __shared__ __align__(16) float cinv[kTC];
   __shared__ double red[kWarps];
-  walk(a, cls, [&](const CDev& d, int, int64_t local) { pass_b_tile<VEC>(d, a, local, cinv, red); });
+  walk(a, cls, [&](const CDev& d, int, int64_t local) { pass_b_tile<VEC, GK>(d, a, local, cinv, red); });
 }
 
 // ---- clip: coef = 1 / max(1, RMS(u) / d), one CTA per tensor ---------------
@@ -445,7 +475,7 @@ __global__ void __launch_bounds__(kThreads) k_came_clip(const __grid_constant__ 
 
 // ---- pass c: momentum and the instability sums (factored); the whole
 // remaining step of 1D tensors ---------------------------------------------------
-template <int VEC>
+template <int VEC, int GK>
 __device__ __forceinline__ void pass_c_tile(const CDev& d, const CArgs& a, int t, int64_t local, float* colbuf,
                                             float* colf) {
   constexpr int CH = Lay<VEC>::CH;
@@ -471,13 +501,13 @@ __device__ __forceinline__ void pass_c_tile(const CDev& d, const CArgs& a, int t
 #pragma unroll
     for (int kg = 0; kg < CH; kg += CG) {
       if (tl.j0 + Lay<VEC>::col(kg, 0) >= d.W) break;
-      GRaw<VEC> raw[CG];
+      typename GSel<VEC, GK>::Raw raw[CG];
       float mv[CG][VEC];
 #pragma unroll
       for (int k = 0; k < CG; ++k) {
         const int64_t j = tl.j0 + Lay<VEC>::col(kg + k, lane);
         if (j < d.W) {
-          load_g(raw[k], d.g, d.gdt, base + i * d.W + j);
+          GSel<VEC, GK>::load(raw[k], d.g, d.gdt, base + i * d.W + j);
           load_f<VEC>(mv[k], d.m + base + i * d.W + j);
         }
       }
@@ -486,7 +516,7 @@ __device__ __forceinline__ void pass_c_tile(const CDev& d, const CArgs& a, int t
         const int cl = Lay<VEC>::col(kg + k, lane);
         if (tl.j0 + cl < d.W) {
           float x[VEC];
-          widen(raw[k], d.gdt, x);
+          GSel<VEC, GK>::unpack(raw[k], d.gdt, x);
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
             const float uh = (x[v] * rf) * colf[cl + v];
@@ -525,14 +555,14 @@ __device__ __forceinline__ void pass_c_1d(const CDev& d, const CArgs& a, int t, 
   }
 }
 
-template <int VEC>
+template <int VEC, int GK>
 __global__ void __launch_bounds__(kThreads, 2) k_came_pass_c(const __grid_constant__ CArgs a, int cls) {
   extern __shared__ __align__(16) unsigned char smem[];
   float* colbuf = reinterpret_cast<float*>(smem);
   float* colf = colbuf + kWarps * kTC;
   walk(a, cls, [&](const CDev& d, int t, int64_t local) {
     if (cls == k1D) pass_c_1d(d, a, t, local);
-    else pass_c_tile<VEC>(d, a, t, local, colbuf, colf);
+    else pass_c_tile<VEC, GK>(d, a, t, local, colbuf, colf);
   });
 }
 
@@ -666,7 +696,7 @@ adaf_status make_plan(const came_tensor* tensors, const came_state* states, int3
       d.cls = k1D;
     } else if (fact) {
       const bool vec = d.W % 8 == 0 && (!need_ptrs || (aligned(d.p, 16) && aligned(d.g, 16) && aligned(d.m, 16)));
-      d.cls = vec ? kVec : kScalar;
+      d.cls = vec ? (x.grad_dtype == ADAF_BFLOAT16 ? kVecBF : kVecF) : kScalar;
       d.cb = cdiv(d.W, kTC);
       d.rb = cdiv(d.H, kTR);
       ntiles = d.B * d.rb * d.cb;
@@ -783,10 +813,12 @@ bool g_attr_done = false;
 cudaError_t set_smem_attrs() {
   if (g_attr_done) return cudaSuccess;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_came_pass_a<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassASmem)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(k_came_pass_a<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassASmem)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(k_came_pass_c<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(k_came_pass_c<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_a<8, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassASmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_a<8, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassASmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_a<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassASmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_c<8, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_c<8, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_pass_c<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
   g_attr_done = true;
   return cudaSuccess;
 }
@@ -902,7 +934,8 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
 
   const int persist = 2 * ds.sms;  // 2 CTAs of 256 threads per SM
   auto grid_for = [&](int64_t units) { return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(persist, units))); };
-  const int64_t tiles[kClasses] = {P.pf[kVec].back(), P.pf[kScalar].back(), P.pf[k1D].back()};
+  int64_t tiles[kClasses];
+  for (int c = 0; c < kClasses; ++c) tiles[c] = P.pf[c].back();
   const int64_t items = P.item_pf.back();
 
   // launch helper: profiling events around each launch
@@ -930,9 +963,10 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
 
   // pass a (and the 1D second moment + sum(u^2))
   CAME_TRY(launch(kSA, [&] {
-    if (tiles[kVec]) k_came_pass_a<8><<<grid_for(tiles[kVec]), kThreads, kPassASmem, s>>>(a, kVec);
-    if (tiles[kScalar]) k_came_pass_a<1><<<grid_for(tiles[kScalar]), kThreads, kPassASmem, s>>>(a, kScalar);
-    if (tiles[k1D]) k_came_pass_a<1><<<grid_for(tiles[k1D]), kThreads, kPassASmem, s>>>(a, k1D);
+    if (tiles[kVecBF]) k_came_pass_a<8, 1><<<grid_for(tiles[kVecBF]), kThreads, kPassASmem, s>>>(a, kVecBF);
+    if (tiles[kVecF]) k_came_pass_a<8, 0><<<grid_for(tiles[kVecF]), kThreads, kPassASmem, s>>>(a, kVecF);
+    if (tiles[kScalar]) k_came_pass_a<1, 0><<<grid_for(tiles[kScalar]), kThreads, kPassASmem, s>>>(a, kScalar);
+    if (tiles[k1D]) k_came_pass_a<1, 0><<<grid_for(tiles[k1D]), kThreads, kPassASmem, s>>>(a, k1D);
   }));
   if (items) {
     a.phase = 0;
@@ -940,15 +974,17 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
     CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
     CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
     CAME_TRY(launch(kSB, [&] {
-      if (tiles[kVec]) k_came_pass_b<8><<<grid_for(tiles[kVec]), kThreads, 0, s>>>(a, kVec);
-      if (tiles[kScalar]) k_came_pass_b<1><<<grid_for(tiles[kScalar]), kThreads, 0, s>>>(a, kScalar);
+      if (tiles[kVecBF]) k_came_pass_b<8, 1><<<grid_for(tiles[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
+      if (tiles[kVecF]) k_came_pass_b<8, 0><<<grid_for(tiles[kVecF]), kThreads, 0, s>>>(a, kVecF);
+      if (tiles[kScalar]) k_came_pass_b<1, 0><<<grid_for(tiles[kScalar]), kThreads, 0, s>>>(a, kScalar);
     }));
   }
   CAME_TRY(launch(kSClip, [&] { k_came_clip<<<n, kThreads, 0, s>>>(a); }));
   CAME_TRY(launch(kSC, [&] {
-    if (tiles[kVec]) k_came_pass_c<8><<<grid_for(tiles[kVec]), kThreads, kPassCSmem, s>>>(a, kVec);
-    if (tiles[kScalar]) k_came_pass_c<1><<<grid_for(tiles[kScalar]), kThreads, kPassCSmem, s>>>(a, kScalar);
-    if (tiles[k1D]) k_came_pass_c<1><<<grid_for(tiles[k1D]), kThreads, kPassCSmem, s>>>(a, k1D);
+    if (tiles[kVecBF]) k_came_pass_c<8, 1><<<grid_for(tiles[kVecBF]), kThreads, kPassCSmem, s>>>(a, kVecBF);
+    if (tiles[kVecF]) k_came_pass_c<8, 0><<<grid_for(tiles[kVecF]), kThreads, kPassCSmem, s>>>(a, kVecF);
+    if (tiles[kScalar]) k_came_pass_c<1, 0><<<grid_for(tiles[kScalar]), kThreads, kPassCSmem, s>>>(a, kScalar);
+    if (tiles[k1D]) k_came_pass_c<1, 0><<<grid_for(tiles[k1D]), kThreads, kPassCSmem, s>>>(a, k1D);
   }));
   if (items) {
     a.phase = 1;
@@ -956,7 +992,8 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
     CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
     CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
     CAME_TRY(launch(kSD, [&] {
-      if (tiles[kVec]) k_came_pass_d<8><<<grid_for(tiles[kVec]), kThreads, 0, s>>>(a, kVec);
+      if (tiles[kVecBF]) k_came_pass_d<8><<<grid_for(tiles[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
+      if (tiles[kVecF]) k_came_pass_d<8><<<grid_for(tiles[kVecF]), kThreads, 0, s>>>(a, kVecF);
       if (tiles[kScalar]) k_came_pass_d<1><<<grid_for(tiles[kScalar]), kThreads, 0, s>>>(a, kScalar);
     }));
   }
