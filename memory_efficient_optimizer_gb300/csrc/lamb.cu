@@ -13,10 +13,12 @@
 //                   order, trust = ||p|| / ||r|| (1 where a norm is 0)
 //   k_lamb_update   m, v, p -> p - lr trust r  (read 12 B, write 4 B)
 //
-// Every tensor is a flat range cut into work units of kUnit values; a
-// persistent grid walks the units round-robin, and each CTA finds its tensor
-// by advancing a cursor over the unit prefix (units rise with the loop, so
-// the cursor only moves forward).  r is computed by the same correctly
+// Every tensor is a flat range cut into work units of kUnit values, numbered
+// with the bf16-gradient tensors first, so that each gradient dtype has its
+// own moments launch (and its own register budget).  A persistent grid walks
+// a launch's units round-robin, and each CTA finds its tensor by advancing a
+// cursor over the unit prefix (units rise with the loop, so the cursor only
+// moves forward).  r is computed by the same correctly
 // rounded intrinsics in both passes, so the update applies exactly the r
 // whose norm set the trust ratio.  All sums are deterministic (fixed-order
 // trees, no atomics).
@@ -40,7 +42,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kVecPerThread = 8;                               // 4-value vectors per thread per unit
 constexpr int64_t kUnit = int64_t{kThreads} * 4 * kVecPerThread;  // 8192 values
-constexpr int kBatchM = 3;  // 4-value vectors per stream in flight per thread, moments pass (4 streams)
+// 4-value vectors per stream in flight per thread, moments pass (4 streams):
+// 4 with bf16 gradients (2 registers each), 3 with fp32 ones
+template <typename GT> struct BatchM { static constexpr int value = 3; };
+template <> struct BatchM<__nv_bfloat16> { static constexpr int value = 4; };
 constexpr int kBatchU = 4;  // the same, update pass (3 streams)
 constexpr int64_t kMaxNumel = int64_t{1} << 40;
 
@@ -51,16 +56,17 @@ struct LDev {
   float* m;
   float* v;
   int64_t numel;
-  int64_t unit0;  // first work unit
-  int32_t gdt;    // ADAF_FLOAT32 / ADAF_BFLOAT16
-  int32_t vec;    // 4-value loads allowed (aligned pointers)
-  int64_t pad;
+  int64_t unit0;   // first work unit
+  int32_t gdt;     // ADAF_FLOAT32 / ADAF_BFLOAT16
+  int32_t vec;     // 4-value loads allowed (aligned pointers)
+  int64_t nunits;  // work units
 };
 static_assert(sizeof(LDev) == 64, "descriptor layout");
 
 struct LArgs {
   const LDev* dev;
-  const int64_t* unit_pf;  // [n + 1]: first unit of each tensor, then the total
+  const int64_t* pf;       // [n + 1]: first unit of each tensor in unit order, then the total
+  const int32_t* ord;      // [n]: the tensor at each position of that order
   double* part;            // [units][2]: sum r^2, sum p^2
   double* trust;           // [n]
   double* coef;            // [n]: lr * trust
@@ -142,11 +148,11 @@ __device__ __forceinline__ void block_sum2(double& x, double& y, double* red) {
 template <typename GT>
 __device__ __forceinline__ void moments_vec(const LDev& d, const LArgs& a, int64_t e0, int64_t nv, float& rs,
                                             float& ps) {
-  for (int64_t v0 = threadIdx.x; v0 < nv; v0 += kBatchM * kThreads) {
-    G4<GT> g[kBatchM];
-    float4 m[kBatchM], v[kBatchM], p[kBatchM];
+  for (int64_t v0 = threadIdx.x; v0 < nv; v0 += BatchM<GT>::value * kThreads) {
+    G4<GT> g[BatchM<GT>::value];
+    float4 m[BatchM<GT>::value], v[BatchM<GT>::value], p[BatchM<GT>::value];
 #pragma unroll
-    for (int k = 0; k < kBatchM; ++k) {
+    for (int k = 0; k < BatchM<GT>::value; ++k) {
       const int64_t e = e0 + 4 * (v0 + k * kThreads);
       if (v0 + k * kThreads < nv) {
         load_g4(g[k], d.g, e);
@@ -156,7 +162,7 @@ __device__ __forceinline__ void moments_vec(const LDev& d, const LArgs& a, int64
       }
     }
 #pragma unroll
-    for (int k = 0; k < kBatchM; ++k) {
+    for (int k = 0; k < BatchM<GT>::value; ++k) {
       if (v0 + k * kThreads < nv) {
         const int64_t e = e0 + 4 * (v0 + k * kThreads);
         float x[4], mo[4], vo[4];
@@ -192,20 +198,33 @@ __device__ __forceinline__ void moments_scalar(const LDev& d, const LArgs& a, in
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_lamb_moments(const __grid_constant__ LArgs a) {
+// Position (in unit order) of the tensor that holds unit u.
+__device__ __forceinline__ int unit_owner(const LArgs& a, int64_t u) {
+  int lo = 0, hi = a.n;  // largest lo with pf[lo] <= u
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (a.pf[mid] <= u) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// Units [u_begin, u_end): the tensors of one gradient dtype.
+template <typename GT>
+__global__ void __launch_bounds__(kThreads, 2) k_lamb_moments(const __grid_constant__ LArgs a, int64_t u_begin,
+                                                              int64_t u_end) {
   __shared__ double red[64];
-  int t = 0;
-  for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
-    while (a.unit_pf[t + 1] <= u) ++t;
-    const LDev d = a.dev[t];
+  int k = unit_owner(a, u_begin + blockIdx.x);
+  for (int64_t u = u_begin + blockIdx.x; u < u_end; u += gridDim.x) {
+    while (a.pf[k + 1] <= u) ++k;
+    const LDev d = a.dev[a.ord[k]];
     const int64_t e0 = (u - d.unit0) * kUnit;
     const int64_t e1 = min(d.numel, e0 + kUnit);
     float rs = 0.f, ps = 0.f;
     int64_t es = e0;  // first value left to the scalar loop
     if (d.vec) {
       const int64_t nv = (e1 - e0) >> 2;
-      if (d.gdt == ADAF_BFLOAT16) moments_vec<__nv_bfloat16>(d, a, e0, nv, rs, ps);
-      else moments_vec<float>(d, a, e0, nv, rs, ps);
+      moments_vec<GT>(d, a, e0, nv, rs, ps);
       es = e0 + 4 * nv;
     }
     moments_scalar(d, a, es, e1, rs, ps);
@@ -222,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_lamb_moments(const __grid_const
 __global__ void __launch_bounds__(kThreads) k_lamb_trust(const __grid_constant__ LArgs a) {
   __shared__ double red[64];
   const int t = blockIdx.x;
-  const int64_t u0 = a.unit_pf[t], u1 = a.unit_pf[t + 1];
+  const LDev d = a.dev[t];
+  const int64_t u0 = d.unit0, u1 = d.unit0 + d.nunits;
   double x = 0.0, y = 0.0;
   for (int64_t u = u0 + threadIdx.x; u < u1; u += kThreads) {
     x += a.part[2 * u];
@@ -267,9 +287,10 @@ __device__ __forceinline__ void update_vec(const LDev& d, const LArgs& a, float 
 }
 
 __global__ void __launch_bounds__(kThreads, 2) k_lamb_update(const __grid_constant__ LArgs a) {
-  int t = 0;
+  int k = unit_owner(a, blockIdx.x);
   for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
-    while (a.unit_pf[t + 1] <= u) ++t;
+    while (a.pf[k + 1] <= u) ++k;
+    const int t = a.ord[k];
     const LDev d = a.dev[t];
     const float c = static_cast<float>(a.coef[t]);
     const int64_t e0 = (u - d.unit0) * kUnit;
@@ -297,7 +318,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 struct Layout {
   int64_t units = 0;
-  size_t off_trust = 0, off_coef = 0, off_dev = 0, off_pf = 0, off_part = 0, bytes = 0;
+  size_t off_trust = 0, off_coef = 0, off_dev = 0, off_pf = 0, off_ord = 0, off_part = 0, bytes = 0;
 };
 
 adaf_status check_list(const lamb_tensor* tensors, int32_t n, Layout* L) {
@@ -319,7 +340,8 @@ adaf_status check_list(const lamb_tensor* tensors, int32_t n, Layout* L) {
   L->off_trust = o; o = round_up(o + sizeof(double) * n, 256);
   L->off_coef = o;  o = round_up(o + sizeof(double) * n, 256);
   L->off_dev = o;   o += sizeof(LDev) * n;
-  L->off_pf = o;    o = round_up(o + sizeof(int64_t) * (n + 1), 256);
+  L->off_pf = o;    o += sizeof(int64_t) * (n + 1);
+  L->off_ord = o;   o = round_up(o + sizeof(int32_t) * n, 256);
   L->off_part = o;  o = round_up(o + sizeof(double) * 2 * units, 256);
   L->bytes = o;
   return ADAF_OK;
@@ -413,34 +435,45 @@ adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const
   if (workspace_bytes < L.bytes)
     return fail(ADAF_ERR_WORKSPACE_TOO_SMALL, "lamb: workspace needs " + std::to_string(L.bytes) + " bytes");
 
-  // Host copy of the descriptors and the unit prefix.
-  const size_t hdr = sizeof(LDev) * n + sizeof(int64_t) * (n + 1);
+  // Host copy of the descriptors, the unit prefix in unit order (tensors
+  // with bf16 gradients first) and the tensor at each position.
+  const size_t hdr = L.off_ord + sizeof(int32_t) * n - L.off_dev;
   std::vector<unsigned char> h(hdr);
   LDev* dv = reinterpret_cast<LDev*>(h.data());
-  int64_t* pf = reinterpret_cast<int64_t*>(h.data() + sizeof(LDev) * n);
-  int64_t u = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    const lamb_tensor& x = tensors[i];
-    LDev d{};
-    d.p = x.p;
-    d.g = x.g;
-    d.m = x.exp_avg;
-    d.v = x.exp_avg_sq;
-    d.numel = x.numel;
-    d.unit0 = u;
-    d.gdt = x.grad_dtype;
-    const size_t ga = x.grad_dtype == ADAF_BFLOAT16 ? 8 : 16;
-    d.vec = aligned(x.p, 16) && aligned(x.exp_avg, 16) && aligned(x.exp_avg_sq, 16) && aligned(x.g, ga);
-    dv[i] = d;
-    pf[i] = u;
-    u += (x.numel + kUnit - 1) / kUnit;
+  int64_t* pf = reinterpret_cast<int64_t*>(h.data() + (L.off_pf - L.off_dev));
+  int32_t* ord = reinterpret_cast<int32_t*>(h.data() + (L.off_ord - L.off_dev));
+  int64_t u = 0, u_bf16 = 0;
+  int32_t pos = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int32_t i = 0; i < n; ++i) {
+      const lamb_tensor& x = tensors[i];
+      if ((x.grad_dtype == ADAF_BFLOAT16) != (pass == 0)) continue;
+      LDev d{};
+      d.p = x.p;
+      d.g = x.g;
+      d.m = x.exp_avg;
+      d.v = x.exp_avg_sq;
+      d.numel = x.numel;
+      d.unit0 = u;
+      d.nunits = (x.numel + kUnit - 1) / kUnit;
+      d.gdt = x.grad_dtype;
+      const size_t ga = x.grad_dtype == ADAF_BFLOAT16 ? 8 : 16;
+      d.vec = aligned(x.p, 16) && aligned(x.exp_avg, 16) && aligned(x.exp_avg_sq, 16) && aligned(x.g, ga);
+      dv[i] = d;
+      pf[pos] = u;
+      ord[pos] = i;
+      ++pos;
+      u += d.nunits;
+    }
+    if (pass == 0) u_bf16 = u;
   }
   pf[n] = u;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   LArgs a{};
   a.dev = reinterpret_cast<const LDev*>(ws + L.off_dev);
-  a.unit_pf = reinterpret_cast<const int64_t*>(ws + L.off_pf);
+  a.pf = reinterpret_cast<const int64_t*>(ws + L.off_pf);
+  a.ord = reinterpret_cast<const int32_t*>(ws + L.off_ord);
   a.part = reinterpret_cast<double*>(ws + L.off_part);
   a.trust = reinterpret_cast<double*>(ws + L.off_trust);
   a.coef = reinterpret_cast<double*>(ws + L.off_coef);
@@ -470,12 +503,15 @@ adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const
     int sms = 0, occ = 0;
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
       return cuda_fail(err, "cudaDeviceGetAttribute");
-    int occ2 = 0;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_lamb_moments, kThreads, 0)) != cudaSuccess)
+    int occ2 = 0, occ3 = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_lamb_moments<__nv_bfloat16>, kThreads, 0)) !=
+        cudaSuccess)
       return cuda_fail(err, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, k_lamb_update, kThreads, 0)) != cudaSuccess)
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, k_lamb_moments<float>, kThreads, 0)) != cudaSuccess)
       return cuda_fail(err, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    ds.grid = sms * std::max(1, std::min(occ, occ2));
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, k_lamb_update, kThreads, 0)) != cudaSuccess)
+      return cuda_fail(err, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    ds.grid = sms * std::max(1, std::min(occ, std::min(occ2, occ3)));
   }
   Slot& sl = ds.ring[ds.next];
   ds.next = (ds.next + 1) % kRing;
@@ -497,7 +533,7 @@ adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const
   if ((err = cudaEventRecord(sl.done, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
   sl.used = true;
 
-  const int grid = static_cast<int>(std::min<int64_t>(ds.grid, std::max<int64_t>(1, L.units)));
+  auto grid_for = [&](int64_t units) { return static_cast<int>(std::min<int64_t>(ds.grid, std::max<int64_t>(1, units))); };
   for (int k = 0; k < kNumKernels; ++k) {
     ProfRecord rec{k, device, nullptr, nullptr};
     if (g_profile) {
@@ -505,9 +541,14 @@ adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const
       if ((err = get_event(ds, &rec.stop)) != cudaSuccess) return cuda_fail(err, "cudaEventCreate (profile)");
       if ((err = cudaEventRecord(rec.start, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord (profile)");
     }
-    if (k == 0) k_lamb_moments<<<grid, kThreads, 0, s>>>(a);
-    else if (k == 1) k_lamb_trust<<<n, kThreads, 0, s>>>(a);
-    else k_lamb_update<<<grid, kThreads, 0, s>>>(a);
+    if (k == 0) {
+      if (u_bf16 > 0) k_lamb_moments<__nv_bfloat16><<<grid_for(u_bf16), kThreads, 0, s>>>(a, 0, u_bf16);
+      if (L.units > u_bf16) k_lamb_moments<float><<<grid_for(L.units - u_bf16), kThreads, 0, s>>>(a, u_bf16, L.units);
+    } else if (k == 1) {
+      k_lamb_trust<<<n, kThreads, 0, s>>>(a);
+    } else if (L.units > 0) {
+      k_lamb_update<<<grid_for(L.units), kThreads, 0, s>>>(a);
+    }
     if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err, kKernelNames[k]);
     if (g_profile) {
       if ((err = cudaEventRecord(rec.stop, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord (profile)");
