@@ -280,7 +280,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
   }
   const size_t nd = plan->dev.size();
   if (shards != nullptr) {
-    // round 1: [column sums of every factored tensor][sum_i row_i per slice][sum(p^2) per tensor]
+    // exchange round 1: [column sums of every factored tensor][sum_i row_i per slice][sum(p^2) per tensor]
     for (size_t k = 0; k < nd; ++k) {
       DevTensor& d = plan->dev[k];
       if (d.kind != meo::kUnfactored) d.x1r += nx1col;
@@ -618,8 +618,8 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
   };
   const int nd_i = static_cast<int>(nd);
   // Phase 0: everything.  Row-sharded: 1 = pass 1, this shard's statistics
-  // into round 1; 2 = column statistics from round 1, pass 2, this shard's
-  // sum(u^2) into round 2; 3 = clip from round 2, apply.
+  // into exchange round 1; 2 = column statistics from exchange round 1, pass 2,
+  // this shard's sum(u^2) into exchange round 2; 3 = clip from exchange round 2, apply.
   auto stats = [&]() -> adaf_status {
     if (!plan.any_factored) return ADAF_OK;
     const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);

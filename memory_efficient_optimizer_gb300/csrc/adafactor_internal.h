@@ -85,9 +85,9 @@ struct DevTensor {
   int64_t hg;         // factored: rows per slice of the whole tensor; ndim < 2: its numel
   int64_t ng;         // numel of the whole tensor
   // Row-sharded steps only (0 otherwise).
-  int64_t x1c;        // double offset in round 1 of the column sums of g^2 [B][W]
-  int64_t x1r;        // double offset in round 1 of sum_i row_i per slice [B]
-  int64_t x1p;        // double offset in round 1 of sum(p^2)
+  int64_t x1c;        // double offset in exchange round 1 of the column sums of g^2 [B][W]
+  int64_t x1r;        // double offset in exchange round 1 of sum_i row_i per slice [B]
+  int64_t x1p;        // double offset in exchange round 1 of sum(p^2)
   int64_t dloc;       // float offset in the workspace of this shard's D_j [B][W] (fused)
   // 8-bit first moment (beta1 with exp_avg_int8): int8 codes [N] and fp32
   // scales, one per group of kQ8Group values along the last dim.

@@ -706,7 +706,7 @@ __device__ __forceinline__ void stats_col_any(const DevTensor& d, const StepArgs
 }
 
 // Row-sharded middle: the column statistic from the column sums of g^2 over
-// all shards (round 1), and for fused tensors this shard's
+// all shards (exchange round 1), and for fused tensors this shard's
 // sum_j D_j / col_j over the chunk's columns.
 __device__ __forceinline__ void stats_col_global(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q,
                                                  double* red) {
@@ -1001,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads) k_clip(const __grid_constant__ StepA
     for (int64_t k = threadIdx.x; k < d.ntiles; k += kThreads) acc += a.spart[d.tile0 + k];
     S = block_sum(acc, red);
   }
-  if (a.phase == 2) {  // row-sharded middle: this shard's sum(u^2) to round 2
+  if (a.phase == 2) {  // row-sharded middle: this shard's sum(u^2) to exchange round 2
     if (threadIdx.x == 0) a.round2[t] = S;
     return;
   }

@@ -216,7 +216,7 @@ class AdafactorShardStep(AdafactorStep):
     [..., W] is the whole one and stays equal on every rank.  allreduce(t)
     must sum a float64 CUDA tensor in place over the group (for example
     ``torch.distributed.all_reduce``); None means a group of one.  Each call
-    is begin, allreduce(round 1), middle, allreduce(round 2), end."""
+    is begin, allreduce(exchange round 1), middle, allreduce(exchange round 2), end."""
 
     def __init__(self, params, grads, states, global_rows, allreduce=None, **hparams):
         super().__init__(params, grads, states, **hparams)

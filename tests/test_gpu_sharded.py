@@ -76,7 +76,7 @@ def test_row_sharded_step_matches_oracle(flags, nranks, grad_dtype):
             before = ref_p[k].copy()
             oracle.step(ref_p[k], to64(g), ref_st[k], t, ohp)
             abs_upd[k] += np.abs(ref_p[k] - before)
-        # begin on every rank, sum round 1, middle, sum round 2, end
+        # begin on every rank, sum exchange round 1, middle, sum exchange round 2, end
         for st in ranks:
             st.begin(t)
         tot = sum(st.round1 for st in ranks)

@@ -50,7 +50,7 @@ def test_single_rank_is_identity():
 # ---- row-sharded step: the exchange protocol on gloo ranks -----------------
 # The library's row-sharded step (adafactor_shard_begin / middle / end)
 # exchanges, per tensor, the column sums of g^2, the sum of the updated row
-# statistic per slice and sum(p^2) (round 1), then sum(u^2) (round 2).  Here
+# statistic per slice and sum(p^2) (exchange round 1), then sum(u^2) (exchange round 2).  Here
 # two gloo ranks run that protocol in float64 numpy on their row blocks, with
 # real all-reduces between the phases, and must reproduce the oracle on the
 # whole tensors; every rank also checks that the library's exchange buffer
@@ -127,7 +127,7 @@ def _shard_worker(rank, world, port, out):
                 else:
                     v = b2 * v + (1 - b2) * q
                     x1 = np.array([np.sum(p * p)])
-                x1 = allreduce(x1)  # round 1
+                x1 = allreduce(x1)  # exchange round 1
                 # middle: column statistic, mean(row), alpha; local sum(u^2)
                 psq = x1[-1]
                 alpha = rho * max(hp.eps[1], np.sqrt(psq / N))
@@ -138,7 +138,7 @@ def _shard_worker(rank, world, port, out):
                     u = g / np.sqrt(row[..., None] / mrow[..., None] * col[..., None, :])
                 else:
                     u = g / np.sqrt(v)
-                x2 = allreduce(np.array([np.sum(u * u)]))  # round 2
+                x2 = allreduce(np.array([np.sum(u * u)]))  # exchange round 2
                 # end: clip, beta1, weight decay, update
                 u = alpha * u / max(1.0, np.sqrt(x2[0] / N) / hp.clip_threshold)
                 m1 = hp.beta1 * m1 + (1 - hp.beta1) * u
