@@ -137,6 +137,7 @@ def test_came_pins_catch_mutant(name, tmp_path):
                            "-o", str(lib), "-lm"])
     env = dict(os.environ, ORACLE_CAME_LIB_OVERRIDE=str(lib))
     res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                          os.path.join(ROOT, "tests", "test_oracle_came_pins.py")],
+                          os.path.join(ROOT, "tests", "test_oracle_came_pins.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_came_bruteforce.py")],
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert res.returncode != 0, f"mutant '{name}' survived the pins:\n{res.stdout[-2000:]}"
