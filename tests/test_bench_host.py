@@ -1,0 +1,83 @@
+"""Host-side logic of bench.py, without a GPU: the algorithmic byte counts
+each roofline divides by, the tensor classes they are split into, the
+oracle sample, the all-cores oracle baseline (spawned workers) and the
+source digests that key the committed DRAM traffic records."""
+import json
+import os
+
+import pytest
+
+import bench
+from memory_efficient_optimizer_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+N_8B = 8_030_261_248
+N_1D = 65 * 4096  # 32 layers x 2 norms + the final norm
+
+
+def test_llama3_8b_bytes_match_the_method_count():
+    """Three reads of bf16 g, p read + write and the factored state: the
+    method's 14 B per value plus the tiny row/col state."""
+    wl = synth.workload("llama3_8b")
+    step, impl, slots = bench.algorithmic_bytes(wl.shapes, 2, False)
+    assert wl.numel == N_8B
+    assert 14 * N_8B < step < 14 * N_8B * 1.001
+    assert impl < step  # the fused pass reads g twice instead of three times
+    assert slots["k_apply[rows_bf16]"] == 61_518_653_440
+
+
+def test_tensor_classes_of_the_8b_list():
+    classes = {bench.tensor_class(s, 2) for _, s in synth.workload("llama3_8b").shapes}
+    assert classes == {"rows_bf16", "wide_bf16", "1d"}
+    assert bench.tensor_class((4096, 14336), 2) == "wide_bf16"
+    assert bench.tensor_class((4096, 4096), 4) == "vec_f32"
+    assert bench.tensor_class((33, 7), 2) == "elem_bf16"
+
+
+def test_lamb_bytes():
+    slots, design, one_pass = bench.lamb_bytes(N_8B, 2)
+    assert slots == {"k_lamb_moments": 22 * N_8B, "k_lamb_update": 16 * N_8B}
+    assert design == 38 * N_8B and one_pass == 26 * N_8B
+
+
+def test_came_bytes():
+    wl = synth.workload("llama3_8b_came")
+    slots, design, one_pass = bench.came_bytes(wl.shapes, 2)
+    nf = N_8B - N_1D
+    assert slots["k_came_pass_a"] == 2 * nf + 10 * N_1D
+    assert slots["k_came_pass_b"] == 2 * nf
+    assert slots["k_came_pass_c"] == 10 * nf + 30 * N_1D
+    assert slots["k_came_pass_d"] == 12 * nf
+    assert design == sum(slots.values()) and one_pass == 18 * N_8B
+
+
+def test_oracle_sample_is_decoder_layer_0():
+    wl = synth.workload("llama3_8b")
+    idx = bench.oracle_sample(wl)
+    assert [wl.shapes[k][0] for k in idx] == [f"layers.0.{n}" for n, _ in synth.llama_layer_shapes()]
+
+
+def test_all_cores_baseline_runs_the_oracle_in_spawned_workers():
+    wl = synth.workload("tiny")
+    out = bench.cpu_baseline_all_cores(wl, "tiny", steps=1)
+    assert out["kind"] == "oracle" and out["cores"] == 2 and out["value"] > 0
+    assert "2 tensors (131,584 values)" in out["sample"]
+
+
+def test_traffic_records_are_keyed_to_their_kernel_sources():
+    """Every committed DRAM traffic record names a kernel whose source digest
+    the bench can compute; the records of different kernel files differ."""
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    assert {"k_apply[rows_bf16]", "k_lamb_moments", "k_came_pass_d"} <= set(rec)
+    digests = {k: bench.kernel_source_digest(k) for k in rec}
+    assert len({digests["k_apply[rows_bf16]"], digests["k_lamb_moments"], digests["k_came_pass_d"]}) == 3
+    for k, entry in rec.items():
+        assert entry["dram_bytes_per_full_launch"] > 0
+        assert len(entry["kernel_source_sha256"]) == 64
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "llama3_8b_lamb", "llama3_8b_came", "llama3_8b_beta1_int8"])
+def test_workloads_resolve_to_a_runner(name):
+    wl = synth.workload(name)
+    assert wl.optimizer in bench.ORACLE_TIMERS
+    assert wl.numel == N_8B
