@@ -1014,31 +1014,84 @@ __global__ void __launch_bounds__(kThreads) k_clip(const __grid_constant__ StepA
 }
 
 // ---- 8-bit first moment ----------------------------------------------------
-// The ms-swift GaLore / Q-GaLore article's block quantisation ("Q-GaLore":
-// groups of 128, scale absmax / 127, symmetric int8 codes) applied to
+// The ms-swift GaLore / Q-GaLore article's block quantisation ("Q-Galore"
+// section, its quantize_tensor / dequantize_tensor listing) applied to
 // exp_avg.  Groups are kQ8Group values along the last dim; a group's state is
-// its codes and one fp32 scale, value = code * scale.  After the moment EMA
-// the new moment is used unquantised for the update, and the group is
-// re-quantised: amax = max |m|, scale = amax / 127, code = rint(m * (127 /
-// amax)), all in fp32 (code 0 and scale 0 for an all-zero group).
+// its codes and one fp32 scale, value = code * scale.  Per step and group:
+// the old moment is dequantised, m = beta1 * old + (1 - beta1) * u, then the
+// group is re-quantised as the listing does, scale = amax / 127 and code =
+// round-half-even(m / scale) (both quotients correctly rounded fp32), and the
+// update applied to the parameter is the dequantised new moment code * scale,
+// the value the stored state holds (the listing dequantises before use).
 __device__ __forceinline__ float q8_value(uint32_t codes4, int v, float scale) {
   const int c = static_cast<int>(static_cast<int8_t>((codes4 >> (8 * v)) & 0xffu));
-  return static_cast<float>(c) * scale;
+  return __fmul_rn(static_cast<float>(c), scale);
 }
 // Warp maximum of non-negative floats: their bit patterns order like
 // unsigned integers, so one redux.sync.max.u32 does it.
 __device__ __forceinline__ float warp_max_nonneg(float v) {
   return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
-// Codes of 4 values, packed little-endian; inv = 127 / amax (0 if amax = 0).
-__device__ __forceinline__ uint32_t q8_pack4(const float (&m)[4], float inv) {
+// Reciprocal with at most 1 ulp of error (rcp.approx.f32: subnormals
+// handled, 1 / 0 = +inf).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// Quantises NG groups of the new moment, each 128 values held 4 per lane by
+// the 32 lanes of a warp (out-of-range values passed as 0; every lane of the
+// warp must call).  sc[g] = amax / 127 of group g (correctly rounded; 0 for
+// an all-zero group); c[g][v] = the code round-half-even(fl(m[g][v] /
+// sc[g])), clamped to [-128, 127], as a float.
+//
+// Each code is first taken from x = fl(m * r) with r = 1 / scale to 1 ulp:
+// |x - fl(m / scale)| <= |m / scale| (2^-23 + 2^-24 + 2^-24) < 3.1e-5, since
+// |m| <= amax makes |m / scale| at most 127 (1 + 2^-23) for a normal scale.
+// Where x lies farther than kQ8TieBand (> 3.1e-5) from every half-integer,
+// rint(x) is therefore the page's code.  Where any value of the NG groups
+// lies closer, or a scale is subnormal, all NG groups take the correctly
+// rounded divisions instead (a warp-uniform branch, rarely taken: about 3 %
+// of the groups).
+constexpr float kQ8TieBand = 1.0f / 8192.0f;
+template <int NG>
+__device__ __forceinline__ void q8_groups(const float (&m)[NG][4], float (&c)[NG][4], float (&sc)[NG]) {
+  bool near = false;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    float amax = fmaxf(fmaxf(fabsf(m[g][0]), fabsf(m[g][1])), fmaxf(fabsf(m[g][2]), fabsf(m[g][3])));
+    amax = warp_max_nonneg(amax);
+    sc[g] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    const float r = sc[g] > 0.f ? rcp_approx(sc[g]) : 0.f;
+    near |= sc[g] > 0.f && sc[g] < 0x1p-126f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float x = __fmul_rn(m[g][v], r);
+      c[g][v] = rintf(x);
+      near |= fabsf(__fsub_rn(x, c[g][v])) > 0.5f - kQ8TieBand;
+    }
+  }
+  if (__any_sync(0xffffffffu, near)) {
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        c[g][v] = sc[g] > 0.f ? fminf(fmaxf(rintf(__fdiv_rn(m[g][v], sc[g])), -128.f), 127.f) : 0.f;
+  }
+}
+// p <- p - wd * alpha * p - code * scale: the dequantised moment is applied
+// with one rounding (fl(code * scale), the stored state's value, differs
+// from the exact product by at most half an ulp of it).
+__device__ __forceinline__ float q8_update(float p, float wda, float c, float sc) {
+  return fmaf(-wda, p, fmaf(-c, sc, p));
+}
+// Codes of 4 values (integral floats in [-128, 127]), packed little-endian.
+__device__ __forceinline__ uint32_t q8_pack4(const float (&c)[4]) {
   uint32_t w = 0;
 #pragma unroll
-  for (int v = 0; v < 4; ++v) w |= (static_cast<uint32_t>(__float2int_rn(__fmul_rn(m[v], inv))) & 0xffu) << (8 * v);
+  for (int v = 0; v < 4; ++v) w |= (static_cast<uint32_t>(__float2int_rn(c[v])) & 0xffu) << (8 * v);
   return w;
 }
-__device__ __forceinline__ float q8_inv(float amax) { return amax > 0.f ? 127.0f / amax : 0.f; }
-__device__ __forceinline__ float q8_scale(float amax) { return amax > 0.f ? amax / 127.0f : 0.f; }
 
 // ---- apply: p <- p - wd*alpha*p - update ----------------------------------
 // colf holds coef * col_j^-1/2 for the tile's columns (shared memory).
@@ -1205,38 +1258,48 @@ __device__ __forceinline__ void apply_factored(const DevTensor& d, const StepArg
           for (int v = 0; v < VEC; ++v) {
             float upd = (x[v] * r_i) * f[v];
             if (B1) {
-              const float old = Q8 ? mv[B1 ? k : 0][v] * qs[Q8 ? k / QPG : 0] : mv[B1 ? k : 0][v];
+              const float old = Q8 ? __fmul_rn(mv[B1 ? k : 0][v], qs[Q8 ? k / QPG : 0]) : mv[B1 ? k : 0][v];
               mv[B1 ? k : 0][v] = fmaf(b1, old, omb1 * upd);
               upd = mv[B1 ? k : 0][v];
             }
-            const float pn = fmaf(-wda, pv[k][v], pv[k][v] - upd);
-            pv[k][v] = pn;
-            if (PSQ) psq = fmaf(pn, pn, psq);
+            if (!Q8) {  // (the 8-bit moment updates p after re-quantising)
+              const float pn = fmaf(-wda, pv[k][v], pv[k][v] - upd);
+              pv[k][v] = pn;
+              if (PSQ) psq = fmaf(pn, pn, psq);
+            }
           }
-          store_f<VEC>(pb + i * W + j, pv[k]);
+          if (!Q8) store_f<VEC>(pb + i * W + j, pv[k]);
           if (B1 && !Q8) store_f<VEC>(mb + i * W + j, mv[B1 ? k : 0]);
         }
       }
       if (Q8) {
-        // re-quantise each group of QPG chunks: warp max of |m|, then codes
+        // re-quantise each group of QPG chunks (warp max of |m|, scale,
+        // codes), then apply the dequantised moment to p
+        static_assert(!Q8 || (QPG == 4 && CG / QPG == 2), "a lane holds 4 values of each of 2 groups");
+        float mg[2][4], c[2][4], sc[2];
 #pragma unroll
-        for (int q = 0; q < CG / QPG; ++q) {
-          float amax = 0.f;
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int kk = 0; kk < QPG; ++kk) {
             const int k = q * QPG + kk;
-            if (j0 + (kg + k) * 32 + lane < W) amax = fmaxf(amax, fabsf(mv[B1 ? k : 0][0]));
+            mg[q][kk] = (j0 + (kg + k) * 32 + lane < W) ? mv[B1 ? k : 0][0] : 0.f;
           }
-          amax = warp_max_nonneg(amax);
-          const float inv = q8_inv(amax);
+        q8_groups<2>(mg, c, sc);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
 #pragma unroll
           for (int kk = 0; kk < QPG; ++kk) {
             const int k = q * QPG + kk;
             const int64_t j = j0 + (kg + k) * 32 + lane;
-            if (j < W) qb[i * W + j] = static_cast<int8_t>(__float2int_rn(__fmul_rn(mv[B1 ? k : 0][0], inv)));
+            if (j < W) {
+              qb[i * W + j] = static_cast<int8_t>(__float2int_rn(c[q][kk]));
+              const float pn = q8_update(pv[k][0], wda, c[q][kk], sc[q]);
+              pb[i * W + j] = pn;
+              if (PSQ) psq = fmaf(pn, pn, psq);
+            }
           }
           const int64_t jg = j0 + (kg + q * QPG) * 32;
-          if (lane == 0 && jg < W) d.ms[(tp.b * H + i) * d.qg + jg / kQ8Group] = q8_scale(amax);
+          if (lane == 0 && jg < W) d.ms[(tp.b * H + i) * d.qg + jg / kQ8Group] = sc[q];
         }
       }
     }
@@ -1326,27 +1389,31 @@ __device__ __forceinline__ void apply_unfactored_q8(const DevTensor& d, const St
 #pragma unroll
     for (int q = 0; q < GP; ++q) {
       const int64_t gb = (g0 + q) * kQ8Group;
-      float amax = 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int64_t e = gb + lane * 4 + k;
         if (e < e1) {
           const float upd = coef * (x[q][k] * rsqrtf(v[q][k]));
-          m[q][k] = fmaf(b1, m[q][k] * sc[q], omb1 * upd);
-          amax = fmaxf(amax, fabsf(m[q][k]));
-          const float pn = fmaf(-wda, pv[q][k], pv[q][k] - m[q][k]);
+          m[q][k] = fmaf(b1, __fmul_rn(m[q][k], sc[q]), omb1 * upd);
+        }
+      }
+    }
+    float c[GP][4], s[GP];
+    q8_groups<GP>(m, c, s);  // warp-uniform: a group is in range for the whole warp or not at all
+#pragma unroll
+    for (int q = 0; q < GP; ++q) {
+      const int64_t gb = (g0 + q) * kQ8Group;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t e = gb + lane * 4 + k;
+        if (e < e1) {
+          d.mq[e] = static_cast<int8_t>(__float2int_rn(c[q][k]));
+          const float pn = q8_update(pv[q][k], wda, c[q][k], s[q]);
           d.p[e] = pn;
           if (PSQ) psq = fmaf(pn, pn, psq);
         }
       }
-      amax = warp_max_nonneg(amax);  // warp-uniform: gb < e1 for the whole warp or none
-      const float inv = q8_inv(amax);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t e = gb + lane * 4 + k;
-        if (e < e1) d.mq[e] = static_cast<int8_t>(__float2int_rn(__fmul_rn(m[q][k], inv)));
-      }
-      if (lane == 0 && gb < e1) d.ms[g0 + q] = q8_scale(amax);
+      if (lane == 0 && gb < e1) d.ms[g0 + q] = s[q];
     }
   }
   if (PSQ) {
@@ -2032,18 +2099,53 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < KW; ++kk) {
           const int k = k0 + kk;
+          if constexpr (Q8) {
+            // each 128-column group: new moments, re-quantisation (the whole
+            // warp, in or out of range), then p from the dequantised moments
+            // (one group at a time: two at once spill under the 96-register cap)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int cl = k * 256 + h * 128 + lane * 4;
+              const float gs = __shfl_sync(0xffffffffu, qcur.s, kk * 2 + h);  // old group scale
+              float mq[1][4] = {{0.f, 0.f, 0.f, 0.f}}, c[1][4], sc[1];
+              float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (j0 + cl < W) {
+                float x[4];
+                quad_g<GT>(x, row, cl);
+                const float4 f = *reinterpret_cast<const float4*>(colf + cl);
+                pv = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
+                const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const float upd = (x[v] * r_i) * fv[v];
+                  mq[0][v] = fmaf(b1, q8_value(qcur.q[kk * 2 + h], v, gs), omb1 * upd);
+                }
+              }
+              q8_groups<1>(mq, c, sc);
+              if (j0 + cl < W) {
+                float* pp = &pv.x;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  pp[v] = q8_update(pp[v], wda, c[0][v], sc[0]);
+                  if (PSQ) psq = fmaf(pp[v], pp[v], psq);
+                }
+                __stcs(reinterpret_cast<float4*>(pg + cl), pv);
+                *reinterpret_cast<uint32_t*>(d.mq + base + i * W + j0 + cl) = q8_pack4(c[0]);
+              }
+              if (lane == 0 && j0 + k * 256 + h * 128 < W)
+                d.ms[(tp.b * H + i) * d.qg + (j0 + k * 256 + h * 128) / 128] = sc[0];
+            }
+          } else {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int cl = k * 256 + h * 128 + lane * 4;
-            const float gs = Q8 ? __shfl_sync(0xffffffffu, qcur.s, kk * 2 + h) : 0.f;  // group scale
-            float mq[4] = {0.f, 0.f, 0.f, 0.f};
             if (j0 + cl < W) {
               float x[4];
               quad_g<GT>(x, row, cl);
               const float4 f = *reinterpret_cast<const float4*>(colf + cl);
               float4 pv = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
               float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (B1 && !Q8) mv = *reinterpret_cast<const float4*>(row + RG::kG + RG::kP + cl * 4);
+              if (B1) mv = *reinterpret_cast<const float4*>(row + RG::kG + RG::kP + cl * 4);
               float* pp = &pv.x;
               float* mp = &mv.x;
               const float fv[4] = {f.x, f.y, f.z, f.w};
@@ -2051,26 +2153,17 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
               for (int v = 0; v < 4; ++v) {
                 float upd = (x[v] * r_i) * fv[v];
                 if (B1) {
-                  const float old = Q8 ? q8_value(qcur.q[kk * 2 + h], v, gs) : mp[v];
-                  mp[v] = fmaf(b1, old, omb1 * upd);
+                  mp[v] = fmaf(b1, mp[v], omb1 * upd);
                   upd = mp[v];
-                  if (Q8) mq[v] = mp[v];
                 }
                 const float pn = fmaf(-wda, pp[v], pp[v] - upd);
                 pp[v] = pn;
                 if (PSQ) psq = fmaf(pn, pn, psq);
               }
               __stcs(reinterpret_cast<float4*>(pg + cl), pv);
-              if (B1 && !Q8) __stcs(reinterpret_cast<float4*>(mg + cl), mv);
+              if (B1) __stcs(reinterpret_cast<float4*>(mg + cl), mv);
             }
-            if (Q8) {  // re-quantise the group (the whole warp, in or out of range)
-              float amax = fmaxf(fmaxf(fabsf(mq[0]), fabsf(mq[1])), fmaxf(fabsf(mq[2]), fabsf(mq[3])));
-              amax = warp_max_nonneg(amax);
-              if (j0 + cl < W)
-                *reinterpret_cast<uint32_t*>(d.mq + base + i * W + j0 + cl) = q8_pack4(mq, q8_inv(amax));
-              if (lane == 0 && j0 + k * 256 + h * 128 < W)
-                d.ms[(tp.b * H + i) * d.qg + (j0 + k * 256 + h * 128) / 128] = q8_scale(amax);
-            }
+          }
           }
         }
       }

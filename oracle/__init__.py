@@ -70,6 +70,16 @@ def _load():
                 dp, dp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), dp, dp, dp,
                 ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_float), dp,
                 ctypes.c_int64, ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
+            i8p, f32p = ctypes.POINTER(ctypes.c_int8), ctypes.POINTER(ctypes.c_float)
+            lib.oracle_q8_moment.restype = ctypes.c_int
+            lib.oracle_q8_moment.argtypes = [
+                dp, dp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), dp, dp, dp, i8p, f32p, dp, dp,
+                ctypes.c_int64, ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
+            lib.oracle_q8_quantize.restype = None
+            lib.oracle_q8_quantize.argtypes = [dp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), i8p, f32p]
+            lib.oracle_q8_apply.restype = None
+            lib.oracle_q8_apply.argtypes = [dp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), i8p, f32p,
+                                            ctypes.c_double, ctypes.POINTER(_HParams)]
             lib.oracle_check_hparams.restype = ctypes.c_int
             lib.oracle_check_hparams.argtypes = [ctypes.POINTER(_HParams), ctypes.c_char_p, ctypes.c_int]
             lib.oracle_rho.restype = ctypes.c_double
@@ -159,7 +169,7 @@ class State:
             rows, groups = q8_groups(shape)
             self.exp_avg_codes = np.zeros(n, np.int8)
             self.exp_avg_scales = np.zeros(rows * groups, np.float32)
-            self.moment = np.zeros(n, np.float64)  # the last step's unquantised moment
+            self.moment = np.zeros(n, np.float64)  # the last step's new moment, before quantisation
         else:
             self.exp_avg_codes = self.exp_avg_scales = self.moment = None
 
@@ -197,3 +207,63 @@ def step(p: np.ndarray, g: np.ndarray, state: State, t: int, hp: HParams) -> Non
         _ptr(state.v), _ptr(state.exp_avg), int(t), ctypes.byref(c), err, 256)
     if rc != 0:
         raise OracleError(err.value.decode())
+
+
+def _shape_arg(shape):
+    shape = tuple(int(s) for s in shape)
+    return (ctypes.c_int64 * max(1, len(shape)))(*shape) if shape else (ctypes.c_int64 * 1)(1), len(shape)
+
+
+def _i8(a):
+    assert a.dtype == np.int8 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int8))
+
+
+def _f32(a):
+    assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def q8_moment(p: np.ndarray, g: np.ndarray, state: State, t: int, hp: HParams):
+    """Part 1 of the 8-bit step: updates the second-moment state of `state` in
+    place and returns (m, alpha): the new first moment (float64, before
+    quantisation) formed from the stored codes and scales, and the step's lr.
+    p is read, not changed."""
+    assert state.q8
+    p_flat = np.ascontiguousarray(p, dtype=np.float64).reshape(-1)
+    g_flat = np.ascontiguousarray(g, dtype=np.float64).reshape(-1)
+    m = np.zeros(p_flat.size, np.float64)
+    alpha = ctypes.c_double(0.0)
+    shp, nd = _shape_arg(state.shape)
+    err = ctypes.create_string_buffer(256)
+    c = hp._c()
+    rc = _load().oracle_q8_moment(
+        _ptr(p_flat), _ptr(g_flat), nd, shp, _ptr(state.row), _ptr(state.col), _ptr(state.v),
+        _i8(state.exp_avg_codes), _f32(state.exp_avg_scales), _ptr(m), ctypes.byref(alpha), int(t),
+        ctypes.byref(c), err, 256)
+    if rc != 0:
+        raise OracleError(err.value.decode())
+    return m, alpha.value
+
+
+def q8_quantize(m: np.ndarray, shape):
+    """Part 2: the page's group quantiser on a moment of the given shape;
+    returns (codes int8 [N], scales float32 [rows * groups])."""
+    m = np.ascontiguousarray(m, dtype=np.float64).reshape(-1)
+    rows, groups = q8_groups(shape)
+    codes = np.zeros(m.size, np.int8)
+    scales = np.zeros(rows * groups, np.float32)
+    shp, nd = _shape_arg(shape)
+    _load().oracle_q8_quantize(_ptr(m), nd, shp, _i8(codes), _f32(scales))
+    return codes, scales
+
+
+def q8_apply(p: np.ndarray, codes: np.ndarray, scales: np.ndarray, shape, alpha: float, hp: HParams) -> None:
+    """Part 3: weight decay and the dequantised moment as the update, on p
+    (float64, contiguous) in place."""
+    if p.dtype != np.float64 or not p.flags["C_CONTIGUOUS"]:
+        raise OracleError("p must be a C-contiguous float64 array (updated in place)")
+    shp, nd = _shape_arg(shape)
+    c = hp._c()
+    _load().oracle_q8_apply(_ptr(p.reshape(-1)), nd, shp, _i8(codes), _f32(scales), float(alpha),
+                            ctypes.byref(c))

@@ -40,20 +40,30 @@
  *
  * Every quantity is float64; the step count t is 1-based.
  *
- * 8-bit first moment (oracle_adafactor_step_q8): the block-quantisation of
- * the ms-swift GaLore / Q-GaLore article ("Q-GaLore" section: groups of 128
- * values, a per-group scale absmax / 127, symmetric int8 codes) applied to
- * exp_avg.  Readings:
+ * 8-bit first moment (oracle_adafactor_step_q8): the block quantisation of
+ * the ms-swift GaLore / Q-GaLore article ("双重压缩：Q-Galore 的量化飞跃"
+ * section) applied to exp_avg.  Its quantize_tensor listing takes groups of
+ * 128 values, scale = (max |x| over the group) / 127, and code = the quotient
+ * x / scale rounded (torch's round: half to even) and clamped to [-128, 127];
+ * its dequantize_tensor is code * scale.  The surrounding QGaloreAdam listing
+ * dequantises the stored moment before the update is formed from it
+ * ("反投影前必须反量化": dequantise before projecting back).  Readings:
  *   - groups are 128 consecutive values along the last dim (a tensor with
- *     ndim < 2 is one row); the last group of a row may be shorter;
- *   - the stored state is the codes and one fp32 scale per group; the old
- *     moment is code * scale (an fp32 product); the new moment
- *     beta1 * old + (1 - beta1) * u is used unquantised for this step's
- *     update, then quantised: amax = max |m| over the group (m rounded to
- *     fp32), scale = amax / 127, code = rint(m * (127 / amax)) (fp32
- *     arithmetic, ties to even; code and scale 0 for an all-zero group).
- *     The rounding decision is taken in fp32, the precision of the stored
- *     state and of the CUDA kernels.
+ *     ndim < 2 is one row); the last group of a row may be shorter (the
+ *     listing's flat reshape(-1, 128) is the same grouping whenever the last
+ *     dim is a multiple of 128);
+ *   - arithmetic of the quantiser in fp32, the listing's tensor precision:
+ *     the new moment is rounded to fp32, amax = max |m|, scale = amax / 127,
+ *     code = rint(m / scale) (two correctly rounded fp32 divisions, ties to
+ *     even); a group whose scale is 0 (all zero, or amax / 127 below the
+ *     smallest fp32 value) stores codes 0 (the listing would divide by 0);
+ *   - one step: old moment = code * scale (fp32 product); new moment
+ *     m = beta1 * old + (1 - beta1) * u in float64; m is quantised; the
+ *     update applied to the parameter is the dequantised new moment
+ *     code * scale (fp32 product), the value the stored state holds.
+ * The three parts are exported separately (oracle_q8_moment,
+ * oracle_q8_quantize, oracle_q8_apply) so that a caller can inspect the
+ * codes between them; oracle_adafactor_step_q8 runs them in order.
  */
 #include <math.h>
 #include <stdint.h>
@@ -269,6 +279,102 @@ int oracle_adafactor_step(double* p, const double* g, int32_t ndim, const int64_
 /* Groups of the 8-bit first moment: 128 values along the last dim. */
 enum { ORACLE_Q8_GROUP = 128 };
 
+/* Rows and groups per row of the 8-bit moment of a tensor of n values. */
+static void q8_layout(int32_t ndim, const int64_t* shape, int64_t n, int64_t* last, int64_t* rows,
+                      int64_t* groups) {
+    *last = ndim >= 2 ? shape[ndim - 1] : n;
+    *rows = *last > 0 ? n / *last : 0;
+    *groups = (*last + ORACLE_Q8_GROUP - 1) / ORACLE_Q8_GROUP;
+}
+
+/* Dequantised value of one stored code: code * scale in fp32. */
+static double q8_dequant(int8_t code, float scale) {
+    const float x = (float)code * scale;
+    return (double)x;
+}
+
+/* Part 1 of the 8-bit step: the clipped, lr-scaled update u of this step
+ * (second-moment state updated in place), then the new first moment
+ * m = beta1 * old + (1 - beta1) * u with old the dequantised stored moment.
+ * moment_out [N] receives m (float64); *alpha_out the step's lr. */
+int oracle_q8_moment(const double* p, const double* g, int32_t ndim, const int64_t* shape, double* row,
+                     double* col, double* v, const int8_t* codes, const float* scales, double* moment_out,
+                     double* alpha_out, int64_t t, const oracle_hparams* hp, char* err, int errlen) {
+    if (!hp->has_beta1) {
+        set_err(err, errlen, "the 8-bit first moment needs beta1");
+        return ORACLE_INVALID;
+    }
+    double* u = NULL;
+    int64_t n = 0;
+    *alpha_out = 0.0;
+    int rc = compute_update(p, g, ndim, shape, row, col, v, t, hp, &u, alpha_out, &n, err, errlen);
+    if (rc != ORACLE_OK || n == 0) return rc;
+    int64_t last, rows, groups;
+    q8_layout(ndim, shape, n, &last, &rows, &groups);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < last; ++j) {
+            const int64_t e = r * last + j;
+            const double old = q8_dequant(codes[e], scales[r * groups + j / ORACLE_Q8_GROUP]);
+            moment_out[e] = hp->beta1 * old + (1.0 - hp->beta1) * u[e];
+        }
+    }
+    free(u);
+    return ORACLE_OK;
+}
+
+/* Part 2: the quantize_tensor listing on each group of the new moment, in
+ * fp32: m rounded to fp32, amax = max |m|, scale = amax / 127, code =
+ * rint(m / scale) clamped to [-128, 127]; codes 0 where the scale is 0 (an
+ * all-zero group, or one whose amax / 127 underflows). */
+void oracle_q8_quantize(const double* moment, int32_t ndim, const int64_t* shape, int8_t* codes,
+                        float* scales) {
+    int64_t n = 1;
+    for (int32_t k = 0; k < ndim; ++k) n *= shape[k];
+    int64_t last, rows, groups;
+    q8_layout(ndim, shape, n, &last, &rows, &groups);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t k = 0; k < groups; ++k) {
+            const int64_t j0 = k * ORACLE_Q8_GROUP;
+            const int64_t j1 = j0 + ORACLE_Q8_GROUP < last ? j0 + ORACLE_Q8_GROUP : last;
+            float amax = 0.0f;
+            for (int64_t j = j0; j < j1; ++j) {
+                const float a = fabsf((float)moment[r * last + j]);
+                if (a > amax) amax = a;
+            }
+            const float scale = amax / 127.0f;
+            scales[r * groups + k] = scale;
+            for (int64_t j = j0; j < j1; ++j) {
+                float q = 0.0f;
+                if (scale > 0.0f) {
+                    const float x = (float)moment[r * last + j] / scale;
+                    q = rintf(x);
+                    if (q < -128.0f) q = -128.0f;
+                    if (q > 127.0f) q = 127.0f;
+                }
+                codes[r * last + j] = (int8_t)q;
+            }
+        }
+    }
+}
+
+/* Part 3: decoupled weight decay, then the dequantised new moment
+ * code * scale as the update. */
+void oracle_q8_apply(double* p, int32_t ndim, const int64_t* shape, const int8_t* codes, const float* scales,
+                     double alpha, const oracle_hparams* hp) {
+    int64_t n = 1;
+    for (int32_t k = 0; k < ndim; ++k) n *= shape[k];
+    if (n == 0) return;
+    int64_t last, rows, groups;
+    q8_layout(ndim, shape, n, &last, &rows, &groups);
+    double* u = (double*)malloc((size_t)n * sizeof(double));
+    if (!u) return;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < last; ++j)
+            u[r * last + j] = q8_dequant(codes[r * last + j], scales[r * groups + j / ORACLE_Q8_GROUP]);
+    apply_update(p, u, n, alpha, hp);
+    free(u);
+}
+
 /* One step with the first moment held as int8 codes [N] and fp32 scales
  * [rows * ceil(last_dim / 128)] (rows = N / last_dim; last_dim = N for
  * ndim < 2).  Requires beta1.  moment_out [N] (may be NULL) receives the
@@ -277,56 +383,20 @@ int oracle_adafactor_step_q8(double* p, const double* g, int32_t ndim, const int
                              double* row, double* col, double* v, int8_t* codes, float* scales,
                              double* moment_out, int64_t t, const oracle_hparams* hp, char* err,
                              int errlen) {
-    if (!hp->has_beta1) {
-        set_err(err, errlen, "the 8-bit first moment needs beta1");
-        return ORACLE_INVALID;
-    }
-    double* u = NULL;
-    double alpha = 0.0;
-    int64_t n = 0;
-    int rc = compute_update(p, g, ndim, shape, row, col, v, t, hp, &u, &alpha, &n, err, errlen);
-    if (rc != ORACLE_OK || n == 0) return rc;
-    const int64_t last = ndim >= 2 ? shape[ndim - 1] : n;
-    const int64_t rows = n / last;
-    const int64_t groups = (last + ORACLE_Q8_GROUP - 1) / ORACLE_Q8_GROUP;
-    float* mq = (float*)malloc((size_t)ORACLE_Q8_GROUP * sizeof(float));
-    if (!mq) {
-        free(u);
+    int64_t n = 1;
+    for (int32_t k = 0; k < ndim && k < 8; ++k) n *= shape[k];
+    double* m = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (!m) {
         set_err(err, errlen, "out of host memory");
         return ORACLE_NOMEM;
     }
-    for (int64_t r = 0; r < rows; ++r) {
-        for (int64_t k = 0; k < groups; ++k) {
-            const int64_t j0 = k * ORACLE_Q8_GROUP;
-            const int64_t j1 = j0 + ORACLE_Q8_GROUP < last ? j0 + ORACLE_Q8_GROUP : last;
-            float* sc = &scales[r * groups + k];
-            float amax = 0.0f;
-            for (int64_t j = j0; j < j1; ++j) {
-                const int64_t e = r * last + j;
-                /* old moment: code * scale in fp32; new moment in float64 */
-                const float old = (float)codes[e] * (*sc);
-                const double m = hp->beta1 * (double)old + (1.0 - hp->beta1) * u[e];
-                u[e] = m;  /* this step's update uses the unquantised moment */
-                if (moment_out) moment_out[e] = m;
-                mq[j - j0] = (float)m;
-                const float a = fabsf(mq[j - j0]);
-                if (a > amax) amax = a;
-            }
-            if (amax > 0.0f) {
-                const float inv = 127.0f / amax;
-                *sc = amax / 127.0f;
-                for (int64_t j = j0; j < j1; ++j) {
-                    const float x = mq[j - j0] * inv;
-                    codes[r * last + j] = (int8_t)rintf(x);
-                }
-            } else {
-                *sc = 0.0f;
-                for (int64_t j = j0; j < j1; ++j) codes[r * last + j] = 0;
-            }
-        }
+    double alpha = 0.0;
+    int rc = oracle_q8_moment(p, g, ndim, shape, row, col, v, codes, scales, m, &alpha, t, hp, err, errlen);
+    if (rc == ORACLE_OK && n > 0) {
+        oracle_q8_quantize(m, ndim, shape, codes, scales);
+        oracle_q8_apply(p, ndim, shape, codes, scales, alpha, hp);
+        if (moment_out) memcpy(moment_out, m, (size_t)n * sizeof(double));
     }
-    free(mq);
-    apply_update(p, u, n, alpha, hp);
-    free(u);
-    return ORACLE_OK;
+    free(m);
+    return rc;
 }

@@ -37,12 +37,16 @@ MUTANTS = {
     "RMS without the mean": ("return sqrt(s / (double)n);", "return sqrt(s);"),
     "update not scaled by lr": ("u[k] = (u[k] / clip_div) * alpha;", "u[k] = (u[k] / clip_div);"),
     "exp_avg not used as the update": ("u[k] = exp_avg[k];", "(void)0;"),
-    "8-bit codes floored": ("codes[r * last + j] = (int8_t)rintf(x);", "codes[r * last + j] = (int8_t)floorf(x);"),
-    "8-bit scale over 128": ("*sc = amax / 127.0f;", "*sc = amax / 128.0f;"),
-    "8-bit groups flat across rows": ("const int64_t last = ndim >= 2 ? shape[ndim - 1] : n;",
-                                      "const int64_t last = n;"),
-    "8-bit moment not used as the update": ("u[e] = m;  /* this step's update uses the unquantised moment */",
-                                            "(void)0;"),
+    "8-bit codes floored": ("q = rintf(x);", "q = floorf(x);"),
+    "8-bit ties rounded away from zero": ("q = rintf(x);", "q = roundf(x);"),
+    "8-bit code by the reciprocal of the scale": (
+        "const float x = (float)moment[r * last + j] / scale;",
+        "const float x = (float)moment[r * last + j] * (127.0f / amax);"),
+    "8-bit scale over 128": ("const float scale = amax / 127.0f;", "const float scale = amax / 128.0f;"),
+    "8-bit groups flat across rows": ("*last = ndim >= 2 ? shape[ndim - 1] : n;", "*last = n;"),
+    "8-bit update from the unquantised moment": ("oracle_q8_apply(p, ndim, shape, codes, scales, alpha, hp);",
+                                                 "apply_update(p, m, n, alpha, hp);"),
+    "8-bit old moment without its scale": ("const float x = (float)code * scale;", "const float x = (float)code;"),
 }
 
 
