@@ -185,34 +185,50 @@ adaf_status adafactor_step(const adaf_tensor* tensors, const adaf_state* states,
                            size_t workspace_bytes, void* stream);
 
 /* adafactor_step_noalloc — the same step as adafactor_step(), with no
- * workspace argument and no allocation of any kind by the library (no
- * cudaMalloc/cudaFree, no pinned host buffer, no events).  The article has no
- * counterpart: this entry point exists for callers that cannot hand out device
- * memory, e.g. code running while a memory pool owns all of the device memory
- * and forbids cudaMalloc, code where an allocation would synchronise the
- * device at a point where that is not allowed, or hosts that link the library
- * without an allocator of their own.
+ * workspace argument and no device, pinned-host or event allocation by the
+ * library (no cudaMalloc/cudaFree, no cudaHostAlloc, no cudaEventCreate).  The
+ * article has no counterpart: this entry point exists for callers that cannot
+ * hand out device memory, e.g. code running while a memory pool owns all of
+ * the device memory and forbids cudaMalloc, code where an allocation would
+ * synchronise the device at a point where that is not allowed, or hosts that
+ * link the library without an allocator of their own.  The host-side planner
+ * still builds each call's descriptor table in ordinary heap memory.
  *   - Scratch: a fixed ADAF_NOALLOC_SCRATCH_BYTES (64 MiB) __device__ array
  *     inside the library.  Every GPU that loads the library holds it until the
  *     process exits.  A tensor list whose scratch need (adafactor_workspace_size)
  *     is larger is rejected with ADAF_ERR_WORKSPACE_TOO_SMALL and a message
  *     giving both sizes, before any CUDA call.
  *   - Set-up: the first call on each device looks up the array's device
- *     address (cudaGetSymbolAddress, with that device current); make that
- *     first call before any stream capture on the device.
+ *     address (cudaGetSymbolAddress, with that device current) and keeps it
+ *     for later calls; make that first call before any stream capture on the
+ *     device.  adafactor_release_cache() forgets the kept addresses: call it
+ *     after a device reset (cudaDeviceReset) before the next call.
+ *   - The descriptor table of each call is copied from a host buffer that
+ *     lives only for the call.  While `stream` is capturing, the call returns
+ *     ADAF_ERR_UNSUPPORTED and enqueues nothing.
  *   - Sharing: every call on a device uses the same array and finds the last
  *     call's contents there.  The step rewrites everything it reads (the
  *     status word is reset by each call), so nothing needs clearing by the
  *     caller, but calls whose work may overlap on the GPU (different streams
  *     without ordering, several host threads) race on the array: order them
  *     on one stream.
- *   - The header of each call is copied from pageable host memory; per-kernel
- *     event timing (adafactor_profile_*) does not cover this entry point.
+ *   - Per-kernel event timing (adafactor_profile_*) does not cover this entry
+ *     point; adafactor_noalloc_device_status() reads its status word.
  * Arguments, errors and results are those of adafactor_step() without the
- * workspace; adafactor_device_status() is not available for it. */
+ * workspace, plus ADAF_ERR_UNSUPPORTED for a capturing stream. */
 #define ADAF_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 adaf_status adafactor_step_noalloc(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
                                    int64_t step, const adaf_hparams* hp, void* stream);
+
+/* Device-side status of the most recent adafactor_step_noalloc() on the
+ * current device (the status word at the start of its scratch array, as
+ * adafactor_device_status() reads it from a workspace): waits on `stream`,
+ * then stores the word in *status (0, or ADAF_DEVICE_WAIT_TIMEOUT when a
+ * bounded wait inside a kernel gave up and that step's results are not
+ * valid).  Allocates nothing; synchronises the host with `stream`.  The
+ * article has no counterpart.  Errors: ADAF_ERR_INVALID_ARGUMENT (status
+ * NULL), ADAF_ERR_CUDA. */
+adaf_status adafactor_noalloc_device_status(void* stream, int32_t* status);
 
 /* ---- Row-sharded step (tensor rows split over several ranks) ------------
  * Step 4 of the article runs Adafactor on parameters split over a tensor-

@@ -28,7 +28,8 @@ EXPORTS = (
     "adafactor_default_hparams", "adafactor_validate", "adafactor_workspace_size",
     "adafactor_step", "adafactor_device_status", "adafactor_last_error", "adafactor_release_cache",
     "adafactor_profile_enable", "adafactor_profile_read", "adafactor_num_kernels",
-    "adafactor_kernel_name", "adafactor_step_noalloc", "adafactor_debug_stall_copies",
+    "adafactor_kernel_name", "adafactor_step_noalloc", "adafactor_noalloc_device_status",
+    "adafactor_debug_stall_copies",
     "adafactor_shard_sizes", "adafactor_shard_begin", "adafactor_shard_middle", "adafactor_shard_end",
 )
 # Entry points declared in include/came.h.
@@ -141,6 +142,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.adafactor_step_noalloc.restype = ctypes.c_int
         lib.adafactor_step_noalloc.argtypes = [P(adaf_tensor), P(adaf_state), ctypes.c_int32, ctypes.c_int64,
                                                P(adaf_hparams), ctypes.c_void_p]
+        lib.adafactor_noalloc_device_status.restype = ctypes.c_int
+        lib.adafactor_noalloc_device_status.argtypes = [ctypes.c_void_p, P(ctypes.c_int32)]
         lib.adafactor_device_status.restype = ctypes.c_int
         lib.adafactor_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, P(ctypes.c_int32)]
         lib.adafactor_debug_stall_copies.restype = None
@@ -276,6 +279,13 @@ def adafactor_shard_end(tensors, states, shards, n: int, step: int, hp: adaf_hpa
 def adafactor_device_status(workspace: int, stream: int) -> int:
     out = ctypes.c_int32(0)
     _check(load().adafactor_device_status(ctypes.c_void_p(workspace), ctypes.c_void_p(stream), ctypes.byref(out)))
+    return int(out.value)
+
+
+def adafactor_noalloc_device_status(stream: int) -> int:
+    """Status word of the last adafactor_step_noalloc() on the current device."""
+    out = ctypes.c_int32(0)
+    _check(load().adafactor_noalloc_device_status(ctypes.c_void_p(stream), ctypes.byref(out)))
     return int(out.value)
 
 

@@ -802,6 +802,7 @@ void adafactor_release_cache(void) {
   }
   g_prof.clear();
   g_cache.clear();
+  meo::noalloc_forget_addresses();
   if (have_dev) cudaSetDevice(cur);
 }
 

@@ -203,4 +203,7 @@ adaf_status step_impl(const adaf_tensor* tensors, const adaf_state* states, int3
                       HeaderStaging staging);
 // Records msg for adafactor_last_error() on this thread; returns st.
 adaf_status set_last_error(adaf_status st, const char* msg);
+// Forgets the per-device addresses of the no-alloc scratch array
+// (adafactor_noalloc.cu); adafactor_release_cache() calls it.
+void noalloc_forget_addresses();
 }  // namespace meo

@@ -58,6 +58,13 @@ adaf_status scratch_address(void** out) {
 
 }  // namespace
 
+namespace meo {
+void noalloc_forget_addresses() {
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  for (void*& a : g_scratch_addr) a = nullptr;
+}
+}  // namespace meo
+
 extern "C" {
 
 adaf_status adafactor_step_noalloc(const adaf_tensor* tensors, const adaf_state* states, int32_t n,
@@ -76,6 +83,21 @@ adaf_status adafactor_step_noalloc(const adaf_tensor* tensors, const adaf_state*
                   need, kNoAllocScratchBytes);
     return meo::set_last_error(ADAF_ERR_WORKSPACE_TOO_SMALL, msg);
   }
+  // The header upload below copies from a host buffer that lives only for
+  // this call; recorded into a graph, the copy would read freed memory on
+  // every replay.  So a capturing stream is turned away before any work.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap);
+  if (e != cudaSuccess) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg), "adafactor_step_noalloc: cudaStreamIsCapturing failed (%s)",
+                  cudaGetErrorString(e));
+    return meo::set_last_error(ADAF_ERR_CUDA, msg);
+  }
+  if (cap != cudaStreamCaptureStatusNone)
+    return meo::set_last_error(ADAF_ERR_UNSUPPORTED,
+                               "adafactor_step_noalloc: the stream is capturing; this entry point uploads its "
+                               "descriptor table from a host buffer that lives only for the call");
   void* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != ADAF_OK) return st;
@@ -83,6 +105,25 @@ adaf_status adafactor_step_noalloc(const adaf_tensor* tensors, const adaf_state*
   // from a pageable host buffer, so no pinned staging is allocated either.
   return meo::step_impl(tensors, states, n, step, hp, scratch, kNoAllocScratchBytes, stream,
                         meo::kStagePageable);
+}
+
+adaf_status adafactor_noalloc_device_status(void* stream, int32_t* status) {
+  if (status == nullptr) return meo::set_last_error(ADAF_ERR_INVALID_ARGUMENT, "status is NULL");
+  void* scratch = nullptr;
+  adaf_status st = scratch_address(&scratch);
+  if (st != ADAF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    char msg[160];
+    std::snprintf(msg, sizeof(msg), "adafactor_noalloc_device_status: reading the status word failed (%s)",
+                  cudaGetErrorString(e));
+    return meo::set_last_error(ADAF_ERR_CUDA, msg);
+  }
+  *status = v;
+  return ADAF_OK;
 }
 
 }  // extern "C"
