@@ -14,9 +14,12 @@ The ``*_lamb`` and ``*_came`` workloads run the multi-tensor LAMB
 line (metrics LAMB_METRIC, CAME_METRIC).
 
 --impl reference times the float64 CPU oracle (single thread) on a bounded
-sample of the same workload per step.  Under torchrun with N > 1 every rank
-runs an independent replica of the step on its own GPU (the step has no
-collective); value = total params/s over all ranks with the slowest rank's time.
+sample of the same workload per step.  With --gpus N > 1 every rank runs an
+independent replica of the step on its own GPU (the step has no collective);
+value = total params/s over all ranks with the slowest rank's time.  Started
+without torchrun, ``--gpus N`` re-launches itself under
+``python -m torch.distributed.run --nproc-per-node N`` (127.0.0.1, a free
+port); under torchrun, WORLD_SIZE must equal N.
 """
 from __future__ import annotations
 
@@ -60,6 +63,26 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return int(sk.getsockname()[1])
+
+
+def torchrun_cmd(nproc: int, script: str, argv, port: int):
+    """The single-node torch.distributed.run command that starts `script`
+    once per rank (one rank per GPU)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={int(nproc)}",
+            "--master-addr", "127.0.0.1", "--master-port", str(int(port)), script, *argv]
+
+
+def launch_ranks(nproc: int, script: str, argv) -> int:
+    """Runs `script` with `argv` as nproc ranks under torch.distributed.run;
+    returns the launcher's exit status (non-zero if any rank failed)."""
+    return subprocess.call(torchrun_cmd(nproc, script, list(argv), free_port()))
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -284,6 +307,86 @@ def traffic_record(kernel):
 
 
 # ---------------------------------------------------------------- our arm --
+def plain_h2d_rate(host_bufs, dev_bufs, dev, world, reps=2):
+    """The box's plain host->device copy rate for the same bytes as one e2e
+    step: one cudaMemcpyAsync per tensor (torch copy_ from pinned memory),
+    single stream, nothing else running; best of `reps`, CUDA events."""
+    nbytes = sum(b.numel() * b.element_size() for b in host_bufs)
+    s = torch.cuda.current_stream(dev)
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(s)
+        for hb, db in zip(host_bufs, dev_bufs):
+            db.copy_(hb, non_blocking=True)
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        best = ms if best is None else min(best, ms)
+    return {"h2d_gbs": nbytes / (best / 1e3) / 1e9, "bytes": nbytes, "ms": best,
+            "how": "one cudaMemcpyAsync per tensor from pinned host memory, one stream, best of "
+                   f"{reps}; frac_of_link = this copy time / the e2e step time"}
+
+
+HOST_NUMA = None
+
+
+def bind_to_gpu_numa_node(local: int):
+    """Restricts this process to the host CPUs of the GPU's NUMA node (from
+    sysfs), before any pinned buffer is allocated, so that pinned pages are
+    first touched on the node nearest the GPU.  Records what it did in
+    HOST_NUMA; leaves the affinity alone where sysfs gives no answer."""
+    global HOST_NUMA
+    info = {"gpu_numa_node": None, "cpus": None, "bound": False}
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(local), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=30).stdout.strip()
+        bus = out.lower()
+        if bus.count(":") == 2 and len(bus.split(":")[0]) == 8:
+            bus = bus[4:]  # nvidia-smi prints an 8-digit domain, sysfs a 4-digit one
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            node = int(f.read().strip())
+        info["gpu_numa_node"] = node
+        if node >= 0:
+            with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+                cpus = set()
+                for part in f.read().strip().split(","):
+                    if "-" in part:
+                        a, b = part.split("-")
+                        cpus.update(range(int(a), int(b) + 1))
+                    elif part:
+                        cpus.add(int(part))
+            allowed = os.sched_getaffinity(0) & cpus
+            if allowed:
+                os.sched_setaffinity(0, allowed)
+                info["cpus"] = len(allowed)
+                info["bound"] = True
+    except (OSError, ValueError, subprocess.SubprocessError):
+        pass
+    HOST_NUMA = info
+    return info
+
+
+class numa_local:
+    """Within the block, the process runs on the CPUs of the GPU's NUMA node
+    (bind_to_gpu_numa_node); the previous affinity comes back afterwards.  The
+    pinned buffers allocated inside keep their node-local pages."""
+
+    def __init__(self, local: int):
+        self.local = local
+        self.saved = None
+
+    def __enter__(self):
+        self.saved = os.sched_getaffinity(0)
+        bind_to_gpu_numa_node(self.local)
+        return self
+
+    def __exit__(self, *exc):
+        os.sched_setaffinity(0, self.saved)
+        return False
+
+
 def run_e2e(args, wl, params, grads, states, step, t, world, dev):
     """End to end through AdafactorStep, as a training loop with host-resident
     gradients would drive it: every step copies that step's bf16 grads from
@@ -367,11 +470,14 @@ def run_e2e(args, wl, params, grads, states, step, t, world, dev):
     run(2)  # warm-up: both step objects marshalled, carry primed
     ms = run(args.e2e_steps)
     norm = float(host_m.sum().sqrt())
+    link = plain_h2d_rate(host_g, grads, dev, world)
     out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": n * 8, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"per-tensor sum(p^2) of the updated params ({n} float64; param norm {norm:.4f})",
            "path": f"pinned host bf16 grads -> device (double-buffered, {ns} copy streams, overlapping the "
-                   "previous step), AdafactorStep, device->host read of the step metric"}
+                   "previous step), AdafactorStep, device->host read of the step metric",
+           "link": link, "host_numa": HOST_NUMA,
+           "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
     if args.readback_steps > 0:
         host_p = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in params]
         rms = run(args.readback_steps, readback=host_p)
@@ -477,7 +583,8 @@ def run_ours(args, world, rank, local):
     # ---- end to end: host grads in, host params out, through the same API
     e2e = None
     if args.e2e_steps > 0 and not args.shards:
-        e2e, t = run_e2e(args, wl, params, grads, states, step, t, world, dev)
+        with numa_local(local):
+            e2e, t = run_e2e(args, wl, params, grads, states, step, t, world, dev)
 
     grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
     step_bytes, impl_bytes, slot_bytes = algorithmic_bytes(wl.shapes, grad_bytes, beta1 is not None, q8)
@@ -598,11 +705,13 @@ def run_lamb_e2e(args, wl, params, grads, step, t, world, dev):
 
     run(2)
     ms = run(args.e2e_steps)
+    link = plain_h2d_rate(host_g, grads, dev, world)
     out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": n * 8, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"per-tensor trust ratios ({n} float64; mean {float(host_tr.mean()):.4f})",
            "path": "pinned host bf16 grads -> device (double-buffered, 1 copy stream, overlapping the previous "
-                   "step), LambStep, device->host read of the trust ratios"}
+                   "step), LambStep, device->host read of the trust ratios",
+           "link": link, "host_numa": HOST_NUMA, "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
     del host_g, grads2
     return out, t
 
@@ -645,7 +754,8 @@ def run_lamb(args, world, rank, local):
     ms_per_step = max_over_ranks(ev0.elapsed_time(ev1), world, dev) / args.steps
     e2e = None
     if args.e2e_steps > 0:
-        e2e, t = run_lamb_e2e(args, wl, params, grads, step, t, world, dev)
+        with numa_local(local):
+            e2e, t = run_lamb_e2e(args, wl, params, grads, step, t, world, dev)
     grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
     slot_bytes, design_bytes, one_pass_bytes = lamb_bytes(wl.numel, grad_bytes)
     peak, peak_kind = measured_hbm_peak()
@@ -759,7 +869,8 @@ def run_came(args, world, rank, local):
                 "algorithmic_bytes_per_launch": slot_bytes[dom_name], "avg_launch_ms": dom_ms / args.steps}
     e2e = None
     if args.e2e_steps > 0:
-        e2e = run_came_e2e(args, wl, params, grads, states, step, t, world, dev)
+        with numa_local(local):
+            e2e = run_came_e2e(args, wl, params, grads, states, step, t, world, dev)
     eff = design_bytes / (ms_per_step / 1e3) / 1e9
     out = {
         "metric": CAME_METRIC, "value": replica_throughput(wl.numel, world, ms_per_step), "unit": "params/s",
@@ -836,11 +947,13 @@ def run_came_e2e(args, wl, params, grads, states, step, t, world, dev):
 
     run(2)
     ms = run(args.e2e_steps)
+    link = plain_h2d_rate(host_g, grads, dev, world)
     out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": n * 4, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"first updated value of each tensor ({n} float32)",
            "path": "pinned host bf16 grads -> device (double-buffered, 1 copy stream, overlapping the previous "
-                   "step), CameStep, device->host read of one value per tensor"}
+                   "step), CameStep, device->host read of one value per tensor",
+           "link": link, "host_numa": HOST_NUMA, "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
     del host_g, grads2
     return out
 
@@ -1008,7 +1121,15 @@ def main():
     ap.add_argument("--shards", type=int, default=0,
                     help="run the row-sharded step with this many row shards on one GPU (exchange on the device)")
     args = ap.parse_args()
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one rank per GPU: start this same command under torch.distributed.run
+        sys.exit(launch_ranks(args.gpus, os.path.abspath(__file__), sys.argv[1:]))
     world, rank, local = dist_env()
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        sys.exit(2)
 
     if args.impl == "reference":
         if rank == 0:

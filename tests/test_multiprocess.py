@@ -42,6 +42,43 @@ def test_two_gloo_ranks_report_slowest_time_and_total_throughput():
     assert tput == pytest.approx(2 * 1_000_000 / 0.015)
 
 
+def test_launcher_starts_n_ranks_with_gloo(capfd):
+    """bench.launch_ranks runs a script as N ranks under torch.distributed.run
+    (the path `bench.py --gpus N` takes when started without torchrun); the
+    probe rank reports the world size and the slowest rank's time."""
+    import json
+    import sys
+    probe = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bench_rank_probe.py")
+    rc = bench.launch_ranks(2, probe, [])
+    assert rc == 0
+    lines = [ln for ln in capfd.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, lines
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2
+    assert rec["ms_per_step"] == 11.0
+    assert rec["value"] == pytest.approx(2 * 1_000_000 / 0.011)
+    assert sys.executable == bench.torchrun_cmd(2, probe, [], 1)[0]
+
+
+def test_bench_main_relaunches_for_gpus_n(monkeypatch):
+    """`bench.py --gpus 3` without WORLD_SIZE re-executes itself as 3 ranks and
+    exits with the launcher's status; under torchrun a WORLD_SIZE that differs
+    from --gpus is an error."""
+    calls = []
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench, "launch_ranks", lambda n, script, argv: calls.append((n, script, list(argv))) or 7)
+    monkeypatch.setattr("sys.argv", ["bench.py", "--gpus", "3", "--steps", "4"])
+    with pytest.raises(SystemExit) as ex:
+        bench.main()
+    assert ex.value.code == 7
+    assert calls == [(3, os.path.abspath(bench.__file__), ["--gpus", "3", "--steps", "4"])]
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setattr("sys.argv", ["bench.py", "--gpus", "4"])
+    with pytest.raises(SystemExit) as ex:
+        bench.main()
+    assert ex.value.code == 2
+
+
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
     assert bench.replica_throughput(8_030_261_248, 1, 20.0) == pytest.approx(8_030_261_248 / 0.02)
