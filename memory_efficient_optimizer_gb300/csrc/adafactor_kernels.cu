@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include "adafactor_internal.h"
+#include "row_panel.cuh"
 
 namespace meo {
 namespace {
@@ -1642,225 +1643,35 @@ __device__ __forceinline__ double consumer_sum(float v, double* red) {
   return s;
 }
 
-// Reduce-scatter of 4 per-lane values over the warp: afterwards lane l holds
-// the warp total of value ((l >> 4) & 1) * 2 + ((l >> 3) & 1), complete in
-// lanes 0, 8, 16, 24.  Fixed exchange pattern, so the sums are deterministic.
-__device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int lane) {
-  const bool h16 = lane & 16, h8 = lane & 8;
-  float k0 = h16 ? v[2] : v[0], k1 = h16 ? v[3] : v[1];
-  const float s0 = h16 ? v[0] : v[2], s1 = h16 ? v[1] : v[3];
-  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-  float k = h8 ? k1 : k0;
-  const float s = h8 ? k0 : k1;
-  k += __shfl_xor_sync(0xffffffffu, s, 8);
-  k += __shfl_xor_sync(0xffffffffu, k, 4);
-  k += __shfl_xor_sync(0xffffffffu, k, 2);
-  k += __shfl_xor_sync(0xffffffffu, k, 1);
-  return k;
-}
-
 // ---- fused pass 1 over row chunks (kFactoredRows) --------------------------
-// A work unit is a chunk of d.pr full rows of one slice, taken by one CTA of
-// NW warps in sub-panels of SR = 32 / NW rows.  Lane l of warp w owns the
-// column groups c * NW + w (c < G) of 256 columns, 8 consecutive columns
-// (256 (c NW + w) + 8 l + [0, 8)) in each, and keeps their column sums C_j
-// and D_j in registers.  Configurations: NW = 8, G = 2 for W <= 4096
-// (2 CTAs per SM); NW = 16, G = 4 for W <= 16384 (1 CTA per SM).
-//
-// Staging: every lane copies its own 16-byte pieces of each sub-panel into
-// its own shared-memory slots with cp.async (completion tracked per thread by
-// commit/wait groups: no spin loop, no mbarrier).  A ring of S sub-panels
-// per CTA keeps S - 1 sub-panels in flight while one is processed,
-// so the bytes in flight do not cost registers, and the second use of the
-// values (phase B) reads shared memory instead of L2 or HBM.  Since a lane
-// only ever reads the slots it filled, the staged data needs no barrier.
-// Per sub-panel k:
-//   wait for this thread's copies of sub-panel k;
-//   A. add the squares into C_j; the warp's share of each row total goes to
-//      shared memory (one reduce-scatter over the lanes covers the SR rows);
-//   -- barrier -- (row shares complete; every lane has finished sub-panel
-//      k - 1, whose stage is refilled now with sub-panel k + 2)
-//   every warp sums the NW shares of each row (lane l: row l / NW, warp
-//   l % NW) and forms row_r = beta2 row_r + (1 - beta2)(sum_j g_rj^2 / W +
-//   eps1) and its reciprocal; warp 0 stores row_r;
-//   B. add g_rj^2 / row_r into D_j from the same staged values.
-// With the column statistic of the step, sum(u^2) = mean(row) * sum_j D_j/col_j,
-// so g is read from HBM once here instead of twice.  Per chunk the warps
-// write C_j and D_j (column partials), and sum_r row_r goes to the row-chunk
-// sums (for mean(row)).
-
-// Configuration of the 2048 <= W <= 4096 class: warps, column groups per
-// lane, ring stages, CTAs per SM.
+// The shared row-panel pass (row_panel.cuh) over chunks of d.pr full rows:
+// the updated row statistic, the column partials C_j of g^2 and D_j of
+// g^2 / row_i, the row-chunk sums of the new row statistic and, when RMS(p)
+// is not carried, sum(p^2).  With the column statistic of the step,
+// sum(u^2) = mean(row) * sum_j D_j / col_j (k_stats, k_scalars), so g is read
+// from HBM once here instead of twice.  Configurations: NW = 8 warps, G = 2
+// column groups of 256 per lane for 2048 <= W <= 4096 (2 CTAs per SM);
+// NW = 16, G = 4 for W <= 16384 (1 CTA per SM).
 constexpr int kRowsNW = 8, kRowsG = 2, kRowsS = 3, kRowsMinB = 2;
 
-// Shared-memory ring of the fused pass: per stage and warp, slot
-// ((rr * G + c) * kPieces + q) * 32 + lane holds 16 bytes (piece q of the 8
-// values of row rr, column group c, lane), so every warp-wide copy and read
-// touches 512 contiguous bytes.
+// Dynamic shared memory of k_pass1_panel: ring and row shares, CTA-sum
+// scratch (64 doubles), member prefix.
 template <typename GT, int NW, int G, int S> struct PanelCfg {
-  static constexpr int kSubRows = 32 / NW;
-  static constexpr int kPieces = static_cast<int>(sizeof(GT)) / 2;  // 16-byte pieces per 8 values
-  static constexpr int kWarpBytes = kSubRows * G * kPieces * 32 * 16;
-  static constexpr int kStageBytes = kWarpBytes * NW;
-  static constexpr size_t kRedOff = static_cast<size_t>(S) * kStageBytes + sizeof(float) * 2 * 32;
+  static constexpr size_t kRedOff = panel::Cfg<GT, NW, G, S>::kBytes;
   static constexpr size_t kSmem = kRedOff + sizeof(double) * 64 + kPrefixBytes;
-  static_assert(kSubRows * NW == 32, "the row statistics take one (row, warp) share per lane");
-  static_assert(NW + 1 <= 64, "the CTA sum needs NW + 1 doubles");
+  static_assert(kRedOff % 8 == 0 && NW + 1 <= 64, "the CTA sum needs NW + 1 aligned doubles");
 };
-
-// 16-byte asynchronous global -> shared copy (bypasses L1).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Waits until at most N of this thread's most recent commit groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// This lane's copies of rows [q0, min(q0 + SR, q1)) into its slots of one
-// stage (dst: shared address of the lane's first slot in that stage).  FULL:
-// all SR rows and all of the lane's column groups are in range.
-template <bool FULL, typename GT, int NW, int G, int S>
-__device__ __forceinline__ void panel_issue(uint32_t dst, const GT* gb, int32_t W, int32_t q0, int32_t q1, int warp,
-                                            int lane) {
-  using C = PanelCfg<GT, NW, G, S>;
-  constexpr int P = C::kPieces;
-  const GT* src0 = gb + static_cast<int64_t>(q0) * W + warp * 256 + lane * 8;
-#pragma unroll
-  for (int rr = 0; rr < C::kSubRows; ++rr) {
-#pragma unroll
-    for (int c = 0; c < G; ++c) {
-      const int32_t j = (c * NW + warp) * 256 + lane * 8;
-      if (FULL || (q0 + rr < q1 && j < W)) {
-        const GT* src = src0 + static_cast<int64_t>(rr) * W + c * NW * 256;
-#pragma unroll
-        for (int q = 0; q < P; ++q)
-          cp_async16(dst + ((rr * G + c) * P + q) * 512, src + q * (16 / static_cast<int>(sizeof(GT))));
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void panel_read(Raw<__nv_bfloat16, 8>& r, const unsigned char* slot) {
-  r.u = *reinterpret_cast<const uint4*>(slot);
-}
-
-// Two-row version of reduce_scatter4: lane l gets the warp total of value
-// l >> 4 (complete in lanes 0 and 16).
-__device__ __forceinline__ float reduce_scatter2(const float (&v)[2], int lane) {
-  const bool h16 = lane & 16;
-  float k = h16 ? v[1] : v[0];
-  k += __shfl_xor_sync(0xffffffffu, h16 ? v[0] : v[1], 16);
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) k += __shfl_xor_sync(0xffffffffu, k, o);
-  return k;
-}
-__device__ __forceinline__ float panel_row_shares(const float (&v)[4], int lane) { return reduce_scatter4(v, lane); }
-__device__ __forceinline__ float panel_row_shares(const float (&v)[2], int lane) { return reduce_scatter2(v, lane); }
-
-// CTA-wide sum over NW warps in a fixed order (red: NW + 1 doubles).
-template <int NW>
-__device__ __forceinline__ double panel_block_sum(double v, double* red) {
-  v = warp_sum(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double s = 0.0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) s += red[w];
-    red[NW] = s;
-  }
-  __syncthreads();
-  const double s = red[NW];
-  __syncthreads();
-  return s;
-}
-
-// Phase A of the fused pass over the staged values of one sub-panel: squares
-// into C_j and this warp's share of each row total (rp).  FULL: every row of
-// the sub-panel and every column group of the lane is in range, so no
-// per-element predicates.  x^2 is exact in fp32 for a bf16 x, so
-// fma(x, x, acc) equals acc + x * x.
-template <bool FULL, typename GT, int NW, int G, bool PSQ>
-__device__ __forceinline__ void panel_phase_a(const unsigned char* st, int32_t s0, int32_t s1, int32_t W, int warp,
-                                              int lane, const float* pb, float2 (&cacc)[G][4],
-                                              float (&rp)[32 / NW], float& psq) {
-  constexpr int SR = 32 / NW, P = PanelCfg<GT, NW, G, 3>::kPieces;
-#pragma unroll
-  for (int rr = 0; rr < SR; ++rr) {
-    float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < G; ++c) {
-      const int32_t j = (c * NW + warp) * 256 + lane * 8;
-      if (FULL || (s0 + rr < s1 && j < W)) {
-        Raw<GT, 8> raw;
-        panel_read(raw, st + (rr * G + c) * P * 512);
-        float2 x[4];
-        widen2(raw, x);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          cacc[c][v] = __ffma2_rn(x[v], x[v], cacc[c][v]);
-          s2 = __ffma2_rn(x[v], x[v], s2);
-        }
-        if (PSQ) {
-          float y[8];
-          load_f<8>(y, pb + static_cast<int64_t>(s0 + rr) * W + j);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) psq = fmaf(y[v], y[v], psq);
-        }
-      }
-    }
-    rp[rr] = s2.x + s2.y;
-  }
-}
-
-// Phase B: g^2 / row_r into D_j (lane rr * NW holds 1 / row of row rr).
-template <bool FULL, typename GT, int NW, int G>
-__device__ __forceinline__ void panel_phase_b(const unsigned char* st, int32_t s0, int32_t s1, int32_t W, int warp,
-                                              int lane, float winv, float2 (&dacc)[G][4]) {
-  constexpr int SR = 32 / NW, P = PanelCfg<GT, NW, G, 3>::kPieces;
-#pragma unroll
-  for (int rr = 0; rr < SR; ++rr) {
-    const float wr = __shfl_sync(0xffffffffu, winv, rr * NW);
-    const float2 w2 = make_float2(wr, wr);
-#pragma unroll
-    for (int c = 0; c < G; ++c) {
-      const int32_t j = (c * NW + warp) * 256 + lane * 8;
-      if (FULL || (s0 + rr < s1 && j < W)) {
-        Raw<GT, 8> raw;
-        panel_read(raw, st + (rr * G + c) * P * 512);
-        float2 x[4];
-        widen2(raw, x);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) dacc[c][v] = __ffma2_rn(__fmul2_rn(x[v], w2), x[v], dacc[c][v]);
-      }
-    }
-  }
-}
 
 template <typename GT, int NW, int G, int S, int MINB, bool PSQ>
 __global__ void __launch_bounds__(NW * 32, MINB)
     k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
-  using C = PanelCfg<GT, NW, G, S>;
-  constexpr int SR = C::kSubRows;
-  static_assert(S >= 2, "the ring needs the stage in use and one in flight");
   extern __shared__ __align__(16) unsigned char smem[];
-  float* part = reinterpret_cast<float*>(smem + S * C::kStageBytes);  // [2][SR][NW]
-  double* red = reinterpret_cast<double*>(smem + C::kRedOff);
+  double* red = reinterpret_cast<double*>(smem + PanelCfg<GT, NW, G, S>::kRedOff);
   int32_t* pf = reinterpret_cast<int32_t*>(red + 64);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
   const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
   const float eps1 = static_cast<float>(a.eps1);
-  const unsigned char* mine = smem + warp * C::kWarpBytes + lane * 16;
-  const uint32_t mine_s = static_cast<uint32_t>(__cvta_generic_to_shared(mine));
-  const int rl = lane / NW;  // row of this lane's (row, warp) share
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
@@ -1869,91 +1680,25 @@ __global__ void __launch_bounds__(NW * 32, MINB)
     const int32_t b = local / d.prb, chunk = local % d.prb;
     const int32_t H = static_cast<int32_t>(d.H), W = static_cast<int32_t>(d.W);
     const int32_t c0 = chunk * d.pr, c1 = min(H, c0 + d.pr);
-    const int32_t nsub = (c1 - c0 + SR - 1) / SR;
     const GT* gb = static_cast<const GT*>(d.g) + static_cast<int64_t>(b) * H * W;
     const float* pb = d.p + static_cast<int64_t>(b) * H * W;
-    float* rowst = d.row + static_cast<int64_t>(b) * H;
-    const float invw = 1.0f / static_cast<float>(W);
-    float2 cacc[G][4], dacc[G][4];
-#pragma unroll
-    for (int c = 0; c < G; ++c) {
-#pragma unroll
-      for (int v = 0; v < 4; ++v) cacc[c][v] = dacc[c][v] = make_float2(0.f, 0.f);
-    }
-    float psq = 0.f, rsum = 0.f;
-    // Prologue: sub-panels 0 .. S - 2 (one commit group each, empty past
-    // the chunk's end, so the group count stays in step).
-#pragma unroll
-    for (int k = 0; k < S - 1; ++k) {
-      if (k < nsub) panel_issue<false, GT, NW, G, S>(mine_s + k * C::kStageBytes, gb, W, c0 + k * SR, c1, warp, lane);
-      cp_async_commit();
-    }
-    // Column groups of this warp all inside the row (warp-uniform).
-    const bool cols_full = ((G - 1) * NW + warp + 1) * 256 <= W;
-    int stage = 0;
-    for (int32_t k = 0; k < nsub; ++k) {
-      const int32_t s0 = c0 + k * SR, s1 = min(c1, s0 + SR);
-      const bool full = cols_full && s1 - s0 == SR;
-      const float row_old = (s0 + rl < s1) ? rowst[s0 + rl] : 0.f;
-      cp_async_wait<S - 2>();  // groups up to sub-panel k are complete
-      const unsigned char* st = mine + stage * C::kStageBytes;
-      float* pk = part + (k & 1) * 32;
-      float rp[SR];
-      if (full) panel_phase_a<true, GT, NW, G, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
-      else panel_phase_a<false, GT, NW, G, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
-      const float tot = panel_row_shares(rp, lane);  // warp total of row rl
-      if (lane % NW == 0) pk[rl * NW + warp] = tot;
-      __syncthreads();
-      // Refill the stage of sub-panel k - 1 (every lane is past it) with k + S - 1.
-      {
-        const int32_t kk = k + S - 1;
-        const int fill = stage == 0 ? S - 1 : stage - 1;
-        if (kk < nsub) {
-          if (cols_full && c0 + (kk + 1) * SR <= c1)
-            panel_issue<true, GT, NW, G, S>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
-          else
-            panel_issue<false, GT, NW, G, S>(mine_s + fill * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
-        }
-        cp_async_commit();
-      }
-      // Row statistics of the sub-panel, in every warp: lane l adds the
-      // shares of row l / NW over the warps (fixed xor tree).
-      float R = pk[lane];
-#pragma unroll
-      for (int o = NW / 2; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
-      const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
-      const float winv = __frcp_rn(rn);  // correctly rounded 1 / rn
-      if (warp == 0 && lane % NW == 0 && s0 + rl < s1) {
-        rowst[s0 + rl] = rn;
-        rsum += rn;
-      }
-      if (full) panel_phase_b<true, GT, NW, G>(st, s0, s1, W, warp, lane, winv, dacc);
-      else panel_phase_b<false, GT, NW, G>(st, s0, s1, W, warp, lane, winv, dacc);
-      stage = stage == S - 1 ? 0 : stage + 1;
-    }
-    // column partials of the chunk
-    float* cp = a.colpart + d.colpart + static_cast<int64_t>(b * d.prb + chunk) * W;
-    float* dp = a.dpart + d.dpart + static_cast<int64_t>(b * d.prb + chunk) * W;
-#pragma unroll
-    for (int c = 0; c < G; ++c) {
-      const int32_t j = (c * NW + warp) * 256 + lane * 8;
-      if (j < W) {
-        *reinterpret_cast<float4*>(cp + j) = make_float4(cacc[c][0].x, cacc[c][0].y, cacc[c][1].x, cacc[c][1].y);
-        *reinterpret_cast<float4*>(cp + j + 4) = make_float4(cacc[c][2].x, cacc[c][2].y, cacc[c][3].x, cacc[c][3].y);
-        *reinterpret_cast<float4*>(dp + j) = make_float4(dacc[c][0].x, dacc[c][0].y, dacc[c][1].x, dacc[c][1].y);
-        *reinterpret_cast<float4*>(dp + j + 4) = make_float4(dacc[c][2].x, dacc[c][2].y, dacc[c][3].x, dacc[c][3].y);
-      }
-    }
+    auto where = [&]() {
+      const int64_t off = static_cast<int64_t>(b * d.prb + chunk) * W;
+      return panel::Partials{a.colpart + d.colpart + off, a.dpart + d.dpart + off};
+    };
+    float rsum = 0.f, psq = 0.f;
+    panel::run_chunk<GT, NW, G, S, PSQ>(smem, gb, pb, d.row + static_cast<int64_t>(b) * H, W, c0, c1, b2, omb2, eps1,
+                                        where, rsum, psq);
     // (the barriers of the CTA sums also order this chunk's last reads of
     // the ring before the next chunk's prologue refills it)
-    const double rtot = panel_block_sum<NW>(static_cast<double>(rsum), red);
+    const double rtot = panel::block_sum<NW>(static_cast<double>(rsum), red);
     if (PSQ) {
-      const double ptot = panel_block_sum<NW>(static_cast<double>(psq), red);
+      const double ptot = panel::block_sum<NW>(static_cast<double>(psq), red);
       if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = ptot;
     }
     if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + chunk] = rtot;
   }
-  cp_async_wait_all();  // only empty groups can be pending here
+  panel::cp_async_wait_all();  // only empty groups can be pending here
 }
 
 // ---- apply (vector path) ---------------------------------------------------
