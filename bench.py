@@ -792,25 +792,38 @@ def run_lamb(args, world, rank, local):
 
 
 # ------------------------------------------------------------------ CAME --
+def came_panel(shape, grad_bytes):
+    """Whether the CAME step takes the row-panel pass for a contiguous,
+    256-byte aligned tensor: bf16 matrices with W % 8 == 0, 2048 <= W <= 16384."""
+    return len(shape) >= 2 and grad_bytes == 2 and int(shape[-1]) % 8 == 0 and 2048 <= int(shape[-1]) <= 16384
+
+
 def came_bytes(shapes, grad_bytes):
     """Algorithmic HBM bytes of a CAME step per launch slot of this design.
-    Factored tensors: pass a reads g; pass b reads g; pass c reads g and m and
-    writes m; pass d reads m and p and writes p.  1D tensors: pass a reads g
-    and v and writes v; pass c reads g, v, m, S, p and writes m, S, p.  (The
-    row/column statistics and partial sums are under 0.2 % and left out.)
-    Returns (slots, per step, one-pass minimum g + m and p read and written)."""
-    nf = n1 = 0
+    Row-panel tensors: the panel pass reads g once (statistics and sum(u^2)).
+    Other factored tensors: pass a reads g; pass b reads g.  Every factored
+    tensor: pass c reads g and m and writes m; pass d reads m and p and writes
+    p.  1D tensors: pass a reads g and v and writes v; pass c reads g, v, m,
+    S, p and writes m, S, p.  (The row/column statistics and partial sums are
+    under 0.2 % and left out.)  Returns (slots, per step, one-pass minimum
+    g + m and p read and written)."""
+    nf = n1 = npan = 0
     for _, s in shapes:
         n = 1
         for d in s:
             n *= int(d)
         if len(s) >= 2:
             nf += n
+            if came_panel(s, grad_bytes):
+                npan += n
         else:
             n1 += n
     g = grad_bytes
-    slots = {"k_came_pass_a": nf * g + n1 * (g + 8), "k_came_pass_b": nf * g,
+    slots = {"k_came_pass_a": (nf - npan) * g + n1 * (g + 8), "k_came_pass_b": (nf - npan) * g,
              "k_came_pass_c": nf * (g + 8) + n1 * (g + 28), "k_came_pass_d": nf * 12}
+    if npan:
+        slots["k_came_panel"] = npan * g
+    slots = {k: v for k, v in slots.items() if v}
     return slots, sum(slots.values()), (nf + n1) * (g + 16)
 
 

@@ -10,7 +10,12 @@
 // passes with small reductions between them:
 //
 //   k_came_pass_a   g -> per-tile row and column sums of g^2        (read g)
-//   k_came_stats    row/col EMAs of the means (+ eps1), row-chunk sums
+//   k_came_panel    (bf16 matrices with 2048 <= W <= 16384, instead of
+//                   passes a and b) g -> the row EMA, per-chunk column sums
+//                   of g^2 and of g^2 / r_i: sum(u^2) without a second read
+//                   of g (the shared row-panel pass, row_panel.cuh)
+//   k_came_stats    row/col EMAs of the means (+ eps1), row-chunk sums;
+//                   panel tensors: the column EMA and sum_j D_j / c_j
 //   k_came_means    mean(r) per slice
 //   k_came_pass_b   per-tile sum(u^2), u = g (r_i/mean r)^-1/2 c_j^-1/2 (read g)
 //   k_came_clip     coef = 1 / max(1, RMS(u) / d) per tensor
@@ -45,6 +50,7 @@
 
 #include "adafactor_internal.h"
 #include "came.h"
+#include "row_panel.cuh"
 
 namespace {
 
@@ -78,13 +84,32 @@ struct CDev {
   int64_t rc0, nrc;    // row-chunk sum slots: B * nrc
   int64_t ncc;         // column items per slice
   int32_t gdt, cls;
+  // Row-panel tensors (panel = 1: 8 warps x 2 groups, W <= 4096; 2: 16 x 4,
+  // W <= 16384; 0: none): chunks of pr rows, prb per slice.
+  int32_t panel, pr;
+  int64_t prb;
+  int64_t pcol;        // float offset of the panel column partials [B][prb][W] (g^2 and g^2 / r)
+  int64_t prc0;        // double offset of the panel row-chunk sums [B][prb]
+  int64_t dsum0;       // double offset of sum_j D_j / c_j per column item [B][ncc]
 };
+
+constexpr int kPanelCfgs = 2;  // row-panel configurations (CDev::panel - 1)
+// Work lists: pass a and pass b walk the tiles of the tensors outside the
+// row panels (kListAB), passes c and d those of every tensor (kListCD).
+enum List : int32_t { kListAB = 0, kListCD = 1 };
 
 struct CArgs {
   const CDev* dev;
-  const int64_t* pf[kClasses];   // per class: first tile of each member, then the total
-  const int32_t* idx[kClasses];  // per class: tensor index of each member
-  int32_t nmem[kClasses];
+  const int64_t* pf[2][kClasses];   // per list and class: first tile of each member, then the total
+  const int32_t* idx[2][kClasses];  // per list and class: tensor index of each member
+  int32_t nmem[2][kClasses];
+  const int64_t* ppf[kPanelCfgs];   // per panel configuration: first chunk of each member, then the total
+  const int32_t* pidx[kPanelCfgs];
+  int32_t pnmem[kPanelCfgs];
+  float* pcolpart;
+  float* pdpart;
+  double* prchunk;
+  double* dsum;
   const int64_t* item_pf;        // statistics items of factored tensors
   const int32_t* item_idx;
   int32_t nfact;
@@ -247,17 +272,20 @@ __device__ __forceinline__ void store_col_sums(const CDev& d, const CArgs& a, co
   __syncthreads();  // colbuf is reused by the next tile
 }
 
-// Walks the tiles of one class: calls body(d, t, local) for each.
+// Walks the units of one member list: calls body(d, t, local) for each.
 template <typename Body>
-__device__ __forceinline__ void walk(const CArgs& a, int cls, Body&& body) {
-  const int64_t* pf = a.pf[cls];
-  const int nm = a.nmem[cls];
+__device__ __forceinline__ void walk_list(const CArgs& a, const int64_t* pf, const int32_t* idx, int nm, Body&& body) {
   int k = 0;
   for (int64_t u = blockIdx.x; u < pf[nm]; u += gridDim.x) {
     while (pf[k + 1] <= u) ++k;
-    const int t = a.idx[cls][k];
+    const int t = idx[k];
     body(a.dev[t], t, u - pf[k]);
   }
+}
+// Walks the tiles of one class in one list (kListAB, kListCD).
+template <typename Body>
+__device__ __forceinline__ void walk(const CArgs& a, int list, int cls, Body&& body) {
+  walk_list(a, a.pf[list][cls], a.idx[list][cls], a.nmem[list][cls], body);
 }
 
 // ---- pass a: row / column sums of g^2 (factored), v and sum(u^2) (1D) -------
@@ -336,10 +364,41 @@ __global__ void __launch_bounds__(kThreads, 2) k_came_pass_a(const __grid_consta
   extern __shared__ __align__(16) unsigned char smem[];
   float* colbuf = reinterpret_cast<float*>(smem);
   double* red = reinterpret_cast<double*>(smem + sizeof(float) * kWarps * kTC);
-  walk(a, cls, [&](const CDev& d, int, int64_t local) {
+  walk(a, kListAB, cls, [&](const CDev& d, int, int64_t local) {
     if (cls == k1D) pass_a_1d(d, a, local, red);
     else pass_a_tile<VEC, GK>(d, a, local, colbuf);
   });
+}
+
+// ---- row-panel pass: statistics and sum(u^2) in one read of g ----------------
+// The shared row-panel pass (row_panel.cuh) over chunks of d.pr full rows of
+// bf16 matrices: r_i updated in place (beta2, eps1), the chunk's column sums
+// C_j of g^2 and D_j of g^2 / r_i, and the chunk's sum of the new r_i.  Then
+// sum(u^2) = sum_ij g^2 mean(r) / (r_i c_j) = mean(r) sum_j D_j / c_j
+// (k_came_stats, k_came_clip): pass b does not run for these tensors.
+template <int NW, int G, int S, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB) k_came_panel(const __grid_constant__ CArgs a, int q) {
+  using C = meo::panel::Cfg<__nv_bfloat16, NW, G, S>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  double* red = reinterpret_cast<double*>(smem + C::kBytes);
+  walk_list(a, a.ppf[q], a.pidx[q], a.pnmem[q], [&](const CDev& d, int, int64_t local) {
+    const int64_t b = local / d.prb, chunk = local % d.prb;
+    const int32_t H = static_cast<int32_t>(d.H), W = static_cast<int32_t>(d.W);
+    const int32_t c0 = static_cast<int32_t>(chunk) * d.pr, c1 = min(H, c0 + d.pr);
+    const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(d.g) + b * d.H * d.W;
+    auto where = [&]() {
+      const int64_t off = d.pcol + (b * d.prb + chunk) * d.W;
+      return meo::panel::Partials{a.pcolpart + off, a.pdpart + off};
+    };
+    float rsum = 0.f, psq = 0.f;
+    meo::panel::run_chunk<__nv_bfloat16, NW, G, S, false>(smem, gb, nullptr, d.row + b * d.H, W, c0, c1, a.b2,
+                                                          a.omb2, a.eps1, where, rsum, psq);
+    // (its barriers also order this chunk's last reads of the ring before
+    // the next chunk's first copies)
+    const double tot = meo::panel::block_sum<NW>(static_cast<double>(rsum), red);
+    if (threadIdx.x == 0) a.prchunk[d.prc0 + b * d.prb + chunk] = tot;
+  });
+  meo::panel::cp_async_wait_all();  // only empty groups can be pending here
 }
 
 // ---- statistics: EMAs of the row / column means, row-chunk sums ------------
@@ -358,7 +417,9 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
     float* rowst = a.phase ? d.rrow : d.row;
     float* colst = a.phase ? d.rcol : d.col;
     const int64_t local = it - a.item_pf[k];
+    const bool panel0 = a.phase == 0 && d.panel != 0;  // rows done by the row-panel pass
     if (local < d.B * d.nrc) {
+      if (panel0) continue;
       const int64_t b = local / d.nrc, q = local % d.nrc;
       const int64_t i0 = q * kRowItem, i1 = min(d.H, i0 + kRowItem);
       double acc = 0.0;
@@ -372,6 +433,27 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
       }
       const double tot = block_sum(acc, red);
       if (threadIdx.x == 0) a.rchunk[d.rc0 + local] = tot;
+    } else if (panel0) {
+      // column EMA from the chunks' sums of g^2, and this item's share of
+      // sum_j D_j / c_j from the chunks' sums of g^2 / r_i
+      const int64_t l2 = local - d.B * d.nrc;
+      const int64_t b = l2 / d.ncc, q = l2 % d.ncc;
+      const int64_t j = q * kColItem + threadIdx.x;
+      double term = 0.0;
+      if (j < d.W) {
+        const int64_t o = d.pcol + b * d.prb * d.W + j;
+        double sc = 0.0, sd = 0.0;
+        for (int64_t r = 0; r < d.prb; ++r) {
+          sc += a.pcolpart[o + r * d.W];
+          sd += a.pdpart[o + r * d.W];
+        }
+        const float mean = static_cast<float>(sc / static_cast<double>(d.H) + eps);
+        const float cn = fmaf(beta, colst[b * d.W + j], omb * mean);
+        colst[b * d.W + j] = cn;
+        term = sd / static_cast<double>(cn);
+      }
+      const double tot = block_sum(term, red);
+      if (threadIdx.x == 0) a.dsum[d.dsum0 + b * d.ncc + q] = tot;
     } else {
       const int64_t l2 = local - d.B * d.nrc;
       const int64_t b = l2 / d.ncc, q = l2 % d.ncc;
@@ -390,9 +472,13 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
 __global__ void __launch_bounds__(kThreads) k_came_means(const __grid_constant__ CArgs a) {
   __shared__ double red[kWarps];
   const CDev d = a.dev[a.item_idx[blockIdx.x]];
+  const bool panel0 = a.phase == 0 && d.panel != 0;  // row sums from the row-panel pass
   for (int64_t b = 0; b < d.B; ++b) {
     double s = 0.0;
-    for (int64_t q = threadIdx.x; q < d.nrc; q += kThreads) s += a.rchunk[d.rc0 + b * d.nrc + q];
+    if (panel0)
+      for (int64_t q = threadIdx.x; q < d.prb; q += kThreads) s += a.prchunk[d.prc0 + b * d.prb + q];
+    else
+      for (int64_t q = threadIdx.x; q < d.nrc; q += kThreads) s += a.rchunk[d.rc0 + b * d.nrc + q];
     const double tot = block_sum(s, red);
     if (threadIdx.x == 0) a.mean[d.slice0 + b] = tot / static_cast<double>(d.H);
   }
@@ -457,16 +543,27 @@ template <int VEC, int GK>
 __global__ void __launch_bounds__(kThreads, 2) k_came_pass_b(const __grid_constant__ CArgs a, int cls) {
   __shared__ __align__(16) float cinv[kTC];
   __shared__ double red[kWarps];
-  walk(a, cls, [&](const CDev& d, int, int64_t local) { pass_b_tile<VEC, GK>(d, a, local, cinv, red); });
+  walk(a, kListAB, cls, [&](const CDev& d, int, int64_t local) { pass_b_tile<VEC, GK>(d, a, local, cinv, red); });
 }
 
 // ---- clip: coef = 1 / max(1, RMS(u) / d), one CTA per tensor ---------------
 __global__ void __launch_bounds__(kThreads) k_came_clip(const __grid_constant__ CArgs a) {
   __shared__ double red[kWarps];
   const CDev d = a.dev[blockIdx.x];
-  double s = 0.0;
-  for (int64_t k = threadIdx.x; k < d.nsp; k += kThreads) s += a.uspart[d.sp0 + k];
-  const double tot = block_sum(s, red);
+  double tot = 0.0;
+  if (d.panel) {
+    // sum(u^2) = sum_b mean(r)_b sum_j D_bj / c_bj (a.mean: mean(r) of phase 0)
+    for (int64_t b = 0; b < d.B; ++b) {
+      double s = 0.0;
+      for (int64_t q = threadIdx.x; q < d.ncc; q += kThreads) s += a.dsum[d.dsum0 + b * d.ncc + q];
+      const double sb = block_sum(s, red);
+      if (threadIdx.x == 0) tot += a.mean[d.slice0 + b] * sb;
+    }
+  } else {
+    double s = 0.0;
+    for (int64_t k = threadIdx.x; k < d.nsp; k += kThreads) s += a.uspart[d.sp0 + k];
+    tot = block_sum(s, red);
+  }
   if (threadIdx.x == 0) {
     const double r = d.n > 0 ? sqrt(tot / static_cast<double>(d.n)) / static_cast<double>(a.clip) : 0.0;
     a.coef[blockIdx.x] = 1.0 / (r > 1.0 ? r : 1.0);
@@ -560,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_came_pass_c(const __grid_consta
   extern __shared__ __align__(16) unsigned char smem[];
   float* colbuf = reinterpret_cast<float*>(smem);
   float* colf = colbuf + kWarps * kTC;
-  walk(a, cls, [&](const CDev& d, int t, int64_t local) {
+  walk(a, kListCD, cls, [&](const CDev& d, int t, int64_t local) {
     if (cls == k1D) pass_c_1d(d, a, t, local);
     else pass_c_tile<VEC, GK>(d, a, t, local, colbuf, colf);
   });
@@ -614,7 +711,7 @@ __device__ __forceinline__ void pass_d_tile(const CDev& d, const CArgs& a, int64
 template <int VEC>
 __global__ void __launch_bounds__(kThreads, 2) k_came_pass_d(const __grid_constant__ CArgs a, int cls) {
   __shared__ __align__(16) float cf[kTC];
-  walk(a, cls, [&](const CDev& d, int, int64_t local) { pass_d_tile<VEC>(d, a, local, cf); });
+  walk(a, kListCD, cls, [&](const CDev& d, int, int64_t local) { pass_d_tile<VEC>(d, a, local, cf); });
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -630,16 +727,29 @@ constexpr size_t kColbufBytes = sizeof(float) * kWarps * kTC;
 constexpr size_t kPassASmem = kColbufBytes + sizeof(double) * kWarps;
 constexpr size_t kPassCSmem = kColbufBytes + sizeof(float) * kTC;
 
+// Row-panel configurations (warps, column groups of 256 per lane, ring
+// stages, CTAs per SM; rows per chunk): the Adafactor step's two.
+constexpr int kP1NW = 8, kP1G = 2, kP1S = 3, kP1MinB = 2, kP1Rows = 256;   // 2048 <= W <= 4096
+constexpr int kP2NW = 16, kP2G = 4, kP2S = 3, kP2MinB = 1, kP2Rows = 128;  // 4096 < W <= 16384
+template <int NW, int G, int S>
+constexpr size_t panel_smem() {
+  return meo::panel::Cfg<__nv_bfloat16, NW, G, S>::kBytes + sizeof(double) * (NW + 1);
+}
+
 // The plan of one call: descriptors, class lists, statistics items, offsets.
 struct Plan {
   std::vector<CDev> dev;
-  std::vector<int64_t> pf[kClasses];
-  std::vector<int32_t> idx[kClasses];
+  std::vector<int64_t> pf[2][kClasses];
+  std::vector<int32_t> idx[2][kClasses];
+  std::vector<int64_t> ppf[kPanelCfgs];
+  std::vector<int32_t> pidx[kPanelCfgs];
   std::vector<int64_t> item_pf;
   std::vector<int32_t> item_idx;
-  int64_t rowpart = 0, colpart = 0, usp = 0, slices = 0, rchunks = 0;
-  size_t off_hdr = 0, hdr_bytes = 0, off_pf[kClasses] = {}, off_idx[kClasses] = {}, off_ipf = 0, off_iidx = 0;
+  int64_t rowpart = 0, colpart = 0, usp = 0, slices = 0, rchunks = 0, pcol = 0, prchunks = 0, dsums = 0;
+  size_t off_hdr = 0, hdr_bytes = 0, off_pf[2][kClasses] = {}, off_idx[2][kClasses] = {}, off_ipf = 0, off_iidx = 0;
+  size_t off_ppf[kPanelCfgs] = {}, off_pidx[kPanelCfgs] = {};
   size_t off_rowpart = 0, off_colpart = 0, off_usp = 0, off_rchunk = 0, off_mean0 = 0, off_mean1 = 0, off_coef = 0;
+  size_t off_pcol = 0, off_pdpart = 0, off_prchunk = 0, off_dsum = 0;
   size_t bytes = 0;
 };
 
@@ -648,7 +758,9 @@ adaf_status make_plan(const came_tensor* tensors, const came_state* states, int3
   if (n > 0 && tensors == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: tensors is NULL");
   if (need_ptrs && n > 0 && states == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "came: states is NULL");
   P->dev.resize(n);
-  for (int c = 0; c < kClasses; ++c) P->pf[c].assign(1, 0);
+  for (int l = 0; l < 2; ++l)
+    for (int c = 0; c < kClasses; ++c) P->pf[l][c].assign(1, 0);
+  for (int q = 0; q < kPanelCfgs; ++q) P->ppf[q].assign(1, 0);
   P->item_pf.assign(1, 0);
   for (int32_t t = 0; t < n; ++t) {
     const came_tensor& x = tensors[t];
@@ -712,32 +824,59 @@ adaf_status make_plan(const came_tensor* tensors, const came_state* states, int3
       P->rchunks += d.B * d.nrc;
       P->item_idx.push_back(t);
       P->item_pf.push_back(P->item_pf.back() + d.B * (d.nrc + d.ncc));
+      // bf16 matrices of 2048 <= W <= 16384 on the vector path take the
+      // row-panel pass instead of passes a and b
+      if (d.cls == kVecBF && d.W >= 2048 && d.W <= 16384) {
+        d.panel = d.W <= 4096 ? 1 : 2;
+        d.pr = d.panel == 1 ? kP1Rows : kP2Rows;
+        d.prb = cdiv(d.H, d.pr);
+        d.pcol = P->pcol;
+        P->pcol += d.B * d.prb * d.W;
+        d.prc0 = P->prchunks;
+        P->prchunks += d.B * d.prb;
+        d.dsum0 = P->dsums;
+        P->dsums += d.B * d.ncc;
+        P->pidx[d.panel - 1].push_back(t);
+        P->ppf[d.panel - 1].push_back(P->ppf[d.panel - 1].back() + d.B * d.prb);
+      }
     } else {
       d.cls = k1D;
       ntiles = cdiv(numel, kUnit1D);
     }
     d.sp0 = P->usp;
-    d.nsp = ntiles;
-    P->usp += ntiles;
+    d.nsp = d.panel ? 0 : ntiles;  // panel tensors: sum(u^2) from the column items
+    P->usp += d.nsp;
     if (ntiles > 0) {
-      P->idx[d.cls].push_back(t);
-      P->pf[d.cls].push_back(P->pf[d.cls].back() + ntiles);
+      for (int l = 0; l < 2; ++l) {
+        if (l == kListAB && d.panel) continue;
+        P->idx[l][d.cls].push_back(t);
+        P->pf[l][d.cls].push_back(P->pf[l][d.cls].back() + ntiles);
+      }
     }
     P->dev[t] = d;
   }
   for (int c = 0; c < kClasses; ++c)
-    if (P->pf[c].back() > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, "came: more than 2^31 tiles");
+    if (P->pf[kListCD][c].back() > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, "came: more than 2^31 tiles");
   if (P->item_pf.back() > INT32_MAX) return fail(ADAF_ERR_UNSUPPORTED, "came: more than 2^31 statistics items");
   // layout: header (descriptors, class lists, items), then the scratch arrays
   size_t o = 0;
   P->off_hdr = o;
   o += sizeof(CDev) * n;
-  for (int c = 0; c < kClasses; ++c) {
+  for (int l = 0; l < 2; ++l) {
+    for (int c = 0; c < kClasses; ++c) {
+      o = round_up(o, 8);
+      P->off_pf[l][c] = o;
+      o += sizeof(int64_t) * P->pf[l][c].size();
+      P->off_idx[l][c] = o;
+      o += sizeof(int32_t) * P->idx[l][c].size();
+    }
+  }
+  for (int q = 0; q < kPanelCfgs; ++q) {
     o = round_up(o, 8);
-    P->off_pf[c] = o;
-    o += sizeof(int64_t) * P->pf[c].size();
-    P->off_idx[c] = o;
-    o += sizeof(int32_t) * P->idx[c].size();
+    P->off_ppf[q] = o;
+    o += sizeof(int64_t) * P->ppf[q].size();
+    P->off_pidx[q] = o;
+    o += sizeof(int32_t) * P->pidx[q].size();
   }
   o = round_up(o, 8);
   P->off_ipf = o;
@@ -753,6 +892,10 @@ adaf_status make_plan(const came_tensor* tensors, const came_state* states, int3
   P->off_mean0 = o;   o = round_up(o + sizeof(double) * P->slices, 256);
   P->off_mean1 = o;   o = round_up(o + sizeof(double) * P->slices, 256);
   P->off_coef = o;    o = round_up(o + sizeof(double) * n, 256);
+  P->off_pcol = o;    o = round_up(o + sizeof(float) * P->pcol, 256);
+  P->off_pdpart = o;  o = round_up(o + sizeof(float) * P->pcol, 256);
+  P->off_prchunk = o; o = round_up(o + sizeof(double) * P->prchunks, 256);
+  P->off_dsum = o;    o = round_up(o + sizeof(double) * P->dsums, 256);
   P->bytes = o;
   return ADAF_OK;
 }
@@ -787,9 +930,10 @@ struct DeviceState {
   std::vector<cudaEvent_t> free_events;
 };
 
-enum KernelSlot { kSA = 0, kSStats, kSMeans, kSB, kSClip, kSC, kSD, kNumKernels };
-const char* const kKernelNames[kNumKernels] = {"k_came_pass_a", "k_came_stats", "k_came_means", "k_came_pass_b",
-                                               "k_came_clip",   "k_came_pass_c", "k_came_pass_d"};
+enum KernelSlot { kSA = 0, kSStats, kSMeans, kSB, kSClip, kSC, kSD, kSPanel, kNumKernels };
+const char* const kKernelNames[kNumKernels] = {"k_came_pass_a", "k_came_stats",  "k_came_means",
+                                               "k_came_pass_b", "k_came_clip",   "k_came_pass_c",
+                                               "k_came_pass_d", "k_came_panel"};
 struct ProfRecord {
   int slot, device;
   cudaEvent_t start, stop;
@@ -819,6 +963,10 @@ cudaError_t set_smem_attrs() {
   if ((e = cudaFuncSetAttribute(k_came_pass_c<8, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(k_came_pass_c<8, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(k_came_pass_c<1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPassCSmem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_panel<kP1NW, kP1G, kP1S, kP1MinB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(panel_smem<kP1NW, kP1G, kP1S>()))) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_came_panel<kP2NW, kP2G, kP2S, kP2MinB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(panel_smem<kP2NW, kP2G, kP2S>()))) != cudaSuccess) return e;
   g_attr_done = true;
   return cudaSuccess;
 }
@@ -866,9 +1014,17 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
 
   std::vector<unsigned char> h(P.hdr_bytes);
   std::memcpy(h.data(), P.dev.data(), sizeof(CDev) * n);
-  for (int c = 0; c < kClasses; ++c) {
-    std::memcpy(h.data() + P.off_pf[c], P.pf[c].data(), sizeof(int64_t) * P.pf[c].size());
-    if (!P.idx[c].empty()) std::memcpy(h.data() + P.off_idx[c], P.idx[c].data(), sizeof(int32_t) * P.idx[c].size());
+  for (int l = 0; l < 2; ++l) {
+    for (int c = 0; c < kClasses; ++c) {
+      std::memcpy(h.data() + P.off_pf[l][c], P.pf[l][c].data(), sizeof(int64_t) * P.pf[l][c].size());
+      if (!P.idx[l][c].empty())
+        std::memcpy(h.data() + P.off_idx[l][c], P.idx[l][c].data(), sizeof(int32_t) * P.idx[l][c].size());
+    }
+  }
+  for (int q = 0; q < kPanelCfgs; ++q) {
+    std::memcpy(h.data() + P.off_ppf[q], P.ppf[q].data(), sizeof(int64_t) * P.ppf[q].size());
+    if (!P.pidx[q].empty())
+      std::memcpy(h.data() + P.off_pidx[q], P.pidx[q].data(), sizeof(int32_t) * P.pidx[q].size());
   }
   std::memcpy(h.data() + P.off_ipf, P.item_pf.data(), sizeof(int64_t) * P.item_pf.size());
   if (!P.item_idx.empty()) std::memcpy(h.data() + P.off_iidx, P.item_idx.data(), sizeof(int32_t) * P.item_idx.size());
@@ -876,11 +1032,22 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   CArgs a{};
   a.dev = reinterpret_cast<const CDev*>(ws + P.off_hdr);
-  for (int c = 0; c < kClasses; ++c) {
-    a.pf[c] = reinterpret_cast<const int64_t*>(ws + P.off_pf[c]);
-    a.idx[c] = reinterpret_cast<const int32_t*>(ws + P.off_idx[c]);
-    a.nmem[c] = static_cast<int32_t>(P.idx[c].size());
+  for (int l = 0; l < 2; ++l) {
+    for (int c = 0; c < kClasses; ++c) {
+      a.pf[l][c] = reinterpret_cast<const int64_t*>(ws + P.off_pf[l][c]);
+      a.idx[l][c] = reinterpret_cast<const int32_t*>(ws + P.off_idx[l][c]);
+      a.nmem[l][c] = static_cast<int32_t>(P.idx[l][c].size());
+    }
   }
+  for (int q = 0; q < kPanelCfgs; ++q) {
+    a.ppf[q] = reinterpret_cast<const int64_t*>(ws + P.off_ppf[q]);
+    a.pidx[q] = reinterpret_cast<const int32_t*>(ws + P.off_pidx[q]);
+    a.pnmem[q] = static_cast<int32_t>(P.pidx[q].size());
+  }
+  a.pcolpart = reinterpret_cast<float*>(ws + P.off_pcol);
+  a.pdpart = reinterpret_cast<float*>(ws + P.off_pdpart);
+  a.prchunk = reinterpret_cast<double*>(ws + P.off_prchunk);
+  a.dsum = reinterpret_cast<double*>(ws + P.off_dsum);
   a.item_pf = reinterpret_cast<const int64_t*>(ws + P.off_ipf);
   a.item_idx = reinterpret_cast<const int32_t*>(ws + P.off_iidx);
   a.nfact = static_cast<int32_t>(P.item_idx.size());
@@ -934,8 +1101,10 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
 
   const int persist = 2 * ds.sms;  // 2 CTAs of 256 threads per SM
   auto grid_for = [&](int64_t units) { return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(persist, units))); };
-  int64_t tiles[kClasses];
-  for (int c = 0; c < kClasses; ++c) tiles[c] = P.pf[c].back();
+  int64_t tiles[2][kClasses];
+  for (int l = 0; l < 2; ++l)
+    for (int c = 0; c < kClasses; ++c) tiles[l][c] = P.pf[l][c].back();
+  const int64_t chunks[kPanelCfgs] = {P.ppf[0].back(), P.ppf[1].back()};
   const int64_t items = P.item_pf.back();
 
   // launch helper: profiling events around each launch
@@ -961,30 +1130,47 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
     if (st_ != ADAF_OK) return st_; \
   } while (0)
 
-  // pass a (and the 1D second moment + sum(u^2))
-  CAME_TRY(launch(kSA, [&] {
-    if (tiles[kVecBF]) k_came_pass_a<8, 1><<<grid_for(tiles[kVecBF]), kThreads, kPassASmem, s>>>(a, kVecBF);
-    if (tiles[kVecF]) k_came_pass_a<8, 0><<<grid_for(tiles[kVecF]), kThreads, kPassASmem, s>>>(a, kVecF);
-    if (tiles[kScalar]) k_came_pass_a<1, 0><<<grid_for(tiles[kScalar]), kThreads, kPassASmem, s>>>(a, kScalar);
-    if (tiles[k1D]) k_came_pass_a<1, 0><<<grid_for(tiles[k1D]), kThreads, kPassASmem, s>>>(a, k1D);
-  }));
+  // row-panel pass of the bf16 matrices, pass a of the rest (and the 1D
+  // second moment + sum(u^2))
+  const int64_t* ta = tiles[kListAB];
+  if (chunks[0] || chunks[1]) {
+    CAME_TRY(launch(kSPanel, [&] {
+      if (chunks[0])
+        k_came_panel<kP1NW, kP1G, kP1S, kP1MinB><<<static_cast<int>(std::min<int64_t>(kP1MinB * ds.sms, chunks[0])),
+                                                   kP1NW * 32, panel_smem<kP1NW, kP1G, kP1S>(), s>>>(a, 0);
+      if (chunks[1])
+        k_came_panel<kP2NW, kP2G, kP2S, kP2MinB><<<static_cast<int>(std::min<int64_t>(kP2MinB * ds.sms, chunks[1])),
+                                                   kP2NW * 32, panel_smem<kP2NW, kP2G, kP2S>(), s>>>(a, 1);
+    }));
+  }
+  if (ta[kVecBF] || ta[kVecF] || ta[kScalar] || ta[k1D]) {
+    CAME_TRY(launch(kSA, [&] {
+      if (ta[kVecBF]) k_came_pass_a<8, 1><<<grid_for(ta[kVecBF]), kThreads, kPassASmem, s>>>(a, kVecBF);
+      if (ta[kVecF]) k_came_pass_a<8, 0><<<grid_for(ta[kVecF]), kThreads, kPassASmem, s>>>(a, kVecF);
+      if (ta[kScalar]) k_came_pass_a<1, 0><<<grid_for(ta[kScalar]), kThreads, kPassASmem, s>>>(a, kScalar);
+      if (ta[k1D]) k_came_pass_a<1, 0><<<grid_for(ta[k1D]), kThreads, kPassASmem, s>>>(a, k1D);
+    }));
+  }
   if (items) {
     a.phase = 0;
     a.mean = mean0;
     CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
     CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
-    CAME_TRY(launch(kSB, [&] {
-      if (tiles[kVecBF]) k_came_pass_b<8, 1><<<grid_for(tiles[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
-      if (tiles[kVecF]) k_came_pass_b<8, 0><<<grid_for(tiles[kVecF]), kThreads, 0, s>>>(a, kVecF);
-      if (tiles[kScalar]) k_came_pass_b<1, 0><<<grid_for(tiles[kScalar]), kThreads, 0, s>>>(a, kScalar);
-    }));
+    if (ta[kVecBF] || ta[kVecF] || ta[kScalar]) {
+      CAME_TRY(launch(kSB, [&] {
+        if (ta[kVecBF]) k_came_pass_b<8, 1><<<grid_for(ta[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
+        if (ta[kVecF]) k_came_pass_b<8, 0><<<grid_for(ta[kVecF]), kThreads, 0, s>>>(a, kVecF);
+        if (ta[kScalar]) k_came_pass_b<1, 0><<<grid_for(ta[kScalar]), kThreads, 0, s>>>(a, kScalar);
+      }));
+    }
   }
   CAME_TRY(launch(kSClip, [&] { k_came_clip<<<n, kThreads, 0, s>>>(a); }));
+  const int64_t* tc = tiles[kListCD];
   CAME_TRY(launch(kSC, [&] {
-    if (tiles[kVecBF]) k_came_pass_c<8, 1><<<grid_for(tiles[kVecBF]), kThreads, kPassCSmem, s>>>(a, kVecBF);
-    if (tiles[kVecF]) k_came_pass_c<8, 0><<<grid_for(tiles[kVecF]), kThreads, kPassCSmem, s>>>(a, kVecF);
-    if (tiles[kScalar]) k_came_pass_c<1, 0><<<grid_for(tiles[kScalar]), kThreads, kPassCSmem, s>>>(a, kScalar);
-    if (tiles[k1D]) k_came_pass_c<1, 0><<<grid_for(tiles[k1D]), kThreads, kPassCSmem, s>>>(a, k1D);
+    if (tc[kVecBF]) k_came_pass_c<8, 1><<<grid_for(tc[kVecBF]), kThreads, kPassCSmem, s>>>(a, kVecBF);
+    if (tc[kVecF]) k_came_pass_c<8, 0><<<grid_for(tc[kVecF]), kThreads, kPassCSmem, s>>>(a, kVecF);
+    if (tc[kScalar]) k_came_pass_c<1, 0><<<grid_for(tc[kScalar]), kThreads, kPassCSmem, s>>>(a, kScalar);
+    if (tc[k1D]) k_came_pass_c<1, 0><<<grid_for(tc[k1D]), kThreads, kPassCSmem, s>>>(a, k1D);
   }));
   if (items) {
     a.phase = 1;
@@ -992,9 +1178,9 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
     CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
     CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
     CAME_TRY(launch(kSD, [&] {
-      if (tiles[kVecBF]) k_came_pass_d<8><<<grid_for(tiles[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
-      if (tiles[kVecF]) k_came_pass_d<8><<<grid_for(tiles[kVecF]), kThreads, 0, s>>>(a, kVecF);
-      if (tiles[kScalar]) k_came_pass_d<1><<<grid_for(tiles[kScalar]), kThreads, 0, s>>>(a, kScalar);
+      if (tc[kVecBF]) k_came_pass_d<8><<<grid_for(tc[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
+      if (tc[kVecF]) k_came_pass_d<8><<<grid_for(tc[kVecF]), kThreads, 0, s>>>(a, kVecF);
+      if (tc[kScalar]) k_came_pass_d<1><<<grid_for(tc[kScalar]), kThreads, 0, s>>>(a, kScalar);
     }));
   }
 #undef CAME_TRY

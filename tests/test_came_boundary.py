@@ -97,4 +97,4 @@ def test_empty_list_is_a_no_op(lib):
 def test_kernel_names(lib):
     assert [B.came_kernel_name(k) for k in range(B.came_num_kernels())] == [
         "k_came_pass_a", "k_came_stats", "k_came_means", "k_came_pass_b", "k_came_clip", "k_came_pass_c",
-        "k_came_pass_d"]
+        "k_came_pass_d", "k_came_panel"]
