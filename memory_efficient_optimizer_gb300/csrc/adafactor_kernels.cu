@@ -115,13 +115,6 @@ __device__ __forceinline__ void widen(const Raw<__nv_bfloat16, 1>& r, float (&x)
 }
 __device__ __forceinline__ void widen(const Raw<float, 1>& r, float (&x)[1]) { x[0] = r.f; }
 
-// The same 8 values as 4 pairs, for the paired fp32 instructions (fma.rn.f32x2).
-__device__ __forceinline__ void widen2(const Raw<__nv_bfloat16, 8>& r, float2 (&x)[4]) {
-  const uint32_t w[4] = {r.u.x, r.u.y, r.u.z, r.u.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) x[k] = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xffff0000u));
-}
-
 __device__ __forceinline__ float load_g1(const void* g, int gdt, int64_t e) {
   if (gdt == kGradBF16) {
     const unsigned short h = __ldcs(static_cast<const unsigned short*>(g) + e);

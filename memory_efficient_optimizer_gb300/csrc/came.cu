@@ -405,8 +405,82 @@ __global__ void __launch_bounds__(NW * 32, MINB) k_came_panel(const __grid_const
 // phase 0: r, c from the g^2 partials (beta2, eps1); phase 1: R, C from the
 // U partials (beta3, eps2).  Items: B * nrc row chunks, then B * ncc column
 // chunks of each factored tensor.
+// Compensated (Kahan) fp32 addition: this GPU's FP64 rate is a small
+// fraction of its FP32 rate, and the partial sums below have up to a few
+// hundred terms.
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = x - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+}
+
+// Column sums of one column item: for the kColItem columns [j0, j0 + 256)
+// (j0 a multiple of 256, W % 8 == 0 when VEC), sums over nr partial rows
+// r of src[r * stride + j] (and of src2 with TWO), compensated fp32.  Warp w
+// adds the rows w, w + 8, ...; lane l the 8 consecutive columns 8 l .. 8 l + 7
+// (VEC) or the columns l + 32 m; then the 8 warp sums of each column are
+// added in warp order through shared memory (part: 2 x kWarps x kColItem
+// floats).  Thread t gets the sums of column j0 + t.  Deterministic: fixed
+// orders throughout.
+template <bool VEC, bool TWO>
+__device__ __forceinline__ void col_item_sums(const float* src, const float* src2, int64_t stride, int64_t nr,
+                                              int64_t j0, int64_t W, float* part, double& s1, double& s2) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float a1[8], c1[8], a2[8], c2[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v) a1[v] = c1[v] = a2[v] = c2[v] = 0.f;
+  auto col = [&](int v) -> int64_t { return VEC ? j0 + lane * 8 + v : j0 + lane + 32 * v; };
+  for (int64_t r = warp; r < nr; r += kWarps) {
+    const float* row1 = src + r * stride;
+    const float* row2 = TWO ? src2 + r * stride : nullptr;
+    if (VEC) {
+      if (col(0) < W) {
+        const float4 x0 = *reinterpret_cast<const float4*>(row1 + col(0));
+        const float4 x1 = *reinterpret_cast<const float4*>(row1 + col(0) + 4);
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int v = 0; v < 8; ++v) kahan_add(a1[v], c1[v], x[v]);
+        if (TWO) {
+          const float4 y0 = *reinterpret_cast<const float4*>(row2 + col(0));
+          const float4 y1 = *reinterpret_cast<const float4*>(row2 + col(0) + 4);
+          const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+          for (int v = 0; v < 8; ++v) kahan_add(a2[v], c2[v], y[v]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        if (col(v) < W) {
+          kahan_add(a1[v], c1[v], row1[col(v)]);
+          if (TWO) kahan_add(a2[v], c2[v], row2[col(v)]);
+        }
+      }
+    }
+  }
+  __syncthreads();  // part of the previous item is read
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const int cl = static_cast<int>(col(v) - j0);
+    part[warp * kColItem + cl] = a1[v];
+    if (TWO) part[(kWarps + warp) * kColItem + cl] = a2[v];
+  }
+  __syncthreads();
+  float t1 = 0.f, k1 = 0.f, t2 = 0.f, k2 = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    kahan_add(t1, k1, part[w * kColItem + threadIdx.x]);
+    if (TWO) kahan_add(t2, k2, part[(kWarps + w) * kColItem + threadIdx.x]);
+  }
+  s1 = t1;
+  s2 = t2;
+}
+
 __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__ CArgs a) {
   __shared__ double red[kWarps];
+  __shared__ float part[2 * kWarps * kColItem];
+  static_assert(kColItem == kThreads && kColItem == 32 * 8, "a column item is one column per thread");
   const float beta = a.phase ? a.b3 : a.b2;
   const float omb = a.phase ? a.omb3 : a.omb2;
   const double eps = a.phase ? a.eps2 : a.eps1;
@@ -439,14 +513,11 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
       const int64_t l2 = local - d.B * d.nrc;
       const int64_t b = l2 / d.ncc, q = l2 % d.ncc;
       const int64_t j = q * kColItem + threadIdx.x;
+      const int64_t o = d.pcol + b * d.prb * d.W;  // panel tensors: W % 8 == 0
+      double sc, sd;
+      col_item_sums<true, true>(a.pcolpart + o, a.pdpart + o, d.W, d.prb, q * kColItem, d.W, part, sc, sd);
       double term = 0.0;
       if (j < d.W) {
-        const int64_t o = d.pcol + b * d.prb * d.W + j;
-        double sc = 0.0, sd = 0.0;
-        for (int64_t r = 0; r < d.prb; ++r) {
-          sc += a.pcolpart[o + r * d.W];
-          sd += a.pdpart[o + r * d.W];
-        }
         const float mean = static_cast<float>(sc / static_cast<double>(d.H) + eps);
         const float cn = fmaf(beta, colst[b * d.W + j], omb * mean);
         colst[b * d.W + j] = cn;
@@ -458,9 +529,12 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
       const int64_t l2 = local - d.B * d.nrc;
       const int64_t b = l2 / d.ncc, q = l2 % d.ncc;
       const int64_t j = q * kColItem + threadIdx.x;
+      const float* src = a.colpart + d.colpart + b * d.W;
+      const bool vec = d.W % 8 == 0 && (d.colpart + b * d.W) % 4 == 0 && (d.B * d.W) % 4 == 0;
+      double s, unused;
+      if (vec) col_item_sums<true, false>(src, nullptr, d.B * d.W, d.rb, q * kColItem, d.W, part, s, unused);
+      else col_item_sums<false, false>(src, nullptr, d.B * d.W, d.rb, q * kColItem, d.W, part, s, unused);
       if (j < d.W) {
-        double s = 0.0;
-        for (int64_t r = 0; r < d.rb; ++r) s += a.colpart[d.colpart + r * (d.B * d.W) + b * d.W + j];
         const float mean = static_cast<float>(s / static_cast<double>(d.H) + eps);
         colst[b * d.W + j] = fmaf(beta, colst[b * d.W + j], omb * mean);
       }
