@@ -166,10 +166,13 @@ adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size
 /* One Adafactor step over tensors[0..n) with states[0..n), step t = `step`
  * (>= 1), enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  * stream).  The call only enqueues work and reads no device memory from the
- * host.  The per-call descriptor table is uploaded from a ring of 4 pinned
- * host buffers per device: a call waits on the host only when the upload of
- * the call 4 calls earlier (on any stream of the device) has not yet run,
- * i.e. when more than 4 steps are queued ahead of the GPU.  Params and states
+ * host.  The per-call descriptor table is staged in a ring of 4 pinned host
+ * buffers per device and read from there by a small kernel on `stream` (no
+ * copy engine: host-to-device copies queued on other streams, such as the
+ * next step's gradients, do not hold the step back); a call waits on the host
+ * only when the upload of the call 4 calls earlier (on any stream of the
+ * device) has not yet run, i.e. when more than 4 steps are queued ahead of
+ * the GPU.  Params and states
  * are updated in place; grads are read only.  The workspace (>= the size
  * reported by adafactor_workspace_size, 256-byte aligned) is scratch owned by
  * this call until the enqueued work completes: calls that may run

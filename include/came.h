@@ -91,7 +91,10 @@ adaf_status came_workspace_size(const came_tensor* tensors, int32_t n, size_t* b
 adaf_status came_step(const came_tensor* tensors, const came_state* states, int32_t n, int64_t step,
                       const came_hparams* hp, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Per-kernel timing with CUDA events (as for the Adafactor step). */
+/* Per-kernel timing with CUDA events (as for the Adafactor step): a slot is
+ * one kernel kind; its time covers the launches of that kind in a call (one
+ * per tensor class that has members), and launches[k] counts those kernel
+ * launches. */
 adaf_status came_profile_enable(int32_t on);
 adaf_status came_profile_read(double* ms, int64_t* launches, int32_t nk);
 int32_t came_num_kernels(void);

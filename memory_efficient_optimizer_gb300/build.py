@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmeo_adafactor.so")
 SOURCES = ["adafactor_kernels.cu", "adafactor_api.cpp", "adafactor_noalloc.cu", "lamb.cu", "came.cu"]
-HEADERS = [os.path.join(CSRC, "adafactor_internal.h"), os.path.join(CSRC, "row_panel.cuh"), os.path.join(INCLUDE, "adafactor.h"),
+HEADERS = [os.path.join(CSRC, "adafactor_internal.h"), os.path.join(CSRC, "row_panel.cuh"), os.path.join(CSRC, "host_copy.cuh"), os.path.join(INCLUDE, "adafactor.h"),
            os.path.join(INCLUDE, "lamb.h"), os.path.join(INCLUDE, "came.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

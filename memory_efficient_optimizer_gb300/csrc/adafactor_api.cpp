@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "adafactor_internal.h"
+#include "host_copy.cuh"
 
 namespace {
 
@@ -352,9 +353,10 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
 }
 
 // ---- pinned staging of the descriptor table -------------------------------
-// A small ring of pinned host buffers per device; a slot is reused only after
-// the event recorded behind its previous copy has completed, so the host never
-// overwrites bytes a pending cudaMemcpyAsync still has to read.
+// A small ring of pinned, device-mapped host buffers per device, read by the
+// upload kernel (host_copy.cuh); a slot is reused only after the event
+// recorded behind its previous upload has completed, so the host never
+// overwrites bytes a pending upload still has to read.
 constexpr int kSlots = 4;
 struct Slot {
   void* host = nullptr;
@@ -518,7 +520,7 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
       slot.host = nullptr;
       slot.cap = 0;
       const size_t cap = align_up(plan.header_bytes, size_t(1) << 16);
-      e = cudaHostAlloc(&slot.host, cap, cudaHostAllocPortable);
+      e = cudaHostAlloc(&slot.host, cap, cudaHostAllocPortable | cudaHostAllocMapped);
       if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc (staging)");
       slot.cap = cap;
     }
@@ -527,8 +529,8 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
       if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate (staging)");
     }
     fill_header(static_cast<unsigned char*>(slot.host), plan);
-    e = cudaMemcpyAsync(ws, slot.host, plan.header_bytes, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (descriptor table)");
+    e = copy_from_host(ws, slot.host, plan.header_bytes, s);  // no copy engine (host_copy.cuh)
+    if (e != cudaSuccess) return cuda_fail(e, "descriptor table upload");
     e = cudaEventRecord(slot.done, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");
     slot.pending = true;

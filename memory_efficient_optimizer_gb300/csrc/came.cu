@@ -49,6 +49,7 @@
 #include <vector>
 
 #include "adafactor_internal.h"
+#include "host_copy.cuh"
 #include "came.h"
 #include "row_panel.cuh"
 
@@ -1011,6 +1012,7 @@ const char* const kKernelNames[kNumKernels] = {"k_came_pass_a", "k_came_stats", 
 struct ProfRecord {
   int slot, device;
   cudaEvent_t start, stop;
+  int count;  // kernels launched between the two events
 };
 
 std::mutex g_mu;
@@ -1158,18 +1160,21 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
   ds.next = (ds.next + 1) % kRing;
   if (sl.used && (err = cudaEventSynchronize(sl.done)) != cudaSuccess)
     return cuda_fail(err, "cudaEventSynchronize (upload ring)");
-  if (sl.cap < P.hdr_bytes) {
+  const size_t up = round_up(P.hdr_bytes, 16);  // the upload moves whole 16-byte words
+  if (sl.cap < up) {
     if (sl.host) cudaFreeHost(sl.host);
     sl.host = nullptr;
     sl.cap = 0;
-    if ((err = cudaMallocHost(&sl.host, P.hdr_bytes)) != cudaSuccess) return cuda_fail(err, "cudaMallocHost");
-    sl.cap = P.hdr_bytes;
+    if ((err = cudaHostAlloc(&sl.host, up, cudaHostAllocPortable | cudaHostAllocMapped)) != cudaSuccess)
+      return cuda_fail(err, "cudaHostAlloc");
+    sl.cap = up;
   }
   if (sl.done == nullptr && (err = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess)
     return cuda_fail(err, "cudaEventCreate");
   std::memcpy(sl.host, h.data(), P.hdr_bytes);
-  if ((err = cudaMemcpyAsync(ws + P.off_hdr, sl.host, P.hdr_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-    return cuda_fail(err, "cudaMemcpyAsync (descriptors)");
+  // a kernel reads the table from host memory: no copy engine (host_copy.cuh)
+  if ((err = meo::copy_from_host(ws + P.off_hdr, sl.host, up, s)) != cudaSuccess)
+    return cuda_fail(err, "descriptor table upload");
   if ((err = cudaEventRecord(sl.done, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
   sl.used = true;
 
@@ -1182,15 +1187,18 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
   const int64_t items = P.item_pf.back();
 
   // launch helper: profiling events around each launch
+  int nk = 0;  // kernels launched so far by this call (a slot may launch one per class)
   auto launch = [&](int slot, auto&& fn) -> adaf_status {
-    ProfRecord rec{slot, device, nullptr, nullptr};
+    ProfRecord rec{slot, device, nullptr, nullptr, 0};
     cudaError_t e;
     if (g_profile) {
       if ((e = get_event(ds, &rec.start)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate (profile)");
       if ((e = get_event(ds, &rec.stop)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate (profile)");
       if ((e = cudaEventRecord(rec.start, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord (profile)");
     }
+    const int before = nk;
     fn();
+    rec.count = nk - before;
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, kKernelNames[slot]);
     if (g_profile) {
       if ((e = cudaEventRecord(rec.stop, s)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord (profile)");
@@ -1209,52 +1217,56 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
   const int64_t* ta = tiles[kListAB];
   if (chunks[0] || chunks[1]) {
     CAME_TRY(launch(kSPanel, [&] {
-      if (chunks[0])
+      if (chunks[0]) {
         k_came_panel<kP1NW, kP1G, kP1S, kP1MinB><<<static_cast<int>(std::min<int64_t>(kP1MinB * ds.sms, chunks[0])),
                                                    kP1NW * 32, panel_smem<kP1NW, kP1G, kP1S>(), s>>>(a, 0);
-      if (chunks[1])
+        ++nk;
+      }
+      if (chunks[1]) {
         k_came_panel<kP2NW, kP2G, kP2S, kP2MinB><<<static_cast<int>(std::min<int64_t>(kP2MinB * ds.sms, chunks[1])),
                                                    kP2NW * 32, panel_smem<kP2NW, kP2G, kP2S>(), s>>>(a, 1);
+        ++nk;
+      }
     }));
   }
   if (ta[kVecBF] || ta[kVecF] || ta[kScalar] || ta[k1D]) {
     CAME_TRY(launch(kSA, [&] {
-      if (ta[kVecBF]) k_came_pass_a<8, 1><<<grid_for(ta[kVecBF]), kThreads, kPassASmem, s>>>(a, kVecBF);
-      if (ta[kVecF]) k_came_pass_a<8, 0><<<grid_for(ta[kVecF]), kThreads, kPassASmem, s>>>(a, kVecF);
-      if (ta[kScalar]) k_came_pass_a<1, 0><<<grid_for(ta[kScalar]), kThreads, kPassASmem, s>>>(a, kScalar);
-      if (ta[k1D]) k_came_pass_a<1, 0><<<grid_for(ta[k1D]), kThreads, kPassASmem, s>>>(a, k1D);
+      if (ta[kVecBF]) { k_came_pass_a<8, 1><<<grid_for(ta[kVecBF]), kThreads, kPassASmem, s>>>(a, kVecBF); ++nk; }
+      if (ta[kVecF]) { k_came_pass_a<8, 0><<<grid_for(ta[kVecF]), kThreads, kPassASmem, s>>>(a, kVecF); ++nk; }
+      if (ta[kScalar]) { k_came_pass_a<1, 0><<<grid_for(ta[kScalar]), kThreads, kPassASmem, s>>>(a, kScalar); ++nk; }
+      if (ta[k1D]) { k_came_pass_a<1, 0><<<grid_for(ta[k1D]), kThreads, kPassASmem, s>>>(a, k1D); ++nk; }
     }));
   }
   if (items) {
     a.phase = 0;
     a.mean = mean0;
-    CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
-    CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
+    CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); ++nk; }));
+    CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); ++nk; }));
     if (ta[kVecBF] || ta[kVecF] || ta[kScalar]) {
       CAME_TRY(launch(kSB, [&] {
-        if (ta[kVecBF]) k_came_pass_b<8, 1><<<grid_for(ta[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
-        if (ta[kVecF]) k_came_pass_b<8, 0><<<grid_for(ta[kVecF]), kThreads, 0, s>>>(a, kVecF);
-        if (ta[kScalar]) k_came_pass_b<1, 0><<<grid_for(ta[kScalar]), kThreads, 0, s>>>(a, kScalar);
+        if (ta[kVecBF]) { k_came_pass_b<8, 1><<<grid_for(ta[kVecBF]), kThreads, 0, s>>>(a, kVecBF); ++nk; }
+        if (ta[kVecF]) { k_came_pass_b<8, 0><<<grid_for(ta[kVecF]), kThreads, 0, s>>>(a, kVecF); ++nk; }
+        if (ta[kScalar]) { k_came_pass_b<1, 0><<<grid_for(ta[kScalar]), kThreads, 0, s>>>(a, kScalar); ++nk; }
       }));
     }
   }
-  CAME_TRY(launch(kSClip, [&] { k_came_clip<<<n, kThreads, 0, s>>>(a); }));
+  CAME_TRY(launch(kSClip, [&] { k_came_clip<<<n, kThreads, 0, s>>>(a); ++nk; }));
   const int64_t* tc = tiles[kListCD];
   CAME_TRY(launch(kSC, [&] {
-    if (tc[kVecBF]) k_came_pass_c<8, 1><<<grid_for(tc[kVecBF]), kThreads, kPassCSmem, s>>>(a, kVecBF);
-    if (tc[kVecF]) k_came_pass_c<8, 0><<<grid_for(tc[kVecF]), kThreads, kPassCSmem, s>>>(a, kVecF);
-    if (tc[kScalar]) k_came_pass_c<1, 0><<<grid_for(tc[kScalar]), kThreads, kPassCSmem, s>>>(a, kScalar);
-    if (tc[k1D]) k_came_pass_c<1, 0><<<grid_for(tc[k1D]), kThreads, kPassCSmem, s>>>(a, k1D);
+    if (tc[kVecBF]) { k_came_pass_c<8, 1><<<grid_for(tc[kVecBF]), kThreads, kPassCSmem, s>>>(a, kVecBF); ++nk; }
+    if (tc[kVecF]) { k_came_pass_c<8, 0><<<grid_for(tc[kVecF]), kThreads, kPassCSmem, s>>>(a, kVecF); ++nk; }
+    if (tc[kScalar]) { k_came_pass_c<1, 0><<<grid_for(tc[kScalar]), kThreads, kPassCSmem, s>>>(a, kScalar); ++nk; }
+    if (tc[k1D]) { k_came_pass_c<1, 0><<<grid_for(tc[k1D]), kThreads, kPassCSmem, s>>>(a, k1D); ++nk; }
   }));
   if (items) {
     a.phase = 1;
     a.mean = mean1;
-    CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); }));
-    CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); }));
+    CAME_TRY(launch(kSStats, [&] { k_came_stats<<<grid_for(items), kThreads, 0, s>>>(a); ++nk; }));
+    CAME_TRY(launch(kSMeans, [&] { k_came_means<<<a.nfact, kThreads, 0, s>>>(a); ++nk; }));
     CAME_TRY(launch(kSD, [&] {
-      if (tc[kVecBF]) k_came_pass_d<8><<<grid_for(tc[kVecBF]), kThreads, 0, s>>>(a, kVecBF);
-      if (tc[kVecF]) k_came_pass_d<8><<<grid_for(tc[kVecF]), kThreads, 0, s>>>(a, kVecF);
-      if (tc[kScalar]) k_came_pass_d<1><<<grid_for(tc[kScalar]), kThreads, 0, s>>>(a, kScalar);
+      if (tc[kVecBF]) { k_came_pass_d<8><<<grid_for(tc[kVecBF]), kThreads, 0, s>>>(a, kVecBF); ++nk; }
+      if (tc[kVecF]) { k_came_pass_d<8><<<grid_for(tc[kVecF]), kThreads, 0, s>>>(a, kVecF); ++nk; }
+      if (tc[kScalar]) { k_came_pass_d<1><<<grid_for(tc[kScalar]), kThreads, 0, s>>>(a, kScalar); ++nk; }
     }));
   }
 #undef CAME_TRY
@@ -1277,7 +1289,7 @@ adaf_status came_profile_read(double* ms, int64_t* launches, int32_t nk) {
     if (e != cudaSuccess && st == ADAF_OK) st = cuda_fail(e, "profile event");
     if (r.slot < nk) {
       if (ms) ms[r.slot] += el;
-      if (launches) launches[r.slot] += 1;
+      if (launches) launches[r.slot] += r.count;
     }
     DeviceState& ds = g_dev[r.device];
     ds.free_events.push_back(r.start);

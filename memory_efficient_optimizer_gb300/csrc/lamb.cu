@@ -35,6 +35,7 @@
 #include <vector>
 
 #include "adafactor_internal.h"
+#include "host_copy.cuh"
 #include "lamb.h"
 
 namespace {
@@ -518,18 +519,21 @@ adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const
   if (sl.used) {
     if ((err = cudaEventSynchronize(sl.done)) != cudaSuccess) return cuda_fail(err, "cudaEventSynchronize (upload ring)");
   }
-  if (sl.cap < hdr) {
+  const size_t up = round_up(hdr, 16);  // the upload moves whole 16-byte words
+  if (sl.cap < up) {
     if (sl.host) cudaFreeHost(sl.host);
     sl.host = nullptr;
     sl.cap = 0;
-    if ((err = cudaMallocHost(&sl.host, hdr)) != cudaSuccess) return cuda_fail(err, "cudaMallocHost");
-    sl.cap = hdr;
+    if ((err = cudaHostAlloc(&sl.host, up, cudaHostAllocPortable | cudaHostAllocMapped)) != cudaSuccess)
+      return cuda_fail(err, "cudaHostAlloc");
+    sl.cap = up;
   }
   if (sl.done == nullptr && (err = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess)
     return cuda_fail(err, "cudaEventCreate");
   std::memcpy(sl.host, h.data(), hdr);
-  if ((err = cudaMemcpyAsync(ws + L.off_dev, sl.host, hdr, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-    return cuda_fail(err, "cudaMemcpyAsync (descriptors)");
+  // a kernel reads the table from host memory: no copy engine (host_copy.cuh)
+  if ((err = meo::copy_from_host(ws + L.off_dev, sl.host, up, s)) != cudaSuccess)
+    return cuda_fail(err, "descriptor table upload");
   if ((err = cudaEventRecord(sl.done, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
   sl.used = true;
 
