@@ -307,26 +307,37 @@ def traffic_record(kernel):
 
 
 # ---------------------------------------------------------------- our arm --
-def plain_h2d_rate(host_bufs, dev_bufs, dev, world, reps=2):
+def flat_views(like, device, pin=False):
+    """One contiguous buffer holding a tensor of each shape/dtype of `like`
+    (offsets rounded up to 256 bytes) and the views into it."""
+    offs, total = [], 0
+    for x in like:
+        offs.append(total)
+        total += (x.numel() * x.element_size() + 255) // 256 * 256
+    buf = torch.empty(max(total, 1), dtype=torch.uint8, device=device, pin_memory=pin)
+    views = [buf[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape) for o, x in zip(offs, like)]
+    return buf, views
+
+
+def plain_h2d_rate(host_flat, dev_flat, dev, world, reps=2):
     """The box's plain host->device copy rate for the same bytes as one e2e
-    step: one cudaMemcpyAsync per tensor (torch copy_ from pinned memory),
-    single stream, nothing else running; best of `reps`, CUDA events."""
-    nbytes = sum(b.numel() * b.element_size() for b in host_bufs)
+    step: one cudaMemcpyAsync of the flat pinned gradient buffer, nothing else
+    running; best of `reps`, CUDA events."""
+    nbytes = host_flat.numel()
     s = torch.cuda.current_stream(dev)
     best = None
     for _ in range(reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(s)
-        for hb, db in zip(host_bufs, dev_bufs):
-            db.copy_(hb, non_blocking=True)
+        dev_flat.copy_(host_flat, non_blocking=True)
         e1.record(s)
         torch.cuda.synchronize(dev)
         ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         best = ms if best is None else min(best, ms)
     return {"h2d_gbs": nbytes / (best / 1e3) / 1e9, "bytes": nbytes, "ms": best,
-            "how": "one cudaMemcpyAsync per tensor from pinned host memory, one stream, best of "
-                   f"{reps}; frac_of_link = this copy time / the e2e step time"}
+            "how": "one cudaMemcpyAsync of the flat pinned gradient buffer, one stream, nothing else running, best "
+                   f"of {reps}; frac_of_link = this copy time / the e2e step time"}
 
 
 HOST_NUMA = None
@@ -387,6 +398,64 @@ class numa_local:
         return False
 
 
+class E2EUploads:
+    """Double-buffered gradient uploads of an end-to-end run.  The step's
+    gradients live in one flat pinned host buffer (as a training loop's flat
+    gradient buffer would), and each step copies it with one cudaMemcpyAsync
+    into one of two flat device buffers, on its own stream, while the
+    previous step runs.  (291 separate pinned buffers, one copy each, measured
+    erratic on the GB300 host: 77 to 294 ms for the same 16 GB, against a
+    steady 76 ms for one flat buffer.)"""
+
+    def __init__(self, grads, dev):
+        self.host, hviews = flat_views(grads, "cpu", pin=True)
+        for hv, g in zip(hviews, grads):
+            hv.copy_(g)
+        self.dev_flat, self.views = [], []
+        for _ in range(2):
+            buf, views = flat_views(grads, dev)
+            self.dev_flat.append(buf)
+            self.views.append(views)
+        self.nbytes = sum(g.numel() * g.element_size() for g in grads)
+        self.s_in = torch.cuda.Stream(dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_step = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+
+    def upload(self, k):
+        b = k % 2
+        if self.used[b]:
+            self.s_in.wait_event(self.ev_step[b])  # the step that last read this buffer is done
+        with torch.cuda.stream(self.s_in):
+            self.dev_flat[b].copy_(self.host, non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+
+    def before_step(self, k, s_comp):
+        s_comp.wait_event(self.ev_in[k % 2])
+
+    def after_step(self, k, s_comp):
+        self.used[k % 2] = True
+        self.ev_step[k % 2].record(s_comp)
+
+    def timed(self, nsteps, compute, s_comp, world, dev):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        e0.record(s_comp)
+        self.s_in.wait_event(e0)
+        self.upload(0)
+        for k in range(nsteps):
+            if k + 1 < nsteps:
+                self.upload(k + 1)
+            self.before_step(k, s_comp)
+            compute(k)
+            self.after_step(k, s_comp)
+        e1.record(s_comp)
+        torch.cuda.synchronize(dev)
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / nsteps
+
+
 def run_e2e(args, wl, params, grads, states, step, t, world, dev):
     """End to end through AdafactorStep, as a training loop with host-resident
     gradients would drive it: every step copies that step's bf16 grads from
@@ -394,100 +463,52 @@ def run_e2e(args, wl, params, grads, states, step, t, world, dev):
     metric, the per-tensor sum(p^2) of the updated parameters (one float64
     per tensor, from which the host forms the parameter norm).  Grads for
     step t+1 go up on their own stream, into the second of two device grad
-    buffers, while step t runs.
+    buffers, while step t runs (E2EUploads).
 
     A second, shorter measurement (`param_readback`) also copies every updated
-    fp32 parameter back to pinned host memory each step, for callers that keep
-    the master weights on the host."""
+    fp32 parameter back to pinned host memory each step (one flat pinned
+    buffer), for callers that keep the master weights on the host."""
     n = len(params)
     psq = torch.zeros(n, dtype=torch.float64, device=dev)
     for k, st in enumerate(states):
         st["param_sq_sum"] = psq[k:k + 1]
-    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
-    for hg, g in zip(host_g, grads):
-        hg.copy_(g)
+    up = E2EUploads(grads, dev)
     host_m = torch.empty(n, dtype=torch.float64, pin_memory=True)
-    grads2 = [torch.empty_like(g) for g in grads]
-    steps = [AdafactorStep(params, grads, states, **wl.hparams), AdafactorStep(params, grads2, states, **wl.hparams)]
-    bufs = [grads, grads2]
-    # The uploads are split over a few copy streams (tensors dealt out by size),
-    # so that several copy engines work on the host->device traffic at once.
-    ns = max(1, int(args.e2e_streams))
-    s_in = [torch.cuda.Stream(dev) for _ in range(ns)]
-    lanes = [[] for _ in range(ns)]
-    load = [0] * ns
-    for k in sorted(range(n), key=lambda k: -grads[k].numel()):
-        q = load.index(min(load))
-        lanes[q].append(k)
-        load[q] += grads[k].numel()
+    steps = [AdafactorStep(params, up.views[b], states, **wl.hparams) for b in range(2)]
     s_comp = torch.cuda.current_stream(dev)
-    ev_in = [[torch.cuda.Event() for _ in range(ns)] for _ in range(2)]
-    ev_step = [torch.cuda.Event() for _ in range(2)]
-    h2d = sum(g.numel() * g.element_size() for g in grads)
-    used = [False, False]
+    readback = None
 
-    def upload(k):
-        b = k % 2
-        for q, sq in enumerate(s_in):
-            if used[b]:
-                sq.wait_event(ev_step[b])  # the step that last read this buffer is done
-            with torch.cuda.stream(sq):
-                for j in lanes[q]:
-                    bufs[b][j].copy_(host_g[j], non_blocking=True)
-                ev_in[b][q].record(sq)
-
-    def compute(k, readback=None):
+    def compute(k):
         nonlocal t
-        b = k % 2
-        for ev in ev_in[b]:
-            s_comp.wait_event(ev)
         t += 1
-        steps[b](t, stream=s_comp)
-        used[b] = True
+        steps[k % 2](t, stream=s_comp)
         host_m.copy_(psq, non_blocking=True)
         if readback is not None:
             for hp_, p in zip(readback, params):
                 hp_.copy_(p, non_blocking=True)
-        ev_step[b].record(s_comp)
 
-    def run(nsteps, readback=None):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            torch.distributed.barrier()
-        e0.record(s_comp)
-        for sq in s_in:
-            sq.wait_event(e0)
-        upload(0)
-        for k in range(nsteps):
-            if k + 1 < nsteps:
-                upload(k + 1)
-            compute(k, readback)
-        e1.record(s_comp)
-        torch.cuda.synchronize(dev)
-        return max_over_ranks(e0.elapsed_time(e1), world, dev) / nsteps
-
-    run(2)  # warm-up: both step objects marshalled, carry primed
-    ms = run(args.e2e_steps)
+    up.timed(2, compute, s_comp, world, dev)  # warm-up: both step objects marshalled, carry primed
+    ms = up.timed(args.e2e_steps, compute, s_comp, world, dev)
     norm = float(host_m.sum().sqrt())
-    link = plain_h2d_rate(host_g, grads, dev, world)
+    link = plain_h2d_rate(up.host, up.dev_flat[0], dev, world)
     out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": n * 8, "steps": args.e2e_steps, "ms_per_step": ms,
+           "h2d_bytes_per_step": up.nbytes, "d2h_bytes_per_step": n * 8, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"per-tensor sum(p^2) of the updated params ({n} float64; param norm {norm:.4f})",
-           "path": f"pinned host bf16 grads -> device (double-buffered, {ns} copy streams, overlapping the "
-                   "previous step), AdafactorStep, device->host read of the step metric",
+           "path": "one flat pinned host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
+                   "overlapping the previous step), AdafactorStep, device->host read of the step metric",
            "link": link, "host_numa": HOST_NUMA,
            "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
     if args.readback_steps > 0:
-        host_p = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in params]
-        rms = run(args.readback_steps, readback=host_p)
+        host_pflat, readback = flat_views(params, "cpu", pin=True)
+        rms = up.timed(args.readback_steps, compute, s_comp, world, dev)
         out["param_readback"] = {"ms_per_step": rms, "value": replica_throughput(wl.numel, world, rms),
                                  "d2h_bytes_per_step": sum(p.numel() * p.element_size() for p in params),
                                  "steps": args.readback_steps}
-        del host_p
+        readback = None
+        del host_pflat
     for st in states:
         st.pop("param_sq_sum", None)
-    del host_g, grads2
+    del up
     return out, t
 
 
@@ -653,68 +674,33 @@ def lamb_bytes(n_values, grad_bytes):
 
 def run_lamb_e2e(args, wl, params, grads, step, t, world, dev):
     """End to end through LambStep: every step copies that step's bf16 grads
-    from pinned host memory (one stream, overlapping the previous step into a
-    second grad buffer), runs the step, and reads back the per-tensor trust
-    ratios (one float64 per tensor) to pinned host memory."""
+    from pinned host memory (E2EUploads: one flat buffer, one copy, own
+    stream, overlapping the previous step into a second grad buffer), runs
+    the step, and reads back the per-tensor trust ratios (one float64 per
+    tensor) to pinned host memory."""
     n = len(params)
-    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
-    for hg, g in zip(host_g, grads):
-        hg.copy_(g)
-    grads2 = [torch.empty_like(g) for g in grads]
-    steps = [step, LambStep(params, grads2, step.states, **step.hparams)]
-    bufs = [grads, grads2]
+    up = E2EUploads(grads, dev)
+    steps = [LambStep(params, up.views[b], step.states, **step.hparams) for b in range(2)]
     host_tr = torch.empty(n, dtype=torch.float64, pin_memory=True)
-    s_in = torch.cuda.Stream(dev)
     s_comp = torch.cuda.current_stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_step = [torch.cuda.Event() for _ in range(2)]
-    used = [False, False]
-    h2d = sum(g.numel() * g.element_size() for g in grads)
-
-    def upload(k):
-        b = k % 2
-        if used[b]:
-            s_in.wait_event(ev_step[b])
-        with torch.cuda.stream(s_in):
-            for j in range(n):
-                bufs[b][j].copy_(host_g[j], non_blocking=True)
-            ev_in[b].record(s_in)
 
     def compute(k):
         nonlocal t
-        b = k % 2
-        s_comp.wait_event(ev_in[b])
         t += 1
-        steps[b](t, stream=s_comp)
-        used[b] = True
-        trust = steps[b].workspace[:8 * n].view(torch.float64)
+        steps[k % 2](t, stream=s_comp)
+        trust = steps[k % 2].workspace[:8 * n].view(torch.float64)
         host_tr.copy_(trust, non_blocking=True)
-        ev_step[b].record(s_comp)
 
-    def run(nsteps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(s_comp)
-        s_in.wait_event(e0)
-        upload(0)
-        for k in range(nsteps):
-            if k + 1 < nsteps:
-                upload(k + 1)
-            compute(k)
-        e1.record(s_comp)
-        torch.cuda.synchronize(dev)
-        return max_over_ranks(e0.elapsed_time(e1), world, dev) / nsteps
-
-    run(2)
-    ms = run(args.e2e_steps)
-    link = plain_h2d_rate(host_g, grads, dev, world)
-    out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": h2d,
+    up.timed(2, compute, s_comp, world, dev)
+    ms = up.timed(args.e2e_steps, compute, s_comp, world, dev)
+    link = plain_h2d_rate(up.host, up.dev_flat[0], dev, world)
+    out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": up.nbytes,
            "d2h_bytes_per_step": n * 8, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"per-tensor trust ratios ({n} float64; mean {float(host_tr.mean()):.4f})",
-           "path": "pinned host bf16 grads -> device (double-buffered, 1 copy stream, overlapping the previous "
-                   "step), LambStep, device->host read of the trust ratios",
+           "path": "one flat pinned host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
+                   "overlapping the previous step), LambStep, device->host read of the trust ratios",
            "link": link, "host_numa": HOST_NUMA, "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
-    del host_g, grads2
+    del up
     return out, t
 
 
@@ -908,70 +894,35 @@ def run_came(args, world, rank, local):
 
 def run_came_e2e(args, wl, params, grads, states, step, t, world, dev):
     """End to end through CameStep: every step copies the step's bf16 grads
-    from pinned host memory (one stream, into the second of two grad buffers
-    while the previous step runs), runs the step, and reads back one value
-    per tensor (the first updated parameter value) to pinned host memory."""
+    from pinned host memory (E2EUploads: one flat buffer, one copy, own
+    stream, into the second of two grad buffers while the previous step
+    runs), runs the step, and reads back one value per tensor (the first
+    updated parameter value) to pinned host memory."""
     n = len(params)
-    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
-    for hg, g in zip(host_g, grads):
-        hg.copy_(g)
-    grads2 = [torch.empty_like(g) for g in grads]
-    steps = [step, CameStep(params, grads2, states, **wl.hparams)]
-    bufs = [grads, grads2]
+    up = E2EUploads(grads, dev)
+    steps = [CameStep(params, up.views[b], states, **wl.hparams) for b in range(2)]
     heads = torch.empty(n, dtype=torch.float32, device=dev)
     host_h = torch.empty(n, dtype=torch.float32, pin_memory=True)
-    s_in = torch.cuda.Stream(dev)
     s_comp = torch.cuda.current_stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_step = [torch.cuda.Event() for _ in range(2)]
-    used = [False, False]
-    h2d = sum(g.numel() * g.element_size() for g in grads)
     firsts = [p.view(-1)[:1] for p in params]
-
-    def upload(k):
-        b = k % 2
-        if used[b]:
-            s_in.wait_event(ev_step[b])
-        with torch.cuda.stream(s_in):
-            for j in range(n):
-                bufs[b][j].copy_(host_g[j], non_blocking=True)
-            ev_in[b].record(s_in)
 
     def compute(k):
         nonlocal t
-        b = k % 2
-        s_comp.wait_event(ev_in[b])
         t += 1
-        steps[b](t, stream=s_comp)
-        used[b] = True
+        steps[k % 2](t, stream=s_comp)
         torch.cat(firsts, out=heads)
         host_h.copy_(heads, non_blocking=True)
-        ev_step[b].record(s_comp)
 
-    def run(nsteps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(s_comp)
-        s_in.wait_event(e0)
-        upload(0)
-        for k in range(nsteps):
-            if k + 1 < nsteps:
-                upload(k + 1)
-            compute(k)
-        e1.record(s_comp)
-        torch.cuda.synchronize(dev)
-        return max_over_ranks(e0.elapsed_time(e1), world, dev) / nsteps
-
-    run(2)
-    ms = run(args.e2e_steps)
-    link = plain_h2d_rate(host_g, grads, dev, world)
-    out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": h2d,
+    up.timed(2, compute, s_comp, world, dev)
+    ms = up.timed(args.e2e_steps, compute, s_comp, world, dev)
+    link = plain_h2d_rate(up.host, up.dev_flat[0], dev, world)
+    out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": up.nbytes,
            "d2h_bytes_per_step": n * 4, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"first updated value of each tensor ({n} float32)",
-           "path": "pinned host bf16 grads -> device (double-buffered, 1 copy stream, overlapping the previous "
-                   "step), CameStep, device->host read of one value per tensor",
+           "path": "one flat pinned host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
+                   "overlapping the previous step), CameStep, device->host read of one value per tensor",
            "link": link, "host_numa": HOST_NUMA, "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
-    del host_g, grads2
+    del up
     return out
 
 
@@ -1132,8 +1083,6 @@ def main():
                              "llama_layer_came"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--readback-steps", type=int, default=2)
-    ap.add_argument("--e2e-streams", type=int, default=1,
-                    help="host->device copy streams of the e2e run (1, 4 and 8 measured alike: the host link bounds it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shards", type=int, default=0,
                     help="run the row-sharded step with this many row shards on one GPU (exchange on the device)")

@@ -6,6 +6,7 @@ import json
 import os
 
 import pytest
+import torch
 
 import bench
 from memory_efficient_optimizer_gb300 import synth
@@ -90,3 +91,18 @@ def test_workloads_resolve_to_a_runner(name):
     wl = synth.workload(name)
     assert wl.optimizer in bench.ORACLE_TIMERS
     assert wl.numel == N_8B
+
+
+def test_flat_views_share_one_buffer_with_256_byte_offsets():
+    """The e2e gradient staging: one contiguous buffer, each view at a
+    256-byte offset, shapes and dtypes kept, writes through a view land in the
+    buffer."""
+    like = [torch.zeros(3, 5, dtype=torch.bfloat16), torch.zeros(7, dtype=torch.float32), torch.zeros(0)]
+    buf, views = bench.flat_views(like, "cpu")
+    assert [v.shape for v in views] == [x.shape for x in like]
+    assert [v.dtype for v in views] == [x.dtype for x in like]
+    base = buf.data_ptr()
+    assert [v.data_ptr() - base for v in views[:2]] == [0, 256]
+    assert buf.numel() == 512
+    views[1].fill_(1.0)
+    assert buf[256:256 + 28].view(torch.float32).sum().item() == 7.0
