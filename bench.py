@@ -112,8 +112,9 @@ def measured_hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-# Classes whose pass 1 is the fused row-chunk pass (g read twice per step, not three times).
-FUSED_CLASSES = ("rows_bf16", "wide_bf16")
+# Classes whose pass 1 also forms sum(u^2) (g read twice per step, not three
+# times): the row-panel pass and the fused flat pass.
+FUSED_CLASSES = ("rows_bf16", "wide_bf16", "flat_bf16", "flat_f32")
 
 
 def tensor_class(shape, grad_bytes):
@@ -121,6 +122,8 @@ def tensor_class(shape, grad_bytes):
     if len(shape) < 2:
         return "1d"
     w = int(shape[-1])
+    if w <= 1024:  # whole rows per tile (every tile start 4-value aligned here)
+        return "flat_" + ("bf16" if grad_bytes == 2 else "f32")
     if w % 8:
         return "elem_" + ("bf16" if grad_bytes == 2 else "f32")
     if grad_bytes == 2 and 2048 <= w <= 4096:

@@ -198,13 +198,20 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       const bool vec_shape = (W % 8 == 0);
       const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxWideW &&
                               H <= INT32_MAX && t.grad_dtype == ADAF_BFLOAT16;
+      // Rows that fit one tile: the fused flat pass 1 (whole rows per tile),
+      // when every tile starts on a 4-value boundary of g and p.
+      const bool flat_shape = W <= meo::kTileCols && !rows_shape;
       bool vec = vec_shape;
       if (full) {
         vec = vec_shape && aligned(t.param, 16) && aligned(t.grad, 16) &&
               (!hp->has_beta1 || (hp->exp_avg_int8 ? aligned(d.mq, 16) : aligned(d.m1, 16)));
-        d.kind = !vec ? meo::kFactoredScalar : (rows_shape ? meo::kFactoredRows : meo::kFactoredVec);
+        const size_t ge = t.grad_dtype == ADAF_BFLOAT16 ? 2 : 4;
+        const bool flat = flat_shape && aligned(t.grad, 4 * ge) && aligned(t.param, 16) &&
+                          (B == 1 || (H * W) % 4 == 0);
+        d.kind = (vec && rows_shape) ? meo::kFactoredRows
+                                     : (flat ? meo::kFactoredFlat : (vec ? meo::kFactoredVec : meo::kFactoredScalar));
       } else {
-        d.kind = rows_shape ? meo::kFactoredRows : meo::kFactoredScalar;
+        d.kind = rows_shape ? meo::kFactoredRows : (flat_shape ? meo::kFactoredFlat : meo::kFactoredScalar);
       }
       // Row-panel geometry (also reserved in the size query for rows_shape).
       int32_t prb_rows = 0;
@@ -212,15 +219,17 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
         d.pr = panel_rows(W);
         prb_rows = static_cast<int32_t>(ceil_div(H, d.pr));
       }
-      const bool fused = d.kind == meo::kFactoredRows;
+      const bool fused = meo::is_fused(d.kind);
       // The layout reserves room for every path the tensor may take (which
       // one depends on pointer alignment), so the workspace size does not
-      // depend on the pointers.
+      // depend on the pointers.  Fused flat tensors take the row tiles as
+      // their chunks.
       const bool need_tiled = true;
-      const bool need_rows = rows_shape;
+      const bool need_rows = rows_shape || flat_shape;
+      if (flat_shape) prb_rows = d.rb;
       d.nrc = fused ? prb_rows : static_cast<int32_t>(ceil_div(H, meo::kRowChunk));
       d.prb = fused ? prb_rows : d.rb;
-      nunits = fused ? B * prb_rows : ntiles;
+      nunits = (d.kind == meo::kFactoredRows) ? B * prb_rows : ntiles;
       items += B * (fused ? d.ncc : (d.nrc + d.ncc));
       d.mslot = nmrow;
       nmrow += B;
@@ -264,7 +273,8 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
         d.x1r = nx1row;  // relative until the column block's size is known
         nx1row += d.B;
       }
-      if (d.pr > 0) {  // may take the fused pass (reserved whatever the pointers' alignment)
+      if (d.pr > 0 || (d.W <= meo::kTileCols && d.kind != meo::kUnfactored)) {
+        // may take a fused pass 1 (reserved whatever the pointers' alignment)
         d.dloc = ndloc;
         ndloc += align_up(static_cast<int64_t>(d.B) * d.W, 4);
       }
@@ -299,7 +309,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
   for (size_t k = 0; k < nd; ++k) {
     const DevTensor& d = plan->dev[k];
     plan->pf_tiles[k + 1] = plan->pf_tiles[k] + static_cast<int32_t>(d.ntiles);
-    const int64_t per_slice = d.kind == meo::kFactoredRows ? d.ncc : (d.nrc + d.ncc);
+    const int64_t per_slice = meo::is_fused(d.kind) ? d.ncc : (d.nrc + d.ncc);
     plan->pf_items[k + 1] =
         plan->pf_items[k] + (d.kind == meo::kUnfactored ? 0 : static_cast<int32_t>(int64_t(d.B) * per_slice));
     int c = meo::kClsUnfactored;
@@ -307,6 +317,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
     if (d.kind == meo::kFactoredVec) c = bf ? meo::kClsVecBF16 : meo::kClsVecF32;
     if (d.kind == meo::kFactoredScalar) c = bf ? meo::kClsScalarBF16 : meo::kClsScalarF32;
     if (d.kind == meo::kFactoredRows) c = d.W <= meo::kMaxRowsW ? meo::kClsRowsBF16 : meo::kClsWideBF16;
+    if (d.kind == meo::kFactoredFlat) c = bf ? meo::kClsFlatBF16 : meo::kClsFlatF32;
     const bool two_pass = d.kind == meo::kFactoredVec || d.kind == meo::kFactoredScalar;
     plan->cls_idx[c].push_back(static_cast<int32_t>(k));
     plan->cls_pf[0][c].push_back(plan->cls_pf[0][c].back() + static_cast<int32_t>(d.p1_n));
@@ -379,8 +390,8 @@ struct ProfRecord {
 // Profiling slots: one per streaming kernel kind and tensor class, one per
 // other kernel kind, in launch order.
 constexpr int kNumSlots = 3 * meo::kNumClasses + 4;
-const char* const kClassNames[meo::kNumClasses] = {"vec_bf16", "vec_f32",  "elem_bf16", "elem_f32",
-                                                   "1d",       "rows_bf16", "wide_bf16"};
+const char* const kClassNames[meo::kNumClasses] = {"vec_bf16",  "vec_f32",   "elem_bf16", "elem_f32", "1d",
+                                                   "rows_bf16", "wide_bf16", "flat_bf16", "flat_f32"};
 
 int profile_slot(KernelId k, int cls) {
   const int C = meo::kNumClasses;

@@ -33,7 +33,11 @@ enum TensorKind : int32_t {
   kFactoredScalar = 1,// ndim >= 2, anything else
   kUnfactored = 2,    // ndim < 2
   kFactoredRows = 3,  // as kFactoredVec with kMinRowsW <= W <= kMaxWideW, bf16 grads: fused pass 1
+  kFactoredFlat = 4,  // W <= kTileCols (rows not of kFactoredRows), aligned tile starts: fused flat pass 1
 };
+// Tensors whose pass 1 also forms the row statistic and the weighted column
+// partials D_j (no pass 2).
+__host__ __device__ inline bool is_fused(int32_t kind) { return kind == kFactoredRows || kind == kFactoredFlat; }
 
 // Fused pass 1 (kFactoredRows): a CTA takes chunks of d.pr full rows and
 // keeps the column sums of the chunk in registers, 8 values x G column
@@ -65,7 +69,7 @@ struct DevTensor {
   int32_t gdt;    // GradType
   int32_t rb;     // row blocks per slice   (ceil(H / kTileRows)); unfactored: 1
   int32_t cb;     // column blocks          (ceil(W / kTileCols)); unfactored: tiles
-  int32_t nrc;    // row-sum chunks per slice: ceil(H / kRowChunk), or panels (kFactoredRows)
+  int32_t nrc;    // row-sum chunks per slice: ceil(H / kRowChunk), or panels / row tiles (fused kinds)
   int32_t ncc;    // column chunks per slice(ceil(W / kColChunk))
   int32_t prb;    // row blocks of the column partials: rb, or panels per slice (kFactoredRows)
   int32_t pr;     // rows per panel (kFactoredRows)
@@ -73,8 +77,8 @@ struct DevTensor {
   int32_t lanes;  // unused (0)
   int64_t ntiles;     // apply tiles
   int64_t p1_0, p1_n; // pass-1 units: global base (Ppart slot) and count
-  int64_t dpart;      // float offset of the weighted column partials [B][prb][W] (kFactoredRows)
-  int64_t dsum;       // double offset of per-chunk sum_j D_j / col_j [B][ncc] (kFactoredRows)
+  int64_t dpart;      // float offset of the weighted column partials [B][prb][W] (fused kinds)
+  int64_t dsum;       // double offset of per-chunk sum_j D_j / col_j [B][ncc] (fused kinds)
   int64_t tile0;      // global index of the tensor's first tile (Spart/Ppart slot)
   int64_t rowpart;    // float offset of rowpart [cb][B*H]
   int64_t colpart;    // float offset of colpart [B][rb][W]
@@ -108,7 +112,9 @@ enum TensorClass : int32_t {
   kClsUnfactored = 4,  // ndim < 2 (any grad dtype)
   kClsRowsBF16 = 5,    // fused pass 1, bf16 grads, 2048 <= W <= 4096
   kClsWideBF16 = 6,    // fused pass 1, bf16 grads, 4096 < W <= 16384
-  kNumClasses = 7
+  kClsFlatBF16 = 7,    // fused flat pass 1 (kFactoredFlat), bf16 grads
+  kClsFlatF32 = 8,     // fused flat pass 1 (kFactoredFlat), fp32 grads
+  kNumClasses = 9
 };
 
 // Per-call scalars and workspace regions, passed by value to every kernel.

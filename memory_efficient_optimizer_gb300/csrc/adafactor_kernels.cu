@@ -345,6 +345,165 @@ __device__ __forceinline__ bool pass1_flat(const DevTensor& d, const StepArgs& a
   return true;
 }
 
+// ---- fused flat pass 1 (kFactoredFlat) ------------------------------------
+// Tensors whose rows fit one tile (W <= kTileCols): a tile holds whole rows
+// [i0, i1) of one slice, so the row statistic can be formed in pass 1, and
+// with it D_j = sum_i g_ij^2 / row_i, as in the row-panel pass:
+// sum(u^2) = mean(row) * sum_j D_j / col_j (k_stats, k_scalars), and g is
+// read once for the statistics and sum(u^2) instead of twice (no pass 2).
+// The tile is streamed by flat index (flat_chunk_issue: 16-byte loads, the
+// next chunk's loads in flight while a chunk is reduced); each chunk of R
+// whole rows is squared into shared memory, then:
+//   row totals: a segment of L lanes per row, L = min(32, max(1, p / 8)) with
+//     p the power of 2 >= W (narrow rows take few lanes each and many rows
+//     per warp); the row EMA is formed and stored in place and 1/row_i kept
+//     in shared memory;
+//   -- barrier --
+//   column sums of g^2 (C_j) and of g^2 / row_i (D_j): for W <= 128,
+//     T = kThreads / W threads per column, each adding every T-th row, their
+//     partials added in order by the column's owner; else one thread per
+//     column (kTileCols / kThreads columns per thread), four interleaved
+//     partial sums.
+// All orders are fixed, so two runs give bit-identical results.
+constexpr int kFlatMinB = 3;  // CTAs per SM of k_pass1_flat
+template <typename GT, bool PSQ>
+__device__ __forceinline__ void pass1_flat_fused(const DevTensor& d, const StepArgs& a, int64_t local, float* stage,
+                                                 float* rinv, float* cw, double* red) {
+  constexpr int kStage = kWarps * kTileCols;
+  constexpr int kCols = kTileCols / kThreads;  // columns per thread (one thread per column)
+  const int64_t H = d.H, W = d.W;
+  const TilePos tp = tile_pos(d, local);  // W <= kTileCols: one column block
+  const int64_t i0 = tp.r * kTileRows;
+  const GT* gt = static_cast<const GT*>(d.g) + tp.b * H * W + i0 * W;
+  const float* pt = d.p + tp.b * H * W + i0 * W;
+  float* rowst = d.row + tp.b * H + i0;
+  const int w = static_cast<int>(W);
+  const int nr = static_cast<int>(min(H, i0 + kTileRows) - i0);
+  const int R = min(nr, (kStage / w) & ~3);  // rows per chunk: chunk starts stay on 4-value boundaries
+  int lp = 0;
+  while ((1 << lp) < w) ++lp;
+  const int lg = max(0, min(5, lp - 3));  // log2 of the lanes per row
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane >> lg, cl0 = lane & ((1 << lg) - 1);
+  const int rpw = 32 >> lg;  // rows per warp pass
+  const int T = w <= kThreads / 2 ? kThreads / w : 1;  // threads per column
+  const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
+  const float eps1 = static_cast<float>(a.eps1);
+  const float invw = 1.0f / static_cast<float>(w);
+
+  float cacc[kCols], dacc[kCols];
+#pragma unroll
+  for (int k = 0; k < kCols; ++k) cacc[k] = dacc[k] = 0.f;
+  float psq = 0.f, tail = 0.f, rsum = 0.f;
+  Raw4<GT> raw[kFlatVec1];
+  flat_chunk_issue<GT, PSQ>(raw, tail, gt, pt, R * w, psq);
+  for (int r0 = 0; r0 < nr; r0 += R) {
+    const int rows = min(R, nr - r0);
+    const int cn = rows * w, nv = cn >> 2;
+#pragma unroll
+    for (int k = 0; k < kFlatVec1; ++k) {
+      const int v = threadIdx.x + k * kThreads;
+      if (v < nv) {
+        float x[4];
+        widen4(raw[k], x);
+        *reinterpret_cast<float4*>(stage + 4 * v) = make_float4(x[0] * x[0], x[1] * x[1], x[2] * x[2], x[3] * x[3]);
+      }
+    }
+    const int te = (nv << 2) + threadIdx.x;
+    if (te < cn) stage[te] = tail * tail;
+    __syncthreads();
+    const int r1 = r0 + R;
+    if (r1 < nr) flat_chunk_issue<GT, PSQ>(raw, tail, gt + r1 * w, pt + r1 * w, min(R, nr - r1) * w, psq);
+    // row totals, the row statistic and its reciprocal
+    for (int rb = warp * rpw; rb < rows; rb += kWarps * rpw) {
+      const int rr = rb + sub;
+      float sr = 0.f;
+      if (rr < rows)
+        for (int c = cl0; c < w; c += 1 << lg) sr += stage[rr * w + c];
+      for (int o = (1 << lg) >> 1; o > 0; o >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, o);
+      if (cl0 == 0 && rr < rows) {
+        const float rn = fmaf(b2, rowst[r0 + rr], omb2 * fmaf(sr, invw, eps1));
+        rowst[r0 + rr] = rn;
+        rinv[rr] = __frcp_rn(rn);  // correctly rounded 1 / rn
+        rsum += rn;
+      }
+    }
+    __syncthreads();
+    // column sums of g^2 and of g^2 / row_i
+    if (T > 1) {
+      const int k = threadIdx.x / w, c = threadIdx.x - k * w;
+      if (k < T) {
+        float sc = 0.f, sd = 0.f;
+        for (int rr = k; rr < rows; rr += T) {
+          const float q = stage[rr * w + c];
+          sc += q;
+          sd = fmaf(q, rinv[rr], sd);
+        }
+        cw[threadIdx.x] = sc;
+        cw[kThreads + threadIdx.x] = sd;
+      }
+      __syncthreads();
+      if (threadIdx.x < w) {
+        float tc = 0.f, td = 0.f;
+        for (int kk = 0; kk < T; ++kk) {
+          tc += cw[kk * w + threadIdx.x];
+          td += cw[kThreads + kk * w + threadIdx.x];
+        }
+        cacc[0] += tc;
+        dacc[0] += td;
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < kCols; ++m) {
+        const int c = threadIdx.x + m * kThreads;
+        if (c < w) {
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+          int rr = 0;
+          for (; rr + 4 <= rows; rr += 4) {
+            const float q0 = stage[rr * w + c], q1 = stage[(rr + 1) * w + c];
+            const float q2 = stage[(rr + 2) * w + c], q3 = stage[(rr + 3) * w + c];
+            s0 += q0; s1 += q1; s2 += q2; s3 += q3;
+            e0 = fmaf(q0, rinv[rr], e0); e1 = fmaf(q1, rinv[rr + 1], e1);
+            e2 = fmaf(q2, rinv[rr + 2], e2); e3 = fmaf(q3, rinv[rr + 3], e3);
+          }
+          for (; rr < rows; ++rr) {
+            const float q = stage[rr * w + c];
+            s0 += q;
+            e0 = fmaf(q, rinv[rr], e0);
+          }
+          cacc[m] += (s0 + s1) + (s2 + s3);
+          dacc[m] += (e0 + e1) + (e2 + e3);
+        }
+      }
+    }
+    __syncthreads();  // stage, rinv and cw are rewritten next
+  }
+  const int64_t off = (tp.b * d.prb + tp.r) * W;
+  float* cp = a.colpart + d.colpart + off;
+  float* dp = a.dpart + d.dpart + off;
+  if (T > 1) {
+    if (threadIdx.x < w) {
+      cp[threadIdx.x] = cacc[0];
+      dp[threadIdx.x] = dacc[0];
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < kCols; ++m) {
+      const int c = threadIdx.x + m * kThreads;
+      if (c < w) {
+        cp[c] = cacc[m];
+        dp[c] = dacc[m];
+      }
+    }
+  }
+  const double rt = block_sum(static_cast<double>(rsum), red);
+  if (threadIdx.x == 0) a.rowchunk[d.rowchunk + tp.b * d.nrc + tp.r] = rt;
+  if (PSQ) {
+    const double ptot = block_sum(static_cast<double>(psq), red);
+    if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = ptot;
+  }
+}
+
 template <typename GT, int VEC, bool PSQ>
 __device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArgs& a, int64_t local,
                                float* colbuf, double* red) {
@@ -529,6 +688,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_f(const __grid_constant__
   }
 }
 
+// Shared memory of k_pass1_flat: the chunk stage, 1/row of the chunk's rows,
+// the column partials of T threads per column, CTA-sum scratch, prefix.
+constexpr size_t kFlatSmem = kColbufBytes + sizeof(float) * (kTileRows + 2 * kThreads) + kRedBytes + kPrefixBytes;
+template <typename GT, bool PSQ>
+__global__ void __launch_bounds__(kThreads, kFlatMinB) k_pass1_flat(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* stage = reinterpret_cast<float*>(smem);
+  float* rinv = stage + kWarps * kTileCols;
+  float* cw = rinv + kTileRows;
+  double* red = reinterpret_cast<double*>(cw + 2 * kThreads);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kColbufBytes + sizeof(float) * (kTileRows + 2 * kThreads) + kRedBytes);
+  const int ng = load_prefix(pf, r);
+  const int64_t u1 = pf[ng];
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    pass1_flat_fused<GT, PSQ>(d, a, u - pf[m], stage, rinv, cw, red);
+  }
+}
+
 template <bool PSQ>
 __global__ void __launch_bounds__(kThreads) k_pass1_u(const __grid_constant__ StepArgs a, const Range r) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -591,7 +770,7 @@ __device__ __forceinline__ void stats_col_item(const DevTensor& d, const StepArg
                                                float* part, double* red) {
   constexpr int kPer = kColChunk / 32;
   constexpr int R = Q4 ? kStatsRows : 2;  // row blocks per warp and iteration
-  const bool fused = d.kind == kFactoredRows;
+  const bool fused = is_fused(d.kind);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t W = d.W;
   const int64_t c0 = q * kColChunk;
@@ -704,7 +883,7 @@ __device__ __forceinline__ void stats_col_any(const DevTensor& d, const StepArgs
 // sum_j D_j / col_j over the chunk's columns.
 __device__ __forceinline__ void stats_col_global(const DevTensor& d, const StepArgs& a, int64_t b, int64_t q,
                                                  double* red) {
-  const bool fused = d.kind == kFactoredRows;
+  const bool fused = is_fused(d.kind);
   const int64_t W = d.W;
   const int64_t jt = q * kColChunk + threadIdx.x;
   float term = 0.f;
@@ -733,7 +912,7 @@ __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ Step
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
     const int64_t local = u - pf[m];
-    if (d.kind == kFactoredRows) {  // rows were updated by the fused pass 1
+    if (is_fused(d.kind)) {  // rows were updated by the fused pass 1
       if (a.phase == 2) stats_col_global(d, a, local / d.ncc, local % d.ncc, red);
       else stats_col_any(d, a, local / d.ncc, local % d.ncc, part, red);
       continue;
@@ -802,7 +981,7 @@ __global__ void __launch_bounds__(kThreads) k_scalars(const __grid_constant__ St
     // mean(row) per slice; for fused tensors also sum(u^2) =
     // sum_b mean(row_b) * sum_j D_bj / col_bj (slices in order within a warp,
     // then warps in order).
-    const bool fused = d.kind == kFactoredRows;
+    const bool fused = is_fused(d.kind);
     double su = 0.0;
     for (int64_t b = warp; b < d.B; b += kWarps) {
       double s = 0.0;
@@ -988,7 +1167,7 @@ __global__ void __launch_bounds__(kThreads) k_clip(const __grid_constant__ StepA
   double S;
   if (a.phase == 3) {
     S = a.round2[t];  // sum over all shards
-  } else if (d.kind == kFactoredRows) {
+  } else if (is_fused(d.kind)) {
     S = a.ssum[t];
   } else {
     double acc = 0.0;
@@ -2008,6 +2187,19 @@ Inst pick_rows(KernelId k, bool psq_in, int mom, bool psq_out) {
   return x;
 }
 
+// The flat class: fused flat pass 1, no pass 2, the element-wise apply.
+template <typename GT>
+Inst pick_flat(KernelId k, bool psq_in, int mom, bool psq_out) {
+  Inst x;
+  if (k == kKPass1) {
+    x.fn = psq_in ? k_pass1_flat<GT, true> : k_pass1_flat<GT, false>;
+    x.smem = kFlatSmem;
+  } else if (k == kKApply) {
+    x = pick_f<GT, 1>(k, psq_in, mom, psq_out);
+  }
+  return x;
+}
+
 // mom: first moment none (0), fp32 exp_avg (1), 8-bit codes + scales (2).
 Inst pick(KernelId k, TensorClass c, bool psq_in, int mom, bool psq_out) {
   Inst x;
@@ -2018,6 +2210,8 @@ Inst pick(KernelId k, TensorClass c, bool psq_in, int mom, bool psq_out) {
     case kClsScalarF32: return pick_f<float, 1>(k, psq_in, mom, psq_out);
     case kClsRowsBF16: return pick_rows<__nv_bfloat16, kRowsNW, kRowsG, kRowsS, kRowsMinB>(k, psq_in, mom, psq_out);
     case kClsWideBF16: return pick_rows<__nv_bfloat16, 16, 4, 3, 1>(k, psq_in, mom, psq_out);
+    case kClsFlatBF16: return pick_flat<__nv_bfloat16>(k, psq_in, mom, psq_out);
+    case kClsFlatF32: return pick_flat<float>(k, psq_in, mom, psq_out);
     case kClsUnfactored:
       x.smem = kRedBytes + kPrefixBytes;
       if (k == kKPass1) x.fn = psq_in ? k_pass1_u<true> : k_pass1_u<false>;

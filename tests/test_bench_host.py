@@ -32,7 +32,10 @@ def test_tensor_classes_of_the_8b_list():
     assert classes == {"rows_bf16", "wide_bf16", "1d"}
     assert bench.tensor_class((4096, 14336), 2) == "wide_bf16"
     assert bench.tensor_class((4096, 4096), 4) == "vec_f32"
-    assert bench.tensor_class((33, 7), 2) == "elem_bf16"
+    assert bench.tensor_class((33, 7), 2) == "flat_bf16"
+    assert bench.tensor_class((8, 1024, 1024), 4) == "flat_f32"
+    assert bench.tensor_class((3, 4097), 4) == "elem_f32"
+    assert bench.tensor_class((17, 100003), 2) == "elem_bf16"
 
 
 def test_lamb_bytes():

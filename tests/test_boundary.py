@@ -197,9 +197,10 @@ def test_shard_sizes_and_argument_errors_before_any_cuda_call(lib):
 
 def test_kernel_names(lib):
     names = [B.adafactor_kernel_name(k) for k in range(B.adafactor_num_kernels())]
-    assert len(names) == 25 and len(set(names)) == 25
+    assert len(names) == 31 and len(set(names)) == 31
     for kind in ("k_pass1", "k_pass2", "k_apply"):
-        for cls in ("vec_bf16", "vec_f32", "elem_bf16", "elem_f32", "1d", "rows_bf16", "wide_bf16"):
+        for cls in ("vec_bf16", "vec_f32", "elem_bf16", "elem_f32", "1d", "rows_bf16", "wide_bf16", "flat_bf16",
+                    "flat_f32"):
             assert f"{kind}[{cls}]" in names
     assert {"k_stats", "k_scalars", "k_clip", "k_psq"} <= set(names)
 
