@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -95,6 +96,12 @@ int stream_slot(KernelId k) { return k == meo::kKPass1 ? 0 : (k == meo::kKPass2 
 
 // Rows per work unit of the fused pass.
 int32_t panel_rows(int64_t W) { return W <= meo::kMaxRowsW ? meo::kRowsChunk : meo::kWideChunk; }
+// Rows per pass-1 unit of the fused flat pass: about 32K values per unit, a
+// multiple of 4 rows (the flat walk's chunk starts), at most kTileRows.
+int32_t flat_rows(int64_t W) {
+  const int64_t r = (32768 / W) & ~int64_t{3};
+  return static_cast<int32_t>(r < 4 ? 4 : (r > meo::kTileRows ? meo::kTileRows : r));
+}
 
 // Checks the tensor list and builds the plan.  With full == false (size
 // query) only the shapes and dtypes are read; states and hp are not touched.
@@ -226,10 +233,13 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       // their chunks.
       const bool need_tiled = true;
       const bool need_rows = rows_shape || flat_shape;
-      if (flat_shape) prb_rows = d.rb;
+      if (flat_shape) {
+        d.pr = flat_rows(W);
+        prb_rows = static_cast<int32_t>(ceil_div(H, d.pr));
+      }
       d.nrc = fused ? prb_rows : static_cast<int32_t>(ceil_div(H, meo::kRowChunk));
       d.prb = fused ? prb_rows : d.rb;
-      nunits = (d.kind == meo::kFactoredRows) ? B * prb_rows : ntiles;
+      nunits = fused ? B * prb_rows : ntiles;
       items += B * (fused ? d.ncc : (d.nrc + d.ncc));
       d.mslot = nmrow;
       nmrow += B;
@@ -318,11 +328,30 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
     if (d.kind == meo::kFactoredScalar) c = bf ? meo::kClsScalarBF16 : meo::kClsScalarF32;
     if (d.kind == meo::kFactoredRows) c = d.W <= meo::kMaxRowsW ? meo::kClsRowsBF16 : meo::kClsWideBF16;
     if (d.kind == meo::kFactoredFlat) c = bf ? meo::kClsFlatBF16 : meo::kClsFlatF32;
-    const bool two_pass = d.kind == meo::kFactoredVec || d.kind == meo::kFactoredScalar;
     plan->cls_idx[c].push_back(static_cast<int32_t>(k));
-    plan->cls_pf[0][c].push_back(plan->cls_pf[0][c].back() + static_cast<int32_t>(d.p1_n));
-    plan->cls_pf[1][c].push_back(plan->cls_pf[1][c].back() + (two_pass ? static_cast<int32_t>(d.ntiles) : 0));
-    plan->cls_pf[2][c].push_back(plan->cls_pf[2][c].back() + static_cast<int32_t>(d.ntiles));
+  }
+  // Members of the tiled classes walked largest tiles first: the persistent
+  // CTAs take the units round-robin, so ragged lists of small matrices end
+  // on small tiles instead of on a few large ones (each tensor's results
+  // land at its own offsets, so the order changes no value).
+  for (int c : {meo::kClsVecBF16, meo::kClsVecF32, meo::kClsScalarBF16, meo::kClsScalarF32, meo::kClsFlatBF16,
+                meo::kClsFlatF32}) {
+    std::vector<int32_t>& m = plan->cls_idx[c];
+    std::stable_sort(m.begin(), m.end(), [&](int32_t x, int32_t y) {
+      const DevTensor& a = plan->dev[x];
+      const DevTensor& b = plan->dev[y];
+      return static_cast<double>(a.n) / static_cast<double>(a.ntiles) >
+             static_cast<double>(b.n) / static_cast<double>(b.ntiles);  // values per tile, descending
+    });
+  }
+  for (int c = 0; c < meo::kNumClasses; ++c) {
+    for (int32_t k : plan->cls_idx[c]) {
+      const DevTensor& d = plan->dev[k];
+      const bool two_pass = d.kind == meo::kFactoredVec || d.kind == meo::kFactoredScalar;
+      plan->cls_pf[0][c].push_back(plan->cls_pf[0][c].back() + static_cast<int32_t>(d.p1_n));
+      plan->cls_pf[1][c].push_back(plan->cls_pf[1][c].back() + (two_pass ? static_cast<int32_t>(d.ntiles) : 0));
+      plan->cls_pf[2][c].push_back(plan->cls_pf[2][c].back() + static_cast<int32_t>(d.ntiles));
+    }
   }
   // Workspace layout: the header (uploaded each call: the device status word
   // at offset 0, the descriptor table at kTableOffset, the prefix arrays)

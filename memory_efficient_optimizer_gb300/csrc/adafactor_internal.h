@@ -72,7 +72,7 @@ struct DevTensor {
   int32_t nrc;    // row-sum chunks per slice: ceil(H / kRowChunk), or panels / row tiles (fused kinds)
   int32_t ncc;    // column chunks per slice(ceil(W / kColChunk))
   int32_t prb;    // row blocks of the column partials: rb, or panels per slice (kFactoredRows)
-  int32_t pr;     // rows per panel (kFactoredRows)
+  int32_t pr;     // rows per pass-1 unit (fused kinds: a panel chunk, or a flat chunk)
   int32_t seg;    // unused (0)
   int32_t lanes;  // unused (0)
   int64_t ntiles;     // apply tiles

@@ -346,8 +346,11 @@ __device__ __forceinline__ bool pass1_flat(const DevTensor& d, const StepArgs& a
 }
 
 // ---- fused flat pass 1 (kFactoredFlat) ------------------------------------
-// Tensors whose rows fit one tile (W <= kTileCols): a tile holds whole rows
-// [i0, i1) of one slice, so the row statistic can be formed in pass 1, and
+// Tensors whose rows fit one tile (W <= kTileCols): a work unit is a chunk of
+// d.pr whole rows [i0, i1) of one slice (d.pr <= kTileRows, chosen by the
+// planner so that a unit holds about 32K values: wide rows make short
+// chunks, which keeps the units of one launch alike), so the row statistic
+// can be formed in pass 1, and
 // with it D_j = sum_i g_ij^2 / row_i, as in the row-panel pass:
 // sum(u^2) = mean(row) * sum_j D_j / col_j (k_stats, k_scalars), and g is
 // read once for the statistics and sum(u^2) instead of twice (no pass 2).
@@ -368,17 +371,18 @@ __device__ __forceinline__ bool pass1_flat(const DevTensor& d, const StepArgs& a
 constexpr int kFlatMinB = 3;  // CTAs per SM of k_pass1_flat
 template <typename GT, bool PSQ>
 __device__ __forceinline__ void pass1_flat_fused(const DevTensor& d, const StepArgs& a, int64_t local, float* stage,
-                                                 float* rinv, float* cw, double* red) {
+                                                 float* rinv, float* rold, float* cw, double* red) {
   constexpr int kStage = kWarps * kTileCols;
   constexpr int kCols = kTileCols / kThreads;  // columns per thread (one thread per column)
   const int64_t H = d.H, W = d.W;
-  const TilePos tp = tile_pos(d, local);  // W <= kTileCols: one column block
-  const int64_t i0 = tp.r * kTileRows;
-  const GT* gt = static_cast<const GT*>(d.g) + tp.b * H * W + i0 * W;
-  const float* pt = d.p + tp.b * H * W + i0 * W;
-  float* rowst = d.row + tp.b * H + i0;
+  // unit: chunk q of d.pr rows of slice b (d.pr <= kTileRows, a multiple of 4)
+  const int64_t b = local / d.prb, q = local % d.prb;
+  const int64_t i0 = q * d.pr;
+  const GT* gt = static_cast<const GT*>(d.g) + b * H * W + i0 * W;
+  const float* pt = d.p + b * H * W + i0 * W;
+  float* rowst = d.row + b * H + i0;
   const int w = static_cast<int>(W);
-  const int nr = static_cast<int>(min(H, i0 + kTileRows) - i0);
+  const int nr = static_cast<int>(min(H, i0 + d.pr) - i0);
   const int R = min(nr, (kStage / w) & ~3);  // rows per chunk: chunk starts stay on 4-value boundaries
   int lp = 0;
   while ((1 << lp) < w) ++lp;
@@ -397,6 +401,9 @@ __device__ __forceinline__ void pass1_flat_fused(const DevTensor& d, const StepA
   float psq = 0.f, tail = 0.f, rsum = 0.f;
   Raw4<GT> raw[kFlatVec1];
   flat_chunk_issue<GT, PSQ>(raw, tail, gt, pt, R * w, psq);
+  // The old row statistic of the whole tile, in one coalesced load while the
+  // first chunk is in flight (a load per row would sit on every row's path).
+  if (threadIdx.x < nr) rold[threadIdx.x] = rowst[threadIdx.x];
   for (int r0 = 0; r0 < nr; r0 += R) {
     const int rows = min(R, nr - r0);
     const int cn = rows * w, nv = cn >> 2;
@@ -422,7 +429,7 @@ __device__ __forceinline__ void pass1_flat_fused(const DevTensor& d, const StepA
         for (int c = cl0; c < w; c += 1 << lg) sr += stage[rr * w + c];
       for (int o = (1 << lg) >> 1; o > 0; o >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, o);
       if (cl0 == 0 && rr < rows) {
-        const float rn = fmaf(b2, rowst[r0 + rr], omb2 * fmaf(sr, invw, eps1));
+        const float rn = fmaf(b2, rold[r0 + rr], omb2 * fmaf(sr, invw, eps1));
         rowst[r0 + rr] = rn;
         rinv[rr] = __frcp_rn(rn);  // correctly rounded 1 / rn
         rsum += rn;
@@ -478,7 +485,7 @@ __device__ __forceinline__ void pass1_flat_fused(const DevTensor& d, const StepA
     }
     __syncthreads();  // stage, rinv and cw are rewritten next
   }
-  const int64_t off = (tp.b * d.prb + tp.r) * W;
+  const int64_t off = (b * d.prb + q) * W;
   float* cp = a.colpart + d.colpart + off;
   float* dp = a.dpart + d.dpart + off;
   if (T > 1) {
@@ -497,7 +504,7 @@ __device__ __forceinline__ void pass1_flat_fused(const DevTensor& d, const StepA
     }
   }
   const double rt = block_sum(static_cast<double>(rsum), red);
-  if (threadIdx.x == 0) a.rowchunk[d.rowchunk + tp.b * d.nrc + tp.r] = rt;
+  if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + q] = rt;
   if (PSQ) {
     const double ptot = block_sum(static_cast<double>(psq), red);
     if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = ptot;
@@ -690,21 +697,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_f(const __grid_constant__
 
 // Shared memory of k_pass1_flat: the chunk stage, 1/row of the chunk's rows,
 // the column partials of T threads per column, CTA-sum scratch, prefix.
-constexpr size_t kFlatSmem = kColbufBytes + sizeof(float) * (kTileRows + 2 * kThreads) + kRedBytes + kPrefixBytes;
+constexpr size_t kFlatSmem = kColbufBytes + sizeof(float) * (2 * kTileRows + 2 * kThreads) + kRedBytes + kPrefixBytes;
 template <typename GT, bool PSQ>
 __global__ void __launch_bounds__(kThreads, kFlatMinB) k_pass1_flat(const __grid_constant__ StepArgs a, const Range r) {
   extern __shared__ __align__(16) unsigned char smem[];
   float* stage = reinterpret_cast<float*>(smem);
   float* rinv = stage + kWarps * kTileCols;
-  float* cw = rinv + kTileRows;
+  float* rold = rinv + kTileRows;
+  float* cw = rold + kTileRows;
   double* red = reinterpret_cast<double*>(cw + 2 * kThreads);
-  int32_t* pf = reinterpret_cast<int32_t*>(smem + kColbufBytes + sizeof(float) * (kTileRows + 2 * kThreads) + kRedBytes);
+  int32_t* pf = reinterpret_cast<int32_t*>(smem + kColbufBytes + sizeof(float) * (2 * kTileRows + 2 * kThreads) +
+                                           kRedBytes);
   const int ng = load_prefix(pf, r);
   const int64_t u1 = pf[ng];
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
-    pass1_flat_fused<GT, PSQ>(d, a, u - pf[m], stage, rinv, cw, red);
+    pass1_flat_fused<GT, PSQ>(d, a, u - pf[m], stage, rinv, rold, cw, red);
   }
 }
 
