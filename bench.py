@@ -553,6 +553,35 @@ class EmulatedRowShards:
             st.end(t)
 
 
+def timed_and_profiled(step, t, nsteps, stream, dev, world, clocks, profile_enable, profile_read):
+    """Times nsteps steps with CUDA events on the launch stream, nothing else
+    recorded in between (the step time reported), then runs nsteps more with
+    the library's per-kernel event pairs on (the per-kernel table).  Returns
+    (ms per timed step, the per-kernel record, the last step number)."""
+    profile_read()  # drop anything recorded so far
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    w0 = time.time()
+    ev0.record(stream)
+    for _ in range(nsteps):
+        t += 1
+        step(t)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(w0, time.time())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev) / nsteps
+    profile_enable(True)
+    for _ in range(nsteps):
+        t += 1
+        step(t)
+    torch.cuda.synchronize(dev)
+    profile_enable(False)
+    clocks.stop()
+    return ms, profile_read(), t
+
+
 def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -584,25 +613,10 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    binding.adafactor_profile_read()  # drop anything recorded so far
-    binding.adafactor_profile_enable(True)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    w0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        t += 1
-        step(t)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark(w0, time.time())
-    clocks.stop()
-    binding.adafactor_profile_enable(False)
-    kernels = binding.adafactor_profile_read()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    ms_per_step, kernels, t = timed_and_profiled(step, t, args.steps, stream, dev, world, clocks,
+                                                 binding.adafactor_profile_enable, binding.adafactor_profile_read)
     if world > 1:
         torch.distributed.barrier()
-    ms_per_step = ms / args.steps
 
     # ---- end to end: host grads in, host params out, through the same API
     e2e = None
@@ -657,6 +671,9 @@ def run_ours(args, world, rank, local):
         "min_bytes_this_design": impl_bytes,
         "gbs_min_bytes_this_design": round(impl_bytes / (ms_per_step / 1e3) / 1e9, 1),
         "kernels": per_kernel,
+        "kernels_note": "per-kernel CUDA-event times from a further run of the same number of steps with the "
+                        "library's event pairs on; ms_per_step and value come from the timed steps, which record "
+                        "no event between launches",
         "roofline": roofline, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
     }
     if args.shards:
@@ -727,22 +744,8 @@ def run_lamb(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    binding.lamb_profile_read()
-    binding.lamb_profile_enable(True)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    w0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        t += 1
-        step(t)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark(w0, time.time())
-    clocks.stop()
-    binding.lamb_profile_enable(False)
-    kernels = binding.lamb_profile_read()
-    ms_per_step = max_over_ranks(ev0.elapsed_time(ev1), world, dev) / args.steps
+    ms_per_step, kernels, t = timed_and_profiled(step, t, args.steps, stream, dev, world, clocks,
+                                                 binding.lamb_profile_enable, binding.lamb_profile_read)
     e2e = None
     if args.e2e_steps > 0:
         with numa_local(local):
@@ -839,22 +842,8 @@ def run_came(args, world, rank, local):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    binding.came_profile_read()
-    binding.came_profile_enable(True)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    w0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        t += 1
-        step(t)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark(w0, time.time())
-    clocks.stop()
-    binding.came_profile_enable(False)
-    kernels = binding.came_profile_read()
-    ms_per_step = max_over_ranks(ev0.elapsed_time(ev1), world, dev) / args.steps
+    ms_per_step, kernels, t = timed_and_profiled(step, t, args.steps, stream, dev, world, clocks,
+                                                 binding.came_profile_enable, binding.came_profile_read)
     grad_bytes = 2 if wl.grad_dtype == torch.bfloat16 else 4
     slot_bytes, design_bytes, one_pass_bytes = came_bytes(wl.shapes, grad_bytes)
     peak, peak_kind = measured_hbm_peak()

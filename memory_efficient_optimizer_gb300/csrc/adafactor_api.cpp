@@ -96,11 +96,13 @@ int stream_slot(KernelId k) { return k == meo::kKPass1 ? 0 : (k == meo::kKPass2 
 
 // Rows per work unit of the fused pass.
 int32_t panel_rows(int64_t W) { return W <= meo::kMaxRowsW ? meo::kRowsChunk : meo::kWideChunk; }
-// Rows per pass-1 unit of the fused flat pass: about 32K values per unit, a
-// multiple of 4 rows (the flat walk's chunk starts), at most kTileRows.
+// Rows per pass-1 unit of the fused flat pass: about 64K values per unit, a
+// multiple of 8 rows (so every unit of a slice starts on a 16-byte boundary
+// of g, fp32 or bf16), at most 1024 rows.  (32K-value units measured 8 %
+// slower on small matrices: the per-unit combine of column partials.)
 int32_t flat_rows(int64_t W) {
-  const int64_t r = (32768 / W) & ~int64_t{3};
-  return static_cast<int32_t>(r < 4 ? 4 : (r > meo::kTileRows ? meo::kTileRows : r));
+  const int64_t r = (65536 / W) & ~int64_t{7};
+  return static_cast<int32_t>(r < 8 ? 8 : (r > 1024 ? 1024 : r));
 }
 
 // Checks the tensor list and builds the plan.  With full == false (size
@@ -205,16 +207,18 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       const bool vec_shape = (W % 8 == 0);
       const bool rows_shape = vec_shape && W >= meo::kMinRowsW && W <= meo::kMaxWideW &&
                               H <= INT32_MAX && t.grad_dtype == ADAF_BFLOAT16;
-      // Rows that fit one tile: the fused flat pass 1 (whole rows per tile),
-      // when every tile starts on a 4-value boundary of g and p.
+      // Rows that fit one tile: the fused flat pass 1 (whole rows per tile)
+      // and the bulk-copy flat apply, when g, p and exp_avg start on 16-byte
+      // boundaries and so does every slice (16-byte pieces of the flat range).
       const bool flat_shape = W <= meo::kTileCols && !rows_shape;
       bool vec = vec_shape;
       if (full) {
         vec = vec_shape && aligned(t.param, 16) && aligned(t.grad, 16) &&
               (!hp->has_beta1 || (hp->exp_avg_int8 ? aligned(d.mq, 16) : aligned(d.m1, 16)));
         const size_t ge = t.grad_dtype == ADAF_BFLOAT16 ? 2 : 4;
-        const bool flat = flat_shape && aligned(t.grad, 4 * ge) && aligned(t.param, 16) &&
-                          (B == 1 || (H * W) % 4 == 0);
+        const bool flat = flat_shape && aligned(t.grad, 16) && aligned(t.param, 16) &&
+                          (!hp->has_beta1 || hp->exp_avg_int8 || aligned(d.m1, 16)) &&
+                          (B == 1 || (H * W) % static_cast<int64_t>(16 / ge) == 0);
         d.kind = (vec && rows_shape) ? meo::kFactoredRows
                                      : (flat ? meo::kFactoredFlat : (vec ? meo::kFactoredVec : meo::kFactoredScalar));
       } else {
@@ -534,14 +538,6 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  int grid_limit[meo::kNumKernels][meo::kNumClasses];
-  for (int k = 0; k < meo::kNumKernels; ++k) {
-    for (int c = 0; c < meo::kNumClasses; ++c) {
-      grid_limit[k][c] = meo::kernel_grid_limit(static_cast<KernelId>(k), static_cast<meo::TensorClass>(c),
-                                                device, &e);
-      if (e != cudaSuccess) return cuda_fail(e, "kernel occupancy query");
-    }
-  }
 
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceCache& dc = g_cache[device];
@@ -618,6 +614,15 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
   a.round1 = round1;
   a.round2 = round2;
   a.dloc = phase != 0 ? reinterpret_cast<float*>(ws + plan.off_dloc) : nullptr;
+  const int variant = meo::kernel_variant(a);
+  int grid_limit[meo::kNumKernels][meo::kNumClasses];
+  for (int k = 0; k < meo::kNumKernels; ++k) {
+    for (int c = 0; c < meo::kNumClasses; ++c) {
+      grid_limit[k][c] = meo::kernel_grid_limit(static_cast<KernelId>(k), static_cast<meo::TensorClass>(c),
+                                                variant, device, &e);
+      if (e != cudaSuccess) return cuda_fail(e, "kernel occupancy query");
+    }
+  }
 
   // One launch helper: optional profiling events around the launch.
   auto run = [&](KernelId k, int cls, auto&& launch) -> adaf_status {

@@ -186,9 +186,13 @@ cudaError_t launch_stream(KernelId k, TensorClass c, const StepArgs& a, const Ra
                           cudaStream_t s);
 cudaError_t launch_stats(const StepArgs& a, const Range& r, int grid, cudaStream_t s);
 cudaError_t launch_per_tensor(KernelId k, const StepArgs& a, int ntensors, cudaStream_t s);
-// Resident-CTA limit (CTAs per SM x SMs) of a kernel kind and tensor class
-// on a device (the class is ignored for the non-streaming kinds).
-int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err);
+// Kernel variant of a step: RMS(p) recomputed in pass 1 (1), first moment
+// none / fp32 / 8-bit (x 2), sum(p_new^2) carried out (6); 0..11.
+int kernel_variant(const StepArgs& a);
+// Resident-CTA limit (CTAs per SM x SMs) of the kernel that a kind, tensor
+// class and variant launch on a device (class and variant are ignored for
+// the non-streaming kinds).
+int kernel_grid_limit(KernelId k, TensorClass c, int variant, int device, cudaError_t* err);
 const char* kernel_name(int k);
 
 // How adafactor-step host code uploads the per-call header to the workspace.

@@ -345,172 +345,6 @@ __device__ __forceinline__ bool pass1_flat(const DevTensor& d, const StepArgs& a
   return true;
 }
 
-// ---- fused flat pass 1 (kFactoredFlat) ------------------------------------
-// Tensors whose rows fit one tile (W <= kTileCols): a work unit is a chunk of
-// d.pr whole rows [i0, i1) of one slice (d.pr <= kTileRows, chosen by the
-// planner so that a unit holds about 32K values: wide rows make short
-// chunks, which keeps the units of one launch alike), so the row statistic
-// can be formed in pass 1, and
-// with it D_j = sum_i g_ij^2 / row_i, as in the row-panel pass:
-// sum(u^2) = mean(row) * sum_j D_j / col_j (k_stats, k_scalars), and g is
-// read once for the statistics and sum(u^2) instead of twice (no pass 2).
-// The tile is streamed by flat index (flat_chunk_issue: 16-byte loads, the
-// next chunk's loads in flight while a chunk is reduced); each chunk of R
-// whole rows is squared into shared memory, then:
-//   row totals: a segment of L lanes per row, L = min(32, max(1, p / 8)) with
-//     p the power of 2 >= W (narrow rows take few lanes each and many rows
-//     per warp); the row EMA is formed and stored in place and 1/row_i kept
-//     in shared memory;
-//   -- barrier --
-//   column sums of g^2 (C_j) and of g^2 / row_i (D_j): for W <= 128,
-//     T = kThreads / W threads per column, each adding every T-th row, their
-//     partials added in order by the column's owner; else one thread per
-//     column (kTileCols / kThreads columns per thread), four interleaved
-//     partial sums.
-// All orders are fixed, so two runs give bit-identical results.
-constexpr int kFlatMinB = 3;  // CTAs per SM of k_pass1_flat
-template <typename GT, bool PSQ>
-__device__ __forceinline__ void pass1_flat_fused(const DevTensor& d, const StepArgs& a, int64_t local, float* stage,
-                                                 float* rinv, float* rold, float* cw, double* red) {
-  constexpr int kStage = kWarps * kTileCols;
-  constexpr int kCols = kTileCols / kThreads;  // columns per thread (one thread per column)
-  const int64_t H = d.H, W = d.W;
-  // unit: chunk q of d.pr rows of slice b (d.pr <= kTileRows, a multiple of 4)
-  const int64_t b = local / d.prb, q = local % d.prb;
-  const int64_t i0 = q * d.pr;
-  const GT* gt = static_cast<const GT*>(d.g) + b * H * W + i0 * W;
-  const float* pt = d.p + b * H * W + i0 * W;
-  float* rowst = d.row + b * H + i0;
-  const int w = static_cast<int>(W);
-  const int nr = static_cast<int>(min(H, i0 + d.pr) - i0);
-  const int R = min(nr, (kStage / w) & ~3);  // rows per chunk: chunk starts stay on 4-value boundaries
-  int lp = 0;
-  while ((1 << lp) < w) ++lp;
-  const int lg = max(0, min(5, lp - 3));  // log2 of the lanes per row
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane >> lg, cl0 = lane & ((1 << lg) - 1);
-  const int rpw = 32 >> lg;  // rows per warp pass
-  const int T = w <= kThreads / 2 ? kThreads / w : 1;  // threads per column
-  const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
-  const float eps1 = static_cast<float>(a.eps1);
-  const float invw = 1.0f / static_cast<float>(w);
-
-  float cacc[kCols], dacc[kCols];
-#pragma unroll
-  for (int k = 0; k < kCols; ++k) cacc[k] = dacc[k] = 0.f;
-  float psq = 0.f, tail = 0.f, rsum = 0.f;
-  Raw4<GT> raw[kFlatVec1];
-  flat_chunk_issue<GT, PSQ>(raw, tail, gt, pt, R * w, psq);
-  // The old row statistic of the whole tile, in one coalesced load while the
-  // first chunk is in flight (a load per row would sit on every row's path).
-  if (threadIdx.x < nr) rold[threadIdx.x] = rowst[threadIdx.x];
-  for (int r0 = 0; r0 < nr; r0 += R) {
-    const int rows = min(R, nr - r0);
-    const int cn = rows * w, nv = cn >> 2;
-#pragma unroll
-    for (int k = 0; k < kFlatVec1; ++k) {
-      const int v = threadIdx.x + k * kThreads;
-      if (v < nv) {
-        float x[4];
-        widen4(raw[k], x);
-        *reinterpret_cast<float4*>(stage + 4 * v) = make_float4(x[0] * x[0], x[1] * x[1], x[2] * x[2], x[3] * x[3]);
-      }
-    }
-    const int te = (nv << 2) + threadIdx.x;
-    if (te < cn) stage[te] = tail * tail;
-    __syncthreads();
-    const int r1 = r0 + R;
-    if (r1 < nr) flat_chunk_issue<GT, PSQ>(raw, tail, gt + r1 * w, pt + r1 * w, min(R, nr - r1) * w, psq);
-    // row totals, the row statistic and its reciprocal
-    for (int rb = warp * rpw; rb < rows; rb += kWarps * rpw) {
-      const int rr = rb + sub;
-      float sr = 0.f;
-      if (rr < rows)
-        for (int c = cl0; c < w; c += 1 << lg) sr += stage[rr * w + c];
-      for (int o = (1 << lg) >> 1; o > 0; o >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, o);
-      if (cl0 == 0 && rr < rows) {
-        const float rn = fmaf(b2, rold[r0 + rr], omb2 * fmaf(sr, invw, eps1));
-        rowst[r0 + rr] = rn;
-        rinv[rr] = __frcp_rn(rn);  // correctly rounded 1 / rn
-        rsum += rn;
-      }
-    }
-    __syncthreads();
-    // column sums of g^2 and of g^2 / row_i
-    if (T > 1) {
-      const int k = threadIdx.x / w, c = threadIdx.x - k * w;
-      if (k < T) {
-        float sc = 0.f, sd = 0.f;
-        for (int rr = k; rr < rows; rr += T) {
-          const float q = stage[rr * w + c];
-          sc += q;
-          sd = fmaf(q, rinv[rr], sd);
-        }
-        cw[threadIdx.x] = sc;
-        cw[kThreads + threadIdx.x] = sd;
-      }
-      __syncthreads();
-      if (threadIdx.x < w) {
-        float tc = 0.f, td = 0.f;
-        for (int kk = 0; kk < T; ++kk) {
-          tc += cw[kk * w + threadIdx.x];
-          td += cw[kThreads + kk * w + threadIdx.x];
-        }
-        cacc[0] += tc;
-        dacc[0] += td;
-      }
-    } else {
-#pragma unroll
-      for (int m = 0; m < kCols; ++m) {
-        const int c = threadIdx.x + m * kThreads;
-        if (c < w) {
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f, e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
-          int rr = 0;
-          for (; rr + 4 <= rows; rr += 4) {
-            const float q0 = stage[rr * w + c], q1 = stage[(rr + 1) * w + c];
-            const float q2 = stage[(rr + 2) * w + c], q3 = stage[(rr + 3) * w + c];
-            s0 += q0; s1 += q1; s2 += q2; s3 += q3;
-            e0 = fmaf(q0, rinv[rr], e0); e1 = fmaf(q1, rinv[rr + 1], e1);
-            e2 = fmaf(q2, rinv[rr + 2], e2); e3 = fmaf(q3, rinv[rr + 3], e3);
-          }
-          for (; rr < rows; ++rr) {
-            const float q = stage[rr * w + c];
-            s0 += q;
-            e0 = fmaf(q, rinv[rr], e0);
-          }
-          cacc[m] += (s0 + s1) + (s2 + s3);
-          dacc[m] += (e0 + e1) + (e2 + e3);
-        }
-      }
-    }
-    __syncthreads();  // stage, rinv and cw are rewritten next
-  }
-  const int64_t off = (b * d.prb + q) * W;
-  float* cp = a.colpart + d.colpart + off;
-  float* dp = a.dpart + d.dpart + off;
-  if (T > 1) {
-    if (threadIdx.x < w) {
-      cp[threadIdx.x] = cacc[0];
-      dp[threadIdx.x] = dacc[0];
-    }
-  } else {
-#pragma unroll
-    for (int m = 0; m < kCols; ++m) {
-      const int c = threadIdx.x + m * kThreads;
-      if (c < w) {
-        cp[c] = cacc[m];
-        dp[c] = dacc[m];
-      }
-    }
-  }
-  const double rt = block_sum(static_cast<double>(rsum), red);
-  if (threadIdx.x == 0) a.rowchunk[d.rowchunk + b * d.nrc + q] = rt;
-  if (PSQ) {
-    const double ptot = block_sum(static_cast<double>(psq), red);
-    if (threadIdx.x == 0) a.ppart[d.p1_0 + local] = ptot;
-  }
-}
-
 template <typename GT, int VEC, bool PSQ>
 __device__ __forceinline__ void pass1_factored(const DevTensor& d, const StepArgs& a, int64_t local,
                                float* colbuf, double* red) {
@@ -692,28 +526,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_pass1_f(const __grid_constant__
     const int m = find_owner(pf, ng, u);
     const DevTensor d = a.tensors[member_tensor(r, m)];
     pass1_factored<GT, VEC, PSQ>(d, a, u - pf[m], colbuf, red);
-  }
-}
-
-// Shared memory of k_pass1_flat: the chunk stage, 1/row of the chunk's rows,
-// the column partials of T threads per column, CTA-sum scratch, prefix.
-constexpr size_t kFlatSmem = kColbufBytes + sizeof(float) * (2 * kTileRows + 2 * kThreads) + kRedBytes + kPrefixBytes;
-template <typename GT, bool PSQ>
-__global__ void __launch_bounds__(kThreads, kFlatMinB) k_pass1_flat(const __grid_constant__ StepArgs a, const Range r) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  float* stage = reinterpret_cast<float*>(smem);
-  float* rinv = stage + kWarps * kTileCols;
-  float* rold = rinv + kTileRows;
-  float* cw = rold + kTileRows;
-  double* red = reinterpret_cast<double*>(cw + 2 * kThreads);
-  int32_t* pf = reinterpret_cast<int32_t*>(smem + kColbufBytes + sizeof(float) * (2 * kTileRows + 2 * kThreads) +
-                                           kRedBytes);
-  const int ng = load_prefix(pf, r);
-  const int64_t u1 = pf[ng];
-  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
-    const int m = find_owner(pf, ng, u);
-    const DevTensor d = a.tensors[member_tensor(r, m)];
-    pass1_flat_fused<GT, PSQ>(d, a, u - pf[m], stage, rinv, rold, cw, red);
   }
 }
 
@@ -1824,6 +1636,372 @@ __device__ __forceinline__ double consumer_sum(float v, double* red) {
   return s;
 }
 
+// ---- fused flat pass 1 (kFactoredFlat) ------------------------------------
+// Tensors whose rows fit one tile (W <= kTileCols): a work unit is a chunk of
+// d.pr whole rows [i0, i1) of one slice (chosen by the planner so that a
+// unit holds about 64K values), so the row statistic can be formed in pass 1,
+// and with it D_j = sum_i g_ij^2 / row_i, as in the row-panel pass:
+// sum(u^2) = mean(row) * sum_j D_j / col_j (k_stats, k_scalars), and g is
+// read once for the statistics and sum(u^2) instead of twice (no pass 2).
+//
+// A unit's rows are one contiguous range of g.  One producer thread streams
+// it, in chunks of R whole rows (at most kFlatChunkBytes, chunk starts on
+// 16-byte boundaries), with cp.async.bulk into a ring of kFlatSlots slots;
+// the 8 consumer warps read the rows back from shared memory.  Each row is
+// taken by a segment of L = min(32, p) lanes (p the power of 2 >= W; 32 / L
+// rows per warp at once), lane c of the segment holding columns c, c + L, ...
+// (CPL = ceil(W / L) <= 16 of them).  Rows wider than 512 values are split
+// between the two warps of a pair (warps w and w + 4): columns [0, 512) and
+// [512, W), 16 per lane each; the pair adds its two half-row sums (low half
+// first) through shared memory at a named barrier of its own.  Warp w (pair
+// p) takes row groups w, w + 8 (p, p + 4), ... of every chunk.  Per row: the
+// segment's xor-butterfly gives every lane the same total (each level adds
+// the same two values, in either order), hence the same row EMA and
+// 1 / row_i; each lane then adds its values to C_j and g^2 / row_i to D_j in
+// registers.  The old row statistics of a warp's rows in a chunk are loaded
+// one chunk ahead, one per lane.  At the unit's end the warps' (pairs')
+// column partials meet in shared memory and are added in warp (pair) order,
+// while the producer already streams the next unit.  The values past a
+// slice's last 16-byte boundary (fewer than 16 bytes) are read from global
+// memory by their lanes.  All orders are fixed, so two runs give bit-identical
+// results.  Every wait is bounded as in k_apply_tma.
+constexpr int kFlatChunkBytes = 16384;         // one ring slot
+constexpr int kFlatSlots = 4;                  // ring slots
+constexpr int kFlatHalfW = 512;                // widest row one warp takes
+constexpr int kFlatPairs = kWarps / 2;         // warp pairs of the wide form
+constexpr int kFlatThreads = (kWarps + 1) * 32;  // 8 consumer warps + the producer warp
+constexpr int kFlatMinB = 2;                   // CTAs per SM
+// Named barrier 2 + pair, the pair's two warps only (barrier 1 is the
+// consumers' barrier).
+__device__ __forceinline__ void pair_sync(int pair) {
+  static_assert(kFlatPairs == 4, "one named barrier per pair");
+  switch (pair) {
+    case 0: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+    case 1: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+    case 2: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+    default: asm volatile("bar.sync 5, 64;" ::: "memory"); break;
+  }
+}
+// Rows per chunk for rows of w values: as many whole rows as fit one slot
+// (at most kTileRows), a multiple of the rows that keep every chunk start on
+// a 16-byte boundary (16 / gcd(16, w * sizeof(GT)) rows).
+template <typename GT>
+__device__ __forceinline__ int flat_chunk_rows(int w) {
+  constexpr int A = 16 / static_cast<int>(sizeof(GT));  // values per 16 bytes
+  const int low = w & -w;                               // largest power of 2 dividing w
+  const int rmin = A / (low < A ? low : A);
+  int R = kFlatChunkBytes / static_cast<int>(sizeof(GT)) / w;
+  if (R > kTileRows) R = kTileRows;
+  return R - R % rmin;
+}
+// One gradient value from shared memory, widened to fp32.
+template <typename GT> __device__ __forceinline__ float smem_val(const GT* p);
+template <> __device__ __forceinline__ float smem_val<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float smem_val<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+}
+// A unit of the flat pass: slice b, chunk q of d.pr rows from row i0.
+struct FlatUnit {
+  int64_t b, q, i0;
+  int w, nr;
+  int cnt, cpy;  // values of the unit; those before its last 16-byte boundary
+};
+template <typename GT>
+__device__ __forceinline__ FlatUnit flat_unit(const DevTensor* d, int64_t local) {
+  FlatUnit f;
+  f.b = local / d->prb;
+  f.q = local % d->prb;
+  f.i0 = f.q * d->pr;
+  f.w = static_cast<int>(d->W);
+  f.nr = static_cast<int>(min(d->H, f.i0 + d->pr) - f.i0);
+  f.cnt = f.nr * f.w;  // at most kTileRows * kTileCols
+  f.cpy = f.cnt & ~(16 / static_cast<int>(sizeof(GT)) - 1);
+  return f;
+}
+
+template <typename GT>
+__device__ __forceinline__ void flat_produce(const StepArgs& a, const Range& r, const int32_t* pf, int ng,
+                                             unsigned char* ring, uint64_t* full, uint64_t* empty) {
+  if (a.stall_copies) return;  // testing hook: the consumers' waits run out
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor* d = a.tensors + member_tensor(r, m);
+    const FlatUnit f = flat_unit<GT>(d, u - pf[m]);
+    const int R = flat_chunk_rows<GT>(f.w);
+    const GT* g = static_cast<const GT*>(d->g) + (f.b * d->H + f.i0) * f.w;
+    for (int r0 = 0; r0 < f.nr; r0 += R, ++it) {
+      const uint32_t slot = it % kFlatSlots, ph = (it / kFlatSlots) & 1u;
+      if (!mbar_wait(&empty[slot], ph ^ 1u)) {
+        atomicOr(a.status, kStatusWaitTimeout);
+        return;
+      }
+      const int e0 = r0 * f.w, e1 = min(min(r0 + R, f.nr) * f.w, f.cpy);
+      const uint32_t bytes = e1 > e0 ? static_cast<uint32_t>(e1 - e0) * static_cast<uint32_t>(sizeof(GT)) : 0u;
+      mbar_arrive_expect_tx(&full[slot], bytes);
+      if (bytes) bulk_g2s(ring + slot * kFlatChunkBytes, g + e0, bytes, &full[slot]);
+    }
+  }
+}
+
+// One unit's rows on the consumer side (CPL columns per lane; HALF: the
+// pair form).  `it` counts the ring's chunks; `dead` is set after a wait ran
+// out (the warp then keeps the control flow, for the pair barriers, but
+// neither waits nor reads).
+template <typename GT, int CPL, bool PSQ, bool HALF>
+__device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs& a, int64_t local,
+                                             const unsigned char* ring, uint64_t* full, uint64_t* empty, float* cw,
+                                             float* xs, double* red, uint32_t& it, bool& dead, int* stop) {
+  // Fields are read where they are used (dt is not restrict: the stores in
+  // between make the compiler read the epilogue's fields again instead of
+  // holding them in registers across the row loop).
+  const DevTensor& d = *dt;
+  static_assert(!HALF || CPL == 16, "a half row is 512 columns, 16 per lane");
+  constexpr int NS = HALF ? kFlatPairs : kWarps;     // column-partial sets
+  constexpr int CS = HALF ? kTileCols : kFlatHalfW;  // columns per set
+  const FlatUnit f = flat_unit<GT>(dt, local);
+  const int w = f.w, nr = f.nr;
+  const int R = flat_chunk_rows<GT>(w);
+  const GT* gt = static_cast<const GT*>(d.g) + (f.b * d.H + f.i0) * w;
+  float* rowst = d.row + f.b * d.H + f.i0;
+  int lg = 5;  // W > 32 whenever CPL > 1
+  if (CPL == 1)
+    while (lg > 0 && (1 << (lg - 1)) >= w) --lg;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int half = HALF ? warp / kFlatPairs : 0;   // column half of the wide form
+  const int set = HALF ? warp % kFlatPairs : warp;  // pair (wide form) or warp
+  const int sub = lane >> lg, cl = lane & ((1 << lg) - 1);
+  const int c0 = half * kFlatHalfW + cl;  // this lane's first column
+  const int spg = 32 >> lg;               // rows per row group
+  const int nk = c0 < w ? (w - c0 + (1 << lg) - 1) >> lg : 0;  // this lane's columns per row
+  const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
+  const float eps1 = static_cast<float>(a.eps1);
+  const float invw = 1.0f / static_cast<float>(w);
+  // lane j holds the old row statistic of this warp's j-th row of a chunk:
+  // row group set + (j / spg) * NS, row j % spg of the group (at most 32 rows)
+  auto load_rold = [&](int r0) {
+    const int rows = min(R, nr - r0);
+    const int rl = (set + (lane / spg) * NS) * spg + lane % spg;
+    return rl < rows ? rowst[r0 + rl] : 0.f;
+  };
+
+  // column sums in pairs of columns (k, k + 1): packed fp32x2 arithmetic
+  constexpr int NP = (CPL + 1) / 2;
+  float2 cacc[NP], dacc[NP];
+#pragma unroll
+  for (int k = 0; k < NP; ++k) cacc[k] = dacc[k] = make_float2(0.f, 0.f);
+  float rsum = 0.f;
+  int parity = 0;  // exchange buffer of the wide form
+  float rcur = load_rold(0);
+#pragma unroll 1
+  for (int r0 = 0; r0 < nr; r0 += R, ++it) {
+    const int rows = min(R, nr - r0);
+    const float rnext = r0 + R < nr ? load_rold(r0 + R) : 0.f;
+    const uint32_t slot = it % kFlatSlots, ph = (it / kFlatSlots) & 1u;
+    if (!dead && !mbar_wait(&full[slot], ph)) {
+      if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+      *stop = 1;
+      dead = true;
+    }
+    const GT* sb = reinterpret_cast<const GT*>(ring + slot * kFlatChunkBytes);
+    // a chunk that reaches past the unit's last 16-byte boundary is read
+    // from global memory (only the last chunk of a slice)
+    const bool from_g = (r0 + rows) * w > f.cpy;
+    const int ngc = (rows + spg - 1) / spg;  // row groups in the chunk
+#pragma unroll 1
+    for (int gi = set, t = 0; gi < ngc; gi += NS, ++t) {
+      const int rl = gi * spg + sub;  // row within the chunk
+      const bool ok = rl < rows && !dead;
+      float x[2 * NP];
+      x[2 * NP - 1] = 0.f;
+      if (from_g) {
+        const GT* src = gt + (r0 + rl) * w + c0;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) x[k] = (ok && k < nk) ? load_g_scalar<GT>(src + (k << lg)) : 0.f;
+      } else {
+        // CPL is ceil(W / 32) rounded up to even, so every lane holds columns
+        // k < CPL - 2 of a row; only the last two need the lane's count
+        // (narrow rows and the upper half of the pair form: all of them)
+        const GT* src = sb + rl * w + c0;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+          const bool v = (HALF || CPL < 4 || k >= CPL - 2) ? (ok && k < nk) : ok;
+          x[k] = v ? smem_val<GT>(src + (k << lg)) : 0.f;
+        }
+      }
+      float2 q[NP];
+      float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < NP; ++m) {
+        const float2 xv = make_float2(x[2 * m], x[2 * m + 1]);
+        q[m] = __fmul2_rn(xv, xv);
+        s2 = __fadd2_rn(s2, q[m]);
+      }
+      float s = s2.x + s2.y;
+      for (int o = (1 << lg) >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (HALF) {
+        // the pair's two half-row sums, low half first in both warps
+        if (lane == 0) xs[parity * kWarps + warp] = s;
+        pair_sync(set);
+        const float other = xs[parity * kWarps + (warp ^ kFlatPairs)];
+        s = half == 0 ? s + other : other + s;
+        parity ^= 1;
+      }
+      const float ro = __shfl_sync(0xffffffffu, rcur, t * spg + sub);
+      float ri = 0.f;
+      if (ok) {
+        const float rn = fmaf(b2, ro, omb2 * fmaf(s, invw, eps1));
+        ri = __frcp_rn(rn);  // correctly rounded 1 / rn
+        if (cl == 0 && half == 0) {
+          rowst[r0 + rl] = rn;
+          rsum += rn;
+        }
+      }
+      const float2 ri2 = make_float2(ri, ri);
+#pragma unroll
+      for (int m = 0; m < NP; ++m) {
+        cacc[m] = __fadd2_rn(cacc[m], q[m]);
+        dacc[m] = __ffma2_rn(q[m], ri2, dacc[m]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && !dead) mbar_arrive(&empty[slot]);
+    rcur = rnext;
+  }
+  // narrow rows: add the warp's row segments column by column (lanes with
+  // the same column differ in the bits above lg)
+  if (lg < 5) {
+    for (int o = 16; o >= (1 << lg); o >>= 1) {
+      cacc[0].x += __shfl_xor_sync(0xffffffffu, cacc[0].x, o);
+      dacc[0].x += __shfl_xor_sync(0xffffffffu, dacc[0].x, o);
+    }
+  }
+  float psq = 0.f;
+  if (PSQ && !dead) {
+    const float* pt = d.p + (f.b * d.H + f.i0) * w;
+    for (int e0 = threadIdx.x; e0 < f.cnt; e0 += 8 * kThreads) {
+      float y[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = e0 + k * kThreads;
+        y[k] = e < f.cnt ? __ldcs(pt + e) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) psq = fmaf(y[k], y[k], psq);
+    }
+  }
+  // the column partials, C then D, through cw[set][j]
+  const int64_t off = (f.b * d.prb + f.q) * w;
+  consumer_sync<kWarps>();  // cw of the previous unit is read
+  if (sub == 0) {
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      const int j = c0 + (k << lg);
+      if (j < w) cw[set * CS + j] = (k & 1) ? cacc[k >> 1].y : cacc[k >> 1].x;
+    }
+  }
+  const double rw = warp_sum(static_cast<double>(rsum));
+  const double pw = PSQ ? warp_sum(static_cast<double>(psq)) : 0.0;
+  if (lane == 0) {
+    red[warp] = rw;
+    if (PSQ) red[kWarps + warp] = pw;  // red holds 2 * kWarps doubles
+  }
+  consumer_sync<kWarps>();
+  float* cp = a.colpart + d.colpart + off;
+  for (int j = threadIdx.x; j < w; j += kThreads) {
+    float tc = 0.f;
+#pragma unroll
+    for (int v = 0; v < NS; ++v) tc += cw[v * CS + j];
+    cp[j] = tc;
+  }
+  if (threadIdx.x == 0 && !*stop) {
+    double rt = 0.0, pt2 = 0.0;
+#pragma unroll
+    for (int v = 0; v < kWarps; ++v) {
+      rt += red[v];
+      if (PSQ) pt2 += red[kWarps + v];
+    }
+    a.rowchunk[d.rowchunk + f.b * d.nrc + f.q] = rt;
+    if (PSQ) a.ppart[d.p1_0 + local] = pt2;
+  }
+  consumer_sync<kWarps>();
+  if (sub == 0) {
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      const int j = c0 + (k << lg);
+      if (j < w) cw[set * CS + j] = (k & 1) ? dacc[k >> 1].y : dacc[k >> 1].x;
+    }
+  }
+  consumer_sync<kWarps>();
+  float* dp = a.dpart + d.dpart + off;
+  for (int j = threadIdx.x; j < w; j += kThreads) {
+    float td = 0.f;
+#pragma unroll
+    for (int v = 0; v < NS; ++v) td += cw[v * CS + j];
+    dp[j] = td;
+  }
+}
+
+// Shared memory of k_pass1_flat: the ring, the column partials (8 sets of
+// 512 columns or 4 pairs of 1024), the pair exchange (2 buffers x 8 warps),
+// CTA-sum scratch (2 x 8 doubles), mbarriers, member prefix.
+constexpr size_t kFlatRing = static_cast<size_t>(kFlatChunkBytes) * kFlatSlots;
+constexpr size_t kFlatCw = sizeof(float) * kWarps * kFlatHalfW;
+constexpr size_t kFlatXs = sizeof(float) * 2 * kWarps;
+constexpr size_t kFlatSmem = kFlatRing + kFlatCw + kFlatXs + kRedBytes + sizeof(uint64_t) * 2 * kFlatSlots +
+                             kPrefixBytes;
+static_assert(kWarps * kFlatHalfW == kFlatPairs * kTileCols && kRedBytes >= sizeof(double) * 2 * kWarps &&
+                  (kFlatRing + kFlatCw + kFlatXs) % 8 == 0,
+              "shared-memory layout of the flat pass");
+template <typename GT, bool PSQ>
+__global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
+    k_pass1_flat(const __grid_constant__ StepArgs a, const Range r) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  float* cw = reinterpret_cast<float*>(smem + kFlatRing);
+  float* xs = reinterpret_cast<float*>(smem + kFlatRing + kFlatCw);
+  double* red = reinterpret_cast<double*>(smem + kFlatRing + kFlatCw + kFlatXs);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + kRedBytes / sizeof(double));
+  uint64_t* empty = full + kFlatSlots;
+  int32_t* pf = reinterpret_cast<int32_t*>(empty + kFlatSlots);
+  __shared__ int stop;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) stop = 0;
+  const int ng = tma_setup<kFlatSlots, kWarps>(pf, r, full, empty);
+  if (warp == kWarps) {
+    if (lane == 0) flat_produce<GT>(a, r, pf, ng, ring, full, empty);
+    return;
+  }
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  bool dead = false;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor* d = a.tensors + member_tensor(r, m);
+    const int64_t local = u - pf[m];
+    // columns per lane, rounded up to even (whole rows per warp up to 512)
+    const int64_t cpl = (d->W + 31) / 32;
+#define MEO_FLAT(C, HF) flat_consume<GT, C, PSQ, HF>(d, a, local, ring, full, empty, cw, xs, red, it, dead, &stop)
+    switch (cpl) {
+      case 1: MEO_FLAT(1, false); break;
+      case 2: MEO_FLAT(2, false); break;
+      case 3: case 4: MEO_FLAT(4, false); break;
+      case 5: case 6: MEO_FLAT(6, false); break;
+      case 7: case 8: MEO_FLAT(8, false); break;
+      case 9: case 10: MEO_FLAT(10, false); break;
+      case 11: case 12: MEO_FLAT(12, false); break;
+      case 13: case 14: MEO_FLAT(14, false); break;
+      case 15: case 16: MEO_FLAT(16, false); break;
+      default: MEO_FLAT(16, true); break;
+    }
+#undef MEO_FLAT
+    consumer_sync<kWarps>();  // stop is settled for every consumer
+    if (stop) break;
+  }
+  if (stop && threadIdx.x == 0) tma_drain<kFlatSlots>(full, it);
+}
+
 // ---- fused pass 1 over row chunks (kFactoredRows) --------------------------
 // The shared row-panel pass (row_panel.cuh) over chunks of d.pr full rows:
 // the updated row statistic, the column partials C_j of g^2 and D_j of
@@ -2104,6 +2282,185 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
   if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
 }
 
+// ---- apply of the flat class: bulk-copy staged runs of whole rows ---------
+// A flat tile (whole rows [i0, i1) of one slice, W <= kTileCols) is one
+// contiguous range of (i1 - i0) * W values of g, p (and exp_avg).  The
+// producer cuts it into pieces of kTileCols values and streams them into the
+// ring of k_apply_tma (kTmaRows pieces per stage); consumer warp w takes
+// piece w of every stage.  Lane l handles the quads k*256 + h*128 + 4l of its
+// piece: the quad's first (row, column) comes from its flat index
+// (flat_row), the other three by stepping along the row.  A tile's copies
+// stop at its last multiple of kFlatAlign<GT> values (16-byte pieces); the
+// up to kFlatAlign - 1 values after that, at the end of a slice only, are
+// read and written with plain loads and stores by the last piece's warp.
+// Waits are bounded as in k_apply_tma.
+template <typename GT> constexpr int64_t kFlatAlign = 16 / sizeof(GT);  // 4 fp32, 8 bf16 values
+
+template <typename GT, class RG>
+__device__ __forceinline__ void tma_produce_flat(const StepArgs& a, const Range& r, const int32_t* pf, int ng,
+                                                 unsigned char* ring, uint64_t* full, uint64_t* empty) {
+  if (a.stall_copies) return;  // testing hook: the consumers' waits run out
+  constexpr int64_t kPiece = kTileCols, kSpan = kTmaRows * kTileCols;
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const int m = find_owner(pf, ng, u);
+    const DevTensor d = a.tensors[member_tensor(r, m)];
+    const TilePos tp = tile_pos(d, u - pf[m]);
+    const int64_t i0 = tp.r * kTileRows, i1 = min(d.H, i0 + kTileRows);
+    const int64_t o = tp.b * d.H * d.W + i0 * d.W;
+    const int64_t cnt = (i1 - i0) * d.W, cpy = cnt & ~(kFlatAlign<GT> - 1);
+    const GT* g = static_cast<const GT*>(d.g) + o;
+    const float* p = d.p + o;
+    const float* mm = RG::kM ? d.m1 + o : nullptr;
+    for (int64_t e0 = 0; e0 < cnt; e0 += kSpan, ++it) {
+      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+      if (!mbar_wait(&empty[slot], ph ^ 1u)) {
+        atomicOr(a.status, kStatusWaitTimeout);
+        return;
+      }
+      const int64_t e1 = min(cpy, e0 + kSpan);
+      const uint32_t per_value = static_cast<uint32_t>(sizeof(GT) + (RG::kP ? 4 : 0) + (RG::kM ? 4 : 0));
+      mbar_arrive_expect_tx(&full[slot], e1 > e0 ? static_cast<uint32_t>(e1 - e0) * per_value : 0u);
+      unsigned char* st = ring + slot * RG::kStage;
+      for (int rr = 0; rr < kTmaRows; ++rr) {
+        const int64_t s0 = e0 + rr * kPiece;
+        if (s0 >= e1) break;
+        const uint32_t n = static_cast<uint32_t>(min(kPiece, e1 - s0));
+        unsigned char* row = st + rr * RG::kRow;
+        bulk_g2s(row, g + s0, n * sizeof(GT), &full[slot]);
+        if (RG::kP) bulk_g2s(row + RG::kG, p + s0, n * 4, &full[slot]);
+        if (RG::kM) bulk_g2s(row + RG::kG + RG::kP, mm + s0, n * 4, &full[slot]);
+      }
+    }
+  }
+}
+
+template <typename GT, bool B1, bool PSQ>
+__global__ void __launch_bounds__(TmaCfg<1>::kThreads, 1)
+    k_apply_tma_flat(const __grid_constant__ StepArgs a, const Range r) {
+  constexpr int NC = TmaCfg<1>::kConsumers;
+  constexpr int64_t kSpan = kTmaRows * kTileCols;
+  using RG = ApplyRing<GT, B1>;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* ring = smem;
+  float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // coef * col_j^-1/2
+  float* rowf = colf + kTileCols;                              // (row_i / mean(row))^-1/2
+  double* red = reinterpret_cast<double*>(rowf + kTileRows);  // NC <= 32 warp sums
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 32);
+  uint64_t* empty = full + RG::kStages;
+  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
+  __shared__ int stop;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = tma_setup<RG::kStages, NC>(pf, r, full, empty);
+  if (warp == NC) {
+    if (lane == 0) tma_produce_flat<GT, RG>(a, r, pf, ng, ring, full, empty);
+    return;
+  }
+  if (threadIdx.x == 0) stop = 0;
+  const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
+  const int64_t u1 = pf[ng];
+  uint32_t it = 0;
+  TileStats<NC> next;  // one tile ahead, as in k_apply_tma
+  if (pf[0] + blockIdx.x < u1) tile_stats_load(next, a, r, pf, ng, pf[0] + blockIdx.x);
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
+    const TileStats<NC> cur = next;
+    const int t = cur.t;
+    const DevTensor d = a.tensors[t];
+    const TilePos tp = tile_pos(d, cur.local);
+    const int64_t H = d.H, W = d.W;
+    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
+    const int64_t o = tp.b * H * W + i0 * W;
+    // Within a tile, flat indices stay below kTileRows * kTileCols: int.
+    const int cnt = static_cast<int>((i1 - i0) * W);
+    const int cpy = cnt & ~static_cast<int>(kFlatAlign<GT> - 1);
+    const int w = static_cast<int>(W);
+    const float invw = 1.0f / static_cast<float>(w);
+    const float wda = static_cast<float>(a.wd * a.alpha[t]);
+    consumer_sync<NC>();  // stop is settled; colf / rowf / red of the previous tile are read
+    if (stop) break;
+#pragma unroll
+    for (int q = 0; q < TileStats<NC>::kCols; ++q) {
+      const int cl = threadIdx.x + q * NC * 32;
+      colf[cl] = (cl < w) ? cur.coef * rsqrtf(cur.col[q]) : 0.f;
+    }
+    if (threadIdx.x < kTileRows) rowf[threadIdx.x] = (i0 + threadIdx.x < i1) ? rsqrtf(cur.row / cur.mr) : 0.f;
+    consumer_sync<NC>();
+    if (u + gridDim.x < u1) tile_stats_load(next, a, r, pf, ng, u + gridDim.x);
+    const GT* gt = static_cast<const GT*>(d.g) + o;
+    float* pt = d.p + o;
+    float* mt = B1 ? d.m1 + o : nullptr;
+    float psq = 0.f;
+    bool ok = true;
+    for (int e0 = 0; e0 < cnt && ok; e0 += static_cast<int>(kSpan), ++it) {
+      const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
+      if (!tma_acquire(&full[slot], ph, a, &stop)) {
+        ok = false;
+        break;
+      }
+      const int s0 = e0 + warp * kTileCols;  // this warp's piece
+      if (s0 < cnt) {
+        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
+        const int nc = s0 < cpy ? min(kTileCols, cpy - s0) : 0;  // staged values (whole quads)
+#pragma unroll
+        for (int k = 0; k < kTileCols / 256; ++k) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cl = k * 256 + h * 128 + lane * 4;
+            if (cl < nc) {
+              float x[4];
+              quad_g<GT>(x, row, cl);
+              float4 pv = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
+              float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (B1) mv = *reinterpret_cast<const float4*>(row + RG::kG + RG::kP + cl * 4);
+              float* pp = &pv.x;
+              float* mp = &mv.x;
+              const int e = s0 + cl;
+              int i = flat_row(e, invw), j = e - i * w;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float upd = (x[v] * rowf[i]) * colf[j];
+                if (B1) {
+                  mp[v] = fmaf(b1, mp[v], omb1 * upd);
+                  upd = mp[v];
+                }
+                const float pn = fmaf(-wda, pp[v], pp[v] - upd);
+                pp[v] = pn;
+                if (PSQ) psq = fmaf(pn, pn, psq);
+                flat_next(i, j, w);
+              }
+              __stcs(reinterpret_cast<float4*>(pt + e), pv);
+              if (B1) __stcs(reinterpret_cast<float4*>(mt + e), mv);
+            }
+          }
+        }
+        // values past the last 16-byte piece of the tile (end of a slice)
+        const int e = s0 + nc + lane;
+        if (nc < kTileCols && e < cnt && e >= cpy) {
+          const int i = flat_row(e, invw), j = e - i * w;
+          float upd = (load_g_scalar<GT>(gt + e) * rowf[i]) * colf[j];
+          if (B1) {
+            const float mn = fmaf(b1, mt[e], omb1 * upd);
+            mt[e] = mn;
+            upd = mn;
+          }
+          const float pv = pt[e];
+          const float pn = fmaf(-wda, pv, pv - upd);
+          pt[e] = pn;
+          if (PSQ) psq = fmaf(pn, pn, psq);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (PSQ) {
+      const double tot = consumer_sum<NC>(psq, red);
+      if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + cur.local] = tot;
+    }
+  }
+  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
+}
+
 // ---- psq: sum(p_new^2) carry, one CTA per tensor --------------------------
 __global__ void __launch_bounds__(kThreads) k_psq(const __grid_constant__ StepArgs a) {
   __shared__ double red[16];
@@ -2196,15 +2553,25 @@ Inst pick_rows(KernelId k, bool psq_in, int mom, bool psq_out) {
   return x;
 }
 
-// The flat class: fused flat pass 1, no pass 2, the element-wise apply.
+// The flat class: fused flat pass 1, no pass 2, the bulk-copy flat apply
+// (the element-wise apply, row by row, with the 8-bit moment).
 template <typename GT>
 Inst pick_flat(KernelId k, bool psq_in, int mom, bool psq_out) {
   Inst x;
   if (k == kKPass1) {
     x.fn = psq_in ? k_pass1_flat<GT, true> : k_pass1_flat<GT, false>;
+    x.threads = kFlatThreads;
     x.smem = kFlatSmem;
   } else if (k == kKApply) {
-    x = pick_f<GT, 1>(k, psq_in, mom, psq_out);
+    if (mom == 2) return pick_f<GT, 1>(k, psq_in, mom, psq_out);
+    x.threads = TmaCfg<1>::kThreads;
+    if (mom == 1) {
+      x.fn = psq_out ? k_apply_tma_flat<GT, true, true> : k_apply_tma_flat<GT, true, false>;
+      x.smem = tma_smem<ApplyRing<GT, true>>(kFactorBytes);
+    } else {
+      x.fn = psq_out ? k_apply_tma_flat<GT, false, true> : k_apply_tma_flat<GT, false, false>;
+      x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
+    }
   }
   return x;
 }
@@ -2236,18 +2603,25 @@ Inst pick(KernelId k, TensorClass c, bool psq_in, int mom, bool psq_out) {
 
 }  // namespace
 
-int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err) {
-  // min over the instantiations of (kind, class) of (resident CTAs per SM) x
-  // SM count, cached per device.  Also raises the dynamic shared-memory limit
-  // of every instantiation that needs more than the 48 KB default.
-  constexpr int kMaxDev = 64;
-  static int cache[kMaxDev][kNumKernels][kNumClasses] = {};
+int kernel_variant(const StepArgs& a) {
+  const int psq_in = (a.scale_parameter && !a.psq_valid) ? 1 : 0;
+  const int mom = a.has_beta1 ? (a.q8 ? 2 : 1) : 0;
+  return psq_in + 2 * mom + (a.want_psq_out != 0 ? 6 : 0);
+}
+
+int kernel_grid_limit(KernelId k, TensorClass c, int variant, int device, cudaError_t* err) {
+  // (resident CTAs per SM) x SM count of the instantiation that (kind, class,
+  // variant) launches, cached per device.  Also raises the dynamic
+  // shared-memory limit of that instantiation where it needs more than the
+  // 48 KB default.
+  constexpr int kMaxDev = 64, kVariants = 12;
+  static int cache[kMaxDev][kNumKernels][kNumClasses][kVariants] = {};
   *err = cudaSuccess;
-  if (device < 0 || device >= kMaxDev) {
-    *err = cudaErrorInvalidDevice;
+  if (device < 0 || device >= kMaxDev || variant < 0 || variant >= kVariants) {
+    *err = device < 0 || device >= kMaxDev ? cudaErrorInvalidDevice : cudaErrorInvalidValue;
     return 0;
   }
-  if (cache[device][k][c] > 0) return cache[device][k][c];
+  if (cache[device][k][c][variant] > 0) return cache[device][k][c][variant];
   int sms = 0;
   *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (*err != cudaSuccess) return 0;
@@ -2263,10 +2637,8 @@ int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err) {
     if (*err == cudaSuccess && b < per_sm) per_sm = b;
   };
   if (k == kKPass1 || k == kKPass2 || k == kKApply) {
-    for (int v = 0; v < 12; ++v) {
-      const Inst x = pick(k, c, v & 1, (v >> 1) % 3, v >= 6);
-      visit(reinterpret_cast<const void*>(x.fn), x.threads, x.smem);
-    }
+    const Inst x = pick(k, c, variant & 1, (variant >> 1) % 3, variant >= 6);
+    visit(reinterpret_cast<const void*>(x.fn), x.threads, x.smem);
   } else if (k == kKStats) {
     visit(reinterpret_cast<const void*>(k_stats), kThreads, kRedBytes + kPrefixBytes + kPartBytes);
   } else {
@@ -2275,15 +2647,15 @@ int kernel_grid_limit(KernelId k, TensorClass c, int device, cudaError_t* err) {
   if (*err != cudaSuccess) return 0;
   if (per_sm < 1) per_sm = 1;
   if (per_sm == (1 << 30)) per_sm = 1;
-  cache[device][k][c] = per_sm * sms;
-  return cache[device][k][c];
+  cache[device][k][c][variant] = per_sm * sms;
+  return cache[device][k][c][variant];
 }
 
 cudaError_t launch_stream(KernelId k, TensorClass c, const StepArgs& a, const Range& r, int grid,
                           cudaStream_t s) {
   if (grid <= 0 || r.m_end <= r.m_begin) return cudaSuccess;
-  const bool psq_in = a.scale_parameter && !a.psq_valid;
-  const Inst x = pick(k, c, psq_in, a.has_beta1 ? (a.q8 ? 2 : 1) : 0, a.want_psq_out != 0);
+  const int v = kernel_variant(a);
+  const Inst x = pick(k, c, v & 1, (v >> 1) % 3, v >= 6);
   if (x.fn == nullptr) return cudaErrorInvalidValue;
   x.fn<<<grid, x.threads, x.smem, s>>>(a, r);
   return cudaGetLastError();

@@ -70,6 +70,9 @@ SMALL_SHAPES = [(1, 1), (2, 3), (3, 2), (1, 5), (5, 1), (2, 2, 3), (4,), (), (60
                 # flat walk over whole rows (W <= 1024, not a multiple of 8): several
                 # staged chunks per tile and a ragged last chunk, 1..8-lane row segments
                 (700, 33), (300, 1023), (513, 7), (260, 1), (1030, 3),
+                # 2, 4, 8 and 16 columns per lane in registers (W <= 512), and the
+                # staged form just above
+                (130, 100), (91, 200), (50, 512), (40, 513), (33, 32), (17, 16),
                 # bf16: fused row-chunk pass, 8-warp configuration (2048 <= W <= 4096): a
                 # one-lane last column group, two chunks with a ragged one, B = 2 slices
                 (300, 2056), (2, 130, 4096),
