@@ -139,12 +139,20 @@ template <> __device__ __forceinline__ void store_f<1>(float* p, const float (&y
 struct TilePos {
   int64_t b, r, c;
 };
+// Unit indices and their divisors fit 32 bits (the planner's prefix arrays
+// are int32), and a 32-bit unsigned division is a short integer sequence,
+// where a 64-bit one goes through the FP64 pipe, which is slow on this part.
+__device__ __forceinline__ void udivmod32(int64_t n, int64_t d, int64_t& q, int64_t& r) {
+  const uint32_t nn = static_cast<uint32_t>(n), dd = static_cast<uint32_t>(d);
+  const uint32_t qq = nn / dd;
+  q = qq;
+  r = nn - qq * dd;
+}
 __device__ __forceinline__ TilePos tile_pos(const DevTensor& d, int64_t local) {
   TilePos t;
-  t.c = local % d.cb;
-  const int64_t q = local / d.cb;
-  t.r = q % d.rb;
-  t.b = q / d.rb;
+  int64_t q;
+  udivmod32(local, d.cb, q, t.c);
+  udivmod32(q, d.rb, t.b, t.r);
   return t;
 }
 
@@ -734,12 +742,14 @@ __global__ void __launch_bounds__(kThreads) k_stats(const __grid_constant__ Step
     const DevTensor d = a.tensors[member_tensor(r, m)];
     const int64_t local = u - pf[m];
     if (is_fused(d.kind)) {  // rows were updated by the fused pass 1
-      if (a.phase == 2) stats_col_global(d, a, local / d.ncc, local % d.ncc, red);
-      else stats_col_any(d, a, local / d.ncc, local % d.ncc, part, red);
+      int64_t b, k;
+      udivmod32(local, d.ncc, b, k);
+      if (a.phase == 2) stats_col_global(d, a, b, k, red);
+      else stats_col_any(d, a, b, k, part, red);
       continue;
     }
-    const int64_t per_slice = d.nrc + d.ncc;
-    const int64_t b = local / per_slice, k = local % per_slice;
+    int64_t b, k;
+    udivmod32(local, d.nrc + d.ncc, b, k);
     if (k < d.nrc) {
       if (a.phase != 2) stats_row_item(d, a, b, k, red);  // rows are local to a shard
     } else if (a.phase == 2) {
@@ -1709,8 +1719,7 @@ struct FlatUnit {
 template <typename GT>
 __device__ __forceinline__ FlatUnit flat_unit(const DevTensor* d, int64_t local) {
   FlatUnit f;
-  f.b = local / d->prb;
-  f.q = local % d->prb;
+  udivmod32(local, d->prb, f.b, f.q);
   f.i0 = f.q * d->pr;
   f.w = static_cast<int>(d->W);
   f.nr = static_cast<int>(min(d->H, f.i0 + d->pr) - f.i0);
@@ -1780,11 +1789,15 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
   const float invw = 1.0f / static_cast<float>(w);
   // lane j holds the old row statistic of this warp's j-th row of a chunk:
   // row group set + (j / spg) * NS, row j % spg of the group (at most 32 rows)
-  auto load_rold = [&](int r0) {
+  // (the groups of a chunk go round the warps starting where the previous
+  // chunk's left off, so a warp's extra rows move to the next warps chunk by
+  // chunk instead of always falling to the same ones)
+  auto load_rold = [&](int r0, int gi0) {
     const int rows = min(R, nr - r0);
-    const int rl = (set + (lane / spg) * NS) * spg + lane % spg;
+    const int rl = (gi0 + (lane / spg) * NS) * spg + lane % spg;
     return rl < rows ? rowst[r0 + rl] : 0.f;
   };
+  auto first_group = [&](int goff) { return (set - goff + NS) % NS; };
 
   // column sums in pairs of columns (k, k + 1): packed fp32x2 arithmetic
   constexpr int NP = (CPL + 1) / 2;
@@ -1793,11 +1806,15 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
   for (int k = 0; k < NP; ++k) cacc[k] = dacc[k] = make_float2(0.f, 0.f);
   float rsum = 0.f;
   int parity = 0;  // exchange buffer of the wide form
-  float rcur = load_rold(0);
+  int goff = 0;  // row groups of the unit's earlier chunks, mod NS
+  float rcur = load_rold(0, first_group(0));
 #pragma unroll 1
   for (int r0 = 0; r0 < nr; r0 += R, ++it) {
     const int rows = min(R, nr - r0);
-    const float rnext = r0 + R < nr ? load_rold(r0 + R) : 0.f;
+    const int ngc = (min(R, nr - r0) + spg - 1) / spg;  // row groups in the chunk
+    const int gi0 = first_group(goff);
+    const int goff_next = (goff + ngc) % NS;
+    const float rnext = r0 + R < nr ? load_rold(r0 + R, first_group(goff_next)) : 0.f;
     const uint32_t slot = it % kFlatSlots, ph = (it / kFlatSlots) & 1u;
     if (!dead && !mbar_wait(&full[slot], ph)) {
       if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
@@ -1808,9 +1825,8 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
     // a chunk that reaches past the unit's last 16-byte boundary is read
     // from global memory (only the last chunk of a slice)
     const bool from_g = (r0 + rows) * w > f.cpy;
-    const int ngc = (rows + spg - 1) / spg;  // row groups in the chunk
 #pragma unroll 1
-    for (int gi = set, t = 0; gi < ngc; gi += NS, ++t) {
+    for (int gi = gi0, t = 0; gi < ngc; gi += NS, ++t) {
       const int rl = gi * spg + sub;  // row within the chunk
       const bool ok = rl < rows && !dead;
       float x[2 * NP];
@@ -1868,6 +1884,7 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
     __syncwarp();
     if (lane == 0 && !dead) mbar_arrive(&empty[slot]);
     rcur = rnext;
+    goff = goff_next;
   }
   // narrow rows: add the warp's row segments column by column (lanes with
   // the same column differ in the bits above lg)
@@ -2285,9 +2302,10 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
 // ---- apply of the flat class: bulk-copy staged runs of whole rows ---------
 // A flat tile (whole rows [i0, i1) of one slice, W <= kTileCols) is one
 // contiguous range of (i1 - i0) * W values of g, p (and exp_avg).  The
-// producer cuts it into pieces of kTileCols values and streams them into the
-// ring of k_apply_tma (kTmaRows pieces per stage); consumer warp w takes
-// piece w of every stage.  Lane l handles the quads k*256 + h*128 + 4l of its
+// producer streams it in spans of kTmaRows * kTileCols values into the ring
+// of k_apply_tma, one copy per stream and span (a stage holds the span's g,
+// then its p, then its exp_avg); consumer warp w takes piece w (kTileCols
+// values) of every span.  Lane l handles the quads k*256 + h*128 + 4l of its
 // piece: the quad's first (row, column) comes from its flat index
 // (flat_row), the other three by stepping along the row.  A tile's copies
 // stop at its last multiple of kFlatAlign<GT> values (16-byte pieces); the
@@ -2300,7 +2318,7 @@ template <typename GT, class RG>
 __device__ __forceinline__ void tma_produce_flat(const StepArgs& a, const Range& r, const int32_t* pf, int ng,
                                                  unsigned char* ring, uint64_t* full, uint64_t* empty) {
   if (a.stall_copies) return;  // testing hook: the consumers' waits run out
-  constexpr int64_t kPiece = kTileCols, kSpan = kTmaRows * kTileCols;
+  constexpr int64_t kSpan = kTmaRows * kTileCols;
   const int64_t u1 = pf[ng];
   uint32_t it = 0;
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
@@ -2321,16 +2339,13 @@ __device__ __forceinline__ void tma_produce_flat(const StepArgs& a, const Range&
       }
       const int64_t e1 = min(cpy, e0 + kSpan);
       const uint32_t per_value = static_cast<uint32_t>(sizeof(GT) + (RG::kP ? 4 : 0) + (RG::kM ? 4 : 0));
-      mbar_arrive_expect_tx(&full[slot], e1 > e0 ? static_cast<uint32_t>(e1 - e0) * per_value : 0u);
+      const uint32_t n = e1 > e0 ? static_cast<uint32_t>(e1 - e0) : 0u;
+      mbar_arrive_expect_tx(&full[slot], n * per_value);
       unsigned char* st = ring + slot * RG::kStage;
-      for (int rr = 0; rr < kTmaRows; ++rr) {
-        const int64_t s0 = e0 + rr * kPiece;
-        if (s0 >= e1) break;
-        const uint32_t n = static_cast<uint32_t>(min(kPiece, e1 - s0));
-        unsigned char* row = st + rr * RG::kRow;
-        bulk_g2s(row, g + s0, n * sizeof(GT), &full[slot]);
-        if (RG::kP) bulk_g2s(row + RG::kG, p + s0, n * 4, &full[slot]);
-        if (RG::kM) bulk_g2s(row + RG::kG + RG::kP, mm + s0, n * 4, &full[slot]);
+      if (n) {
+        bulk_g2s(st, g + e0, n * sizeof(GT), &full[slot]);
+        if (RG::kP) bulk_g2s(st + kTmaRows * RG::kG, p + e0, n * 4, &full[slot]);
+        if (RG::kM) bulk_g2s(st + kTmaRows * (RG::kG + RG::kP), mm + e0, n * 4, &full[slot]);
       }
     }
   }
@@ -2342,6 +2357,7 @@ __global__ void __launch_bounds__(TmaCfg<1>::kThreads, 1)
   constexpr int NC = TmaCfg<1>::kConsumers;
   constexpr int64_t kSpan = kTmaRows * kTileCols;
   using RG = ApplyRing<GT, B1>;
+  static_assert(RG::kP == kTileCols * 4 && (!B1 || RG::kM == RG::kP), "stage layout: g, p, exp_avg blocks");
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* ring = smem;
   float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // coef * col_j^-1/2
@@ -2400,7 +2416,10 @@ __global__ void __launch_bounds__(TmaCfg<1>::kThreads, 1)
       }
       const int s0 = e0 + warp * kTileCols;  // this warp's piece
       if (s0 < cnt) {
-        const unsigned char* row = ring + slot * RG::kStage + warp * RG::kRow;
+        const unsigned char* st = ring + slot * RG::kStage;
+        const unsigned char* gs = st + warp * RG::kG;                                   // this piece's g
+        const unsigned char* ps = st + kTmaRows * RG::kG + warp * RG::kP;                // its p
+        const unsigned char* ms = st + kTmaRows * (RG::kG + RG::kP) + warp * RG::kP;     // its exp_avg
         const int nc = s0 < cpy ? min(kTileCols, cpy - s0) : 0;  // staged values (whole quads)
 #pragma unroll
         for (int k = 0; k < kTileCols / 256; ++k) {
@@ -2409,10 +2428,10 @@ __global__ void __launch_bounds__(TmaCfg<1>::kThreads, 1)
             const int cl = k * 256 + h * 128 + lane * 4;
             if (cl < nc) {
               float x[4];
-              quad_g<GT>(x, row, cl);
-              float4 pv = *reinterpret_cast<const float4*>(row + RG::kG + cl * 4);
+              quad_g<GT>(x, gs, cl);
+              float4 pv = *reinterpret_cast<const float4*>(ps + cl * 4);
               float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (B1) mv = *reinterpret_cast<const float4*>(row + RG::kG + RG::kP + cl * 4);
+              if (B1) mv = *reinterpret_cast<const float4*>(ms + cl * 4);
               float* pp = &pv.x;
               float* mp = &mv.x;
               const int e = s0 + cl;

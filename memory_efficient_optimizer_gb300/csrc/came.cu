@@ -238,12 +238,19 @@ struct Tile {
   int64_t b, r, c;  // slice, row tile, column tile
   int64_t i0, i1, j0;
 };
+// Unit indices and their divisors fit 32 bits (int32 prefix arrays); a
+// 32-bit unsigned division avoids the FP64 pipe that 64-bit division uses.
+__device__ __forceinline__ void udivmod32(int64_t n, int64_t d, int64_t& q, int64_t& r) {
+  const uint32_t nn = static_cast<uint32_t>(n), dd = static_cast<uint32_t>(d);
+  const uint32_t qq = nn / dd;
+  q = qq;
+  r = nn - qq * dd;
+}
 __device__ __forceinline__ Tile tile_of(const CDev& d, int64_t local) {
   Tile t;
-  t.c = local % d.cb;
-  const int64_t q = local / d.cb;
-  t.r = q % d.rb;
-  t.b = q / d.rb;
+  int64_t q;
+  udivmod32(local, d.cb, q, t.c);
+  udivmod32(q, d.rb, t.b, t.r);
   t.i0 = t.r * kTR;
   t.i1 = min(d.H, t.i0 + kTR);
   t.j0 = t.c * kTC;
@@ -383,7 +390,8 @@ __global__ void __launch_bounds__(NW * 32, MINB) k_came_panel(const __grid_const
   extern __shared__ __align__(16) unsigned char smem[];
   double* red = reinterpret_cast<double*>(smem + C::kBytes);
   walk_list(a, a.ppf[q], a.pidx[q], a.pnmem[q], [&](const CDev& d, int, int64_t local) {
-    const int64_t b = local / d.prb, chunk = local % d.prb;
+    int64_t b, chunk;
+    udivmod32(local, d.prb, b, chunk);
     const int32_t H = static_cast<int32_t>(d.H), W = static_cast<int32_t>(d.W);
     const int32_t c0 = static_cast<int32_t>(chunk) * d.pr, c1 = min(H, c0 + d.pr);
     const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(d.g) + b * d.H * d.W;
@@ -495,7 +503,8 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
     const bool panel0 = a.phase == 0 && d.panel != 0;  // rows done by the row-panel pass
     if (local < d.B * d.nrc) {
       if (panel0) continue;
-      const int64_t b = local / d.nrc, q = local % d.nrc;
+      int64_t b, q;
+      udivmod32(local, d.nrc, b, q);
       const int64_t i0 = q * kRowItem, i1 = min(d.H, i0 + kRowItem);
       double acc = 0.0;
       for (int64_t i = i0 + threadIdx.x; i < i1; i += kThreads) {
@@ -512,7 +521,8 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
       // column EMA from the chunks' sums of g^2, and this item's share of
       // sum_j D_j / c_j from the chunks' sums of g^2 / r_i
       const int64_t l2 = local - d.B * d.nrc;
-      const int64_t b = l2 / d.ncc, q = l2 % d.ncc;
+      int64_t b, q;
+      udivmod32(l2, d.ncc, b, q);
       const int64_t j = q * kColItem + threadIdx.x;
       const int64_t o = d.pcol + b * d.prb * d.W;  // panel tensors: W % 8 == 0
       double sc, sd;
@@ -528,7 +538,8 @@ __global__ void __launch_bounds__(kThreads) k_came_stats(const __grid_constant__
       if (threadIdx.x == 0) a.dsum[d.dsum0 + b * d.ncc + q] = tot;
     } else {
       const int64_t l2 = local - d.B * d.nrc;
-      const int64_t b = l2 / d.ncc, q = l2 % d.ncc;
+      int64_t b, q;
+      udivmod32(l2, d.ncc, b, q);
       const int64_t j = q * kColItem + threadIdx.x;
       const float* src = a.colpart + d.colpart + b * d.W;
       const bool vec = d.W % 8 == 0 && (d.colpart + b * d.W) % 4 == 0 && (d.B * d.W) % 4 == 0;
