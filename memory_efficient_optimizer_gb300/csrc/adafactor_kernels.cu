@@ -1761,7 +1761,8 @@ __device__ __forceinline__ void flat_produce(const StepArgs& a, const Range& r, 
 template <typename GT, int CPL, bool PSQ, bool HALF>
 __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs& a, int64_t local,
                                              const unsigned char* ring, uint64_t* full, uint64_t* empty, float* cw,
-                                             float* xs, double* red, uint32_t& it, bool& dead, int* stop) {
+                                             float* xs, double* red, uint32_t& it, bool& dead, int* stop,
+                                             const float3 bc) {
   // Fields are read where they are used (dt is not restrict: the stores in
   // between make the compiler read the epilogue's fields again instead of
   // holding them in registers across the row loop).
@@ -1784,8 +1785,7 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
   const int c0 = half * kFlatHalfW + cl;  // this lane's first column
   const int spg = 32 >> lg;               // rows per row group
   const int nk = c0 < w ? (w - c0 + (1 << lg) - 1) >> lg : 0;  // this lane's columns per row
-  const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
-  const float eps1 = static_cast<float>(a.eps1);
+  const float b2 = bc.x, omb2 = bc.y, eps1 = bc.z;
   const float invw = 1.0f / static_cast<float>(w);
   // lane j holds the old row statistic of this warp's j-th row of a chunk:
   // row group set + (j / spg) * NS, row j % spg of the group (at most 32 rows)
@@ -1918,8 +1918,9 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
       if (j < w) cw[set * CS + j] = (k & 1) ? cacc[k >> 1].y : cacc[k >> 1].x;
     }
   }
-  const double rw = warp_sum(static_cast<double>(rsum));
-  const double pw = PSQ ? warp_sum(static_cast<double>(psq)) : 0.0;
+  // (warp sums in fp32: the row statistics and p^2 of one warp's rows)
+  const double rw = warp_sum(rsum);
+  const double pw = PSQ ? warp_sum(psq) : 0.f;
   if (lane == 0) {
     red[warp] = rw;
     if (PSQ) red[kWarps + warp] = pw;  // red holds 2 * kWarps doubles
@@ -1993,13 +1994,17 @@ __global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
   const int64_t u1 = pf[ng];
   uint32_t it = 0;
   bool dead = false;
+  // beta2, 1 - beta2 and eps1 in fp32, once (conversions from fp64 run on
+  // the FP64 pipe, which is slow on this part)
+  const float3 bc = make_float3(static_cast<float>(a.beta2), static_cast<float>(1.0 - a.beta2),
+                                static_cast<float>(a.eps1));
   for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
     const int m = find_owner(pf, ng, u);
     const DevTensor* d = a.tensors + member_tensor(r, m);
     const int64_t local = u - pf[m];
     // columns per lane, rounded up to even (whole rows per warp up to 512)
     const int64_t cpl = (d->W + 31) / 32;
-#define MEO_FLAT(C, HF) flat_consume<GT, C, PSQ, HF>(d, a, local, ring, full, empty, cw, xs, red, it, dead, &stop)
+#define MEO_FLAT(C, HF) flat_consume<GT, C, PSQ, HF>(d, a, local, ring, full, empty, cw, xs, red, it, dead, &stop, bc)
     switch (cpl) {
       case 1: MEO_FLAT(1, false); break;
       case 2: MEO_FLAT(2, false); break;
