@@ -2316,7 +2316,11 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
 // stop at its last multiple of kFlatAlign<GT> values (16-byte pieces); the
 // up to kFlatAlign - 1 values after that, at the end of a slice only, are
 // read and written with plain loads and stores by the last piece's warp.
-// Waits are bounded as in k_apply_tma.
+// A tenth warp builds each tile's factor tables (coef * col_j^-1/2,
+// (row_i / mean)^-1/2) and geometry one or two tiles ahead in two table
+// slots, so the consumer warps never wait on one another: each waits for
+// its tile's table and its stages, and releases both.  Waits are bounded as
+// in k_apply_tma.
 template <typename GT> constexpr int64_t kFlatAlign = 16 / sizeof(GT);  // 4 fp32, 8 bf16 values
 
 template <typename GT, class RG>
@@ -2356,66 +2360,167 @@ __device__ __forceinline__ void tma_produce_flat(const StepArgs& a, const Range&
   }
 }
 
+// One flat tile's factors and geometry, built ahead by the table warp.
+struct FlatTab {
+  float colf[kTileCols];  // coef * col_j^-1/2
+  float rowf[kTileRows];  // (row_i / mean(row))^-1/2
+  double psq[kTmaRows];   // the consumer warps' sum(p_new^2) over the tile
+  const void* g;
+  float* p;
+  float* m;
+  int64_t ppart;  // the tile's entry of the sum(p^2) partials
+  float wda;      // wd * alpha
+  int w, cnt, cpy;
+};
+constexpr int kFlatTabs = 2;  // table slots
+constexpr int kFlatApplyThreads = (kTmaRows + 2) * 32;  // consumers, producer warp, table warp
+
+// The table warp: every tile of this CTA in turn, into table slot k % 2
+// once the consumers released it; before refilling a slot it adds the
+// consumer warps' sum(p^2) partials of the slot's previous tile in warp
+// order (and those of the last tiles at the end).
 template <typename GT, bool B1, bool PSQ>
-__global__ void __launch_bounds__(TmaCfg<1>::kThreads, 1)
+__device__ __forceinline__ void flat_tables(const StepArgs& a, const Range& r, const int32_t* pf, int ng,
+                                            FlatTab* tab, uint64_t* tfull, uint64_t* tempty) {
+  const int lane = threadIdx.x & 31;
+  const int64_t u1 = pf[ng];
+  uint32_t k = 0;
+  auto flush = [&](const FlatTab& T) {
+    if (PSQ && lane == 0) {
+      double tot = 0.0;
+#pragma unroll
+      for (int v = 0; v < kTmaRows; ++v) tot += T.psq[v];
+      a.ppart[T.ppart] = tot;
+    }
+  };
+  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x, ++k) {
+    const uint32_t s = k % kFlatTabs, ph = (k / kFlatTabs) & 1u;
+    if (!mbar_wait(&tempty[s], ph ^ 1u)) {
+      if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+      return;
+    }
+    FlatTab& T = tab[s];
+    if (k >= kFlatTabs) flush(T);
+    __syncwarp();
+    const int m = find_owner(pf, ng, u);
+    const int t = member_tensor(r, m);
+    const DevTensor* d = a.tensors + t;
+    const int64_t local = u - pf[m];
+    const TilePos tp = tile_pos(*d, local);
+    const int64_t H = d->H, W = d->W;
+    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
+    const int64_t o = tp.b * H * W + i0 * W;
+    const float coef = static_cast<float>(a.coef[t]);
+    const float mr = static_cast<float>(a.mrow[d->mslot + tp.b]);
+    const float* col = d->col + tp.b * W;
+    const float* row = d->row + tp.b * H + i0;
+    // all of the lane's loads first, so they are in flight together
+    float cv[kTileCols / 32], rv[kTileRows / 32];
+#pragma unroll
+    for (int q = 0; q < kTileCols / 32; ++q) {
+      const int j = lane + 32 * q;
+      cv[q] = j < W ? col[j] : 1.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kTileRows / 32; ++q) {
+      const int i = lane + 32 * q;
+      rv[q] = i0 + i < i1 ? row[i] : 1.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kTileCols / 32; ++q) {
+      const int j = lane + 32 * q;
+      T.colf[j] = j < W ? coef * rsqrtf(cv[q]) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kTileRows / 32; ++q) {
+      const int i = lane + 32 * q;
+      T.rowf[i] = i0 + i < i1 ? rsqrtf(rv[q] / mr) : 0.f;
+    }
+    if (lane == 0) {
+      T.g = static_cast<const GT*>(d->g) + o;
+      T.p = d->p + o;
+      T.m = B1 ? d->m1 + o : nullptr;
+      T.ppart = d->tile0 + local;
+      T.wda = static_cast<float>(a.wd * a.alpha[t]);
+      T.w = static_cast<int>(W);
+      T.cnt = static_cast<int>((i1 - i0) * W);  // at most kTileRows * kTileCols
+      T.cpy = T.cnt & ~static_cast<int>(kFlatAlign<GT> - 1);
+    }
+    mbar_arrive(&tfull[s]);  // every lane (count 32): its own writes are released
+  }
+  // the partials of the last tiles
+  for (uint32_t q = k > kFlatTabs ? k - kFlatTabs : 0; q < k; ++q) {
+    const uint32_t s = q % kFlatTabs, ph = (q / kFlatTabs) & 1u;
+    if (!mbar_wait(&tempty[s], ph)) {
+      if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+      return;
+    }
+    flush(tab[s]);
+  }
+}
+
+template <typename GT, bool B1, bool PSQ>
+__global__ void __launch_bounds__(kFlatApplyThreads, 1)
     k_apply_tma_flat(const __grid_constant__ StepArgs a, const Range r) {
-  constexpr int NC = TmaCfg<1>::kConsumers;
+  constexpr int NC = kTmaRows;  // consumer warps, one piece of a span each
   constexpr int64_t kSpan = kTmaRows * kTileCols;
   using RG = ApplyRing<GT, B1>;
   static_assert(RG::kP == kTileCols * 4 && (!B1 || RG::kM == RG::kP), "stage layout: g, p, exp_avg blocks");
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* ring = smem;
-  float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // coef * col_j^-1/2
-  float* rowf = colf + kTileCols;                              // (row_i / mean(row))^-1/2
-  double* red = reinterpret_cast<double*>(rowf + kTileRows);  // NC <= 32 warp sums
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 32);
+  FlatTab* tab = reinterpret_cast<FlatTab*>(smem + RG::kBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tab + kFlatTabs);
   uint64_t* empty = full + RG::kStages;
-  int32_t* pf = reinterpret_cast<int32_t*>(empty + RG::kStages);
-  __shared__ int stop;
+  uint64_t* tfull = empty + RG::kStages;
+  uint64_t* tempty = tfull + kFlatTabs;
+  int32_t* pf = reinterpret_cast<int32_t*>(tempty + kFlatTabs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ng = tma_setup<RG::kStages, NC>(pf, r, full, empty);
+  const int ng = load_prefix(pf, r);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RG::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NC);
+    }
+    for (int s = 0; s < kFlatTabs; ++s) {
+      mbar_init(&tfull[s], 32);
+      mbar_init(&tempty[s], NC);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
   if (warp == NC) {
     if (lane == 0) tma_produce_flat<GT, RG>(a, r, pf, ng, ring, full, empty);
     return;
   }
-  if (threadIdx.x == 0) stop = 0;
+  if (warp == NC + 1) {
+    flat_tables<GT, B1, PSQ>(a, r, pf, ng, tab, tfull, tempty);
+    return;
+  }
   const float b1 = static_cast<float>(a.beta1), omb1 = static_cast<float>(1.0 - a.beta1);
   const int64_t u1 = pf[ng];
-  uint32_t it = 0;
-  TileStats<NC> next;  // one tile ahead, as in k_apply_tma
-  if (pf[0] + blockIdx.x < u1) tile_stats_load(next, a, r, pf, ng, pf[0] + blockIdx.x);
-  for (int64_t u = pf[0] + blockIdx.x; u < u1; u += gridDim.x) {
-    const TileStats<NC> cur = next;
-    const int t = cur.t;
-    const DevTensor d = a.tensors[t];
-    const TilePos tp = tile_pos(d, cur.local);
-    const int64_t H = d.H, W = d.W;
-    const int64_t i0 = tp.r * kTileRows, i1 = min(H, i0 + kTileRows);
-    const int64_t o = tp.b * H * W + i0 * W;
-    // Within a tile, flat indices stay below kTileRows * kTileCols: int.
-    const int cnt = static_cast<int>((i1 - i0) * W);
-    const int cpy = cnt & ~static_cast<int>(kFlatAlign<GT> - 1);
-    const int w = static_cast<int>(W);
-    const float invw = 1.0f / static_cast<float>(w);
-    const float wda = static_cast<float>(a.wd * a.alpha[t]);
-    consumer_sync<NC>();  // stop is settled; colf / rowf / red of the previous tile are read
-    if (stop) break;
-#pragma unroll
-    for (int q = 0; q < TileStats<NC>::kCols; ++q) {
-      const int cl = threadIdx.x + q * NC * 32;
-      colf[cl] = (cl < w) ? cur.coef * rsqrtf(cur.col[q]) : 0.f;
+  uint32_t it = 0, k = 0;
+  bool ok = true;
+  for (int64_t u = pf[0] + blockIdx.x; u < u1 && ok; u += gridDim.x, ++k) {
+    const uint32_t ts = k % kFlatTabs, tph = (k / kFlatTabs) & 1u;
+    if (!mbar_wait(&tfull[ts], tph)) {
+      if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+      ok = false;
+      break;
     }
-    if (threadIdx.x < kTileRows) rowf[threadIdx.x] = (i0 + threadIdx.x < i1) ? rsqrtf(cur.row / cur.mr) : 0.f;
-    consumer_sync<NC>();
-    if (u + gridDim.x < u1) tile_stats_load(next, a, r, pf, ng, u + gridDim.x);
-    const GT* gt = static_cast<const GT*>(d.g) + o;
-    float* pt = d.p + o;
-    float* mt = B1 ? d.m1 + o : nullptr;
+    const FlatTab& T = tab[ts];
+    const float* colf = T.colf;
+    const float* rowf = T.rowf;
+    const int cnt = T.cnt, cpy = T.cpy, w = T.w;
+    const float invw = 1.0f / static_cast<float>(w);
+    const float wda = T.wda;
+    const GT* gt = static_cast<const GT*>(T.g);
+    float* pt = T.p;
+    float* mt = T.m;
     float psq = 0.f;
-    bool ok = true;
-    for (int e0 = 0; e0 < cnt && ok; e0 += static_cast<int>(kSpan), ++it) {
+    for (int e0 = 0; e0 < cnt; e0 += static_cast<int>(kSpan), ++it) {
       const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
-      if (!tma_acquire(&full[slot], ph, a, &stop)) {
+      if (!mbar_wait(&full[slot], ph)) {
+        if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
         ok = false;
         break;
       }
@@ -2427,10 +2532,10 @@ __global__ void __launch_bounds__(TmaCfg<1>::kThreads, 1)
         const unsigned char* ms = st + kTmaRows * (RG::kG + RG::kP) + warp * RG::kP;     // its exp_avg
         const int nc = s0 < cpy ? min(kTileCols, cpy - s0) : 0;  // staged values (whole quads)
 #pragma unroll
-        for (int k = 0; k < kTileCols / 256; ++k) {
+        for (int kk = 0; kk < kTileCols / 256; ++kk) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int cl = k * 256 + h * 128 + lane * 4;
+            const int cl = kk * 256 + h * 128 + lane * 4;
             if (cl < nc) {
               float x[4];
               quad_g<GT>(x, gs, cl);
@@ -2477,12 +2582,15 @@ __global__ void __launch_bounds__(TmaCfg<1>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
+    if (!ok) break;
     if (PSQ) {
-      const double tot = consumer_sum<NC>(psq, red);
-      if (threadIdx.x == 0 && !stop) a.ppart[d.tile0 + cur.local] = tot;
+      const float ws = warp_sum(psq);
+      if (lane == 0) tab[ts].psq[warp] = static_cast<double>(ws);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[ts]);  // the tile's tables are read
   }
-  if (stop && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
+  if (!ok && threadIdx.x == 0) tma_drain<RG::kStages>(full, it);
 }
 
 // ---- psq: sum(p_new^2) carry, one CTA per tensor --------------------------
@@ -2514,6 +2622,11 @@ constexpr size_t tma_smem(size_t extra) {
   return RG::kBytes + extra + sizeof(double) * 32 + sizeof(uint64_t) * 2 * RG::kStages + kPrefixBytes;
 }
 constexpr size_t kFactorBytes = sizeof(float) * (kTileCols + kTileRows);
+// k_apply_tma_flat: ring, table slots, mbarriers (stages and tables), prefix.
+template <class RG>
+constexpr size_t flat_apply_smem() {
+  return RG::kBytes + sizeof(FlatTab) * kFlatTabs + sizeof(uint64_t) * 2 * (RG::kStages + kFlatTabs) + kPrefixBytes;
+}
 
 using KernelFn = void (*)(StepArgs, Range);
 
@@ -2588,13 +2701,13 @@ Inst pick_flat(KernelId k, bool psq_in, int mom, bool psq_out) {
     x.smem = kFlatSmem;
   } else if (k == kKApply) {
     if (mom == 2) return pick_f<GT, 1>(k, psq_in, mom, psq_out);
-    x.threads = TmaCfg<1>::kThreads;
+    x.threads = kFlatApplyThreads;
     if (mom == 1) {
       x.fn = psq_out ? k_apply_tma_flat<GT, true, true> : k_apply_tma_flat<GT, true, false>;
-      x.smem = tma_smem<ApplyRing<GT, true>>(kFactorBytes);
+      x.smem = flat_apply_smem<ApplyRing<GT, true>>();
     } else {
       x.fn = psq_out ? k_apply_tma_flat<GT, false, true> : k_apply_tma_flat<GT, false, false>;
-      x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
+      x.smem = flat_apply_smem<ApplyRing<GT, false>>();
     }
   }
   return x;
