@@ -166,13 +166,16 @@ adaf_status adafactor_workspace_size(const adaf_tensor* tensors, int32_t n, size
 /* One Adafactor step over tensors[0..n) with states[0..n), step t = `step`
  * (>= 1), enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  * stream).  The call only enqueues work and reads no device memory from the
- * host.  The per-call descriptor table is staged in a ring of 4 pinned host
- * buffers per device and read from there by a small kernel on `stream` (no
- * copy engine: host-to-device copies queued on other streams, such as the
- * next step's gradients, do not hold the step back); a call waits on the host
- * only when the upload of the call 4 calls earlier (on any stream of the
- * device) has not yet run, i.e. when more than 4 steps are queued ahead of
- * the GPU.  Params and states
+ * host.  The per-call descriptor table (pointers, shapes, work lists) is
+ * built on the host; the library keeps device copies of up to 8 distinct
+ * tables per device, and a call whose table equals a kept one reads that copy
+ * and uploads nothing (a one-thread kernel on `stream` clears the status
+ * word).  A new table is staged in a ring of 4 pinned host buffers per device
+ * and read from there by a small kernel on `stream`, into a new device copy
+ * (no copy engine: host-to-device copies queued on other streams do not hold
+ * it back); such a call waits on the host only when the upload of the call 4
+ * uploads earlier has not yet run.  A step whose table is new on the device
+ * allocates its copy with cudaMalloc.  Params and states
  * are updated in place; grads are read only.  The workspace (>= the size
  * reported by adafactor_workspace_size, 256-byte aligned) is scratch owned by
  * this call until the enqueued work completes: calls that may run
@@ -317,8 +320,13 @@ void adafactor_debug_stall_copies(int32_t on);
 /* Message of the last failing call on this host thread ("" if none). */
 const char* adafactor_last_error(void);
 
-/* Frees the library's host-side caches (pinned staging buffers, events) for
- * every device.  Call only when no adafactor_step() work is in flight. */
+/* Frees the library's caches for every device: the pinned staging buffers
+ * and events, and the device copies of descriptor tables that adafactor_step,
+ * the row-sharded calls, lamb_step and came_step keep (up to 8 per device and
+ * optimizer, each the size of one call's table: a step whose table bytes equal
+ * a kept copy's reads that copy instead of uploading its table again).  Waits
+ * for the steps that read those copies.  Call only when no step work is in
+ * flight, and after a device reset before the next step. */
 void adafactor_release_cache(void);
 
 /* ---- Kernel timing (CUDA events on the launching stream) ----------------

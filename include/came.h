@@ -85,8 +85,11 @@ adaf_status came_workspace_size(const came_tensor* tensors, int32_t n, size_t* b
  * the legacy default stream).  workspace: >= came_workspace_size() bytes of
  * device memory, 256-byte aligned, not in use by another call in flight.
  * step >= 1.  All checks run before the first CUDA call.  The descriptor
- * upload uses a pinned ring of 4 host buffers (a call waits on the host only
- * when more than 4 steps are queued).  Errors: ADAF_ERR_INVALID_ARGUMENT,
+ * table is read from a device copy the library keeps (up to 8 distinct tables
+ * per device) when one holds the same bytes; a new table goes through a
+ * pinned ring of 4 host buffers into a new device copy (cudaMalloc), and the
+ * call waits on the host only when the upload of 4 uploads earlier has not
+ * run.  adafactor_release_cache() frees the copies.  Errors: ADAF_ERR_INVALID_ARGUMENT,
  * ADAF_ERR_UNSUPPORTED, ADAF_ERR_WORKSPACE_TOO_SMALL, ADAF_ERR_CUDA. */
 adaf_status came_step(const came_tensor* tensors, const came_state* states, int32_t n, int64_t step,
                       const came_hparams* hp, void* workspace, size_t workspace_bytes, void* stream);

@@ -71,9 +71,12 @@ adaf_status lamb_workspace_size(const lamb_tensor* tensors, int32_t n, size_t* b
  * lamb_workspace_size() bytes, 256-byte aligned, not used by another call
  * that is in flight.  Three launches: moments + per-unit norm partials,
  * per-tensor trust ratios, update.  step >= 1.  All argument checks run
- * before the first CUDA call.  The per-call descriptor upload goes through a
- * pinned ring of 4 host buffers, so the call waits on the host only when
- * more than 4 steps are queued.  Errors: ADAF_ERR_INVALID_ARGUMENT,
+ * before the first CUDA call.  The per-call descriptor table is read from a
+ * device copy the library keeps (up to 8 distinct tables per device) when one
+ * holds the same bytes; a new table goes through a pinned ring of 4 host
+ * buffers into a new device copy (cudaMalloc), and the call waits on the host
+ * only when the upload of 4 uploads earlier has not run.  adafactor_release_cache()
+ * frees the copies.  Errors: ADAF_ERR_INVALID_ARGUMENT,
  * ADAF_ERR_UNSUPPORTED, ADAF_ERR_WORKSPACE_TOO_SMALL, ADAF_ERR_CUDA. */
 adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const lamb_hparams* hp,
                       void* workspace, size_t workspace_bytes, void* stream);

@@ -412,6 +412,8 @@ struct DeviceCache {
   Slot slots[kSlots];
   int next = 0;
   std::vector<cudaEvent_t> free_events;
+  meo::TableCache tables;              // device copies of the header (host_copy.cuh)
+  std::vector<unsigned char> scratch;  // this call's header, built on the host
 };
 
 struct ProfRecord {
@@ -541,35 +543,49 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
 
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceCache& dc = g_cache[device];
+  const unsigned char* hbase = ws;  // where the kernels read the header (descriptors, prefix arrays)
+  RecordOnExit used_guard;
   if (staging == kStagePinned) {
-    // Stage the header (descriptors + prefix arrays) in a pinned ring slot and
-    // copy it to the workspace.
-    Slot& slot = dc.slots[dc.next];
-    dc.next = (dc.next + 1) % kSlots;
-    if (slot.pending) {
-      e = cudaEventSynchronize(slot.done);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize (staging slot)");
-      slot.pending = false;
-    }
-    if (slot.cap < plan.header_bytes) {
-      if (slot.host != nullptr) cudaFreeHost(slot.host);
-      slot.host = nullptr;
-      slot.cap = 0;
-      const size_t cap = align_up(plan.header_bytes, size_t(1) << 16);
-      e = cudaHostAlloc(&slot.host, cap, cudaHostAllocPortable | cudaHostAllocMapped);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc (staging)");
-      slot.cap = cap;
-    }
-    if (slot.done == nullptr) {
-      e = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate (staging)");
-    }
-    fill_header(static_cast<unsigned char*>(slot.host), plan);
-    e = copy_from_host(ws, slot.host, plan.header_bytes, s);  // no copy engine (host_copy.cuh)
+    // The header is kept on the device per distinct content (TableCache): a
+    // step whose header equals a kept one reads that copy; otherwise the
+    // header is staged in a pinned ring slot and uploaded into a new device
+    // copy.  The status word stays in the workspace and is cleared by a
+    // one-thread kernel.
+    dc.scratch.resize(plan.header_bytes);
+    fill_header(dc.scratch.data(), plan);
+    auto upload = [&](unsigned char* dst) -> cudaError_t {
+      Slot& slot = dc.slots[dc.next];
+      dc.next = (dc.next + 1) % kSlots;
+      cudaError_t err = cudaSuccess;
+      if (slot.pending) {
+        err = cudaEventSynchronize(slot.done);
+        if (err != cudaSuccess) return err;
+        slot.pending = false;
+      }
+      if (slot.cap < plan.header_bytes) {
+        if (slot.host != nullptr) cudaFreeHost(slot.host);
+        slot.host = nullptr;
+        slot.cap = 0;
+        const size_t cap = align_up(plan.header_bytes, size_t(1) << 16);
+        err = cudaHostAlloc(&slot.host, cap, cudaHostAllocPortable | cudaHostAllocMapped);
+        if (err != cudaSuccess) return err;
+        slot.cap = cap;
+      }
+      if (slot.done == nullptr && (err = cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming)) != cudaSuccess)
+        return err;
+      std::memcpy(slot.host, dc.scratch.data(), plan.header_bytes);
+      if ((err = copy_from_host(dst, slot.host, plan.header_bytes, s)) != cudaSuccess) return err;  // no copy engine
+      if ((err = cudaEventRecord(slot.done, s)) != cudaSuccess) return err;
+      slot.pending = true;
+      return cudaSuccess;
+    };
+    unsigned char* dev = nullptr;
+    e = dc.tables.lookup(dc.scratch.data(), plan.header_bytes, s, upload, &dev, &used_guard.ev);
     if (e != cudaSuccess) return cuda_fail(e, "descriptor table upload");
-    e = cudaEventRecord(slot.done, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");
-    slot.pending = true;
+    used_guard.s = s;
+    hbase = dev;
+    e = zero_word(reinterpret_cast<int32_t*>(ws), s);  // this step's status word
+    if (e != cudaSuccess) return cuda_fail(e, "status word reset");
   } else {
     // Pageable staging: the runtime copies the host bytes out before the
     // call returns, so a local buffer suffices.
@@ -582,10 +598,10 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
 
   StepArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.tensors = reinterpret_cast<const DevTensor*>(ws + kTableOffset);
+  a.tensors = reinterpret_cast<const DevTensor*>(hbase + kTableOffset);
   a.status = reinterpret_cast<int32_t*>(ws);
-  a.pf_tiles = reinterpret_cast<const int32_t*>(ws + plan.off_pf_tiles);
-  a.pf_items = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
+  a.pf_tiles = reinterpret_cast<const int32_t*>(hbase + plan.off_pf_tiles);
+  a.pf_items = reinterpret_cast<const int32_t*>(hbase + plan.off_pf_items);
   a.alpha = reinterpret_cast<double*>(ws + plan.off_alpha);
   a.coef = reinterpret_cast<double*>(ws + plan.off_coef);
   a.mrow = reinterpret_cast<double*>(ws + plan.off_mrow);
@@ -648,8 +664,8 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
       if (factored_only && c == meo::kClsUnfactored) continue;
       const int32_t m = static_cast<int32_t>(plan.cls_idx[c].size());
       const int q = stream_slot(k);
-      const int32_t* pf_dev = reinterpret_cast<const int32_t*>(ws + plan.off_cls_pf[q][c]);
-      const int32_t* idx_dev = reinterpret_cast<const int32_t*>(ws + plan.off_cls_idx[c]);
+      const int32_t* pf_dev = reinterpret_cast<const int32_t*>(hbase + plan.off_cls_pf[q][c]);
+      const int32_t* idx_dev = reinterpret_cast<const int32_t*>(hbase + plan.off_cls_idx[c]);
       for (int32_t g0 = 0; g0 < m; g0 += meo::kMaxGroup) {
         const int32_t g1 = g0 + meo::kMaxGroup < m ? g0 + meo::kMaxGroup : m;
         const int64_t units = plan.cls_pf[q][c][g1] - plan.cls_pf[q][c][g0];
@@ -669,7 +685,7 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
   // this shard's sum(u^2) into exchange round 2; 3 = clip from exchange round 2, apply.
   auto stats = [&]() -> adaf_status {
     if (!plan.any_factored) return ADAF_OK;
-    const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
+    const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(hbase + plan.off_pf_items);
     for (int32_t g0 = 0; g0 < nd_i; g0 += meo::kMaxGroup) {
       const int32_t g1 = g0 + meo::kMaxGroup < nd_i ? g0 + meo::kMaxGroup : nd_i;
       const int64_t units = plan.pf_items[g1] - plan.pf_items[g0];
@@ -703,7 +719,7 @@ adaf_status step_core(const adaf_tensor* tensors, const adaf_state* states, cons
   }
   if ((st = stream_all(meo::kKPass1, false)) != ADAF_OK) return st;
   if (plan.any_factored) {
-    const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(ws + plan.off_pf_items);
+    const int32_t* pf_items_dev = reinterpret_cast<const int32_t*>(hbase + plan.off_pf_items);
     for (int32_t g0 = 0; g0 < nd_i; g0 += meo::kMaxGroup) {
       const int32_t g1 = g0 + meo::kMaxGroup < nd_i ? g0 + meo::kMaxGroup : nd_i;
       const int64_t units = plan.pf_items[g1] - plan.pf_items[g0];
@@ -840,6 +856,7 @@ void adafactor_release_cache(void) {
     }
     for (cudaEvent_t ev : kv.second.free_events) cudaEventDestroy(ev);
     kv.second.free_events.clear();
+    kv.second.tables.clear();
   }
   for (ProfRecord& r : g_prof) {
     if (cudaSetDevice(r.device) == cudaSuccess) {
@@ -850,6 +867,8 @@ void adafactor_release_cache(void) {
   g_prof.clear();
   g_cache.clear();
   meo::noalloc_forget_addresses();
+  meo::lamb_forget_tables();
+  meo::came_forget_tables();
   if (have_dev) cudaSetDevice(cur);
 }
 

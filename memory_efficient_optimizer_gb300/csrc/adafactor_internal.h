@@ -216,4 +216,8 @@ adaf_status set_last_error(adaf_status st, const char* msg);
 // Forgets the per-device addresses of the no-alloc scratch array
 // (adafactor_noalloc.cu); adafactor_release_cache() calls it.
 void noalloc_forget_addresses();
+// Drop the device copies of the LAMB and CAME descriptor tables (they wait
+// for the steps that read them); adafactor_release_cache calls them.
+void lamb_forget_tables();
+void came_forget_tables();
 }  // namespace meo

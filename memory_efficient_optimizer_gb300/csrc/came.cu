@@ -1014,6 +1014,7 @@ struct DeviceState {
   int next = 0;
   int sms = 0;
   std::vector<cudaEvent_t> free_events;
+  meo::TableCache tables;  // device copies of the descriptor table (host_copy.cuh)
 };
 
 enum KernelSlot { kSA = 0, kSStats, kSMeans, kSB, kSClip, kSC, kSD, kSPanel, kNumKernels };
@@ -1167,27 +1168,50 @@ adaf_status came_step(const came_tensor* tensors, const came_state* states, int3
   DeviceState& ds = g_dev[device];
   if (ds.sms == 0 && (err = cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
     return cuda_fail(err, "cudaDeviceGetAttribute");
-  Slot& sl = ds.ring[ds.next];
-  ds.next = (ds.next + 1) % kRing;
-  if (sl.used && (err = cudaEventSynchronize(sl.done)) != cudaSuccess)
-    return cuda_fail(err, "cudaEventSynchronize (upload ring)");
-  const size_t up = round_up(P.hdr_bytes, 16);  // the upload moves whole 16-byte words
-  if (sl.cap < up) {
-    if (sl.host) cudaFreeHost(sl.host);
-    sl.host = nullptr;
-    sl.cap = 0;
-    if ((err = cudaHostAlloc(&sl.host, up, cudaHostAllocPortable | cudaHostAllocMapped)) != cudaSuccess)
-      return cuda_fail(err, "cudaHostAlloc");
-    sl.cap = up;
-  }
-  if (sl.done == nullptr && (err = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess)
-    return cuda_fail(err, "cudaEventCreate");
-  std::memcpy(sl.host, h.data(), P.hdr_bytes);
-  // a kernel reads the table from host memory: no copy engine (host_copy.cuh)
-  if ((err = meo::copy_from_host(ws + P.off_hdr, sl.host, up, s)) != cudaSuccess)
+  // The descriptor table comes from a kept device copy when one holds the
+  // same bytes (TableCache); otherwise it is staged in a pinned ring slot and
+  // a kernel reads it from host memory (no copy engine, host_copy.cuh).
+  auto upload = [&](unsigned char* dst) -> cudaError_t {
+    Slot& sl = ds.ring[ds.next];
+    ds.next = (ds.next + 1) % kRing;
+    cudaError_t e = cudaSuccess;
+    if (sl.used && (e = cudaEventSynchronize(sl.done)) != cudaSuccess) return e;
+    const size_t up = round_up(P.hdr_bytes, 16);  // the upload moves whole 16-byte words
+    if (sl.cap < up) {
+      if (sl.host) cudaFreeHost(sl.host);
+      sl.host = nullptr;
+      sl.cap = 0;
+      if ((e = cudaHostAlloc(&sl.host, up, cudaHostAllocPortable | cudaHostAllocMapped)) != cudaSuccess) return e;
+      sl.cap = up;
+    }
+    if (sl.done == nullptr && (e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess)
+      return e;
+    std::memcpy(sl.host, h.data(), P.hdr_bytes);
+    if ((e = meo::copy_from_host(dst, sl.host, up, s)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(sl.done, s)) != cudaSuccess) return e;
+    sl.used = true;
+    return cudaSuccess;
+  };
+  unsigned char* tab = nullptr;
+  meo::RecordOnExit used_guard;
+  if ((err = ds.tables.lookup(h.data(), P.hdr_bytes, s, upload, &tab, &used_guard.ev)) != cudaSuccess)
     return cuda_fail(err, "descriptor table upload");
-  if ((err = cudaEventRecord(sl.done, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
-  sl.used = true;
+  used_guard.s = s;
+  // the table's arrays at their offsets within the kept copy
+  auto at = [&](size_t off) { return tab + (off - P.off_hdr); };
+  a.dev = reinterpret_cast<const CDev*>(at(P.off_hdr));
+  for (int l = 0; l < 2; ++l) {
+    for (int c = 0; c < kClasses; ++c) {
+      a.pf[l][c] = reinterpret_cast<const int64_t*>(at(P.off_pf[l][c]));
+      a.idx[l][c] = reinterpret_cast<const int32_t*>(at(P.off_idx[l][c]));
+    }
+  }
+  for (int q = 0; q < kPanelCfgs; ++q) {
+    a.ppf[q] = reinterpret_cast<const int64_t*>(at(P.off_ppf[q]));
+    a.pidx[q] = reinterpret_cast<const int32_t*>(at(P.off_pidx[q]));
+  }
+  a.item_pf = reinterpret_cast<const int64_t*>(at(P.off_ipf));
+  a.item_idx = reinterpret_cast<const int32_t*>(at(P.off_iidx));
 
   const int persist = 2 * ds.sms;  // 2 CTAs of 256 threads per SM
   auto grid_for = [&](int64_t units) { return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(persist, units))); };
@@ -1315,3 +1339,16 @@ int32_t came_num_kernels(void) { return kNumKernels; }
 const char* came_kernel_name(int32_t k) { return (k >= 0 && k < kNumKernels) ? kKernelNames[k] : ""; }
 
 }  // extern "C"
+
+namespace meo {
+void came_forget_tables() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  const bool have_dev = cudaGetDevice(&cur) == cudaSuccess;
+  for (auto& kv : g_dev) {
+    if (cudaSetDevice(kv.first) == cudaSuccess) kv.second.tables.clear();
+  }
+  if (have_dev) cudaSetDevice(cur);
+}
+}  // namespace meo
+

@@ -14,6 +14,9 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstring>
+#include <utility>
+#include <vector>
 
 namespace meo {
 namespace {
@@ -39,6 +42,99 @@ inline cudaError_t copy_from_host(void* dst, const void* host, size_t bytes, cud
   const int64_t blocks = (n16 + 255) / 256;
   k_copy_from_host<<<static_cast<int>(blocks < 64 ? blocks : 64), 256, 0, s>>>(
       static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
+  return cudaGetLastError();
+}
+
+// Device copies of a step's descriptor table, one per distinct content.  A
+// step whose table bytes equal a kept copy's reads that copy and uploads
+// nothing: the upload kernel's host reads share the host link with the
+// caller's own host-to-device copies, and a 16 GB gradient upload on a side
+// stream (the next step's) was measured to hold a step back for most of its
+// 76 ms on some boxes.
+struct TableCache {
+  struct Entry {
+    std::vector<unsigned char> bytes;  // the table as uploaded
+    unsigned char* dev = nullptr;      // its device copy
+    cudaEvent_t ready = nullptr;       // recorded after the upload
+    cudaEvent_t used = nullptr;        // recorded after the last step that read it
+    uint64_t stamp = 0;                // last use, for eviction
+  };
+  static constexpr size_t kMax = 8;  // copies kept per device
+  std::vector<Entry> entries;
+  uint64_t clock = 0;
+
+  static void release(Entry& e) {
+    if (e.used) cudaEventSynchronize(e.used);  // no step still reads it
+    if (e.dev) cudaFree(e.dev);
+    if (e.ready) cudaEventDestroy(e.ready);
+    if (e.used) cudaEventDestroy(e.used);
+    e = Entry();
+  }
+  void clear() {
+    for (Entry& e : entries) release(e);
+    entries.clear();
+  }
+  // The device copy of bytes[0, n): a kept one (s waits for its upload), or
+  // a new one that upload(dev) fills on s (the least recently used copy is
+  // dropped when kMax are kept).  *used is the event to record on s after the
+  // step's last launch.
+  template <class Upload>
+  cudaError_t lookup(const unsigned char* bytes, size_t n, cudaStream_t s, Upload&& upload, unsigned char** dev,
+                     cudaEvent_t* used) {
+    Entry* hit = nullptr;
+    for (Entry& e : entries) {
+      if (e.bytes.size() == n && std::memcmp(e.bytes.data(), bytes, n) == 0) {
+        hit = &e;
+        break;
+      }
+    }
+    cudaError_t err = cudaSuccess;
+    if (hit != nullptr) {
+      err = cudaStreamWaitEvent(s, hit->ready, 0);  // the copy may have been made on another stream
+      if (err != cudaSuccess) return err;
+    } else {
+      if (entries.size() >= kMax) {
+        size_t lru = 0;
+        for (size_t k = 1; k < entries.size(); ++k)
+          if (entries[k].stamp < entries[lru].stamp) lru = k;
+        release(entries[lru]);
+        entries.erase(entries.begin() + static_cast<std::ptrdiff_t>(lru));
+      }
+      Entry ne;
+      err = cudaMalloc(reinterpret_cast<void**>(&ne.dev), (n + 255) & ~size_t{255});  // whole 16-byte words
+      if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ne.ready, cudaEventDisableTiming);
+      if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ne.used, cudaEventDisableTiming);
+      if (err == cudaSuccess) err = upload(ne.dev);
+      if (err == cudaSuccess) err = cudaEventRecord(ne.ready, s);
+      if (err != cudaSuccess) {
+        release(ne);
+        return err;
+      }
+      ne.bytes.assign(bytes, bytes + n);
+      entries.push_back(std::move(ne));
+      hit = &entries.back();
+    }
+    hit->stamp = ++clock;
+    *dev = hit->dev;
+    *used = hit->used;
+    return cudaSuccess;
+  }
+};
+
+// Records `ev` on `s` when a step's launch sequence is left, on every path.
+struct RecordOnExit {
+  cudaEvent_t ev = nullptr;
+  cudaStream_t s = nullptr;
+  ~RecordOnExit() {
+    if (ev) cudaEventRecord(ev, s);
+  }
+};
+
+__global__ void k_zero_word(int32_t* p) { *p = 0; }
+
+// Enqueues *p = 0 on s (a one-thread kernel: no copy engine either).
+inline cudaError_t zero_word(int32_t* p, cudaStream_t s) {
+  k_zero_word<<<1, 1, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -375,6 +375,7 @@ struct DeviceState {
   int next = 0;
   int grid = 0;  // persistent CTAs for the streaming passes
   std::vector<cudaEvent_t> free_events;
+  meo::TableCache tables;  // device copies of the descriptor table (host_copy.cuh)
 };
 
 const char* const kKernelNames[] = {"k_lamb_moments", "k_lamb_trust", "k_lamb_update"};
@@ -514,28 +515,38 @@ adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const
       return cuda_fail(err, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     ds.grid = sms * std::max(1, std::min(occ, std::min(occ2, occ3)));
   }
-  Slot& sl = ds.ring[ds.next];
-  ds.next = (ds.next + 1) % kRing;
-  if (sl.used) {
-    if ((err = cudaEventSynchronize(sl.done)) != cudaSuccess) return cuda_fail(err, "cudaEventSynchronize (upload ring)");
-  }
-  const size_t up = round_up(hdr, 16);  // the upload moves whole 16-byte words
-  if (sl.cap < up) {
-    if (sl.host) cudaFreeHost(sl.host);
-    sl.host = nullptr;
-    sl.cap = 0;
-    if ((err = cudaHostAlloc(&sl.host, up, cudaHostAllocPortable | cudaHostAllocMapped)) != cudaSuccess)
-      return cuda_fail(err, "cudaHostAlloc");
-    sl.cap = up;
-  }
-  if (sl.done == nullptr && (err = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess)
-    return cuda_fail(err, "cudaEventCreate");
-  std::memcpy(sl.host, h.data(), hdr);
-  // a kernel reads the table from host memory: no copy engine (host_copy.cuh)
-  if ((err = meo::copy_from_host(ws + L.off_dev, sl.host, up, s)) != cudaSuccess)
+  // The descriptor table comes from a kept device copy when one holds the
+  // same bytes (TableCache); otherwise it is staged in a pinned ring slot and
+  // a kernel reads it from host memory (no copy engine, host_copy.cuh).
+  auto upload = [&](unsigned char* dst) -> cudaError_t {
+    Slot& sl = ds.ring[ds.next];
+    ds.next = (ds.next + 1) % kRing;
+    cudaError_t e = cudaSuccess;
+    if (sl.used && (e = cudaEventSynchronize(sl.done)) != cudaSuccess) return e;
+    const size_t up = round_up(hdr, 16);  // the upload moves whole 16-byte words
+    if (sl.cap < up) {
+      if (sl.host) cudaFreeHost(sl.host);
+      sl.host = nullptr;
+      sl.cap = 0;
+      if ((e = cudaHostAlloc(&sl.host, up, cudaHostAllocPortable | cudaHostAllocMapped)) != cudaSuccess) return e;
+      sl.cap = up;
+    }
+    if (sl.done == nullptr && (e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess)
+      return e;
+    std::memcpy(sl.host, h.data(), hdr);
+    if ((e = meo::copy_from_host(dst, sl.host, up, s)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(sl.done, s)) != cudaSuccess) return e;
+    sl.used = true;
+    return cudaSuccess;
+  };
+  unsigned char* tab = nullptr;
+  meo::RecordOnExit used_guard;
+  if ((err = ds.tables.lookup(h.data(), hdr, s, upload, &tab, &used_guard.ev)) != cudaSuccess)
     return cuda_fail(err, "descriptor table upload");
-  if ((err = cudaEventRecord(sl.done, s)) != cudaSuccess) return cuda_fail(err, "cudaEventRecord");
-  sl.used = true;
+  used_guard.s = s;
+  a.dev = reinterpret_cast<const LDev*>(tab);
+  a.pf = reinterpret_cast<const int64_t*>(tab + (L.off_pf - L.off_dev));
+  a.ord = reinterpret_cast<const int32_t*>(tab + (L.off_ord - L.off_dev));
 
   auto grid_for = [&](int64_t units) { return static_cast<int>(std::min<int64_t>(ds.grid, std::max<int64_t>(1, units))); };
   for (int k = 0; k < kNumKernels; ++k) {
@@ -561,6 +572,22 @@ adaf_status lamb_step(const lamb_tensor* tensors, int32_t n, int64_t step, const
   }
   return ADAF_OK;
 }
+
+}  // extern "C"
+
+namespace meo {
+void lamb_forget_tables() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  const bool have_dev = cudaGetDevice(&cur) == cudaSuccess;
+  for (auto& kv : g_dev) {
+    if (cudaSetDevice(kv.first) == cudaSuccess) kv.second.tables.clear();
+  }
+  if (have_dev) cudaSetDevice(cur);
+}
+}  // namespace meo
+
+extern "C" {
 
 adaf_status lamb_trust_ratios(const void* workspace, int32_t n, double* out, void* stream) {
   if (n < 0 || (n > 0 && (workspace == nullptr || out == nullptr)))

@@ -35,6 +35,10 @@ def test_bounded_wait_runs_out_reports_and_context_survives():
         binding.adafactor_debug_stall_copies(False)
     assert status & binding.ADAF_DEVICE_WAIT_TIMEOUT
     assert waited < 60.0
+    # the next call of the same step (its descriptor table is kept on the
+    # device, nothing uploaded) starts from a cleared status word
+    step(2)
+    assert step.device_status() == 0
     # the context is still usable: a normal run agrees with the oracle
     wl = synth.Workload("after_timeout", [(f"t{k}", s) for k, s in enumerate(shapes)], torch.bfloat16, 1e-2,
                         {}, 3)
