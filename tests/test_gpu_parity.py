@@ -251,3 +251,35 @@ def test_more_tensors_than_one_launch_group():
     wl = synth.Workload("groups", [(f"t{k}", s) for k, s in enumerate(shapes)], torch.bfloat16, 1e-2,
                         dict(beta1=0.9, weight_decay=0.01), 3)
     run_parity(wl)
+
+
+def test_two_step_objects_alternating_share_kept_tables():
+    """Two AdafactorStep objects over the same params and states, each with its
+    own gradient buffers, called in turn (the double-buffered upload pattern
+    of a training loop): every call after the first two reads a descriptor
+    table kept on the device.  Results must equal the oracle's, and a third
+    object over a different list in between must not disturb them."""
+    import oracle
+    from parity_util import oracle_hp
+    shapes = [(300, 2056), (130, 100), (17, 16), (513,), (2, 40, 600)]
+    hp = dict(beta1=0.9)
+    params = [synth.make_param(s, k).cuda() for k, s in enumerate(shapes)]
+    refs = [to64(p) for p in params]
+    rst = [oracle.State(s, True) for s in shapes]
+    states = init_state(params, beta1=0.9)
+    bufs = [[torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in shapes] for _ in range(2)]
+    steps = [AdafactorStep(params, bufs[b], states, **hp) for b in range(2)]
+    other_p = [synth.make_param((64, 64), 99).cuda()]
+    other = AdafactorStep(other_p, [torch.zeros(64, 64, device="cuda")], init_state(other_p))
+    for t in range(1, 7):
+        b = t % 2
+        for k, s in enumerate(shapes):
+            bufs[b][k].copy_(synth.make_grad(s, k, t, dtype=torch.bfloat16))
+            oracle.step(refs[k], to64(bufs[b][k]), rst[k], t, oracle_hp(hp))
+        steps[b](t)
+        if t == 3:
+            other(1)
+    torch.cuda.synchronize()
+    assert steps[0].device_status() == 0 and steps[1].device_status() == 0
+    for k in range(len(shapes)):
+        check(f"alternating[{k}]", to64(params[k]), refs[k])
