@@ -1476,22 +1476,25 @@ __global__ void __launch_bounds__(kThreads) k_apply_u(const __grid_constant__ St
 // and all consumers leave together at the next tile boundary.
 constexpr int kTmaRows = kWarps;  // rows per stage
 // SPLIT consumer warps per row (column blocks of kTileCols / SPLIT): 1 for
-// the plain and fp32-moment apply, 2 for the 8-bit moment, whose per-group
-// re-quantisation needs more warps to hide its dependent arithmetic.
-template <int SPLIT> struct TmaCfg {
-  static constexpr int kConsumers = kTmaRows * SPLIT;
+// the plain apply, 2 for the 8-bit moment, whose per-group re-quantisation
+// needs more warps to hide its dependent arithmetic, and 2 for the fp32
+// moment, whose stages hold 4 rows (RS) instead of 8: its rows are 10 KB
+// (bf16 g, p, exp_avg), and 8-row stages left only two in the ring.
+template <int SPLIT, int RS = kTmaRows> struct TmaCfg {
+  static constexpr int kConsumers = RS * SPLIT;
   static constexpr int kThreads = (kConsumers + 1) * 32;
   static_assert(kTileCols % (256 * SPLIT) == 0, "a consumer warp takes whole 256-column chunks");
   static_assert(kConsumers <= 32, "consumer warp sums fit the reduction buffer");
 };
 
-template <typename GT, bool WP, bool WM, size_t kBudget>
+template <typename GT, bool WP, bool WM, size_t kBudget, int RS = kTmaRows>
 struct Ring {
+  static constexpr int kRows = RS;  // tile rows per stage
   static constexpr int kG = kTileCols * sizeof(GT);
   static constexpr int kP = WP ? kTileCols * 4 : 0;
   static constexpr int kM = WM ? kTileCols * 4 : 0;
   static constexpr int kRow = kG + kP + kM;
-  static constexpr int kStage = kTmaRows * kRow;
+  static constexpr int kStage = RS * kRow;
   static constexpr int kStages = kBudget / kStage < 16 ? static_cast<int>(kBudget / kStage) : 16;
   static constexpr size_t kBytes = static_cast<size_t>(kStages) * kStage;
   static_assert(kStages >= 2, "stage ring too small");
@@ -1559,7 +1562,7 @@ __device__ __forceinline__ int tma_setup(int32_t* pf, const Range& r, uint64_t* 
   return ng;
 }
 
-// The producer (one thread): every 8-row stage of every tile of this CTA.
+// The producer (one thread): every RG::kRows-row stage of every tile of this CTA.
 template <typename GT, class RG>
 __device__ __forceinline__ void tma_produce(const StepArgs& a, const Range& r, const int32_t* pf, int ng,
                                             unsigned char* ring, uint64_t* full, uint64_t* empty) {
@@ -1574,13 +1577,13 @@ __device__ __forceinline__ void tma_produce(const StepArgs& a, const Range& r, c
     const int64_t j0 = tp.c * kTileCols;
     const uint32_t ncol = static_cast<uint32_t>(min(static_cast<int64_t>(kTileCols), d.W - j0));
     const int64_t base = tp.b * d.H * d.W;
-    for (int64_t rs = i0; rs < i1; rs += kTmaRows, ++it) {
+    for (int64_t rs = i0; rs < i1; rs += RG::kRows, ++it) {
       const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
       if (!mbar_wait(&empty[slot], ph ^ 1u)) {
         atomicOr(a.status, kStatusWaitTimeout);
         return;
       }
-      const int nrows = static_cast<int>(min(static_cast<int64_t>(kTmaRows), i1 - rs));
+      const int nrows = static_cast<int>(min(static_cast<int64_t>(RG::kRows), i1 - rs));
       const uint32_t per_row = ncol * static_cast<uint32_t>(sizeof(GT) + (RG::kP ? 4 : 0) + (RG::kM ? 4 : 0));
       mbar_arrive_expect_tx(&full[slot], nrows * per_row);
       unsigned char* st = ring + slot * RG::kStage;
@@ -2083,8 +2086,8 @@ __global__ void __launch_bounds__(NW * 32, MINB)
 }
 
 // ---- apply (vector path) ---------------------------------------------------
-template <typename GT, bool B1>
-using ApplyRing = Ring<GT, true, B1, 200 * 1024>;
+template <typename GT, bool B1, int RS = kTmaRows>
+using ApplyRing = Ring<GT, true, B1, 200 * 1024, RS>;
 
 // Codes (4 per lane and 128-column half-chunk: exactly one 8-bit group) and
 // this lane's group scale (lanes 0..7: the segment's 8 groups) of one row
@@ -2139,14 +2142,19 @@ __device__ __forceinline__ void tile_stats_load(TileStats<NC>& s, const StepArgs
   s.row = (threadIdx.x < kTileRows && i < d.H) ? d.row[tp.b * d.H + i] : 1.f;
 }
 
+template <bool B1, bool Q8> struct ApplyShape {  // rows per stage, consumer warps per row
+  static constexpr int kRows = (B1 && !Q8) ? 4 : kTmaRows;
+  static constexpr int kSplit = Q8 ? kQ8Split : (B1 ? 2 : 1);
+};
 template <typename GT, bool B1, bool Q8, bool PSQ>
-__global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
+__global__ void __launch_bounds__(TmaCfg<ApplyShape<B1, Q8>::kSplit, ApplyShape<B1, Q8>::kRows>::kThreads, 1)
     k_apply_tma(const __grid_constant__ StepArgs a, const Range r) {
-  constexpr int SPLIT = Q8 ? kQ8Split : 1;
-  constexpr int NC = TmaCfg<SPLIT>::kConsumers;
+  constexpr int SPLIT = ApplyShape<B1, Q8>::kSplit;
+  constexpr int RS = ApplyShape<B1, Q8>::kRows;
+  constexpr int NC = TmaCfg<SPLIT, RS>::kConsumers;
   static_assert(!Q8 || B1, "the 8-bit moment needs beta1");
   static_assert(kQ8Group == 128, "a 128-column half-chunk is one 8-bit group");
-  using RG = ApplyRing<GT, B1 && !Q8>;
+  using RG = ApplyRing<GT, B1 && !Q8, RS>;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* ring = smem;
   float* colf = reinterpret_cast<float*>(smem + RG::kBytes);  // coef * col_j^-1/2
@@ -2198,18 +2206,18 @@ __global__ void __launch_bounds__(TmaCfg<Q8 ? kQ8Split : 1>::kThreads, 1)
     if (kAhead && u + gridDim.x < u1) tile_stats_load(next, a, r, pf, ng, u + gridDim.x);
     float psq = 0.f;
     bool ok = true;
-    const int wr = warp % kTmaRows;                              // row of the stage
+    const int wr = warp % RS;                                    // row of the stage
     constexpr int KW = kTileCols / 256 / SPLIT;                   // 256-column chunks per warp
-    const int k0 = (warp / kTmaRows) * KW;                        // first chunk of this warp
+    const int k0 = (warp / RS) * KW;                              // first chunk of this warp
     const int64_t jw = j0 + k0 * 256;
     Q8Row qnext;  // codes / scales of this warp's next row
     if (Q8 && i0 + wr < i1) q8_load_row(qnext, d, tp.b * H + i0 + wr, base + (i0 + wr) * W, jw, lane);
-    for (int64_t rs = i0; rs < i1 && ok; rs += kTmaRows, ++it) {
+    for (int64_t rs = i0; rs < i1 && ok; rs += RS, ++it) {
       const int64_t i = rs + wr;
       Q8Row qcur;
       if (Q8) {
         qcur = qnext;
-        const int64_t inext = i + kTmaRows;
+        const int64_t inext = i + RS;
         if (inext < i1) q8_load_row(qnext, d, tp.b * H + inext, base + inext * W, jw, lane);
       }
       const uint32_t slot = it % RG::kStages, ph = (it / RG::kStages) & 1u;
@@ -2652,14 +2660,16 @@ Inst pick_f(KernelId k, bool psq_in, int mom, bool psq_out) {
       return x;
     case kKApply:
       if constexpr (VEC == 8) {  // vector path: bulk-copy staged rows
-        x.threads = mom == 2 ? TmaCfg<kQ8Split>::kThreads : TmaCfg<1>::kThreads;
         if (mom == 2) {
+          x.threads = TmaCfg<ApplyShape<true, true>::kSplit, ApplyShape<true, true>::kRows>::kThreads;
           x.fn = psq_out ? k_apply_tma<GT, true, true, true> : k_apply_tma<GT, true, true, false>;
-          x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
+          x.smem = tma_smem<ApplyRing<GT, false, ApplyShape<true, true>::kRows>>(kFactorBytes);
         } else if (b1) {
+          x.threads = TmaCfg<ApplyShape<true, false>::kSplit, ApplyShape<true, false>::kRows>::kThreads;
           x.fn = psq_out ? k_apply_tma<GT, true, false, true> : k_apply_tma<GT, true, false, false>;
-          x.smem = tma_smem<ApplyRing<GT, true>>(kFactorBytes);
+          x.smem = tma_smem<ApplyRing<GT, true, ApplyShape<true, false>::kRows>>(kFactorBytes);
         } else {
+          x.threads = TmaCfg<1>::kThreads;
           x.fn = psq_out ? k_apply_tma<GT, false, false, true> : k_apply_tma<GT, false, false, false>;
           x.smem = tma_smem<ApplyRing<GT, false>>(kFactorBytes);
         }
