@@ -293,15 +293,19 @@ def kernel_source_digest(kernel):
     return hashlib.sha256((header + text).encode()).hexdigest()
 
 
-def traffic_record(kernel):
-    """dram bytes per full launch from the committed ncu summary, or None when
-    the kernel's source changed since the counters were taken."""
+def traffic_record(kernel, workload):
+    """dram bytes per full launch of `kernel` in `workload` from the committed
+    ncu summary (records are keyed "workload/kernel": a launch slot moves
+    different bytes in different workloads), or None when there is no record
+    or the kernel's source changed since the counters were taken."""
+    if workload is None:
+        return None
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
         sha = kernel_source_digest(kernel)
-        entry = rec.get(kernel)
+        entry = rec.get(f"{workload}/{kernel}")
         if entry and entry.get("kernel_source_sha256") == sha:
             return float(entry["dram_bytes_per_full_launch"])
     except (OSError, ValueError, KeyError):
@@ -648,7 +652,8 @@ def run_ours(args, world, rank, local):
         ach = slot_bytes[dom_name] / (dom_ms / dom_per / 1e3) / 1e9
         roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_kind,
-                    "traffic": traffic_record(dom_name), "algorithmic_bytes_per_launch": slot_bytes[dom_name],
+                    "traffic": traffic_record(dom_name, None if args.shards else args.workload),
+                    "algorithmic_bytes_per_launch": slot_bytes[dom_name],
                     "avg_launch_ms": dom_ms / dom_per}
     eff_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     clk = clocks.summary()
@@ -765,7 +770,7 @@ def run_lamb(args, world, rank, local):
     dom_name, (dom_ms, dom_n) = max(kernels.items(), key=lambda kv: kv[1][0])
     ach = slot_bytes[dom_name] / (dom_ms / dom_n / 1e3) / 1e9
     roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_source": peak_kind, "traffic": traffic_record(dom_name),
+                "frac": round(ach / peak, 4), "peak_source": peak_kind, "traffic": traffic_record(dom_name, args.workload),
                 "algorithmic_bytes_per_launch": slot_bytes[dom_name], "avg_launch_ms": dom_ms / dom_n}
     eff = design_bytes / (ms_per_step / 1e3) / 1e9
     out = {
@@ -860,7 +865,7 @@ def run_came(args, world, rank, local):
     dom_name, (dom_ms, dom_n) = max(kernels.items(), key=lambda kv: kv[1][0])
     ach = slot_bytes[dom_name] / (dom_ms / args.steps / 1e3) / 1e9
     roofline = {"kernel": dom_name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_source": peak_kind, "traffic": traffic_record(dom_name),
+                "frac": round(ach / peak, 4), "peak_source": peak_kind, "traffic": traffic_record(dom_name, args.workload),
                 "algorithmic_bytes_per_launch": slot_bytes[dom_name], "avg_launch_ms": dom_ms / args.steps}
     e2e = None
     if args.e2e_steps > 0:

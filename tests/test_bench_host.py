@@ -77,16 +77,24 @@ def test_all_cores_baseline_runs_the_oracle_in_spawned_workers():
     assert "2 tensors (131,584 values)" in out["sample"]
 
 
-def test_traffic_records_are_keyed_to_their_kernel_sources():
-    """Every committed DRAM traffic record names a kernel whose source digest
-    the bench can compute; the records of different kernel files differ."""
+def test_traffic_records_are_keyed_to_their_workload_and_kernel_sources():
+    """Every committed DRAM traffic record is keyed "workload/kernel" (a launch
+    slot moves different bytes in different workloads) and names a kernel
+    whose source digest the bench can compute; the records of different
+    kernel files differ, and a workload without a record gets none."""
     rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    assert {"k_apply[rows_bf16]", "k_lamb_moments", "k_came_pass_d"} <= set(rec)
-    digests = {k: bench.kernel_source_digest(k) for k in rec}
-    assert len({digests["k_apply[rows_bf16]"], digests["k_lamb_moments"], digests["k_came_pass_d"]}) == 3
+    assert {"llama3_8b/k_apply[rows_bf16]", "llama3_8b_lamb/k_lamb_moments", "llama3_8b_came/k_came_pass_d"} <= set(rec)
+    for k in rec:
+        wl, kernel = k.split("/")
+        assert synth.workload(wl).numel > 0
+    digests = {k: bench.kernel_source_digest(k.split("/")[1]) for k in rec}
+    assert len({digests["llama3_8b/k_apply[rows_bf16]"], digests["llama3_8b_lamb/k_lamb_moments"],
+                digests["llama3_8b_came/k_came_pass_d"]}) == 3
     for k, entry in rec.items():
         assert entry["dram_bytes_per_full_launch"] > 0
         assert len(entry["kernel_source_sha256"]) == 64
+    assert bench.traffic_record("k_apply[rows_bf16]", "llama3_8b_beta1") is None
+    assert bench.traffic_record("k_apply[rows_bf16]", None) is None
 
 
 @pytest.mark.parametrize("name", ["llama3_8b", "llama3_8b_lamb", "llama3_8b_came", "llama3_8b_beta1_int8"])
