@@ -271,7 +271,8 @@ def device_uuid(dev):
 # a launch slot's code; the traffic record of the slot stays valid while
 # these sections and the shared header are unchanged.
 KERNEL_SECTIONS = {
-    "k_apply": ("small helpers", "per-tile column factors", "apply: ", "vector path of apply", "apply (vector path)"),
+    "k_apply": ("small helpers", "per-tile column factors", "apply: ", "vector path of apply", "apply (vector path)",
+                "apply of the flat class"),
 }
 
 
