@@ -28,6 +28,7 @@ import csv
 import hashlib
 import io
 import json
+import mmap
 import re
 import os
 import statistics
@@ -315,16 +316,53 @@ def traffic_record(kernel, workload):
 
 
 # ---------------------------------------------------------------- our arm --
-def flat_views(like, device, pin=False):
+class HugePinned:
+    """Page-locked host memory backed by transparent huge pages: anonymous
+    memory advised MADV_HUGEPAGE, touched, then registered with
+    cudaHostRegister.  The GPU's DMA then walks one translation per huge page
+    (512 MB on the 64 KB-page Arm hosts) instead of one per base page.
+    Measured on the GB300 host after a process that had used some 40 GB of
+    host memory exited: the double-buffered e2e upload from a torch pinned
+    buffer (base pages) took 152 ms per step while the device step ran
+    beside it, from this buffer 79 ms (the plain copy alone: 76 ms in both).
+    `tensor` is a uint8 tensor over the memory; close() unregisters it."""
+
+    def __init__(self, nbytes):
+        self.nbytes = max(int(nbytes), 1)
+        self.mm = mmap.mmap(-1, self.nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        if hasattr(self.mm, "madvise") and hasattr(mmap, "MADV_HUGEPAGE"):
+            self.mm.madvise(mmap.MADV_HUGEPAGE)
+        self.tensor = torch.frombuffer(self.mm, dtype=torch.uint8)
+        self.tensor.fill_(0)  # fault the pages in (huge pages where the kernel has them)
+        rc = torch.cuda.cudart().cudaHostRegister(self.tensor.data_ptr(), self.nbytes, 0)
+        self.registered = int(rc) == 0
+        if not self.registered:
+            raise RuntimeError(f"cudaHostRegister failed: {rc}")
+
+    def close(self):
+        if self.registered:
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaHostUnregister(self.tensor.data_ptr())
+            self.registered = False
+
+
+def flat_views(like, device, pin=False, huge=False):
     """One contiguous buffer holding a tensor of each shape/dtype of `like`
-    (offsets rounded up to 256 bytes) and the views into it."""
+    (offsets rounded up to 256 bytes) and the views into it.  With huge=True
+    (host only) the buffer is a HugePinned block; its owner is returned as a
+    third value (None otherwise), to be closed when the views are done."""
     offs, total = [], 0
     for x in like:
         offs.append(total)
         total += (x.numel() * x.element_size() + 255) // 256 * 256
-    buf = torch.empty(max(total, 1), dtype=torch.uint8, device=device, pin_memory=pin)
+    owner = None
+    if huge:
+        owner = HugePinned(total)
+        buf = owner.tensor
+    else:
+        buf = torch.empty(max(total, 1), dtype=torch.uint8, device=device, pin_memory=pin)
     views = [buf[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape) for o, x in zip(offs, like)]
-    return buf, views
+    return (buf, views, owner) if huge else (buf, views)
 
 
 def plain_h2d_rate(host_flat, dev_flat, dev, world, reps=2):
@@ -409,14 +447,14 @@ class numa_local:
 class E2EUploads:
     """Double-buffered gradient uploads of an end-to-end run.  The step's
     gradients live in one flat pinned host buffer (as a training loop's flat
-    gradient buffer would), and each step copies it with one cudaMemcpyAsync
-    into one of two flat device buffers, on its own stream, while the
-    previous step runs.  (291 separate pinned buffers, one copy each, measured
-    erratic on the GB300 host: 77 to 294 ms for the same 16 GB, against a
-    steady 76 ms for one flat buffer.)"""
+    gradient buffer would; huge-page backed, HugePinned), and each step
+    copies it with one cudaMemcpyAsync into one of two flat device buffers,
+    on its own stream, while the previous step runs.  (291 separate pinned
+    buffers, one copy each, measured erratic on the GB300 host: 77 to 294 ms
+    for the same 16 GB, against a steady 76 ms for one flat buffer.)"""
 
     def __init__(self, grads, dev):
-        self.host, hviews = flat_views(grads, "cpu", pin=True)
+        self.host, hviews, self.owner = flat_views(grads, "cpu", huge=True)
         for hv, g in zip(hviews, grads):
             hv.copy_(g)
         self.dev_flat, self.views = [], []
@@ -502,7 +540,7 @@ def run_e2e(args, wl, params, grads, states, step, t, world, dev):
     out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s",
            "h2d_bytes_per_step": up.nbytes, "d2h_bytes_per_step": n * 8, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"per-tensor sum(p^2) of the updated params ({n} float64; param norm {norm:.4f})",
-           "path": "one flat pinned host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
+           "path": "one flat pinned (huge-page backed) host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
                    "overlapping the previous step), AdafactorStep, device->host read of the step metric",
            "link": link, "host_numa": HOST_NUMA,
            "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
@@ -516,6 +554,7 @@ def run_e2e(args, wl, params, grads, states, step, t, world, dev):
         del host_pflat
     for st in states:
         st.pop("param_sq_sum", None)
+    up.owner.close()
     del up
     return out, t
 
@@ -724,9 +763,10 @@ def run_lamb_e2e(args, wl, params, grads, step, t, world, dev):
     out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": up.nbytes,
            "d2h_bytes_per_step": n * 8, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"per-tensor trust ratios ({n} float64; mean {float(host_tr.mean()):.4f})",
-           "path": "one flat pinned host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
+           "path": "one flat pinned (huge-page backed) host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
                    "overlapping the previous step), LambStep, device->host read of the trust ratios",
            "link": link, "host_numa": HOST_NUMA, "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
+    up.owner.close()
     del up
     return out, t
 
@@ -918,9 +958,10 @@ def run_came_e2e(args, wl, params, grads, states, step, t, world, dev):
     out = {"value": replica_throughput(wl.numel, world, ms), "unit": "params/s", "h2d_bytes_per_step": up.nbytes,
            "d2h_bytes_per_step": n * 4, "steps": args.e2e_steps, "ms_per_step": ms,
            "result_read": f"first updated value of each tensor ({n} float32)",
-           "path": "one flat pinned host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
+           "path": "one flat pinned (huge-page backed) host buffer of bf16 grads -> device in one copy (double-buffered, own stream, "
                    "overlapping the previous step), CameStep, device->host read of one value per tensor",
            "link": link, "host_numa": HOST_NUMA, "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
+    up.owner.close()
     del up
     return out
 
