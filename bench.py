@@ -544,7 +544,8 @@ def run_e2e(args, wl, params, grads, states, step, t, world, dev):
                    "overlapping the previous step), AdafactorStep, device->host read of the step metric",
            "link": link, "host_numa": HOST_NUMA,
            "frac_of_link": (link["ms"] / ms) if ms > 0 else None}
-    if args.readback_steps > 0:
+    # (one GPU only: each rank would pin another 32 GB of host memory)
+    if args.readback_steps > 0 and world == 1:
         host_pflat, readback = flat_views(params, "cpu", pin=True)
         rms = up.timed(args.readback_steps, compute, s_comp, world, dev)
         out["param_readback"] = {"ms_per_step": rms, "value": replica_throughput(wl.numel, world, rms),
