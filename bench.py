@@ -129,7 +129,7 @@ def tensor_class(shape, grad_bytes):
         return "elem_" + ("bf16" if grad_bytes == 2 else "f32")
     if grad_bytes == 2 and 2048 <= w <= 4096:
         return "rows_bf16"
-    if grad_bytes == 2 and 4096 < w <= 16384:
+    if grad_bytes == 2 and 4096 < w <= 14336:
         return "wide_bf16"
     return "vec_" + ("bf16" if grad_bytes == 2 else "f32")
 
@@ -837,8 +837,8 @@ def run_lamb(args, world, rank, local):
 # ------------------------------------------------------------------ CAME --
 def came_panel(shape, grad_bytes):
     """Whether the CAME step takes the row-panel pass for a contiguous,
-    256-byte aligned tensor: bf16 matrices with W % 8 == 0, 2048 <= W <= 16384."""
-    return len(shape) >= 2 and grad_bytes == 2 and int(shape[-1]) % 8 == 0 and 2048 <= int(shape[-1]) <= 16384
+    256-byte aligned tensor: bf16 matrices with W % 8 == 0, 2048 <= W <= 14336."""
+    return len(shape) >= 2 and grad_bytes == 2 and int(shape[-1]) % 8 == 0 and 2048 <= int(shape[-1]) <= 14336
 
 
 def came_bytes(shapes, grad_bytes):

@@ -43,10 +43,10 @@ __host__ __device__ inline bool is_fused(int32_t kind) { return kind == kFactore
 // keeps the column sums of the chunk in registers, 8 values x G column
 // groups of 256 per lane.  Two configurations:
 //   rows:  2048 <= W <= 4096,  8 warps x 2 groups, 256-row chunks;
-//   wide:  4096 <  W <= 16384, 16 warps x 4 groups, 128-row chunks.
+//   wide:  4096 <  W <= 14336, 14 warps x 4 groups, 128-row chunks.
 constexpr int kMinRowsW = 2048;   // narrower rows keep the tiled two-pass path
 constexpr int kMaxRowsW = 4096;   // 8 warps x 2 groups x 256 columns
-constexpr int kMaxWideW = 16384;  // 16 warps x 4 groups x 256 columns
+constexpr int kMaxWideW = 14336;  // 14 warps x 4 groups x 256 columns
 constexpr int kRowsChunk = 256;   // rows per work unit (rows configuration)
 constexpr int kQ8Group = 128;     // values per group of the 8-bit first moment
 constexpr int kWideChunk = 128;   // rows per work unit (wide configuration)
@@ -111,7 +111,7 @@ enum TensorClass : int32_t {
   kClsScalarF32 = 3,   // factored, element-wise path, fp32 grads
   kClsUnfactored = 4,  // ndim < 2 (any grad dtype)
   kClsRowsBF16 = 5,    // fused pass 1, bf16 grads, 2048 <= W <= 4096
-  kClsWideBF16 = 6,    // fused pass 1, bf16 grads, 4096 < W <= 16384
+  kClsWideBF16 = 6,    // fused pass 1, bf16 grads, 4096 < W <= 14336
   kClsFlatBF16 = 7,    // fused flat pass 1 (kFactoredFlat), bf16 grads
   kClsFlatF32 = 8,     // fused flat pass 1 (kFactoredFlat), fp32 grads
   kNumClasses = 9

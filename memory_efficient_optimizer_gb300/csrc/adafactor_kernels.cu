@@ -2035,7 +2035,9 @@ __global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
 // sum(u^2) = mean(row) * sum_j D_j / col_j (k_stats, k_scalars), so g is read
 // from HBM once here instead of twice.  Configurations: NW = 8 warps, G = 2
 // column groups of 256 per lane for 2048 <= W <= 4096 (2 CTAs per SM);
-// NW = 16, G = 4 for W <= 16384 (1 CTA per SM).
+// NW = 14, G = 4 for W <= 14336 (1 CTA per SM; the 56 column groups of
+// W = 14336 give every warp four: with 16 warps, half had three and waited
+// at each sub-panel's barrier for the others).
 constexpr int kRowsNW = 8, kRowsG = 2, kRowsS = 3, kRowsMinB = 2;
 
 // Dynamic shared memory of k_pass1_panel: ring and row shares, CTA-sum
@@ -2732,7 +2734,7 @@ Inst pick(KernelId k, TensorClass c, bool psq_in, int mom, bool psq_out) {
     case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, mom, psq_out);
     case kClsScalarF32: return pick_f<float, 1>(k, psq_in, mom, psq_out);
     case kClsRowsBF16: return pick_rows<__nv_bfloat16, kRowsNW, kRowsG, kRowsS, kRowsMinB>(k, psq_in, mom, psq_out);
-    case kClsWideBF16: return pick_rows<__nv_bfloat16, 16, 4, 3, 1>(k, psq_in, mom, psq_out);
+    case kClsWideBF16: return pick_rows<__nv_bfloat16, 14, 4, 3, 1>(k, psq_in, mom, psq_out);
     case kClsFlatBF16: return pick_flat<__nv_bfloat16>(k, psq_in, mom, psq_out);
     case kClsFlatF32: return pick_flat<float>(k, psq_in, mom, psq_out);
     case kClsUnfactored:

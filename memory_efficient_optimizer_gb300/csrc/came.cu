@@ -10,7 +10,7 @@
 // passes with small reductions between them:
 //
 //   k_came_pass_a   g -> per-tile row and column sums of g^2        (read g)
-//   k_came_panel    (bf16 matrices with 2048 <= W <= 16384, instead of
+//   k_came_panel    (bf16 matrices with 2048 <= W <= 14336, instead of
 //                   passes a and b) g -> the row EMA, per-chunk column sums
 //                   of g^2 and of g^2 / r_i: sum(u^2) without a second read
 //                   of g (the shared row-panel pass, row_panel.cuh)
@@ -86,7 +86,7 @@ struct CDev {
   int64_t ncc;         // column items per slice
   int32_t gdt, cls;
   // Row-panel tensors (panel = 1: 8 warps x 2 groups, W <= 4096; 2: 16 x 4,
-  // W <= 16384; 0: none): chunks of pr rows, prb per slice.
+  // W <= 14336; 0: none): chunks of pr rows, prb per slice.
   int32_t panel, pr;
   int64_t prb;
   int64_t pcol;        // float offset of the panel column partials [B][prb][W] (g^2 and g^2 / r)
@@ -816,7 +816,7 @@ constexpr size_t kPassCSmem = kColbufBytes + sizeof(float) * kTC;
 // Row-panel configurations (warps, column groups of 256 per lane, ring
 // stages, CTAs per SM; rows per chunk): the Adafactor step's two.
 constexpr int kP1NW = 8, kP1G = 2, kP1S = 3, kP1MinB = 2, kP1Rows = 256;   // 2048 <= W <= 4096
-constexpr int kP2NW = 16, kP2G = 4, kP2S = 3, kP2MinB = 1, kP2Rows = 128;  // 4096 < W <= 16384
+constexpr int kP2NW = 14, kP2G = 4, kP2S = 3, kP2MinB = 1, kP2Rows = 128;  // 4096 < W <= 14336
 template <int NW, int G, int S>
 constexpr size_t panel_smem() {
   return meo::panel::Cfg<__nv_bfloat16, NW, G, S>::kBytes + sizeof(double) * (NW + 1);
@@ -910,9 +910,9 @@ adaf_status make_plan(const came_tensor* tensors, const came_state* states, int3
       P->rchunks += d.B * d.nrc;
       P->item_idx.push_back(t);
       P->item_pf.push_back(P->item_pf.back() + d.B * (d.nrc + d.ncc));
-      // bf16 matrices of 2048 <= W <= 16384 on the vector path take the
+      // bf16 matrices of 2048 <= W <= 14336 on the vector path take the
       // row-panel pass instead of passes a and b
-      if (d.cls == kVecBF && d.W >= 2048 && d.W <= 16384) {
+      if (d.cls == kVecBF && d.W >= 2048 && d.W <= meo::kMaxWideW) {
         d.panel = d.W <= 4096 ? 1 : 2;
         d.pr = d.panel == 1 ? kP1Rows : kP2Rows;
         d.prb = cdiv(d.H, d.pr);

@@ -13,7 +13,7 @@
 // instead of twice.
 //
 // A work unit is a chunk of full rows [c0, c1) of one slice, taken by one CTA
-// of NW warps in sub-panels of SR = 32 / NW rows.  Lane l of warp w owns the
+// of NW warps in sub-panels of SR rows (32 / NW for NW <= 8, else 2).  Lane l of warp w owns the
 // column groups c * NW + w (c < G) of 256 columns, 8 consecutive columns
 // (256 (c NW + w) + 8 l + [0, 8)) in each, and keeps their column sums C_j
 // and D_j in registers.
@@ -52,13 +52,16 @@ namespace panel {
 // group c, lane), so every warp-wide copy and read touches 512 contiguous
 // bytes.  After the ring: the row shares [2][32] floats (kPartOff).
 template <typename GT, int NW, int G, int S> struct Cfg {
-  static constexpr int kSubRows = 32 / NW;
+  static constexpr int kSubRows = NW <= 8 ? 32 / NW : 2;
+  // a warp's total of row r is complete in lane r * kShareLanes after row_shares
+  static constexpr int kShareLanes = 32 / kSubRows;
   static constexpr int kPieces = static_cast<int>(sizeof(GT)) / 2;  // 16-byte pieces per 8 values
   static constexpr int kWarpBytes = kSubRows * G * kPieces * 32 * 16;
   static constexpr int kStageBytes = kWarpBytes * NW;
   static constexpr size_t kPartOff = static_cast<size_t>(S) * kStageBytes;
   static constexpr size_t kBytes = kPartOff + sizeof(float) * 2 * 32;  // ring + row shares
-  static_assert(kSubRows * NW == 32, "the row statistics take one (row, warp) share per lane");
+  static_assert(kSubRows * NW <= 32 && kShareLanes * kSubRows == 32 && (kSubRows == 2 || kSubRows == 4),
+                "the row statistics take at most one (row, warp) share per lane");
   static_assert(S >= 2, "the ring needs the stage in use and one in flight");
 };
 
@@ -289,8 +292,8 @@ __device__ __forceinline__ void run_chunk(unsigned char* smem, const GT* gb, con
     float rp[SR];
     if (full) phase_a<true, GT, NW, G, S, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
     else phase_a<false, GT, NW, G, S, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
-    const float tot = row_shares(rp, lane);  // warp total of row rl
-    if (lane % NW == 0) pk[rl * NW + warp] = tot;
+    const float tot = row_shares(rp, lane);  // warp total of row lane / kShareLanes
+    if (lane % C::kShareLanes == 0) pk[(lane / C::kShareLanes) * NW + warp] = tot;
     __syncthreads();
     // Refill the stage of sub-panel k - 1 (every lane is past it) with k + S - 1.
     {
@@ -305,10 +308,19 @@ __device__ __forceinline__ void run_chunk(unsigned char* smem, const GT* gb, con
       cp_async_commit();
     }
     // Row statistics of the sub-panel, in every warp: lane l adds the shares
-    // of row l / NW over the warps (fixed xor tree).
-    float R = pk[lane];
+    // of row l / NW over the warps (a fixed xor tree where SR * NW = 32, else
+    // in warp order; lanes past SR * NW hold no row).
+    float R = 0.f;
+    if constexpr (SR * NW == 32) {
+      R = pk[lane];
 #pragma unroll
-    for (int o = NW / 2; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
+      for (int o = NW / 2; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
+    } else {
+      if (rl < SR) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) R += pk[rl * NW + w];
+      }
+    }
     const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
     const float winv = __frcp_rn(rn);  // correctly rounded 1 / rn
     if (warp == 0 && lane % NW == 0 && s0 + rl < s1) {

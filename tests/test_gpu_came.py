@@ -47,9 +47,10 @@ def oracle_hp(hp):
 # matrices, 1-D tensors around the 8192-value units, an empty tensor; with
 # bf16 gradients the row-panel pass takes (4, 4096), (3, 2056) and (300, 2048)
 # (256-row chunks, a ragged last chunk), (2, 70, 4104) (128-row chunks, two
-# slices, a ragged column group) and (1, 16384)
+# slices, a ragged column group) and (1, 14336); (1, 16384) stays on the tiled passes
 SHAPES = [(1,), (5,), (8193,), (0,), (7, 13), (1, 37), (37, 1), (64, 64), (300, 1030), (257, 1032),
-          (2, 3, 520, 264), (2, 5, 9), (1000, 40), (4, 4096), (3, 2056), (300, 2048), (2, 70, 4104), (1, 16384)]
+          (2, 3, 520, 264), (2, 5, 9), (1000, 40), (4, 4096), (3, 2056), (300, 2048), (2, 70, 4104), (1, 14336),
+          (1, 16384)]
 HPARAMS = [
     dict(lr=1e-3),
     dict(lr=1e-3, weight_decay=0.1, clip_threshold=0.05),

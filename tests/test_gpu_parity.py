@@ -76,9 +76,9 @@ SMALL_SHAPES = [(1, 1), (2, 3), (3, 2), (1, 5), (5, 1), (2, 2, 3), (4,), (), (60
                 # bf16: fused row-chunk pass, 8-warp configuration (2048 <= W <= 4096): a
                 # one-lane last column group, two chunks with a ragged one, B = 2 slices
                 (300, 2056), (2, 130, 4096),
-                # bf16: 16-warp configuration (4096 < W <= 16384): ragged chunks and
-                # sub-panels, the widest row; W = 16392 and W = 2040 stay tiled
-                (131, 4104), (67, 14336), (3, 16384), (5, 16392), (9, 2040)]
+                # bf16: 14-warp configuration (4096 < W <= 14336): ragged chunks and
+                # sub-panels, the widest row; W = 16384, 16392 and 2040 stay tiled
+                (131, 4104), (67, 14336), (3, 16384), (5, 16392), (9, 2040), (7, 9000)]
 FLAGS = [
     dict(),
     dict(beta1=0.9, weight_decay=0.1),
