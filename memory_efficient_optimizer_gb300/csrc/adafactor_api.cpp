@@ -116,7 +116,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
                       const adaf_hparams* hp, bool full, Plan* plan, const adaf_shard* shards = nullptr) {
   if (n < 0) return fail(ADAF_ERR_INVALID_ARGUMENT, "n must be >= 0");
   if (n > 0 && tensors == nullptr) return fail(ADAF_ERR_INVALID_ARGUMENT, "tensors is NULL");
-  int64_t tiles = 0, p1units = 0, items = 0, nmrow = 0, nrowchunk = 0, ndsum = 0;
+  int64_t tiles = 0, p1units = 0, p1bound = 0, items = 0, nmrow = 0, nrowchunk = 0, ndsum = 0;
   int64_t nrowpart = 0, ncolpart = 0, ndpart = 0;
   int64_t nx1col = 0, nx1row = 0, ndloc = 0;
   plan->dev.clear();
@@ -244,6 +244,8 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       d.nrc = fused ? prb_rows : static_cast<int32_t>(ceil_div(H, meo::kRowChunk));
       d.prb = fused ? prb_rows : d.rb;
       nunits = fused ? B * prb_rows : ntiles;
+      // pass-1 units of either path (the sum(p^2) partials are per unit)
+      p1bound += std::max<int64_t>(ntiles, need_rows ? B * prb_rows : 0);
       items += B * (fused ? d.ncc : (d.nrc + d.ncc));
       d.mslot = nmrow;
       nmrow += B;
@@ -269,6 +271,7 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
       d.cb = static_cast<int32_t>(ntiles > INT32_MAX ? INT32_MAX : ntiles);
       d.kind = meo::kUnfactored;
       d.qg = ceil_div(numel, meo::kQ8Group);
+      p1bound += ntiles;
     }
     // Normalisation over the whole tensor, and the exchange layout of a row
     // shard (identical on every shard: it depends on B and W only).
@@ -374,8 +377,17 @@ adaf_status make_plan(const adaf_tensor* tensors, const adaf_state* states, int3
     off += align_up(plan->cls_idx[c].size() * sizeof(int32_t), 16);
   }
   plan->header_bytes = off;
-  off = align_up(off, 256);
-  const int64_t nppart = std::max(tiles, p1units);
+  // Scratch starts after a bound on the header that depends on the tensor
+  // count only: a tensor's class follows its pointers' alignment, and the
+  // 16-byte rounding of the per-class arrays with it, so the size query
+  // (without pointers) and the step must not use the header's exact size.
+  // Per class: three prefix arrays of members + 1 entries and the index
+  // array, each rounded up by at most 12 bytes; every tensor is in one class.
+  const size_t header_bound = kTableOffset + align_up(nd * sizeof(DevTensor), 256) +
+                              2 * align_up((nd + 1) * sizeof(int32_t), 16) +
+                              (4 * nd + 3 * meo::kNumClasses) * sizeof(int32_t) + 4 * 12 * meo::kNumClasses;
+  off = align_up(header_bound, 256);
+  const int64_t nppart = std::max(tiles, std::max(p1units, p1bound));
   auto region = [&](size_t* where, size_t bytes) {
     *where = off;
     off = align_up(off + bytes, 256);

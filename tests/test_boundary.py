@@ -133,6 +133,38 @@ def test_step_argument_errors_before_any_cuda_call(lib):
     assert str(need) in B.adafactor_last_error()
 
 
+# Shapes of every class (flat, rows, wide, tiled vector and element-wise, 1D)
+SIZE_SHAPES = [(1, 1), (2, 3), (3, 2), (1, 5), (5, 1), (2, 2, 3), (4,), (), (600, 2100), (257, 1025), (3, 4097),
+               (1000, 1032), (2, 3, 520, 264), (7, 1, 9), (1, 65536), (9000,), (700, 33), (300, 1023), (513, 7),
+               (260, 1), (1030, 3), (130, 100), (91, 200), (50, 512), (40, 513), (33, 32), (17, 16), (300, 2056),
+               (2, 130, 4096), (131, 4104), (67, 14336), (3, 16384), (5, 16392), (9, 2040), (7, 9000), (129, 5000),
+               (1, 8192)]
+
+
+@pytest.mark.parametrize("dtype", [B.ADAF_FLOAT32, B.ADAF_BFLOAT16])
+@pytest.mark.parametrize("misalign", [(), (1, 5, 9), tuple(range(0, 20, 2)), tuple(range(20))])
+def test_workspace_size_does_not_depend_on_pointer_alignment(lib, dtype, misalign):
+    """The size query has no pointers; the step picks each tensor's path from
+    its pointers' alignment (16-byte aligned rows take the vector, row-chunk
+    and flat paths, others the element-wise one).  The query's size must do
+    for every such choice: the step's own check passes (and, without a GPU,
+    the call then fails at its first CUDA call instead)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU")
+    ts, ss = fake_list(SIZE_SHAPES, dtype=dtype)
+    esz = 2 if dtype == B.ADAF_BFLOAT16 else 4
+    for k in misalign:
+        ts[k].grad += esz  # still aligned to its element, no longer to 16 bytes
+    need = B.adafactor_workspace_size(ts, len(SIZE_SHAPES))
+    assert call_step(ts, ss, len(SIZE_SHAPES), wsb=need) == B.ADAF_ERR_CUDA, B.adafactor_last_error()
+    sh = fake_shards([s[-2] * 2 if len(s) >= 2 else (s[0] if s else 1) * 2 for s in SIZE_SHAPES])
+    ws, r1, r2 = B.adafactor_shard_sizes(ts, sh, len(SIZE_SHAPES))
+    rounds = [1 << 41]
+    assert call_shard("adafactor_shard_begin", ts, ss, sh, len(SIZE_SHAPES), rounds, wsb=ws) == B.ADAF_ERR_CUDA, \
+        B.adafactor_last_error()
+
+
 def test_empty_list_and_empty_tensors_are_no_ops(lib):
     ts, ss = fake_list([(0, 5), (0,)])
     ts[0].param = ts[0].grad = ts[1].param = ts[1].grad = 0  # empty tensors may have no storage

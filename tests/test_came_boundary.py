@@ -98,3 +98,24 @@ def test_kernel_names(lib):
     assert [B.came_kernel_name(k) for k in range(B.came_num_kernels())] == [
         "k_came_pass_a", "k_came_stats", "k_came_means", "k_came_pass_b", "k_came_clip", "k_came_pass_c",
         "k_came_pass_d", "k_came_panel"]
+
+
+@pytest.mark.parametrize("dtype", [B.ADAF_FLOAT32, B.ADAF_BFLOAT16])
+@pytest.mark.parametrize("misalign", [(), (1, 5, 9), tuple(range(0, 16, 2)), tuple(range(16))])
+def test_workspace_size_does_not_depend_on_pointer_alignment(lib, dtype, misalign):
+    """The size query has no pointers; the step picks each tensor's path from
+    its pointers' alignment.  The query's size must do for every choice: the
+    step's own check passes and, without a GPU, the call fails at its first
+    CUDA call instead."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU")
+    shapes = [(1, 1), (2, 3), (5, 1), (2, 2, 3), (4,), (), (600, 2100), (257, 1025), (1000, 1032), (700, 33),
+              (300, 2056), (2, 130, 4096), (131, 4104), (67, 14336), (3, 16384), (129, 5000)]
+    t = tensors(shapes, dtype)
+    for k in misalign:
+        t[k].g += 2 if dtype == B.ADAF_BFLOAT16 else 4
+    need = B.came_workspace_size(t, len(shapes))
+    with pytest.raises(B.AdafactorError) as e:
+        B.came_step(t, states(shapes), len(shapes), 1, make_came_hparams(lr=1e-3), 1 << 40, need, 0)
+    assert e.value.status == B.ADAF_ERR_CUDA, str(e.value)

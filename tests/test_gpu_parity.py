@@ -77,8 +77,10 @@ SMALL_SHAPES = [(1, 1), (2, 3), (3, 2), (1, 5), (5, 1), (2, 2, 3), (4,), (), (60
                 # one-lane last column group, two chunks with a ragged one, B = 2 slices
                 (300, 2056), (2, 130, 4096),
                 # bf16: 14-warp configuration (4096 < W <= 14336): ragged chunks and
-                # sub-panels, the widest row; W = 16384, 16392 and 2040 stay tiled
-                (131, 4104), (67, 14336), (3, 16384), (5, 16392), (9, 2040), (7, 9000)]
+                # sub-panels, the widest row, chunks of one sub-panel; W = 16384, 16392
+                # and 2040 stay tiled
+                (131, 4104), (67, 14336), (3, 16384), (5, 16392), (9, 2040), (7, 9000), (129, 5000),
+                (1, 8192)]
 FLAGS = [
     dict(),
     dict(beta1=0.9, weight_decay=0.1),

@@ -82,3 +82,23 @@ def test_empty_list_is_a_no_op(lib):
 def test_kernel_names(lib):
     assert [B.lamb_kernel_name(k) for k in range(B.lamb_num_kernels())] == [
         "k_lamb_moments", "k_lamb_trust", "k_lamb_update"]
+
+
+@pytest.mark.parametrize("dtype", [B.ADAF_FLOAT32, B.ADAF_BFLOAT16])
+@pytest.mark.parametrize("misalign", [(), (1, 3), tuple(range(0, 8, 2)), tuple(range(8))])
+def test_workspace_size_does_not_depend_on_pointer_alignment(lib, dtype, misalign):
+    """The size query has no pointers; the step picks each tensor's path from
+    its pointers' alignment.  The query's size must do for every choice: the
+    step's own check passes and, without a GPU, the call fails at its first
+    CUDA call instead."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU")
+    sizes = [1, 7, 100, 4096, 8192 * 3 + 5, 1 << 20, 33, 8]
+    t = tensors(sizes, dtype)
+    for k in misalign:
+        t[k].g += 2 if dtype == B.ADAF_BFLOAT16 else 4
+    need = B.lamb_workspace_size(t, len(sizes))
+    with pytest.raises(B.AdafactorError) as e:
+        B.lamb_step(t, len(sizes), 1, hp(), 1 << 40, need, 0)
+    assert e.value.status == B.ADAF_ERR_CUDA, str(e.value)
