@@ -1672,7 +1672,7 @@ __device__ __forceinline__ double consumer_sum(float v, double* red) {
 // the same two values, in either order), hence the same row EMA and
 // 1 / row_i; each lane then adds its values to C_j and g^2 / row_i to D_j in
 // registers.  The old row statistics of a warp's rows in a chunk are loaded
-// one chunk ahead, one per lane.  At the unit's end the warps' (pairs')
+// kFlatRoldAhead chunks ahead, one per lane.  At the unit's end the warps' (pairs')
 // column partials meet in shared memory and are added in warp (pair) order,
 // while the producer already streams the next unit.  The values past a
 // slice's last 16-byte boundary (fewer than 16 bytes) are read from global
@@ -1684,6 +1684,7 @@ constexpr int kFlatHalfW = 512;                // widest row one warp takes
 constexpr int kFlatPairs = kWarps / 2;         // warp pairs of the wide form
 constexpr int kFlatThreads = (kWarps + 1) * 32;  // 8 consumer warps + the producer warp
 constexpr int kFlatMinB = 2;                   // CTAs per SM
+constexpr int kFlatRoldAhead = 4;              // chunks of old row statistics in flight per warp
 // Named barrier 2 + pair, the pair's two warps only (barrier 1 is the
 // consumers' barrier).
 __device__ __forceinline__ void pair_sync(int pair) {
@@ -1764,7 +1765,7 @@ __device__ __forceinline__ void flat_produce(const StepArgs& a, const Range& r, 
 template <typename GT, int CPL, bool PSQ, bool HALF>
 __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs& a, int64_t local,
                                              const unsigned char* ring, uint64_t* full, uint64_t* empty, float* cw,
-                                             float* xs, double* red, uint32_t& it, bool& dead, int* stop,
+                                             float* xs, float* rq, double* red, uint32_t& it, bool& dead, int* stop,
                                              const float3 bc) {
   // Fields are read where they are used (dt is not restrict: the stores in
   // between make the compiler read the epilogue's fields again instead of
@@ -1795,12 +1796,27 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
   // (the groups of a chunk go round the warps starting where the previous
   // chunk's left off, so a warp's extra rows move to the next warps chunk by
   // chunk instead of always falling to the same ones)
-  auto load_rold = [&](int r0, int gi0) {
-    const int rows = min(R, nr - r0);
-    const int rl = (gi0 + (lane / spg) * NS) * spg + lane % spg;
-    return rl < rows ? rowst[r0 + rl] : 0.f;
-  };
   auto first_group = [&](int goff) { return (set - goff + NS) % NS; };
+  // The old row statistics are copied kFlatRoldAhead chunks ahead (a chunk
+  // is a few hundred cycles of work per warp, less than a load from HBM
+  // takes while the copies stream), each lane's value with a 4-byte
+  // cp.async into its slot of this warp's queue rq (kFlatRoldAhead + 1
+  // slots of 32 floats: the slot being refilled is never the one being
+  // read), one commit group per chunk.  Every chunk before the last has
+  // gpc row groups, so the chunk kFlatRoldAhead ahead of one with group
+  // offset goff starts at group offset goff + kFlatRoldAhead * gpc.
+  const int gpc = (R + spg - 1) / spg;
+  auto prefetch = [&](int c0r, int cgoff, int slot) {
+    if (c0r < nr) {
+      const int rl = (first_group(cgoff) + (lane / spg) * NS) * spg + lane % spg;
+      if (rl < min(R, nr - c0r))
+        panel::cp_async4(static_cast<uint32_t>(__cvta_generic_to_shared(rq + slot * 32 + lane)), rowst + c0r + rl);
+    }
+    panel::cp_async_commit();  // (empty past the unit's end: the group count stays in step)
+  };
+#pragma unroll 1
+  for (int k = 0; k < kFlatRoldAhead; ++k) prefetch(k * R, (k * gpc) % NS, k);
+  int cq = 0;  // slot of the current chunk
 
   // column sums in pairs of columns (k, k + 1): packed fp32x2 arithmetic
   constexpr int NP = (CPL + 1) / 2;
@@ -1810,14 +1826,17 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
   float rsum = 0.f;
   int parity = 0;  // exchange buffer of the wide form
   int goff = 0;  // row groups of the unit's earlier chunks, mod NS
-  float rcur = load_rold(0, first_group(0));
 #pragma unroll 1
   for (int r0 = 0; r0 < nr; r0 += R, ++it) {
     const int rows = min(R, nr - r0);
     const int ngc = (min(R, nr - r0) + spg - 1) / spg;  // row groups in the chunk
     const int gi0 = first_group(goff);
     const int goff_next = (goff + ngc) % NS;
-    const float rnext = r0 + R < nr ? load_rold(r0 + R, first_group(goff_next)) : 0.f;
+    // this chunk's group is complete once at most kFlatRoldAhead - 1 are pending
+    panel::cp_async_wait<kFlatRoldAhead - 1>();
+    const float rcur = (gi0 + (lane / spg) * NS) * spg + lane % spg < rows ? rq[cq * 32 + lane] : 0.f;
+    prefetch(r0 + kFlatRoldAhead * R, (goff + kFlatRoldAhead * gpc) % NS, cq == 0 ? kFlatRoldAhead : cq - 1);
+    cq = cq == kFlatRoldAhead ? 0 : cq + 1;
     const uint32_t slot = it % kFlatSlots, ph = (it / kFlatSlots) & 1u;
     if (!dead && !mbar_wait(&full[slot], ph)) {
       if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
@@ -1825,13 +1844,15 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
       dead = true;
     }
     const GT* sb = reinterpret_cast<const GT*>(ring + slot * kFlatChunkBytes);
-    // a chunk that reaches past the unit's last 16-byte boundary is read
-    // from global memory (only the last chunk of a slice)
-    const bool from_g = (r0 + rows) * w > f.cpy;
+    // the row group that reaches past the unit's last 16-byte boundary (in
+    // the last chunk of a slice) is read from global memory: the bulk copy
+    // stops at the boundary
+    const bool tail = (r0 + rows) * w > f.cpy;
 #pragma unroll 1
     for (int gi = gi0, t = 0; gi < ngc; gi += NS, ++t) {
       const int rl = gi * spg + sub;  // row within the chunk
       const bool ok = rl < rows && !dead;
+      const bool from_g = tail && (r0 + min((gi + 1) * spg, rows)) * w > f.cpy;  // warp-uniform
       float x[2 * NP];
       x[2 * NP - 1] = 0.f;
       if (from_g) {
@@ -1886,7 +1907,6 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
     }
     __syncwarp();
     if (lane == 0 && !dead) mbar_arrive(&empty[slot]);
-    rcur = rnext;
     goff = goff_next;
   }
   // narrow rows: add the warp's row segments column by column (lanes with
@@ -1966,14 +1986,17 @@ __device__ __forceinline__ void flat_consume(const DevTensor* dt, const StepArgs
 
 // Shared memory of k_pass1_flat: the ring, the column partials (8 sets of
 // 512 columns or 4 pairs of 1024), the pair exchange (2 buffers x 8 warps),
-// CTA-sum scratch (2 x 8 doubles), mbarriers, member prefix.
+// the warps' queues of old row statistics, CTA-sum scratch (2 x 8 doubles),
+// mbarriers, member prefix.
 constexpr size_t kFlatRing = static_cast<size_t>(kFlatChunkBytes) * kFlatSlots;
 constexpr size_t kFlatCw = sizeof(float) * kWarps * kFlatHalfW;
 constexpr size_t kFlatXs = sizeof(float) * 2 * kWarps;
-constexpr size_t kFlatSmem = kFlatRing + kFlatCw + kFlatXs + kRedBytes + sizeof(uint64_t) * 2 * kFlatSlots +
-                             kPrefixBytes;
+constexpr size_t kFlatRqWarp = static_cast<size_t>(kFlatRoldAhead + 1) * 32;  // floats per warp
+constexpr size_t kFlatRq = sizeof(float) * kWarps * kFlatRqWarp;
+constexpr size_t kFlatSmem = kFlatRing + kFlatCw + kFlatXs + kFlatRq + kRedBytes +
+                             sizeof(uint64_t) * 2 * kFlatSlots + kPrefixBytes;
 static_assert(kWarps * kFlatHalfW == kFlatPairs * kTileCols && kRedBytes >= sizeof(double) * 2 * kWarps &&
-                  (kFlatRing + kFlatCw + kFlatXs) % 8 == 0,
+                  (kFlatRing + kFlatCw + kFlatXs + kFlatRq) % 8 == 0,
               "shared-memory layout of the flat pass");
 template <typename GT, bool PSQ>
 __global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
@@ -1982,7 +2005,7 @@ __global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
   unsigned char* ring = smem;
   float* cw = reinterpret_cast<float*>(smem + kFlatRing);
   float* xs = reinterpret_cast<float*>(smem + kFlatRing + kFlatCw);
-  double* red = reinterpret_cast<double*>(smem + kFlatRing + kFlatCw + kFlatXs);
+  double* red = reinterpret_cast<double*>(smem + kFlatRing + kFlatCw + kFlatXs + kFlatRq);
   uint64_t* full = reinterpret_cast<uint64_t*>(red + kRedBytes / sizeof(double));
   uint64_t* empty = full + kFlatSlots;
   int32_t* pf = reinterpret_cast<int32_t*>(empty + kFlatSlots);
@@ -1994,6 +2017,7 @@ __global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
     if (lane == 0) flat_produce<GT>(a, r, pf, ng, ring, full, empty);
     return;
   }
+  float* rq = reinterpret_cast<float*>(smem + kFlatRing + kFlatCw + kFlatXs) + warp * kFlatRqWarp;  // this warp's
   const int64_t u1 = pf[ng];
   uint32_t it = 0;
   bool dead = false;
@@ -2007,7 +2031,7 @@ __global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
     const int64_t local = u - pf[m];
     // columns per lane, rounded up to even (whole rows per warp up to 512)
     const int64_t cpl = (d->W + 31) / 32;
-#define MEO_FLAT(C, HF) flat_consume<GT, C, PSQ, HF>(d, a, local, ring, full, empty, cw, xs, red, it, dead, &stop, bc)
+#define MEO_FLAT(C, HF) flat_consume<GT, C, PSQ, HF>(d, a, local, ring, full, empty, cw, xs, rq, red, it, dead, &stop, bc)
     switch (cpl) {
       case 1: MEO_FLAT(1, false); break;
       case 2: MEO_FLAT(2, false); break;
@@ -2037,24 +2061,47 @@ __global__ void __launch_bounds__(kFlatThreads, kFlatMinB)
 // column groups of 256 per lane for 2048 <= W <= 4096 (2 CTAs per SM);
 // NW = 14, G = 4 for W <= 14336 (1 CTA per SM; the 56 column groups of
 // W = 14336 give every warp four: with 16 warps, half had three and waited
-// at each sub-panel's barrier for the others).
+// at each sub-panel's barrier for the others), in the split form (a ring of
+// 4 stages of 2-row sub-panels; the row shares meet at an mbarrier that each
+// warp waits on one sub-panel later, instead of at a CTA barrier).
 constexpr int kRowsNW = 8, kRowsG = 2, kRowsS = 3, kRowsMinB = 2;
 
 // Dynamic shared memory of k_pass1_panel: ring and row shares, CTA-sum
-// scratch (64 doubles), member prefix.
+// scratch (64 doubles), and the member prefix where it still fits the CTA's
+// 227 KB (a ring of 4 stages of 56 KB does not leave room for it; the prefix
+// is then read from global memory, a few loads per chunk of rows).
 template <typename GT, int NW, int G, int S> struct PanelCfg {
   static constexpr size_t kRedOff = panel::Cfg<GT, NW, G, S>::kBytes;
-  static constexpr size_t kSmem = kRedOff + sizeof(double) * 64 + kPrefixBytes;
+  static constexpr size_t kBase = kRedOff + sizeof(double) * 64;
+  static constexpr bool kSmemPrefix = kBase + kPrefixBytes <= 227 * 1024;
+  static constexpr size_t kSmem = kBase + (kSmemPrefix ? kPrefixBytes : 0);
   static_assert(kRedOff % 8 == 0 && NW + 1 <= 64, "the CTA sum needs NW + 1 aligned doubles");
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 };
 
 template <typename GT, int NW, int G, int S, int MINB, bool PSQ>
 __global__ void __launch_bounds__(NW * 32, MINB)
     k_pass1_panel(const __grid_constant__ StepArgs a, const Range r) {
+  using PC = PanelCfg<GT, NW, G, S>;
   extern __shared__ __align__(16) unsigned char smem[];
-  double* red = reinterpret_cast<double*>(smem + PanelCfg<GT, NW, G, S>::kRedOff);
-  int32_t* pf = reinterpret_cast<int32_t*>(red + 64);
-  const int ng = load_prefix(pf, r);
+  double* red = reinterpret_cast<double*>(smem + PC::kRedOff);
+  const int32_t* pf;
+  int ng;
+  if constexpr (PC::kSmemPrefix) {
+    int32_t* spf = reinterpret_cast<int32_t*>(red + 64);
+    ng = load_prefix(spf, r);
+    pf = spf;
+  } else {
+    ng = r.m_end - r.m_begin;
+    pf = r.pf + r.m_begin;
+  }
+  constexpr bool kSplit = panel::Cfg<GT, NW, G, S>::kSplit;
+  if constexpr (kSplit) {
+    if (threadIdx.x == 0) panel::split_init<GT, NW, G, S>(smem);
+    __syncthreads();
+  }
+  uint32_t q = 0;     // sub-panels done (split form)
+  bool dead = false;  // a split-form wait ran out
   const int64_t u1 = pf[ng];
   const float b2 = static_cast<float>(a.beta2), omb2 = static_cast<float>(1.0 - a.beta2);
   const float eps1 = static_cast<float>(a.eps1);
@@ -2073,8 +2120,12 @@ __global__ void __launch_bounds__(NW * 32, MINB)
       return panel::Partials{a.colpart + d.colpart + off, a.dpart + d.dpart + off};
     };
     float rsum = 0.f, psq = 0.f;
-    panel::run_chunk<GT, NW, G, S, PSQ>(smem, gb, pb, d.row + static_cast<int64_t>(b) * H, W, c0, c1, b2, omb2, eps1,
-                                        where, rsum, psq);
+    if constexpr (kSplit)
+      panel::run_chunk_split<GT, NW, G, S, PSQ>(smem, gb, pb, d.row + static_cast<int64_t>(b) * H, W, c0, c1, b2,
+                                                omb2, eps1, where, rsum, psq, q, dead, a.status);
+    else
+      panel::run_chunk<GT, NW, G, S, PSQ>(smem, gb, pb, d.row + static_cast<int64_t>(b) * H, W, c0, c1, b2, omb2,
+                                          eps1, where, rsum, psq);
     // (the barriers of the CTA sums also order this chunk's last reads of
     // the ring before the next chunk's prologue refills it)
     const double rtot = panel::block_sum<NW>(static_cast<double>(rsum), red);
@@ -2734,7 +2785,7 @@ Inst pick(KernelId k, TensorClass c, bool psq_in, int mom, bool psq_out) {
     case kClsScalarBF16: return pick_f<__nv_bfloat16, 1>(k, psq_in, mom, psq_out);
     case kClsScalarF32: return pick_f<float, 1>(k, psq_in, mom, psq_out);
     case kClsRowsBF16: return pick_rows<__nv_bfloat16, kRowsNW, kRowsG, kRowsS, kRowsMinB>(k, psq_in, mom, psq_out);
-    case kClsWideBF16: return pick_rows<__nv_bfloat16, 14, 4, 3, 1>(k, psq_in, mom, psq_out);
+    case kClsWideBF16: return pick_rows<__nv_bfloat16, 14, 4, 4, 1>(k, psq_in, mom, psq_out);
     case kClsFlatBF16: return pick_flat<__nv_bfloat16>(k, psq_in, mom, psq_out);
     case kClsFlatF32: return pick_flat<float>(k, psq_in, mom, psq_out);
     case kClsUnfactored:

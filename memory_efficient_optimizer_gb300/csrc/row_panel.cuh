@@ -37,6 +37,15 @@
 //   B. add g_rj^2 / r into D_j from the same staged values.
 // Per chunk the warps write C_j and D_j (column partials of the chunk), and
 // warp 0 accumulates sum_r r (for mean(r)).
+//
+// Split form (rings of S >= 4 stages, run_chunk_split): the CTA barrier is
+// replaced by an mbarrier per sub-panel that the lanes holding row shares
+// arrive on after phase A, and the warps wait on it only one sub-panel later:
+// iteration k runs phase A of sub-panel k, then the row statistics and phase
+// B of sub-panel k - 1.  A warp that is ahead no longer stops at every
+// sub-panel for the slowest one; it waits only when it is a whole phase
+// ahead.  Two sub-panels are in use per lane (k and k - 1), so the ring needs
+// a fourth stage to keep two in flight.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -44,25 +53,38 @@
 
 #include <cstdint>
 
+#include "adafactor_internal.h"
+
 namespace meo {
 namespace panel {
 
 // Shared-memory ring: per stage and warp, slot ((rr * G + c) * kPieces + q)
 // * 32 + lane holds 16 bytes (piece q of the 8 values of row rr, column
 // group c, lane), so every warp-wide copy and read touches 512 contiguous
-// bytes.  After the ring: the row shares [2][32] floats (kPartOff).
+// bytes.  After the ring: the row shares, kShareBufs buffers of 32 floats
+// (kPartOff; share of row r from warp w at r * kShareLanes + w), then, in
+// the split form, its two mbarriers (kBarOff).
 template <typename GT, int NW, int G, int S> struct Cfg {
   static constexpr int kSubRows = NW <= 8 ? 32 / NW : 2;
-  // a warp's total of row r is complete in lane r * kShareLanes after row_shares
+  // a warp's total of row r is complete in lane r * kShareLanes after
+  // row_shares; after the row statistics, lane r * kShareLanes holds 1 / r
   static constexpr int kShareLanes = 32 / kSubRows;
   static constexpr int kPieces = static_cast<int>(sizeof(GT)) / 2;  // 16-byte pieces per 8 values
   static constexpr int kWarpBytes = kSubRows * G * kPieces * 32 * 16;
   static constexpr int kStageBytes = kWarpBytes * NW;
+  static constexpr bool kSplit = S >= 4;
+  // share buffers: written at sub-panel q, read at q + 1; in the split form
+  // a warp can write q + 3 only after every warp has arrived for q + 2, so
+  // after every warp has read q (4 buffers)
+  static constexpr int kShareBufs = kSplit ? 4 : 2;
   static constexpr size_t kPartOff = static_cast<size_t>(S) * kStageBytes;
-  static constexpr size_t kBytes = kPartOff + sizeof(float) * 2 * 32;  // ring + row shares
-  static_assert(kSubRows * NW <= 32 && kShareLanes * kSubRows == 32 && (kSubRows == 2 || kSubRows == 4),
+  static constexpr size_t kBarOff = kPartOff + sizeof(float) * 32 * kShareBufs;
+  static constexpr size_t kBytes = kBarOff + (kSplit ? 2 * sizeof(uint64_t) : 0);
+  static_assert(kSubRows * NW <= 32 && kShareLanes * kSubRows == 32 && NW <= kShareLanes &&
+                    (kSubRows == 2 || kSubRows == 4),
                 "the row statistics take at most one (row, warp) share per lane");
   static_assert(S >= 2, "the ring needs the stage in use and one in flight");
+  static_assert(kBarOff % 8 == 0, "mbarrier alignment");
 };
 
 // 16-byte asynchronous global -> shared copy (bypasses L1).
@@ -182,9 +204,9 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
 // in fp32 for a bf16 x, so fma(x, x, acc) equals acc + x * x.
 template <bool FULL, typename GT, int NW, int G, int S, bool PSQ>
 __device__ __forceinline__ void phase_a(const unsigned char* st, int32_t s0, int32_t s1, int32_t W, int warp,
-                                        int lane, const float* pb, float2 (&cacc)[G][4], float (&rp)[32 / NW],
-                                        float& psq) {
-  constexpr int SR = 32 / NW, P = Cfg<GT, NW, G, S>::kPieces;
+                                        int lane, const float* pb, float2 (&cacc)[G][4],
+                                        float (&rp)[Cfg<GT, NW, G, S>::kSubRows], float& psq) {
+  constexpr int SR = Cfg<GT, NW, G, S>::kSubRows, P = Cfg<GT, NW, G, S>::kPieces;
 #pragma unroll
   for (int rr = 0; rr < SR; ++rr) {
     float2 s2 = make_float2(0.f, 0.f);
@@ -213,14 +235,14 @@ __device__ __forceinline__ void phase_a(const unsigned char* st, int32_t s0, int
   }
 }
 
-// Phase B: g^2 / r into D_j (lane rr * NW holds 1 / r of row rr).
+// Phase B: g^2 / r into D_j (lane rr * kShareLanes holds 1 / r of row rr).
 template <bool FULL, typename GT, int NW, int G, int S>
 __device__ __forceinline__ void phase_b(const unsigned char* st, int32_t s0, int32_t s1, int32_t W, int warp,
                                         int lane, float winv, float2 (&dacc)[G][4]) {
-  constexpr int SR = 32 / NW, P = Cfg<GT, NW, G, S>::kPieces;
+  constexpr int SR = Cfg<GT, NW, G, S>::kSubRows, P = Cfg<GT, NW, G, S>::kPieces;
 #pragma unroll
   for (int rr = 0; rr < SR; ++rr) {
-    const float wr = __shfl_sync(0xffffffffu, winv, rr * NW);
+    const float wr = __shfl_sync(0xffffffffu, winv, rr * Cfg<GT, NW, G, S>::kShareLanes);
     const float2 w2 = make_float2(wr, wr);
 #pragma unroll
     for (int c = 0; c < G; ++c) {
@@ -235,21 +257,62 @@ __device__ __forceinline__ void phase_b(const unsigned char* st, int32_t s0, int
   }
 }
 
+
+// Row statistics of a sub-panel from its row shares pk (share of row r from
+// warp w at r * kShareLanes + w): lane l adds the NW shares of row
+// l / kShareLanes with a fixed xor tree over its kShareLanes lanes (slots
+// past NW hold no share and count 0), forms r = b2 r_old + (1 - b2)(sum / W +
+// eps1) and returns 1 / r; r is stored (and added to rsum) by warp 0's lane
+// of each row inside [s0, s1).
+template <typename GT, int NW, int G, int S>
+__device__ __forceinline__ float row_stats(const float* pk, int lane, int warp, float row_old, int32_t s0,
+                                           int32_t s1, float* rowst, float invw, float b2, float omb2, float eps1,
+                                           float& rsum) {
+  constexpr int SL = Cfg<GT, NW, G, S>::kShareLanes;
+  const int rl = lane / SL;
+  float R = (lane % SL < NW) ? pk[lane] : 0.f;
+#pragma unroll
+  for (int o = SL / 2; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
+  const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
+  if (warp == 0 && lane % SL == 0 && s0 + rl < s1) {
+    rowst[s0 + rl] = rn;
+    rsum += rn;
+  }
+  return __frcp_rn(rn);  // correctly rounded 1 / rn
+}
+
 // Where a chunk's column partials go: C_j to cp[0, W), D_j to dp[0, W).
 struct Partials {
   float* cp;
   float* dp;
 };
 
+template <int NW, int G>
+__device__ __forceinline__ void store_partials(const Partials& out, int32_t W, int warp, int lane,
+                                               const float2 (&cacc)[G][4], const float2 (&dacc)[G][4]) {
+#pragma unroll
+  for (int c = 0; c < G; ++c) {
+    const int32_t j = (c * NW + warp) * 256 + lane * 8;
+    if (j < W) {
+      float* cp = out.cp + j;
+      float* dp = out.dp + j;
+      *reinterpret_cast<float4*>(cp) = make_float4(cacc[c][0].x, cacc[c][0].y, cacc[c][1].x, cacc[c][1].y);
+      *reinterpret_cast<float4*>(cp + 4) = make_float4(cacc[c][2].x, cacc[c][2].y, cacc[c][3].x, cacc[c][3].y);
+      *reinterpret_cast<float4*>(dp) = make_float4(dacc[c][0].x, dacc[c][0].y, dacc[c][1].x, dacc[c][1].y);
+      *reinterpret_cast<float4*>(dp + 4) = make_float4(dacc[c][2].x, dacc[c][2].y, dacc[c][3].x, dacc[c][3].y);
+    }
+  }
+}
+
 // One chunk of rows [c0, c1) of one slice (gb: the slice's gradient, pb its
 // parameter, read only with PSQ; rowst: the slice's row statistic, updated in
 // place).  Writes the chunk's column partials to where(), a callable that
 // returns a Partials (evaluated after the rows, so that its operands need not
 // stay in registers through the loop).  On return rsum holds, in lanes
-// l % NW == 0 of warp 0, this thread's part of sum_r r over the chunk (0
-// elsewhere), and psq this thread's part of sum(p^2); the caller adds them
-// over the CTA.  smem: the ring and row shares of Cfg (kBytes).  Every
-// thread of the CTA must call; the next call may follow directly (the
+// l % kShareLanes == 0 of warp 0, this thread's part of sum_r r over the
+// chunk (0 elsewhere), and psq this thread's part of sum(p^2); the caller
+// adds them over the CTA.  smem: the ring and row shares of Cfg (kBytes).
+// Every thread of the CTA must call; the next call may follow directly (the
 // caller's CTA barrier, e.g. the one in block_sum, separates this chunk's
 // last reads of the ring from the next chunk's first copies).
 template <typename GT, int NW, int G, int S, bool PSQ, typename Where>
@@ -258,11 +321,11 @@ __device__ __forceinline__ void run_chunk(unsigned char* smem, const GT* gb, con
                                           Where&& where, float& rsum, float& psq) {
   using C = Cfg<GT, NW, G, S>;
   constexpr int SR = C::kSubRows;
-  float* part = reinterpret_cast<float*>(smem + C::kPartOff);  // [2][SR][NW]
+  float* part = reinterpret_cast<float*>(smem + C::kPartOff);  // [2][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned char* mine = smem + warp * C::kWarpBytes + lane * 16;
   const uint32_t mine_s = static_cast<uint32_t>(__cvta_generic_to_shared(mine));
-  const int rl = lane / NW;  // row of this lane's (row, warp) share
+  const int rl = lane / C::kShareLanes;  // row of this lane's row statistic
   const int32_t nsub = (c1 - c0 + SR - 1) / SR;
   const float invw = 1.0f / static_cast<float>(W);
   float2 cacc[G][4], dacc[G][4];
@@ -293,7 +356,7 @@ __device__ __forceinline__ void run_chunk(unsigned char* smem, const GT* gb, con
     if (full) phase_a<true, GT, NW, G, S, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
     else phase_a<false, GT, NW, G, S, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
     const float tot = row_shares(rp, lane);  // warp total of row lane / kShareLanes
-    if (lane % C::kShareLanes == 0) pk[(lane / C::kShareLanes) * NW + warp] = tot;
+    if (lane % C::kShareLanes == 0) pk[lane + warp] = tot;
     __syncthreads();
     // Refill the stage of sub-panel k - 1 (every lane is past it) with k + S - 1.
     {
@@ -307,44 +370,134 @@ __device__ __forceinline__ void run_chunk(unsigned char* smem, const GT* gb, con
       }
       cp_async_commit();
     }
-    // Row statistics of the sub-panel, in every warp: lane l adds the shares
-    // of row l / NW over the warps (a fixed xor tree where SR * NW = 32, else
-    // in warp order; lanes past SR * NW hold no row).
-    float R = 0.f;
-    if constexpr (SR * NW == 32) {
-      R = pk[lane];
-#pragma unroll
-      for (int o = NW / 2; o > 0; o >>= 1) R += __shfl_xor_sync(0xffffffffu, R, o);
-    } else {
-      if (rl < SR) {
-#pragma unroll
-        for (int w = 0; w < NW; ++w) R += pk[rl * NW + w];
-      }
-    }
-    const float rn = fmaf(b2, row_old, omb2 * fmaf(R, invw, eps1));
-    const float winv = __frcp_rn(rn);  // correctly rounded 1 / rn
-    if (warp == 0 && lane % NW == 0 && s0 + rl < s1) {
-      rowst[s0 + rl] = rn;
-      rsum += rn;
-    }
+    const float winv = row_stats<GT, NW, G, S>(pk, lane, warp, row_old, s0, s1, rowst, invw, b2, omb2, eps1, rsum);
     if (full) phase_b<true, GT, NW, G, S>(st, s0, s1, W, warp, lane, winv, dacc);
     else phase_b<false, GT, NW, G, S>(st, s0, s1, W, warp, lane, winv, dacc);
     stage = stage == S - 1 ? 0 : stage + 1;
   }
-  // column partials of the chunk
-  const Partials out = where();
-  float* cp = out.cp;
-  float* dp = out.dp;
+  store_partials<NW, G>(where(), W, warp, lane, cacc, dacc);
+}
+
+// The split form's barriers: two mbarriers at kBarOff, each completed by the
+// NW * kSubRows lanes that hold row shares.  One thread of the CTA, before
+// the first chunk; the caller's CTA barrier makes the initialisation visible.
+template <typename GT, int NW, int G, int S>
+__device__ __forceinline__ void split_init(unsigned char* smem) {
+  using C = Cfg<GT, NW, G, S>;
+  static_assert(C::kSplit, "the split form needs a ring of 4 stages or more");
+  const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(smem + C::kBarOff));
+  for (int b = 0; b < 2; ++b)
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar + 8 * b), "r"(NW * C::kSubRows) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Waits for the phase of parity `parity` of the mbarrier at `bar`; false
+// after meo::kWaitCycles.
+__device__ __forceinline__ bool split_wait(uint32_t bar, uint32_t parity) {
+  auto done = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (done()) return true;
+  const long long t0 = clock64();
+  while (!done()) {
+    if (clock64() - t0 > meo::kWaitCycles) return false;
+  }
+  return true;
+}
+
+// run_chunk in the split form (S >= 4; arguments and results as there).  q
+// counts the sub-panels this CTA has finished over all its chunks (it picks
+// the mbarrier, its phase and the share buffer) and is advanced by the
+// chunk's sub-panels.  A wait that runs out sets kStatusWaitTimeout in
+// *status and `dead`; a dead CTA waits no more (its results are not used).
+template <typename GT, int NW, int G, int S, bool PSQ, typename Where>
+__device__ __forceinline__ void run_chunk_split(unsigned char* smem, const GT* gb, const float* pb, float* rowst,
+                                                int32_t W, int32_t c0, int32_t c1, float b2, float omb2,
+                                                float eps1, Where&& where, float& rsum, float& psq, uint32_t& q,
+                                                bool& dead, int32_t* status) {
+  using C = Cfg<GT, NW, G, S>;
+  static_assert(C::kSplit, "the split form needs a ring of 4 stages or more");
+  constexpr int SR = C::kSubRows, SL = C::kShareLanes;
+  float* part = reinterpret_cast<float*>(smem + C::kPartOff);  // [4][32]
+  const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(smem + C::kBarOff));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned char* mine = smem + warp * C::kWarpBytes + lane * 16;
+  const uint32_t mine_s = static_cast<uint32_t>(__cvta_generic_to_shared(mine));
+  const int rl = lane / SL;  // row of this lane's share and row statistic
+  const int32_t nsub = (c1 - c0 + SR - 1) / SR;
+  const float invw = 1.0f / static_cast<float>(W);
+  float2 cacc[G][4], dacc[G][4];
 #pragma unroll
   for (int c = 0; c < G; ++c) {
-    const int32_t j = (c * NW + warp) * 256 + lane * 8;
-    if (j < W) {
-      *reinterpret_cast<float4*>(cp + j) = make_float4(cacc[c][0].x, cacc[c][0].y, cacc[c][1].x, cacc[c][1].y);
-      *reinterpret_cast<float4*>(cp + j + 4) = make_float4(cacc[c][2].x, cacc[c][2].y, cacc[c][3].x, cacc[c][3].y);
-      *reinterpret_cast<float4*>(dp + j) = make_float4(dacc[c][0].x, dacc[c][0].y, dacc[c][1].x, dacc[c][1].y);
-      *reinterpret_cast<float4*>(dp + j + 4) = make_float4(dacc[c][2].x, dacc[c][2].y, dacc[c][3].x, dacc[c][3].y);
-    }
+#pragma unroll
+    for (int v = 0; v < 4; ++v) cacc[c][v] = dacc[c][v] = make_float2(0.f, 0.f);
   }
+  rsum = 0.f;
+  // Prologue: sub-panels 0 .. S - 1, one commit group each (empty past the
+  // chunk's end).  Iteration k >= 1 commits one group (sub-panel k - 1 + S),
+  // so when sub-panel k is waited for, the groups of sub-panels up to
+  // k + S - 2 are committed and sub-panel k is complete once at most S - 2
+  // are pending.
+#pragma unroll
+  for (int k = 0; k < S; ++k) {
+    if (k < nsub) issue<false, GT, NW, G, S>(mine_s + k * C::kStageBytes, gb, W, c0 + k * SR, c1, warp, lane);
+    cp_async_commit();
+  }
+  const bool cols_full = ((G - 1) * NW + warp + 1) * 256 <= W;
+  float old_prev = 0.f;  // old row statistic of this lane's row in sub-panel k - 1
+  for (int32_t k = 0; k <= nsub; ++k) {
+    float old_cur = 0.f;
+    if (k < nsub) {
+      const int32_t s0 = c0 + k * SR, s1 = min(c1, s0 + SR);
+      const bool full = cols_full && s1 - s0 == SR;
+      old_cur = (s0 + rl < s1) ? rowst[s0 + rl] : 0.f;
+      cp_async_wait<S - 2>();
+      const unsigned char* st = mine + (k % S) * C::kStageBytes;
+      float rp[SR];
+      if (full) phase_a<true, GT, NW, G, S, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
+      else phase_a<false, GT, NW, G, S, PSQ>(st, s0, s1, W, warp, lane, pb, cacc, rp, psq);
+      const float tot = row_shares(rp, lane);  // warp total of row lane / SL
+      if (lane % SL == 0) {
+        const uint32_t qk = q + static_cast<uint32_t>(k);
+        part[(qk % 4) * 32 + lane + warp] = tot;
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar + 8 * (qk & 1)) : "memory");
+      }
+    }
+    if (k > 0) {
+      // row statistics and phase B of sub-panel k - 1
+      const uint32_t qp = q + static_cast<uint32_t>(k) - 1;
+      if (!dead && !split_wait(bar + 8 * (qp & 1), (qp >> 1) & 1)) {
+        dead = true;
+        if (lane == 0) atomicOr(status, meo::kStatusWaitTimeout);
+      }
+      const int32_t s0 = c0 + (k - 1) * SR, s1 = min(c1, s0 + SR);
+      const bool full = cols_full && s1 - s0 == SR;
+      const float winv = row_stats<GT, NW, G, S>(part + (qp % 4) * 32, lane, warp, old_prev, s0, s1, rowst, invw,
+                                                 b2, omb2, eps1, rsum);
+      const int stage = (k - 1) % S;
+      const unsigned char* st = mine + stage * C::kStageBytes;
+      if (full) phase_b<true, GT, NW, G, S>(st, s0, s1, W, warp, lane, winv, dacc);
+      else phase_b<false, GT, NW, G, S>(st, s0, s1, W, warp, lane, winv, dacc);
+      // this lane is past sub-panel k - 1: refill its stage with k - 1 + S
+      const int32_t kk = k - 1 + S;
+      if (kk < nsub) {
+        if (cols_full && c0 + (kk + 1) * SR <= c1)
+          issue<true, GT, NW, G, S>(mine_s + stage * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
+        else
+          issue<false, GT, NW, G, S>(mine_s + stage * C::kStageBytes, gb, W, c0 + kk * SR, c1, warp, lane);
+      }
+      cp_async_commit();
+    }
+    old_prev = old_cur;
+  }
+  q += static_cast<uint32_t>(nsub);
+  store_partials<NW, G>(where(), W, warp, lane, cacc, dacc);
 }
 
 }  // namespace panel
