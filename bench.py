@@ -53,6 +53,7 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "adafactor_kernels.cu")
 KERNEL_HDR = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "adafactor_internal.h")
+PANEL_HDR = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "row_panel.cuh")
 LAMB_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "lamb.cu")
 LAMB_HDR = os.path.join(ROOT, "include", "lamb.h")
 CAME_SRC = os.path.join(ROOT, "memory_efficient_optimizer_gb300", "csrc", "came.cu")
@@ -279,10 +280,12 @@ KERNEL_SECTIONS = {
 
 def kernel_source_digest(kernel):
     """sha256 of the source a launch slot's kernel is built from: the shared
-    header plus the slot's sections of the kernel file (the whole file for
-    slots without a section list); for the LAMB and CAME kernels, their
-    own source file and header."""
-    for prefix, files in (("k_lamb", (LAMB_SRC, LAMB_HDR)), ("k_came", (CAME_SRC, CAME_HDR))):
+    headers (adafactor_internal.h, row_panel.cuh) plus the slot's sections of
+    the kernel file (the whole file for slots without a section list); for
+    the LAMB and CAME kernels, their own source file and header with the
+    shared headers they include."""
+    for prefix, files in (("k_lamb", (LAMB_SRC, LAMB_HDR, KERNEL_HDR)),
+                          ("k_came", (CAME_SRC, CAME_HDR, KERNEL_HDR, PANEL_HDR))):
         if kernel.startswith(prefix):
             text = "".join(open(f, encoding="utf-8").read() for f in files)
             return hashlib.sha256(text.encode()).hexdigest()
@@ -291,7 +294,7 @@ def kernel_source_digest(kernel):
     if titles:
         parts = re.split(r"(?m)^// ---- ", text)[1:]
         text = "".join(p for p in parts if p.startswith(titles))
-    header = open(KERNEL_HDR, encoding="utf-8").read()
+    header = "".join(open(f, encoding="utf-8").read() for f in (KERNEL_HDR, PANEL_HDR))
     return hashlib.sha256((header + text).encode()).hexdigest()
 
 
