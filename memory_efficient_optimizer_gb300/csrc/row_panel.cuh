@@ -415,7 +415,8 @@ __device__ __forceinline__ bool split_wait(uint32_t bar, uint32_t parity) {
 // counts the sub-panels this CTA has finished over all its chunks (it picks
 // the mbarrier, its phase and the share buffer) and is advanced by the
 // chunk's sub-panels.  A wait that runs out sets kStatusWaitTimeout in
-// *status and `dead`; a dead CTA waits no more (its results are not used).
+// *status and `dead`, after which the thread waits no more (the step's
+// results are then not used).
 template <typename GT, int NW, int G, int S, bool PSQ, typename Where>
 __device__ __forceinline__ void run_chunk_split(unsigned char* smem, const GT* gb, const float* pb, float* rowst,
                                                 int32_t W, int32_t c0, int32_t c1, float b2, float omb2,
