@@ -285,3 +285,17 @@ def test_two_step_objects_alternating_share_kept_tables():
     assert steps[0].device_status() == 0 and steps[1].device_status() == 0
     for k in range(len(shapes)):
         check(f"alternating[{k}]", to64(params[k]), refs[k])
+
+
+def test_wide_chunks_run_back_to_back_in_one_cta():
+    """More wide-class chunks than one CTA per SM: 400 bf16 matrices of 3 or 5
+    rows of 4104 or 9000 values (one chunk each, of 2 or 3 sub-panels), so
+    most CTAs of the wide pass run two or three chunks in a row and carry the
+    mbarrier phases and share buffers of the split form from one chunk to the
+    next, against the oracle; with and without sum(p^2) recomputed in pass 1."""
+    kinds = [(3, 4104), (5, 9000), (3, 9000), (5, 4104)]
+    shapes = [kinds[k % len(kinds)] for k in range(400)]
+    for hp in (dict(), dict(beta1=0.9, weight_decay=0.01)):
+        wl = synth.Workload("wide_many", [(f"t{k}", s) for k, s in enumerate(shapes)], torch.bfloat16, 1e-2,
+                            hp, 4)
+        run_parity(wl)
